@@ -1,0 +1,313 @@
+"""Pins for the CPU oracle, checked against things other than the oracle itself:
+worked blocks from the pages' definitions (tests/golden), library routines
+(torch and numpy IEEE fp16 conversion, numpy float64 matmul), closed forms
+(integer-grid inputs), invariants of the quantizers and brute force on tiny
+inputs.  No GPU."""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import oracle as O
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(":", 1)
+            out[k.strip()] = v.split()
+    return out
+
+
+# ----------------------------------------------------------------- fp16
+def test_f16_decode_exhaustive_vs_numpy():
+    h = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = O.f16_bits_to_f32(h)
+    ref = h.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_f16_encode_exhaustive_vs_torch():
+    """All 2^32 fp32 bit patterns against torch's CPU round-to-nearest-even .half()."""
+    import torch
+    chunk = 1 << 24
+    base = np.arange(chunk, dtype=np.uint32)
+    for start in range(0, 1 << 32, chunk):
+        bits = base + np.uint32(start)
+        f = bits.view(np.float32)
+        ours = O.f32_to_f16_bits(f)
+        ref = torch.from_numpy(f).half().view(torch.int16).numpy().view(np.uint16)
+        nan = np.isnan(f)
+        if nan.any():
+            # NaN in -> NaN out (payload not specified)
+            assert np.all((ours[nan] & 0x7C00) == 0x7C00) and np.all((ours[nan] & 0x3FF) != 0)
+            ok = (ours == ref) | nan
+        else:
+            ok = ours == ref
+        if not ok.all():
+            i = int(np.nonzero(~ok)[0][0])
+            raise AssertionError(f"fp32 bits {bits[i]:#x}: ours {ours[i]:#x}, torch {ref[i]:#x}")
+
+
+def test_f16_encode_rounding_boundaries_vs_torch():
+    """Every exponent x mantissa-top x the rounding-critical low bits, against torch CPU .half()."""
+    import torch
+    hi = np.arange(1 << 19, dtype=np.uint32) << 13  # sign, exponent, top 10 mantissa bits
+    lows = np.array([0, 1, 0x0FFF, 0x1000, 0x1001, 0x1FFF], dtype=np.uint32)
+    bits = (hi[:, None] | lows[None, :]).reshape(-1)
+    bits = bits[(bits & 0x7F800000) != 0x7F800000]  # no inf/NaN
+    f = bits.view(np.float32)
+    ours = O.f32_to_f16_bits(f)
+    ref = torch.from_numpy(f.copy()).half().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ----------------------------------------------------------------- quantizers
+def test_q8_0_worked_block():
+    g = _golden("q8_0_ramp_block.txt")
+    x = np.array([float(v) for v in g["x"]], np.float32)
+    q, d = O.quantize_q8_0(x[None])
+    assert d[0, 0] == int(g["d16"][0], 16)
+    assert q[0].tolist() == [int(v) for v in g["q"]]
+
+
+def test_q4_0_worked_block():
+    g = _golden("q4_0_small_block.txt")
+    w = np.array([float(v) for v in g["w"]], np.float32)
+    q, d = O.quantize_q4_0(w[None])
+    assert d[0, 0] == int(g["d16"][0], 16)
+    assert q[0].tolist() == [int(v) for v in g["q"]]
+
+
+def test_q4_0_block_format_sizes():
+    g = _golden("q4_0_block_format.txt")
+    assert int(g["values_per_block"][0]) == O.QK
+    rng = np.random.default_rng(1)
+    q = rng.integers(-8, 8, size=(3, 64)).astype(np.int8)
+    d = rng.integers(0, 0x7C00, size=(3, 2)).astype(np.uint16)
+    blocks = O.pack_q4_0_blocks(q, d)
+    assert blocks.shape[-1] == int(g["block_bytes"][0]) == int(g["scale_bytes"][0]) + int(g["nibble_bytes"][0])
+    # scale is the first 2 bytes, little endian
+    assert np.array_equal(blocks[..., 0].astype(np.uint16) | (blocks[..., 1].astype(np.uint16) << 8), d)
+    # 32 four-bit values in 16 bytes: element j low nibble, j+16 high nibble, offset 8
+    assert np.array_equal((blocks[0, 0, 2:] & 0xF).astype(np.int8) - 8, q[0, :16])
+    assert np.array_equal((blocks[0, 0, 2:] >> 4).astype(np.int8) - 8, q[0, 16:32])
+    q2, d2 = O.unpack_q4_0_blocks(blocks, 3, 64)
+    assert np.array_equal(q2, q) and np.array_equal(d2, d)
+    total = sum(workloads.q4_0_bytes(N, K) for _, N, K in workloads.tinyllama_matrices())
+    assert total == 581_861_376
+    assert abs(total / 1e6 - float(g["tinyllama_4bit_mb_approx"][0])) / 600 < 0.05
+
+
+def _numpy_quantize(v, qmax, qmin):
+    """Independent restatement with numpy fp32 ops (division, |.|, floor)."""
+    v = v.astype(np.float32).reshape(-1, 32)
+    amax = np.abs(v).max(axis=1)
+    d32 = (amax / np.float32(qmax)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = (v / d32[:, None]).astype(np.float32)
+    a = np.floor(np.abs(r).astype(np.float64) + 0.5) * np.sign(r)
+    a = np.where(amax[:, None] == 0, 0, a)
+    q = np.clip(a, qmin, qmax).astype(np.int8)
+    return q, d32
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_q8_0_matches_numpy_restatement(seed):
+    x = workloads.activations(4, 2048, seed=seed).numpy()
+    q, d = O.quantize_q8_0(x)
+    qn, d32 = _numpy_quantize(x, 127, -127)
+    assert np.array_equal(q.reshape(-1, 32), qn)
+    assert np.array_equal(d.reshape(-1), d32.astype(np.float16).view(np.uint16))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_q4_0_matches_numpy_restatement(seed):
+    w = workloads.weights(64, 2048, seed=seed).numpy()
+    q, d = O.quantize_q4_0(w)
+    qn, d32 = _numpy_quantize(w, 7, -8)
+    assert np.array_equal(q.reshape(-1, 32), qn)
+    assert np.array_equal(d.reshape(-1), d32.astype(np.float16).view(np.uint16))
+
+
+def _adversarial_blocks(rng, n):
+    """Random blocks plus zero blocks, amax at every lane, exact .5 ties."""
+    x = rng.standard_normal((n, 32)).astype(np.float32)
+    x[0] = 0
+    for lane in range(32):
+        x[1 + lane] = rng.uniform(-1, 1, 32).astype(np.float32)
+        x[1 + lane, lane] = 4.0 * (-1) ** lane
+    # ties: amax 127 -> d32 = 1, values k + 0.5 are exact ties
+    x[40] = (np.arange(32) - 16 + 0.5).astype(np.float32)
+    x[40, 0] = 127
+    x[41] = -x[40]
+    return x
+
+
+def test_q8_0_invariants():
+    rng = np.random.default_rng(7)
+    x = _adversarial_blocks(rng, 256)
+    q, d = O.quantize_q8_0(x.reshape(1, -1))
+    q = q.reshape(-1, 32)
+    d = d.reshape(-1)
+    # zero block
+    assert d[0] == 0 and not q[0].any()
+    # every nonzero block reaches |q| = 127
+    nz = np.abs(x).max(axis=1) > 0
+    assert np.all(np.abs(q[nz]).max(axis=1) == 127)
+    assert q.min() >= -127 and q.max() <= 127
+    # ties round half away from zero (x = k + 0.5 with d32 = 1)
+    assert q[40, 1:].tolist() == [int(np.sign(v) * np.floor(abs(v) + 0.5)) for v in x[40, 1:]]
+    # sign symmetry
+    qn, dn = O.quantize_q8_0(-x.reshape(1, -1))
+    assert np.array_equal(qn.reshape(-1, 32), -q) and np.array_equal(dn.reshape(-1), d)
+    # power-of-two scaling leaves q unchanged and scales d exactly
+    q2, d2 = O.quantize_q8_0((x * np.float32(4)).reshape(1, -1))
+    assert np.array_equal(q2.reshape(-1, 32), q)
+    f = O.f16_bits_to_f32(d)
+    f2 = O.f16_bits_to_f32(d2.reshape(-1))
+    assert np.array_equal(f2, f * 4)
+    # round-trip bound |x - d32*q| <= d32/2 (+ 1 ulp of the product)
+    amax = np.abs(x).max(axis=1)
+    d32 = (amax / np.float32(127)).astype(np.float32)
+    err = np.abs(x.astype(np.float64) - d32[:, None].astype(np.float64) * q)
+    bound = d32[:, None].astype(np.float64) / 2 * (1 + 1e-6) + np.spacing(np.abs(x)).astype(np.float64)
+    assert np.all(err <= bound)
+
+
+def test_q4_0_invariants():
+    rng = np.random.default_rng(8)
+    w = _adversarial_blocks(rng, 256) * np.float32(0.01)
+    q, d = O.quantize_q4_0(w.reshape(1, -1))
+    q = q.reshape(-1, 32)
+    nz = np.abs(w).max(axis=1) > 0
+    assert np.all(np.abs(q[nz]).max(axis=1) == 7)
+    assert q.min() >= -7 and q.max() <= 7  # Delta = amax/7 never reaches -8
+    assert not q[0].any() and d.reshape(-1)[0] == 0
+    qn, dn = O.quantize_q4_0(-w.reshape(1, -1))
+    assert np.array_equal(qn.reshape(-1, 32), -q) and np.array_equal(dn, d)
+
+
+# ----------------------------------------------------------------- products
+def _rand_q(rng, N, M, K):
+    qw = rng.integers(-8, 8, size=(N, K)).astype(np.int8)  # all 16 nibble values incl. -8
+    qx = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    dw = rng.integers(0x1000, 0x2C00, size=(N, K // 32)).astype(np.uint16)
+    dx = rng.integers(0x1000, 0x3C00, size=(M, K // 32)).astype(np.uint16)
+    return qw, dw, qx, dx
+
+
+def test_single_product_table_exhaustive():
+    """All 16 weight values x all 255 activation values through the block dot."""
+    qw = np.repeat(np.arange(-8, 8, dtype=np.int8)[:, None], 32, axis=1)
+    qx = np.repeat(np.arange(-127, 128, dtype=np.int8)[:, None], 32, axis=1)
+    dots = O.block_dots(qw, qx)[:, :, 0]
+    assert np.array_equal(dots, 32 * np.outer(np.arange(-127, 128), np.arange(-8, 8)))
+
+
+def test_integer_grid_closed_form():
+    """With d = 1 on both sides, y is exactly the integer product W x."""
+    rng = np.random.default_rng(3)
+    N, M, K = 37, 5, 256
+    w = rng.integers(-7, 8, size=(N, K)).astype(np.float32)
+    w[:, ::32] = 7  # every block holds a 7 -> Delta = 1
+    x = rng.integers(-127, 128, size=(M, K)).astype(np.float32)
+    x[:, 5::32] = -127  # every block holds a -127 -> d = 1
+    qw, dw = O.quantize_q4_0(w)
+    qx, dx = O.quantize_q8_0(x)
+    assert np.all(dw == 0x3C00) and np.all(dx == 0x3C00)
+    y, _ = O.matmul_int(qw, dw, qx, dx)
+    exact = x.astype(np.int64) @ w.astype(np.int64).T
+    assert np.array_equal(y, exact.astype(np.float64))
+    yd = O.matmul_dequant(qw, dw, qx, dx)
+    assert np.array_equal(yd, exact.astype(np.float64))
+
+
+@pytest.mark.parametrize("N,M,K", [(1, 1, 32), (8, 3, 64), (5, 2, 96), (3, 4, 160)])
+def test_brute_force_dequantized_matmul(N, M, K):
+    rng = np.random.default_rng(N * 100 + K)
+    qw, dw, qx, dx = _rand_q(rng, N, M, K)
+    W = np.repeat(dw.view(np.float16).astype(np.float64), 32, axis=1) * qw
+    X = np.repeat(dx.view(np.float16).astype(np.float64), 32, axis=1) * qx
+    ref = X @ W.T
+    y, S = O.matmul_int(qw, dw, qx, dx)
+    yd = O.matmul_dequant(qw, dw, qx, dx)
+    scale = np.abs(X) @ np.abs(W).T + 1e-300
+    assert np.all(np.abs(y - ref) <= 1e-13 * scale)
+    assert np.all(np.abs(yd - ref) <= 1e-13 * scale)
+    # S bounds |y| and is what the fp32 tolerance is built on
+    assert np.all(np.abs(y) <= S * (1 + 1e-15))
+    dots = O.block_dots(qw, qx)
+    manual = np.einsum("nbi,mbi->mnb", qw.reshape(N, -1, 32).astype(np.int64),
+                       qx.reshape(M, -1, 32).astype(np.int64))
+    assert np.array_equal(dots, manual)
+
+
+def test_int_and_dequant_paths_agree_realistic():
+    w = workloads.weights(96, 2048, seed=0).numpy()
+    x = workloads.activations(2, 2048, seed=0).numpy()
+    qw, dw = O.quantize_q4_0(w)
+    qx, dx = O.quantize_q8_0(x)
+    y, S = O.matmul_int(qw, dw, qx, dx)
+    yd = O.matmul_dequant(qw, dw, qx, dx)
+    assert np.all(np.abs(y - yd) <= 1e-12 * S + 1e-300)
+    # and the quantized product approximates the fp32 product
+    exact = x.astype(np.float64) @ w.astype(np.float64).T
+    rel = np.linalg.norm(y - exact) / np.linalg.norm(exact)
+    assert rel < 0.1
+
+
+def test_row_subset_and_threads():
+    rng = np.random.default_rng(11)
+    qw, dw, qx, dx = _rand_q(rng, 50, 3, 128)
+    y, S = O.matmul_int(qw, dw, qx, dx)
+    rows = np.array([49, 0, 7, 7, 31])
+    ys, Ss = O.matmul_int(qw, dw, qx, dx, rows=rows, nthreads=3)
+    assert np.array_equal(ys, y[:, rows]) and np.array_equal(Ss, S[:, rows])
+    y4, _ = O.matmul_int(qw, dw, qx, dx, nthreads=4)
+    assert np.array_equal(y4, y)
+
+
+# ----------------------------------------------------------------- MoE pieces
+def test_router_topk_order_ties_and_normalisation():
+    logits = np.array([[0.0, 2.0, 2.0, -1.0, 5.0, 2.0]], np.float32)
+    ids, g = O.router_topk(logits, 3)
+    assert ids[0].tolist() == [4, 1, 2]  # ties -> lower index first
+    s = 1 / (1 + np.exp(-logits[0, [4, 1, 2]].astype(np.float64)))
+    assert np.allclose(g[0], s / s.sum(), rtol=1e-15)
+    assert abs(g.sum() - 1) < 1e-15
+    L = workloads.router_logits(16, 256).numpy()
+    ids, g = O.router_topk(L, 8)
+    for t in range(16):
+        assert len(set(ids[t].tolist())) == 8
+        assert ids[t].tolist() == np.argsort(-L[t], kind="stable")[:8].tolist()  # sigmoid is monotone
+
+
+def test_swiglu_identities():
+    a = np.array([0.0, 1.0, -1.0, 30.0, -30.0, 0.5], np.float64)
+    b = np.ones_like(a)
+    h = O.swiglu(a, b)
+    assert h[0] == 0.0
+    # silu(a) - silu(-a) = a
+    assert abs((float(h[1]) - float(h[2])) - 1.0) < 1e-7
+    assert abs(float(h[3]) - 30.0) < 1e-6 and abs(float(h[4])) < 1e-10
+    h2 = O.swiglu(a, 2 * b)
+    assert np.array_equal(h2, (2 * h.astype(np.float64)).astype(np.float32))
+
+
+def test_moe_combine_linear():
+    rng = np.random.default_rng(5)
+    z = rng.standard_normal((2, 3, 4))
+    g = np.array([[1, 0, 0], [0.25, 0.5, 0.25]], np.float32)
+    y = O.moe_combine(z, g)
+    assert np.array_equal(y[0], z[0, 0])
+    assert np.allclose(y[1], 0.25 * z[1, 0] + 0.5 * z[1, 1] + 0.25 * z[1, 2], rtol=0, atol=1e-15)
