@@ -1,0 +1,464 @@
+#!/usr/bin/env python
+"""Benchmark of the Q4_0 x Q8_0 decode path on GB300.
+
+Headline (the JSON line's `value`): batch-1 GEMV weight GB/s over a
+TinyLLaMA-1.1B-shaped decode step -- 22 layers of fused QKV 2048->2560,
+O 2048->2048, gate|up 2048->2x5632 (one launch), down 5632->2048 (SwiGLU +
+Q8_0 fused in front, residual add behind), then lm_head 2048->32000: 89
+dependent GEMV launches per step, each quantizing its fp32 input to Q8_0
+inside the launch, chained with programmatic dependent launch and replayed
+from a CUDA graph.  581,861,376 weight bytes per step (> L2, so no flush).
+
+Also reported on the same line (`also`): batch-16 GEMM TOPS on the large
+dense FFN + lm_head shapes, and the GLM-scale MoE layer.
+
+`--impl reference` times the CPU oracle on a bounded row sample of the same
+decode step (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------- dist
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- decode step
+class TinyLlamaDecode:
+    """Weights and buffers of the TinyLLaMA-shaped decode step, and the step itself."""
+
+    def __init__(self, qmm, torch, seed=0, dev="cuda"):
+        c = workloads.TINYLLAMA
+        self.qmm, self.torch, self.dev = qmm, torch, dev
+        self.H, self.F, self.Q, self.V, self.L = c["hidden"], c["ffn"], c["qkv"], c["vocab"], c["layers"]
+        sigma = c["sigma"]
+        self.layers = []
+        idx = 0
+
+        def planes(N, K):
+            nonlocal idx
+            w = workloads.weights(N, K, sigma=sigma, seed=seed, index=idx, device=dev)
+            idx += 1
+            qs, d = qmm.quantize_q4_0(w)
+            del w
+            return qs, d
+
+        for _ in range(self.L):
+            qkv = planes(self.Q, self.H)
+            o = planes(self.H, self.H)
+            g = planes(self.F, self.H)
+            u = planes(self.F, self.H)
+            # gate and up rows stacked: one launch yields [gate | up]
+            gu = (torch.cat([g[0], u[0]]), torch.cat([g[1], u[1]]))
+            down = planes(self.H, self.F)
+            self.layers.append({"qkv": qkv, "o": o, "gu": gu, "down": down})
+        self.lm_head = planes(self.V, self.H)
+        self.weight_bytes = sum(workloads.q4_0_bytes(N, K) for _, N, K in workloads.tinyllama_matrices())
+        f32 = lambda n: torch.zeros(n, dtype=torch.float32, device=dev)  # noqa: E731
+        self.x_in = workloads.activations(1, self.H, seed=seed, device=dev)[0].contiguous()
+        self.h = [f32(self.H), f32(self.H)]
+        self.qkv_out, self.o_out, self.gu_out = f32(self.Q), f32(self.H), f32(2 * self.F)
+        self.logits = f32(self.V)
+        self.launches_per_step = 4 * self.L + 1
+        # algorithmic bytes per step: weights + fp32 activations read + outputs written (+ residual)
+        act = 0
+        for _ in range(self.L):
+            act += 4 * (self.H + self.Q) + 4 * (self.H + self.H) + 4 * (self.H + 2 * self.F) + 4 * (2 * self.F + 2 * self.H)
+        act += 4 * (self.H + self.V)
+        self.algo_bytes = self.weight_bytes + act
+
+    def step(self, stream=None):
+        q, H, F = self.qmm, self.H, self.F
+        h_prev = self.x_in
+        for li, Lw in enumerate(self.layers):
+            h_next = self.h[li % 2]
+            q.qmm_gemv_q4_0_f32(*Lw["qkv"], self.Q, H, h_prev, 0, None, self.qkv_out, chain=1, stream=stream)
+            # attention is outside this path: the O projection reads the q slice
+            q.qmm_gemv_q4_0_f32(*Lw["o"], H, H, self.qkv_out, 0, None, self.o_out, chain=1, stream=stream)
+            q.qmm_gemv_q4_0_f32(*Lw["gu"], 2 * F, H, self.o_out, 0, None, self.gu_out, chain=1, stream=stream)
+            q.qmm_gemv_q4_0_f32(*Lw["down"], H, F, self.gu_out, 1, h_prev, h_next, chain=1, stream=stream)
+            h_prev = h_next
+        q.qmm_gemv_q4_0_f32(*self.lm_head, self.V, H, h_prev, 0, None, self.logits, chain=1, stream=stream)
+
+
+def _graph(torch, fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm: lazy attribute set-up happens outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def _time_graph(torch, g, steps, warmup):
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(steps):
+        g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3  # seconds
+
+
+def _flush_l2(torch, buf):
+    buf.add_(1.0)
+
+
+# ---------------------------------------------------------------------------- extras
+def bench_gemm_b16(qmm, torch, reps=20, dev="cuda"):
+    """Batch-16 GEMM on the large dense FFN + lm_head shapes (TOPS = 2*M*N*K per second)."""
+    mats = workloads.large_dense_matrices()
+    sigma = workloads.LARGE_DENSE["sigma"]
+    M = 16
+    ws, xs, ys, ops, wbytes = [], [], [], 0, 0
+    for i, (_, N, K) in enumerate(mats):
+        w = workloads.weights(N, K, sigma=sigma, seed=0, index=100 + i, device=dev)
+        ws.append((qmm.quantize_q4_0(w), N, K))
+        del w
+        x = workloads.activations(M, K, seed=0, index=600 + i, device=dev)
+        xs.append(qmm.quantize_q8_0(x))
+        ys.append(torch.empty(M, N, device=dev))
+        ops += 2 * M * N * K
+        wbytes += workloads.q4_0_bytes(N, K)
+
+    def run():
+        for ((qs, d), N, K), (xq, xd), y in zip(ws, xs, ys):
+            qmm.qmm_gemm_q4_0_q8_0(qs, d, N, K, M, xq, xd, y, N)
+
+    g = _graph(torch, run)
+    t = _time_graph(torch, g, reps, 3)
+    per = t / reps
+    return {"metric": "batch-16 Q4_0xQ8_0 GEMM TOPS", "value": round(ops / per / 1e12, 2), "unit": "TOPS",
+            "ms_per_step": round(per * 1e3, 4), "weight_GBps": round(wbytes / per / 1e9, 1),
+            "config": {"workload": workloads.LARGE_DENSE["name"] + ", batch 16", "M": M,
+                       "shapes": [[N, K] for _, N, K in mats], "l2": "inputs larger than L2 (987 MB weights)"}}
+
+
+def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
+    """GLM-scale MoE layer, T tokens: quantize x, gate and up expert GEMVs,
+    SwiGLU + Q8_0, down expert GEMV, combine."""
+    import numpy as np
+    c = workloads.MOE
+    H, F, E, k = c["hidden"], c["expert_ffn"], c["experts"], c["top_k"]
+    sigma = c["sigma"]
+
+    def experts(N, K, base):
+        qs = torch.empty(E, N, K // 2, dtype=torch.uint8, device=dev)
+        d = torch.empty(E, N, K // 32, dtype=torch.int16, device=dev)
+        for e in range(E):
+            w = workloads.weights(N, K, sigma=sigma, seed=0, index=base + e, device=dev)
+            qmm.qmm_quantize_q4_0(w, N, K, K, qs[e], d[e])
+        return qs, d
+
+    gate, up, down = experts(F, H, 0), experts(F, H, 1000), experts(H, F, 2000)
+    logits = workloads.router_logits(T, E, seed=0)
+    # top-k of sigmoid scores == top-k of logits; gates normalised over the k
+    s = torch.sigmoid(logits.double())
+    top = torch.topk(s, k, dim=1, sorted=True)
+    ids = top.indices.to(torch.int32).to(dev)
+    gts = (top.values / top.values.sum(1, keepdim=True)).float().to(dev)
+    uniq = len(np.unique(top.indices.numpy()))
+    x = workloads.activations(T, H, seed=0, device=dev)
+    xq = torch.empty(T, H, dtype=torch.int8, device=dev)
+    xd = torch.empty(T, H // 32, dtype=torch.int16, device=dev)
+    yg = torch.empty(T * k, F, device=dev)
+    yu = torch.empty(T * k, F, device=dev)
+    hq = torch.empty(T * k, F, dtype=torch.int8, device=dev)
+    hd = torch.empty(T * k, F // 32, dtype=torch.int16, device=dev)
+    z = torch.empty(T * k, H, device=dev)
+    y = torch.empty(T, H, device=dev)
+    wsb = qmm.qmm_moe_workspace_size(E, T, k)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    def run():
+        qmm.qmm_quantize_q8_0(x, T, H, H, xq, xd)
+        qmm.qmm_moe_gemv(*gate, E, F, H, ids, T, k, xq, xd, 0, yg, ws, wsb)
+        qmm.qmm_moe_gemv(*up, E, F, H, ids, T, k, xq, xd, 0, yu, ws, wsb)
+        qmm.qmm_swiglu_quantize_q8_0(yg, yu, T * k, F, F, hq, hd)
+        qmm.qmm_moe_gemv(*down, E, H, F, ids, T, k, hq, hd, 1, z, ws, wsb)
+        qmm.qmm_moe_combine(z, gts, T, k, H, y)
+
+    g = _graph(torch, run)
+    t = _time_graph(torch, g, reps, 3)
+    per = t / reps
+    wbytes = uniq * 3 * workloads.q4_0_bytes(F, H)
+    return {"metric": "MoE layer expert-weight GB/s", "value": round(wbytes / per / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(per * 1e3, 4), "tokens_per_s": round(T / per, 1), "unique_experts": uniq,
+            "config": {"workload": c["name"], "T": T, "experts": E, "top_k": k, "hidden": H, "expert_ffn": F}}
+
+
+# ---------------------------------------------------------------------------- CPU oracle baseline
+def oracle_decode_sample(torch, rows=256):
+    """Oracle inputs for a row sample of every matrix of the decode step: the
+    first `rows` rows of each (weights drawn with the same recipe on the CPU
+    and quantized by the oracle) and the Q8_0 activation of each width."""
+    from oracle import oracle as O
+    mats = workloads.tinyllama_matrices()
+    sigma = workloads.TINYLLAMA["sigma"]
+    xs, out = {}, []
+    for i, (_, N, K) in enumerate(mats):
+        g = torch.Generator().manual_seed(i)
+        w = (torch.randn(min(rows, N), K, generator=g) * sigma).numpy()
+        if K not in xs:
+            xs[K] = O.quantize_q8_0(workloads.activations(1, K, seed=0).numpy())
+        out.append(O.quantize_q4_0(w) + xs[K])
+    return out, f"first {rows} rows of each of the {len(mats)} decode matrices"
+
+
+def oracle_pass(prep, threads):
+    """One pass of the oracle's integer path over the sample; returns weight bytes."""
+    from oracle import oracle as O
+    for qw, dw, qx, dx in prep:
+        O.matmul_int(qw, dw, qx, dx, nthreads=threads)
+    return sum(workloads.q4_0_bytes(*p[0].shape) for p in prep)
+
+
+def cpu_oracle_sample(torch, target_s=12.0, threads=None):
+    """Time the oracle on the row sample, repeated for about `target_s`
+    seconds of CPU work.  Returns (weight GB/s, seconds, threads, description)."""
+    threads = threads or os.cpu_count() or 1
+    prep, desc = oracle_decode_sample(torch)
+    t0 = time.perf_counter()
+    nbytes, passes = 0, 0
+    while True:
+        nbytes += oracle_pass(prep, threads)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s:
+            break
+    return nbytes / dt / 1e9, dt, threads, f"{desc}, {passes} passes"
+
+
+# ---------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="qmm", choices=["qmm", "reference"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=256, help="rows per matrix per reference-arm step")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
+    args = ap.parse_args()
+    ws, rank, local = _dist()
+
+    import torch
+
+    if args.impl == "reference":
+        return main_reference(args, torch, ws, rank)
+
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from block_quantized_int4_gb300 import _build
+    if rank == 0 or ws == 1:
+        _build.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    from block_quantized_int4_gb300 import qmm
+
+    dec = TinyLlamaDecode(qmm, torch)
+    g = _graph(torch, dec.step)
+
+    # e2e through the C ABI with host buffers: pinned x in, logits out, every step
+    x_host = dec.x_in.cpu().pin_memory()
+    logits_host = torch.empty(dec.V, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        dec.x_in.copy_(x_host, non_blocking=True)
+        g.replay()
+        logits_host.copy_(dec.logits, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        g.replay()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t = _time_graph(torch, g, args.steps, 0)
+        # e2e leg
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        st = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(st)
+        torch.cuda.synchronize()
+        t_e2e = e0.elapsed_time(e1) / 1e3
+    if ws > 1:
+        tt = torch.tensor([t, t_e2e], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t, t_e2e = tt.tolist()
+        torch.distributed.barrier()
+
+    per = t / args.steps
+    value = ws * dec.weight_bytes / per / 1e9
+    e2e_value = ws * dec.weight_bytes / (t_e2e / args.steps) / 1e9
+    peak, peak_kind = _peaks()
+    achieved = dec.algo_bytes / per / 1e9
+    extras = {}
+    if not args.no_extras and rank == 0:
+        extras["gemm_batch16"] = bench_gemm_b16(qmm, torch)
+        extras["moe_T16"] = bench_moe(qmm, torch, T=16)
+        extras["moe_T1"] = bench_moe(qmm, torch, T=1)
+    cpu = None
+    if rank == 0 and ws >= 1:
+        gbs, dt, thr, desc = cpu_oracle_sample(torch, target_s=args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": thr, "kind": "oracle",
+               "sample": desc + f" ({dt:.1f} s of CPU work)"}
+    if rank == 0:
+        line = {
+            "metric": "batch-1 Q4_0xQ8_0 GEMV weight GB/s (TinyLLaMA-1.1B-shaped decode step)",
+            "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(per * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int4xint8->fp32", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations with 1% x20 outliers)",
+            "config": {"workload": workloads.TINYLLAMA["name"], "layers": dec.L, "hidden": dec.H, "ffn": dec.F,
+                       "qkv": dec.Q, "vocab": dec.V, "batch": 1, "weight_bytes_per_step": dec.weight_bytes,
+                       "launches_per_step": dec.launches_per_step, "parallelism": f"replicas x{ws}",
+                       "l2": "inputs larger than L2 (582 MB of weights per step, each read once)",
+                       "pct_of_hbm_peak": round(100 * value / ws / peak, 1)},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "kernel": "rows_kernel<1,X_F32|X_SWIGLU> (all launches of the step)",
+                         "peak_kind": peak_kind},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": dec.H * 4,
+                    "d2h_bytes_per_step": dec.V * 4},
+            "gpu_launches": dec.launches_per_step * args.steps,
+            "clocks": clk.summary(),
+            "also": extras,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main_reference(args, torch, ws, rank):
+    """The oracle on the host cores, same metric and config, bounded sample per step."""
+    if ws > 1 and rank != 0:
+        return
+    from oracle import oracle as O
+    O.build()
+    threads = os.cpu_count() or 1
+    prep, desc = oracle_decode_sample(torch, rows=args.cpu_rows)
+    desc += " per step"
+    for _ in range(args.warmup):
+        oracle_pass(prep, threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        nbytes = oracle_pass(prep, threads)
+    dt = time.perf_counter() - t0
+    value = nbytes * args.steps / dt / 1e9
+    line = {"impl": "reference", "metric": "batch-1 Q4_0xQ8_0 GEMV weight GB/s (TinyLLaMA-1.1B-shaped decode step)",
+            "value": round(value, 4), "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int4xint8->f64", "data": "synthetic",
+            "config": {"workload": workloads.TINYLLAMA["name"], "batch": 1, "sample": desc},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,395 @@
+// qmm_api.cu -- the C ABI of libqmm (declared in include/qmm.h): argument
+// validation on the host, launch configuration, error reporting.  Every
+// entry enqueues work on the caller's stream and returns; nothing here
+// allocates device memory or synchronises (except qmm_last_device_error).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "qmm.h"
+#include "qmm_kernels.cuh"
+
+using namespace qmm;
+
+// Device error word: bit ERR_BAD_EXPERT / ERR_TIMEOUT, or-ed by kernels.
+static __device__ int g_err_word;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+struct DevInfo {
+    bool ready = false;
+    bool ok = false;
+    int sms = 0;
+    int smem_optin = 0;
+    int* err = nullptr;  // device address of g_err_word
+};
+
+std::mutex g_mu;
+DevInfo g_dev[MAX_DEVICES];
+
+// Per-device facts, looked up once.  Requires an sm_103 device.
+const DevInfo* device_info() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo& d = g_dev[dev];
+    if (!d.ready) {
+        d.ready = true;
+        int major = 0, minor = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        void* p = nullptr;
+        const bool sym = cudaGetSymbolAddress(&p, g_err_word) == cudaSuccess;
+        d.err = static_cast<int*>(p);
+        d.ok = (major == 10 && minor == 3) && sym && d.sms > 0;
+        cudaGetLastError();
+    }
+    return d.ok ? &d : nullptr;
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline qmm_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+}
+
+inline cudaStream_t S(void* s) { return static_cast<cudaStream_t>(s); }
+
+// Opt a kernel into the device's full dynamic shared memory, once per
+// (kernel, device); later calls are a lookup (safe during stream capture).
+std::mutex g_attr_mu;
+std::set<std::pair<const void*, int>> g_attr_done;
+
+template <typename K>
+bool smem_optin(K kernel, int bytes, int optin) {
+    if (bytes <= 48 * 1024) return true;
+    if (bytes > optin) return false;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (g_attr_done.count(key)) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    g_attr_done.insert(key);
+    return true;
+}
+
+int grid_for(int64_t work_items, int per_sm, int sms) {
+    int64_t g = std::min<int64_t>(work_items, (int64_t)sms * per_sm);
+    return (int)std::max<int64_t>(g, 1);
+}
+
+// Launch with or without programmatic dependent launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                   Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// Rows-kernel dispatch over the token-group width MT.
+template <int MT, int XM>
+qmm_status rows_launch(const DevInfo* di, RowsArgs a, bool pdl, cudaStream_t st) {
+    const int64_t B = a.K / QK;
+    const int per_block = xtile_bytes_per_block();
+    // Stage all of K when it fits, else chunks of a multiple of 32 blocks.
+    int64_t cap = (int64_t)std::min(di->smem_optin, 200 * 1024) / (MT * per_block);
+    int64_t Bc = B <= cap ? B : std::max<int64_t>(32, cap / 32 * 32);
+    if (XM != X_Q8 && Bc < B) return QMM_ERR_SHAPE;  // fp32 prologue needs the whole row on chip
+    a.chunk_blocks = (int)Bc;
+    const int smem = (int)(MT * Bc * per_block);
+    auto kern = rows_kernel<MT, XM>;
+    if (!smem_optin(kern, smem, di->smem_optin)) return QMM_ERR_SHAPE;
+    const int64_t ntiles = (a.N + ROWS_WARPS - 1) / ROWS_WARPS;
+    const int per_sm = std::max(1, std::min(8, (di->smem_optin / std::max(smem, 1))));
+    dim3 grid(grid_for(ntiles, per_sm, di->sms), (unsigned)((a.M + MT - 1) / MT));
+    cudaError_t e = launch(kern, grid, dim3(ROWS_THREADS), smem, st, pdl, a);
+    return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
+}
+
+bool valid_k(int64_t K) { return K > 0 && K % QK == 0 && K <= (int64_t)1 << 30; }
+
+}  // namespace
+
+// ============================================================================
+extern "C" {
+
+const char* qmm_status_string(int s) {
+    switch (s) {
+        case QMM_OK: return "QMM_OK";
+        case QMM_ERR_ARG: return "QMM_ERR_ARG: null pointer or negative size";
+        case QMM_ERR_SHAPE: return "QMM_ERR_SHAPE: K not a positive multiple of 32, empty, or too large";
+        case QMM_ERR_ALIGN: return "QMM_ERR_ALIGN: pointer misaligned for the documented layout";
+        case QMM_ERR_DEVICE: return "QMM_ERR_DEVICE: current device is not sm_103";
+        case QMM_ERR_CUDA: return "QMM_ERR_CUDA: CUDA runtime call or launch failed";
+        case QMM_ERR_TIMEOUT: return "QMM_ERR_TIMEOUT: a bounded device-side wait gave up";
+        case QMM_ERR_BAD_EXPERT_ID: return "QMM_ERR_BAD_EXPERT_ID: expert id outside [0, E) skipped";
+        case QMM_ERR_WORKSPACE: return "QMM_ERR_WORKSPACE: workspace missing or too small";
+        default: return "QMM_ERR_UNKNOWN";
+    }
+}
+
+int qmm_abi_version(void) { return QMM_ABI_VERSION; }
+
+qmm_status qmm_quantize_q4_0(const float* w, int64_t N, int64_t K, int64_t ldw, uint8_t* qs, uint16_t* d,
+                             void* stream) {
+    if (N < 0 || ldw < K) return QMM_ERR_ARG;
+    if (!valid_k(K)) return QMM_ERR_SHAPE;
+    if (N == 0) return QMM_OK;
+    if (!w || !qs || !d) return QMM_ERR_ARG;
+    if (!aligned(w, 16) || ldw % 4 || !aligned(qs, 16) || !aligned(d, 2)) return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    const int64_t warps = (N * (K / QK) + 3) / 4;
+    quantize_q4_0_kernel<<<grid_for((warps + 7) / 8, 16, di->sms), 256, 0, S(stream)>>>(w, N, K, ldw, qs, d);
+    return launch_status();
+}
+
+qmm_status qmm_repack_q4_0(const uint8_t* blocks, int64_t N, int64_t K, uint8_t* qs, uint16_t* d, void* stream) {
+    if (N < 0) return QMM_ERR_ARG;
+    if (!valid_k(K)) return QMM_ERR_SHAPE;
+    if (N == 0) return QMM_OK;
+    if (!blocks || !qs || !d) return QMM_ERR_ARG;
+    if (!aligned(qs, 16) || !aligned(d, 2)) return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    const int64_t nblk = N * (K / QK);
+    repack_q4_0_kernel<<<grid_for((nblk + 255) / 256, 16, di->sms), 256, 0, S(stream)>>>(blocks, nblk, qs, d);
+    return launch_status();
+}
+
+qmm_status qmm_quantize_q8_0(const float* x, int64_t M, int64_t K, int64_t ldx, int8_t* q, uint16_t* d,
+                             void* stream) {
+    if (M < 0 || ldx < K) return QMM_ERR_ARG;
+    if (!valid_k(K)) return QMM_ERR_SHAPE;
+    if (M == 0) return QMM_OK;
+    if (!x || !q || !d) return QMM_ERR_ARG;
+    if (!aligned(x, 16) || ldx % 4 || !aligned(q, 16) || !aligned(d, 2)) return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    const int64_t warps = (M * (K / QK) + 3) / 4;
+    quantize_q8_0_kernel<<<grid_for((warps + 7) / 8, 16, di->sms), 256, 0, S(stream)>>>(x, M, K, ldx, q, d);
+    return launch_status();
+}
+
+qmm_status qmm_swiglu_quantize_q8_0(const float* gate, const float* up, int64_t rows, int64_t K, int64_t ld,
+                                    int8_t* q, uint16_t* d, float* h_out, void* stream) {
+    if (rows < 0 || ld < K) return QMM_ERR_ARG;
+    if (!valid_k(K)) return QMM_ERR_SHAPE;
+    if (rows == 0) return QMM_OK;
+    if (!gate || !up || !q || !d) return QMM_ERR_ARG;
+    if (!aligned(gate, 16) || !aligned(up, 16) || ld % 4 || !aligned(q, 16) || !aligned(d, 2) ||
+        (h_out && !aligned(h_out, 16)))
+        return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    const int64_t warps = (rows * (K / QK) + 3) / 4;
+    swiglu_quantize_kernel<<<grid_for((warps + 7) / 8, 16, di->sms), 256, 0, S(stream)>>>(gate, up, rows, K, ld, q,
+                                                                                           d, h_out);
+    return launch_status();
+}
+
+qmm_status qmm_gemv_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, const int8_t* xq,
+                              const uint16_t* xd, float* y, void* stream) {
+    return qmm_gemm_q4_0_q8_0(w_qs, w_d, N, K, 1, xq, xd, y, N, stream);
+}
+
+qmm_status qmm_gemv_q4_0_f32(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, const float* x,
+                             int gate_up, const float* residual, float* y, int8_t* xq_out, uint16_t* xd_out,
+                             int chain, void* stream) {
+    if (N < 0) return QMM_ERR_ARG;
+    if (!valid_k(K) || N == 0) return QMM_ERR_SHAPE;
+    if (!w_qs || !w_d || !x || !y) return QMM_ERR_ARG;
+    if (K > 40960) return QMM_ERR_SHAPE;
+    if (!aligned(w_qs, 16) || !aligned(w_d, 2) || !aligned(x, 16) || !aligned(y, 4) ||
+        (residual && !aligned(residual, 4)) || (xq_out && !aligned(xq_out, 16)) || (xd_out && !aligned(xd_out, 2)))
+        return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    RowsArgs a = {};
+    a.residual = residual;
+    a.qs = w_qs;
+    a.d = w_d;
+    a.N = N;
+    a.K = K;
+    a.M = 1;
+    a.xf = x;
+    a.xq_out = xq_out;
+    a.xd_out = xd_out;
+    a.y = y;
+    a.ldy = N;
+    return gate_up ? rows_launch<1, X_SWIGLU>(di, a, chain != 0, S(stream))
+                   : rows_launch<1, X_F32>(di, a, chain != 0, S(stream));
+}
+
+qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,
+                              const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy, void* stream) {
+    if (N < 0 || M < 0 || ldy < N) return QMM_ERR_ARG;
+    if (!valid_k(K) || N == 0 || M == 0 || M > 65535 * 8) return QMM_ERR_SHAPE;
+    if (!w_qs || !w_d || !xq || !xd || !y) return QMM_ERR_ARG;
+    if (!aligned(w_qs, 16) || !aligned(w_d, 2) || !aligned(xq, 16) || !aligned(xd, 2) || !aligned(y, 4))
+        return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    RowsArgs a = {};
+    a.qs = w_qs;
+    a.d = w_d;
+    a.N = N;
+    a.K = K;
+    a.M = M;
+    a.xq = xq;
+    a.xd = xd;
+    a.y = y;
+    a.ldy = ldy;
+    cudaStream_t st = S(stream);
+    if (M == 1) return rows_launch<1, X_Q8>(di, a, false, st);
+    if (M == 2) return rows_launch<2, X_Q8>(di, a, false, st);
+    if (M <= 4) return rows_launch<4, X_Q8>(di, a, false, st);
+    return rows_launch<8, X_Q8>(di, a, false, st);
+}
+
+qmm_status qmm_debug_block_dots(const uint8_t* w_qs, int64_t N, int64_t K, int64_t M, const int8_t* xq,
+                                int32_t* dots, void* stream) {
+    if (N < 0 || M < 0) return QMM_ERR_ARG;
+    if (!valid_k(K) || N == 0 || M == 0) return QMM_ERR_SHAPE;
+    if (!w_qs || !xq || !dots) return QMM_ERR_ARG;
+    if (!aligned(w_qs, 16) || !aligned(xq, 16) || !aligned(dots, 4)) return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    const int64_t total = M * N * (K / QK);
+    block_dots_kernel<<<grid_for((total + 255) / 256, 16, di->sms), 256, 0, S(stream)>>>(w_qs, N, K, M, xq, dots);
+    return launch_status();
+}
+
+qmm_status qmm_moe_workspace_size(int32_t E, int32_t T, int32_t k, size_t* bytes) {
+    if (!bytes || E <= 0 || T < 0 || k <= 0) return QMM_ERR_ARG;
+    *bytes = moe_ws_bytes(E, (int64_t)T * k);
+    return QMM_OK;
+}
+
+qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K, const int32_t* ids,
+                        int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd, int x_per_slot, float* y,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    if (E <= 0 || N <= 0 || T < 0 || k <= 0) return QMM_ERR_ARG;
+    if (!valid_k(K) || (int64_t)T * k > (1 << 24)) return QMM_ERR_SHAPE;
+    if (T == 0) return QMM_OK;
+    if (!w_qs || !w_d || !ids || !xq || !xd || !y) return QMM_ERR_ARG;
+    if (!workspace || workspace_bytes < moe_ws_bytes(E, (int64_t)T * k)) return QMM_ERR_WORKSPACE;
+    if (!aligned(w_qs, 16) || !aligned(w_d, 2) || !aligned(xq, 16) || !aligned(xd, 2) || !aligned(y, 4) ||
+        !aligned(ids, 4) || !aligned(workspace, 16))
+        return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    cudaStream_t st = S(stream);
+    MoeWs ws = moe_ws(workspace, E);
+    moe_group_kernel<<<1, GROUP_THREADS, 0, st>>>(ids, T * k, E, ws, di->err);
+    qmm_status s = launch_status();
+    if (s != QMM_OK) return s;
+
+    MoeArgs a = {};
+    a.qs = w_qs;
+    a.d = w_d;
+    a.N = N;
+    a.K = K;
+    a.E = E;
+    a.k = k;
+    a.xq = xq;
+    a.xd = xd;
+    a.x_per_slot = x_per_slot;
+    a.y = y;
+    a.ws = ws;
+    a.rows_per_item = 8 * ROWS_WARPS;
+    const int64_t B = K / QK;
+    const int per_block = xtile_bytes_per_block();
+    const int64_t cap = std::min(di->smem_optin, 200 * 1024);
+    // Token-group width: widest that stages the whole K.
+    int mt = 8;
+    while (mt > 1 && (int64_t)mt * B * per_block > cap) mt /= 2;
+    if ((int64_t)mt * B * per_block > cap) return QMM_ERR_SHAPE;
+    // Tokens per expert on average decides how wide a group is useful.
+    const int64_t nslots = (int64_t)T * k;
+    const int64_t max_slots = std::min<int64_t>(nslots, 8);
+    while (mt > 1 && mt / 2 >= max_slots) mt /= 2;
+    const int smem = (int)(mt * B * per_block);
+    const int64_t row_blocks = (N + a.rows_per_item - 1) / a.rows_per_item;
+    const int64_t max_items = std::min<int64_t>(E, nslots) * row_blocks;
+    const int per_sm = std::max(1, std::min(4, di->smem_optin / std::max(smem, 1)));
+    dim3 grid(grid_for(max_items, per_sm, di->sms));
+    cudaError_t e;
+    switch (mt) {
+        case 8:
+            if (!smem_optin(moe_rows_kernel<8>, smem, di->smem_optin)) return QMM_ERR_SHAPE;
+            e = launch(moe_rows_kernel<8>, grid, dim3(ROWS_THREADS), smem, st, false, a);
+            break;
+        case 4:
+            if (!smem_optin(moe_rows_kernel<4>, smem, di->smem_optin)) return QMM_ERR_SHAPE;
+            e = launch(moe_rows_kernel<4>, grid, dim3(ROWS_THREADS), smem, st, false, a);
+            break;
+        case 2:
+            if (!smem_optin(moe_rows_kernel<2>, smem, di->smem_optin)) return QMM_ERR_SHAPE;
+            e = launch(moe_rows_kernel<2>, grid, dim3(ROWS_THREADS), smem, st, false, a);
+            break;
+        default:
+            if (!smem_optin(moe_rows_kernel<1>, smem, di->smem_optin)) return QMM_ERR_SHAPE;
+            e = launch(moe_rows_kernel<1>, grid, dim3(ROWS_THREADS), smem, st, false, a);
+            break;
+    }
+    return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
+}
+
+qmm_status qmm_moe_combine(const float* z, const float* gates, int32_t T, int32_t k, int64_t N, float* y,
+                           void* stream) {
+    if (T < 0 || k <= 0 || N <= 0) return QMM_ERR_ARG;
+    if (T == 0) return QMM_OK;
+    if (!z || !gates || !y) return QMM_ERR_ARG;
+    if (!aligned(z, 4) || !aligned(gates, 4) || !aligned(y, 4)) return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    const int64_t total = (int64_t)T * N;
+    moe_combine_kernel<<<grid_for((total + 255) / 256, 16, di->sms), 256, 0, S(stream)>>>(z, gates, T, k, N, y);
+    return launch_status();
+}
+
+qmm_status qmm_last_device_error(void* stream) {
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    if (cudaStreamSynchronize(S(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return QMM_ERR_CUDA;
+    }
+    int v = 0;
+    if (cudaMemcpy(&v, di->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return QMM_ERR_CUDA;
+    if (v) {
+        const int zero = 0;
+        if (cudaMemcpy(di->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return QMM_ERR_CUDA;
+    }
+    if (v & ERR_TIMEOUT) return QMM_ERR_TIMEOUT;
+    if (v & ERR_BAD_EXPERT) return QMM_ERR_BAD_EXPERT_ID;
+    return QMM_OK;
+}
+
+}  // extern "C"

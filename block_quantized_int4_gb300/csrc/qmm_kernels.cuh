@@ -1,0 +1,568 @@
+// qmm_kernels.cuh -- the libqmm CUDA kernels (CUDA-core paths):
+//   quantize_q8_0 / quantize_q4_0 / repack / swiglu+quantize   (set-up and a1, a8)
+//   rows kernel: batch-1 GEMV and small-batch GEMM with dp4a   (a2-a6)
+//   MoE grouping, expert-grouped GEMV and combine              (a7)
+//   per-block debug dots
+//
+// Method: llama.cpp guide (kenji.blog/id) section 2.2; Q4_0 block format:
+// TinyLLaMA C++ guide (kenji.blog) section 6.1; Q8_0-style activations and
+// the routed-expert MoE: Colibri page (kerneldigest.dev), "Arquitectura del
+// Sistema"; SwiGLU: TinyLLaMA guide section 4.4.
+#pragma once
+
+#include "qmm_device.cuh"
+
+namespace qmm {
+
+// ============================================================================
+// Quantizers
+// ============================================================================
+
+// Codes of one block spread over 8 lanes (4 values each).  qmax 127 (Q8_0)
+// or 7 (Q4_0); codes are clamped to [qlo, qmax].
+struct Quad {
+    int c[4];
+    float d32;
+};
+
+__device__ __forceinline__ Quad quad_codes(float4 v, float qmax, float qlo) {
+    float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 4));
+    Quad r;
+    r.d32 = __fdiv_rn(a, qmax);
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (a != 0.0f) {
+            float t = roundf(__fdiv_rn(vv[i], r.d32));
+            r.c[i] = (int)fminf(fmaxf(t, qlo), qmax);
+        } else {
+            r.c[i] = 0;
+        }
+    }
+    return r;
+}
+
+// x [M][K] fp32 -> q [M][K] int8, d [M][B] fp16 bits.  Each warp handles 4
+// blocks per step (8 lanes per block, one float4 per lane).
+__global__ void quantize_q8_0_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
+                                     int8_t* __restrict__ q, uint16_t* __restrict__ d) {
+    const int64_t B = K / QK;
+    const int64_t nblk = M * B;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t g = warp; g * 4 < nblk; g += nwarps) {
+        const int64_t blk = g * 4 + (lane >> 3);
+        const bool valid = blk < nblk;
+        int64_t m = 0, b = 0;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
+            m = blk / B;
+            b = blk - m * B;
+            v = *reinterpret_cast<const float4*>(x + m * ldx + b * QK + (lane & 7) * 4);
+        }
+        Quad r = quad_codes(v, 127.0f, -127.0f);
+        if (valid) {
+            int packed = (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) | ((r.c[3] & 0xff) << 24);
+            *reinterpret_cast<int*>(q + m * K + b * QK + (lane & 7) * 4) = packed;
+            if ((lane & 7) == 0) d[m * B + b] = f32_to_f16_bits(r.d32);
+        }
+    }
+}
+
+// SwiGLU(gate, up) then Q8_0, row by row; optional fp32 h out.
+__global__ void swiglu_quantize_kernel(const float* __restrict__ gate, const float* __restrict__ up, int64_t rows,
+                                       int64_t K, int64_t ld, int8_t* __restrict__ q, uint16_t* __restrict__ d,
+                                       float* __restrict__ h_out) {
+    const int64_t B = K / QK;
+    const int64_t nblk = rows * B;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t g = warp; g * 4 < nblk; g += nwarps) {
+        const int64_t blk = g * 4 + (lane >> 3);
+        const bool valid = blk < nblk;
+        int64_t m = 0, b = 0;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
+            m = blk / B;
+            b = blk - m * B;
+            const int64_t off = m * ld + b * QK + (lane & 7) * 4;
+            float4 gg = *reinterpret_cast<const float4*>(gate + off);
+            float4 uu = *reinterpret_cast<const float4*>(up + off);
+            v = make_float4(swiglu1(gg.x, uu.x), swiglu1(gg.y, uu.y), swiglu1(gg.z, uu.z), swiglu1(gg.w, uu.w));
+            if (h_out) *reinterpret_cast<float4*>(h_out + off) = v;
+        }
+        Quad r = quad_codes(v, 127.0f, -127.0f);
+        if (valid) {
+            int packed = (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) | ((r.c[3] & 0xff) << 24);
+            *reinterpret_cast<int*>(q + m * K + b * QK + (lane & 7) * 4) = packed;
+            if ((lane & 7) == 0) d[m * B + b] = f32_to_f16_bits(r.d32);
+        }
+    }
+}
+
+// w [N][K] fp32 -> Q4_0 planes.  Lane i of a block group holds elements
+// 4i..4i+3; lanes 0..3 (elements 0..15) pair with lanes 4..7 (16..31) to
+// form bytes u[j] | u[j+16] << 4.
+__global__ void quantize_q4_0_kernel(const float* __restrict__ w, int64_t N, int64_t K, int64_t ldw,
+                                     uint8_t* __restrict__ qs, uint16_t* __restrict__ d) {
+    const int64_t B = K / QK;
+    const int64_t nblk = N * B;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t g = warp; g * 4 < nblk; g += nwarps) {
+        const int64_t blk = g * 4 + (lane >> 3);
+        const bool valid = blk < nblk;
+        int64_t n = 0, b = 0;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
+            n = blk / B;
+            b = blk - n * B;
+            v = *reinterpret_cast<const float4*>(w + n * ldw + b * QK + (lane & 7) * 4);
+        }
+        Quad r = quad_codes(v, 7.0f, -8.0f);
+        unsigned u = (unsigned)(r.c[0] + 8) | ((unsigned)(r.c[1] + 8) << 8) | ((unsigned)(r.c[2] + 8) << 16) |
+                     ((unsigned)(r.c[3] + 8) << 24);
+        unsigned hi = __shfl_down_sync(FULL, u, 4);
+        if (valid && (lane & 7) < 4) {
+            *reinterpret_cast<unsigned*>(qs + blk * 16 + (lane & 7) * 4) = u | (hi << 4);
+            if ((lane & 7) == 0) d[blk] = f32_to_f16_bits(r.d32);
+        }
+    }
+}
+
+// Page-format 18-byte blocks -> planes.  One thread per block.
+__global__ void repack_q4_0_kernel(const uint8_t* __restrict__ blocks, int64_t nblk, uint8_t* __restrict__ qs,
+                                   uint16_t* __restrict__ d) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblk; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint8_t* src = blocks + i * 18;
+        d[i] = (uint16_t)(src[0] | (src[1] << 8));
+        unsigned wds[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            wds[k] = (unsigned)src[2 + 4 * k] | ((unsigned)src[3 + 4 * k] << 8) | ((unsigned)src[4 + 4 * k] << 16) |
+                     ((unsigned)src[5 + 4 * k] << 24);
+        *reinterpret_cast<uint4*>(qs + i * 16) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+    }
+}
+
+// ============================================================================
+// Rows kernel: y[m][n] = sum_b d_w * d_x * dot over a row tile, with the
+// activation block(s) staged in shared memory and weights streamed with
+// 16-byte loads.  One warp per row; lane l takes blocks l, l+32, ...
+// ============================================================================
+
+// Shared-memory image of MT activation rows over Bc blocks: 16-byte halves
+// of each block in two planes (so a warp's 16-byte reads are contiguous and
+// bank-conflict free), the fp32 scale and the block's code sum.
+struct XTile {
+    int4* lo;
+    int4* hi;
+    float* s;
+    int* sum;
+};
+
+__device__ __forceinline__ XTile xtile_at(void* smem, int MT, int Bc) {
+    XTile t;
+    t.lo = reinterpret_cast<int4*>(smem);
+    t.hi = t.lo + MT * Bc;
+    t.s = reinterpret_cast<float*>(t.hi + MT * Bc);
+    t.sum = reinterpret_cast<int*>(t.s + MT * Bc);
+    return t;
+}
+
+__host__ __device__ constexpr int xtile_bytes_per_block() { return 16 + 16 + 4 + 4; }
+
+__device__ __forceinline__ int block_qsum(int4 lo, int4 hi) {
+    const int ones = 0x01010101;
+    int s = 0;
+    s = __dp4a(lo.x, ones, s);
+    s = __dp4a(lo.y, ones, s);
+    s = __dp4a(lo.z, ones, s);
+    s = __dp4a(lo.w, ones, s);
+    s = __dp4a(hi.x, ones, s);
+    s = __dp4a(hi.y, ones, s);
+    s = __dp4a(hi.z, ones, s);
+    s = __dp4a(hi.w, ones, s);
+    return s;
+}
+
+// Copy Q8_0 rows into the tile: tile row t <- activation row xrow[t]
+// (xrow[t] < 0: zero fill).  Blocks [b0, b0 + nb).  Whole CTA.
+template <int MT>
+__device__ __forceinline__ void stage_q8(const XTile& xt, int Bc, const int8_t* __restrict__ xq,
+                                         const uint16_t* __restrict__ xd, int64_t K, const int64_t* xrow, int b0,
+                                         int nb) {
+    const int64_t B = K / QK;
+    for (int i = threadIdx.x; i < MT * Bc; i += blockDim.x) {
+        const int t = i / Bc, b = i - t * Bc;
+        int4 lo = make_int4(0, 0, 0, 0), hi = lo;
+        float s = 0.f;
+        if (xrow[t] >= 0 && b < nb) {
+            const int8_t* src = xq + xrow[t] * K + (int64_t)(b0 + b) * QK;
+            lo = *reinterpret_cast<const int4*>(src);
+            hi = *reinterpret_cast<const int4*>(src + 16);
+            s = f16_bits_to_f32(xd[xrow[t] * B + b0 + b]);
+        }
+        xt.lo[i] = lo;
+        xt.hi[i] = hi;
+        xt.s[i] = s;
+        xt.sum[i] = block_qsum(lo, hi);
+    }
+}
+
+// Quantize one fp32 activation row (K values; or SwiGLU of gate = x[0..K),
+// up = x[K..2K)) straight into tile row 0.  CTA 0 also writes the Q8_0
+// result out when xq_out/xd_out are given.  Whole CTA; blockDim % 32 == 0.
+template <bool GATE_UP>
+__device__ __forceinline__ void stage_f32(const XTile& xt, const float* __restrict__ x, int64_t K,
+                                          int8_t* __restrict__ xq_out, uint16_t* __restrict__ xd_out) {
+    const int B = (int)(K / QK);
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const bool writer = blockIdx.x == 0 && blockIdx.y == 0;
+    for (int g = warp; g * 4 < B; g += nwarps) {
+        const int b = g * 4 + (lane >> 3);
+        const int part = lane & 7;  // which 4 values of the block
+        const bool valid = b < B;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (valid) {
+            const int64_t off = (int64_t)b * QK + part * 4;
+            v = *reinterpret_cast<const float4*>(x + off);
+            if (GATE_UP) {
+                float4 u = *reinterpret_cast<const float4*>(x + K + off);
+                v = make_float4(swiglu1(v.x, u.x), swiglu1(v.y, u.y), swiglu1(v.z, u.z), swiglu1(v.w, u.w));
+            }
+        }
+        Quad r = quad_codes(v, 127.0f, -127.0f);
+        const int packed = (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) | ((r.c[3] & 0xff) << 24);
+        int s = r.c[0] + r.c[1] + r.c[2] + r.c[3];
+        s += __shfl_xor_sync(FULL, s, 1);
+        s += __shfl_xor_sync(FULL, s, 2);
+        s += __shfl_xor_sync(FULL, s, 4);
+        if (valid) {
+            int* plane = reinterpret_cast<int*>(part < 4 ? &xt.lo[b] : &xt.hi[b]);
+            plane[part & 3] = packed;
+            if (part == 0) {
+                const unsigned short h = f32_to_f16_bits(r.d32);
+                xt.s[b] = f16_bits_to_f32(h);
+                xt.sum[b] = s;
+                if (writer && xd_out) xd_out[b] = h;
+            }
+            if (writer && xq_out) *reinterpret_cast<int*>(xq_out + (int64_t)b * QK + part * 4) = packed;
+        }
+    }
+}
+
+// Accumulate one weight row against MT staged activation rows, blocks
+// [0, nb) of the tile (weight blocks wq/wd already offset to the tile's b0).
+template <int MT>
+__device__ __forceinline__ void row_accumulate(const XTile& xt, int Bc, const uint8_t* __restrict__ wq,
+                                               const uint16_t* __restrict__ wd, int nb, int lane, float (&acc)[MT]) {
+    constexpr int U = 4;
+    int b = lane;
+    for (; b + 32 * (U - 1) < nb; b += 32 * U) {
+        uint4 w[U];
+        float dw[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            w[u] = ld_stream_v4(wq + (int64_t)(b + 32 * u) * 16);
+            dw[u] = f16_bits_to_f32(ld_stream_u16(wd + b + 32 * u));
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int bb = b + 32 * u;
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                const int i = t * Bc + bb;
+                const int dot = block_dot_u(w[u], xt.lo[i], xt.hi[i]) - 8 * xt.sum[i];
+                acc[t] = fmaf(dw[u] * xt.s[i], (float)dot, acc[t]);
+            }
+        }
+    }
+    for (; b < nb; b += 32) {
+        const uint4 w = ld_stream_v4(wq + (int64_t)b * 16);
+        const float dw = f16_bits_to_f32(ld_stream_u16(wd + b));
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+            const int i = t * Bc + b;
+            const int dot = block_dot_u(w, xt.lo[i], xt.hi[i]) - 8 * xt.sum[i];
+            acc[t] = fmaf(dw * xt.s[i], (float)dot, acc[t]);
+        }
+    }
+}
+
+enum XMode { X_Q8 = 0, X_F32 = 1, X_SWIGLU = 2 };
+
+struct RowsArgs {
+    const uint8_t* qs;
+    const uint16_t* d;
+    int64_t N, K;
+    int64_t M;          // tokens
+    const int8_t* xq;   // X_Q8
+    const uint16_t* xd;
+    const float* xf;    // X_F32 / X_SWIGLU (M == 1)
+    const float* residual;  // optional, added to y (fp32 modes, M == 1)
+    int8_t* xq_out;     // optional Q8_0 copy of the activation (fp32 modes)
+    uint16_t* xd_out;
+    float* y;
+    int64_t ldy;
+    int chunk_blocks;   // Bc: blocks of K staged at once
+};
+
+constexpr int ROWS_THREADS = 256;
+constexpr int ROWS_WARPS = ROWS_THREADS / 32;
+
+// Grid: x = row tiles (ROWS_WARPS rows each, grid-stride), y = token groups
+// of MT.  Dynamic shared memory: MT * Bc * 40 bytes.
+template <int MT, int XMODE>
+__global__ void __launch_bounds__(ROWS_THREADS) rows_kernel(RowsArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    // Let a dependent launch (programmatic stream serialization) start its
+    // prologue; it still waits for this grid before touching our outputs.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    const int Bc = a.chunk_blocks;
+    const XTile xt = xtile_at(smem_raw, MT, Bc);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t B = a.K / QK;
+    const int nchunks = (int)((B + Bc - 1) / Bc);
+    const int64_t m0 = (int64_t)blockIdx.y * MT;
+    int64_t xrow[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) xrow[t] = (m0 + t < a.M) ? m0 + t : -1;
+
+    // The activation is produced by the preceding kernel: wait for it.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    if (nchunks == 1) {
+        if (XMODE == X_Q8) stage_q8<MT>(xt, Bc, a.xq, a.xd, a.K, xrow, 0, (int)B);
+        else stage_f32<XMODE == X_SWIGLU>(xt, a.xf, a.K, a.xq_out, a.xd_out);
+        __syncthreads();
+    }
+    const int64_t ntiles = (a.N + ROWS_WARPS - 1) / ROWS_WARPS;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t row = tile * ROWS_WARPS + warp;
+        float acc[MT];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+        for (int c = 0; c < nchunks; ++c) {
+            const int b0 = c * Bc;
+            const int nb = (int)min((int64_t)Bc, B - b0);
+            if (nchunks > 1) {
+                __syncthreads();
+                stage_q8<MT>(xt, Bc, a.xq, a.xd, a.K, xrow, b0, nb);
+                __syncthreads();
+            }
+            if (row < a.N) row_accumulate<MT>(xt, Bc, a.qs + (row * B + b0) * 16, a.d + row * B + b0, nb, lane, acc);
+        }
+        if (row < a.N) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                float v = warp_sum(acc[t]);
+                if (lane == 0 && xrow[t] >= 0) {
+                    if (XMODE != X_Q8 && a.residual) v += a.residual[row];
+                    a.y[xrow[t] * a.ldy + row] = v;
+                }
+            }
+        }
+    }
+}
+
+// ============================================================================
+// Debug: per-block integer dots with the same unpack/dot code.
+// ============================================================================
+__global__ void block_dots_kernel(const uint8_t* __restrict__ qs, int64_t N, int64_t K, int64_t M,
+                                  const int8_t* __restrict__ xq, int32_t* __restrict__ dots) {
+    const int64_t B = K / QK;
+    const int64_t total = M * N * B;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = i % B, n = (i / B) % N, m = i / (B * N);
+        const uint4 w = *reinterpret_cast<const uint4*>(qs + (n * B + b) * 16);
+        const int4 lo = *reinterpret_cast<const int4*>(xq + m * K + b * QK);
+        const int4 hi = *reinterpret_cast<const int4*>(xq + m * K + b * QK + 16);
+        dots[i] = block_dot_u(w, lo, hi) - 8 * block_qsum(lo, hi);
+    }
+}
+
+// ============================================================================
+// MoE: group slots by expert, expert-grouped rows kernel, combine.
+// ============================================================================
+
+// Workspace (int32 words): counts[E] | offsets[E+1] | cursor[E] | active[E]
+// | n_active[1] | slot_list[T*k]
+struct MoeWs {
+    int* counts;
+    int* offsets;
+    int* cursor;
+    int* active;
+    int* n_active;
+    int* slots;
+};
+
+__host__ __device__ inline MoeWs moe_ws(void* base, int E) {
+    MoeWs w;
+    w.counts = reinterpret_cast<int*>(base);
+    w.offsets = w.counts + E;
+    w.cursor = w.offsets + E + 1;
+    w.active = w.cursor + E;
+    w.n_active = w.active + E;
+    w.slots = w.n_active + 1;
+    return w;
+}
+
+__host__ __device__ inline size_t moe_ws_bytes(int E, int64_t nslots) {
+    size_t words = (size_t)E * 4 + 2 + (size_t)nslots;
+    return (words * 4 + 15) / 16 * 16;
+}
+
+// One CTA.  Counting sort of slots by expert id; slots inside one expert's
+// list come out in any order (each slot's output is computed on its own,
+// so the order does not change any result).
+constexpr int GROUP_THREADS = 1024;
+
+__global__ void __launch_bounds__(GROUP_THREADS) moe_group_kernel(const int32_t* __restrict__ ids, int nslots, int E,
+                                                                  MoeWs w, int* err) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) w.counts[e] = 0;
+    __syncthreads();
+    for (int s = threadIdx.x; s < nslots; s += blockDim.x) {
+        const int e = ids[s];
+        if (e < 0 || e >= E) {
+            atomicOr(err, ERR_BAD_EXPERT);
+            continue;
+        }
+        atomicAdd(&w.counts[e], 1);
+    }
+    __syncthreads();
+    // Exclusive scans of counts (-> offsets) and of (counts > 0) (-> active
+    // positions), each thread owning a contiguous chunk of experts.
+    const int per = (E + blockDim.x - 1) / blockDim.x;
+    const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
+    int csum = 0, asum = 0;
+    for (int e = e0; e < e1; ++e) {
+        csum += w.counts[e];
+        asum += w.counts[e] > 0;
+    }
+    // block-wide exclusive scan of (csum, asum) packed into one 64-bit lane value
+    long long v = ((long long)csum << 32) | (unsigned)asum;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    long long incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        long long n = __shfl_up_sync(FULL, incl, o);
+        if (lane >= o) incl += n;
+    }
+    __shared__ long long wsum[32];
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        long long t = (lane < (int)(blockDim.x >> 5)) ? wsum[lane] : 0;
+        for (int o = 1; o < 32; o <<= 1) {
+            long long n = __shfl_up_sync(FULL, t, o);
+            if (lane >= o) t += n;
+        }
+        wsum[lane] = t;  // inclusive over warps
+    }
+    __syncthreads();
+    long long excl = incl - v + (wid > 0 ? wsum[wid - 1] : 0);
+    int coff = (int)(excl >> 32), aoff = (int)(excl & 0xffffffff);
+    for (int e = e0; e < e1; ++e) {
+        const int c = w.counts[e];
+        w.offsets[e] = coff;
+        w.cursor[e] = coff;
+        if (c > 0) w.active[aoff++] = e;
+        coff += c;
+    }
+    if (threadIdx.x == blockDim.x - 1) {
+        w.offsets[E] = coff;
+        *w.n_active = aoff;
+    }
+    __syncthreads();
+    for (int s = threadIdx.x; s < nslots; s += blockDim.x) {
+        const int e = ids[s];
+        if (e < 0 || e >= E) continue;
+        const int pos = atomicAdd(&w.cursor[e], 1);
+        w.slots[pos] = s;
+    }
+}
+
+struct MoeArgs {
+    const uint8_t* qs;
+    const uint16_t* d;
+    int64_t N, K;
+    int E, k;
+    const int8_t* xq;
+    const uint16_t* xd;
+    int x_per_slot;
+    float* y;
+    MoeWs ws;
+    int rows_per_item;  // multiple of ROWS_WARPS
+};
+
+// Work item = (active expert a, block of rows_per_item rows).  For each
+// group of MT slots routed to the expert: stage their activations, then each
+// warp applies its rows (rows_per_item / ROWS_WARPS of them) to all staged
+// slots.  The whole K is staged at once (host checks it fits).
+template <int MT>
+__global__ void __launch_bounds__(ROWS_THREADS) moe_rows_kernel(MoeArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int64_t B = a.K / QK;
+    const int Bc = (int)B;
+    const XTile xt = xtile_at(smem_raw, MT, Bc);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t row_blocks = (a.N + a.rows_per_item - 1) / a.rows_per_item;
+    const int n_active = *a.ws.n_active;
+    const int64_t total = (int64_t)n_active * row_blocks;
+    const int64_t e_qs = a.N * B * 16, e_d = a.N * B;
+    for (int64_t item = blockIdx.x; item < total; item += gridDim.x) {
+        const int ai = (int)(item / row_blocks);
+        const int64_t r0 = (item - (int64_t)ai * row_blocks) * a.rows_per_item;
+        const int e = a.ws.active[ai];
+        const int s_begin = a.ws.offsets[e], s_end = a.ws.offsets[e + 1];
+        const uint8_t* qs = a.qs + (int64_t)e * e_qs;
+        const uint16_t* dd = a.d + (int64_t)e * e_d;
+        for (int s0 = s_begin; s0 < s_end; s0 += MT) {
+            int64_t xrow[MT];
+            int slot[MT];
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                slot[t] = (s0 + t < s_end) ? a.ws.slots[s0 + t] : -1;
+                xrow[t] = slot[t] < 0 ? -1 : (a.x_per_slot ? slot[t] : slot[t] / a.k);
+            }
+            __syncthreads();
+            stage_q8<MT>(xt, Bc, a.xq, a.xd, a.K, xrow, 0, Bc);
+            __syncthreads();
+            for (int64_t row = r0 + warp; row < min(a.N, r0 + a.rows_per_item); row += ROWS_WARPS) {
+                float acc[MT];
+#pragma unroll
+                for (int t = 0; t < MT; ++t) acc[t] = 0.f;
+                row_accumulate<MT>(xt, Bc, qs + row * B * 16, dd + row * B, Bc, lane, acc);
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    const float v = warp_sum(acc[t]);
+                    if (lane == 0 && slot[t] >= 0) a.y[(int64_t)slot[t] * a.N + row] = v;
+                }
+            }
+        }
+    }
+}
+
+// y[t][n] = sum_j g[t][j] * z[t][j][n], j ascending.
+__global__ void moe_combine_kernel(const float* __restrict__ z, const float* __restrict__ gates, int T, int k,
+                                   int64_t N, float* __restrict__ y) {
+    const int64_t total = (int64_t)T * N;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / N, n = i - t * N;
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) acc = fmaf(gates[t * k + j], z[(t * k + j) * N + n], acc);
+        y[i] = acc;
+    }
+}
+
+}  // namespace qmm

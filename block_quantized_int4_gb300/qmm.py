@@ -1,0 +1,194 @@
+"""Thin ctypes binding of libqmm (include/qmm.h).
+
+Argument marshalling only: every ``qmm_*`` function here has the C entry
+point's name and argument order; tensors become device pointers
+(``data_ptr()``), ``None`` becomes NULL, ints pass through, and the stream
+defaults to torch's current CUDA stream.  A nonzero status raises
+``QmmError``.  All arithmetic runs in the CUDA kernels of libqmm.so; if the
+library is missing this module raises on import -- there is no fallback.
+
+A few helpers at the bottom allocate outputs with torch and call the entry
+points (``quantize_q8_0``, ``quantize_q4_0``, ``gemv``, ``gemm``, ...).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqmm.so")
+QK = 32
+
+STATUS = {0: "QMM_OK", 1: "QMM_ERR_ARG", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_ALIGN", 4: "QMM_ERR_DEVICE",
+          5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT", 7: "QMM_ERR_BAD_EXPERT_ID", 8: "QMM_ERR_WORKSPACE"}
+
+
+class QmmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_lib.qmm_status_string(status).decode()} (status {status})")
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libqmm.so not built at {LIB_PATH}: run __graft_entry__.build() "
+                      "(no CPU fallback exists)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+_P, _I64, _I32, _INT, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int, ctypes.c_size_t
+
+# name -> argtypes (the trailing stream is a void*)
+SIGNATURES = {
+    "qmm_quantize_q4_0": [_P, _I64, _I64, _I64, _P, _P, _P],
+    "qmm_repack_q4_0": [_P, _I64, _I64, _P, _P, _P],
+    "qmm_quantize_q8_0": [_P, _I64, _I64, _I64, _P, _P, _P],
+    "qmm_swiglu_quantize_q8_0": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
+    "qmm_gemv_q4_0_q8_0": [_P, _P, _I64, _I64, _P, _P, _P, _P],
+    "qmm_gemv_q4_0_f32": [_P, _P, _I64, _I64, _P, _INT, _P, _P, _P, _P, _INT, _P],
+    "qmm_gemm_q4_0_q8_0": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P],
+    "qmm_debug_block_dots": [_P, _I64, _I64, _I64, _P, _P, _P],
+    "qmm_moe_workspace_size": [_I32, _I32, _I32, ctypes.POINTER(_SZ)],
+    "qmm_moe_gemv": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
+    "qmm_moe_combine": [_P, _P, _I32, _I32, _I64, _P, _P],
+    "qmm_last_device_error": [_P],
+}
+for _name, _args in SIGNATURES.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = ctypes.c_int
+_lib.qmm_status_string.argtypes = [ctypes.c_int]
+_lib.qmm_status_string.restype = ctypes.c_char_p
+_lib.qmm_abi_version.argtypes = []
+_lib.qmm_abi_version.restype = ctypes.c_int
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise QmmError(st, where)
+
+
+def status_string(status: int) -> str:
+    return _lib.qmm_status_string(status).decode()
+
+
+def abi_version() -> int:
+    return _lib.qmm_abi_version()
+
+
+def library_handle():
+    return _lib
+
+
+# ------------------------------------------------------------------ raw entry points
+def qmm_quantize_q4_0(w, N, K, ldw, qs, d, stream=None):
+    _check(_lib.qmm_quantize_q4_0(_ptr(w), N, K, ldw, _ptr(qs), _ptr(d), _stream(stream)), "qmm_quantize_q4_0")
+
+
+def qmm_repack_q4_0(blocks, N, K, qs, d, stream=None):
+    _check(_lib.qmm_repack_q4_0(_ptr(blocks), N, K, _ptr(qs), _ptr(d), _stream(stream)), "qmm_repack_q4_0")
+
+
+def qmm_quantize_q8_0(x, M, K, ldx, q, d, stream=None):
+    _check(_lib.qmm_quantize_q8_0(_ptr(x), M, K, ldx, _ptr(q), _ptr(d), _stream(stream)), "qmm_quantize_q8_0")
+
+
+def qmm_swiglu_quantize_q8_0(gate, up, rows, K, ld, q, d, h_out=None, stream=None):
+    _check(_lib.qmm_swiglu_quantize_q8_0(_ptr(gate), _ptr(up), rows, K, ld, _ptr(q), _ptr(d), _ptr(h_out),
+                                         _stream(stream)), "qmm_swiglu_quantize_q8_0")
+
+
+def qmm_gemv_q4_0_q8_0(w_qs, w_d, N, K, xq, xd, y, stream=None):
+    _check(_lib.qmm_gemv_q4_0_q8_0(_ptr(w_qs), _ptr(w_d), N, K, _ptr(xq), _ptr(xd), _ptr(y), _stream(stream)),
+           "qmm_gemv_q4_0_q8_0")
+
+
+def qmm_gemv_q4_0_f32(w_qs, w_d, N, K, x, gate_up, residual, y, xq_out=None, xd_out=None, chain=0, stream=None):
+    _check(_lib.qmm_gemv_q4_0_f32(_ptr(w_qs), _ptr(w_d), N, K, _ptr(x), int(gate_up), _ptr(residual), _ptr(y),
+                                  _ptr(xq_out), _ptr(xd_out), int(chain), _stream(stream)), "qmm_gemv_q4_0_f32")
+
+
+def qmm_gemm_q4_0_q8_0(w_qs, w_d, N, K, M, xq, xd, y, ldy, stream=None):
+    _check(_lib.qmm_gemm_q4_0_q8_0(_ptr(w_qs), _ptr(w_d), N, K, M, _ptr(xq), _ptr(xd), _ptr(y), ldy,
+                                   _stream(stream)), "qmm_gemm_q4_0_q8_0")
+
+
+def qmm_debug_block_dots(w_qs, N, K, M, xq, dots, stream=None):
+    _check(_lib.qmm_debug_block_dots(_ptr(w_qs), N, K, M, _ptr(xq), _ptr(dots), _stream(stream)),
+           "qmm_debug_block_dots")
+
+
+def qmm_moe_workspace_size(E, T, k) -> int:
+    out = _SZ(0)
+    _check(_lib.qmm_moe_workspace_size(E, T, k, ctypes.byref(out)), "qmm_moe_workspace_size")
+    return out.value
+
+
+def qmm_moe_gemv(w_qs, w_d, E, N, K, ids, T, k, xq, xd, x_per_slot, y, workspace, workspace_bytes, stream=None):
+    _check(_lib.qmm_moe_gemv(_ptr(w_qs), _ptr(w_d), E, N, K, _ptr(ids), T, k, _ptr(xq), _ptr(xd), int(x_per_slot),
+                             _ptr(y), _ptr(workspace), workspace_bytes, _stream(stream)), "qmm_moe_gemv")
+
+
+def qmm_moe_combine(z, gates, T, k, N, y, stream=None):
+    _check(_lib.qmm_moe_combine(_ptr(z), _ptr(gates), T, k, N, _ptr(y), _stream(stream)), "qmm_moe_combine")
+
+
+def qmm_last_device_error(stream=None) -> int:
+    """Returns the status code (does not raise), after synchronising the stream."""
+    return _lib.qmm_last_device_error(_stream(stream))
+
+
+# ------------------------------------------------------------------ helpers (allocate with torch)
+def q4_0_planes(N: int, K: int, device="cuda"):
+    """Empty Q4_0 planes for an N x K matrix: (qs uint8 [N][K/2], d int16-as-fp16-bits [N][K/32])."""
+    return (torch.empty(N, K // 2, dtype=torch.uint8, device=device),
+            torch.empty(N, K // QK, dtype=torch.int16, device=device))
+
+
+def quantize_q4_0(w: torch.Tensor):
+    N, K = w.shape
+    qs, d = q4_0_planes(N, K, w.device)
+    qmm_quantize_q4_0(w, N, K, w.stride(0), qs, d)
+    return qs, d
+
+
+def quantize_q8_0(x: torch.Tensor):
+    if x.dim() == 1:
+        x = x[None]
+    M, K = x.shape
+    q = torch.empty(M, K, dtype=torch.int8, device=x.device)
+    d = torch.empty(M, K // QK, dtype=torch.int16, device=x.device)
+    qmm_quantize_q8_0(x, M, K, x.stride(0), q, d)
+    return q, d
+
+
+def gemv(qs, d, xq, xd, out=None):
+    N, K = qs.shape[0], qs.shape[1] * 2
+    y = out if out is not None else torch.empty(N, dtype=torch.float32, device=qs.device)
+    qmm_gemv_q4_0_q8_0(qs, d, N, K, xq, xd, y)
+    return y
+
+
+def gemm(qs, d, xq, xd, out=None):
+    N, K = qs.shape[0], qs.shape[1] * 2
+    M = xq.shape[0]
+    y = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=qs.device)
+    qmm_gemm_q4_0_q8_0(qs, d, N, K, M, xq, xd, y, y.stride(0))
+    return y

@@ -1,0 +1,200 @@
+/*
+ * qmm.h -- C ABI of libqmm: block-quantized int4 x int8 matrix products on
+ * one GB300 (sm_103a).
+ *
+ * The method (what every product entry computes):
+ *  - Weights are Q4_0 blocks of 32 values with one fp16 scale
+ *    (TinyLLaMA C++ guide, kenji.blog, section 6.1 "Arquitectura de
+ *    cuantizacion por bloques"): w_i ~ Delta * q_i, q_i in [-8, 7],
+ *    Delta = max|w_i| / 7 (llama.cpp guide, kenji.blog/id, section 2.2).
+ *  - Activations are quantized on the fly to Q8_0-style int8 blocks of 32
+ *    (Colibri page, kerneldigest.dev, "Arquitectura del Sistema"):
+ *    d = max|x| / 127 kept as fp16, q = round-half-away(x / d) in [-127,127].
+ *  - Each output is y = sum over blocks b of d_w[b] * d_x[b] * dot_b, where
+ *    dot_b = sum_{i<32} q_w,i * q_x,i is an exact int32 (llama.cpp guide 2.2,
+ *    y ~ Delta * Delta_x * sum q_i q_x,i), accumulated in fp32.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *    and allocates every buffer (the library allocates no device memory).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every entry only enqueues work on it and returns; none
+ *    synchronises except qmm_last_device_error.
+ *  - Shapes: W is N x K (N output rows, K reduction length), K % 32 == 0,
+ *    B = K / 32 blocks per row.  Activations are M x K.
+ *  - Return value: QMM_OK (0) or a nonzero qmm_status.  On an argument
+ *    error nothing is launched.  Launch errors surface as QMM_ERR_CUDA from
+ *    cudaGetLastError right after the launch.
+ *
+ * Device layout of a Q4_0 matrix ("planes", bytes identical to the page's
+ * 18-byte blocks, split so each 16-byte nibble group is 16-byte aligned):
+ *  - qs : uint8 [N][B][16].  Byte j of block b holds element 32b+j in its low
+ *         nibble and element 32b+j+16 in its high nibble, each stored as
+ *         u = q + 8 (all 16 nibble values are accepted).  Must be 16-byte
+ *         aligned.
+ *  - d  : uint16 [N][B], the fp16 bit pattern of each block's scale.
+ *         Must be 2-byte aligned.
+ * Q8_0 activations: q int8 [M][K] (16-byte aligned, row stride K) and
+ * d uint16 [M][B] fp16 bit patterns (row stride B).
+ */
+#ifndef QMM_H_
+#define QMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QMM_API __attribute__((visibility("default")))
+#else
+#define QMM_API
+#endif
+
+#define QMM_QK 32        /* values per block */
+#define QMM_ABI_VERSION 1
+
+typedef enum qmm_status {
+    QMM_OK = 0,
+    QMM_ERR_ARG = 1,            /* NULL pointer or negative size            */
+    QMM_ERR_SHAPE = 2,          /* K % 32 != 0, empty where not allowed, too large */
+    QMM_ERR_ALIGN = 3,          /* pointer misaligned for the documented layout */
+    QMM_ERR_DEVICE = 4,         /* current device is not sm_103 (or no device) */
+    QMM_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed     */
+    QMM_ERR_TIMEOUT = 6,        /* a bounded device-side wait gave up       */
+    QMM_ERR_BAD_EXPERT_ID = 7,  /* an expert id outside [0, E) was skipped  */
+    QMM_ERR_WORKSPACE = 8       /* workspace NULL or smaller than required  */
+} qmm_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+QMM_API const char* qmm_status_string(int status);
+
+/* QMM_ABI_VERSION of the loaded library. */
+QMM_API int qmm_abi_version(void);
+
+/* ---------------------------------------------------------------------
+ * Weight preparation (set-up time, not on the decode path)
+ * ------------------------------------------------------------------- */
+
+/* Quantize fp32 weights w [N][K] (row stride ldw >= K floats) to Q4_0
+ * planes, per block: amax = max|w|, d32 = amax/7 (IEEE fp32 division),
+ * q = clamp(round-half-away(w/d32), -8, 7), d = fp16(d32) (round to nearest
+ * even); an all-zero block gives d = 0, q = 0.  (llama.cpp guide 2.2.)
+ * N == 0 is a no-op. */
+QMM_API qmm_status qmm_quantize_q4_0(const float* w, int64_t N, int64_t K, int64_t ldw,
+                             uint8_t* qs, uint16_t* d, void* stream);
+
+/* Split page-format Q4_0 blocks (TinyLLaMA guide 6.1: 2-byte fp16 scale,
+ * little endian, then 16 nibble bytes; 18 bytes per block, [N][B][18], on
+ * the device, any alignment) into the planes above.  N == 0 is a no-op. */
+QMM_API qmm_status qmm_repack_q4_0(const uint8_t* blocks, int64_t N, int64_t K,
+                           uint8_t* qs, uint16_t* d, void* stream);
+
+/* ---------------------------------------------------------------------
+ * Activation quantizer
+ * ------------------------------------------------------------------- */
+
+/* Q8_0 of x [M][K] (fp32, row stride ldx >= K floats, 16-byte aligned,
+ * ldx % 4 == 0): per block amax, d32 = amax/127 (IEEE division), q =
+ * clamp(round-half-away(x/d32), -127, 127), d = fp16(d32); zero block ->
+ * d = 0, q = 0.  Non-finite inputs, or amax/127 above 65504, are outside
+ * the domain (result unspecified).  Outputs q [M][K], d [M][B].
+ * M == 0 is a no-op. */
+QMM_API qmm_status qmm_quantize_q8_0(const float* x, int64_t M, int64_t K, int64_t ldx,
+                             int8_t* q, uint16_t* d, void* stream);
+
+/* SwiGLU then Q8_0 (TinyLLaMA guide 4.4: SwiGLU = Swish(x W_gate) * (x W_up),
+ * Swish(z) = z * sigmoid(z)): h = gate / (1 + expf(-gate)) * up in fp32,
+ * then Q8_0 of each row of h as qmm_quantize_q8_0.  gate/up/h are
+ * [rows][K] with row stride ld floats (16-byte aligned, ld % 4 == 0).
+ * h_out may be NULL; when given it receives the fp32 h.  rows == 0 is a
+ * no-op. */
+QMM_API qmm_status qmm_swiglu_quantize_q8_0(const float* gate, const float* up, int64_t rows, int64_t K,
+                                    int64_t ld, int8_t* q, uint16_t* d, float* h_out, void* stream);
+
+/* ---------------------------------------------------------------------
+ * Products
+ * ------------------------------------------------------------------- */
+
+/* Batch-1 GEMV (llama.cpp guide 2.1-2.2: the decode-time bottleneck):
+ * y[n] = sum_b fp32(d_w[n][b]) * fp32(d_x[b]) * dot(n, b), n < N.
+ * xq int8 [K] (16-byte aligned), xd uint16 [B], y fp32 [N].  N >= 1. */
+QMM_API qmm_status qmm_gemv_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
+                              const int8_t* xq, const uint16_t* xd, float* y, void* stream);
+
+/* Batch-1 GEMV from fp32 activations: quantizes x [K] (16-byte aligned)
+ * to Q8_0 exactly as qmm_quantize_q8_0 inside the same launch, then does
+ * the GEMV.  If `gate_up` is nonzero, x is read as two vectors gate =
+ * x[0..K) and up = x[K..2K) and the activation quantized is SwiGLU(gate, up)
+ * computed as qmm_swiglu_quantize_q8_0 does (the down projection of a
+ * SwiGLU FFN, TinyLLaMA guide 4.4).  `residual` [N] may be NULL; when given,
+ * y[n] = residual[n] + sum_b ... (the residual add of a transformer block,
+ * TinyLLaMA guide 5.2 graph); y must not alias x or residual.
+ * xq_out [K] / xd_out [B] may be NULL; when given they receive the Q8_0
+ * activation.  `chain` nonzero launches with programmatic dependent launch:
+ * the kernel may start before the preceding kernel on `stream` has finished
+ * and reads x and residual only after it has.  The fp32 activation must
+ * fit on chip: K <= 40960. */
+QMM_API qmm_status qmm_gemv_q4_0_f32(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
+                             const float* x, int gate_up, const float* residual, float* y,
+                             int8_t* xq_out, uint16_t* xd_out, int chain, void* stream);
+
+/* Small-batch GEMM (batched decode, speculative verify -- Colibri page,
+ * MTP drafts verified in one batched forward): for m < M, n < N,
+ * y[m*ldy + n] = sum_b d_w[n][b] * d_x[m][b] * dot(m, n, b).
+ * xq int8 [M][K], xd [M][B]; ldy >= N.  M >= 1. */
+QMM_API qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
+                              int64_t M, const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy,
+                              void* stream);
+
+/* Per-block integer dots, for bit-exact checking: dots[(m*N + n)*B + b] =
+ * sum_{i<32} q_w * q_x, int32, computed with the product kernels' own
+ * unpack and dot code.  M, N >= 1. */
+QMM_API qmm_status qmm_debug_block_dots(const uint8_t* w_qs, int64_t N, int64_t K, int64_t M, const int8_t* xq,
+                                int32_t* dots, void* stream);
+
+/* ---------------------------------------------------------------------
+ * MoE expert-grouped GEMV (Colibri page: only the routed experts of each
+ * token are applied; sigmoid router, top-k)
+ * ------------------------------------------------------------------- */
+
+/* Bytes of workspace qmm_moe_gemv needs for E experts and T*k slots. */
+QMM_API qmm_status qmm_moe_workspace_size(int32_t E, int32_t T, int32_t k, size_t* bytes);
+
+/* For every slot s = t*k + j (t < T, j < k) with expert e = ids[s]:
+ *   y[s][n] = sum_b d_w(e)[n][b] * d_x[b] * dot, n < N,
+ * where expert e's planes are w_qs + e*N*K/2 and w_d + e*N*B (experts
+ * stored back to back), and the activation is row t of xq/xd
+ * (x_per_slot == 0: xq [T][K], xd [T][B]) or row s (x_per_slot != 0:
+ * xq [T*k][K], xd [T*k][B]).  y is fp32 [T*k][N].  Each distinct expert's
+ * weights are streamed once per call and applied to all slots routed to it.
+ * ids int32 [T][k] on the device; an id outside [0, E) is skipped (its y
+ * row is left untouched) and sets the device error word, reported by
+ * qmm_last_device_error as QMM_ERR_BAD_EXPERT_ID.  Duplicate ids are
+ * allowed.  workspace: device, >= qmm_moe_workspace_size bytes, 16-byte
+ * aligned, contents need not be initialised.  T == 0 is a no-op. */
+QMM_API qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,
+                        const int32_t* ids, int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd,
+                        int x_per_slot, float* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/* y[t][n] = sum_{j=0..k-1} gates[t][j] * z[t][j][n], j ascending (fixed
+ * order, deterministic).  z fp32 [T][k][N], gates fp32 [T][k], y [T][N]. */
+QMM_API qmm_status qmm_moe_combine(const float* z, const float* gates, int32_t T, int32_t k, int64_t N, float* y,
+                           void* stream);
+
+/* ---------------------------------------------------------------------
+ * Errors raised on the device
+ * ------------------------------------------------------------------- */
+
+/* Synchronises `stream`, reads and clears the device error word of the
+ * current device: QMM_OK, QMM_ERR_BAD_EXPERT_ID or QMM_ERR_TIMEOUT (a
+ * bounded wait gave up).  QMM_ERR_CUDA if the synchronisation failed. */
+QMM_API qmm_status qmm_last_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H_ */

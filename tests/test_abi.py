@@ -1,0 +1,93 @@
+"""The C-ABI library: it builds, loads, exports every entry point that
+include/qmm.h declares, and rejects bad arguments on the host (status codes,
+nothing launched).  No GPU needed: every call here fails validation before
+any CUDA call, or reports that no sm_103 device is present."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def qmm():
+    from block_quantized_int4_gb300 import _build
+    _build.build()
+    from block_quantized_int4_gb300 import qmm as m
+    return m
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "qmm.h")).read()
+    return re.findall(r"^QMM_API\s+[\w\s\*]+?\b(qmm_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_entry_points():
+    names = set(_header_functions())
+    for n in ["qmm_quantize_q8_0", "qmm_gemv_q4_0_q8_0", "qmm_gemm_q4_0_q8_0", "qmm_moe_gemv",
+              "qmm_quantize_q4_0", "qmm_repack_q4_0", "qmm_swiglu_quantize_q8_0", "qmm_debug_block_dots",
+              "qmm_last_device_error", "qmm_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(qmm):
+    lib = ctypes.CDLL(qmm.LIB_PATH)
+    for name in _header_functions():
+        assert hasattr(lib, name), f"{name} declared in qmm.h but not exported"
+    assert set(qmm.SIGNATURES) <= set(_header_functions())
+
+
+def test_status_strings_and_version(qmm):
+    assert qmm.abi_version() == 1
+    for code, name in qmm.STATUS.items():
+        assert qmm.status_string(code).startswith(name)
+    assert "UNKNOWN" in qmm.status_string(99)
+
+
+def _call(qmm, name, *args):
+    return getattr(qmm.library_handle(), name)(*args)
+
+
+def test_shape_and_argument_errors_return_status(qmm):
+    A16 = 0x10000  # a fake, 16-byte aligned address: never dereferenced
+    # K not a multiple of 32
+    assert _call(qmm, "qmm_gemv_q4_0_q8_0", A16, A16, 64, 48, A16, A16, A16, None) == 2
+    assert _call(qmm, "qmm_quantize_q8_0", A16, 1, 33, 33, A16, A16, None) == 2
+    # negative sizes / null pointers
+    assert _call(qmm, "qmm_gemm_q4_0_q8_0", A16, A16, -1, 64, 1, A16, A16, A16, 64, None) == 1
+    assert _call(qmm, "qmm_gemm_q4_0_q8_0", None, A16, 64, 64, 1, A16, A16, A16, 64, None) == 1
+    assert _call(qmm, "qmm_quantize_q8_0", None, 1, 64, 64, A16, A16, None) == 1
+    # ldy < N
+    assert _call(qmm, "qmm_gemm_q4_0_q8_0", A16, A16, 64, 64, 2, A16, A16, A16, 32, None) == 1
+    # empty products are shape errors, empty quantizations are no-ops
+    assert _call(qmm, "qmm_gemm_q4_0_q8_0", A16, A16, 64, 64, 0, A16, A16, A16, 64, None) == 2
+    assert _call(qmm, "qmm_quantize_q8_0", A16, 0, 64, 64, A16, A16, None) == 0
+    assert _call(qmm, "qmm_moe_gemv", A16, A16, 4, 64, 64, A16, 0, 2, A16, A16, 0, A16, A16, 1 << 20, None) == 0
+
+
+def test_alignment_errors(qmm):
+    A16, ODD = 0x10000, 0x10001
+    assert _call(qmm, "qmm_gemv_q4_0_q8_0", A16 + 8, A16, 64, 64, A16, A16, A16, None) == 3  # qs not 16-B
+    assert _call(qmm, "qmm_gemv_q4_0_q8_0", A16, ODD, 64, 64, A16, A16, A16, None) == 3  # d not 2-B
+    assert _call(qmm, "qmm_gemv_q4_0_q8_0", A16, A16, 64, 64, A16 + 4, A16, A16, None) == 3  # xq not 16-B
+    assert _call(qmm, "qmm_quantize_q8_0", A16 + 4, 1, 64, 64, A16, A16, None) == 3
+    assert _call(qmm, "qmm_quantize_q8_0", A16, 2, 64, 66, A16, A16, None) == 3  # ldx % 4
+
+
+def test_workspace_rules(qmm):
+    n = qmm.qmm_moe_workspace_size(256, 16, 8)
+    assert n % 16 == 0 and n >= 4 * (256 * 4 + 2 + 128)
+    A16 = 0x10000
+    assert _call(qmm, "qmm_moe_gemv", A16, A16, 256, 64, 64, A16, 16, 8, A16, A16, 0, A16, A16, n - 16, None) == 8
+    assert _call(qmm, "qmm_moe_gemv", A16, A16, 256, 64, 64, A16, 16, 8, A16, A16, 0, A16, None, n, None) == 8
+
+
+def test_valid_call_without_gpu_reports_device_error(qmm):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    A16 = 0x10000
+    assert _call(qmm, "qmm_gemv_q4_0_q8_0", A16, A16, 64, 64, A16, A16, A16, None) == 4
+    assert _call(qmm, "qmm_last_device_error", None) == 4

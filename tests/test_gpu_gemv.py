@@ -1,0 +1,232 @@
+"""GPU GEMV / small-batch GEMM / block dots against the CPU oracle.
+
+Block dots: bit-exact.  fp32 outputs: |y_gpu - y_ref| <= 1e-5*S + 1e-6 with
+S = sum_b |d_w d_x dot_b| (the oracle computes y and S in float64)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+import workloads
+from parity import lib, u16, assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _rand_codes(N, M, K, seed):
+    """Random codes using every nibble value (including -8) and random scales."""
+    rng = np.random.default_rng(seed)
+    qw = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    dw = rng.integers(0x1000, 0x2C00, size=(N, K // 32)).astype(np.uint16)
+    qx = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    dx = rng.integers(0x1000, 0x3C00, size=(M, K // 32)).astype(np.uint16)
+    return qw, dw, qx, dx
+
+
+def _to_device_planes(qmm, qw, dw):
+    N, K = qw.shape
+    blocks = torch.from_numpy(O.pack_q4_0_blocks(qw, dw).reshape(-1).copy()).to(DEV)
+    qs, d = qmm.q4_0_planes(N, K)
+    qmm.qmm_repack_q4_0(blocks, N, K, qs, d)
+    return qs, d
+
+
+def _dev_q8(qx, dx):
+    return torch.from_numpy(qx).to(DEV), torch.from_numpy(dx.view(np.int16)).to(DEV)
+
+
+@pytest.mark.parametrize("N,M,K", [(1, 1, 32), (13, 3, 96), (70, 2, 2048), (9, 5, 5632)])
+def test_block_dots_bit_exact(N, M, K):
+    qmm = lib()
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + K)
+    qs, d = _to_device_planes(qmm, qw, dw)
+    xq, _ = _dev_q8(qx, dx)
+    dots = torch.empty(M, N, K // 32, dtype=torch.int32, device=DEV)
+    qmm.qmm_debug_block_dots(qs, N, K, M, xq, dots)
+    assert np.array_equal(dots.cpu().numpy(), O.block_dots(qw, qx))
+
+
+@pytest.mark.parametrize("N,K", [(1, 32), (7, 64), (257, 96), (1000, 2048), (2048, 2048), (33, 5632), (100, 28672)])
+def test_gemv_random_codes(N, K):
+    """Random nibbles incl. -8; rows not a multiple of the 8-row tile; K from one block to 896."""
+    qmm = lib()
+    qw, dw, qx, dx = _rand_codes(N, 1, K, seed=7 * N + K)
+    qs, d = _to_device_planes(qmm, qw, dw)
+    xq, xd = _dev_q8(qx, dx)
+    y = qmm.gemv(qs, d, xq[0], xd[0])
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y[None], ref, S, f"gemv {N}x{K}")
+
+
+def test_gemv_integer_grid_exact():
+    """d = 1 on both sides: the GEMV is the exact integer product."""
+    qmm = lib()
+    rng = np.random.default_rng(3)
+    N, K = 300, 2048
+    w = rng.integers(-7, 8, size=(N, K)).astype(np.float32)
+    w[:, ::32] = 7
+    x = rng.integers(-127, 128, size=(1, K)).astype(np.float32)
+    x[:, 3::32] = 127
+    qs, d = qmm.quantize_q4_0(torch.from_numpy(w).to(DEV))
+    xq, xd = qmm.quantize_q8_0(torch.from_numpy(x).to(DEV))
+    y = qmm.gemv(qs, d, xq[0], xd[0])
+    exact = (w.astype(np.int64) @ x[0].astype(np.int64)).astype(np.float32)
+    assert np.array_equal(y.cpu().numpy(), exact)
+
+
+def test_single_gemv_2048_seeded():
+    """The 2048 x 2048 single GEMV: W ~ N(0, 0.02), x ~ N(0,1) with 1% x20 outliers, seed 0."""
+    qmm = lib()
+    c = workloads.SINGLE_GEMV
+    w = workloads.weights(c["N"], c["K"], sigma=c["sigma"], seed=0, index=0)
+    x = workloads.activations(1, c["K"], seed=0)
+    qs, d = qmm.quantize_q4_0(w.to(DEV))
+    xq, xd = qmm.quantize_q8_0(x.to(DEV))
+    y = qmm.gemv(qs, d, xq[0], xd[0])
+    qw, dw = O.quantize_q4_0(w.numpy())
+    qx, dx = O.quantize_q8_0(x.numpy())
+    assert np.array_equal(xq.cpu().numpy(), qx) and np.array_equal(u16(xd), dx)
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y[None], ref, S, "single gemv")
+
+
+@pytest.mark.parametrize("gate_up", [0, 1])
+@pytest.mark.parametrize("N,K", [(2560, 2048), (2048, 5632), (31, 96)])
+def test_fused_f32_gemv(gate_up, N, K):
+    """fp32 activation quantized inside the GEMV launch: the Q8_0 it writes is
+    bit-exact with the oracle quantizer (of SwiGLU(gate, up) in gate_up mode,
+    fed the GPU's own h), and y is within tolerance."""
+    qmm = lib()
+    w = workloads.weights(N, K, seed=2, index=N)
+    xin = workloads.activations(1, K * (2 if gate_up else 1), seed=4)[0]
+    qs, d = qmm.quantize_q4_0(w.to(DEV))
+    y = torch.empty(N, dtype=torch.float32, device=DEV)
+    xq = torch.empty(K, dtype=torch.int8, device=DEV)
+    xd = torch.empty(K // 32, dtype=torch.int16, device=DEV)
+    xdev = xin.to(DEV)
+    qmm.qmm_gemv_q4_0_f32(qs, d, N, K, xdev, gate_up, None, y, xq, xd, 0)
+    if gate_up:
+        hq = torch.empty(1, K, dtype=torch.int8, device=DEV)
+        hd = torch.empty(1, K // 32, dtype=torch.int16, device=DEV)
+        h = torch.empty(1, K, dtype=torch.float32, device=DEV)
+        qmm.qmm_swiglu_quantize_q8_0(xdev[:K], xdev[K:], 1, K, K, hq, hd, h)
+        qx, dx = O.quantize_q8_0(h.cpu().numpy())
+    else:
+        qx, dx = O.quantize_q8_0(xin.numpy()[None])
+    assert np.array_equal(xq.cpu().numpy(), qx[0]) and np.array_equal(u16(xd), dx[0])
+    qw, dw = O.quantize_q4_0(w.numpy())
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y[None], ref, S, "fused gemv")
+
+
+def test_chained_gemv_launches():
+    """Back-to-back dependent GEMVs launched with programmatic dependent launch:
+    each reads the previous one's output."""
+    qmm = lib()
+    K = 2048
+    ws = [workloads.weights(K, K, seed=9, index=i) for i in range(3)]
+    planes = [qmm.quantize_q4_0(w.to(DEV)) for w in ws]
+    x0 = workloads.activations(1, K, seed=9)[0].to(DEV)
+    bufs = [x0] + [torch.empty(K, dtype=torch.float32, device=DEV) for _ in ws]
+    qouts = [(torch.empty(K, dtype=torch.int8, device=DEV), torch.empty(K // 32, dtype=torch.int16, device=DEV))
+             for _ in ws]
+    for i, (qs, d) in enumerate(planes):
+        qmm.qmm_gemv_q4_0_f32(qs, d, K, K, bufs[i], 0, None, bufs[i + 1], qouts[i][0], qouts[i][1], 1)
+    torch.cuda.synchronize()
+    for i, w in enumerate(ws):
+        qx, dx = O.quantize_q8_0(bufs[i].cpu().numpy()[None])
+        assert np.array_equal(qouts[i][0].cpu().numpy(), qx[0])
+        qw, dw = O.quantize_q4_0(w.numpy())
+        ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+        assert_close(bufs[i + 1][None], ref, S, f"chain step {i}")
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 9, 16, 33, 64])
+def test_gemm_small_batch(M):
+    qmm = lib()
+    N, K = 517, 2048
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=M)
+    qs, d = _to_device_planes(qmm, qw, dw)
+    xq, xd = _dev_q8(qx, dx)
+    y = qmm.gemm(qs, d, xq, xd)
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y, ref, S, f"gemm M={M}")
+
+
+def test_gemm_ldy_and_chunked_k():
+    """Output row stride > N, and K too long to stage for 8 tokens at once."""
+    qmm = lib()
+    N, K, M, ldy = 40, 28672, 8, 64
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=1)
+    qs, d = _to_device_planes(qmm, qw, dw)
+    xq, xd = _dev_q8(qx, dx)
+    y = torch.full((M, ldy), 7.0, device=DEV)
+    qmm.qmm_gemm_q4_0_q8_0(qs, d, N, K, M, xq, xd, y, ldy)
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y[:, :N], ref, S, "gemm chunked")
+    assert torch.all(y[:, N:] == 7.0)
+
+
+@pytest.mark.parametrize("N,K", [(5632, 2048), (2048, 5632)])
+def test_batched_decode_shapes_full(N, K):
+    """Batched-decode shapes, M = 16, all rows against the oracle."""
+    qmm = lib()
+    M = 16
+    w = workloads.weights(N, K, seed=0, index=N)
+    x = workloads.activations(M, K, seed=0)
+    qs, d = qmm.quantize_q4_0(w.to(DEV))
+    xq, xd = qmm.quantize_q8_0(x.to(DEV))
+    y = qmm.gemm(qs, d, xq, xd)
+    qw, dw = O.quantize_q4_0(w.numpy())
+    qx, dx = O.quantize_q8_0(x.numpy())
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y, ref, S, f"batched {N}x{K}")
+
+
+def _sampled_rows(N, n, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, n)]))
+    return rows
+
+
+@pytest.mark.parametrize("name,N,K,M", [("tinyllama.qkv", 2560, 2048, 1), ("tinyllama.down", 2048, 5632, 1),
+                                        ("tinyllama.lm_head", 32000, 2048, 1),
+                                        ("dense.gate", 28672, 8192, 1), ("dense.down", 8192, 28672, 16),
+                                        ("dense.lm_head", 128256, 8192, 1)])
+def test_full_size_sampled_rows(name, N, K, M):
+    """Full-size matrices on the GPU (weights drawn on the device), sampled
+    rows recomputed by the oracle from the same fp32 rows."""
+    qmm = lib()
+    sigma = 0.01 if name.startswith("dense") else 0.02
+    w = workloads.weights(N, K, sigma=sigma, seed=0, index=N + K, device=DEV)
+    x = workloads.activations(M, K, seed=0, device=DEV)
+    qs, d = qmm.quantize_q4_0(w)
+    xq, xd = qmm.quantize_q8_0(x)
+    y = qmm.gemm(qs, d, xq, xd) if M > 1 else qmm.gemv(qs, d, xq[0], xd[0])[None]
+    rows = _sampled_rows(N, 64, N)
+    wr = w[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    qw, dw = O.quantize_q4_0(wr)
+    qx, dx = O.quantize_q8_0(x.cpu().numpy())
+    assert np.array_equal(xq.cpu().numpy(), qx)
+    # the sampled rows' device planes equal the oracle's quantization of the same rows
+    assert np.array_equal(u16(d[torch.from_numpy(rows).to(DEV)]), dw)
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y[:, rows], ref, S, name)
+
+
+def test_fused_gemv_residual():
+    """y = residual + W x (residual add in the epilogue)."""
+    qmm = lib()
+    N, K = 2048, 5632
+    w = workloads.weights(N, K, seed=5, index=1)
+    gu = workloads.activations(1, 2 * K, seed=5)[0]
+    r = workloads.activations(1, N, seed=6)[0]
+    qs, d = qmm.quantize_q4_0(w.to(DEV))
+    y = torch.empty(N, device=DEV)
+    y0 = torch.empty(N, device=DEV)
+    g = gu.to(DEV)
+    qmm.qmm_gemv_q4_0_f32(qs, d, N, K, g, 1, r.to(DEV), y)
+    qmm.qmm_gemv_q4_0_f32(qs, d, N, K, g, 1, None, y0)
+    diff = (y - y0).cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(diff - r.numpy()) <= np.spacing(np.abs(y.cpu().numpy())) + 1e-30)
