@@ -3,8 +3,9 @@
 
 Headline (the JSON line's `value`): batch-1 GEMV weight GB/s over a
 TinyLLaMA-1.1B-shaped decode step -- 22 layers of fused QKV 2048->2560,
-O 2048->2048, gate|up 2048->2x5632 (one launch), down 5632->2048 (SwiGLU +
-Q8_0 fused in front, residual add behind), then lm_head 2048->32000: 89
+O 2048->2048, gate/up 2048->2x5632 (one launch over interleaved rows, SwiGLU
+in its epilogue), down 5632->2048 (residual add in its epilogue), then
+lm_head 2048->32000: 89
 dependent GEMV launches per step, each quantizing its fp32 input to Q8_0
 inside the launch, chained with programmatic dependent launch and replayed
 from a CUDA graph.  581,861,376 weight bytes per step (> L2, so no flush).
@@ -134,8 +135,10 @@ class TinyLlamaDecode:
             o = planes(self.H, self.H)
             g = planes(self.F, self.H)
             u = planes(self.F, self.H)
-            # gate and up rows stacked: one launch yields [gate | up]
-            gu = (torch.cat([g[0], u[0]]), torch.cat([g[1], u[1]]))
+            # gate and up rows interleaved (g0, u0, g1, u1, ...): one launch
+            # computes both and writes SwiGLU(g, u) from each row pair
+            gu = (torch.stack([g[0], u[0]], 1).reshape(2 * self.F, -1).contiguous(),
+                  torch.stack([g[1], u[1]], 1).reshape(2 * self.F, -1).contiguous())
             down = planes(self.H, self.F)
             self.layers.append({"qkv": qkv, "o": o, "gu": gu, "down": down})
         self.lm_head = planes(self.V, self.H)
@@ -143,28 +146,29 @@ class TinyLlamaDecode:
         f32 = lambda n: torch.zeros(n, dtype=torch.float32, device=dev)  # noqa: E731
         self.x_in = workloads.activations(1, self.H, seed=seed, device=dev)[0].contiguous()
         self.h = [f32(self.H), f32(self.H)]
-        self.qkv_out, self.o_out, self.gu_out = f32(self.Q), f32(self.H), f32(2 * self.F)
+        self.qkv_out, self.o_out, self.h_ffn = f32(self.Q), f32(self.H), f32(self.F)
         self.logits = f32(self.V)
         self.launches_per_step = 4 * self.L + 1
         # algorithmic bytes per step: weights + fp32 activations read + outputs written (+ residual)
         act = 0
         for _ in range(self.L):
-            act += 4 * (self.H + self.Q) + 4 * (self.H + self.H) + 4 * (self.H + 2 * self.F) + 4 * (2 * self.F + 2 * self.H)
+            act += 4 * (self.H + self.Q) + 4 * (self.H + self.H) + 4 * (self.H + self.F) + 4 * (self.F + 2 * self.H)
         act += 4 * (self.H + self.V)
         self.algo_bytes = self.weight_bytes + act
 
     def step(self, stream=None):
         q, H, F = self.qmm, self.H, self.F
+        C, YS = q.CHAIN, q.Y_SWIGLU_PAIRS
         h_prev = self.x_in
         for li, Lw in enumerate(self.layers):
             h_next = self.h[li % 2]
-            q.qmm_gemv_q4_0_f32(*Lw["qkv"], self.Q, H, h_prev, 0, None, self.qkv_out, chain=1, stream=stream)
+            q.qmm_gemv_q4_0_f32(*Lw["qkv"], self.Q, H, h_prev, None, self.qkv_out, flags=C, stream=stream)
             # attention is outside this path: the O projection reads the q slice
-            q.qmm_gemv_q4_0_f32(*Lw["o"], H, H, self.qkv_out, 0, None, self.o_out, chain=1, stream=stream)
-            q.qmm_gemv_q4_0_f32(*Lw["gu"], 2 * F, H, self.o_out, 0, None, self.gu_out, chain=1, stream=stream)
-            q.qmm_gemv_q4_0_f32(*Lw["down"], H, F, self.gu_out, 1, h_prev, h_next, chain=1, stream=stream)
+            q.qmm_gemv_q4_0_f32(*Lw["o"], H, H, self.qkv_out, None, self.o_out, flags=C, stream=stream)
+            q.qmm_gemv_q4_0_f32(*Lw["gu"], 2 * F, H, self.o_out, None, self.h_ffn, flags=C | YS, stream=stream)
+            q.qmm_gemv_q4_0_f32(*Lw["down"], H, F, self.h_ffn, h_prev, h_next, flags=C, stream=stream)
             h_prev = h_next
-        q.qmm_gemv_q4_0_f32(*self.lm_head, self.V, H, h_prev, 0, None, self.logits, chain=1, stream=stream)
+        q.qmm_gemv_q4_0_f32(*self.lm_head, self.V, H, h_prev, None, self.logits, flags=C, stream=stream)
 
 
 def _graph(torch, fn):
@@ -419,7 +423,7 @@ def main():
                        "pct_of_hbm_peak": round(100 * value / ws / peak, 1)},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": "rows_kernel<1,X_F32|X_SWIGLU> (all launches of the step)",
+                         "kernel": "stream_rows_kernel<1,X_F32,*> (all launches of the step)",
                          "peak_kind": peak_kind},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": dec.H * 4,

@@ -11,6 +11,7 @@
 
 #include "qmm.h"
 #include "qmm_kernels.cuh"
+#include "qmm_stream.cuh"
 
 using namespace qmm;
 
@@ -133,6 +134,51 @@ qmm_status rows_launch(const DevInfo* di, RowsArgs a, bool pdl, cudaStream_t st)
 
 bool valid_k(int64_t K) { return K > 0 && K % QK == 0 && K <= (int64_t)1 << 30; }
 
+// Streaming kernel: eligible when the scale plane can be bulk-copied in row
+// ranges (B % 8 == 0, i.e. K % 256 == 0; d 16-byte aligned) and the staged
+// activation tile fits.
+constexpr int STREAM_XTILE_CAP = 64 * 1024;
+constexpr int STREAM_SMEM_CAP = 110 * 1024;  // two CTAs of consecutive kernels fit on one SM
+constexpr int STREAM_STAGE_TARGET = 16 * 1024;
+
+bool stream_eligible(int64_t K, const void* qs, const void* d, int MT) {
+    const int64_t B = K / QK;
+    return (B % 8 == 0) && aligned(qs, 16) && aligned(d, 16) &&
+           (int64_t)MT * B * xtile_bytes_per_block() <= STREAM_XTILE_CAP;
+}
+
+inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+template <int MT, int XM, int YM>
+qmm_status stream_launch(const DevInfo* di, StreamArgs a, bool pdl, cudaStream_t st) {
+    const int64_t B = a.K / QK;
+    const int64_t row_bytes = a.K / 2 + B * 2;
+    int64_t rpc = round_up((a.N + di->sms - 1) / di->sms, 2);
+    const int64_t G = (a.N + rpc - 1) / rpc;
+    int64_t stage_rows = std::max<int64_t>(2, (STREAM_STAGE_TARGET / row_bytes) & ~int64_t(1));
+    stage_rows = std::min(stage_rows, rpc);
+    const int64_t stage_bytes = round_up(stage_rows * row_bytes, 128);
+    const int64_t xtile = round_up((int64_t)MT * B * xtile_bytes_per_block(), 128);
+    const int64_t nchunks = (rpc + stage_rows - 1) / stage_rows;
+    int64_t room = (STREAM_SMEM_CAP - STREAM_HDR - xtile) / stage_bytes;
+    int64_t nst = std::min<int64_t>({nchunks, room, (int64_t)STREAM_MAX_STAGES});
+    if (nst < 1) return QMM_ERR_SHAPE;
+    const int smem = (int)(STREAM_HDR + xtile + nst * stage_bytes);
+    a.rows_per_cta = (int)rpc;
+    a.stage_rows = (int)stage_rows;
+    a.nstages = (int)nst;
+    a.stage_bytes = (int)stage_bytes;
+    a.xtile_bytes = (int)xtile;
+    a.err = di->err;
+    auto kern = stream_rows_kernel<MT, XM, YM>;
+    if (!smem_optin(kern, smem, di->smem_optin)) return QMM_ERR_SHAPE;
+    dim3 grid((unsigned)G, (unsigned)((a.M + MT - 1) / MT));
+    cudaError_t e = launch(kern, grid, dim3(STREAM_THREADS), smem, st, pdl, a);
+    return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
+}
+
+
+
 }  // namespace
 
 // ============================================================================
@@ -219,31 +265,51 @@ qmm_status qmm_gemv_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
 }
 
 qmm_status qmm_gemv_q4_0_f32(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, const float* x,
-                             int gate_up, const float* residual, float* y, int8_t* xq_out, uint16_t* xd_out,
-                             int chain, void* stream) {
-    if (N < 0) return QMM_ERR_ARG;
-    if (!valid_k(K) || N == 0) return QMM_ERR_SHAPE;
+                             const float* residual, float* y, int8_t* xq_out, uint16_t* xd_out, int flags,
+                             void* stream) {
+    if (N < 0 || (flags & ~(QMM_X_SWIGLU | QMM_Y_SWIGLU_PAIRS | QMM_CHAIN))) return QMM_ERR_ARG;
+    if (!valid_k(K) || N == 0 || K > 40960) return QMM_ERR_SHAPE;
     if (!w_qs || !w_d || !x || !y) return QMM_ERR_ARG;
-    if (K > 40960) return QMM_ERR_SHAPE;
+    const bool xs = flags & QMM_X_SWIGLU, ys = flags & QMM_Y_SWIGLU_PAIRS, pdl = flags & QMM_CHAIN;
+    if (ys && (N % 2 || residual)) return QMM_ERR_ARG;
     if (!aligned(w_qs, 16) || !aligned(w_d, 2) || !aligned(x, 16) || !aligned(y, 4) ||
         (residual && !aligned(residual, 4)) || (xq_out && !aligned(xq_out, 16)) || (xd_out && !aligned(xd_out, 2)))
         return QMM_ERR_ALIGN;
     const DevInfo* di = device_info();
     if (!di) return QMM_ERR_DEVICE;
+    cudaStream_t st = S(stream);
+    if (stream_eligible(K, w_qs, w_d, 1)) {
+        StreamArgs a = {};
+        a.qs = w_qs;
+        a.d = w_d;
+        a.N = N;
+        a.K = K;
+        a.M = 1;
+        a.xf = x;
+        a.residual = residual;
+        a.xq_out = xq_out;
+        a.xd_out = xd_out;
+        a.y = y;
+        a.ldy = ys ? N / 2 : N;
+        if (ys) return xs ? stream_launch<1, X_SWIGLU, Y_SWIGLU_PAIRS>(di, a, pdl, st)
+                          : stream_launch<1, X_F32, Y_SWIGLU_PAIRS>(di, a, pdl, st);
+        return xs ? stream_launch<1, X_SWIGLU, Y_PLAIN>(di, a, pdl, st)
+                  : stream_launch<1, X_F32, Y_PLAIN>(di, a, pdl, st);
+    }
+    if (ys) return QMM_ERR_SHAPE;  // paired rows need the streaming kernel (K % 256 == 0, d 16-byte aligned)
     RowsArgs a = {};
-    a.residual = residual;
     a.qs = w_qs;
     a.d = w_d;
     a.N = N;
     a.K = K;
     a.M = 1;
     a.xf = x;
+    a.residual = residual;
     a.xq_out = xq_out;
     a.xd_out = xd_out;
     a.y = y;
     a.ldy = N;
-    return gate_up ? rows_launch<1, X_SWIGLU>(di, a, chain != 0, S(stream))
-                   : rows_launch<1, X_F32>(di, a, chain != 0, S(stream));
+    return xs ? rows_launch<1, X_SWIGLU>(di, a, pdl, st) : rows_launch<1, X_F32>(di, a, pdl, st);
 }
 
 qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,
@@ -266,6 +332,25 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
     a.y = y;
     a.ldy = ldy;
     cudaStream_t st = S(stream);
+    const int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
+    if (stream_eligible(K, w_qs, w_d, mt)) {
+        StreamArgs s = {};
+        s.qs = w_qs;
+        s.d = w_d;
+        s.N = N;
+        s.K = K;
+        s.M = M;
+        s.xq = xq;
+        s.xd = xd;
+        s.y = y;
+        s.ldy = ldy;
+        switch (mt) {
+            case 1: return stream_launch<1, X_Q8, Y_PLAIN>(di, s, false, st);
+            case 2: return stream_launch<2, X_Q8, Y_PLAIN>(di, s, false, st);
+            case 4: return stream_launch<4, X_Q8, Y_PLAIN>(di, s, false, st);
+            default: return stream_launch<8, X_Q8, Y_PLAIN>(di, s, false, st);
+        }
+    }
     if (M == 1) return rows_launch<1, X_Q8>(di, a, false, st);
     if (M == 2) return rows_launch<2, X_Q8>(di, a, false, st);
     if (M <= 4) return rows_launch<4, X_Q8>(di, a, false, st);

@@ -63,46 +63,7 @@ __device__ __forceinline__ int block_dot_u(uint4 w, int4 xlo, int4 xhi) {
     return s;
 }
 
-// ---------------------------------------------------------------- Q8_0 quantizer
-// Eight consecutive lanes (lane % 8 == 0 .. 7) hold one block of 32 values,
-// four consecutive values each.  All 32 lanes of the warp must call this.
-// Per block: amax, d32 = amax/127 (IEEE division), q = clamp(rha(v/d32),
-// -127, 127) with round-half-away (roundf), zero block -> q = 0, d32 = 0.
-// Returns the four int8 codes packed little-endian; d32 and the block's code
-// sum are returned in every lane of the group.
-struct Q8Quad {
-    int packed;
-    float d32;
-    int qsum;
-};
-
-__device__ __forceinline__ int q8_code(float v, float d32, bool nonzero) {
-    if (!nonzero) return 0;
-    float r = roundf(__fdiv_rn(v, d32));
-    r = fminf(fmaxf(r, -127.0f), 127.0f);
-    return (int)r;
-}
-
-__device__ __forceinline__ Q8Quad q8_0_quad(float4 v) {
-    float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-    a = fmaxf(a, __shfl_xor_sync(FULL, a, 1));
-    a = fmaxf(a, __shfl_xor_sync(FULL, a, 2));
-    a = fmaxf(a, __shfl_xor_sync(FULL, a, 4));
-    const float d32 = __fdiv_rn(a, 127.0f);
-    const bool nz = a != 0.0f;
-    int q0 = q8_code(v.x, d32, nz), q1 = q8_code(v.y, d32, nz);
-    int q2 = q8_code(v.z, d32, nz), q3 = q8_code(v.w, d32, nz);
-    int s = q0 + q1 + q2 + q3;
-    s += __shfl_xor_sync(FULL, s, 1);
-    s += __shfl_xor_sync(FULL, s, 2);
-    s += __shfl_xor_sync(FULL, s, 4);
-    Q8Quad r;
-    r.packed = (q0 & 0xff) | ((q1 & 0xff) << 8) | ((q2 & 0xff) << 16) | ((q3 & 0xff) << 24);
-    r.d32 = d32;
-    r.qsum = s;
-    return r;
-}
-
+// ---------------------------------------------------------------- fp16 bits
 __device__ __forceinline__ unsigned short f32_to_f16_bits(float f) {
     return __half_as_ushort(__float2half_rn(f));
 }
@@ -115,6 +76,69 @@ __device__ __forceinline__ float f16_bits_to_f32(unsigned short h) {
 __device__ __forceinline__ float swiglu1(float g, float u) {
     return __fdiv_rn(g, 1.0f + expf(-g)) * u;
 }
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Every wait on the device is bounded: this one gives up after `limit_ns`
+// of wall time (or as soon as *abort is set) and returns false.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+    return true;
+}
+
+// Bulk copy global -> this CTA's shared memory, completion counted in bytes
+// on `bar`.  dst/src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
 
 // ---------------------------------------------------------------- warp reduce
 __device__ __forceinline__ float warp_sum(float v) {

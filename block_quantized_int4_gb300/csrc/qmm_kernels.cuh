@@ -197,9 +197,9 @@ __device__ __forceinline__ int block_qsum(int4 lo, int4 hi) {
 template <int MT>
 __device__ __forceinline__ void stage_q8(const XTile& xt, int Bc, const int8_t* __restrict__ xq,
                                          const uint16_t* __restrict__ xd, int64_t K, const int64_t* xrow, int b0,
-                                         int nb) {
+                                         int nb, int tid, int nthr) {
     const int64_t B = K / QK;
-    for (int i = threadIdx.x; i < MT * Bc; i += blockDim.x) {
+    for (int i = tid; i < MT * Bc; i += nthr) {
         const int t = i / Bc, b = i - t * Bc;
         int4 lo = make_int4(0, 0, 0, 0), hi = lo;
         float s = 0.f;
@@ -221,10 +221,11 @@ __device__ __forceinline__ void stage_q8(const XTile& xt, int Bc, const int8_t* 
 // result out when xq_out/xd_out are given.  Whole CTA; blockDim % 32 == 0.
 template <bool GATE_UP>
 __device__ __forceinline__ void stage_f32(const XTile& xt, const float* __restrict__ x, int64_t K,
-                                          int8_t* __restrict__ xq_out, uint16_t* __restrict__ xd_out) {
+                                          int8_t* __restrict__ xq_out, uint16_t* __restrict__ xd_out, int tid,
+                                          int nthr) {
     const int B = (int)(K / QK);
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int lane = tid & 31;
+    const int warp = tid >> 5, nwarps = nthr >> 5;
     const bool writer = blockIdx.x == 0 && blockIdx.y == 0;
     for (int g = warp; g * 4 < B; g += nwarps) {
         const int b = g * 4 + (lane >> 3);
@@ -341,8 +342,8 @@ __global__ void __launch_bounds__(ROWS_THREADS) rows_kernel(RowsArgs a) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (nchunks == 1) {
-        if (XMODE == X_Q8) stage_q8<MT>(xt, Bc, a.xq, a.xd, a.K, xrow, 0, (int)B);
-        else stage_f32<XMODE == X_SWIGLU>(xt, a.xf, a.K, a.xq_out, a.xd_out);
+        if (XMODE == X_Q8) stage_q8<MT>(xt, Bc, a.xq, a.xd, a.K, xrow, 0, (int)B, threadIdx.x, blockDim.x);
+        else stage_f32<XMODE == X_SWIGLU>(xt, a.xf, a.K, a.xq_out, a.xd_out, threadIdx.x, blockDim.x);
         __syncthreads();
     }
     const int64_t ntiles = (a.N + ROWS_WARPS - 1) / ROWS_WARPS;
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(ROWS_THREADS) rows_kernel(RowsArgs a) {
             const int nb = (int)min((int64_t)Bc, B - b0);
             if (nchunks > 1) {
                 __syncthreads();
-                stage_q8<MT>(xt, Bc, a.xq, a.xd, a.K, xrow, b0, nb);
+                stage_q8<MT>(xt, Bc, a.xq, a.xd, a.K, xrow, b0, nb, threadIdx.x, blockDim.x);
                 __syncthreads();
             }
             if (row < a.N) row_accumulate<MT>(xt, Bc, a.qs + (row * B + b0) * 16, a.d + row * B + b0, nb, lane, acc);
@@ -536,7 +537,7 @@ __global__ void __launch_bounds__(ROWS_THREADS) moe_rows_kernel(MoeArgs a) {
                 xrow[t] = slot[t] < 0 ? -1 : (a.x_per_slot ? slot[t] : slot[t] / a.k);
             }
             __syncthreads();
-            stage_q8<MT>(xt, Bc, a.xq, a.xd, a.K, xrow, 0, Bc);
+            stage_q8<MT>(xt, Bc, a.xq, a.xd, a.K, xrow, 0, Bc, threadIdx.x, blockDim.x);
             __syncthreads();
             for (int64_t row = r0 + warp; row < min(a.N, r0 + a.rows_per_item); row += ROWS_WARPS) {
                 float acc[MT];

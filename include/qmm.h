@@ -124,22 +124,30 @@ QMM_API qmm_status qmm_swiglu_quantize_q8_0(const float* gate, const float* up, 
 QMM_API qmm_status qmm_gemv_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
                               const int8_t* xq, const uint16_t* xd, float* y, void* stream);
 
-/* Batch-1 GEMV from fp32 activations: quantizes x [K] (16-byte aligned)
- * to Q8_0 exactly as qmm_quantize_q8_0 inside the same launch, then does
- * the GEMV.  If `gate_up` is nonzero, x is read as two vectors gate =
- * x[0..K) and up = x[K..2K) and the activation quantized is SwiGLU(gate, up)
- * computed as qmm_swiglu_quantize_q8_0 does (the down projection of a
- * SwiGLU FFN, TinyLLaMA guide 4.4).  `residual` [N] may be NULL; when given,
- * y[n] = residual[n] + sum_b ... (the residual add of a transformer block,
- * TinyLLaMA guide 5.2 graph); y must not alias x or residual.
+/* Flags of qmm_gemv_q4_0_f32. */
+#define QMM_X_SWIGLU 1       /* x holds gate = x[0..K) and up = x[K..2K); the activation
+                                quantized is SwiGLU(gate, up) as in qmm_swiglu_quantize_q8_0 */
+#define QMM_Y_SWIGLU_PAIRS 2 /* rows interleaved gate_0, up_0, gate_1, up_1, ...: the output
+                                is y[i] = Swish(g_i) * u_i, g_i = row 2i . x, u_i = row 2i+1 . x
+                                (N even, y has N/2 entries, no residual; needs K % 256 == 0
+                                and a 16-byte aligned w_d) */
+#define QMM_CHAIN 4          /* programmatic dependent launch (see below) */
+
+/* Batch-1 GEMV from fp32 activations: quantizes x [K] (16-byte aligned) to
+ * Q8_0 exactly as qmm_quantize_q8_0 inside the same launch, then
+ * y[n] = sum_b d_w[n][b] * d_x[b] * dot(n, b) (+ residual[n] when residual
+ * is not NULL: the residual add of a transformer block, TinyLLaMA guide 5.2
+ * graph).  SwiGLU (TinyLLaMA guide 4.4) can be fused on either side with
+ * QMM_X_SWIGLU / QMM_Y_SWIGLU_PAIRS.  y must not alias x or residual.
  * xq_out [K] / xd_out [B] may be NULL; when given they receive the Q8_0
- * activation.  `chain` nonzero launches with programmatic dependent launch:
- * the kernel may start before the preceding kernel on `stream` has finished
- * and reads x and residual only after it has.  The fp32 activation must
- * fit on chip: K <= 40960. */
+ * activation.  With QMM_CHAIN the kernel may start before the preceding
+ * kernel on `stream` has finished and stream its weights meanwhile; it
+ * reads x and residual only after that kernel has completed.  So the
+ * weight planes must not be written by any kernel still running when this
+ * call is enqueued.  The fp32 activation is staged on chip: K <= 40960. */
 QMM_API qmm_status qmm_gemv_q4_0_f32(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
-                             const float* x, int gate_up, const float* residual, float* y,
-                             int8_t* xq_out, uint16_t* xd_out, int chain, void* stream);
+                             const float* x, const float* residual, float* y,
+                             int8_t* xq_out, uint16_t* xd_out, int flags, void* stream);
 
 /* Small-batch GEMM (batched decode, speculative verify -- Colibri page,
  * MTP drafts verified in one batched forward): for m < M, n < N,

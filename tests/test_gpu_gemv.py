@@ -92,7 +92,7 @@ def test_single_gemv_2048_seeded():
 
 
 @pytest.mark.parametrize("gate_up", [0, 1])
-@pytest.mark.parametrize("N,K", [(2560, 2048), (2048, 5632), (31, 96)])
+@pytest.mark.parametrize("N,K", [(2560, 2048), (2048, 5632), (31, 96), (32000, 2048), (3, 8192), (300, 28672)])
 def test_fused_f32_gemv(gate_up, N, K):
     """fp32 activation quantized inside the GEMV launch: the Q8_0 it writes is
     bit-exact with the oracle quantizer (of SwiGLU(gate, up) in gate_up mode,
@@ -105,7 +105,7 @@ def test_fused_f32_gemv(gate_up, N, K):
     xq = torch.empty(K, dtype=torch.int8, device=DEV)
     xd = torch.empty(K // 32, dtype=torch.int16, device=DEV)
     xdev = xin.to(DEV)
-    qmm.qmm_gemv_q4_0_f32(qs, d, N, K, xdev, gate_up, None, y, xq, xd, 0)
+    qmm.qmm_gemv_q4_0_f32(qs, d, N, K, xdev, None, y, xq, xd, flags=qmm.X_SWIGLU if gate_up else 0)
     if gate_up:
         hq = torch.empty(1, K, dtype=torch.int8, device=DEV)
         hd = torch.empty(1, K // 32, dtype=torch.int16, device=DEV)
@@ -132,7 +132,7 @@ def test_chained_gemv_launches():
     qouts = [(torch.empty(K, dtype=torch.int8, device=DEV), torch.empty(K // 32, dtype=torch.int16, device=DEV))
              for _ in ws]
     for i, (qs, d) in enumerate(planes):
-        qmm.qmm_gemv_q4_0_f32(qs, d, K, K, bufs[i], 0, None, bufs[i + 1], qouts[i][0], qouts[i][1], 1)
+        qmm.qmm_gemv_q4_0_f32(qs, d, K, K, bufs[i], None, bufs[i + 1], qouts[i][0], qouts[i][1], flags=qmm.CHAIN)
     torch.cuda.synchronize()
     for i, w in enumerate(ws):
         qx, dx = O.quantize_q8_0(bufs[i].cpu().numpy()[None])
@@ -226,7 +226,46 @@ def test_fused_gemv_residual():
     y = torch.empty(N, device=DEV)
     y0 = torch.empty(N, device=DEV)
     g = gu.to(DEV)
-    qmm.qmm_gemv_q4_0_f32(qs, d, N, K, g, 1, r.to(DEV), y)
-    qmm.qmm_gemv_q4_0_f32(qs, d, N, K, g, 1, None, y0)
+    qmm.qmm_gemv_q4_0_f32(qs, d, N, K, g, r.to(DEV), y, flags=qmm.X_SWIGLU)
+    qmm.qmm_gemv_q4_0_f32(qs, d, N, K, g, None, y0, flags=qmm.X_SWIGLU)
     diff = (y - y0).cpu().numpy().astype(np.float64)
     assert np.all(np.abs(diff - r.numpy()) <= np.spacing(np.abs(y.cpu().numpy())) + 1e-30)
+
+
+@pytest.mark.parametrize("F,K", [(5632, 2048), (40, 256), (2048, 6144)])
+def test_swiglu_pairs_epilogue(F, K):
+    """Interleaved gate/up rows: y[i] = Swish(g_i) * u_i from the row pair
+    (2i, 2i+1).  Checked against the oracle's float64 g, u and SwiGLU with the
+    GEMV tolerance carried through: |dh| <= 1.1 |u| tol_g + |Swish(g)| tol_u
+    (|Swish'| <= 1.1) plus 8 fp32 ulp of h."""
+    qmm = lib()
+    wg = workloads.weights(F, K, seed=7, index=1)
+    wu = workloads.weights(F, K, seed=7, index=2)
+    x = workloads.activations(1, K, seed=7)[0]
+    w = torch.stack([wg, wu], dim=1).reshape(2 * F, K)  # rows g0, u0, g1, u1, ...
+    qs, d = qmm.quantize_q4_0(w.to(DEV))
+    h = torch.empty(F, device=DEV)
+    qmm.qmm_gemv_q4_0_f32(qs, d, 2 * F, K, x.to(DEV), None, h, flags=qmm.Y_SWIGLU_PAIRS)
+    qx, dx = O.quantize_q8_0(x.numpy()[None])
+    g, Sg = O.matmul_int(*O.quantize_q4_0(wg.numpy()), qx, dx, nthreads=8)
+    u, Su = O.matmul_int(*O.quantize_q4_0(wu.numpy()), qx, dx, nthreads=8)
+    h_ref = O.swiglu(g[0], u[0]).astype(np.float64)
+    sw = g[0] / (1 + np.exp(-g[0]))
+    tol = 1.1 * np.abs(u[0]) * (1e-5 * Sg[0] + 1e-6) + np.abs(sw) * (1e-5 * Su[0] + 1e-6)
+    tol += 8 * np.spacing(np.abs(h_ref).astype(np.float32)).astype(np.float64)
+    err = np.abs(h.cpu().numpy().astype(np.float64) - h_ref)
+    assert np.all(err <= tol), float((err - tol).max())
+
+
+def test_stream_and_fallback_paths_agree_on_odd_k():
+    """K % 256 != 0 takes the per-row kernel; results stay within tolerance."""
+    qmm = lib()
+    N, K = 130, 2080
+    w = workloads.weights(N, K, seed=8)
+    x = workloads.activations(1, K, seed=8)[0]
+    qs, d = qmm.quantize_q4_0(w.to(DEV))
+    y = torch.empty(N, device=DEV)
+    qmm.qmm_gemv_q4_0_f32(qs, d, N, K, x.to(DEV), None, y)
+    qx, dx = O.quantize_q8_0(x.numpy()[None])
+    ref, S = O.matmul_int(*O.quantize_q4_0(w.numpy()), qx, dx, nthreads=8)
+    assert_close(y[None], ref, S, "odd K")
