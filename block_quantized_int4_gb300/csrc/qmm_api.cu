@@ -12,6 +12,7 @@
 #include "qmm.h"
 #include "qmm_kernels.cuh"
 #include "qmm_stream.cuh"
+#include "qmm_tc.h"
 
 using namespace qmm;
 
@@ -135,11 +136,10 @@ qmm_status rows_launch(const DevInfo* di, RowsArgs a, bool pdl, cudaStream_t st)
 bool valid_k(int64_t K) { return K > 0 && K % QK == 0 && K <= (int64_t)1 << 30; }
 
 // Streaming kernel: eligible when the scale plane can be bulk-copied in row
-// ranges (B % 8 == 0, i.e. K % 256 == 0; d 16-byte aligned) and the staged
+// segments (B % 8 == 0, i.e. K % 256 == 0; d 16-byte aligned) and the staged
 // activation tile fits.
 constexpr int STREAM_XTILE_CAP = 64 * 1024;
-constexpr int STREAM_SMEM_CAP = 110 * 1024;  // two CTAs of consecutive kernels fit on one SM
-constexpr int STREAM_STAGE_TARGET = 16 * 1024;
+constexpr int64_t CHAIN_MATRIX_BYTES = 64ll << 20;  // below this, leave room for a neighbour CTA
 
 bool stream_eligible(int64_t K, const void* qs, const void* d, int MT) {
     const int64_t B = K / QK;
@@ -152,22 +152,20 @@ inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 template <int MT, int XM, int YM>
 qmm_status stream_launch(const DevInfo* di, StreamArgs a, bool pdl, cudaStream_t st) {
     const int64_t B = a.K / QK;
-    const int64_t row_bytes = a.K / 2 + B * 2;
-    int64_t rpc = round_up((a.N + di->sms - 1) / di->sms, 2);
+    const int64_t rpc = round_up((a.N + di->sms - 1) / di->sms, 2);
     const int64_t G = (a.N + rpc - 1) / rpc;
-    int64_t stage_rows = std::max<int64_t>(2, (STREAM_STAGE_TARGET / row_bytes) & ~int64_t(1));
-    stage_rows = std::min(stage_rows, rpc);
-    const int64_t stage_bytes = round_up(stage_rows * row_bytes, 128);
     const int64_t xtile = round_up((int64_t)MT * B * xtile_bytes_per_block(), 128);
-    const int64_t nchunks = (rpc + stage_rows - 1) / stage_rows;
-    int64_t room = (STREAM_SMEM_CAP - STREAM_HDR - xtile) / stage_bytes;
-    int64_t nst = std::min<int64_t>({nchunks, room, (int64_t)STREAM_MAX_STAGES});
+    const int64_t partb = (int64_t)SW * 32 * MT * 4;
+    const int64_t nunits = ((rpc + UNIT_ROWS - 1) / UNIT_ROWS) * ((B + UNIT_KB - 1) / UNIT_KB);
+    // Small matrices (decode chains): stay under ~110 KB so the next chained
+    // kernel's CTA can be resident and prefetch beside this one.
+    const int64_t cap = a.N * (a.K / 2 + B * 2) <= CHAIN_MATRIX_BYTES ? 110 * 1024 : 200 * 1024;
+    const int64_t room = (cap - STREAM_HDR - xtile - partb) / STAGE_BYTES;
+    const int64_t nst = std::min<int64_t>({nunits, room, (int64_t)STREAM_MAX_STAGES});
     if (nst < 1) return QMM_ERR_SHAPE;
-    const int smem = (int)(STREAM_HDR + xtile + nst * stage_bytes);
+    const int smem = (int)(STREAM_HDR + xtile + nst * STAGE_BYTES + partb);
     a.rows_per_cta = (int)rpc;
-    a.stage_rows = (int)stage_rows;
     a.nstages = (int)nst;
-    a.stage_bytes = (int)stage_bytes;
     a.xtile_bytes = (int)xtile;
     a.err = di->err;
     auto kern = stream_rows_kernel<MT, XM, YM>;
@@ -176,8 +174,6 @@ qmm_status stream_launch(const DevInfo* di, StreamArgs a, bool pdl, cudaStream_t
     cudaError_t e = launch(kern, grid, dim3(STREAM_THREADS), smem, st, pdl, a);
     return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
 }
-
-
 
 }  // namespace
 
@@ -332,6 +328,8 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
     a.y = y;
     a.ldy = ldy;
     cudaStream_t st = S(stream);
+    if (M >= 16 && gemm_tc_eligible(N, K, M, w_qs, w_d, xq, xd) && ldy >= N)
+        return gemm_tc_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->err, st);
     const int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
     if (stream_eligible(K, w_qs, w_d, mt)) {
         StreamArgs s = {};

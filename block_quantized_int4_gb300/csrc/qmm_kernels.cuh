@@ -223,39 +223,55 @@ template <bool GATE_UP>
 __device__ __forceinline__ void stage_f32(const XTile& xt, const float* __restrict__ x, int64_t K,
                                           int8_t* __restrict__ xq_out, uint16_t* __restrict__ xd_out, int tid,
                                           int nthr) {
+    // Each warp takes 4 blocks per step (8 lanes per block, one float4 per
+    // lane).  Up to STEPS steps are loaded before any is quantized, so the
+    // activation costs one memory round trip per STEPS * nwarps * 4 blocks.
+    constexpr int STEPS = 8;
     const int B = (int)(K / QK);
     const int lane = tid & 31;
     const int warp = tid >> 5, nwarps = nthr >> 5;
+    const int part = lane & 7;  // which 4 values of the block
     const bool writer = blockIdx.x == 0 && blockIdx.y == 0;
-    for (int g = warp; g * 4 < B; g += nwarps) {
-        const int b = g * 4 + (lane >> 3);
-        const int part = lane & 7;  // which 4 values of the block
-        const bool valid = b < B;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (valid) {
-            const int64_t off = (int64_t)b * QK + part * 4;
-            v = *reinterpret_cast<const float4*>(x + off);
-            if (GATE_UP) {
-                float4 u = *reinterpret_cast<const float4*>(x + K + off);
-                v = make_float4(swiglu1(v.x, u.x), swiglu1(v.y, u.y), swiglu1(v.z, u.z), swiglu1(v.w, u.w));
+    for (int g0 = warp; g0 * 4 < B; g0 += nwarps * STEPS) {
+        float4 v[STEPS];
+#pragma unroll
+        for (int i = 0; i < STEPS; ++i) {
+            const int b = (g0 + i * nwarps) * 4 + (lane >> 3);
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (b < B) {
+                const int64_t off = (int64_t)b * QK + part * 4;
+                v[i] = *reinterpret_cast<const float4*>(x + off);
+                if (GATE_UP) {
+                    const float4 u = *reinterpret_cast<const float4*>(x + K + off);
+                    v[i] = make_float4(swiglu1(v[i].x, u.x), swiglu1(v[i].y, u.y), swiglu1(v[i].z, u.z),
+                                       swiglu1(v[i].w, u.w));
+                }
             }
         }
-        Quad r = quad_codes(v, 127.0f, -127.0f);
-        const int packed = (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) | ((r.c[3] & 0xff) << 24);
-        int s = r.c[0] + r.c[1] + r.c[2] + r.c[3];
-        s += __shfl_xor_sync(FULL, s, 1);
-        s += __shfl_xor_sync(FULL, s, 2);
-        s += __shfl_xor_sync(FULL, s, 4);
-        if (valid) {
-            int* plane = reinterpret_cast<int*>(part < 4 ? &xt.lo[b] : &xt.hi[b]);
-            plane[part & 3] = packed;
-            if (part == 0) {
-                const unsigned short h = f32_to_f16_bits(r.d32);
-                xt.s[b] = f16_bits_to_f32(h);
-                xt.sum[b] = s;
-                if (writer && xd_out) xd_out[b] = h;
+#pragma unroll
+        for (int i = 0; i < STEPS; ++i) {
+            const int g = g0 + i * nwarps;
+            if (g * 4 >= B) break;  // warp-uniform
+            const int b = g * 4 + (lane >> 3);
+            const bool valid = b < B;
+            Quad r = quad_codes(v[i], 127.0f, -127.0f);
+            const int packed =
+                (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) | ((r.c[3] & 0xff) << 24);
+            int s = r.c[0] + r.c[1] + r.c[2] + r.c[3];
+            s += __shfl_xor_sync(FULL, s, 1);
+            s += __shfl_xor_sync(FULL, s, 2);
+            s += __shfl_xor_sync(FULL, s, 4);
+            if (valid) {
+                int* plane = reinterpret_cast<int*>(part < 4 ? &xt.lo[b] : &xt.hi[b]);
+                plane[part & 3] = packed;
+                if (part == 0) {
+                    const unsigned short h = f32_to_f16_bits(r.d32);
+                    xt.s[b] = f16_bits_to_f32(h);
+                    xt.sum[b] = s;
+                    if (writer && xd_out) xd_out[b] = h;
+                }
+                if (writer && xq_out) *reinterpret_cast<int*>(xq_out + (int64_t)b * QK + part * 4) = packed;
             }
-            if (writer && xq_out) *reinterpret_cast<int*>(xq_out + (int64_t)b * QK + part * 4) = packed;
         }
     }
 }

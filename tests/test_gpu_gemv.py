@@ -269,3 +269,25 @@ def test_stream_and_fallback_paths_agree_on_odd_k():
     qx, dx = O.quantize_q8_0(x.numpy()[None])
     ref, S = O.matmul_int(*O.quantize_q4_0(w.numpy()), qx, dx, nthreads=8)
     assert_close(y[None], ref, S, "odd K")
+
+
+@pytest.mark.parametrize("M", [16, 17, 32, 48, 64])
+def test_gemm_tensor_core_integer_grid_exact(M):
+    """Batches of 16..64 tokens take the tensor-core path; with d = 1 on both
+    sides every output is an exact integer, so any loss in the MMA's integer
+    sums (or a wrong operand layout) shows as an inequality."""
+    qmm = lib()
+    rng = np.random.default_rng(M)
+    N, K = 300, 2048
+    w = rng.integers(-7, 8, size=(N, K)).astype(np.float32)
+    w[:, ::32] = 7
+    w[:5, :64] = -8 * 0 + np.array([7, -7] * 32, dtype=np.float32)  # both signs at the block edges
+    x = rng.integers(-127, 128, size=(M, K)).astype(np.float32)
+    x[:, 3::32] = 127
+    x[0, :32] = 127  # largest |sum q_x| in a block
+    qs, d = qmm.quantize_q4_0(torch.from_numpy(w).to(DEV))
+    xq, xd = qmm.quantize_q8_0(torch.from_numpy(x).to(DEV))
+    y = qmm.gemm(qs, d, xq, xd)
+    exact = (x.astype(np.int64) @ w.astype(np.int64).T).astype(np.float32)
+    assert np.array_equal(y.cpu().numpy(), exact)
+    assert qmm.qmm_last_device_error() == 0
