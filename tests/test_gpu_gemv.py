@@ -281,7 +281,7 @@ def test_gemm_tensor_core_integer_grid_exact(M):
     N, K = 300, 2048
     w = rng.integers(-7, 8, size=(N, K)).astype(np.float32)
     w[:, ::32] = 7
-    w[:5, :64] = -8 * 0 + np.array([7, -7] * 32, dtype=np.float32)  # both signs at the block edges
+    w[:5, :64] = np.array([7, -7] * 32, dtype=np.float32)  # both signs, whole blocks
     x = rng.integers(-127, 128, size=(M, K)).astype(np.float32)
     x[:, 3::32] = 127
     x[0, :32] = 127  # largest |sum q_x| in a block
