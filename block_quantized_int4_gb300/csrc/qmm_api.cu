@@ -141,37 +141,48 @@ bool valid_k(int64_t K) { return K > 0 && K % QK == 0 && K <= (int64_t)1 << 30; 
 constexpr int STREAM_XTILE_CAP = 64 * 1024;
 constexpr int64_t CHAIN_MATRIX_BYTES = 64ll << 20;  // below this, leave room for a neighbour CTA
 
-bool stream_eligible(int64_t K, const void* qs, const void* d, int MT) {
+bool stream_eligible(int64_t N, int64_t K, const void* qs, const void* d, int MT) {
     const int64_t B = K / QK;
-    return (B % 8 == 0) && aligned(qs, 16) && aligned(d, 16) &&
+    return (B % 8 == 0) && aligned(qs, 16) && aligned(d, 16) && N < (int64_t(1) << 31) &&
            (int64_t)MT * B * xtile_bytes_per_block() <= STREAM_XTILE_CAP;
 }
 
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
 template <int MT, int XM, int YM>
-qmm_status stream_launch(const DevInfo* di, StreamArgs a, bool pdl, cudaStream_t st) {
+qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d, StreamArgs a, bool pdl,
+                         cudaStream_t st) {
     const int64_t B = a.K / QK;
+    const int64_t row_bytes = a.K / 2 + B * 2;
     const int64_t rpc = round_up((a.N + di->sms - 1) / di->sms, 2);
     const int64_t G = (a.N + rpc - 1) / rpc;
+    const int rb = (int)std::min<int64_t>(GROUP_ROWS, rpc);
+    const int ckb = (int)std::min<int64_t>(CHUNK_KB, B);
     const int64_t xtile = round_up((int64_t)MT * B * xtile_bytes_per_block(), 128);
-    const int64_t partb = (int64_t)SW * 32 * MT * 4;
-    const int64_t nunits = ((rpc + UNIT_ROWS - 1) / UNIT_ROWS) * ((B + UNIT_KB - 1) / UNIT_KB);
+    const int64_t nunits = ((rpc + rb - 1) / rb) * ((B + ckb - 1) / ckb);
     // Small matrices (decode chains): stay under ~110 KB so the next chained
     // kernel's CTA can be resident and prefetch beside this one.
-    const int64_t cap = a.N * (a.K / 2 + B * 2) <= CHAIN_MATRIX_BYTES ? 110 * 1024 : 200 * 1024;
-    const int64_t room = (cap - STREAM_HDR - xtile - partb) / STAGE_BYTES;
+    const int64_t cap = a.N * row_bytes <= CHAIN_MATRIX_BYTES ? 110 * 1024 : 200 * 1024;
+    const int64_t room = (cap - STREAM_HDR - xtile) / STAGE_BYTES;
     const int64_t nst = std::min<int64_t>({nunits, room, (int64_t)STREAM_MAX_STAGES});
     if (nst < 1) return QMM_ERR_SHAPE;
-    const int smem = (int)(STREAM_HDR + xtile + nst * STAGE_BYTES + partb);
+    CUtensorMap mq, md;
+    if (!make_tensor_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT32, qs, (uint64_t)a.K / 8, (uint64_t)a.N,
+                            (uint64_t)a.K / 2, (uint32_t)ckb * 4, (uint32_t)rb, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tensor_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT16, d, (uint64_t)B, (uint64_t)a.N, (uint64_t)B * 2,
+                            (uint32_t)ckb, (uint32_t)rb, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return QMM_ERR_CUDA;
+    const int smem = (int)(STREAM_HDR + xtile + nst * STAGE_BYTES);
     a.rows_per_cta = (int)rpc;
+    a.rb = rb;
+    a.ckb = ckb;
     a.nstages = (int)nst;
     a.xtile_bytes = (int)xtile;
     a.err = di->err;
     auto kern = stream_rows_kernel<MT, XM, YM>;
     if (!smem_optin(kern, smem, di->smem_optin)) return QMM_ERR_SHAPE;
     dim3 grid((unsigned)G, (unsigned)((a.M + MT - 1) / MT));
-    cudaError_t e = launch(kern, grid, dim3(STREAM_THREADS), smem, st, pdl, a);
+    cudaError_t e = launch(kern, grid, dim3(STREAM_THREADS), smem, st, pdl, mq, md, a);
     return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
 }
 
@@ -274,10 +285,8 @@ qmm_status qmm_gemv_q4_0_f32(const uint8_t* w_qs, const uint16_t* w_d, int64_t N
     const DevInfo* di = device_info();
     if (!di) return QMM_ERR_DEVICE;
     cudaStream_t st = S(stream);
-    if (stream_eligible(K, w_qs, w_d, 1)) {
+    if (stream_eligible(N, K, w_qs, w_d, 1)) {
         StreamArgs a = {};
-        a.qs = w_qs;
-        a.d = w_d;
         a.N = N;
         a.K = K;
         a.M = 1;
@@ -287,10 +296,10 @@ qmm_status qmm_gemv_q4_0_f32(const uint8_t* w_qs, const uint16_t* w_d, int64_t N
         a.xd_out = xd_out;
         a.y = y;
         a.ldy = ys ? N / 2 : N;
-        if (ys) return xs ? stream_launch<1, X_SWIGLU, Y_SWIGLU_PAIRS>(di, a, pdl, st)
-                          : stream_launch<1, X_F32, Y_SWIGLU_PAIRS>(di, a, pdl, st);
-        return xs ? stream_launch<1, X_SWIGLU, Y_PLAIN>(di, a, pdl, st)
-                  : stream_launch<1, X_F32, Y_PLAIN>(di, a, pdl, st);
+        if (ys) return xs ? stream_launch<1, X_SWIGLU, Y_SWIGLU_PAIRS>(di, w_qs, w_d, a, pdl, st)
+                          : stream_launch<1, X_F32, Y_SWIGLU_PAIRS>(di, w_qs, w_d, a, pdl, st);
+        return xs ? stream_launch<1, X_SWIGLU, Y_PLAIN>(di, w_qs, w_d, a, pdl, st)
+                  : stream_launch<1, X_F32, Y_PLAIN>(di, w_qs, w_d, a, pdl, st);
     }
     if (ys) return QMM_ERR_SHAPE;  // paired rows need the streaming kernel (K % 256 == 0, d 16-byte aligned)
     RowsArgs a = {};
@@ -331,10 +340,8 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
     if (M >= 16 && gemm_tc_eligible(N, K, M, w_qs, w_d, xq, xd) && ldy >= N)
         return gemm_tc_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->err, st);
     const int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
-    if (stream_eligible(K, w_qs, w_d, mt)) {
+    if (stream_eligible(N, K, w_qs, w_d, mt)) {
         StreamArgs s = {};
-        s.qs = w_qs;
-        s.d = w_d;
         s.N = N;
         s.K = K;
         s.M = M;
@@ -343,10 +350,10 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
         s.y = y;
         s.ldy = ldy;
         switch (mt) {
-            case 1: return stream_launch<1, X_Q8, Y_PLAIN>(di, s, false, st);
-            case 2: return stream_launch<2, X_Q8, Y_PLAIN>(di, s, false, st);
-            case 4: return stream_launch<4, X_Q8, Y_PLAIN>(di, s, false, st);
-            default: return stream_launch<8, X_Q8, Y_PLAIN>(di, s, false, st);
+            case 1: return stream_launch<1, X_Q8, Y_PLAIN>(di, w_qs, w_d, s, false, st);
+            case 2: return stream_launch<2, X_Q8, Y_PLAIN>(di, w_qs, w_d, s, false, st);
+            case 4: return stream_launch<4, X_Q8, Y_PLAIN>(di, w_qs, w_d, s, false, st);
+            default: return stream_launch<8, X_Q8, Y_PLAIN>(di, w_qs, w_d, s, false, st);
         }
     }
     if (M == 1) return rows_launch<1, X_Q8>(di, a, false, st);

@@ -119,10 +119,24 @@ __device__ __forceinline__ uint64_t global_ns() {
 // of wall time (or as soon as *abort is set) and returns false.
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s
 
+// try_wait that lets the hardware suspend the thread for up to `ns` while
+// the phase is incomplete (no busy polling of the issue slots)
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, 20000)) {
         if (*abort) return false;
         if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
     }

@@ -37,11 +37,14 @@ namespace tc {
 
 constexpr int ROWS = 128;           // MMA M (weight rows per CTA)
 constexpr int KB_STAGE = 8;         // K blocks per TMA stage
-constexpr int RAW_STAGES = 4;
-constexpr int CONV_BUFS = 4;        // converted K blocks in flight
+constexpr int RAW_STAGES = 2;
+constexpr int CONV_BUFS_MAX = 16;   // converted K blocks in flight (per NTOK, see conv_bufs)
 constexpr int THREADS = 320;
 constexpr int WARP_TMA = 0, WARP_MMA = 1, WARP_CONV0 = 2, WARP_EPI0 = 6;
 constexpr int NCONV = 4, NEPI = 4;
+
+// converted K blocks in flight: as many as shared memory allows
+__host__ __device__ constexpr int conv_bufs(int ntok) { return ntok <= 16 ? 16 : ntok <= 32 ? 12 : 8; }
 
 struct Layout {
     // byte offsets in dynamic shared memory (base aligned to 1024)
@@ -61,7 +64,7 @@ __host__ __device__ inline Layout layout(int ntok, int slots) {
     L.conv_a = 0;                                // 4 chunks x 128 rows x 16 B
     L.conv_b = ROWS * 64;                        // 6 chunks x ntok x 16 B
     L.conv_stride = (L.conv_b + 6 * ntok * 16 + 127) / 128 * 128;
-    L.aextra = L.conv + CONV_BUFS * L.conv_stride;  // 2 chunks x 128 rows x 16 B
+    L.aextra = L.conv + conv_bufs(ntok) * L.conv_stride;  // 2 chunks x 128 rows x 16 B
     L.a_nib = 0;                                 // 128 rows x 128 B, 128B-swizzled (1024-aligned)
     L.a_d = ROWS * 128;                          // 128 rows x 8 fp16
     L.x_q = L.a_d + ROWS * 16;                   // ntok rows x 256 B int8
@@ -71,16 +74,16 @@ __host__ __device__ inline Layout layout(int ntok, int slots) {
     L.scal = L.raw + RAW_STAGES * L.raw_stage;
     L.scal_stride = (ROWS + ntok) * 4;
     L.bars = (L.scal + slots * L.scal_stride + 127) / 128 * 128;
-    L.total = L.bars + 512;
+    L.total = L.bars + 1024;
     return L;
 }
 
 // mbarrier slots inside the barrier area
 struct Bars {
-    uint64_t* raw_full;    // [RAW_STAGES]  TMA bytes
-    uint64_t* raw_empty;   // [RAW_STAGES]  converters (4 warps)
-    uint64_t* conv_full;   // [CONV_BUFS]   converters (4 warps)
-    uint64_t* conv_empty;  // [CONV_BUFS]   MMA commit
+    uint64_t* raw_full;    // [RAW_STAGES]    TMA bytes
+    uint64_t* raw_empty;   // [RAW_STAGES]    converters (4 warps)
+    uint64_t* conv_full;   // [CONV_BUFS_MAX] converters (4 warps)
+    uint64_t* conv_empty;  // [CONV_BUFS_MAX] MMA commit
     uint64_t* tm_full;     // [slots]       MMA commit
     uint64_t* tm_empty;    // [slots]       epilogue (4 warps)
     uint64_t* sc_full;     // [slots]       converters (4 warps)
@@ -95,8 +98,8 @@ __device__ inline Bars bars_at(uint8_t* p, int slots) {
     b.raw_full = q;
     b.raw_empty = q + RAW_STAGES;
     b.conv_full = b.raw_empty + RAW_STAGES;
-    b.conv_empty = b.conv_full + CONV_BUFS;
-    b.tm_full = b.conv_empty + CONV_BUFS;
+    b.conv_empty = b.conv_full + CONV_BUFS_MAX;
+    b.tm_full = b.conv_empty + CONV_BUFS_MAX;
     b.tm_empty = b.tm_full + slots;
     b.sc_full = b.tm_empty + slots;
     b.mma_done = b.sc_full + slots;
@@ -145,17 +148,16 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 16 consecutive TMEM columns of this thread's lane; completes at tmem_wait_ld()
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // bf16 pair from two small integers (exact for |v| < 256)
 __device__ __forceinline__ uint32_t bf16x2_from_ints(int lo, int hi) {
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int SL = a.ntok_slots;
+    constexpr int CB = conv_bufs(NTOK);
     const Layout L = layout(NTOK, SL);
     const Bars br = bars_at(smem + L.bars, SL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&br.raw_full[i], 1);
             mbar_init(&br.raw_empty[i], NCONV);
         }
-        for (int i = 0; i < CONV_BUFS; ++i) {
+        for (int i = 0; i < CB; ++i) {
             mbar_init(&br.conv_full[i], NCONV);
             mbar_init(&br.conv_empty[i], 1);
         }
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (i < ROWS) v.x = 0x43084308u;  // bf16(136) twice: K elements 0 and 1 of chunk 0
         *reinterpret_cast<uint4*>(smem + L.aextra + i * 16) = v;
     }
-    for (int cb = 0; cb < CONV_BUFS; ++cb)
+    for (int cb = 0; cb < CB; ++cb)
         for (int i = tid; i < 2 * NTOK; i += THREADS)
             *reinterpret_cast<uint4*>(smem + L.conv + cb * L.conv_stride + L.conv_b + (4 * NTOK + i) * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -260,8 +263,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool ok = true;
             int done = 0;
             for (int j = 0; j < nkb; ++j) {
-                const int cb = j % CONV_BUFS, sl = j % SL;
-                if (!mbar_wait(&br.conv_full[cb], (j / CONV_BUFS) & 1, br.abort)) { ok = false; break; }
+                const int cb = j % CB, sl = j % SL;
+                if (!mbar_wait(&br.conv_full[cb], (j / CB) & 1, br.abort)) { ok = false; break; }
                 if (j >= SL && !mbar_wait(&br.tm_empty[sl], ((j / SL) - 1) & 1, br.abort)) { ok = false; break; }
                 tc_fence_after();
                 const uint8_t* cbuf = smem + L.conv + cb * L.conv_stride;
@@ -292,12 +295,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r = tid - WARP_CONV0 * 32;
         for (int j = 0; j < nkb; ++j) {
             const int s = j / KB_STAGE, bi = j % KB_STAGE;
-            const int rs = s % RAW_STAGES, cb = j % CONV_BUFS, sl = j % SL;
+            const int rs = s % RAW_STAGES, cb = j % CB, sl = j % SL;
             // every lane waits (acquire), then the warp agrees, so the warp-wide
             // shuffles below are never reached by only part of it
             bool ok = true;
             if (bi == 0) ok = mbar_wait(&br.raw_full[rs], (s / RAW_STAGES) & 1, br.abort);
-            if (ok && j >= CONV_BUFS) ok = mbar_wait(&br.conv_empty[cb], ((j / CONV_BUFS) - 1) & 1, br.abort);
+            if (ok && j >= CB) ok = mbar_wait(&br.conv_empty[cb], ((j / CB) - 1) & 1, br.abort);
             if (ok && j >= SL) ok = mbar_wait(&br.tm_empty[sl], ((j / SL) - 1) & 1, br.abort);
             if (!__all_sync(0xffffffffu, ok)) {
                 *br.abort = 1;
@@ -363,33 +366,60 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ---------------- epilogue: thread owns row (warp % 4) * 32 + lane
+        // G K blocks per round: wait for all G slots, issue every TMEM load,
+        // one wait, then the fp32 scale-and-add.
+        constexpr int G = NTOK >= 64 ? 1 : 64 / NTOK;
         const int q = warp & 3;
         const int row = q * 32 + lane;
         float acc[NTOK];
 #pragma unroll
         for (int t = 0; t < NTOK; ++t) acc[t] = 0.f;
         bool ok = true;
-        for (int j = 0; j < nkb; ++j) {
-            const int sl = j % SL;
-            bool got = mbar_wait(&br.tm_full[sl], (j / SL) & 1, br.abort) &&
-                       mbar_wait(&br.sc_full[sl], (j / SL) & 1, br.abort);
+        for (int j0 = 0; j0 < nkb; j0 += G) {
+            const int ng = min(G, nkb - j0);
+            bool got = true;
+            for (int g = 0; g < ng && got; ++g) {
+                const int j = j0 + g, sl = j % SL;
+                got = mbar_wait(&br.tm_full[sl], (j / SL) & 1, br.abort) &&
+                      mbar_wait(&br.sc_full[sl], (j / SL) & 1, br.abort);
+            }
             if (!__all_sync(0xffffffffu, got)) {  // tcgen05.ld below is warp-collective
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const float* sc = reinterpret_cast<const float*>(smem + L.scal + sl * L.scal_stride);
-            const float dw = sc[row];
+            uint32_t v[G][NTOK];
 #pragma unroll
-            for (int t0 = 0; t0 < NTOK; t0 += 16) {
-                float v[16];
-                tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(sl * NTOK + t0), v);
+            for (int g = 0; g < G; ++g) {
+                if (g < ng) {
+                    const int sl = (j0 + g) % SL;
 #pragma unroll
-                for (int t = 0; t < 16; ++t) acc[t0 + t] = fmaf(dw * sc[ROWS + t0 + t], v[t], acc[t0 + t]);
+                    for (int t0 = 0; t0 < NTOK; t0 += 16)
+                        tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(sl * NTOK + t0), &v[g][t0]);
+                }
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                if (g < ng) {
+                    const int sl = (j0 + g) % SL;
+                    const float* sc = reinterpret_cast<const float*>(smem + L.scal + sl * L.scal_stride);
+                    const float dw = sc[row];
+                    const float4* sx = reinterpret_cast<const float4*>(sc + ROWS);
+#pragma unroll
+                    for (int t4 = 0; t4 < NTOK / 4; ++t4) {
+                        const float4 dx = sx[t4];
+                        acc[4 * t4 + 0] = fmaf(dw * dx.x, __uint_as_float(v[g][4 * t4 + 0]), acc[4 * t4 + 0]);
+                        acc[4 * t4 + 1] = fmaf(dw * dx.y, __uint_as_float(v[g][4 * t4 + 1]), acc[4 * t4 + 1]);
+                        acc[4 * t4 + 2] = fmaf(dw * dx.z, __uint_as_float(v[g][4 * t4 + 2]), acc[4 * t4 + 2]);
+                        acc[4 * t4 + 3] = fmaf(dw * dx.w, __uint_as_float(v[g][4 * t4 + 3]), acc[4 * t4 + 3]);
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&br.tm_empty[sl]);
+            if (lane == 0)
+                for (int g = 0; g < ng; ++g) mbar_arrive(&br.tm_empty[(j0 + g) % SL]);
         }
         if (!ok) {
             if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
@@ -427,7 +457,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-    auto fn = encode_fn();
+    return make_tensor_map_2d(m, dt, base, inner, outer, row_bytes, box_inner, box_outer, sw);
+}
+
+}  // namespace tc
+
+bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    auto fn = tc::encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {row_bytes};
@@ -436,6 +473,8 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
     return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace tc {
 
 template <int NTOK>
 qmm_status launch_ntok(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, const int8_t* xq,

@@ -25,6 +25,18 @@ struct Quad {
     float d32;
 };
 
+// Correctly rounded x / d (IEEE round to nearest) from r = RN(1/d): the
+// first quotient RN(x * r) is within one ulp of x / d, the FMA gives the
+// exact remainder x - q0 * d, and one more FMA lands on RN(x / d)
+// (Markstein's theorem on division by FMA, as in the Handbook of
+// Floating-Point Arithmetic, ch. 5).  Valid for finite normal operands
+// without overflow; callers fall back to __fdiv_rn outside that range.
+__device__ __forceinline__ float div_rn_fma(float x, float d, float r) {
+    const float q0 = __fmul_rn(x, r);
+    const float rem = __fmaf_rn(-q0, d, x);
+    return __fmaf_rn(rem, r, q0);
+}
+
 __device__ __forceinline__ Quad quad_codes(float4 v, float qmax, float qlo) {
     float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     a = fmaxf(a, __shfl_xor_sync(FULL, a, 1));
@@ -33,10 +45,14 @@ __device__ __forceinline__ Quad quad_codes(float4 v, float qmax, float qlo) {
     Quad r;
     r.d32 = __fdiv_rn(a, qmax);
     const float vv[4] = {v.x, v.y, v.z, v.w};
+    // d32 in [2^-100, 1e30] keeps 1/d32 and every quotient (|x/d32| <= qmax) in range
+    const bool fast = r.d32 >= 7.8886091e-31f && r.d32 <= 1.0e30f;
+    const float rc = fast ? __frcp_rn(r.d32) : 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         if (a != 0.0f) {
-            float t = roundf(__fdiv_rn(vv[i], r.d32));
+            const float qf = fast ? div_rn_fma(vv[i], r.d32, rc) : __fdiv_rn(vv[i], r.d32);
+            const float t = roundf(qf);
             r.c[i] = (int)fminf(fmaxf(t, qlo), qmax);
         } else {
             r.c[i] = 0;

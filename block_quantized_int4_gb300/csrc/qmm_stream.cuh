@@ -1,14 +1,17 @@
 // qmm_stream.cuh -- streaming GEMV / small-batch GEMM for Q4_0 x Q8_0.
 //
-// Each CTA owns a contiguous range of weight rows, taken 32 rows at a time
-// (one row per lane) and 64 K blocks at a time (a "unit").  A producer warp
-// moves each unit's nibble and scale bytes HBM -> shared memory with bulk
-// copies (one per row segment, into padded rows so that the 32 lanes'
-// 16-byte reads fall in distinct bank groups), through a ring of stages.
-// Eight consumer warps each own one eighth of the unit's K blocks: lane l
-// accumulates row l over its warp's blocks with dp4a against the staged
-// activation (a warp-uniform broadcast read), then the eight partial sums of
-// every row are added in a fixed order.  No per-row shuffle reduction.
+// Each CTA owns a contiguous range of weight rows and walks it in groups of
+// RB (<= 32) rows; a group is streamed in K chunks of up to 64 blocks.  One
+// (group, chunk) "unit" is two 2D TMA copies -- the nibble tile (RB rows x
+// 1 KB) and the scale tile (RB rows x 128 B) -- issued by one producer
+// thread into a ring of shared-memory stages.  Eight consumer warps each own
+// four rows of the group (2w, 2w+1, 2w+16, 2w+17: gate/up pairs stay in one
+// warp) for the whole K range: per chunk a lane loads the staged activation
+// of its two blocks (lane, lane+32) once into registers and applies it to its
+// four rows with dp4a, so the activation is read from shared memory once per
+// four rows and no cross-warp reduction is needed.  After the last chunk the
+// warp reduces each row across lanes and writes y (plus a residual, or
+// SwiGLU of a gate/up pair).
 //
 // Decode chains: the producer starts copying before the kernel waits on the
 // preceding grid (griddepcontrol.wait), so under programmatic dependent
@@ -20,25 +23,25 @@
 // section 6.1; SwiGLU of the gate/up pair: TinyLLaMA guide section 4.4.
 #pragma once
 
+#include <cuda.h>
+
 #include "qmm_kernels.cuh"
 
 namespace qmm {
 
 enum YMode { Y_PLAIN = 0, Y_SWIGLU_PAIRS = 1 };
 
-constexpr int SW = 8;                       // consumer warps
+constexpr int SW = 8;  // consumer warps
 constexpr int STREAM_THREADS = (SW + 1) * 32;
-constexpr int STREAM_HDR = 256;             // barriers + flags
+constexpr int STREAM_HDR = 256;  // barriers + flags
 constexpr int STREAM_MAX_STAGES = 8;
-constexpr int UNIT_ROWS = 32;               // rows per unit (one per lane)
-constexpr int UNIT_KB = 64;                 // K blocks per unit (8 per consumer warp)
-constexpr int QSTR = UNIT_KB * 16 + 16;     // padded nibble row in a stage
-constexpr int DSTR = UNIT_KB * 2 + 16;      // padded scale row in a stage
-constexpr int STAGE_BYTES = UNIT_ROWS * (QSTR + DSTR);  // 37,888
+constexpr int GROUP_ROWS = 32;   // rows per group (4 per consumer warp)
+constexpr int CHUNK_KB = 64;     // K blocks per unit (2 per lane)
+constexpr int STAGE_Q = GROUP_ROWS * CHUNK_KB * 16;  // 32 KB
+constexpr int STAGE_D = GROUP_ROWS * CHUNK_KB * 2;   //  4 KB
+constexpr int STAGE_BYTES = STAGE_Q + STAGE_D;
 
 struct StreamArgs {
-    const uint8_t* qs;   // [N][K/2]
-    const uint16_t* d;   // [N][B]
     int64_t N, K, M;
     const int8_t* xq;    // X_Q8: [M][K]
     const uint16_t* xd;  // X_Q8: [M][B]
@@ -49,13 +52,25 @@ struct StreamArgs {
     float* y;
     int64_t ldy;
     int rows_per_cta;    // even
+    int rb;              // rows per group = TMA box rows (even, <= 32)
+    int ckb;             // K blocks per chunk = TMA box width in blocks (multiple of 8, <= 64)
     int nstages;
     int xtile_bytes;     // multiple of 128
     int* err;
 };
 
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
 template <int MT, int XMODE, int YMODE>
-__global__ void __launch_bounds__(STREAM_THREADS) stream_rows_kernel(StreamArgs a) {
+__global__ void __launch_bounds__(STREAM_THREADS)
+    stream_rows_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_d,
+                       StreamArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + STREAM_MAX_STAGES;
@@ -63,17 +78,17 @@ __global__ void __launch_bounds__(STREAM_THREADS) stream_rows_kernel(StreamArgs 
     const int B = (int)(a.K / QK);
     const XTile xt = xtile_at(smem + STREAM_HDR, MT, B);
     uint8_t* ring = smem + STREAM_HDR + a.xtile_bytes;
-    float* part = reinterpret_cast<float*>(ring + (size_t)a.nstages * STAGE_BYTES);  // [SW][32][MT]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+    const int RB = a.rb, CKB = a.ckb;
     const int64_t row_begin = (int64_t)blockIdx.x * a.rows_per_cta;
     const int64_t row_end = min(a.N, row_begin + a.rows_per_cta);
     const int nrows = (int)max((int64_t)0, row_end - row_begin);
-    const int ngroups = (nrows + UNIT_ROWS - 1) / UNIT_ROWS;
-    const int nkc = (B + UNIT_KB - 1) / UNIT_KB;  // K chunks per group
+    const int ngroups = (nrows + RB - 1) / RB;
+    const int nkc = (B + CKB - 1) / CKB;
     const int nunits = ngroups * nkc;
     const int S = a.nstages;
-    const int64_t qrow = a.K / 2;
+    const uint32_t unit_bytes = (uint32_t)(RB * CKB * 18);  // full boxes, OOB parts zero-filled
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -98,17 +113,11 @@ __global__ void __launch_bounds__(STREAM_THREADS) stream_rows_kernel(StreamArgs 
                     break;
                 }
                 const int g = u / nkc, kc = u - g * nkc;
-                const int64_t r0 = row_begin + (int64_t)g * UNIT_ROWS;
-                const int nr = (int)min((int64_t)UNIT_ROWS, row_end - r0);
-                const int b0 = kc * UNIT_KB, nb = min(UNIT_KB, B - b0);
+                const int r0 = (int)(row_begin + (int64_t)g * RB);
                 uint8_t* st = ring + (size_t)s * STAGE_BYTES;
-                mbar_arrive_expect_tx(&full[s], (uint32_t)(nr * nb * 18));
-                const uint8_t* qsrc = a.qs + r0 * qrow + b0 * 16;
-                const uint16_t* dsrc = a.d + r0 * B + b0;
-                for (int r = 0; r < nr; ++r) {
-                    bulk_g2s(st + r * QSTR, qsrc + r * qrow, (uint32_t)(nb * 16), &full[s]);
-                    bulk_g2s(st + UNIT_ROWS * QSTR + r * DSTR, dsrc + (int64_t)r * B, (uint32_t)(nb * 2), &full[s]);
-                }
+                mbar_arrive_expect_tx(&full[s], unit_bytes);
+                tma_load_2d(st, &map_q, kc * CKB * 4, r0, &full[s]);           // u32 columns
+                tma_load_2d(st + STAGE_Q, &map_d, kc * CKB, r0, &full[s]);     // fp16 columns
                 issued = u + 1;
             }
             if (!ok) {
@@ -135,68 +144,90 @@ __global__ void __launch_bounds__(STREAM_THREADS) stream_rows_kernel(StreamArgs 
     else stage_f32<XMODE == X_SWIGLU>(xt, a.xf, a.K, a.xq_out, a.xd_out, tid, NTHR);
     asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
 
-    constexpr int J = UNIT_KB / SW;  // blocks per warp per unit
+    // this warp's rows inside a group
+    int lr[4];
+    lr[0] = 2 * warp;
+    lr[1] = 2 * warp + 1;
+    lr[2] = 2 * warp + 16;
+    lr[3] = 2 * warp + 17;
+    bool failed = false;
     for (int g = 0; g < ngroups; ++g) {
-        const int64_t r0 = row_begin + (int64_t)g * UNIT_ROWS;
-        const int nr = (int)min((int64_t)UNIT_ROWS, row_end - r0);
-        float acc[MT], acc2[MT];
+        const int64_t r0 = row_begin + (int64_t)g * RB;
+        const int nr = (int)min((int64_t)RB, row_end - r0);
+        float acc[4][MT];
 #pragma unroll
-        for (int t = 0; t < MT; ++t) acc[t] = acc2[t] = 0.f;
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[i][t] = 0.f;
         for (int kc = 0; kc < nkc; ++kc) {
             const int u = g * nkc + kc, s = u % S;
             // On a timeout keep going without computing: every later wait returns
-            // at once (abort flag) and all warps still meet at the named barriers.
-            const bool ok = mbar_wait(&full[s], (u / S) & 1, abort_flag);
-            if (!ok) {
+            // at once (abort flag), and the kernel ends with the error word set.
+            const bool ok = !failed && mbar_wait(&full[s], (u / S) & 1, abort_flag);
+            if (!ok && !failed) {
                 if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
                 *abort_flag = 1;
+                failed = true;
             }
-            const int b0 = kc * UNIT_KB, nb = min(UNIT_KB, B - b0);
-            const int jb = warp * J;  // this warp's first block in the unit
-            if (ok && lane < nr && jb < nb) {
-                const uint8_t* st = ring + (size_t)s * STAGE_BYTES;
-                const uint8_t* qr = st + lane * QSTR;
-                // eight scales of this row, one 16-byte read
-                const uint4 dv = lds128(st + UNIT_ROWS * QSTR + lane * DSTR + jb * 2);
-                const unsigned short* dh = reinterpret_cast<const unsigned short*>(&dv);
+            const int b0 = kc * CKB, nb = min(CKB, B - b0);
+            if (ok) {
+                const uint8_t* stq = ring + (size_t)s * STAGE_BYTES;
+                const uint16_t* std_ = reinterpret_cast<const uint16_t*>(stq + STAGE_Q);
 #pragma unroll
-                for (int j = 0; j < J; ++j) {
-                    const int bl = jb + j;  // nb is a multiple of 8, so all J blocks are valid
-                    const uint4 w = lds128(qr + bl * 16);
-                    const float dw = f16_bits_to_f32(dh[j]);
+                for (int h = 0; h < 2; ++h) {
+                    const int bl = lane + 32 * h;  // block inside the chunk
+                    if (bl >= nb) break;
+                    int4 xl[MT], xh[MT];
+                    float xs[MT];
+                    int xc[MT];
 #pragma unroll
                     for (int t = 0; t < MT; ++t) {
                         const int i = t * B + b0 + bl;
-                        const int dot = block_dot_u(w, xt.lo[i], xt.hi[i]) - 8 * xt.sum[i];
-                        if (j & 1) acc2[t] = fmaf(dw * xt.s[i], (float)dot, acc2[t]);
-                        else acc[t] = fmaf(dw * xt.s[i], (float)dot, acc[t]);
+                        xl[t] = xt.lo[i];
+                        xh[t] = xt.hi[i];
+                        xs[t] = xt.s[i];
+                        xc[t] = 8 * xt.sum[i];
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (lr[i] >= nr) continue;
+                        const uint4 w = lds128(stq + (lr[i] * CKB + bl) * 16);
+                        const float dw = f16_bits_to_f32(std_[lr[i] * CKB + bl]);
+#pragma unroll
+                        for (int t = 0; t < MT; ++t) {
+                            const int dot = block_dot_u(w, xl[t], xh[t]) - xc[t];
+                            acc[i][t] = fmaf(dw * xs[t], (float)dot, acc[i][t]);
+                        }
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
-        // fixed-order reduction of the eight warps' partial sums
+        // reduce each of the warp's rows across lanes, write
 #pragma unroll
-        for (int t = 0; t < MT; ++t) part[(warp * 32 + lane) * MT + t] = acc[t] + acc2[t];
-        asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
-        if (warp == 0) {
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[i][t] = warp_sum(acc[i][t]);
+        }
+        if (lane == 0 && !failed) {
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
-                float v = 0.f;
-#pragma unroll
-                for (int w = 0; w < SW; ++w) v += part[(w * 32 + lane) * MT + t];
-                const int64_t row = r0 + lane;
+                if (xrow[t] < 0) continue;
+                float* yr = a.y + xrow[t] * a.ldy;
                 if (YMODE == Y_SWIGLU_PAIRS) {
-                    const float up = __shfl_down_sync(FULL, v, 1);
-                    if ((lane & 1) == 0 && lane < nr && xrow[t] >= 0) a.y[xrow[t] * a.ldy + row / 2] = swiglu1(v, up);
-                } else if (lane < nr && xrow[t] >= 0) {
-                    if (a.residual) v += a.residual[row];
-                    a.y[xrow[t] * a.ldy + row] = v;
+                    if (lr[0] < nr) yr[(r0 + lr[0]) / 2] = swiglu1(acc[0][t], acc[1][t]);
+                    if (lr[2] < nr) yr[(r0 + lr[2]) / 2] = swiglu1(acc[2][t], acc[3][t]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (lr[i] >= nr) continue;
+                        const int64_t row = r0 + lr[i];
+                        yr[row] = acc[i][t] + (a.residual ? a.residual[row] : 0.f);
+                    }
                 }
             }
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
     }
 }
 

@@ -2,6 +2,7 @@
 // tensor-core GEMM translation unit (qmm_gemm_tc.cu).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -19,5 +20,11 @@ bool gemm_tc_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const v
 // device error word (bounded waits that expire set ERR_TIMEOUT in it).
 qmm_status gemm_tc_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,
                           const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy, int* err, cudaStream_t st);
+
+// Encode a 2D tiled TMA descriptor (row-major [outer][inner] tensor of
+// `dt` elements, row pitch `row_bytes`) with the driver's encoder, fetched
+// through the runtime; false if the encoder is unavailable or rejects it.
+bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
 }  // namespace qmm

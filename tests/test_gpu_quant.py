@@ -97,3 +97,24 @@ def test_swiglu_quantize(rows, K):
     assert np.all(np.abs(hg.astype(np.float64) - h_ref) <= 8 * ulp + 1e-30)
     qo, do = O.quantize_q8_0(hg)
     assert np.array_equal(q.cpu().numpy(), qo) and np.array_equal(u16(d), do)
+
+
+def test_q8_0_bit_exact_across_scales():
+    """Blocks whose magnitudes span 1e-30 .. 1e30 (scale of each block drawn
+    log-uniformly), plus exact .5 ties at many scales: the GPU quantizer's
+    division must agree with the oracle's IEEE division everywhere."""
+    qmm = lib()
+    g = torch.Generator().manual_seed(21)
+    M, K = 64, 8192
+    x = torch.randn(M, K, generator=g)
+    scale = torch.pow(10.0, torch.empty(M, K // 32).uniform_(-30, 30, generator=g))
+    x = (x.view(M, K // 32, 32) * scale[..., None]).view(M, K)
+    ties = (torch.arange(32) - 16 + 0.5)
+    for b in range(0, K // 32, 7):
+        s = float(2.0 ** ((b % 61) - 30))
+        x[0, 32 * b:32 * b + 32] = ties * s
+        x[0, 32 * b] = 127 * s
+    q, d = qmm.quantize_q8_0(x.to(DEV))
+    qo, do = O.quantize_q8_0(x.numpy())
+    assert np.array_equal(u16(d), do)
+    assert np.array_equal(q.cpu().numpy(), qo)
