@@ -6,9 +6,9 @@ TinyLLaMA-1.1B-shaped decode step -- 22 layers of fused QKV 2048->2560,
 O 2048->2048, gate/up 2048->2x5632 (one launch over interleaved rows, SwiGLU
 in its epilogue), down 5632->2048 (residual add in its epilogue), then
 lm_head 2048->32000: 89
-dependent GEMV launches per step, each quantizing its fp32 input to Q8_0
-inside the launch, chained with programmatic dependent launch and replayed
-from a CUDA graph.  581,861,376 weight bytes per step (> L2, so no flush).
+dependent GEMV launches per step, each writing its output already in Q8_0
+for the next one (the first quantizes the fp32 token activation), chained
+with programmatic dependent launch and replayed from a CUDA graph.  581,861,376 weight bytes per step (> L2, so no flush).
 
 Also reported on the same line (`also`): batch-16 GEMM TOPS on the large
 dense FFN + lm_head shapes, and the GLM-scale MoE layer.
@@ -144,31 +144,45 @@ class TinyLlamaDecode:
         self.lm_head = planes(self.V, self.H)
         self.weight_bytes = sum(workloads.q4_0_bytes(N, K) for _, N, K in workloads.tinyllama_matrices())
         f32 = lambda n: torch.zeros(n, dtype=torch.float32, device=dev)  # noqa: E731
+        q8 = lambda n: (torch.zeros(n, dtype=torch.int8, device=dev),  # noqa: E731
+                        torch.zeros(n // 32, dtype=torch.int16, device=dev))
         self.x_in = workloads.activations(1, self.H, seed=seed, device=dev)[0].contiguous()
-        self.h = [f32(self.H), f32(self.H)]
-        self.qkv_out, self.o_out, self.h_ffn = f32(self.Q), f32(self.H), f32(self.F)
+        self.h = [f32(self.H), f32(self.H)]       # fp32 residual stream (ping-pong)
+        self.hq = q8(self.H)                       # Q8_0 of the residual stream
+        self.qkv_q, self.o_q, self.ffn_q = q8(self.Q), q8(self.H), q8(self.F)
         self.logits = f32(self.V)
         self.launches_per_step = 4 * self.L + 1
-        # algorithmic bytes per step: weights + fp32 activations read + outputs written (+ residual)
-        act = 0
-        for _ in range(self.L):
-            act += 4 * (self.H + self.Q) + 4 * (self.H + self.H) + 4 * (self.H + self.F) + 4 * (self.F + 2 * self.H)
-        act += 4 * (self.H + self.V)
+        # algorithmic bytes per step: weights + activations read + outputs written
+        # (Q8_0 activations: 34 bytes per 32 values; fp32 residual / logits)
+        q8b = lambda n: n // 32 * 34  # noqa: E731
+        act = 4 * self.H  # the fp32 token activation
+        for li in range(self.L):
+            act += (0 if li == 0 else q8b(self.H)) + q8b(self.Q)        # QKV
+            act += q8b(self.H) + q8b(self.H)                             # O
+            act += q8b(self.H) + q8b(self.F)                             # gate/up
+            act += q8b(self.F) + 4 * self.H + 4 * self.H + q8b(self.H)   # down (+ residual in, fp32 + Q8 out)
+        act += q8b(self.H) + 4 * self.V                                  # lm_head
         self.algo_bytes = self.weight_bytes + act
 
     def step(self, stream=None):
+        """One decode token: every GEMV quantizes (or copies) its activation
+        inside the launch and hands the next one a Q8_0 output."""
         q, H, F = self.qmm, self.H, self.F
         C, YS = q.CHAIN, q.Y_SWIGLU_PAIRS
+        f = q.qmm_gemv_fused
         h_prev = self.x_in
         for li, Lw in enumerate(self.layers):
             h_next = self.h[li % 2]
-            q.qmm_gemv_q4_0_f32(*Lw["qkv"], self.Q, H, h_prev, None, self.qkv_out, flags=C, stream=stream)
+            if li == 0:  # fp32 token activation in
+                f(*Lw["qkv"], self.Q, H, self.x_in, None, None, None, None, *self.qkv_q, flags=C, stream=stream)
+            else:
+                f(*Lw["qkv"], self.Q, H, None, *self.hq, None, None, *self.qkv_q, flags=C, stream=stream)
             # attention is outside this path: the O projection reads the q slice
-            q.qmm_gemv_q4_0_f32(*Lw["o"], H, H, self.qkv_out, None, self.o_out, flags=C, stream=stream)
-            q.qmm_gemv_q4_0_f32(*Lw["gu"], 2 * F, H, self.o_out, None, self.h_ffn, flags=C | YS, stream=stream)
-            q.qmm_gemv_q4_0_f32(*Lw["down"], H, F, self.h_ffn, h_prev, h_next, flags=C, stream=stream)
+            f(*Lw["o"], H, H, None, *self.qkv_q, None, None, *self.o_q, flags=C, stream=stream)
+            f(*Lw["gu"], 2 * F, H, None, *self.o_q, None, None, *self.ffn_q, flags=C | YS, stream=stream)
+            f(*Lw["down"], H, F, None, *self.ffn_q, h_prev, h_next, *self.hq, flags=C, stream=stream)
             h_prev = h_next
-        q.qmm_gemv_q4_0_f32(*self.lm_head, self.V, H, h_prev, None, self.logits, flags=C, stream=stream)
+        f(*self.lm_head, self.V, H, None, *self.hq, None, self.logits, None, None, flags=C, stream=stream)
 
 
 def _graph(torch, fn):
@@ -423,7 +437,7 @@ def main():
                        "pct_of_hbm_peak": round(100 * value / ws / peak, 1)},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": None,
-                         "kernel": "stream_rows_kernel<1,X_F32,*> (all launches of the step)",
+                         "kernel": "stream_rows_kernel<1,*,*,*> (all 89 launches of the step)",
                          "peak_kind": peak_kind},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": dec.H * 4,

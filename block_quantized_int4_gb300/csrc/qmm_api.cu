@@ -149,21 +149,25 @@ bool stream_eligible(int64_t N, int64_t K, const void* qs, const void* d, int MT
 
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
-template <int MT, int XM, int YM>
+template <int MT, int XM, int YM, bool QOUT>
 qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d, StreamArgs a, bool pdl,
                          cudaStream_t st) {
     const int64_t B = a.K / QK;
     const int64_t row_bytes = a.K / 2 + B * 2;
-    const int64_t rpc = round_up((a.N + di->sms - 1) / di->sms, 2);
+    const int64_t opr = YM == Y_SWIGLU_PAIRS ? 2 : 1;
+    // rows per CTA: even; with a Q8_0 output, whole blocks of 32 outputs
+    const int64_t align = QOUT ? QK * opr : 2;
+    const int64_t rpc = round_up((a.N + di->sms - 1) / di->sms, align);
     const int64_t G = (a.N + rpc - 1) / rpc;
     const int rb = (int)std::min<int64_t>(GROUP_ROWS, rpc);
     const int ckb = (int)std::min<int64_t>(CHUNK_KB, B);
     const int64_t xtile = round_up((int64_t)MT * B * xtile_bytes_per_block(), 128);
+    const int64_t ybuf = QOUT ? round_up(rpc / opr * 4, 128) : 0;
     const int64_t nunits = ((rpc + rb - 1) / rb) * ((B + ckb - 1) / ckb);
     // Small matrices (decode chains): stay under ~110 KB so the next chained
     // kernel's CTA can be resident and prefetch beside this one.
     const int64_t cap = a.N * row_bytes <= CHAIN_MATRIX_BYTES ? 110 * 1024 : 200 * 1024;
-    const int64_t room = (cap - STREAM_HDR - xtile) / STAGE_BYTES;
+    const int64_t room = (cap - STREAM_HDR - xtile - ybuf) / STAGE_BYTES;
     const int64_t nst = std::min<int64_t>({nunits, room, (int64_t)STREAM_MAX_STAGES});
     if (nst < 1) return QMM_ERR_SHAPE;
     CUtensorMap mq, md;
@@ -172,18 +176,28 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
         !make_tensor_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT16, d, (uint64_t)B, (uint64_t)a.N, (uint64_t)B * 2,
                             (uint32_t)ckb, (uint32_t)rb, CU_TENSOR_MAP_SWIZZLE_NONE))
         return QMM_ERR_CUDA;
-    const int smem = (int)(STREAM_HDR + xtile + nst * STAGE_BYTES);
+    const int smem = (int)(STREAM_HDR + xtile + nst * STAGE_BYTES + ybuf);
     a.rows_per_cta = (int)rpc;
     a.rb = rb;
     a.ckb = ckb;
     a.nstages = (int)nst;
     a.xtile_bytes = (int)xtile;
     a.err = di->err;
-    auto kern = stream_rows_kernel<MT, XM, YM>;
+    auto kern = stream_rows_kernel<MT, XM, YM, QOUT>;
     if (!smem_optin(kern, smem, di->smem_optin)) return QMM_ERR_SHAPE;
     dim3 grid((unsigned)G, (unsigned)((a.M + MT - 1) / MT));
     cudaError_t e = launch(kern, grid, dim3(STREAM_THREADS), smem, st, pdl, mq, md, a);
     return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
+}
+
+// Batch-1 fused launch over the (input form, output form) combinations.
+template <int XM>
+qmm_status fused_dispatch(const DevInfo* di, const uint8_t* qs, const uint16_t* d, StreamArgs a, bool pairs, bool qout,
+                          bool pdl, cudaStream_t st) {
+    if (pairs) return qout ? stream_launch<1, XM, Y_SWIGLU_PAIRS, true>(di, qs, d, a, pdl, st)
+                           : stream_launch<1, XM, Y_SWIGLU_PAIRS, false>(di, qs, d, a, pdl, st);
+    return qout ? stream_launch<1, XM, Y_PLAIN, true>(di, qs, d, a, pdl, st)
+                : stream_launch<1, XM, Y_PLAIN, false>(di, qs, d, a, pdl, st);
 }
 
 }  // namespace
@@ -296,10 +310,8 @@ qmm_status qmm_gemv_q4_0_f32(const uint8_t* w_qs, const uint16_t* w_d, int64_t N
         a.xd_out = xd_out;
         a.y = y;
         a.ldy = ys ? N / 2 : N;
-        if (ys) return xs ? stream_launch<1, X_SWIGLU, Y_SWIGLU_PAIRS>(di, w_qs, w_d, a, pdl, st)
-                          : stream_launch<1, X_F32, Y_SWIGLU_PAIRS>(di, w_qs, w_d, a, pdl, st);
-        return xs ? stream_launch<1, X_SWIGLU, Y_PLAIN>(di, w_qs, w_d, a, pdl, st)
-                  : stream_launch<1, X_F32, Y_PLAIN>(di, w_qs, w_d, a, pdl, st);
+        return xs ? fused_dispatch<X_SWIGLU>(di, w_qs, w_d, a, ys, false, pdl, st)
+                  : fused_dispatch<X_F32>(di, w_qs, w_d, a, ys, false, pdl, st);
     }
     if (ys) return QMM_ERR_SHAPE;  // paired rows need the streaming kernel (K % 256 == 0, d 16-byte aligned)
     RowsArgs a = {};
@@ -315,6 +327,43 @@ qmm_status qmm_gemv_q4_0_f32(const uint8_t* w_qs, const uint16_t* w_d, int64_t N
     a.y = y;
     a.ldy = N;
     return xs ? rows_launch<1, X_SWIGLU>(di, a, pdl, st) : rows_launch<1, X_F32>(di, a, pdl, st);
+}
+
+qmm_status qmm_gemv_fused(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, const float* x,
+                          const int8_t* xq, const uint16_t* xd, const float* residual, float* y, int8_t* yq,
+                          uint16_t* yd, int flags, void* stream) {
+    if (N < 0 || (flags & ~(QMM_X_SWIGLU | QMM_Y_SWIGLU_PAIRS | QMM_CHAIN))) return QMM_ERR_ARG;
+    if (!valid_k(K) || N == 0 || K > 40960) return QMM_ERR_SHAPE;
+    const bool xs = flags & QMM_X_SWIGLU, ys = flags & QMM_Y_SWIGLU_PAIRS, pdl = flags & QMM_CHAIN;
+    const bool qout = yq != nullptr || yd != nullptr;
+    if (!w_qs || !w_d || (!x && (!xq || !xd)) || (!y && !qout) || (qout && (!yq || !yd))) return QMM_ERR_ARG;
+    if (xs && !x) return QMM_ERR_ARG;
+    if (ys && (N % 2 || residual)) return QMM_ERR_ARG;
+    const int64_t nout = ys ? N / 2 : N;
+    if (qout && nout % QK) return QMM_ERR_SHAPE;
+    if (!aligned(w_qs, 16) || !aligned(w_d, 16) || (x && !aligned(x, 16)) || (xq && !aligned(xq, 16)) ||
+        (xd && !aligned(xd, 2)) || (y && !aligned(y, 4)) || (residual && !aligned(residual, 4)) ||
+        (yq && !aligned(yq, 16)) || (yd && !aligned(yd, 2)))
+        return QMM_ERR_ALIGN;
+    if (!stream_eligible(N, K, w_qs, w_d, 1)) return QMM_ERR_SHAPE;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    StreamArgs a = {};
+    a.N = N;
+    a.K = K;
+    a.M = 1;
+    a.xf = x;
+    a.xq = xq;
+    a.xd = xd;
+    a.residual = residual;
+    a.y = y;
+    a.ldy = nout;
+    a.yq = yq;
+    a.yd = yd;
+    cudaStream_t st = S(stream);
+    if (x) return xs ? fused_dispatch<X_SWIGLU>(di, w_qs, w_d, a, ys, qout, pdl, st)
+                     : fused_dispatch<X_F32>(di, w_qs, w_d, a, ys, qout, pdl, st);
+    return fused_dispatch<X_Q8>(di, w_qs, w_d, a, ys, qout, pdl, st);
 }
 
 qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,
@@ -350,10 +399,10 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
         s.y = y;
         s.ldy = ldy;
         switch (mt) {
-            case 1: return stream_launch<1, X_Q8, Y_PLAIN>(di, w_qs, w_d, s, false, st);
-            case 2: return stream_launch<2, X_Q8, Y_PLAIN>(di, w_qs, w_d, s, false, st);
-            case 4: return stream_launch<4, X_Q8, Y_PLAIN>(di, w_qs, w_d, s, false, st);
-            default: return stream_launch<8, X_Q8, Y_PLAIN>(di, w_qs, w_d, s, false, st);
+            case 1: return stream_launch<1, X_Q8, Y_PLAIN, false>(di, w_qs, w_d, s, false, st);
+            case 2: return stream_launch<2, X_Q8, Y_PLAIN, false>(di, w_qs, w_d, s, false, st);
+            case 4: return stream_launch<4, X_Q8, Y_PLAIN, false>(di, w_qs, w_d, s, false, st);
+            default: return stream_launch<8, X_Q8, Y_PLAIN, false>(di, w_qs, w_d, s, false, st);
         }
     }
     if (M == 1) return rows_launch<1, X_Q8>(di, a, false, st);

@@ -4,14 +4,15 @@
 // RB (<= 32) rows; a group is streamed in K chunks of up to 64 blocks.  One
 // (group, chunk) "unit" is two 2D TMA copies -- the nibble tile (RB rows x
 // 1 KB) and the scale tile (RB rows x 128 B) -- issued by one producer
-// thread into a ring of shared-memory stages.  Eight consumer warps each own
-// four rows of the group (2w, 2w+1, 2w+16, 2w+17: gate/up pairs stay in one
+// thread into a ring of shared-memory stages.  Sixteen consumer warps each
+// own two adjacent rows of the group (2w, 2w+1: a gate/up pair stays in one
 // warp) for the whole K range: per chunk a lane loads the staged activation
-// of its two blocks (lane, lane+32) once into registers and applies it to its
-// four rows with dp4a, so the activation is read from shared memory once per
-// four rows and no cross-warp reduction is needed.  After the last chunk the
-// warp reduces each row across lanes and writes y (plus a residual, or
-// SwiGLU of a gate/up pair).
+// of its two blocks (lane, lane+32) once into registers and applies it to
+// both rows with dp4a; no cross-warp reduction is needed.  After the last
+// chunk the warp reduces each row across lanes and writes y (plus a
+// residual, or SwiGLU of a gate/up pair).  With a Q8_0 output the CTA's row
+// range covers whole 32-output blocks, and the CTA quantizes its own
+// outputs, so the next GEMV of a chain only copies its activation.
 //
 // Decode chains: the producer starts copying before the kernel waits on the
 // preceding grid (griddepcontrol.wait), so under programmatic dependent
@@ -31,11 +32,11 @@ namespace qmm {
 
 enum YMode { Y_PLAIN = 0, Y_SWIGLU_PAIRS = 1 };
 
-constexpr int SW = 8;  // consumer warps
+constexpr int SW = 16;  // consumer warps (two rows each)
 constexpr int STREAM_THREADS = (SW + 1) * 32;
 constexpr int STREAM_HDR = 256;  // barriers + flags
 constexpr int STREAM_MAX_STAGES = 8;
-constexpr int GROUP_ROWS = 32;   // rows per group (4 per consumer warp)
+constexpr int GROUP_ROWS = 32;   // rows per group (2 per consumer warp)
 constexpr int CHUNK_KB = 64;     // K blocks per unit (2 per lane)
 constexpr int STAGE_Q = GROUP_ROWS * CHUNK_KB * 16;  // 32 KB
 constexpr int STAGE_D = GROUP_ROWS * CHUNK_KB * 2;   //  4 KB
@@ -49,8 +50,10 @@ struct StreamArgs {
     const float* residual;  // optional [N] (Y_PLAIN, M == 1)
     int8_t* xq_out;
     uint16_t* xd_out;
-    float* y;
+    float* y;            // may be NULL when a Q8_0 output is requested
     int64_t ldy;
+    int8_t* yq;          // QOUT: Q8_0 codes of the output [N_out]
+    uint16_t* yd;        // QOUT: Q8_0 scales [N_out / 32]
     int rows_per_cta;    // even
     int rb;              // rows per group = TMA box rows (even, <= 32)
     int ckb;             // K blocks per chunk = TMA box width in blocks (multiple of 8, <= 64)
@@ -67,8 +70,10 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
-template <int MT, int XMODE, int YMODE>
-__global__ void __launch_bounds__(STREAM_THREADS)
+// Up to two CTAs per SM for the batch-1 variants (<= 60 registers), so a
+// chained kernel's CTA fits beside the one before it.
+template <int MT, int XMODE, int YMODE, bool QOUT>
+__global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
     stream_rows_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_d,
                        StreamArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -78,6 +83,7 @@ __global__ void __launch_bounds__(STREAM_THREADS)
     const int B = (int)(a.K / QK);
     const XTile xt = xtile_at(smem + STREAM_HDR, MT, B);
     uint8_t* ring = smem + STREAM_HDR + a.xtile_bytes;
+    float* ybuf = reinterpret_cast<float*>(ring + (size_t)a.nstages * STAGE_BYTES);  // QOUT: this CTA's outputs
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     const int RB = a.rb, CKB = a.ckb;
@@ -145,20 +151,15 @@ __global__ void __launch_bounds__(STREAM_THREADS)
     asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
 
     // this warp's rows inside a group
-    int lr[4];
-    lr[0] = 2 * warp;
-    lr[1] = 2 * warp + 1;
-    lr[2] = 2 * warp + 16;
-    lr[3] = 2 * warp + 17;
+    const int lr0 = 2 * warp, lr1 = 2 * warp + 1;
+    constexpr int OPR = YMODE == Y_SWIGLU_PAIRS ? 2 : 1;  // rows per output
     bool failed = false;
     for (int g = 0; g < ngroups; ++g) {
         const int64_t r0 = row_begin + (int64_t)g * RB;
         const int nr = (int)min((int64_t)RB, row_end - r0);
-        float acc[4][MT];
+        float acc0[MT], acc1[MT];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int t = 0; t < MT; ++t) acc[i][t] = 0.f;
+        for (int t = 0; t < MT; ++t) acc0[t] = acc1[t] = 0.f;
         for (int kc = 0; kc < nkc; ++kc) {
             const int u = g * nkc + kc, s = u % S;
             // On a timeout keep going without computing: every later wait returns
@@ -170,62 +171,84 @@ __global__ void __launch_bounds__(STREAM_THREADS)
                 failed = true;
             }
             const int b0 = kc * CKB, nb = min(CKB, B - b0);
-            if (ok) {
+            if (ok && lr0 < nr) {
                 const uint8_t* stq = ring + (size_t)s * STAGE_BYTES;
                 const uint16_t* std_ = reinterpret_cast<const uint16_t*>(stq + STAGE_Q);
+                const bool has1 = lr1 < nr;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int bl = lane + 32 * h;  // block inside the chunk
                     if (bl >= nb) break;
-                    int4 xl[MT], xh[MT];
-                    float xs[MT];
-                    int xc[MT];
+                    const uint4 w0 = lds128(stq + (lr0 * CKB + bl) * 16);
+                    const uint4 w1 = has1 ? lds128(stq + (lr1 * CKB + bl) * 16) : make_uint4(0, 0, 0, 0);
+                    const float d0 = f16_bits_to_f32(std_[lr0 * CKB + bl]);
+                    const float d1 = has1 ? f16_bits_to_f32(std_[lr1 * CKB + bl]) : 0.f;
 #pragma unroll
                     for (int t = 0; t < MT; ++t) {
                         const int i = t * B + b0 + bl;
-                        xl[t] = xt.lo[i];
-                        xh[t] = xt.hi[i];
-                        xs[t] = xt.s[i];
-                        xc[t] = 8 * xt.sum[i];
-                    }
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if (lr[i] >= nr) continue;
-                        const uint4 w = lds128(stq + (lr[i] * CKB + bl) * 16);
-                        const float dw = f16_bits_to_f32(std_[lr[i] * CKB + bl]);
-#pragma unroll
-                        for (int t = 0; t < MT; ++t) {
-                            const int dot = block_dot_u(w, xl[t], xh[t]) - xc[t];
-                            acc[i][t] = fmaf(dw * xs[t], (float)dot, acc[i][t]);
-                        }
+                        const int4 xl = xt.lo[i], xh = xt.hi[i];
+                        const float xs = xt.s[i];
+                        const int xc = 8 * xt.sum[i];
+                        const int p0 = block_dot_u(w0, xl, xh) - xc;
+                        const int p1 = block_dot_u(w1, xl, xh) - xc;
+                        acc0[t] = fmaf(d0 * xs, (float)p0, acc0[t]);
+                        acc1[t] = fmaf(d1 * xs, (float)p1, acc1[t]);
                     }
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
-        // reduce each of the warp's rows across lanes, write
+        // reduce the warp's two rows across lanes, write
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-            for (int t = 0; t < MT; ++t) acc[i][t] = warp_sum(acc[i][t]);
+        for (int t = 0; t < MT; ++t) {
+            acc0[t] = warp_sum(acc0[t]);
+            acc1[t] = warp_sum(acc1[t]);
         }
-        if (lane == 0 && !failed) {
+        if (lane == 0 && !failed && lr0 < nr) {
+            const bool has1 = lr1 < nr;
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 if (xrow[t] < 0) continue;
-                float* yr = a.y + xrow[t] * a.ldy;
                 if (YMODE == Y_SWIGLU_PAIRS) {
-                    if (lr[0] < nr) yr[(r0 + lr[0]) / 2] = swiglu1(acc[0][t], acc[1][t]);
-                    if (lr[2] < nr) yr[(r0 + lr[2]) / 2] = swiglu1(acc[2][t], acc[3][t]);
+                    const float v = swiglu1(acc0[t], acc1[t]);
+                    const int64_t o = (r0 + lr0) / 2;
+                    if (a.y) a.y[xrow[t] * a.ldy + o] = v;
+                    if (QOUT) ybuf[o - row_begin / 2] = v;
                 } else {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if (lr[i] >= nr) continue;
-                        const int64_t row = r0 + lr[i];
-                        yr[row] = acc[i][t] + (a.residual ? a.residual[row] : 0.f);
+                    const int64_t row = r0 + lr0;
+                    const float v0 = acc0[t] + (a.residual ? a.residual[row] : 0.f);
+                    const float v1 = has1 ? acc1[t] + (a.residual ? a.residual[row + 1] : 0.f) : 0.f;
+                    if (a.y) {
+                        a.y[xrow[t] * a.ldy + row] = v0;
+                        if (has1) a.y[xrow[t] * a.ldy + row + 1] = v1;
+                    }
+                    if (QOUT) {
+                        ybuf[row - row_begin] = v0;
+                        if (has1) ybuf[row + 1 - row_begin] = v1;
                     }
                 }
+            }
+        }
+    }
+    if (QOUT) {
+        // Q8_0 of this CTA's outputs (whole blocks of 32; M == 1): warp w takes
+        // blocks 4w.., eight lanes per block, same rounding as the quantizers.
+        asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
+        const int nout = nrows / OPR;
+        const int nblk = nout / QK;
+        const int64_t out0 = row_begin / OPR;
+        for (int blk0 = warp * 4; blk0 < nblk; blk0 += SW * 4) {
+            const int blk = blk0 + (lane >> 3), part = lane & 7;
+            const bool valid = blk < nblk && !failed;
+            const float4 v = valid ? *reinterpret_cast<const float4*>(ybuf + blk * QK + part * 4)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            const Quad r = quad_codes(v, 127.0f, -127.0f);
+            if (valid) {
+                const int packed = (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) |
+                                   ((r.c[3] & 0xff) << 24);
+                *reinterpret_cast<int*>(a.yq + (out0 + blk * QK) + part * 4) = packed;
+                if (part == 0) a.yd[out0 / QK + blk] = f32_to_f16_bits(r.d32);
             }
         }
     }

@@ -47,6 +47,7 @@ SIGNATURES = {
     "qmm_swiglu_quantize_q8_0": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _P],
     "qmm_gemv_q4_0_q8_0": [_P, _P, _I64, _I64, _P, _P, _P, _P],
     "qmm_gemv_q4_0_f32": [_P, _P, _I64, _I64, _P, _P, _P, _P, _P, _INT, _P],
+    "qmm_gemv_fused": [_P, _P, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _INT, _P],
     "qmm_gemm_q4_0_q8_0": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P],
     "qmm_debug_block_dots": [_P, _I64, _I64, _I64, _P, _P, _P],
     "qmm_moe_workspace_size": [_I32, _I32, _I32, ctypes.POINTER(_SZ)],
@@ -126,6 +127,11 @@ X_SWIGLU, Y_SWIGLU_PAIRS, CHAIN = 1, 2, 4  # flags of qmm_gemv_q4_0_f32
 def qmm_gemv_q4_0_f32(w_qs, w_d, N, K, x, residual, y, xq_out=None, xd_out=None, flags=0, stream=None):
     _check(_lib.qmm_gemv_q4_0_f32(_ptr(w_qs), _ptr(w_d), N, K, _ptr(x), _ptr(residual), _ptr(y), _ptr(xq_out),
                                   _ptr(xd_out), int(flags), _stream(stream)), "qmm_gemv_q4_0_f32")
+
+
+def qmm_gemv_fused(w_qs, w_d, N, K, x, xq, xd, residual, y, yq, yd, flags=0, stream=None):
+    _check(_lib.qmm_gemv_fused(_ptr(w_qs), _ptr(w_d), N, K, _ptr(x), _ptr(xq), _ptr(xd), _ptr(residual), _ptr(y),
+                               _ptr(yq), _ptr(yd), int(flags), _stream(stream)), "qmm_gemv_fused")
 
 
 def qmm_gemm_q4_0_q8_0(w_qs, w_d, N, K, M, xq, xd, y, ldy, stream=None):

@@ -149,6 +149,24 @@ QMM_API qmm_status qmm_gemv_q4_0_f32(const uint8_t* w_qs, const uint16_t* w_d, i
                              const float* x, const float* residual, float* y,
                              int8_t* xq_out, uint16_t* xd_out, int flags, void* stream);
 
+/* Batch-1 GEMV of a decode chain, input and output forms chosen per call:
+ *  - activation: fp32 x [K] (quantized to Q8_0 inside the launch, as in
+ *    qmm_gemv_q4_0_f32, QMM_X_SWIGLU allowed) when x is not NULL, else the
+ *    Q8_0 activation xq [K] (16-byte aligned) / xd [B];
+ *  - output: fp32 y [N_out] (+ residual [N] when not NULL) when y is not
+ *    NULL, and/or its Q8_0 encoding yq [N_out] (16-byte aligned) / yd
+ *    [N_out/32] when yq and yd are not NULL -- exactly what
+ *    qmm_quantize_q8_0 would make of y, so the next GEMV of a chain reads it
+ *    with no quantization of its own.  N_out = N, or N/2 with
+ *    QMM_Y_SWIGLU_PAIRS.  A Q8_0 output needs N_out % 32 == 0.
+ * flags: QMM_X_SWIGLU, QMM_Y_SWIGLU_PAIRS, QMM_CHAIN as for
+ * qmm_gemv_q4_0_f32.  Requires K % 256 == 0 and w_d 16-byte aligned (the
+ * weights are streamed by the tensor-memory-access engine); K <= 40960. */
+QMM_API qmm_status qmm_gemv_fused(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
+                                  const float* x, const int8_t* xq, const uint16_t* xd,
+                                  const float* residual, float* y, int8_t* yq, uint16_t* yd,
+                                  int flags, void* stream);
+
 /* Small-batch GEMM (batched decode, speculative verify -- Colibri page,
  * MTP drafts verified in one batched forward): for m < M, n < N,
  * y[m*ldy + n] = sum_b d_w[n][b] * d_x[m][b] * dot(m, n, b).

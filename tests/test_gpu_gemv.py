@@ -291,3 +291,97 @@ def test_gemm_tensor_core_integer_grid_exact(M):
     exact = (x.astype(np.int64) @ w.astype(np.int64).T).astype(np.float32)
     assert np.array_equal(y.cpu().numpy(), exact)
     assert qmm.qmm_last_device_error() == 0
+
+
+@pytest.mark.parametrize("case", ["f32_in_plain", "q8_in_pairs", "q8_in_residual", "f32_in_swiglu_x"])
+def test_gemv_fused_q8_outputs(case):
+    """qmm_gemv_fused: fp32 or Q8_0 activation in; fp32 y within tolerance of
+    the oracle; the Q8_0 output is bit-identical to qmm_quantize_q8_0 applied
+    to that y (the standalone quantizer is itself bit-exact against the
+    oracle), i.e. the epilogue quantizes exactly like the quantizer."""
+    qmm = lib()
+    if case == "f32_in_plain":
+        N, K, flags = 2560, 2048, 0
+    elif case == "q8_in_pairs":
+        N, K, flags = 2 * 5632, 2048, qmm.Y_SWIGLU_PAIRS
+    elif case == "q8_in_residual":
+        N, K, flags = 2048, 5632, 0
+    else:
+        N, K, flags = 2048, 5632, qmm.X_SWIGLU
+    w = workloads.weights(N, K, seed=3, index=N + K)
+    qs, d = qmm.quantize_q4_0(w.to(DEV))
+    xin = workloads.activations(1, K * (2 if flags & qmm.X_SWIGLU else 1), seed=3)[0]
+    xdev = xin.to(DEV)
+    nout = N // 2 if flags & qmm.Y_SWIGLU_PAIRS else N
+    y = torch.full((nout,), float("nan"), device=DEV)
+    yq = torch.zeros(nout, dtype=torch.int8, device=DEV)
+    yd = torch.zeros(nout // 32, dtype=torch.int16, device=DEV)
+    res = workloads.activations(1, N, seed=4)[0] if case == "q8_in_residual" else None
+    if case.startswith("q8_in"):
+        xq, xd = qmm.quantize_q8_0(xdev)
+        qmm.qmm_gemv_fused(qs, d, N, K, None, xq, xd, None if res is None else res.to(DEV), y, yq, yd, flags=flags)
+        qx, dx = O.quantize_q8_0(xin.numpy()[None])
+        assert np.array_equal(xq.cpu().numpy(), qx)
+    else:
+        qmm.qmm_gemv_fused(qs, d, N, K, xdev, None, None, None, y, yq, yd, flags=flags)
+        if flags & qmm.X_SWIGLU:
+            h = torch.empty(1, K, device=DEV)
+            hq = torch.empty(1, K, dtype=torch.int8, device=DEV)
+            hd = torch.empty(1, K // 32, dtype=torch.int16, device=DEV)
+            qmm.qmm_swiglu_quantize_q8_0(xdev[:K], xdev[K:], 1, K, K, hq, hd, h)
+            qx, dx = O.quantize_q8_0(h.cpu().numpy())
+        else:
+            qx, dx = O.quantize_q8_0(xin.numpy()[None])
+    qw, dw = O.quantize_q4_0(w.numpy())
+    if flags & qmm.Y_SWIGLU_PAIRS:
+        ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+        g, u = ref[0, 0::2], ref[0, 1::2]
+        h_ref = O.swiglu(g, u).astype(np.float64)
+        sw = g / (1 + np.exp(-g))
+        tol = 1.1 * np.abs(u) * (1e-5 * S[0, 0::2] + 1e-6) + np.abs(sw) * (1e-5 * S[0, 1::2] + 1e-6)
+        tol += 8 * np.spacing(np.abs(h_ref).astype(np.float32)).astype(np.float64)
+        assert np.all(np.abs(y.cpu().numpy().astype(np.float64) - h_ref) <= tol)
+    else:
+        ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+        if res is not None:
+            ref = ref + res.numpy().astype(np.float64)[None]
+            # the fp32 add of the residual rounds once more: 2e-7 |y| > 1 ulp
+            S = S + 0.02 * np.abs(ref)
+        assert_close(y[None], ref, S, case)
+    yq2, yd2 = qmm.quantize_q8_0(y)
+    assert np.array_equal(yq.cpu().numpy(), yq2.cpu().numpy()[0])
+    assert np.array_equal(u16(yd), u16(yd2)[0])
+
+
+def test_gemv_fused_chain_of_q8_outputs():
+    """Four chained launches (programmatic dependent launch), each reading the
+    previous launch's Q8_0 output.  The oracle runs its own chain from the
+    same fp32 input: the first step matches element by element; later steps
+    can differ where a tiny fp32 difference moves an activation code at a
+    rounding boundary, so they are held to a relative L2 bound of 1e-3.
+    Every Q8_0 output equals qmm_quantize_q8_0 of the launch's own y."""
+    qmm = lib()
+    K = 2048
+    ws = [workloads.weights(K, K, seed=12, index=i) for i in range(4)]
+    planes = [qmm.quantize_q4_0(w.to(DEV)) for w in ws]
+    x0 = workloads.activations(1, K, seed=12)[0]
+    ys = [torch.empty(K, device=DEV) for _ in ws]
+    qs_ = [(torch.empty(K, dtype=torch.int8, device=DEV), torch.empty(K // 32, dtype=torch.int16, device=DEV))
+           for _ in ws]
+    for i, (qs, d) in enumerate(planes):
+        if i == 0:
+            qmm.qmm_gemv_fused(qs, d, K, K, x0.to(DEV), None, None, None, ys[i], *qs_[i], flags=qmm.CHAIN)
+        else:
+            qmm.qmm_gemv_fused(qs, d, K, K, None, *qs_[i - 1], None, ys[i], *qs_[i], flags=qmm.CHAIN)
+    torch.cuda.synchronize()
+    x_ref = x0.numpy().astype(np.float32)[None]
+    for i, w in enumerate(ws):
+        ref, S = O.matmul_int(*O.quantize_q4_0(w.numpy()), *O.quantize_q8_0(x_ref), nthreads=8)
+        if i == 0:
+            assert_close(ys[i][None], ref, S, "chain step 0")
+        yg = ys[i].cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(yg - ref[0]) <= 1e-3 * np.linalg.norm(ref[0]), i
+        yq2, yd2 = qmm.quantize_q8_0(ys[i])
+        assert np.array_equal(qs_[i][0].cpu().numpy(), yq2.cpu().numpy()[0])
+        assert np.array_equal(u16(qs_[i][1]), u16(yd2)[0])
+        x_ref = ref.astype(np.float32)
