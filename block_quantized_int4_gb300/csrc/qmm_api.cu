@@ -157,7 +157,17 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
     const int64_t opr = YM == Y_SWIGLU_PAIRS ? 2 : 1;
     // rows per CTA: even; with a Q8_0 output, whole blocks of 32 outputs
     const int64_t align = QOUT ? QK * opr : 2;
-    const int64_t rpc = round_up((a.N + di->sms - 1) / di->sms, align);
+    // Large matrices: two CTAs per SM (more warps to hide latency); small
+    // ones (decode chains): one per SM, leaving room for the next kernel.
+#ifndef QMM_STREAM_BIG_CTAS_PER_SM
+#define QMM_STREAM_BIG_CTAS_PER_SM 2
+#endif
+#ifndef QMM_STREAM_BIG_SMEM_KB
+#define QMM_STREAM_BIG_SMEM_KB 110
+#endif
+    const bool chain_sized = a.N * row_bytes <= CHAIN_MATRIX_BYTES;
+    const int64_t ctas = chain_sized ? di->sms : QMM_STREAM_BIG_CTAS_PER_SM * (int64_t)di->sms;
+    const int64_t rpc = round_up((a.N + ctas - 1) / ctas, align);
     const int64_t G = (a.N + rpc - 1) / rpc;
     const int rb = (int)std::min<int64_t>(GROUP_ROWS, rpc);
     const int ckb = (int)std::min<int64_t>(CHUNK_KB, B);
@@ -166,7 +176,7 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
     const int64_t nunits = ((rpc + rb - 1) / rb) * ((B + ckb - 1) / ckb);
     // Small matrices (decode chains): stay under ~110 KB so the next chained
     // kernel's CTA can be resident and prefetch beside this one.
-    const int64_t cap = a.N * row_bytes <= CHAIN_MATRIX_BYTES ? 110 * 1024 : 200 * 1024;
+    const int64_t cap = chain_sized ? 110 * 1024 : QMM_STREAM_BIG_SMEM_KB * 1024;  // two CTAs fit on one SM
     const int64_t room = (cap - STREAM_HDR - xtile - ybuf) / STAGE_BYTES;
     const int64_t nst = std::min<int64_t>({nunits, room, (int64_t)STREAM_MAX_STAGES});
     if (nst < 1) return QMM_ERR_SHAPE;
@@ -449,6 +459,57 @@ qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int
     qmm_status s = launch_status();
     if (s != QMM_OK) return s;
 
+    const int64_t B = K / QK;
+    const int64_t nslots = (int64_t)T * k;
+    const bool streamable = (B % 8 == 0) && aligned(w_qs, 16) && aligned(w_d, 16) &&
+                            (int64_t)E * N < (int64_t(1) << 31) && E <= 2048 &&
+                            4 * B * xtile_bytes_per_block() <= STREAM_XTILE_CAP;
+    if (streamable) {
+        MoeStreamArgs m = {};
+        m.N = N;
+        m.K = K;
+        m.E = E;
+        m.k = k;
+        m.xq = xq;
+        m.xd = xd;
+        m.x_per_slot = x_per_slot;
+        m.y = y;
+        m.ws = ws;
+        m.rb = GROUP_ROWS;
+        m.ckb = (int)std::min<int64_t>(CHUNK_KB, B);
+        m.err = di->err;
+        // Slots per weight pass: one, unless experts average two or more
+        // routed slots (then four per pass).  Measured on the GLM-scale layer
+        // (T = 1 and 16, top-8 of 256): one slot per pass is faster even though
+        // an expert with several slots is streamed once per slot.
+        const int mt = nslots >= 2 * (int64_t)E ? 4 : 1;
+        const int64_t xtile = round_up((int64_t)mt * B * xtile_bytes_per_block(), 128);
+        const int64_t tables = round_up((int64_t)E * 12, 128);  // active list + slot spans in shared memory
+        // two CTAs per SM (110 KB each): more warps to hide the dot-product latency
+        const int64_t nst =
+            std::min<int64_t>((110 * 1024 - STREAM_HDR - xtile - tables) / STAGE_BYTES, STREAM_MAX_STAGES);
+        if (nst < 1) return QMM_ERR_SHAPE;
+        m.nstages = (int)nst;
+        m.xtile_bytes = (int)xtile;
+        const int smem = (int)(STREAM_HDR + xtile + nst * STAGE_BYTES + tables);
+        CUtensorMap mq, md;
+        if (!make_tensor_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT32, w_qs, (uint64_t)K / 8, (uint64_t)E * N,
+                                (uint64_t)K / 2, (uint32_t)m.ckb * 4, GROUP_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !make_tensor_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT16, w_d, (uint64_t)B, (uint64_t)E * N,
+                                (uint64_t)B * 2, (uint32_t)m.ckb, GROUP_ROWS, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return QMM_ERR_CUDA;
+        cudaError_t e;
+        dim3 grid(2 * di->sms);
+        if (mt == 4) {
+            if (!smem_optin(moe_stream_kernel<4>, smem, di->smem_optin)) return QMM_ERR_SHAPE;
+            e = launch(moe_stream_kernel<4>, grid, dim3(STREAM_THREADS), smem, st, false, mq, md, m);
+        } else {
+            if (!smem_optin(moe_stream_kernel<1>, smem, di->smem_optin)) return QMM_ERR_SHAPE;
+            e = launch(moe_stream_kernel<1>, grid, dim3(STREAM_THREADS), smem, st, false, mq, md, m);
+        }
+        return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
+    }
+
     MoeArgs a = {};
     a.qs = w_qs;
     a.d = w_d;
@@ -462,7 +523,6 @@ qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int
     a.y = y;
     a.ws = ws;
     a.rows_per_item = 8 * ROWS_WARPS;
-    const int64_t B = K / QK;
     const int per_block = xtile_bytes_per_block();
     const int64_t cap = std::min(di->smem_optin, 200 * 1024);
     // Token-group width: widest that stages the whole K.
@@ -470,7 +530,6 @@ qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int
     while (mt > 1 && (int64_t)mt * B * per_block > cap) mt /= 2;
     if ((int64_t)mt * B * per_block > cap) return QMM_ERR_SHAPE;
     // Tokens per expert on average decides how wide a group is useful.
-    const int64_t nslots = (int64_t)T * k;
     const int64_t max_slots = std::min<int64_t>(nslots, 8);
     while (mt > 1 && mt / 2 >= max_slots) mt /= 2;
     const int smem = (int)(mt * B * per_block);

@@ -63,6 +63,36 @@ __device__ __forceinline__ int block_dot_u(uint4 w, int4 xlo, int4 xhi) {
     return s;
 }
 
+// Sixteen times the block dot, with the -8 offset folded in: c = -128 *
+// sum(q_x) seeds the high-nibble chain, and the high nibbles stay in place
+// (w & 0xF0F0F0F0 contributes 16 * u_hi), so no shifts are needed:
+// 16 * sum_lo + (16 * sum_hi - 128 * sum(q_x)) = 16 * sum_i q_w,i * q_x,i.
+__device__ __forceinline__ int block_dot16(uint4 w, int4 xlo, int4 xhi, int c) {
+    constexpr unsigned LO = 0x0F0F0F0Fu, HI = 0xF0F0F0F0u;
+    int lo = dp4a_us(w.x & LO, xlo.x, 0);
+    int hi = dp4a_us(w.x & HI, xhi.x, c);
+    lo = dp4a_us(w.y & LO, xlo.y, lo);
+    hi = dp4a_us(w.y & HI, xhi.y, hi);
+    lo = dp4a_us(w.z & LO, xlo.z, lo);
+    hi = dp4a_us(w.z & HI, xhi.z, hi);
+    lo = dp4a_us(w.w & LO, xlo.w, lo);
+    hi = dp4a_us(w.w & HI, xhi.w, hi);
+    return lo * 16 + hi;
+}
+
+// Packed pair of fp32 lanes (two weight rows): acc += (a * b) * c elementwise,
+// each product and sum rounded exactly as the scalar fmaf(a * b, c, acc).
+__device__ __forceinline__ float2 ffma2_scaled(float2 a, float2 b, float2 c, float2 acc) {
+    unsigned long long ua, ub, uc, ud, um, r;
+    ua = *reinterpret_cast<unsigned long long*>(&a);
+    ub = *reinterpret_cast<unsigned long long*>(&b);
+    uc = *reinterpret_cast<unsigned long long*>(&c);
+    ud = *reinterpret_cast<unsigned long long*>(&acc);
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(um) : "l"(ua), "l"(ub));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(um), "l"(uc), "l"(ud));
+    return *reinterpret_cast<float2*>(&r);
+}
+
 // ---------------------------------------------------------------- fp16 bits
 __device__ __forceinline__ unsigned short f32_to_f16_bits(float f) {
     return __half_as_ushort(__float2half_rn(f));

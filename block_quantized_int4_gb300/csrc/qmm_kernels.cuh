@@ -179,16 +179,14 @@ __global__ void repack_q4_0_kernel(const uint8_t* __restrict__ blocks, int64_t n
 struct XTile {
     int4* lo;
     int4* hi;
-    float* s;
-    int* sum;
+    int2* sc;  // (fp32 bits of the scale, sum of the block's codes): one 8-byte read
 };
 
 __device__ __forceinline__ XTile xtile_at(void* smem, int MT, int Bc) {
     XTile t;
     t.lo = reinterpret_cast<int4*>(smem);
     t.hi = t.lo + MT * Bc;
-    t.s = reinterpret_cast<float*>(t.hi + MT * Bc);
-    t.sum = reinterpret_cast<int*>(t.s + MT * Bc);
+    t.sc = reinterpret_cast<int2*>(t.hi + MT * Bc);
     return t;
 }
 
@@ -227,8 +225,7 @@ __device__ __forceinline__ void stage_q8(const XTile& xt, int Bc, const int8_t* 
         }
         xt.lo[i] = lo;
         xt.hi[i] = hi;
-        xt.s[i] = s;
-        xt.sum[i] = block_qsum(lo, hi);
+        xt.sc[i] = make_int2(__float_as_int(s), block_qsum(lo, hi));
     }
 }
 
@@ -282,8 +279,7 @@ __device__ __forceinline__ void stage_f32(const XTile& xt, const float* __restri
                 plane[part & 3] = packed;
                 if (part == 0) {
                     const unsigned short h = f32_to_f16_bits(r.d32);
-                    xt.s[b] = f16_bits_to_f32(h);
-                    xt.sum[b] = s;
+                    xt.sc[b] = make_int2(__float_as_int(f16_bits_to_f32(h)), s);
                     if (writer && xd_out) xd_out[b] = h;
                 }
                 if (writer && xq_out) *reinterpret_cast<int*>(xq_out + (int64_t)b * QK + part * 4) = packed;
@@ -313,8 +309,9 @@ __device__ __forceinline__ void row_accumulate(const XTile& xt, int Bc, const ui
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 const int i = t * Bc + bb;
-                const int dot = block_dot_u(w[u], xt.lo[i], xt.hi[i]) - 8 * xt.sum[i];
-                acc[t] = fmaf(dw[u] * xt.s[i], (float)dot, acc[t]);
+                const int2 sc = xt.sc[i];
+                const int dot = block_dot_u(w[u], xt.lo[i], xt.hi[i]) - 8 * sc.y;
+                acc[t] = fmaf(dw[u] * __int_as_float(sc.x), (float)dot, acc[t]);
             }
         }
     }
@@ -324,8 +321,9 @@ __device__ __forceinline__ void row_accumulate(const XTile& xt, int Bc, const ui
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
             const int i = t * Bc + b;
-            const int dot = block_dot_u(w, xt.lo[i], xt.hi[i]) - 8 * xt.sum[i];
-            acc[t] = fmaf(dw * xt.s[i], (float)dot, acc[t]);
+            const int2 sc = xt.sc[i];
+            const int dot = block_dot_u(w, xt.lo[i], xt.hi[i]) - 8 * sc.y;
+            acc[t] = fmaf(dw * __int_as_float(sc.x), (float)dot, acc[t]);
         }
     }
 }

@@ -32,12 +32,19 @@ namespace qmm {
 
 enum YMode { Y_PLAIN = 0, Y_SWIGLU_PAIRS = 1 };
 
-constexpr int SW = 16;  // consumer warps (two rows each)
+// Tiling constants (overridable at build time for tuning sweeps).
+#ifndef QMM_STREAM_WARPS
+#define QMM_STREAM_WARPS 8
+#endif
+#ifndef QMM_STREAM_CHUNK_KB
+#define QMM_STREAM_CHUNK_KB 64
+#endif
+constexpr int SW = QMM_STREAM_WARPS;  // consumer warps (four rows each)
 constexpr int STREAM_THREADS = (SW + 1) * 32;
 constexpr int STREAM_HDR = 256;  // barriers + flags
 constexpr int STREAM_MAX_STAGES = 8;
-constexpr int GROUP_ROWS = 32;   // rows per group (2 per consumer warp)
-constexpr int CHUNK_KB = 64;     // K blocks per unit (2 per lane)
+constexpr int GROUP_ROWS = 4 * SW;              // rows per group (4 per consumer warp)
+constexpr int CHUNK_KB = QMM_STREAM_CHUNK_KB;   // K blocks per unit (CHUNK_KB / 32 per lane)
 constexpr int STAGE_Q = GROUP_ROWS * CHUNK_KB * 16;  // 32 KB
 constexpr int STAGE_D = GROUP_ROWS * CHUNK_KB * 2;   //  4 KB
 constexpr int STAGE_BYTES = STAGE_Q + STAGE_D;
@@ -68,6 +75,52 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         "[%4];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+// A warp's four weight rows of one K block, read out of a ring stage into
+// registers (so the stage can be handed back to the producer before the
+// arithmetic): q points at this lane's block of the warp's first row, rows
+// are qrs bytes apart; dd likewise, drs elements apart.
+struct Quad4 {
+    uint4 w[4];
+    float d[4];
+};
+
+__device__ __forceinline__ Quad4 quad_load(const uint8_t* q, int qrs, const uint16_t* dd, int drs) {
+    Quad4 r;
+    r.w[0] = lds128(q);
+    r.w[1] = lds128(q + qrs);
+    r.w[2] = lds128(q + 16 * qrs);
+    r.w[3] = lds128(q + 17 * qrs);
+    r.d[0] = f16_bits_to_f32(dd[0]);
+    r.d[1] = f16_bits_to_f32(dd[drs]);
+    r.d[2] = f16_bits_to_f32(dd[16 * drs]);
+    r.d[3] = f16_bits_to_f32(dd[17 * drs]);
+    return r;
+}
+
+// The four rows against MT staged activations: each activation block (two
+// 16-byte halves and its scale/code-sum pair) is read once for all four
+// rows.  acc[t][0] holds rows (r0, r1), acc[t][1] rows (r2, r3).  The block
+// dot is taken as 16 * dot (block_dot16) and the scale as d_w * d_x / 16:
+// the same fp32 product and sum as d_w * d_x * dot.
+template <int MT>
+__device__ __forceinline__ void quad_compute(const Quad4& q, const XTile& xt, int B, int ib, float2 (&acc)[MT][2],
+                                             int mt = MT) {
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+        if (t >= mt) break;  // warp-uniform: tokens past mt are absent
+        const int i = t * B + ib;
+        const int4 xl = xt.lo[i], xh = xt.hi[i];
+        const int2 sc = xt.sc[i];
+        const float xs16 = __int_as_float(sc.x) * 0.0625f;
+        const int c = -128 * sc.y;
+        const float2 xs2 = make_float2(xs16, xs16);
+        const int D0 = block_dot16(q.w[0], xl, xh, c), D1 = block_dot16(q.w[1], xl, xh, c);
+        const int D2 = block_dot16(q.w[2], xl, xh, c), D3 = block_dot16(q.w[3], xl, xh, c);
+        acc[t][0] = ffma2_scaled(make_float2(q.d[0], q.d[1]), xs2, make_float2((float)D0, (float)D1), acc[t][0]);
+        acc[t][1] = ffma2_scaled(make_float2(q.d[2], q.d[3]), xs2, make_float2((float)D2, (float)D3), acc[t][1]);
+    }
 }
 
 // Up to two CTAs per SM for the batch-1 variants (<= 60 registers), so a
@@ -150,16 +203,17 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
     else stage_f32<XMODE == X_SWIGLU>(xt, a.xf, a.K, a.xq_out, a.xd_out, tid, NTHR);
     asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
 
-    // this warp's rows inside a group
-    const int lr0 = 2 * warp, lr1 = 2 * warp + 1;
+    // this warp's rows inside a group: pairs (2w, 2w+1) and (2w+16, 2w+17),
+    // so a gate/up pair always sits in one warp
+    const int rA = 2 * warp, rB = 2 * warp + 16;
     constexpr int OPR = YMODE == Y_SWIGLU_PAIRS ? 2 : 1;  // rows per output
     bool failed = false;
     for (int g = 0; g < ngroups; ++g) {
         const int64_t r0 = row_begin + (int64_t)g * RB;
         const int nr = (int)min((int64_t)RB, row_end - r0);
-        float acc0[MT], acc1[MT];
+        float2 acc[MT][2];
 #pragma unroll
-        for (int t = 0; t < MT; ++t) acc0[t] = acc1[t] = 0.f;
+        for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = make_float2(0.f, 0.f);
         for (int kc = 0; kc < nkc; ++kc) {
             const int u = g * nkc + kc, s = u % S;
             // On a timeout keep going without computing: every later wait returns
@@ -171,61 +225,61 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
                 failed = true;
             }
             const int b0 = kc * CKB, nb = min(CKB, B - b0);
-            if (ok && lr0 < nr) {
-                const uint8_t* stq = ring + (size_t)s * STAGE_BYTES;
-                const uint16_t* std_ = reinterpret_cast<const uint16_t*>(stq + STAGE_Q);
-                const bool has1 = lr1 < nr;
+            // rows past nr hold stale or zero-filled bytes: computed, never written
+            constexpr int H = CHUNK_KB / 32;
+            Quad4 qd[H];
+            const bool work = ok && rA < nr;
+            if (work) {
+                const uint8_t* stq = ring + (size_t)s * STAGE_BYTES + (rA * CKB + lane) * 16;
+                const uint16_t* std_ = reinterpret_cast<const uint16_t*>(ring + (size_t)s * STAGE_BYTES + STAGE_Q) +
+                                       rA * CKB + lane;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int bl = lane + 32 * h;  // block inside the chunk
-                    if (bl >= nb) break;
-                    const uint4 w0 = lds128(stq + (lr0 * CKB + bl) * 16);
-                    const uint4 w1 = has1 ? lds128(stq + (lr1 * CKB + bl) * 16) : make_uint4(0, 0, 0, 0);
-                    const float d0 = f16_bits_to_f32(std_[lr0 * CKB + bl]);
-                    const float d1 = has1 ? f16_bits_to_f32(std_[lr1 * CKB + bl]) : 0.f;
-#pragma unroll
-                    for (int t = 0; t < MT; ++t) {
-                        const int i = t * B + b0 + bl;
-                        const int4 xl = xt.lo[i], xh = xt.hi[i];
-                        const float xs = xt.s[i];
-                        const int xc = 8 * xt.sum[i];
-                        const int p0 = block_dot_u(w0, xl, xh) - xc;
-                        const int p1 = block_dot_u(w1, xl, xh) - xc;
-                        acc0[t] = fmaf(d0 * xs, (float)p0, acc0[t]);
-                        acc1[t] = fmaf(d1 * xs, (float)p1, acc1[t]);
-                    }
-                }
+                for (int h = 0; h < H; ++h)
+                    if (lane + 32 * h < nb) qd[h] = quad_load(stq + 512 * h, CKB * 16, std_ + 32 * h, CKB);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (lane == 0) mbar_arrive(&empty[s]);  // stage read: the producer may refill it
+            if (work) {
+#pragma unroll
+                for (int h = 0; h < H; ++h)
+                    if (lane + 32 * h < nb) quad_compute<MT>(qd[h], xt, B, b0 + lane + 32 * h, acc);
+            }
         }
-        // reduce the warp's two rows across lanes, write
+        // reduce the warp's four rows across lanes, write
+        float v[MT][4];
 #pragma unroll
         for (int t = 0; t < MT; ++t) {
-            acc0[t] = warp_sum(acc0[t]);
-            acc1[t] = warp_sum(acc1[t]);
+            v[t][0] = warp_sum(acc[t][0].x);
+            v[t][1] = warp_sum(acc[t][0].y);
+            v[t][2] = warp_sum(acc[t][1].x);
+            v[t][3] = warp_sum(acc[t][1].y);
         }
-        if (lane == 0 && !failed && lr0 < nr) {
-            const bool has1 = lr1 < nr;
+        if (lane == 0 && !failed) {
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 if (xrow[t] < 0) continue;
-                if (YMODE == Y_SWIGLU_PAIRS) {
-                    const float v = swiglu1(acc0[t], acc1[t]);
-                    const int64_t o = (r0 + lr0) / 2;
-                    if (a.y) a.y[xrow[t] * a.ldy + o] = v;
-                    if (QOUT) ybuf[o - row_begin / 2] = v;
-                } else {
-                    const int64_t row = r0 + lr0;
-                    const float v0 = acc0[t] + (a.residual ? a.residual[row] : 0.f);
-                    const float v1 = has1 ? acc1[t] + (a.residual ? a.residual[row + 1] : 0.f) : 0.f;
-                    if (a.y) {
-                        a.y[xrow[t] * a.ldy + row] = v0;
-                        if (has1) a.y[xrow[t] * a.ldy + row + 1] = v1;
-                    }
-                    if (QOUT) {
-                        ybuf[row - row_begin] = v0;
-                        if (has1) ybuf[row + 1 - row_begin] = v1;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const int lr = p ? rB : rA;
+                    if (lr >= nr) continue;
+                    const int64_t row = r0 + lr;
+                    if (YMODE == Y_SWIGLU_PAIRS) {
+                        const float h = swiglu1(v[t][2 * p], v[t][2 * p + 1]);
+                        const int64_t o = row / 2;
+                        if (a.y) a.y[xrow[t] * a.ldy + o] = h;
+                        if (QOUT) ybuf[o - row_begin / 2] = h;
+                    } else {
+                        const bool has1 = lr + 1 < nr;
+                        const float o0 = v[t][2 * p] + (a.residual ? a.residual[row] : 0.f);
+                        const float o1 = has1 ? v[t][2 * p + 1] + (a.residual ? a.residual[row + 1] : 0.f) : 0.f;
+                        if (a.y) {
+                            a.y[xrow[t] * a.ldy + row] = o0;
+                            if (has1) a.y[xrow[t] * a.ldy + row + 1] = o1;
+                        }
+                        if (QOUT) {
+                            ybuf[row - row_begin] = o0;
+                            if (has1) ybuf[row + 1 - row_begin] = o1;
+                        }
                     }
                 }
             }
@@ -249,6 +303,204 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
                                    ((r.c[3] & 0xff) << 24);
                 *reinterpret_cast<int*>(a.yq + (out0 + blk * QK) + part * 4) = packed;
                 if (part == 0) a.yd[out0 / QK + blk] = f32_to_f16_bits(r.d32);
+            }
+        }
+    }
+}
+
+// ============================================================================
+// MoE expert-grouped GEMV on the same streaming scheme.  The rows of all
+// active experts (in the order of the device-built active list) form one row
+// space; CTA c takes the slice [c*R/G, (c+1)*R/G) of it, so a CTA meets only
+// a few expert boundaries and restages the routed activations only there.
+// Weights of all E experts are one 2D tensor [E*N rows][K/2 bytes].  A row
+// group is applied to MT of the expert's slots per pass; an expert with more
+// routed slots is streamed once per MT slots.
+// ============================================================================
+struct MoeStreamArgs {
+    int64_t N, K;
+    int E, k;
+    const int8_t* xq;
+    const uint16_t* xd;
+    int x_per_slot;
+    float* y;  // [T*k][N]
+    MoeWs ws;
+    int rb, ckb, nstages, xtile_bytes;
+    int* err;
+};
+
+// The unit sequence of one CTA, walked identically by producer and consumers.
+struct MoeCursor {
+    int64_t gr, gr1;  // position in the row space, end of this CTA's slice
+    int64_t N;
+    int rb;
+    // current group
+    int e, nr, nsb, sbeg, send;
+    int64_t r;
+    // active: expert of each active index; span: (first slot, end slot) of
+    // each active index -- shared-memory copies of the grouping
+    __device__ bool next_group(const int* active, const int2* span) {
+        if (gr >= gr1) return false;
+        const int ai = (int)(gr / N);
+        r = gr - (int64_t)ai * N;
+        nr = (int)min((int64_t)rb, min(N - r, gr1 - gr));
+        e = active[ai];
+        sbeg = span[ai].x;
+        send = span[ai].y;
+        gr += nr;
+        return true;
+    }
+};
+
+template <int MT>
+__global__ void __launch_bounds__(STREAM_THREADS, 2)
+    moe_stream_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_d,
+                      MoeStreamArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + STREAM_MAX_STAGES;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STREAM_MAX_STAGES);
+    const int B = (int)(a.K / QK);
+    const XTile xt = xtile_at(smem + STREAM_HDR, MT, B);
+    uint8_t* ring = smem + STREAM_HDR + a.xtile_bytes;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int S = a.nstages, CKB = a.ckb;
+    const int nkc = (B + CKB - 1) / CKB;
+    const uint32_t unit_bytes = (uint32_t)(a.rb * CKB * 18);
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], SW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the grouping written by the kernel before
+
+    // the active-expert list and each one's slot span, read once into shared
+    // memory (the walk below consults them for every row group)
+    const int n_active = *a.ws.n_active;
+    int* s_active = reinterpret_cast<int*>(ring + (size_t)S * STAGE_BYTES);
+    int2* s_span = reinterpret_cast<int2*>(s_active + a.E);
+    for (int i = tid; i < n_active; i += blockDim.x) {
+        const int e = a.ws.active[i];
+        s_active[i] = e;
+        s_span[i] = make_int2(a.ws.offsets[e], a.ws.offsets[e + 1]);
+    }
+    __syncthreads();
+    const int64_t total = (int64_t)n_active * a.N;
+    MoeCursor cur;
+    cur.gr = total * blockIdx.x / gridDim.x;
+    cur.gr1 = total * (blockIdx.x + 1) / gridDim.x;
+    cur.N = a.N;
+    cur.rb = a.rb;
+
+    if (warp == SW) {
+        if (lane == 0) {
+            int u = 0, issued = 0;
+            bool ok = true;
+            while (ok && cur.next_group(s_active, s_span)) {
+                const int nsb = (cur.send - cur.sbeg + MT - 1) / MT;
+                const int row = (int)((int64_t)cur.e * a.N + cur.r);
+                for (int sb = 0; sb < nsb && ok; ++sb)
+                    for (int kc = 0; kc < nkc; ++kc, ++u) {
+                        const int s = u % S;
+                        if (u >= S && !mbar_wait(&empty[s], ((u / S) - 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        uint8_t* st = ring + (size_t)s * STAGE_BYTES;
+                        mbar_arrive_expect_tx(&full[s], unit_bytes);
+                        tma_load_2d(st, &map_q, kc * CKB * 4, row, &full[s]);
+                        tma_load_2d(st + STAGE_Q, &map_d, kc * CKB, row, &full[s]);
+                        issued = u + 1;
+                    }
+            }
+            if (!ok) {
+                atomicOr(a.err, ERR_TIMEOUT);
+                *abort_flag = 1;
+                for (int v = max(0, issued - S); v < issued; ++v) {
+                    const uint64_t t0 = global_ns();
+                    while (!mbar_try_wait(&full[v % S], (v / S) & 1) && global_ns() - t0 < WAIT_LIMIT_NS) {
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    constexpr int NTHR = SW * 32;
+    const int rA = 2 * warp, rB = 2 * warp + 16;
+    int u = 0;
+    bool failed = false;
+    while (cur.next_group(s_active, s_span)) {
+        const int nslots = cur.send - cur.sbeg;
+        const int nsb = (nslots + MT - 1) / MT;
+        for (int sb = 0; sb < nsb; ++sb) {
+            const int mt = min(MT, nslots - sb * MT);  // slots in this pass
+            int slot[MT];
+            int64_t xrow[MT];
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                const int j = sb * MT + t;
+                slot[t] = j < nslots ? a.ws.slots[cur.sbeg + j] : -1;
+                xrow[t] = slot[t] < 0 ? -1 : (a.x_per_slot ? slot[t] : slot[t] / a.k);
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");  // everyone is done with the old tile
+            stage_q8<MT>(xt, B, a.xq, a.xd, a.K, xrow, 0, B, tid, NTHR);
+            asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
+            float2 acc[MT][2];
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = make_float2(0.f, 0.f);
+            for (int kc = 0; kc < nkc; ++kc, ++u) {
+                const int s = u % S;
+                const bool ok = !failed && mbar_wait(&full[s], (u / S) & 1, abort_flag);
+                if (!ok && !failed) {
+                    if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+                    *abort_flag = 1;
+                    failed = true;
+                }
+                const int b0 = kc * CKB, nb = min(CKB, B - b0);
+                constexpr int H = CHUNK_KB / 32;
+                Quad4 qd[H];
+                const bool work = ok && rA < cur.nr;
+                if (work) {
+                    const uint8_t* stq = ring + (size_t)s * STAGE_BYTES + (rA * CKB + lane) * 16;
+                    const uint16_t* std_ =
+                        reinterpret_cast<const uint16_t*>(ring + (size_t)s * STAGE_BYTES + STAGE_Q) + rA * CKB + lane;
+#pragma unroll
+                    for (int h = 0; h < H; ++h)
+                        if (lane + 32 * h < nb) qd[h] = quad_load(stq + 512 * h, CKB * 16, std_ + 32 * h, CKB);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                if (work) {
+#pragma unroll
+                    for (int h = 0; h < H; ++h)
+                        if (lane + 32 * h < nb) quad_compute<MT>(qd[h], xt, B, b0 + lane + 32 * h, acc, mt);
+                }
+            }
+            float v[MT][4];
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+                v[t][0] = warp_sum(acc[t][0].x);
+                v[t][1] = warp_sum(acc[t][0].y);
+                v[t][2] = warp_sum(acc[t][1].x);
+                v[t][3] = warp_sum(acc[t][1].y);
+            }
+            if (lane == 0 && !failed) {
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    if (slot[t] < 0) continue;
+                    float* yr = a.y + (int64_t)slot[t] * a.N + cur.r;
+                    const int lrs[4] = {rA, rA + 1, rB, rB + 1};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (lrs[q] < cur.nr) yr[lrs[q]] = v[t][q];
+                }
             }
         }
     }
