@@ -45,6 +45,8 @@ constexpr int NCONV = 4, NEPI = 4;
 
 // converted K blocks in flight: as many as shared memory allows
 __host__ __device__ constexpr int conv_bufs(int ntok) { return ntok <= 16 ? 16 : ntok <= 32 ? 12 : 8; }
+// K blocks converted per handshake with the MMA warp (divides KB_STAGE and conv_bufs)
+__host__ __device__ constexpr int conv_group(int ntok) { return ntok <= 16 ? 8 : 4; }
 
 struct Layout {
     // byte offsets in dynamic shared memory (base aligned to 1024)
@@ -262,22 +264,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                                    ((uint32_t)(ROWS >> 4) << 24);
             bool ok = true;
             int done = 0;
-            for (int j = 0; j < nkb; ++j) {
-                const int cb = j % CB, sl = j % SL;
-                if (!mbar_wait(&br.conv_full[cb], (j / CB) & 1, br.abort)) { ok = false; break; }
-                if (j >= SL && !mbar_wait(&br.tm_empty[sl], ((j / SL) - 1) & 1, br.abort)) { ok = false; break; }
-                tc_fence_after();
-                const uint8_t* cbuf = smem + L.conv + cb * L.conv_stride;
-                const uint32_t d = tmem + (uint32_t)(sl * NTOK);
-                const uint32_t lbo_a = ROWS * 16, lbo_b = NTOK * 16;
-                umma_f16(d, umma_desc(cbuf + L.conv_a, lbo_a, 128), umma_desc(cbuf + L.conv_b, lbo_b, 128), idesc, 0);
-                umma_f16(d, umma_desc(cbuf + L.conv_a + 2 * ROWS * 16, lbo_a, 128),
-                         umma_desc(cbuf + L.conv_b + 2 * NTOK * 16, lbo_b, 128), idesc, 1);
-                umma_f16(d, umma_desc(smem + L.aextra, lbo_a, 128),
-                         umma_desc(cbuf + L.conv_b + 4 * NTOK * 16, lbo_b, 128), idesc, 1);
-                umma_commit(&br.conv_empty[cb]);
-                umma_commit(&br.tm_full[sl]);
-                done = j + 1;
+            constexpr int CG = conv_group(NTOK), NSLOT = CB / CG;
+            for (int g = 0; g * CG < nkb && ok; ++g) {
+                if (!mbar_wait(&br.conv_full[g % NSLOT], (g / NSLOT) & 1, br.abort)) { ok = false; break; }
+                for (int jj = 0; jj < CG; ++jj) {
+                    const int j = g * CG + jj, cb = j % CB, sl = j % SL;
+                    if (j >= SL && !mbar_wait(&br.tm_empty[sl], ((j / SL) - 1) & 1, br.abort)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint8_t* cbuf = smem + L.conv + cb * L.conv_stride;
+                    const uint32_t d = tmem + (uint32_t)(sl * NTOK);
+                    const uint32_t lbo_a = ROWS * 16, lbo_b = NTOK * 16;
+                    umma_f16(d, umma_desc(cbuf + L.conv_a, lbo_a, 128), umma_desc(cbuf + L.conv_b, lbo_b, 128), idesc,
+                             0);
+                    umma_f16(d, umma_desc(cbuf + L.conv_a + 2 * ROWS * 16, lbo_a, 128),
+                             umma_desc(cbuf + L.conv_b + 2 * NTOK * 16, lbo_b, 128), idesc, 1);
+                    umma_f16(d, umma_desc(smem + L.aextra, lbo_a, 128),
+                             umma_desc(cbuf + L.conv_b + 4 * NTOK * 16, lbo_b, 128), idesc, 1);
+                    umma_commit(&br.tm_full[sl]);
+                    done = j + 1;
+                }
+                if (ok) umma_commit(&br.conv_empty[g % NSLOT]);  // the group's buffers may be refilled
             }
             if (!ok) {
                 atomicOr(a.err, ERR_TIMEOUT);
@@ -291,77 +297,85 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else if (warp < WARP_EPI0) {
-        // ---------------- converters: thread r (0..127) owns weight row r
+        // ---------------- converters: thread r (0..127) owns weight row r;
+        // CG K blocks per handshake (one wait, one proxy fence, one arrive)
         const int r = tid - WARP_CONV0 * 32;
-        for (int j = 0; j < nkb; ++j) {
-            const int s = j / KB_STAGE, bi = j % KB_STAGE;
-            const int rs = s % RAW_STAGES, cb = j % CB, sl = j % SL;
+        constexpr int CG = conv_group(NTOK), NSLOT = CB / CG;
+        for (int g = 0; g * CG < nkb; ++g) {
+            const int j0 = g * CG;
+            const int s = j0 / KB_STAGE, rs = s % RAW_STAGES;
             // every lane waits (acquire), then the warp agrees, so the warp-wide
             // shuffles below are never reached by only part of it
             bool ok = true;
-            if (bi == 0) ok = mbar_wait(&br.raw_full[rs], (s / RAW_STAGES) & 1, br.abort);
-            if (ok && j >= CB) ok = mbar_wait(&br.conv_empty[cb], ((j / CB) - 1) & 1, br.abort);
-            if (ok && j >= SL) ok = mbar_wait(&br.tm_empty[sl], ((j / SL) - 1) & 1, br.abort);
+            if (j0 % KB_STAGE == 0) ok = mbar_wait(&br.raw_full[rs], (s / RAW_STAGES) & 1, br.abort);
+            if (ok && g >= NSLOT) ok = mbar_wait(&br.conv_empty[g % NSLOT], ((g / NSLOT) - 1) & 1, br.abort);
+            // scale slots of this group are free once the epilogue released the last of them
+            const int jl = j0 + CG - 1;
+            if (ok && jl >= SL) ok = mbar_wait(&br.tm_empty[jl % SL], ((jl / SL) - 1) & 1, br.abort);
             if (!__all_sync(0xffffffffu, ok)) {
                 *br.abort = 1;
                 break;
             }
             const uint8_t* st = smem + L.raw + rs * L.raw_stage;
-            uint8_t* cbuf = smem + L.conv + cb * L.conv_stride;
-            float* sc = reinterpret_cast<float*>(smem + L.scal + sl * L.scal_stride);
-            // A: 16 nibble bytes of (row r, block bi), 128B-swizzled tile
-            const uint4 w = lds128(st + L.a_nib + r * 128 + ((bi ^ (r & 7)) << 4));
-            const uint32_t C = 0x43u, LO = 0x0F0F0F0Fu;
-            const uint32_t lo0 = w.x & LO, lo1 = w.y & LO, lo2 = w.z & LO, lo3 = w.w & LO;
-            const uint32_t hi0 = (w.x >> 4) & LO, hi1 = (w.y >> 4) & LO, hi2 = (w.z >> 4) & LO,
-                           hi3 = (w.w >> 4) & LO;
-            uint8_t* ca = cbuf + L.conv_a + r * 16;
-            *reinterpret_cast<uint4*>(ca + 0 * ROWS * 16) =
-                make_uint4(__byte_perm(lo0, C, 0x4140), __byte_perm(lo0, C, 0x4342), __byte_perm(lo1, C, 0x4140),
-                           __byte_perm(lo1, C, 0x4342));
-            *reinterpret_cast<uint4*>(ca + 1 * ROWS * 16) =
-                make_uint4(__byte_perm(lo2, C, 0x4140), __byte_perm(lo2, C, 0x4342), __byte_perm(lo3, C, 0x4140),
-                           __byte_perm(lo3, C, 0x4342));
-            *reinterpret_cast<uint4*>(ca + 2 * ROWS * 16) =
-                make_uint4(__byte_perm(hi0, C, 0x4140), __byte_perm(hi0, C, 0x4342), __byte_perm(hi1, C, 0x4140),
-                           __byte_perm(hi1, C, 0x4342));
-            *reinterpret_cast<uint4*>(ca + 3 * ROWS * 16) =
-                make_uint4(__byte_perm(hi2, C, 0x4140), __byte_perm(hi2, C, 0x4342), __byte_perm(hi3, C, 0x4140),
-                           __byte_perm(hi3, C, 0x4342));
             const uint16_t* wd = reinterpret_cast<const uint16_t*>(st + L.a_d);
-            sc[r] = f16_bits_to_f32(wd[r * KB_STAGE + bi]);
-            // B: 4 threads per token, 8 activations each
-            for (int t = r; t < 4 * NTOK; t += NCONV * 32) {
-                const int tok = t >> 2, c = t & 3;
-                const uint2 q8 = *reinterpret_cast<const uint2*>(st + L.x_q + tok * 256 + bi * 32 + c * 8);
-                int v[8];
+            const uint16_t* xdp = reinterpret_cast<const uint16_t*>(st + L.x_d);
+#pragma unroll 2
+            for (int jj = 0; jj < CG; ++jj) {
+                const int j = j0 + jj, bi = j % KB_STAGE, cb = j % CB, sl = j % SL;
+                uint8_t* cbuf = smem + L.conv + cb * L.conv_stride;
+                float* sc = reinterpret_cast<float*>(smem + L.scal + sl * L.scal_stride);
+                // A: 16 nibble bytes of (row r, block bi), 128B-swizzled tile
+                const uint4 w = lds128(st + L.a_nib + r * 128 + ((bi ^ (r & 7)) << 4));
+                const uint32_t C = 0x43u, LO = 0x0F0F0F0Fu;
+                const uint32_t lo0 = w.x & LO, lo1 = w.y & LO, lo2 = w.z & LO, lo3 = w.w & LO;
+                const uint32_t hi0 = (w.x >> 4) & LO, hi1 = (w.y >> 4) & LO, hi2 = (w.z >> 4) & LO,
+                               hi3 = (w.w >> 4) & LO;
+                uint8_t* ca = cbuf + L.conv_a + r * 16;
+                *reinterpret_cast<uint4*>(ca + 0 * ROWS * 16) =
+                    make_uint4(__byte_perm(lo0, C, 0x4140), __byte_perm(lo0, C, 0x4342), __byte_perm(lo1, C, 0x4140),
+                               __byte_perm(lo1, C, 0x4342));
+                *reinterpret_cast<uint4*>(ca + 1 * ROWS * 16) =
+                    make_uint4(__byte_perm(lo2, C, 0x4140), __byte_perm(lo2, C, 0x4342), __byte_perm(lo3, C, 0x4140),
+                               __byte_perm(lo3, C, 0x4342));
+                *reinterpret_cast<uint4*>(ca + 2 * ROWS * 16) =
+                    make_uint4(__byte_perm(hi0, C, 0x4140), __byte_perm(hi0, C, 0x4342), __byte_perm(hi1, C, 0x4140),
+                               __byte_perm(hi1, C, 0x4342));
+                *reinterpret_cast<uint4*>(ca + 3 * ROWS * 16) =
+                    make_uint4(__byte_perm(hi2, C, 0x4140), __byte_perm(hi2, C, 0x4342), __byte_perm(hi3, C, 0x4140),
+                               __byte_perm(hi3, C, 0x4342));
+                sc[r] = f16_bits_to_f32(wd[r * KB_STAGE + bi]);
+                // B: 4 threads per token, 8 activations each
+                for (int t = r; t < 4 * NTOK; t += NCONV * 32) {
+                    const int tok = t >> 2, c = t & 3;
+                    const uint2 q8 = *reinterpret_cast<const uint2*>(st + L.x_q + tok * 256 + bi * 32 + c * 8);
+                    int v[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    v[i] = (int)(int8_t)(q8.x >> (8 * i));
-                    v[4 + i] = (int)(int8_t)(q8.y >> (8 * i));
-                }
-                *reinterpret_cast<uint4*>(cbuf + L.conv_b + (c * NTOK + tok) * 16) =
-                    make_uint4(bf16x2_from_ints(v[0], v[1]), bf16x2_from_ints(v[2], v[3]),
-                               bf16x2_from_ints(v[4], v[5]), bf16x2_from_ints(v[6], v[7]));
-                int sum = v[0] + v[1] + v[2] + v[3] + v[4] + v[5] + v[6] + v[7];
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                if (c == 0) {
-                    // -sum = -64*hi - lo exactly, both bf16-exact; the A tile holds 136 twice
-                    const int hi = sum >> 6, lo = sum - 64 * hi;
-                    *reinterpret_cast<uint4*>(cbuf + L.conv_b + (4 * NTOK + tok) * 16) =
-                        make_uint4(bf16x2_from_ints(-64 * hi, -lo), 0u, 0u, 0u);
-                } else if (c == 1) {
-                    const uint16_t* xd = reinterpret_cast<const uint16_t*>(st + L.x_d);
-                    sc[ROWS + tok] = f16_bits_to_f32(xd[tok * KB_STAGE + bi]);
+                    for (int i = 0; i < 4; ++i) {
+                        v[i] = (int)(int8_t)(q8.x >> (8 * i));
+                        v[4 + i] = (int)(int8_t)(q8.y >> (8 * i));
+                    }
+                    *reinterpret_cast<uint4*>(cbuf + L.conv_b + (c * NTOK + tok) * 16) =
+                        make_uint4(bf16x2_from_ints(v[0], v[1]), bf16x2_from_ints(v[2], v[3]),
+                                   bf16x2_from_ints(v[4], v[5]), bf16x2_from_ints(v[6], v[7]));
+                    int sum = v[0] + v[1] + v[2] + v[3] + v[4] + v[5] + v[6] + v[7];
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                    if (c == 0) {
+                        // -sum = -64*hi - lo exactly, both bf16-exact; the A tile holds 136 twice
+                        const int hi = sum >> 6, lo = sum - 64 * hi;
+                        *reinterpret_cast<uint4*>(cbuf + L.conv_b + (4 * NTOK + tok) * 16) =
+                            make_uint4(bf16x2_from_ints(-64 * hi, -lo), 0u, 0u, 0u);
+                    } else if (c == 1) {
+                        sc[ROWS + tok] = f16_bits_to_f32(xdp[tok * KB_STAGE + bi]);
+                    }
                 }
             }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&br.conv_full[cb]);
-                mbar_arrive(&br.sc_full[sl]);
-                if (bi == KB_STAGE - 1) mbar_arrive(&br.raw_empty[rs]);
+                mbar_arrive(&br.conv_full[g % NSLOT]);
+                for (int jj = 0; jj < CG; ++jj) mbar_arrive(&br.sc_full[(j0 + jj) % SL]);
+                if ((j0 + CG) % KB_STAGE == 0) mbar_arrive(&br.raw_empty[rs]);
             }
         }
     } else {
