@@ -226,6 +226,8 @@ const char* qmm_status_string(int s) {
         case QMM_ERR_TIMEOUT: return "QMM_ERR_TIMEOUT: a bounded device-side wait gave up";
         case QMM_ERR_BAD_EXPERT_ID: return "QMM_ERR_BAD_EXPERT_ID: expert id outside [0, E) skipped";
         case QMM_ERR_WORKSPACE: return "QMM_ERR_WORKSPACE: workspace missing or too small";
+        case QMM_ERR_SCRATCH_LIMIT:
+            return "QMM_ERR_SCRATCH_LIMIT: needs more than the fixed scratch (QMM_MOE_STATIC_SCRATCH_BYTES)";
         default: return "QMM_ERR_UNKNOWN";
     }
 }

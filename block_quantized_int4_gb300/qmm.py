@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(_PKG, "libqmm.so")
 QK = 32
 
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_ARG", 2: "QMM_ERR_SHAPE", 3: "QMM_ERR_ALIGN", 4: "QMM_ERR_DEVICE",
-          5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT", 7: "QMM_ERR_BAD_EXPERT_ID", 8: "QMM_ERR_WORKSPACE"}
+          5: "QMM_ERR_CUDA", 6: "QMM_ERR_TIMEOUT", 7: "QMM_ERR_BAD_EXPERT_ID", 8: "QMM_ERR_WORKSPACE",
+          9: "QMM_ERR_SCRATCH_LIMIT"}
 
 
 class QmmError(RuntimeError):
@@ -52,6 +53,7 @@ SIGNATURES = {
     "qmm_debug_block_dots": [_P, _I64, _I64, _I64, _P, _P, _P],
     "qmm_moe_workspace_size": [_I32, _I32, _I32, ctypes.POINTER(_SZ)],
     "qmm_moe_gemv": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
+    "qmm_moe_gemv_static": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P],
     "qmm_moe_combine": [_P, _P, _I32, _I32, _I64, _P, _P],
     "qmm_last_device_error": [_P],
 }
@@ -153,6 +155,11 @@ def qmm_moe_workspace_size(E, T, k) -> int:
 def qmm_moe_gemv(w_qs, w_d, E, N, K, ids, T, k, xq, xd, x_per_slot, y, workspace, workspace_bytes, stream=None):
     _check(_lib.qmm_moe_gemv(_ptr(w_qs), _ptr(w_d), E, N, K, _ptr(ids), T, k, _ptr(xq), _ptr(xd), int(x_per_slot),
                              _ptr(y), _ptr(workspace), workspace_bytes, _stream(stream)), "qmm_moe_gemv")
+
+
+def qmm_moe_gemv_static(w_qs, w_d, E, N, K, ids, T, k, xq, xd, x_per_slot, y, stream=None):
+    _check(_lib.qmm_moe_gemv_static(_ptr(w_qs), _ptr(w_d), E, N, K, _ptr(ids), T, k, _ptr(xq), _ptr(xd),
+                                    int(x_per_slot), _ptr(y), _stream(stream)), "qmm_moe_gemv_static")
 
 
 def qmm_moe_combine(z, gates, T, k, N, y, stream=None):

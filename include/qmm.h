@@ -65,7 +65,8 @@ typedef enum qmm_status {
     QMM_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed     */
     QMM_ERR_TIMEOUT = 6,        /* a bounded device-side wait gave up       */
     QMM_ERR_BAD_EXPERT_ID = 7,  /* an expert id outside [0, E) was skipped  */
-    QMM_ERR_WORKSPACE = 8       /* workspace NULL or smaller than required  */
+    QMM_ERR_WORKSPACE = 8,      /* workspace NULL or smaller than required  */
+    QMM_ERR_SCRATCH_LIMIT = 9   /* larger than the library's fixed scratch  */
 } qmm_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -209,6 +210,47 @@ QMM_API qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_
  * order, deterministic).  z fp32 [T][k][N], gates fp32 [T][k], y [T][N]. */
 QMM_API qmm_status qmm_moe_combine(const float* z, const float* gates, int32_t T, int32_t k, int64_t N, float* y,
                            void* stream);
+
+/* ---------------------------------------------------------------------
+ * MoE expert GEMV without a caller workspace.  A library addition: the
+ * pages have no counterpart (they say nothing about device memory).
+ * ------------------------------------------------------------------- */
+
+/* Size of the fixed scratch that qmm_moe_gemv_static uses in place of a
+ * workspace: 256 KiB.  Enough whenever qmm_moe_workspace_size(E, T, k) is
+ * at most this, e.g. E = 256 experts with up to 64,510 routed slots T*k. */
+#define QMM_MOE_STATIC_SCRATCH_BYTES (256 * 1024)
+
+/* Same computation, arguments, layouts, results and error codes as
+ * qmm_moe_gemv, without the workspace arguments, and it allocates nothing:
+ * the routing tables go to a fixed array inside the library (a file-scope
+ * __device__ array of QMM_MOE_STATIC_SCRATCH_BYTES, 256-byte aligned, one
+ * per device).
+ *
+ * Meant for callers that cannot allocate device memory when they call: a
+ * serving loop that reserved all device memory at start-up, code that must
+ * not call an allocator in the step (cudaMalloc may synchronise the device
+ * and fails under memory pressure), or a plain C caller with no memory pool
+ * to carve a workspace from.
+ *
+ *  - Limit: if qmm_moe_workspace_size(E, T, k) exceeds
+ *    QMM_MOE_STATIC_SCRATCH_BYTES the call returns QMM_ERR_SCRATCH_LIMIT and
+ *    launches nothing; use qmm_moe_gemv with a workspace for such sizes.
+ *  - Nothing has to start at zero: every call rebuilds the tables from ids
+ *    before reading them, so what an earlier call left there is never used.
+ *  - Setup: the first call on a device (with that device current) looks up
+ *    the scratch's device address once (cudaGetSymbolAddress) and sets the
+ *    kernels' shared-memory attributes; later calls reuse both.  Make that
+ *    first call before beginning a stream capture on the device.
+ *  - Concurrency: every call on one device shares the one scratch.  Calls on
+ *    one stream run in order and are safe.  Calls that can run at the same
+ *    time on one device (streams with no ordering between them, e.g. from
+ *    several host threads) race on the scratch and may write wrong outputs:
+ *    order them on one stream or with events.
+ *  - T == 0 is a no-op and needs no device. */
+QMM_API qmm_status qmm_moe_gemv_static(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,
+                               const int32_t* ids, int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd,
+                               int x_per_slot, float* y, void* stream);
 
 /* ---------------------------------------------------------------------
  * Errors raised on the device

@@ -84,10 +84,25 @@ def test_workspace_rules(qmm):
     assert _call(qmm, "qmm_moe_gemv", A16, A16, 256, 64, 64, A16, 16, 8, A16, A16, 0, A16, None, n, None) == 8
 
 
+def test_static_scratch_limit_and_arguments(qmm):
+    """qmm_moe_gemv_static checks its fixed scratch limit (256 KiB) on the
+    host before touching a device."""
+    A16 = 0x10000
+    assert qmm.qmm_moe_workspace_size(256, 8064, 8) > 256 * 1024
+    assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 256, 64, 64, A16, 8064, 8, A16, A16, 0, A16, None) == 9
+    assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 0, 64, 64, A16, 1, 8, A16, A16, 0, A16, None) == 1
+    assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 0, 64, A16, 1, 8, A16, A16, 0, A16, None) == 1
+    assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 48, A16, 1, 2, A16, A16, 0, A16, None) == 2
+    assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, A16, 0, 2, A16, A16, 0, A16, None) == 0
+    assert _call(qmm, "qmm_moe_gemv_static", A16 + 2, A16, 8, 64, 64, A16, 1, 2, A16, A16, 0, A16, None) == 3
+    assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, None, 1, 2, A16, A16, 0, A16, None) == 1
+
+
 def test_valid_call_without_gpu_reports_device_error(qmm):
     import torch
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     A16 = 0x10000
     assert _call(qmm, "qmm_gemv_q4_0_q8_0", A16, A16, 64, 64, A16, A16, A16, None) == 4
+    assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, A16, 1, 2, A16, A16, 0, A16, None) == 4
     assert _call(qmm, "qmm_last_device_error", None) == 4
