@@ -300,6 +300,82 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
             "config": {"workload": c["name"], "T": T, "experts": E, "top_k": k, "hidden": H, "expert_ffn": F}}
 
 
+# ---------------------------------------------------------------------------- single-kernel cases
+def run_case(qmm, torch, name, calls, dev="cuda"):
+    """One kernel of the path on one workload shape, called `calls` times
+    with CUDA-event timing of each call (no flush: every case reads more than
+    L2 per call except decode_gateup, 13 MB, which is what one launch of the
+    decode step reads).  For profiler captures (`ncu -k ... -s 3 -c 1`)."""
+    M, flags = 1, 0
+    if name == "decode_gateup":  # gate/up of one TinyLLaMA layer: interleaved rows, SwiGLU pairs, Q8 in and out
+        c = workloads.TINYLLAMA
+        N, K, sigma = 2 * c["ffn"], c["hidden"], c["sigma"]
+    elif name == "lm_head_8192":
+        N, K, sigma = workloads.LARGE_DENSE["vocab"], workloads.LARGE_DENSE["hidden"], workloads.LARGE_DENSE["sigma"]
+    elif name in ("gemm_b16", "gemm_b64"):
+        N, K, sigma = workloads.LARGE_DENSE["ffn"], workloads.LARGE_DENSE["hidden"], workloads.LARGE_DENSE["sigma"]
+        M = 16 if name == "gemm_b16" else 64
+    elif name == "moe_T16":
+        return _moe_case(qmm, torch, calls, dev)
+    else:
+        raise SystemExit(f"unknown case {name}")
+    w = workloads.weights(N, K, sigma=sigma, seed=0, index=0, device=dev)
+    qs, d = qmm.quantize_q4_0(w)
+    del w
+    xq, xd = qmm.quantize_q8_0(workloads.activations(M, K, seed=0, device=dev))
+    y = torch.empty(M, N, device=dev)
+    if name == "decode_gateup":
+        yq = torch.empty(N // 2, dtype=torch.int8, device=dev)
+        yd = torch.empty(N // 64, dtype=torch.int16, device=dev)
+        op = lambda: qmm.qmm_gemv_fused(qs, d, N, K, None, xq, xd, None, None, yq, yd,  # noqa: E731
+                                        flags=qmm.CHAIN | qmm.Y_SWIGLU_PAIRS)
+    elif M == 1:
+        op = lambda: qmm.qmm_gemv_q4_0_q8_0(qs, d, N, K, xq, xd, y)  # noqa: E731
+    else:
+        op = lambda: qmm.qmm_gemm_q4_0_q8_0(qs, d, N, K, M, xq, xd, y, N)  # noqa: E731
+    ts = _time_calls(torch, op, calls)
+    wbytes = workloads.q4_0_bytes(N, K)
+    return {"case": name, "N": N, "K": K, "M": M, "us_per_call": [round(t * 1e6, 2) for t in ts],
+            "weight_GBps_best": round(wbytes / min(ts) / 1e9, 1), "TOPS_best": round(2 * M * N * K / min(ts) / 1e12, 2)}
+
+
+def _time_calls(torch, op, calls):
+    st = torch.cuda.current_stream()
+    ts = []
+    for _ in range(calls):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        op()
+        e1.record(st)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    return ts
+
+
+def _moe_case(qmm, torch, calls, dev):
+    """The gate-projection expert GEMV of the GLM-scale MoE layer at 16 tokens
+    (256 experts resident, top-8 of a seeded sigmoid router)."""
+    import numpy as np
+    c = workloads.MOE
+    H, F, E, k, T = c["hidden"], c["expert_ffn"], c["experts"], c["top_k"], 16
+    qs = torch.empty(E, F, H // 2, dtype=torch.uint8, device=dev)
+    d = torch.empty(E, F, H // 32, dtype=torch.int16, device=dev)
+    for e in range(E):
+        w = workloads.weights(F, H, sigma=c["sigma"], seed=0, index=e, device=dev)
+        qmm.qmm_quantize_q4_0(w, F, H, H, qs[e], d[e])
+    top = torch.topk(torch.sigmoid(workloads.router_logits(T, E, seed=0).double()), k, dim=1, sorted=True)
+    ids = top.indices.to(torch.int32).to(dev)
+    uniq = len(np.unique(top.indices.numpy()))
+    xq, xd = qmm.quantize_q8_0(workloads.activations(T, H, seed=0, device=dev))
+    y = torch.empty(T * k, F, device=dev)
+    wsb = qmm.qmm_moe_workspace_size(E, T, k)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ts = _time_calls(torch, lambda: qmm.qmm_moe_gemv(qs, d, E, F, H, ids, T, k, xq, xd, 0, y, ws, wsb), calls)
+    wbytes = uniq * workloads.q4_0_bytes(F, H)
+    return {"case": "moe_T16", "E": E, "N": F, "K": H, "T": T, "unique_experts": uniq,
+            "us_per_call": [round(t * 1e6, 2) for t in ts], "weight_GBps_best": round(wbytes / min(ts) / 1e9, 1)}
+
+
 # ---------------------------------------------------------------------------- CPU oracle baseline
 def oracle_decode_sample(torch, rows=256):
     """Oracle inputs for a row sample of every matrix of the decode step: the
@@ -352,10 +428,20 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=256, help="rows per matrix per reference-arm step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
+    ap.add_argument("--case", default=None,
+                    help="time one kernel instead: decode_gateup, lm_head_8192, gemm_b16, gemm_b64, moe_T16")
     args = ap.parse_args()
     ws, rank, local = _dist()
 
     import torch
+
+    if args.case:
+        torch.cuda.set_device(local)
+        from block_quantized_int4_gb300 import _build
+        _build.build()
+        from block_quantized_int4_gb300 import qmm
+        print(json.dumps(run_case(qmm, torch, args.case, max(args.steps, 1))), flush=True)
+        return
 
     if args.impl == "reference":
         return main_reference(args, torch, ws, rank)

@@ -271,14 +271,16 @@ def test_stream_and_fallback_paths_agree_on_odd_k():
     assert_close(y[None], ref, S, "odd K")
 
 
-@pytest.mark.parametrize("M", [16, 17, 32, 48, 64])
-def test_gemm_tensor_core_integer_grid_exact(M):
-    """Batches of 16..64 tokens take the tensor-core path; with d = 1 on both
-    sides every output is an exact integer, so any loss in the MMA's integer
-    sums (or a wrong operand layout) shows as an inequality."""
+@pytest.mark.parametrize("M,K", [(48, 2048), (49, 2048), (64, 2048), (32, 28672)])
+def test_gemm_tensor_core_integer_grid_exact(M, K):
+    """Shapes routed to the tensor-core kernel (at least 32 tiles of 128 rows,
+    here with a ragged last tile; 48..64 tokens, or 32 with K too long to stage
+    x for the streaming kernel).  With d = 1 on both sides every output is an
+    exact integer, so any loss in the MMA's integer sums (or a wrong operand
+    layout) shows as an inequality."""
     qmm = lib()
     rng = np.random.default_rng(M)
-    N, K = 300, 2048
+    N = 4100
     w = rng.integers(-7, 8, size=(N, K)).astype(np.float32)
     w[:, ::32] = 7
     w[:5, :64] = np.array([7, -7] * 32, dtype=np.float32)  # both signs, whole blocks
