@@ -12,6 +12,7 @@
 #include "qmm.h"
 #include "qmm_kernels.cuh"
 #include "qmm_stream.cuh"
+#include "qmm_mma.h"
 #include "qmm_tc.h"
 
 using namespace qmm;
@@ -398,15 +399,12 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
     a.y = y;
     a.ldy = ldy;
     cudaStream_t st = S(stream);
+    // Two or more tokens: the warp-MMA kernel (exact fp16 products, fp32
+    // block sums) streams the weights once per 64 tokens.
+    if (M >= 2 && gemm_mma_eligible(N, K, M, w_qs, w_d, xq, xd) && ldy >= N)
+        return gemm_mma_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->sms, di->smem_optin, di->err, st);
     const int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
     const bool streamable = stream_eligible(N, K, w_qs, w_d, mt);
-    // tcgen05 GEMM only where it measured faster than the dp4a kernels: from
-    // 48 tokens, or from 32 where the streaming kernel cannot stage x, and
-    // with at least 32 tiles of 128 rows to spread over the SMs (shapes
-    // 28672x8192, 8192x28672, 5632x2048, 2048x5632 at 16..64 tokens).
-    const bool tc = (M >= 48 || (M >= 32 && !streamable)) && N >= 32 * 128;
-    if (tc && gemm_tc_eligible(N, K, M, w_qs, w_d, xq, xd) && ldy >= N)
-        return gemm_tc_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->err, st);
     if (streamable) {
         StreamArgs s = {};
         s.N = N;

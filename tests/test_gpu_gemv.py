@@ -154,6 +154,24 @@ def test_gemm_small_batch(M):
     assert_close(y, ref, S, f"gemm M={M}")
 
 
+@pytest.mark.parametrize("K", [256, 768])
+@pytest.mark.parametrize("M", [2, 17, 40])
+def test_gemm_row_groups_and_ragged_edges(M, K):
+    """Enough rows that a CTA walks a full group of 128 rows and a remainder
+    group whose row tiles split K across warps; K ends inside a unit (some
+    8-block columns absent); the last token tile is ragged.  All rows
+    against the oracle."""
+    qmm = lib()
+    N = 20000
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=M + K)
+    qs, d = _to_device_planes(qmm, qw, dw)
+    xq, xd = _dev_q8(qx, dx)
+    y = qmm.gemm(qs, d, xq, xd)
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y, ref, S, f"gemm {N}x{K} M={M}")
+    assert qmm.qmm_last_device_error() == 0
+
+
 def test_gemm_ldy_and_chunked_k():
     """Output row stride > N, and K too long to stage for 8 tokens at once."""
     qmm = lib()
@@ -193,7 +211,9 @@ def _sampled_rows(N, n, seed):
 @pytest.mark.parametrize("name,N,K,M", [("tinyllama.qkv", 2560, 2048, 1), ("tinyllama.down", 2048, 5632, 1),
                                         ("tinyllama.lm_head", 32000, 2048, 1),
                                         ("dense.gate", 28672, 8192, 1), ("dense.down", 8192, 28672, 16),
-                                        ("dense.lm_head", 128256, 8192, 1)])
+                                        ("dense.lm_head", 128256, 8192, 1), ("dense.gate", 28672, 8192, 16),
+                                        ("dense.lm_head", 128256, 8192, 16), ("dense.up", 28672, 8192, 64),
+                                        ("batched.gate", 5632, 2048, 64)])
 def test_full_size_sampled_rows(name, N, K, M):
     """Full-size matrices on the GPU (weights drawn on the device), sampled
     rows recomputed by the oracle from the same fp32 rows."""
