@@ -13,7 +13,7 @@
 #include "qmm_kernels.cuh"
 #include "qmm_stream.cuh"
 #include "qmm_mma.h"
-#include "qmm_tc.h"
+#include "qmm_tmap.h"
 
 using namespace qmm;
 

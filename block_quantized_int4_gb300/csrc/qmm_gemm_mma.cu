@@ -19,16 +19,17 @@
 // registers.
 //
 // Work layout:
-//  - A CTA owns rows_per_cta consecutive weight rows (a multiple of 16),
-//    walked in groups of up to 128 rows = 8 row tiles of 16.  A group is
-//    streamed in units of UKB blocks by a producer warp: per row tile, one
-//    2D TMA copy of 16 rows x 8 blocks of nibbles (128-byte swizzled, which
-//    makes the fragment loads below bank-conflict free) per 8 blocks, and
-//    one of the 16 rows x UKB scales (swizzled over its own row pitch).
-//  - Eight consumer warps.  In a full group warp w owns row tile w for the
-//    whole K range.  In a CTA's last group of T < 8 tiles, warp w takes tile
-//    w % T and every P-th block of each unit (P = warps on that tile); their
-//    partial sums meet in shared memory at the end of the group.
+//  - A CTA owns rows_per_cta consecutive weight rows (a multiple of the
+//    group height R = 16, 32, 48 or 64), walked group by group; each group is
+//    streamed in units of UKB blocks by a producer warp: one 2D TMA copy of
+//    R rows x 8 blocks of nibbles per 8-block column (128-byte swizzled,
+//    which makes the fragment loads below bank-conflict free) and one of the
+//    R rows x UKB scales (swizzled over its own row pitch).
+//  - Eight consumer warps.  A warp takes all R / 16 row tiles of the group
+//    against up to two token tiles of 8, and 4 contiguous blocks of each
+//    unit; the KP warps sharing a token group add their partial sums in
+//    shared memory at the end of the group.  So each activation fragment read
+//    from shared memory serves up to four row tiles.
 //  - Activations: per unit, the consumer threads turn the unit's Q8_0 codes
 //    of up to 8 * NT tokens into fp16 B fragments in shared memory (double
 //    buffered), while the next unit's codes are already being loaded into
@@ -52,7 +53,7 @@
 
 #include "qmm_device.cuh"
 #include "qmm_mma.h"
-#include "qmm_tc.h"
+#include "qmm_tmap.h"
 
 namespace qmm {
 namespace mmak {
@@ -60,24 +61,17 @@ namespace mmak {
 constexpr int CW = 8;              // consumer warps
 constexpr int NCT = CW * 32;       // consumer threads
 constexpr int THREADS = NCT + 32;  // + one producer warp
-constexpr int GROUP_TILES = CW;    // row tiles of 16 per full group
-constexpr int GROUP_ROWS = 16 * GROUP_TILES;
 constexpr int MAX_STAGES = 8;
-constexpr int XPER = 2;            // activation items per consumer thread per unit (8 * NT * UKB <= 512)
-constexpr int SPER = 1;            // scale items per consumer thread per unit (4 * NT * UKB <= 256)
-
-// Blocks per unit for NT token tiles: the unit's fp16 fragments (NT * UKB *
-// 512 bytes) stay at 32 KB or less.
-__host__ __device__ constexpr int unit_blocks(int nt) { return nt >= 8 ? 8 : nt >= 4 ? 16 : 32; }
+constexpr int MAX_XITEMS = 512;    // (token, block) activation items per unit: 8 * NT * UKB
 
 struct Args {
     int64_t N, K, M, ldy;
     const int8_t* xq;
     const uint16_t* xd;
     float* y;
-    int rows_per_cta;  // a multiple of 16
+    int rows_per_cta;  // a multiple of the group height
     int nstages;
-    int stage_bytes;   // GROUP_ROWS * UKB * 18, rounded up to 1024
+    int stage_bytes;   // R * UKB * 18, rounded up to 1024
     int off_xbuf, off_xsc, off_red;  // from the 1024-aligned base; the ring starts at 1024
     int* err;
 };
@@ -90,7 +84,7 @@ __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, int x, 
         : "memory");
 }
 
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"r"(NCT) : "memory"); }
+__device__ __forceinline__ void consumers_sync(int n) { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
 
 __device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
     uint32_t r;
@@ -104,30 +98,44 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
     return r;
 }
 
-// fp16 bit patterns used below: 0x6400 = 1024 (unit spacing, so OR-ing a
-// small integer n into the mantissa gives 1024 + n exactly); 0xE408 = -1032,
-// 0xE480 = -1152, 0x2C00 = 1/16, 0xD480 = -72.
+// Operand encodings (fp16 bit patterns: 0x6400 = 1024 with unit spacing, so
+// OR-ing a small integer n into the mantissa gives 1024 + n exactly; 0xE480 =
+// -1152, 0x2C00 = 1/16, 0xD480 = -72).
 //
-// One word of a weight row (bytes 4t..4t+3 of a block, byte i = u_i | v_i << 4
-// with u = element 4t+i, v = element 16+4t+i, codes stored as q + 8) -> the
-// four fp16 pairs (q of elements (4t, 4t+2), (4t+1, 4t+3), and the same +16).
-// Low nibbles: (1024 + u) - 1032 = u - 8.  High nibbles stay in place:
-// (1024 + 16 v) / 16 - 72 = v - 8.  All exact.
+// Weights: one word of a weight row (bytes 4t..4t+3 of a block, byte i =
+// u_i | v_i << 4 with u = element 4t+i, v = element 16+4t+i, codes stored as
+// q + 8) -> four fp16 pairs, with no arithmetic beyond masking:
+//   o[0] = 1024 + u for elements (4t, 4t+2), o[1] the same for (4t+1, 4t+3),
+//   o[2] = 1024 + 16 v for elements (16+4t, 16+4t+2), o[3] for (16+4t+1, ..+3).
+// Activations: the low half block as x itself, the high half as x / 16 (exact:
+// (1152 + x) / 16 - 72).  Then the low-half MMA sums (1024 + u) x = (q + 1032) x
+// and the high-half MMA sums (1024 + 16 v) x / 16 = (q + 72) x, so seeding the
+// accumulator with c = -(1032 * sum x_lo + 72 * sum x_hi) leaves exactly
+// sum q * x.  Every product and partial sum is an integer below 2^23 in
+// magnitude, exact in fp32.
 __device__ __forceinline__ void nibbles_to_f16(uint32_t w, uint32_t (&o)[4]) {
     const uint32_t w8 = w >> 8;
-    o[0] = hadd2((w & 0x000F000Fu) ^ 0x64006400u, 0xE408E408u);
-    o[1] = hadd2((w8 & 0x000F000Fu) ^ 0x64006400u, 0xE408E408u);
-    o[2] = hfma2((w & 0x00F000F0u) ^ 0x64006400u, 0x2C002C00u, 0xD480D480u);
-    o[3] = hfma2((w8 & 0x00F000F0u) ^ 0x64006400u, 0x2C002C00u, 0xD480D480u);
+    o[0] = (w & 0x000F000Fu) ^ 0x64006400u;
+    o[1] = (w8 & 0x000F000Fu) ^ 0x64006400u;
+    o[2] = (w & 0x00F000F0u) ^ 0x64006400u;
+    o[3] = (w8 & 0x00F000F0u) ^ 0x64006400u;
 }
 
-// One word of activation codes (four int8 x0..x3) -> B fragment registers
-// (x0, x2) and (x1, x3) as fp16 pairs: (1024 + (x + 128)) - 1152 = x, exact
-// (x ^ 0x80 = x + 128 for a two's-complement byte).
-__device__ __forceinline__ uint2 codes_to_f16(uint32_t x) {
+// One word of activation codes (four int8 x0..x3) -> the B fragment pair
+// (x0, x2), (x1, x3) as fp16: (1024 + (x + 128)) - 1152 = x (x ^ 0x80 = x + 128
+// for a two's-complement byte).
+__device__ __forceinline__ uint2 codes_lo_f16(uint32_t x) {
     uint2 r;
     r.x = hadd2((x & 0x00FF00FFu) ^ 0x64806480u, 0xE480E480u);
     r.y = hadd2(((x >> 8) & 0x00FF00FFu) ^ 0x64806480u, 0xE480E480u);
+    return r;
+}
+
+// The same pairs divided by 16: (1152 + x) / 16 - 72 = x / 16, exact.
+__device__ __forceinline__ uint2 codes_hi_f16(uint32_t x) {
+    uint2 r;
+    r.x = hfma2((x & 0x00FF00FFu) ^ 0x64806480u, 0x2C002C00u, 0xD480D480u);
+    r.y = hfma2(((x >> 8) & 0x00FF00FFu) ^ 0x64806480u, 0x2C002C00u, 0xD480D480u);
     return r;
 }
 
@@ -140,12 +148,30 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
           "f"(c[3]));
 }
 
-template <int NT>
+// Shape of one kernel instance: NT token tiles of 8 (up to 8 * NT tokens per
+// weight pass); TW row tiles of 16 per warp = the group height R / 16.
+template <int NT, int TW>
+struct Shape {
+    static constexpr int NTW = NT < 2 ? NT : 2;          // token tiles per warp
+    static constexpr int TGN = NT / NTW;                 // token groups
+    static constexpr int KP = CW / TGN;                  // warps splitting the blocks of a unit
+    static constexpr int R = 16 * TW;                    // rows per group
+    static constexpr int UKB = 64 / NT < 32 ? 64 / NT : 32;  // blocks per unit: 32, 32, 16, 8
+    static constexpr int KB_PART = UKB / KP;             // contiguous blocks per warp per unit (4)
+    static constexpr int QBYTES = UKB / 8 * R * 128;     // nibble tiles of a stage
+    static constexpr int STAGE = (QBYTES + R * UKB * 2 + 1023) / 1024 * 1024;
+    static constexpr int XBUF = UKB * NT * 512;          // B fragments of one unit
+    static constexpr int XSC = UKB * NT * 4 * 32;        // seeds and scales of one unit
+    static constexpr int RED = (CW - TGN) * TW * NTW * 512;  // partial-sum slots
+    static_assert(KP * TGN == CW && KB_PART == 4, "warp split");
+};
+
+template <int NT, int TW>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_mma_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_d, Args a) {
-    constexpr int UKB = unit_blocks(NT);
-    constexpr int QBYTES = UKB / 8 * GROUP_ROWS * 128;  // nibble tiles of one stage
-    constexpr int U = NT >= 4 ? 2 : 4;                   // blocks in flight per warp
+    using SH = Shape<NT, TW>;
+    constexpr int NTW = SH::NTW, KP = SH::KP, R = SH::R, UKB = SH::UKB, QBYTES = SH::QBYTES;
+    constexpr int XPER = (MAX_XITEMS + NCT - 1) / NCT;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* full = reinterpret_cast<uint64_t*>(base);
@@ -158,8 +184,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int64_t row_begin = (int64_t)blockIdx.x * a.rows_per_cta;
     const int64_t row_end = min(a.N, row_begin + a.rows_per_cta);
     const int nrows = (int)max((int64_t)0, row_end - row_begin);
-    const int ntiles = (nrows + 15) / 16;
-    const int ngroups = (ntiles + GROUP_TILES - 1) / GROUP_TILES;
+    const int ngroups = (nrows + R - 1) / R;
     const int nkc = (B + UKB - 1) / UKB;
     const int nunits = ngroups * nkc;
 
@@ -175,7 +200,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == CW) {
-        // ---------------- producer warp: lane 0 paces the ring, all lanes issue copies
+        // ---------------- producer warp: lane 0 paces the ring, lanes issue the copies
         int issued = 0;
         bool ok = true;
         for (int u = 0; u < nunits; ++u) {
@@ -189,23 +214,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             const int g = u / nkc, kc = u - g * nkc;
-            const int tiles = min(GROUP_TILES, ntiles - g * GROUP_TILES);
-            const int r0 = (int)(row_begin + (int64_t)g * GROUP_ROWS);
-            const int b0 = kc * UKB, nb = min(UKB, B - b0);
-            const int nbox = (nb + 7) / 8;  // 8-block columns wholly past K are not copied
+            const int r0 = (int)(row_begin + (int64_t)g * R);
+            const int b0 = kc * UKB, nbox = min(UKB, B - b0) / 8;  // K % 256 == 0: whole 8-block columns
             uint8_t* st = ring + (size_t)s * a.stage_bytes;
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(tiles * 16 * (nbox * 128 + UKB * 2)));
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(nbox * R * 128 + R * UKB * 2));
             __syncwarp();
-            const int nq = tiles * nbox;
-            for (int i = lane; i < nq + tiles; i += 32) {
-                if (i < nq) {
-                    const int t = i / nbox, j = i - t * nbox;
-                    tma2d(st + j * GROUP_ROWS * 128 + t * 16 * 128, &map_q, (b0 + 8 * j) * 16, r0 + 16 * t, &full[s]);
-                } else {
-                    const int t = i - nq;
-                    tma2d(st + QBYTES + t * 16 * UKB * 2, &map_d, b0, r0 + 16 * t, &full[s]);
-                }
-            }
+            if (lane < nbox) tma2d(st + lane * R * 128, &map_q, (b0 + 8 * lane) * 16, r0, &full[s]);
+            else if (lane == UKB / 8) tma2d(st + QBYTES, &map_d, b0, r0, &full[s]);
             issued = u + 1;
         }
         if (!ok && lane == 0) {
@@ -223,124 +238,110 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- consumers
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int g8 = lane >> 2, t4 = lane & 3;
+    const int kp = warp % KP, tg = warp / KP;
+    // B fragment slot of this lane: the four 16-byte chunks of a token are
+    // stored rotated by (token / 2) mod 4, so that both the per-token stores
+    // and these per-lane loads are bank-conflict free
+    const int fslot = (lane & ~3) | (((lane & 3) + (lane >> 3)) & 3);
     const int64_t m0 = (int64_t)blockIdx.y * (8 * NT);
-    uint8_t* xbuf = base + a.off_xbuf;  // 2 x [UKB][2 halves][NT][32 lanes] uint2 fragments
-    float2* xsc = reinterpret_cast<float2*>(base + a.off_xsc);  // 2 x [UKB][NT][4] (d_x of tokens 2t, 2t+1)
-    float* red = reinterpret_cast<float*>(base + a.off_red);    // [7 slots][NT][4][32] partial sums
-    constexpr int XBUF_BYTES = UKB * 2 * NT * 256;
-    constexpr int XSC_N = UKB * NT * 4;
-    constexpr int XITEMS = 8 * NT * UKB, SITEMS = 4 * NT * UKB;
-    static_assert(XITEMS <= XPER * NCT && SITEMS <= SPER * NCT, "activation items per unit");
+    // Per buffer: B fragments [UKB][NT][32 lanes] x 16 bytes (the pair of the
+    // low half, then the pair of the high half), and per token pair
+    // [UKB][NT * 4] x (c even, c odd, c even, c odd | d_x even, d_x odd, -, -):
+    // the MMA accumulator seed of rows g and g + 8, then the scales.
+    uint8_t* xbuf = base + a.off_xbuf;
+    float4* xsc = reinterpret_cast<float4*>(base + a.off_xsc);
+    float* red = reinterpret_cast<float*>(base + a.off_red);  // slots of TW * NTW * 128 floats
+    constexpr int XBUF_BYTES = SH::XBUF;
+    constexpr int XSC_N = SH::XSC / 16;   // float4 per buffer
+    constexpr int XITEMS = 8 * NT * UKB;  // (token, block) pairs of one unit
+    static_assert(XITEMS <= XPER * NCT, "activation items per unit");
 
     uint4 px[XPER][2];
-    uint32_t ps[SPER];
-    // Activation codes and scales of unit column kc into registers.
+    uint32_t ps[XPER];
+    // Activation codes and scale of each (token, block) item of unit column kc into registers.
     auto load_x = [&](int kc) {
         const int b0 = kc * UKB;
 #pragma unroll
         for (int r = 0; r < XPER; ++r) {
             const int q = tid + NCT * r;
             px[r][0] = px[r][1] = make_uint4(0u, 0u, 0u, 0u);
+            ps[r] = 0u;
             const int tok = q % (8 * NT), bl = q / (8 * NT);
             if (q < XITEMS && m0 + tok < a.M && b0 + bl < B) {
-                const uint4* src = reinterpret_cast<const uint4*>(a.xq + (m0 + tok) * a.K + (int64_t)(b0 + bl) * QK);
+                const int64_t m = m0 + tok;
+                const uint4* src = reinterpret_cast<const uint4*>(a.xq + m * a.K + (int64_t)(b0 + bl) * QK);
                 px[r][0] = __ldg(src);
                 px[r][1] = __ldg(src + 1);
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < SPER; ++r) {
-            const int i = tid + NCT * r;
-            ps[r] = 0u;
-            const int bl = i / (4 * NT), j = (i >> 2) % NT, tt = i & 3;
-            const int64_t m = m0 + 8 * j + 2 * tt;
-            if (i < SITEMS && b0 + bl < B) {
-                const uint32_t lo = m < a.M ? __ldg(a.xd + m * B + b0 + bl) : 0u;
-                const uint32_t hi = m + 1 < a.M ? __ldg(a.xd + (m + 1) * B + b0 + bl) : 0u;
-                ps[r] = lo | (hi << 16);
+                ps[r] = __ldg(a.xd + m * B + b0 + bl);
             }
         }
     };
-    // Registers -> fp16 fragments and fp32 scale pairs in buffer `buf`.
+    // Registers -> fragments, scales and accumulator seeds in buffer `buf`.
     auto store_x = [&](int buf) {
         uint8_t* xb = xbuf + buf * XBUF_BYTES;
+        float* xs = reinterpret_cast<float*>(xsc + buf * XSC_N);
 #pragma unroll
         for (int r = 0; r < XPER; ++r) {
             const int q = tid + NCT * r;
             if (q < XITEMS) {
                 const int tok = q % (8 * NT), bl = q / (8 * NT);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint4 v = px[r][h];
-                    const uint2 f0 = codes_to_f16(v.x), f1 = codes_to_f16(v.y);
-                    const uint2 f2 = codes_to_f16(v.z), f3 = codes_to_f16(v.w);
-                    uint4* dst = reinterpret_cast<uint4*>(xb + (bl * 2 + h) * NT * 256 + tok * 32);
-                    dst[0] = make_uint4(f0.x, f0.y, f1.x, f1.y);
-                    dst[1] = make_uint4(f2.x, f2.y, f3.x, f3.y);
-                }
+                const uint4 lo = px[r][0], hi = px[r][1];
+                int slo = __dp4a((int)lo.x, 0x01010101, 0);
+                slo = __dp4a((int)lo.y, 0x01010101, slo);
+                slo = __dp4a((int)lo.z, 0x01010101, slo);
+                slo = __dp4a((int)lo.w, 0x01010101, slo);
+                int shi = __dp4a((int)hi.x, 0x01010101, 0);
+                shi = __dp4a((int)hi.y, 0x01010101, shi);
+                shi = __dp4a((int)hi.z, 0x01010101, shi);
+                shi = __dp4a((int)hi.w, 0x01010101, shi);
+                // lane (g, t) of token tile j = tok / 8 holds word t of token g =
+                // tok % 8, in chunk (t + g / 2) mod 4 of the token's 64 bytes
+                uint4* dst = reinterpret_cast<uint4*>(xb + (bl * NT * 32 + tok * 4) * 16);
+                const int rot = (tok >> 1) & 3;
+                uint2 l, h;
+                l = codes_lo_f16(lo.x), h = codes_hi_f16(hi.x);
+                dst[rot] = make_uint4(l.x, l.y, h.x, h.y);
+                l = codes_lo_f16(lo.y), h = codes_hi_f16(hi.y);
+                dst[(rot + 1) & 3] = make_uint4(l.x, l.y, h.x, h.y);
+                l = codes_lo_f16(lo.z), h = codes_hi_f16(hi.z);
+                dst[(rot + 2) & 3] = make_uint4(l.x, l.y, h.x, h.y);
+                l = codes_lo_f16(lo.w), h = codes_hi_f16(hi.w);
+                dst[(rot + 3) & 3] = make_uint4(l.x, l.y, h.x, h.y);
+                const int pr = (bl * NT * 8 + tok) >> 1, od = tok & 1;
+                const float c = (float)(-(1032 * slo + 72 * shi));
+                xs[pr * 8 + od] = c;
+                xs[pr * 8 + 2 + od] = c;
+                xs[pr * 8 + 4 + od] = f16_bits_to_f32((unsigned short)ps[r]);
             }
         }
-        float2* xs = xsc + buf * XSC_N;
-#pragma unroll
-        for (int r = 0; r < SPER; ++r) {
-            const int i = tid + NCT * r;
-            if (i < SITEMS)
-                xs[i] = make_float2(f16_bits_to_f32((unsigned short)(ps[r] & 0xffffu)),
-                                    f16_bits_to_f32((unsigned short)(ps[r] >> 16)));
-        }
     };
 
-    const float zero[4] = {0.f, 0.f, 0.f, 0.f};
-    float2 acc[NT][2];
+    float2 acc[TW][NTW][2];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = make_float2(0.f, 0.f);
+    for (int i = 0; i < TW; ++i)
+#pragma unroll
+        for (int j = 0; j < NTW; ++j) acc[i][j][0] = acc[i][j][1] = make_float2(0.f, 0.f);
     constexpr int DPITCH = UKB * 2;        // bytes per row of the scale tile
     constexpr int DMASK = DPITCH / 16 - 1;  // its swizzle: 16-byte chunk ^= (row * pitch / 128) & DMASK
-    bool failed = false;
-
-    // One block: nibble words of rows ra, ra + 8 and their scales -> MMAs
-    // against every token tile -> rescaled into the accumulators.
-    auto block = [&](const uint8_t* st, const uint8_t* xb, const float2* xs, int b, int ra, int dsw_a, int dsw_b) {
-        const uint8_t* box = st + (b >> 3) * GROUP_ROWS * 128;
-        const int sw = (((b & 7) ^ g8) << 4) + 4 * t4;  // 128-byte swizzle: row & 7 == g8
-        const uint32_t w0 = *reinterpret_cast<const uint32_t*>(box + ra * 128 + sw);
-        const uint32_t w1 = *reinterpret_cast<const uint32_t*>(box + (ra + 8) * 128 + sw);
-        const uint16_t* sd = reinterpret_cast<const uint16_t*>(st + QBYTES);
-        const int dchunk = b >> 3, dlo = b & 7;
-        const float dw0 = f16_bits_to_f32(sd[ra * UKB + (((dchunk ^ dsw_a) << 3) | dlo)]);
-        const float dw1 = f16_bits_to_f32(sd[(ra + 8) * UKB + (((dchunk ^ dsw_b) << 3) | dlo)]);
-        uint32_t q0[4], q1[4];
-        nibbles_to_f16(w0, q0);
-        nibbles_to_f16(w1, q1);
-        const uint32_t ah0[4] = {q0[0], q1[0], q0[1], q1[1]};  // elements 0..15 of the block
-        const uint32_t ah1[4] = {q0[2], q1[2], q0[3], q1[3]};  // elements 16..31
-        const uint8_t* xbb = xb + b * 2 * NT * 256;
-        const float2* xsb = xs + b * NT * 4;
-        const float2 dwa = make_float2(dw0, dw0), dwb = make_float2(dw1, dw1);
+    // This warp's blocks in every unit: 4 contiguous ones, b = 4 kp .. 4 kp + 3,
+    // inside 8-block column kb = kp / 2; this lane's rows: 16 i + g8 (+ 8).
+    const int kb = kp >> 1, c0 = (kp & 1) << 2;
+    int doff[TW][2];  // scale-tile offsets (fp16 units) of this lane's rows, for the warp's 4 blocks
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const uint2 f0 = *reinterpret_cast<const uint2*>(xbb + j * 256);
-            const uint2 f1 = *reinterpret_cast<const uint2*>(xbb + (NT + j) * 256);
-            float dd[4];
-            mma16816(dd, ah0, f0.x, f0.y, zero);
-            mma16816(dd, ah1, f1.x, f1.y, dd);  // exact integer block dots
-            const float2 sx = xsb[j * 4];       // d_x of tokens 2t, 2t+1
-            acc[j][0] = ffma2_scaled(dwa, sx, make_float2(dd[0], dd[1]), acc[j][0]);  // row ra
-            acc[j][1] = ffma2_scaled(dwb, sx, make_float2(dd[2], dd[3]), acc[j][1]);  // row ra + 8
+    for (int i = 0; i < TW; ++i)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+            const int r = 16 * i + g8 + 8 * hr;
+            doff[i][hr] = r * UKB + (((kb ^ (((r * DPITCH) >> 7) & DMASK)) << 3) | c0);
         }
-    };
+    bool failed = false;
 
     if (nunits > 0) load_x(0);
     for (int u = 0; u < nunits; ++u) {
         const int g = u / nkc, kc = u - g * nkc, s = u % S, buf = u & 1;
-        const int T = min(GROUP_TILES, ntiles - g * GROUP_TILES);  // tiles in this group
-        const int tile = warp % T, part = warp / T;
-        const int P = (CW - tile + T - 1) / T;  // warps on this warp's tile
-        const int ra = 16 * tile + g8;           // this lane's rows in the group: ra and ra + 8
-        const int dsw_a = ((ra * DPITCH) >> 7) & DMASK, dsw_b = (((ra + 8) * DPITCH) >> 7) & DMASK;
         store_x(buf);
         if (u + 1 < nunits) load_x((u + 1) % nkc);
-        consumers_sync();  // fragments of this unit complete (and the unit before last fully read)
+        consumers_sync(NCT);  // fragments of this unit complete (and the unit before last fully read)
         // On a timeout keep going without computing: every later wait returns
         // at once (abort flag), and the kernel ends with the error word set.
         const bool ok = !failed && mbar_wait(&full[s], (u / S) & 1, abort_flag);
@@ -352,64 +353,120 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int nb = min(UKB, B - kc * UKB);
         if (ok) {
             const uint8_t* st = ring + (size_t)s * a.stage_bytes;
-            const uint8_t* xb = xbuf + buf * XBUF_BYTES + lane * 8;
-            const float2* xs = xsc + buf * XSC_N + t4;
-            int b = part;
-            for (; b + (U - 1) * P < nb; b += U * P) {
+            const uint16_t* sd = reinterpret_cast<const uint16_t*>(st + QBYTES);
+            const uint8_t* xf0 = xbuf + buf * XBUF_BYTES + (tg * NTW * 32 + fslot) * 16;
+            const float4* xs0 = xsc + buf * XSC_N + (tg * NTW * 4 + t4) * 2;
+            // the scales of this lane's rows for the warp's 4 blocks
+            uint2 dq[TW][2];
 #pragma unroll
-                for (int i = 0; i < U; ++i) block(st, xb, xs, b + i * P, ra, dsw_a, dsw_b);
+            for (int i = 0; i < TW; ++i)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) dq[i][hr] = *reinterpret_cast<const uint2*>(sd + doff[i][hr]);
+            const uint8_t* bx0 = st + kb * R * 128 + g8 * 128 + 4 * t4;
+#pragma unroll
+            for (int bb = 0; bb < SH::KB_PART; ++bb) {
+                const int b = 4 * kp + bb;
+                if (b < nb) {
+                    const int sw = ((c0 + bb) ^ g8) << 4;  // 128-byte swizzle: row & 7 == g8
+                    uint32_t ah[TW][2][4];
+                    float dw[TW][2];
+#pragma unroll
+                    for (int i = 0; i < TW; ++i) {
+                        const uint8_t* bx = bx0 + i * 16 * 128 + sw;
+                        uint32_t q0[4], q1[4];
+                        nibbles_to_f16(*reinterpret_cast<const uint32_t*>(bx), q0);
+                        nibbles_to_f16(*reinterpret_cast<const uint32_t*>(bx + 8 * 128), q1);
+                        ah[i][0][0] = q0[0], ah[i][0][1] = q1[0], ah[i][0][2] = q0[1], ah[i][0][3] = q1[1];
+                        ah[i][1][0] = q0[2], ah[i][1][1] = q1[2], ah[i][1][2] = q0[3], ah[i][1][3] = q1[3];
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const uint32_t wd = (bb < 2) ? dq[i][hr].x : dq[i][hr].y;
+                            dw[i][hr] = f16_bits_to_f32((unsigned short)(wd >> (16 * (bb & 1))));
+                        }
+                    }
+                    const uint8_t* xf = xf0 + b * NT * 512;
+                    const float4* xs = xs0 + b * NT * 8;
+#pragma unroll
+                    for (int j = 0; j < NTW; ++j) {
+                        const uint4 f = *reinterpret_cast<const uint4*>(xf + j * 512);
+                        const float4 cq = xs[j * 8];  // accumulator seed, tokens 2t, 2t+1 of the tile
+                        const float2 sx = *reinterpret_cast<const float2*>(xs + j * 8 + 1);  // their d_x
+                        const float c4[4] = {cq.x, cq.y, cq.z, cq.w};
+#pragma unroll
+                        for (int i = 0; i < TW; ++i) {
+                            float dd[4];
+                            mma16816(dd, ah[i][0], f.x, f.y, c4);
+                            mma16816(dd, ah[i][1], f.z, f.w, dd);  // exact integer block dots
+                            acc[i][j][0] = ffma2_scaled(make_float2(dw[i][0], dw[i][0]), sx,
+                                                        make_float2(dd[0], dd[1]), acc[i][j][0]);
+                            acc[i][j][1] = ffma2_scaled(make_float2(dw[i][1], dw[i][1]), sx,
+                                                        make_float2(dd[2], dd[3]), acc[i][j][1]);
+                        }
+                    }
+                }
             }
-            for (; b < nb; b += P) block(st, xb, xs, b, ra, dsw_a, dsw_b);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);  // stage read: the producer may refill it
 
         if (kc == nkc - 1) {
-            // end of the group: a split tile's partial sums meet in slot
-            // (part - 1) * T + tile; the part-0 warp adds them and writes y
-            if (T < GROUP_TILES) {
-                if (part > 0) {
-                    float* rp = red + ((part - 1) * T + tile) * NT * 128 + lane;
+            // end of the group: the KP warps of (rows, tokens) meet; part 0 adds and writes y
+            if (KP > 1) {
+                constexpr int SLOT = TW * NTW * 128;
+                const int slot0 = tg * (KP - 1);
+                if (kp > 0) {
+                    float* rp = red + (slot0 + kp - 1) * SLOT + lane;
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) {
-                        rp[j * 128 + 0] = acc[j][0].x;
-                        rp[j * 128 + 32] = acc[j][0].y;
-                        rp[j * 128 + 64] = acc[j][1].x;
-                        rp[j * 128 + 96] = acc[j][1].y;
+                    for (int i = 0; i < TW; ++i)
+#pragma unroll
+                        for (int j = 0; j < NTW; ++j) {
+                            float* q = rp + (i * NTW + j) * 128;
+                            q[0] = acc[i][j][0].x;
+                            q[32] = acc[i][j][0].y;
+                            q[64] = acc[i][j][1].x;
+                            q[96] = acc[i][j][1].y;
+                        }
+                }
+                consumers_sync(NCT);
+                if (kp == 0) {
+#pragma unroll
+                    for (int p = 1; p < KP; ++p) {
+                        const float* rp = red + (slot0 + p - 1) * SLOT + lane;
+#pragma unroll
+                        for (int i = 0; i < TW; ++i)
+#pragma unroll
+                            for (int j = 0; j < NTW; ++j) {
+                                const float* q = rp + (i * NTW + j) * 128;
+                                acc[i][j][0].x += q[0];
+                                acc[i][j][0].y += q[32];
+                                acc[i][j][1].x += q[64];
+                                acc[i][j][1].y += q[96];
+                            }
                     }
                 }
-                consumers_sync();
-                if (part == 0) {
-                    for (int p = 1; p < P; ++p) {
-                        const float* rp = red + ((p - 1) * T + tile) * NT * 128 + lane;
+            }
+            const int64_t r0 = row_begin + (int64_t)g * R;
+            const int nr = (int)min((int64_t)R, row_end - r0);
+            if (kp == 0 && !failed) {
 #pragma unroll
-                        for (int j = 0; j < NT; ++j) {
-                            acc[j][0].x += rp[j * 128 + 0];
-                            acc[j][0].y += rp[j * 128 + 32];
-                            acc[j][1].x += rp[j * 128 + 64];
-                            acc[j][1].y += rp[j * 128 + 96];
+                for (int i = 0; i < TW; ++i)
+#pragma unroll
+                    for (int j = 0; j < NTW; ++j) {
+                        const int64_t m = m0 + 8 * (tg * NTW + j) + 2 * t4;
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int lr = 16 * i + g8 + 8 * hr;
+                            if (lr >= nr) continue;
+                            const int64_t row = r0 + lr;
+                            if (m < a.M) a.y[m * a.ldy + row] = acc[i][j][hr].x;
+                            if (m + 1 < a.M) a.y[(m + 1) * a.ldy + row] = acc[i][j][hr].y;
                         }
                     }
-                }
-            }
-            const int64_t r0 = row_begin + (int64_t)g * GROUP_ROWS;
-            const int nr = (int)min((int64_t)GROUP_ROWS, row_end - r0);
-            if (part == 0 && !failed) {
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const int64_t m = m0 + 8 * j + 2 * t4;
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int lr = ra + 8 * hr;
-                        if (lr >= nr) continue;
-                        const int64_t row = r0 + lr;
-                        if (m < a.M) a.y[m * a.ldy + row] = acc[j][hr].x;
-                        if (m + 1 < a.M) a.y[(m + 1) * a.ldy + row] = acc[j][hr].y;
-                    }
-                }
             }
 #pragma unroll
-            for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = make_float2(0.f, 0.f);
+            for (int i = 0; i < TW; ++i)
+#pragma unroll
+                for (int j = 0; j < NTW; ++j) acc[i][j][0] = acc[i][j][1] = make_float2(0.f, 0.f);
         }
     }
 }
@@ -437,21 +494,16 @@ bool allow_smem(Kern kernel, int bytes) {
 
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
-template <int NT>
-qmm_status launch_nt(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, const int8_t* xq,
-                     const uint16_t* xd, float* y, int64_t ldy, int sms, int smem_optin, int* err, cudaStream_t st) {
-    constexpr int UKB = unit_blocks(NT);
+template <int NT, int TW>
+qmm_status launch_shape(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,
+                        const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy, int64_t rpc, int smem_optin,
+                        int* err, cudaStream_t st) {
+    using SH = Shape<NT, TW>;
     const int64_t B = K / QK;
-    // Rows per CTA: the fewest row tiles that cover N with one CTA per SM.
-    const int64_t rpc = round_up((N + sms - 1) / sms, 16);
     const int64_t G = (N + rpc - 1) / rpc;
-    const int stage = (int)round_up((int64_t)GROUP_ROWS * UKB * 18, 1024);
-    const int xbuf = 2 * UKB * 2 * NT * 256;
-    const int xsc = 2 * UKB * NT * 4 * 8;
-    const int redb = (CW - 1) * NT * 128 * 4;
-    const int fixed = 1024 + xbuf + xsc + redb + 1024;  // header, buffers, alignment slack
-    const int64_t nunits = ((rpc + GROUP_ROWS - 1) / GROUP_ROWS) * ((B + UKB - 1) / UKB);
-    const int64_t nst = std::min<int64_t>({(int64_t)MAX_STAGES, (smem_optin - fixed) / stage, nunits});
+    const int fixed = 1024 + 2 * SH::XBUF + 2 * SH::XSC + SH::RED + 1024;  // header, buffers, alignment slack
+    const int64_t nunits = (rpc / SH::R) * ((B + SH::UKB - 1) / SH::UKB);
+    const int64_t nst = std::min<int64_t>({(int64_t)MAX_STAGES, (smem_optin - fixed) / SH::STAGE, nunits});
     if (nst < 1) return QMM_ERR_SHAPE;
     Args a = {};
     a.N = N;
@@ -463,26 +515,44 @@ qmm_status launch_nt(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_
     a.y = y;
     a.rows_per_cta = (int)rpc;
     a.nstages = (int)nst;
-    a.stage_bytes = stage;
-    a.off_xbuf = 1024 + (int)nst * stage;
-    a.off_xsc = a.off_xbuf + xbuf;
-    a.off_red = a.off_xsc + xsc;
+    a.stage_bytes = SH::STAGE;
+    a.off_xbuf = 1024 + (int)nst * SH::STAGE;
+    a.off_xsc = a.off_xbuf + 2 * SH::XBUF;
+    a.off_red = a.off_xsc + 2 * SH::XSC;
     a.err = err;
-    const int smem = a.off_red + redb + 1024;
-    const CUtensorMapSwizzle dsw = UKB == 8 ? CU_TENSOR_MAP_SWIZZLE_NONE
-                                   : UKB == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
-                                               : CU_TENSOR_MAP_SWIZZLE_64B;
+    const int smem = a.off_red + SH::RED + 1024;
+    const CUtensorMapSwizzle dsw = SH::UKB == 8    ? CU_TENSOR_MAP_SWIZZLE_NONE
+                                   : SH::UKB == 16 ? CU_TENSOR_MAP_SWIZZLE_32B
+                                                   : CU_TENSOR_MAP_SWIZZLE_64B;
     CUtensorMap mq, md;
     if (!make_tensor_map_2d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_qs, (uint64_t)K / 2, (uint64_t)N, (uint64_t)K / 2,
-                            128, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                            128, (uint32_t)SH::R, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT16, w_d, (uint64_t)B, (uint64_t)N, (uint64_t)B * 2,
-                            (uint32_t)UKB, 16, dsw))
+                            (uint32_t)SH::UKB, (uint32_t)SH::R, dsw))
         return QMM_ERR_CUDA;
-    auto kern = gemm_mma_kernel<NT>;
+    auto kern = gemm_mma_kernel<NT, TW>;
     if (smem > smem_optin || !allow_smem(kern, smem_optin)) return QMM_ERR_SHAPE;
     const dim3 grid((unsigned)G, (unsigned)((M + 8 * NT - 1) / (8 * NT)));
     kern<<<grid, THREADS, smem, st>>>(mq, md, a);
     return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+}
+
+// Group height R = 16 TW rows: the tallest (TW = 4, 3, 2, 1) whose
+// rows-per-CTA at one CTA per SM stays within 8% of the 16-row minimum, so
+// that a CTA stages each activation unit as few times as possible.
+template <int NT>
+qmm_status launch_nt(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, const int8_t* xq,
+                     const uint16_t* xd, float* y, int64_t ldy, int sms, int smem_optin, int* err, cudaStream_t st) {
+    const int64_t need = (N + sms - 1) / sms;
+    const int64_t r16 = round_up(need, 16);
+    auto fits = [&](int tw) { return round_up(need, 16 * tw) * 100 <= r16 * 108; };
+    if (fits(4))
+        return launch_shape<NT, 4>(w_qs, w_d, N, K, M, xq, xd, y, ldy, round_up(need, 64), smem_optin, err, st);
+    if (fits(3))
+        return launch_shape<NT, 3>(w_qs, w_d, N, K, M, xq, xd, y, ldy, round_up(need, 48), smem_optin, err, st);
+    if (fits(2))
+        return launch_shape<NT, 2>(w_qs, w_d, N, K, M, xq, xd, y, ldy, round_up(need, 32), smem_optin, err, st);
+    return launch_shape<NT, 1>(w_qs, w_d, N, K, M, xq, xd, y, ldy, r16, smem_optin, err, st);
 }
 
 }  // namespace mmak

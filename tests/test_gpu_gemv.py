@@ -292,11 +292,10 @@ def test_stream_and_fallback_paths_agree_on_odd_k():
 
 
 @pytest.mark.parametrize("M,K", [(48, 2048), (49, 2048), (64, 2048), (32, 28672)])
-def test_gemm_tensor_core_integer_grid_exact(M, K):
-    """Shapes routed to the tensor-core kernel (at least 32 tiles of 128 rows,
-    here with a ragged last tile; 48..64 tokens, or 32 with K too long to stage
-    x for the streaming kernel).  With d = 1 on both sides every output is an
-    exact integer, so any loss in the MMA's integer sums (or a wrong operand
+def test_gemm_mma_integer_grid_exact(M, K):
+    """The warp-MMA GEMM with d = 1 on both sides: every output is an exact
+    integer (32..64 tokens, a ragged last row tile, full-magnitude codes), so
+    any loss in the MMA's fp32 sums of the offset codes (or a wrong operand
     layout) shows as an inequality."""
     qmm = lib()
     rng = np.random.default_rng(M)
