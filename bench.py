@@ -19,8 +19,10 @@ decode step (the reference arm of this build).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -34,6 +36,27 @@ import workloads  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
+# ncu summary of the decode kernel (DRAM traffic per launch) and the sources it was taken from
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "stream_rows_tinyllama_decode.md")
+DECODE_KERNEL_SOURCES = [os.path.join(ROOT, "block_quantized_int4_gb300", "csrc", f)
+                         for f in ("qmm_stream.cuh", "qmm_kernels.cuh", "qmm_device.cuh", "qmm_api.cu")]
+
+
+def _profiled_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, or None once the kernel sources differ from the captured ones."""
+    try:
+        with open(DECODE_PROFILE) as f:
+            text = f.read()
+        traffic = int(re.search(r"traffic_bytes_per_launch:\s*(\d+)", text).group(1))
+        digest = re.search(r"kernel_sources_sha256:\s*([0-9a-f]+)", text).group(1)
+        h = hashlib.sha256()
+        for path in DECODE_KERNEL_SOURCES:
+            with open(path, "rb") as f:
+                h.update(f.read())
+    except Exception:
+        return None
+    return traffic if h.hexdigest().startswith(digest) else None
 
 
 def _peaks():
@@ -376,6 +399,96 @@ def _moe_case(qmm, torch, calls, dev):
             "us_per_call": [round(t * 1e6, 2) for t in ts], "weight_GBps_best": round(wbytes / min(ts) / 1e9, 1)}
 
 
+# ---------------------------------------------------------------------------- every config
+L2_BYTES = 129 << 20
+
+
+def _rotated_us(torch, make_op, nbytes, calls_min=24):
+    """Device time per call of an op over `copies` distinct weight copies
+    (together at least 3x the L2), launched back to back from a CUDA graph,
+    so every call reads its weights from HBM."""
+    copies = int(max(2, min(128, -(-3 * L2_BYTES // max(nbytes, 1)))))
+    ops = [make_op() for _ in range(copies)]
+    reps = max(1, -(-calls_min // copies))
+
+    def run():
+        for _ in range(reps):
+            for op in ops:
+                op()
+
+    g = _graph(torch, run)
+    t = _time_graph(torch, g, 5, 3)
+    return t / 5 / (reps * copies) * 1e6
+
+
+def run_configs(qmm, torch, dev="cuda"):
+    """One JSON line per workload of the five configurations: kernel-only
+    device time per call with weights cold in HBM, weight GB/s (and % of the
+    measured copy peak), TOPS."""
+    peak, peak_kind = _peaks()
+    out = []
+
+    def line(cfg, name, N, K, M, us, extra=None):
+        wb = workloads.q4_0_bytes(N, K)
+        d = {"config": cfg, "workload": name, "N": N, "K": K, "M": M, "us_per_call": round(us, 2),
+             "weight_GBps": round(wb / us / 1e3, 1), "pct_of_hbm_peak": round(100 * wb / us / 1e3 / peak, 1),
+             "TOPS": round(2 * M * N * K / us / 1e6, 2), "peak_kind": peak_kind}
+        if extra:
+            d.update(extra)
+        print(json.dumps(d), flush=True)
+        out.append(d)
+
+    def product(N, K, M, sigma, fused_f32=False):
+        w = workloads.weights(N, K, sigma=sigma, seed=0, index=0, device=dev)
+        qs, d = qmm.quantize_q4_0(w)
+        del w
+        x = workloads.activations(M, K, seed=0, device=dev)
+        xq, xd = qmm.quantize_q8_0(x)
+        y = torch.empty(M, N, device=dev)
+
+        def make():
+            q2, d2 = qs.clone(), d.clone()
+            if fused_f32:
+                return lambda: qmm.qmm_gemv_fused(q2, d2, N, K, x[0], None, None, None, y[0], None, None)
+            if M == 1:
+                return lambda: qmm.qmm_gemv_q4_0_q8_0(q2, d2, N, K, xq[0], xd[0], y[0])
+            return lambda: qmm.qmm_gemm_q4_0_q8_0(q2, d2, N, K, M, xq, xd, y, N)
+
+        us = _rotated_us(torch, make, workloads.q4_0_bytes(N, K))
+        del qs, d
+        torch.cuda.empty_cache()
+        return us
+
+    c = workloads.SINGLE_GEMV
+    line(0, c["name"] + " (Q8_0 activation in)", c["N"], c["K"], 1, product(c["N"], c["K"], 1, c["sigma"]))
+    line(0, c["name"] + " (fp32 activation in, quantized in the launch)", c["N"], c["K"], 1,
+         product(c["N"], c["K"], 1, c["sigma"], fused_f32=True))
+    dec = TinyLlamaDecode(qmm, torch)
+    g = _graph(torch, dec.step)
+    per = _time_graph(torch, g, 50, 5) / 50
+    d1 = {"config": 1, "workload": workloads.TINYLLAMA["name"] + ": whole decode step, 89 chained launches",
+          "M": 1, "us_per_call": round(per * 1e6, 2), "weight_bytes": dec.weight_bytes,
+          "weight_GBps": round(dec.weight_bytes / per / 1e9, 1),
+          "pct_of_hbm_peak": round(100 * dec.weight_bytes / per / 1e9 / peak, 1),
+          "TOPS": round(2 * dec.weight_bytes / 0.5625 / per / 1e12, 3), "tokens_per_s": round(1 / per, 1),
+          "peak_kind": peak_kind}
+    print(json.dumps(d1), flush=True)
+    out.append(d1)
+    del dec, g
+    torch.cuda.empty_cache()
+    for N, K in workloads.BATCHED["shapes"]:
+        for M in workloads.BATCHED["M"]:
+            line(2, f"batched decode GEMM {N}x{K}", N, K, M, product(N, K, M, workloads.BATCHED["sigma"]))
+    for name, N, K in workloads.large_dense_matrices():
+        for M in workloads.LARGE_DENSE["M"]:
+            line(3, f"large dense {name} {N}x{K}", N, K, M, product(N, K, M, workloads.LARGE_DENSE["sigma"]))
+    for T in workloads.MOE["T"]:
+        r = bench_moe(qmm, torch, T=T)
+        print(json.dumps({"config": 4, **r}), flush=True)
+        out.append(r)
+    return out
+
+
 # ---------------------------------------------------------------------------- CPU oracle baseline
 def oracle_decode_sample(torch, rows=256):
     """Oracle inputs for a row sample of every matrix of the decode step: the
@@ -428,6 +541,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=256, help="rows per matrix per reference-arm step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the cpu_baseline sample")
+    ap.add_argument("--configs", action="store_true",
+                    help="time every workload of the five configurations instead (one JSON line each)")
     ap.add_argument("--case", default=None,
                     help="time one kernel instead: decode_gateup, lm_head_8192, gemm_b16, gemm_b64, moe_T16")
     args = ap.parse_args()
@@ -435,6 +550,13 @@ def main():
 
     import torch
 
+    if args.configs:
+        torch.cuda.set_device(local)
+        from block_quantized_int4_gb300 import _build
+        _build.build()
+        from block_quantized_int4_gb300 import qmm
+        run_configs(qmm, torch)
+        return
     if args.case:
         torch.cuda.set_device(local)
         from block_quantized_int4_gb300 import _build
@@ -522,9 +644,11 @@ def main():
                        "l2": "inputs larger than L2 (582 MB of weights per step, each read once)",
                        "pct_of_hbm_peak": round(100 * value / ws / peak, 1)},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "frac": round(achieved / peak, 4), "traffic": _profiled_traffic(),
                          "kernel": "stream_rows_kernel<1,*,*,*> (all 89 launches of the step)",
-                         "peak_kind": peak_kind},
+                         "algorithmic_bytes_per_launch": round(dec.algo_bytes / dec.launches_per_step),
+                         "avg_launch_us": round(per / dec.launches_per_step * 1e6, 3),
+                         "peak_kind": peak_kind, "frac_of": peak_kind + " HBM copy bandwidth"},
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": dec.H * 4,
                     "d2h_bytes_per_step": dec.V * 4},
