@@ -70,6 +70,7 @@ def _load():
                 "oq_router_topk": [P, I, I, I, P, P],
                 "oq_swiglu": [P, P, I, P],
                 "oq_moe_combine": [P, P, I, I, I, P],
+                "oq_rmsnorm": [P, P, I, ctypes.c_double, P],
             }.items():
                 f = getattr(lib, name)
                 f.restype = None
@@ -221,6 +222,23 @@ def swiglu(a, b) -> np.ndarray:
     h = np.empty(a.shape, np.float32)
     _load().oq_swiglu(_p(a), _p(b), a.size, _p(h))
     return h
+
+
+def rmsnorm(x, gamma, eps: float = 1e-5) -> np.ndarray:
+    """RMSNorm of each row of x (fp32 [..., d]) with weight gamma [d], in
+    double, rounded once to fp32 (TinyLLaMA guide 4.1)."""
+    x = _c(x, np.float32)
+    gamma = _c(gamma, np.float32)
+    d = x.shape[-1]
+    assert gamma.shape == (d,)
+    rows = x.reshape(-1, d)
+    out = np.empty_like(rows)
+    for r in range(rows.shape[0]):
+        row = np.ascontiguousarray(rows[r])
+        o = np.empty(d, np.float32)
+        _load().oq_rmsnorm(_p(row), _p(gamma), d, ctypes.c_double(eps), _p(o))
+        out[r] = o
+    return out.reshape(x.shape)
 
 
 def moe_combine(z, gates) -> np.ndarray:

@@ -26,6 +26,8 @@
  *    section 6, GEMM equation.
  *  - SwiGLU(x) = Swish(x W_gate) (x) (x W_up), Swish(z) = z*sigmoid(z):
  *    TinyLLaMA guide, section 4.4.
+ *  - RMSNorm(x) = x / sqrt(mean(x^2) + eps) (.) gamma: TinyLLaMA guide,
+ *    section 4.1 (eps is not given there; callers pass it).
  *  - Sigmoid router selecting experts: Colibri page, "Arquitectura del
  *    Sistema" (DeepSeek-V3-style sigmoid router).  Normalisation of the
  *    selected gates, tie-break and absence of bias are this oracle's reading
@@ -343,6 +345,16 @@ void oq_swiglu(const double* a, const double* b, int64_t n, float* h)
         double sw = a[i] / (1.0 + exp(-a[i]));
         h[i] = (float)(sw * b[i]);
     }
+}
+
+/* RMSNorm of one vector of d values: y_i = x_i / sqrt((1/d) sum_j x_j^2 + eps)
+ * * gamma_i, all in double, each y_i rounded once to fp32. */
+void oq_rmsnorm(const float* x, const float* gamma, int64_t d, double eps, float* y)
+{
+    double ss = 0.0;
+    for (int64_t j = 0; j < d; ++j) ss += (double)x[j] * (double)x[j];
+    const double r = sqrt(ss / (double)d + eps);
+    for (int64_t i = 0; i < d; ++i) y[i] = (float)((double)x[i] / r * (double)gamma[i]);
 }
 
 /* y[t][n] = sum_{j=0..k-1} gates[t][j] * z[t][j][n], in that order, double. */

@@ -311,3 +311,41 @@ def test_moe_combine_linear():
     y = O.moe_combine(z, g)
     assert np.array_equal(y[0], z[0, 0])
     assert np.allclose(y[1], 0.25 * z[1, 0] + 0.5 * z[1, 1] + 0.25 * z[1, 2], rtol=0, atol=1e-15)
+
+
+# ---------------------------------------------------------------- RMSNorm (TinyLLaMA guide 4.1)
+def _golden_kv(name):
+    out = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        if line.startswith("#") or not line.strip():
+            continue
+        k, *v = line.split()
+        out[k] = [float(t) for t in v]
+    return out
+
+
+def test_rmsnorm_worked_example():
+    g = _golden_kv("rmsnorm_small.txt")
+    y = O.rmsnorm(np.array(g["x"], np.float32), np.array(g["gamma"], np.float32), eps=g["eps"][0])
+    assert np.array_equal(y, np.array(g["y"], np.float32))
+
+
+def test_rmsnorm_closed_forms_and_invariants():
+    rng = np.random.default_rng(5)
+    d = 96
+    gamma = rng.normal(1.0, 0.1, d).astype(np.float32)
+    # a constant vector c: every element becomes c / sqrt(c^2 + eps) * gamma_i
+    for c, eps in [(3.0, 0.0), (-0.5, 1e-5), (1e-3, 1e-5)]:
+        y = O.rmsnorm(np.full(d, c, np.float32), gamma, eps=eps)
+        want = (np.float64(np.float32(c)) / np.sqrt(np.float64(np.float32(c)) ** 2 + eps) * gamma).astype(np.float32)
+        assert np.array_equal(y, want)
+    # scale invariance (eps = 0): powers of two change nothing; sign flips the output
+    x = rng.standard_normal((3, d)).astype(np.float32)
+    y = O.rmsnorm(x, gamma, eps=0.0)
+    assert np.array_equal(O.rmsnorm(x * 8, gamma, eps=0.0), y)
+    assert np.array_equal(O.rmsnorm(-x, gamma, eps=0.0), -y)
+    # unit gamma: the output's mean square is 1 (up to the fp32 rounding of each element)
+    y1 = O.rmsnorm(x, np.ones(d, np.float32), eps=0.0).astype(np.float64)
+    assert np.allclose((y1 ** 2).mean(axis=1), 1.0, rtol=1e-6)
+    # eps > 0 shrinks the output towards zero
+    assert (np.abs(O.rmsnorm(x, gamma, eps=1.0)) <= np.abs(y)).all()
