@@ -5,10 +5,12 @@ Headline (the JSON line's `value`): batch-1 GEMV weight GB/s over a
 TinyLLaMA-1.1B-shaped decode step -- 22 layers of fused QKV 2048->2560,
 O 2048->2048, gate/up 2048->2x5632 (one launch over interleaved rows, SwiGLU
 in its epilogue), down 5632->2048 (residual add in its epilogue), then
-lm_head 2048->32000: 89
-dependent GEMV launches per step, each writing its output already in Q8_0
-for the next one (the first quantizes the fp32 token activation), chained
-with programmatic dependent launch and replayed from a CUDA graph.  581,861,376 weight bytes per step (> L2, so no flush).
+lm_head 2048->32000: 89 dependent GEMVs per step.  The residual stream stays
+fp32 and is RMSNorm-ed and quantized to Q8_0 inside the GEMV that reads it;
+QKV and gate/up hand the next GEMV a Q8_0 output; O and down add the
+residual.  The step runs as 89 launches chained with programmatic dependent
+launch (qmm_gemv_fused_op), replayed from a CUDA graph; the one-launch form
+(qmm_gemv_chain) gives identical outputs and is timed by --configs.  581,861,376 weight bytes per step (> L2, so no flush).
 
 Also reported on the same line (`also`): batch-16 GEMM TOPS on the large
 dense FFN + lm_head shapes, and the GLM-scale MoE layer.
@@ -169,43 +171,67 @@ class TinyLlamaDecode:
         f32 = lambda n: torch.zeros(n, dtype=torch.float32, device=dev)  # noqa: E731
         q8 = lambda n: (torch.zeros(n, dtype=torch.int8, device=dev),  # noqa: E731
                         torch.zeros(n // 32, dtype=torch.int16, device=dev))
+        # RMSNorm weights ahead of attention and FFN in every layer, and the final one
+        self.norms = [(workloads.norm_weights(self.H, seed=seed, index=2000 + 2 * li, device=dev),
+                       workloads.norm_weights(self.H, seed=seed, index=2001 + 2 * li, device=dev))
+                      for li in range(self.L)]
+        self.norm_final = workloads.norm_weights(self.H, seed=seed, index=1999, device=dev)
+        self.eps = 1e-5
         self.x_in = workloads.activations(1, self.H, seed=seed, device=dev)[0].contiguous()
-        self.h = [f32(self.H), f32(self.H)]       # fp32 residual stream (ping-pong)
-        self.hq = q8(self.H)                       # Q8_0 of the residual stream
-        self.qkv_q, self.o_q, self.ffn_q = q8(self.Q), q8(self.H), q8(self.F)
+        self.h = [f32(self.H), f32(self.H)]       # fp32 residual stream after each layer (ping-pong)
+        self.hmid = f32(self.H)                   # ... after the attention half of a layer
+        self.qkv_q, self.ffn_q = q8(self.Q), q8(self.F)
         self.logits = f32(self.V)
-        self.launches_per_step = 4 * self.L + 1
-        # algorithmic bytes per step: weights + activations read + outputs written
-        # (Q8_0 activations: 34 bytes per 32 values; fp32 residual / logits)
+        self.launches_per_step = 4 * self.L + 1  # step(): one launch per GEMV
+        # algorithmic bytes per step: weights + activations and norm weights
+        # read + outputs written (Q8_0: 34 bytes per 32 values; fp32: 4)
         q8b = lambda n: n // 32 * 34  # noqa: E731
-        act = 4 * self.H  # the fp32 token activation
-        for li in range(self.L):
-            act += (0 if li == 0 else q8b(self.H)) + q8b(self.Q)        # QKV
-            act += q8b(self.H) + q8b(self.H)                             # O
-            act += q8b(self.H) + q8b(self.F)                             # gate/up
-            act += q8b(self.F) + 4 * self.H + 4 * self.H + q8b(self.H)   # down (+ residual in, fp32 + Q8 out)
-        act += q8b(self.H) + 4 * self.V                                  # lm_head
+        H4 = 4 * self.H
+        act = 0
+        for _ in range(self.L):
+            act += H4 + H4 + q8b(self.Q)              # QKV: RMSNorm(h) -> Q8_0 out
+            act += q8b(self.H) + H4 + H4              # O: q slice in, residual in, fp32 out
+            act += H4 + H4 + q8b(self.F)              # gate/up: RMSNorm(h1), SwiGLU pairs -> Q8_0 out
+            act += q8b(self.F) + H4 + H4              # down: residual in, fp32 out
+        act += H4 + H4 + 4 * self.V                   # lm_head: RMSNorm(h) -> logits
         self.algo_bytes = self.weight_bytes + act
 
-    def step(self, stream=None):
-        """One decode token: every GEMV quantizes (or copies) its activation
-        inside the launch and hands the next one a Q8_0 output."""
+        self.op_list = self._ops()
+        self.n_ops = len(self.op_list)
+        self.op_array = (qmm.GemvOp * self.n_ops)(*self.op_list)
+        self.ws_bytes = qmm.qmm_gemv_chain_workspace_size(self.n_ops)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # counters: zero, left zero
+
+    def _ops(self):
+        """The decode step as qmm_gemv_op descriptors, in order.  Per layer
+        (TinyLLaMA guide 5.2 graph; attention itself is outside this path):
+        QKV on RMSNorm(h) -> Q8_0; O on the q slice, + h -> h1 (fp32); gate/up
+        on RMSNorm(h1) with SwiGLU of row pairs -> Q8_0; down, + h1 -> next h.
+        Then the lm_head on RMSNorm(h)."""
         q, H, F = self.qmm, self.H, self.F
-        C, YS = q.CHAIN, q.Y_SWIGLU_PAIRS
-        f = q.qmm_gemv_fused
-        h_prev = self.x_in
+        op, eps = q.gemv_op, self.eps
+        ops, h_in = [], self.x_in
         for li, Lw in enumerate(self.layers):
-            h_next = self.h[li % 2]
-            if li == 0:  # fp32 token activation in
-                f(*Lw["qkv"], self.Q, H, self.x_in, None, None, None, None, *self.qkv_q, flags=C, stream=stream)
-            else:
-                f(*Lw["qkv"], self.Q, H, None, *self.hq, None, None, *self.qkv_q, flags=C, stream=stream)
-            # attention is outside this path: the O projection reads the q slice
-            f(*Lw["o"], H, H, None, *self.qkv_q, None, None, *self.o_q, flags=C, stream=stream)
-            f(*Lw["gu"], 2 * F, H, None, *self.o_q, None, None, *self.ffn_q, flags=C | YS, stream=stream)
-            f(*Lw["down"], H, F, None, *self.ffn_q, h_prev, h_next, *self.hq, flags=C, stream=stream)
-            h_prev = h_next
-        f(*self.lm_head, self.V, H, None, *self.hq, None, self.logits, None, None, flags=C, stream=stream)
+            g_attn, g_ffn = self.norms[li]
+            h_out = self.h[li % 2]
+            ops.append(op(*Lw["qkv"], self.Q, H, x=h_in, norm_w=g_attn, norm_eps=eps, yq=self.qkv_q[0],
+                          yd=self.qkv_q[1]))
+            ops.append(op(*Lw["o"], H, H, xq=self.qkv_q[0], xd=self.qkv_q[1], residual=h_in, y=self.hmid))
+            ops.append(op(*Lw["gu"], 2 * F, H, x=self.hmid, norm_w=g_ffn, norm_eps=eps, yq=self.ffn_q[0],
+                          yd=self.ffn_q[1], flags=q.Y_SWIGLU_PAIRS))
+            ops.append(op(*Lw["down"], H, F, xq=self.ffn_q[0], xd=self.ffn_q[1], residual=self.hmid, y=h_out))
+            h_in = h_out
+        ops.append(op(*self.lm_head, self.V, H, x=h_in, norm_w=self.norm_final, norm_eps=eps, y=self.logits))
+        return ops
+
+    def step(self, stream=None):
+        """The step as 89 GEMV launches chained with programmatic dependent launch."""
+        for o in self.op_list:
+            self.qmm.qmm_gemv_fused_op(o, self.qmm.CHAIN, stream=stream)
+
+    def chain_step(self, stream=None):
+        """The step as one persistent launch of the whole chain."""
+        self.qmm.qmm_gemv_chain(self.op_array, self.n_ops, self.ws, self.ws_bytes, stream=stream)
 
 
 def _graph(torch, fn):
@@ -340,6 +366,11 @@ def run_case(qmm, torch, name, calls, dev="cuda"):
         M = 16 if name == "gemm_b16" else 64
     elif name == "moe_T16":
         return _moe_case(qmm, torch, calls, dev)
+    elif name in ("decode_chain", "decode_pdl"):  # the whole TinyLLaMA-shaped decode step
+        dec = TinyLlamaDecode(qmm, torch)
+        ts = _time_calls(torch, dec.chain_step if name == "decode_chain" else dec.step, calls)
+        return {"case": name, "us_per_call": [round(t * 1e6, 2) for t in ts],
+                "weight_GBps_best": round(dec.weight_bytes / min(ts) / 1e9, 1)}
     else:
         raise SystemExit(f"unknown case {name}")
     w = workloads.weights(N, K, sigma=sigma, seed=0, index=0, device=dev)
@@ -464,17 +495,20 @@ def run_configs(qmm, torch, dev="cuda"):
     line(0, c["name"] + " (fp32 activation in, quantized in the launch)", c["N"], c["K"], 1,
          product(c["N"], c["K"], 1, c["sigma"], fused_f32=True))
     dec = TinyLlamaDecode(qmm, torch)
-    g = _graph(torch, dec.step)
-    per = _time_graph(torch, g, 50, 5) / 50
-    d1 = {"config": 1, "workload": workloads.TINYLLAMA["name"] + ": whole decode step, 89 chained launches",
-          "M": 1, "us_per_call": round(per * 1e6, 2), "weight_bytes": dec.weight_bytes,
-          "weight_GBps": round(dec.weight_bytes / per / 1e9, 1),
-          "pct_of_hbm_peak": round(100 * dec.weight_bytes / per / 1e9 / peak, 1),
-          "TOPS": round(2 * dec.weight_bytes / 0.5625 / per / 1e12, 3), "tokens_per_s": round(1 / per, 1),
-          "peak_kind": peak_kind}
-    print(json.dumps(d1), flush=True)
-    out.append(d1)
-    del dec, g
+    for path, fn in (("one persistent launch (qmm_gemv_chain)", dec.chain_step),
+                     ("89 launches chained with PDL (qmm_gemv_fused)", dec.step)):
+        g = _graph(torch, fn)
+        per = _time_graph(torch, g, 50, 5) / 50
+        d1 = {"config": 1, "workload": workloads.TINYLLAMA["name"] + ": whole decode step, " + path,
+              "M": 1, "us_per_call": round(per * 1e6, 2), "weight_bytes": dec.weight_bytes,
+              "weight_GBps": round(dec.weight_bytes / per / 1e9, 1),
+              "pct_of_hbm_peak": round(100 * dec.weight_bytes / per / 1e9 / peak, 1),
+              "TOPS": round(2 * dec.weight_bytes / 0.5625 / per / 1e12, 3), "tokens_per_s": round(1 / per, 1),
+              "peak_kind": peak_kind}
+        print(json.dumps(d1), flush=True)
+        out.append(d1)
+        del g
+    del dec
     torch.cuda.empty_cache()
     for N, K in workloads.BATCHED["shapes"]:
         for M in workloads.BATCHED["M"]:
@@ -544,7 +578,8 @@ def main():
     ap.add_argument("--configs", action="store_true",
                     help="time every workload of the five configurations instead (one JSON line each)")
     ap.add_argument("--case", default=None,
-                    help="time one kernel instead: decode_gateup, lm_head_8192, gemm_b16, gemm_b64, moe_T16")
+                    help="time one kernel instead: decode_gateup, decode_chain, decode_pdl, lm_head_8192, gemm_b16, "
+                         "gemm_b64, moe_T16")
     args = ap.parse_args()
     ws, rank, local = _dist()
 
@@ -580,6 +615,8 @@ def main():
     from block_quantized_int4_gb300 import qmm
 
     dec = TinyLlamaDecode(qmm, torch)
+    # the 89 PDL-chained launches measured faster than the one-launch chain
+    # (qmm_gemv_chain) on this workload; both give identical outputs
     g = _graph(torch, dec.step)
 
     # e2e through the C ABI with host buffers: pinned x in, logits out, every step

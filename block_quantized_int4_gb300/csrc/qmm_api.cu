@@ -10,6 +10,7 @@
 #include <utility>
 
 #include "qmm.h"
+#include "qmm_chain.cuh"
 #include "qmm_kernels.cuh"
 #include "qmm_stream.cuh"
 #include "qmm_mma.h"
@@ -29,6 +30,7 @@ struct DevInfo {
     bool ok = false;
     int sms = 0;
     int smem_optin = 0;
+    int smem_per_sm = 0;
     int* err = nullptr;  // device address of g_err_word
 };
 
@@ -51,6 +53,7 @@ const DevInfo* device_info() {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
         cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
         void* p = nullptr;
         const bool sym = cudaGetSymbolAddress(&p, g_err_word) == cudaSuccess;
         d.err = static_cast<int*>(p);
@@ -425,6 +428,149 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
     if (M == 2) return rows_launch<2, X_Q8>(di, a, false, st);
     if (M <= 4) return rows_launch<4, X_Q8>(di, a, false, st);
     return rows_launch<8, X_Q8>(di, a, false, st);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Host checks of one qmm_gemv_op (shared by the single-op and chain entries).
+qmm_status validate_op(const qmm_gemv_op& o) {
+    if (o.N <= 0 || (o.flags & ~QMM_Y_SWIGLU_PAIRS)) return QMM_ERR_ARG;
+    if (!valid_k(o.K) || o.K % 256 != 0 || o.K > 40960 || o.N >= (int64_t(1) << 31)) return QMM_ERR_SHAPE;
+    const bool pairs = o.flags & QMM_Y_SWIGLU_PAIRS;
+    const bool qout = o.yq != nullptr || o.yd != nullptr;
+    if (!o.w_qs || !o.w_d || (!o.x && (!o.xq || !o.xd)) || (!o.y && !qout) || (qout && (!o.yq || !o.yd)))
+        return QMM_ERR_ARG;
+    if (o.x && (o.xq == nullptr) != (o.xd == nullptr)) return QMM_ERR_ARG;
+    if (o.norm_w && (!o.x || !(o.norm_eps >= 0.0f))) return QMM_ERR_ARG;
+    if (pairs && (o.N % 2 || o.residual)) return QMM_ERR_ARG;
+    const int64_t nout = pairs ? o.N / 2 : o.N;
+    if (qout && nout % QK) return QMM_ERR_SHAPE;
+    if (!aligned(o.w_qs, 16) || !aligned(o.w_d, 16) || (o.x && !aligned(o.x, 16)) ||
+        (o.norm_w && !aligned(o.norm_w, 16)) || (o.xq && !aligned(o.xq, 16)) || (o.xd && !aligned(o.xd, 2)) ||
+        (o.y && !aligned(o.y, 4)) || (o.residual && !aligned(o.residual, 4)) || (o.yq && !aligned(o.yq, 16)) ||
+        (o.yd && !aligned(o.yd, 2)))
+        return QMM_ERR_ALIGN;
+    return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qmm_status qmm_gemv_fused_op(const qmm_gemv_op* op, int flags, void* stream) {
+    if (!op || (flags & ~QMM_CHAIN)) return QMM_ERR_ARG;
+    const qmm_gemv_op& o = *op;
+    const qmm_status v = validate_op(o);
+    if (v != QMM_OK) return v;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    const bool pairs = o.flags & QMM_Y_SWIGLU_PAIRS, qout = o.yq != nullptr;
+    StreamArgs a = {};
+    a.N = o.N;
+    a.K = o.K;
+    a.M = 1;
+    a.xf = o.x;
+    a.gamma = o.x ? o.norm_w : nullptr;
+    a.eps = o.norm_eps;
+    if (o.x) {
+        a.xq_out = const_cast<int8_t*>(o.xq);
+        a.xd_out = const_cast<uint16_t*>(o.xd);
+    } else {
+        a.xq = o.xq;
+        a.xd = o.xd;
+    }
+    a.residual = o.residual;
+    a.y = o.y;
+    a.ldy = pairs ? o.N / 2 : o.N;
+    a.yq = o.yq;
+    a.yd = o.yd;
+    const bool pdl = flags & QMM_CHAIN;
+    cudaStream_t st = S(stream);
+    return o.x ? fused_dispatch<X_F32>(di, o.w_qs, o.w_d, a, pairs, qout, pdl, st)
+               : fused_dispatch<X_Q8>(di, o.w_qs, o.w_d, a, pairs, qout, pdl, st);
+}
+
+qmm_status qmm_gemv_chain_workspace_size(int32_t n_ops, size_t* bytes) {
+    if (!bytes || n_ops < 1 || n_ops > QMM_CHAIN_MAX_OPS) return QMM_ERR_ARG;
+    *bytes = (size_t)(n_ops * 4 + 15) / 16 * 16;
+    return QMM_OK;
+}
+
+qmm_status qmm_gemv_chain(const qmm_gemv_op* ops, int32_t n_ops, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    static_assert(QMM_CHAIN_MAX_OPS == CHAIN_MAX_OPS, "chain size");
+    if (!ops || n_ops < 1 || n_ops > QMM_CHAIN_MAX_OPS) return QMM_ERR_ARG;
+    if (!workspace || workspace_bytes < (size_t)n_ops * 4) return QMM_ERR_WORKSPACE;
+    if (!aligned(workspace, 4)) return QMM_ERR_ALIGN;
+    // validate every op first: nothing is launched on an error
+    for (int i = 0; i < n_ops; ++i) {
+        const qmm_status v = validate_op(ops[i]);
+        if (v != QMM_OK) return v;
+    }
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    const int per_sm = 1;  // one CTA per SM: the whole ring per SM for weight look-ahead
+    const int G = per_sm * di->sms;
+    ChainArgs a = {};
+    a.n_ops = n_ops;
+    int64_t xtile = 0, ybuf = 0;
+    for (int i = 0; i < n_ops; ++i) {
+        const qmm_gemv_op& o = ops[i];
+        ChainOp& c = a.ops[i];
+        const bool pairs = o.flags & QMM_Y_SWIGLU_PAIRS;
+        const bool qout = o.yq != nullptr;
+        const int64_t opr = pairs ? 2 : 1;
+        const int64_t B = o.K / QK;
+        c.qs = o.w_qs;
+        c.d = o.w_d;
+        c.xf = o.x;
+        c.gamma = o.x ? o.norm_w : nullptr;
+        c.eps = o.norm_eps;
+        c.xq = o.xq;  // with x: optional output of the staged activation
+        c.xd = o.x && !o.xq ? nullptr : o.xd;
+        c.residual = o.residual;
+        c.y = o.y;
+        c.yq = qout ? o.yq : nullptr;
+        c.yd = qout ? o.yd : nullptr;
+        c.N = (int)o.N;
+        c.K = (int)o.K;
+        c.rows_per_cta = (int)round_up((o.N + G - 1) / G, qout ? QK * opr : 2);
+        c.ckb = (int)std::min<int64_t>(CHUNK_KB, B);
+        c.pairs = pairs ? 1 : 0;
+        xtile = std::max(xtile, B * xtile_bytes_per_block());
+        if (qout) ybuf = std::max<int64_t>(ybuf, c.rows_per_cta / opr * 4);
+    }
+    a.xtile_bytes = (int)round_up(xtile, 128);
+    ybuf = round_up(std::max<int64_t>(ybuf, 4), 128);
+    const int64_t room = (di->smem_optin - STREAM_HDR - a.xtile_bytes - ybuf) / STAGE_BYTES;
+    const int64_t nst = std::min<int64_t>(room, STREAM_MAX_STAGES);
+    if (nst < 2) return QMM_ERR_SHAPE;
+    a.nstages = (int)nst;
+    a.counters = static_cast<unsigned*>(workspace);
+    a.err = di->err;
+    const int smem = (int)(STREAM_HDR + a.xtile_bytes + nst * STAGE_BYTES + ybuf);
+    if (!smem_optin(gemv_chain_kernel, smem, di->smem_optin)) return QMM_ERR_SHAPE;
+    int resident = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, gemv_chain_kernel, STREAM_THREADS, smem) !=
+            cudaSuccess ||
+        resident < per_sm) {
+        cudaGetLastError();
+        return QMM_ERR_DEVICE;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)G);
+    cfg.blockDim = dim3(STREAM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = S(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: they wait on one another
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_chain_kernel, a);
+    return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
 }
 
 qmm_status qmm_debug_block_dots(const uint8_t* w_qs, int64_t N, int64_t K, int64_t M, const int8_t* xq,

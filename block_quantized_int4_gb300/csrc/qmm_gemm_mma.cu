@@ -76,11 +76,13 @@ struct Args {
     int* err;
 };
 
-__device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+// 2D tile copy of weight bytes, evicted first from L2 (l2_evict_first_policy).
+__device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                      uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
@@ -201,6 +203,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (warp == CW) {
         // ---------------- producer warp: lane 0 paces the ring, lanes issue the copies
+        const uint64_t pol = l2_evict_first_policy();
         int issued = 0;
         bool ok = true;
         for (int u = 0; u < nunits; ++u) {
@@ -219,8 +222,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint8_t* st = ring + (size_t)s * a.stage_bytes;
             if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(nbox * R * 128 + R * UKB * 2));
             __syncwarp();
-            if (lane < nbox) tma2d(st + lane * R * 128, &map_q, (b0 + 8 * lane) * 16, r0, &full[s]);
-            else if (lane == UKB / 8) tma2d(st + QBYTES, &map_d, b0, r0, &full[s]);
+            if (lane < nbox) tma2d(st + lane * R * 128, &map_q, (b0 + 8 * lane) * 16, r0, &full[s], pol);
+            else if (lane == UKB / 8) tma2d(st + QBYTES, &map_d, b0, r0, &full[s], pol);
             issued = u + 1;
         }
         if (!ok && lane == 0) {

@@ -229,13 +229,146 @@ __device__ __forceinline__ void stage_q8(const XTile& xt, int Bc, const int8_t* 
     }
 }
 
+// RMSNorm factor of one vector (TinyLLaMA guide 4.1): 1 / sqrt(mean(x^2) +
+// eps).  The sum of squares is taken in one fixed order for a given thread
+// count -- each thread sums x[tid], x[tid + nthr], ...; then each warp; then
+// thread 0 adds the warp partials in warp order -- so every CTA normalizing
+// the same vector with the same thread count gets the same factor.  Threads
+// [0, nthr) take part (nthr % 32 == 0, <= 1024), synchronised with named
+// barrier `bar`; red: 33 floats of shared memory.  Coherent loads (x may have
+// been written by another SM of the same or the preceding launch).
+__device__ __forceinline__ float rms_inv(const float* x, int64_t K, float eps, float* red, int tid, int nthr,
+                                         int bar) {
+    float s = 0.f;
+    for (int64_t i = tid; i < K; i += nthr) {
+        const float v = __ldcg(x + i);
+        s = __fmaf_rn(v, v, s);
+    }
+    s = warp_sum(s);
+    if ((tid & 31) == 0) red[tid >> 5] = s;
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthr) : "memory");
+    if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < nthr / 32; ++w) t = __fadd_rn(t, red[w]);
+        red[32] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)K), eps)));
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthr) : "memory");
+    return red[32];
+}
+
 // Quantize one fp32 activation row (K values; or SwiGLU of gate = x[0..K),
-// up = x[K..2K)) straight into tile row 0.  CTA 0 also writes the Q8_0
-// result out when xq_out/xd_out are given.  Whole CTA; blockDim % 32 == 0.
+// up = x[K..2K)) straight into tile row 0.  With gamma, the row is first
+// normalized: x_i * inv * gamma_i (inv from rms_inv), each product rounded
+// to fp32.  CTA 0 also writes the Q8_0 result out when xq_out/xd_out are
+// given.  Whole CTA; blockDim % 32 == 0.  Coherent loads.
 template <bool GATE_UP>
 __device__ __forceinline__ void stage_f32(const XTile& xt, const float* __restrict__ x, int64_t K,
                                           int8_t* __restrict__ xq_out, uint16_t* __restrict__ xd_out, int tid,
-                                          int nthr) {
+                                          int nthr, const float* gamma = nullptr, float inv = 1.0f);
+
+// RMSNorm + Q8_0 of one activation row into tile row 0 (TinyLLaMA guide
+// 4.1), for rows of at most RMS_STEPS * 4 blocks per warp: the gamma values
+// a thread needs are loaded first (rms_gamma_load -- they do not depend on
+// the activation, so a kernel loads them before it waits for the producer of
+// x); then every x value is loaded once into registers, the sum of squares
+// is taken from the registers in a fixed order (each lane over its values,
+// then butterfly within the warp, then the warps in order), and the
+// normalized values x_i * inv * gamma_i are quantized from the registers.
+// Longer rows take rms_inv + stage_f32 (two passes).  Threads [0, nthr) of
+// the CTA, named barrier `bar`; red: 33 floats of shared memory.  CTA 0
+// writes the Q8_0 row out when xq_out/xd_out are given.
+constexpr int RMS_STEPS = 4;
+
+struct RmsGamma {
+    float4 g[RMS_STEPS];
+};
+
+__device__ __forceinline__ bool rms_one_pass(int64_t K, int nthr) { return K / QK <= (nthr >> 5) * 4 * RMS_STEPS; }
+
+__device__ __forceinline__ RmsGamma rms_gamma_load(const float* gamma, int64_t K, int tid, int nthr) {
+    RmsGamma r;
+    const int B = (int)(K / QK);
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+#pragma unroll
+    for (int i = 0; i < RMS_STEPS; ++i) {
+        const int b = (warp + i * nwarps) * 4 + (lane >> 3);
+        r.g[i] = b < B && rms_one_pass(K, nthr)
+                     ? __ldg(reinterpret_cast<const float4*>(gamma + (int64_t)b * QK + (lane & 7) * 4))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return r;
+}
+
+__device__ __forceinline__ void stage_f32_rmsnorm(const XTile& xt, const float* x, const float* gamma,
+                                                  const RmsGamma& gr, int64_t K, float eps, int8_t* xq_out,
+                                                  uint16_t* xd_out, float* red, int tid, int nthr, int bar) {
+    const int B = (int)(K / QK);
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    if (!rms_one_pass(K, nthr)) {
+        const float inv = rms_inv(x, K, eps, red, tid, nthr, bar);
+        stage_f32<false>(xt, x, K, xq_out, xd_out, tid, nthr, gamma, inv);
+        return;
+    }
+    const int part = lane & 7;
+    const bool writer = blockIdx.x == 0 && blockIdx.y == 0;
+    float4 v[RMS_STEPS];
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < RMS_STEPS; ++i) {
+        const int b = (warp + i * nwarps) * 4 + (lane >> 3);
+        v[i] = b < B ? __ldcg(reinterpret_cast<const float4*>(x + (int64_t)b * QK + part * 4))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < RMS_STEPS; ++i) {
+        ss = __fmaf_rn(v[i].x, v[i].x, ss);
+        ss = __fmaf_rn(v[i].y, v[i].y, ss);
+        ss = __fmaf_rn(v[i].z, v[i].z, ss);
+        ss = __fmaf_rn(v[i].w, v[i].w, ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthr) : "memory");
+    if (tid == 0) {
+        float t = 0.f;
+        for (int w = 0; w < nwarps; ++w) t = __fadd_rn(t, red[w]);
+        red[32] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)K), eps)));
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthr) : "memory");
+    const float inv = red[32];
+#pragma unroll
+    for (int i = 0; i < RMS_STEPS; ++i) {
+        const int gi = warp + i * nwarps;
+        if (gi * 4 >= B) break;  // warp-uniform
+        const int b = gi * 4 + (lane >> 3);
+        const bool valid = b < B;
+        const float4 g = gr.g[i];
+        const float4 w = make_float4(__fmul_rn(__fmul_rn(v[i].x, inv), g.x), __fmul_rn(__fmul_rn(v[i].y, inv), g.y),
+                                     __fmul_rn(__fmul_rn(v[i].z, inv), g.z), __fmul_rn(__fmul_rn(v[i].w, inv), g.w));
+        const Quad r = quad_codes(w, 127.0f, -127.0f);
+        const int packed =
+            (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) | ((r.c[3] & 0xff) << 24);
+        int s = r.c[0] + r.c[1] + r.c[2] + r.c[3];
+        s += __shfl_xor_sync(FULL, s, 1);
+        s += __shfl_xor_sync(FULL, s, 2);
+        s += __shfl_xor_sync(FULL, s, 4);
+        if (valid) {
+            int* plane = reinterpret_cast<int*>(part < 4 ? &xt.lo[b] : &xt.hi[b]);
+            plane[part & 3] = packed;
+            if (part == 0) {
+                const unsigned short h = f32_to_f16_bits(r.d32);
+                xt.sc[b] = make_int2(__float_as_int(f16_bits_to_f32(h)), s);
+                if (writer && xd_out) xd_out[b] = h;
+            }
+            if (writer && xq_out) *reinterpret_cast<int*>(xq_out + (int64_t)b * QK + part * 4) = packed;
+        }
+    }
+}
+
+template <bool GATE_UP>
+__device__ __forceinline__ void stage_f32(const XTile& xt, const float* __restrict__ x, int64_t K,
+                                          int8_t* __restrict__ xq_out, uint16_t* __restrict__ xd_out, int tid,
+                                          int nthr, const float* gamma, float inv) {
     // Each warp takes 4 blocks per step (8 lanes per block, one float4 per
     // lane).  Up to STEPS steps are loaded before any is quantized, so the
     // activation costs one memory round trip per STEPS * nwarps * 4 blocks.
@@ -253,11 +386,15 @@ __device__ __forceinline__ void stage_f32(const XTile& xt, const float* __restri
             v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (b < B) {
                 const int64_t off = (int64_t)b * QK + part * 4;
-                v[i] = *reinterpret_cast<const float4*>(x + off);
+                v[i] = __ldcg(reinterpret_cast<const float4*>(x + off));
                 if (GATE_UP) {
-                    const float4 u = *reinterpret_cast<const float4*>(x + K + off);
+                    const float4 u = __ldcg(reinterpret_cast<const float4*>(x + K + off));
                     v[i] = make_float4(swiglu1(v[i].x, u.x), swiglu1(v[i].y, u.y), swiglu1(v[i].z, u.z),
                                        swiglu1(v[i].w, u.w));
+                } else if (gamma) {
+                    const float4 g = __ldg(reinterpret_cast<const float4*>(gamma + off));
+                    v[i] = make_float4(__fmul_rn(__fmul_rn(v[i].x, inv), g.x), __fmul_rn(__fmul_rn(v[i].y, inv), g.y),
+                                       __fmul_rn(__fmul_rn(v[i].z, inv), g.z), __fmul_rn(__fmul_rn(v[i].w, inv), g.w));
                 }
             }
         }

@@ -41,7 +41,7 @@ enum YMode { Y_PLAIN = 0, Y_SWIGLU_PAIRS = 1 };
 #endif
 constexpr int SW = QMM_STREAM_WARPS;  // consumer warps (four rows each)
 constexpr int STREAM_THREADS = (SW + 1) * 32;
-constexpr int STREAM_HDR = 256;  // barriers + flags
+constexpr int STREAM_HDR = 512;  // barriers, flags, reduction scratch (from byte 256)
 constexpr int STREAM_MAX_STAGES = 8;
 constexpr int GROUP_ROWS = 4 * SW;              // rows per group (4 per consumer warp)
 constexpr int CHUNK_KB = QMM_STREAM_CHUNK_KB;   // K blocks per unit (CHUNK_KB / 32 per lane)
@@ -55,6 +55,8 @@ struct StreamArgs {
     const uint16_t* xd;  // X_Q8: [M][B]
     const float* xf;     // X_F32 / X_SWIGLU: [K] (or [2K])
     const float* residual;  // optional [N] (Y_PLAIN, M == 1)
+    const float* gamma;     // X_F32: RMSNorm weight [K] (normalize x first), or NULL
+    float eps;              // its epsilon
     int8_t* xq_out;
     uint16_t* xd_out;
     float* y;            // may be NULL when a Q8_0 output is requested
@@ -69,11 +71,13 @@ struct StreamArgs {
     int* err;
 };
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+// 2D tile copy of weight bytes, evicted first from L2 (l2_evict_first_policy).
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
@@ -163,6 +167,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
     if (warp == SW) {
         // ---------------- producer: weights only, independent of earlier grids
         if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
             int issued = 0;
             bool ok = true;
             for (int u = 0; u < nunits; ++u) {
@@ -175,8 +180,8 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
                 const int r0 = (int)(row_begin + (int64_t)g * RB);
                 uint8_t* st = ring + (size_t)s * STAGE_BYTES;
                 mbar_arrive_expect_tx(&full[s], unit_bytes);
-                tma_load_2d(st, &map_q, kc * CKB * 4, r0, &full[s]);           // u32 columns
-                tma_load_2d(st + STAGE_Q, &map_d, kc * CKB, r0, &full[s]);     // fp16 columns
+                tma_load_2d(st, &map_q, kc * CKB * 4, r0, &full[s], pol);           // u32 columns
+                tma_load_2d(st + STAGE_Q, &map_d, kc * CKB, r0, &full[s], pol);     // fp16 columns
                 issued = u + 1;
             }
             if (!ok) {
@@ -193,14 +198,21 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
     }
 
     // ---------------- consumers
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     constexpr int NTHR = SW * 32;
+    // RMSNorm weights do not depend on the preceding kernel: load them first
+    RmsGamma gr;
+    if (XMODE == X_F32 && a.gamma) gr = rms_gamma_load(a.gamma, a.K, tid, NTHR);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t m0 = (int64_t)blockIdx.y * MT;
     int64_t xrow[MT];
 #pragma unroll
     for (int t = 0; t < MT; ++t) xrow[t] = (m0 + t < a.M) ? m0 + t : -1;
     if (XMODE == X_Q8) stage_q8<MT>(xt, B, a.xq, a.xd, a.K, xrow, 0, B, tid, NTHR);
-    else stage_f32<XMODE == X_SWIGLU>(xt, a.xf, a.K, a.xq_out, a.xd_out, tid, NTHR);
+    else if (XMODE == X_F32 && a.gamma)
+        stage_f32_rmsnorm(xt, a.xf, a.gamma, gr, a.K, a.eps, a.xq_out, a.xd_out, reinterpret_cast<float*>(smem + 256),
+                          tid, NTHR, 1);
+    else
+        stage_f32<XMODE == X_SWIGLU>(xt, a.xf, a.K, a.xq_out, a.xd_out, tid, NTHR);
     asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
 
     // this warp's rows inside a group: pairs (2w, 2w+1) and (2w+16, 2w+17),
@@ -400,6 +412,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
 
     if (warp == SW) {
         if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
             int u = 0, issued = 0;
             bool ok = true;
             while (ok && cur.next_group(s_active, s_span)) {
@@ -414,8 +427,8 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
                         }
                         uint8_t* st = ring + (size_t)s * STAGE_BYTES;
                         mbar_arrive_expect_tx(&full[s], unit_bytes);
-                        tma_load_2d(st, &map_q, kc * CKB * 4, row, &full[s]);
-                        tma_load_2d(st + STAGE_Q, &map_d, kc * CKB, row, &full[s]);
+                        tma_load_2d(st, &map_q, kc * CKB * 4, row, &full[s], pol);
+                        tma_load_2d(st + STAGE_Q, &map_d, kc * CKB, row, &full[s], pol);
                         issued = u + 1;
                     }
             }

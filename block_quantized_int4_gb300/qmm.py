@@ -40,6 +40,15 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 _P, _I64, _I32, _INT, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int, ctypes.c_size_t
 
+class GemvOp(ctypes.Structure):
+    """qmm_gemv_op of include/qmm.h (one op of qmm_gemv_chain)."""
+    _fields_ = [("w_qs", ctypes.c_void_p), ("w_d", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("x", ctypes.c_void_p), ("norm_w", ctypes.c_void_p), ("xq", ctypes.c_void_p),
+                ("xd", ctypes.c_void_p), ("residual", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("yq", ctypes.c_void_p), ("yd", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
+                ("flags", ctypes.c_int32)]
+
+
 # name -> argtypes (the trailing stream is a void*)
 SIGNATURES = {
     "qmm_quantize_q4_0": [_P, _I64, _I64, _I64, _P, _P, _P],
@@ -51,6 +60,9 @@ SIGNATURES = {
     "qmm_gemv_fused": [_P, _P, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _INT, _P],
     "qmm_gemm_q4_0_q8_0": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P],
     "qmm_debug_block_dots": [_P, _I64, _I64, _I64, _P, _P, _P],
+    "qmm_gemv_chain_workspace_size": [_I32, ctypes.POINTER(_SZ)],
+    "qmm_gemv_chain": [ctypes.POINTER(GemvOp), _I32, _P, _SZ, _P],
+    "qmm_gemv_fused_op": [ctypes.POINTER(GemvOp), _INT, _P],
     "qmm_moe_workspace_size": [_I32, _I32, _I32, ctypes.POINTER(_SZ)],
     "qmm_moe_gemv": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
     "qmm_moe_gemv_static": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P],
@@ -144,6 +156,29 @@ def qmm_gemm_q4_0_q8_0(w_qs, w_d, N, K, M, xq, xd, y, ldy, stream=None):
 def qmm_debug_block_dots(w_qs, N, K, M, xq, dots, stream=None):
     _check(_lib.qmm_debug_block_dots(_ptr(w_qs), N, K, M, _ptr(xq), _ptr(dots), _stream(stream)),
            "qmm_debug_block_dots")
+
+
+def gemv_op(w_qs, w_d, N, K, x=None, xq=None, xd=None, residual=None, y=None, yq=None, yd=None, flags=0,
+            norm_w=None, norm_eps=1e-5):
+    """A qmm_gemv_op from tensors (or None / raw pointers)."""
+    return GemvOp(_ptr(w_qs), _ptr(w_d), N, K, _ptr(x), _ptr(norm_w), _ptr(xq), _ptr(xd), _ptr(residual), _ptr(y),
+                  _ptr(yq), _ptr(yd), float(norm_eps), int(flags))
+
+
+def qmm_gemv_fused_op(op, flags=0, stream=None):
+    _check(_lib.qmm_gemv_fused_op(ctypes.byref(op), int(flags), _stream(stream)), "qmm_gemv_fused_op")
+
+
+def qmm_gemv_chain_workspace_size(n_ops) -> int:
+    out = _SZ(0)
+    _check(_lib.qmm_gemv_chain_workspace_size(n_ops, ctypes.byref(out)), "qmm_gemv_chain_workspace_size")
+    return out.value
+
+
+def qmm_gemv_chain(ops, n_ops, workspace, workspace_bytes, stream=None):
+    """ops: a sequence of GemvOp (or a ctypes array of them)."""
+    arr = ops if isinstance(ops, ctypes.Array) else (GemvOp * len(ops))(*ops)
+    _check(_lib.qmm_gemv_chain(arr, n_ops, _ptr(workspace), workspace_bytes, _stream(stream)), "qmm_gemv_chain")
 
 
 def qmm_moe_workspace_size(E, T, k) -> int:

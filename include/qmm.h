@@ -183,6 +183,69 @@ QMM_API qmm_status qmm_debug_block_dots(const uint8_t* w_qs, int64_t N, int64_t 
                                 int32_t* dots, void* stream);
 
 /* ---------------------------------------------------------------------
+ * A chain of dependent batch-1 GEMVs in one launch (a decode step's
+ * projections, TinyLLaMA guide section 5 graph; each op as qmm_gemv_fused)
+ * ------------------------------------------------------------------- */
+
+/* One batch-1 GEMV op.  Pointers are device pointers; the fields mean what
+ * the arguments of qmm_gemv_fused mean:
+ *  - weights w_qs/w_d of N x K (K % 256 == 0, K <= 40960, both planes
+ *    16-byte aligned);
+ *  - activation: fp32 x [K] (16-byte aligned) when x is not NULL -- first
+ *    normalized by RMSNorm (TinyLLaMA guide 4.1: x / sqrt(mean(x^2) + eps)
+ *    (.) gamma, in fp32) when norm_w (gamma [K], 16-byte aligned) is not
+ *    NULL -- then quantized to Q8_0 exactly as qmm_quantize_q8_0; xq/xd,
+ *    when not NULL, then RECEIVE that Q8_0 activation.  With x NULL the
+ *    activation is the Q8_0 xq [K] / xd [K/32];
+ *  - outputs y (fp32 [N_out], + residual [N_out] when residual is not NULL)
+ *    and/or yq/yd (Q8_0 of y, N_out % 32 == 0);
+ *  - flags 0 or QMM_Y_SWIGLU_PAIRS (N_out = N / 2, no residual). */
+typedef struct qmm_gemv_op {
+    const uint8_t* w_qs;
+    const uint16_t* w_d;
+    int64_t N, K;
+    const float* x;
+    const float* norm_w;
+    const int8_t* xq;
+    const uint16_t* xd;
+    const float* residual;
+    float* y;
+    int8_t* yq;
+    uint16_t* yd;
+    float norm_eps;
+    int32_t flags;
+} qmm_gemv_op;
+
+/* One op as one launch of the streaming GEMV kernel.  flags: 0 or
+ * QMM_CHAIN (programmatic dependent launch, as for qmm_gemv_q4_0_f32). */
+QMM_API qmm_status qmm_gemv_fused_op(const qmm_gemv_op* op, int flags, void* stream);
+
+#define QMM_CHAIN_MAX_OPS 96
+
+/* Bytes of workspace qmm_gemv_chain needs for n_ops ops (one completion
+ * counter per op). */
+QMM_API qmm_status qmm_gemv_chain_workspace_size(int32_t n_ops, size_t* bytes);
+
+/* Runs ops[0..n_ops) in order as one persistent cooperative launch (one CTA
+ * per SM): op i starts once op i-1 has finished on every CTA, so op i may
+ * read any output of an earlier op.  Results are those of calling
+ * qmm_gemv_fused for each op in turn.  The weights of all ops stream from
+ * HBM back to back, ahead of the activations.
+ *  - ops: host array of n_ops (1..QMM_CHAIN_MAX_OPS) descriptors, read
+ *    during the call (copied into the launch).
+ *  - workspace: device, >= qmm_gemv_chain_workspace_size bytes, 4-byte
+ *    aligned, and ALL ZERO before the first call.  A call that completes
+ *    leaves it zero again, so it can be reused by the next call on the same
+ *    stream (including replays of a captured graph).  After a call that
+ *    reported QMM_ERR_TIMEOUT through qmm_last_device_error it must be
+ *    zeroed again.  Two chains must not share a workspace concurrently.
+ *  - An op's outputs must not alias its own inputs.  An op may overwrite
+ *    a buffer that an earlier op read (ops run strictly one after another).
+ * Returns QMM_ERR_DEVICE if the device cannot hold one CTA per SM. */
+QMM_API qmm_status qmm_gemv_chain(const qmm_gemv_op* ops, int32_t n_ops, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* ---------------------------------------------------------------------
  * MoE expert-grouped GEMV (Colibri page: only the routed experts of each
  * token are applied; sigmoid router, top-k)
  * ------------------------------------------------------------------- */

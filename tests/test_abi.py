@@ -98,6 +98,29 @@ def test_static_scratch_limit_and_arguments(qmm):
     assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, None, 1, 2, A16, A16, 0, A16, None) == 1
 
 
+def test_chain_validation(qmm):
+    """qmm_gemv_chain rejects bad descriptors before any launch."""
+    A16 = 0x10000
+    ws = qmm.qmm_gemv_chain_workspace_size(3)
+    assert ws >= 12 and ws % 16 == 0
+    good = dict(w_qs=A16, w_d=A16, N=64, K=256, xq=A16, xd=A16, yq=A16, yd=A16)
+
+    def run(ops, n=None, wsp=A16, wsb=ws):
+        arr = (qmm.GemvOp * len(ops))(*[qmm.gemv_op(**o) for o in ops])
+        return qmm.library_handle().qmm_gemv_chain(arr, len(ops) if n is None else n, wsp, wsb, None)
+
+    assert run([good], n=0) == 1
+    assert run([good], n=97) == 1                        # more than QMM_CHAIN_MAX_OPS
+    assert run([good], wsp=None) == 8
+    assert run([good], wsb=2) == 8
+    assert run([good, dict(good, K=288)]) == 2          # K % 256 != 0
+    assert run([good, dict(good, flags=4)]) == 1        # only Y_SWIGLU_PAIRS allowed
+    assert run([good, dict(good, N=48)]) == 2           # Q8_0 output needs N % 32 == 0
+    assert run([dict(good, w_d=A16 + 2)]) == 3          # scale plane 16-byte aligned
+    assert run([dict(good, yq=None, yd=None)]) == 1     # no output at all
+    assert run([dict(good, flags=2, residual=A16)]) == 1  # pairs with a residual
+
+
 def test_valid_call_without_gpu_reports_device_error(qmm):
     import torch
     if torch.cuda.is_available():
@@ -105,4 +128,6 @@ def test_valid_call_without_gpu_reports_device_error(qmm):
     A16 = 0x10000
     assert _call(qmm, "qmm_gemv_q4_0_q8_0", A16, A16, 64, 64, A16, A16, A16, None) == 4
     assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, A16, 1, 2, A16, A16, 0, A16, None) == 4
+    arr = (qmm.GemvOp * 1)(qmm.gemv_op(A16, A16, 64, 256, xq=A16, xd=A16, y=A16))
+    assert qmm.library_handle().qmm_gemv_chain(arr, 1, A16, 16, None) == 4
     assert _call(qmm, "qmm_last_device_error", None) == 4

@@ -1,0 +1,173 @@
+"""qmm_gemv_chain: a chain of dependent GEMVs in one launch gives exactly the
+outputs of the same ops run one by one through qmm_gemv_fused (same per-row
+arithmetic), and the oracle's within the fp32 tolerance for the first op and
+a propagated tolerance for the chain."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+import workloads
+from parity import lib, u16, assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+class MiniDecode:
+    """Decoder layers shaped like the bench's TinyLLaMA step, small dims: QKV on
+    RMSNorm(h) -> Q8_0; O on the q slice + h -> h1; gate/up on RMSNorm(h1)
+    with SwiGLU pairs -> Q8_0; down + h1 -> h; lm_head on RMSNorm(h)."""
+
+    def __init__(self, qmm, H=512, Q=640, F=1024, V=1000, L=2, seed=7):
+        self.qmm, self.H, self.Q, self.F, self.V, self.L = qmm, H, Q, F, V, L
+        idx = [0]
+
+        def planes(N, K):
+            w = workloads.weights(N, K, sigma=0.02, seed=seed, index=idx[0], device=DEV)
+            idx[0] += 1
+            return qmm.quantize_q4_0(w)
+
+        self.layers = []
+        for li in range(L):
+            qkv, o = planes(Q, H), planes(H, H)
+            g, u = planes(F, H), planes(F, H)
+            gu = (torch.stack([g[0], u[0]], 1).reshape(2 * F, -1).contiguous(),
+                  torch.stack([g[1], u[1]], 1).reshape(2 * F, -1).contiguous())
+            norms = (workloads.norm_weights(H, seed=seed, index=2 * li, device=DEV),
+                     workloads.norm_weights(H, seed=seed, index=2 * li + 1, device=DEV))
+            self.layers.append((qkv, o, gu, planes(H, F), norms))
+        self.lm = planes(V, H)
+        self.norm_final = workloads.norm_weights(H, seed=seed, index=99, device=DEV)
+        z = lambda n, dt=torch.float32: torch.zeros(n, dtype=dt, device=DEV)  # noqa: E731
+        q8 = lambda n: (z(n, torch.int8), z(n // 32, torch.int16))  # noqa: E731
+        self.x = workloads.activations(1, H, seed=seed, device=DEV)[0].contiguous()
+        self.h = [z(H), z(H)]
+        self.hmid = z(H)
+        self.qkv_q, self.ffn_q = q8(Q), q8(F)
+        self.a0 = q8(H)  # the staged (normalized, quantized) activation of op 0
+        self.logits = z(V)
+
+    def ops(self):
+        m, H, Q, F, V = self.qmm, self.H, self.Q, self.F, self.V
+        ops, h_in = [], self.x
+        for li, (qkv, o, gu, down, (ga, gf)) in enumerate(self.layers):
+            h_out = self.h[li % 2]
+            extra = dict(xq=self.a0[0], xd=self.a0[1]) if li == 0 else {}
+            ops.append(m.gemv_op(*qkv, Q, H, x=h_in, norm_w=ga, yq=self.qkv_q[0], yd=self.qkv_q[1], **extra))
+            ops.append(m.gemv_op(*o, H, H, xq=self.qkv_q[0], xd=self.qkv_q[1], residual=h_in, y=self.hmid))
+            ops.append(m.gemv_op(*gu, 2 * F, H, x=self.hmid, norm_w=gf, yq=self.ffn_q[0], yd=self.ffn_q[1],
+                                 flags=m.Y_SWIGLU_PAIRS))
+            ops.append(m.gemv_op(*down, H, F, xq=self.ffn_q[0], xd=self.ffn_q[1], residual=self.hmid, y=h_out))
+            h_in = h_out
+        ops.append(m.gemv_op(*self.lm, V, H, x=h_in, norm_w=self.norm_final, y=self.logits))
+        return ops
+
+    def buffers(self):
+        return (self.logits, self.h[0], self.h[1], self.hmid, *self.qkv_q, *self.ffn_q, *self.a0)
+
+    def run_one_by_one(self):
+        for op in self.ops():
+            self.qmm.qmm_gemv_fused_op(op)
+
+    def snapshot(self):
+        return [t.clone() for t in self.buffers()]
+
+    def reset_outputs(self):
+        for t in self.buffers():
+            t.fill_(0)
+
+
+def test_chain_equals_ops_one_by_one_and_leaves_workspace_zero():
+    qmm = lib()
+    qmm.qmm_last_device_error()
+    dec = MiniDecode(qmm)
+    dec.run_one_by_one()
+    torch.cuda.synchronize()
+    ref = dec.snapshot()
+    dec.reset_outputs()
+    ops = dec.ops()
+    wsb = qmm.qmm_gemv_chain_workspace_size(len(ops))
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    for rep in range(2):  # twice in a row on the same workspace
+        dec.reset_outputs()
+        qmm.qmm_gemv_chain(ops, len(ops), ws, wsb)
+        assert qmm.qmm_last_device_error() == 0
+        got = dec.snapshot()
+        for i, (a, b) in enumerate(zip(got, ref)):
+            assert torch.equal(a, b), f"output {i} differs from the one-by-one ops (call {rep})"
+        assert int(ws.count_nonzero()) == 0
+
+
+def _planes_to_oracle(qs, d, N, K):
+    blocks = np.zeros((N, K // 32, 18), np.uint8)
+    blocks[..., :2] = u16(d).reshape(N, K // 32, 1).view(np.uint8)
+    blocks[..., 2:] = qs.cpu().numpy().reshape(N, K // 32, 16)
+    return O.unpack_q4_0_blocks(blocks, N, K)
+
+
+def test_chain_first_op_and_end_to_end_against_oracle():
+    """Op 0: the GPU's Q8_0 of RMSNorm(x) against the oracle's (codes within
+    one step, scales equal on nearly every block: fp32 sums in another order
+    may move a rounding boundary); its output against the oracle's product of
+    the GPU's own codes.  Then the oracle runs the whole chain on its own
+    (RMSNorm, Q8_0 of each intermediate) and the logits agree to a relative
+    L2 of 1e-3."""
+    qmm = lib()
+    dec = MiniDecode(qmm, L=1)
+    ops = dec.ops()
+    wsb = qmm.qmm_gemv_chain_workspace_size(len(ops))
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    qmm.qmm_gemv_chain(ops, len(ops), ws, wsb)
+    assert qmm.qmm_last_device_error() == 0
+    H, Q, F, V = dec.H, dec.Q, dec.F, dec.V
+    (qkv, o, gu, down, (ga, gf)) = dec.layers[0]
+    x = dec.x.cpu().numpy()[None]
+    a_ref = O.rmsnorm(x, ga.cpu().numpy(), eps=1e-5)
+    qa, da = O.quantize_q8_0(a_ref)
+    gqa, gda = dec.a0[0].cpu().numpy()[None], u16(dec.a0[1])[None]
+    assert (np.abs(gqa.astype(int) - qa.astype(int)) <= 1).all()
+    assert (gqa == qa).mean() > 0.99 and (gda == da).mean() > 0.95
+    # QKV of the GPU's own codes: the Q8_0 output within one step of the oracle's
+    yq_ref, S = O.matmul_int(*_planes_to_oracle(*qkv, Q, H), gqa, gda)
+    qy, dy = O.quantize_q8_0(yq_ref.astype(np.float32))
+    assert (np.abs(dec.qkv_q[0].cpu().numpy().astype(int) - qy[0].astype(int)) <= 1).all()
+    # the oracle's own chain
+    qx, dx = qa, da
+    t, _ = O.matmul_int(*_planes_to_oracle(*qkv, Q, H), qx, dx)
+    q1, d1 = O.quantize_q8_0(t.astype(np.float32))
+    t, _ = O.matmul_int(*_planes_to_oracle(*o, H, H), q1[:, :H], d1[:, :H // 32])
+    h1 = (t + x).astype(np.float32)
+    b = O.rmsnorm(h1, gf.cpu().numpy(), eps=1e-5)
+    qb, db = O.quantize_q8_0(b)
+    g_u, _ = O.matmul_int(*_planes_to_oracle(*gu, 2 * F, H), qb, db)
+    hm = O.swiglu(g_u[:, 0::2], g_u[:, 1::2])
+    qm, dm = O.quantize_q8_0(hm)
+    t, _ = O.matmul_int(*_planes_to_oracle(*down, H, F), qm, dm)
+    h2 = (t + h1).astype(np.float32)
+    c = O.rmsnorm(h2, dec.norm_final.cpu().numpy(), eps=1e-5)
+    qc, dc = O.quantize_q8_0(c)
+    logits, _ = O.matmul_int(*_planes_to_oracle(*dec.lm, V, H), qc, dc)
+    g = dec.logits.cpu().numpy().astype(np.float64)
+    assert np.isfinite(g).all()
+    rel = np.linalg.norm(g - logits[0]) / np.linalg.norm(logits[0])
+    assert rel < 1e-3, rel
+
+
+def test_chain_full_decode_step_equals_per_op_chain():
+    """The TinyLLaMA-shaped decode step of bench.py (89 ops, 22 layers): the
+    one-launch chain and the 89 PDL-chained launches give identical, finite
+    logits."""
+    qmm = lib()
+    import bench
+    dec = bench.TinyLlamaDecode(qmm, torch, seed=3)
+    dec.step()
+    torch.cuda.synchronize()
+    ref = dec.logits.clone()
+    href = dec.h[(dec.L - 1) % 2].clone()
+    dec.logits.fill_(0)
+    dec.chain_step()
+    assert qmm.qmm_last_device_error() == 0
+    assert torch.isfinite(ref).all()
+    assert torch.equal(dec.logits, ref)
+    assert torch.equal(dec.h[(dec.L - 1) % 2], href)

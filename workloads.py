@@ -11,7 +11,9 @@ depend on generation order):
   model);
 * activations x[M][K] ~ N(0, 1), fp32, with round(1% of M*K) entries, chosen
   uniformly without replacement, multiplied by 20 (outliers);
-* router logits [T][E] ~ N(0, 1), fp32.
+* router logits [T][E] ~ N(0, 1), fp32;
+* RMSNorm weights gamma[K] = 1 + 0.1 * N(0, 1), fp32 (the decode step's
+  normalizations; a trained gamma stays near 1).
 
 Generation runs on the requested device with torch's generator for that
 device (CPU: mt19937; CUDA: Philox), so one seed gives
@@ -51,6 +53,11 @@ def activations(M: int, K: int, seed: int = 0, index: int = 500, outlier_frac: f
 def router_logits(T: int, E: int, seed: int = 0, index: int = 900, device="cpu") -> torch.Tensor:
     g = _gen(seed, index, device)
     return torch.randn(T, E, generator=g, device=device, dtype=torch.float32)
+
+
+def norm_weights(K: int, seed: int = 0, index: int = 700, device="cpu") -> torch.Tensor:
+    g = _gen(seed, index, device)
+    return 1.0 + 0.1 * torch.randn(K, generator=g, device=device, dtype=torch.float32)
 
 
 # --------------------------------------------------------------------------
