@@ -356,9 +356,10 @@ def run_case(qmm, torch, name, calls, dev="cuda"):
     L2 per call except decode_gateup, 13 MB, which is what one launch of the
     decode step reads).  For profiler captures (`ncu -k ... -s 3 -c 1`)."""
     M, flags = 1, 0
-    if name == "decode_gateup":  # gate/up of one TinyLLaMA layer: interleaved rows, SwiGLU pairs, Q8 in and out
+    if name in ("decode_gateup", "decode_qkv_norm"):  # one launch of the TinyLLaMA decode step
         c = workloads.TINYLLAMA
-        N, K, sigma = 2 * c["ffn"], c["hidden"], c["sigma"]
+        N, K, sigma = (2 * c["ffn"], c["hidden"], c["sigma"]) if name == "decode_gateup" else \
+            (c["qkv"], c["hidden"], c["sigma"])
     elif name == "lm_head_8192":
         N, K, sigma = workloads.LARGE_DENSE["vocab"], workloads.LARGE_DENSE["hidden"], workloads.LARGE_DENSE["sigma"]
     elif name in ("gemm_b16", "gemm_b64"):
@@ -378,11 +379,18 @@ def run_case(qmm, torch, name, calls, dev="cuda"):
     del w
     xq, xd = qmm.quantize_q8_0(workloads.activations(M, K, seed=0, device=dev))
     y = torch.empty(M, N, device=dev)
-    if name == "decode_gateup":
+    if name == "decode_gateup":  # gate/up: interleaved rows, SwiGLU pairs, Q8_0 in and out
         yq = torch.empty(N // 2, dtype=torch.int8, device=dev)
         yd = torch.empty(N // 64, dtype=torch.int16, device=dev)
         op = lambda: qmm.qmm_gemv_fused(qs, d, N, K, None, xq, xd, None, None, yq, yd,  # noqa: E731
                                         flags=qmm.CHAIN | qmm.Y_SWIGLU_PAIRS)
+    elif name == "decode_qkv_norm":  # QKV: fp32 residual stream in, RMSNorm + Q8_0 in the launch, Q8_0 out
+        yq = torch.empty(N, dtype=torch.int8, device=dev)
+        yd = torch.empty(N // 32, dtype=torch.int16, device=dev)
+        h = workloads.activations(1, K, seed=0, device=dev)[0].contiguous()
+        g = workloads.norm_weights(K, seed=0, device=dev)
+        o1 = qmm.gemv_op(qs, d, N, K, x=h, norm_w=g, yq=yq, yd=yd)
+        op = lambda: qmm.qmm_gemv_fused_op(o1, qmm.CHAIN)  # noqa: E731
     elif M == 1:
         op = lambda: qmm.qmm_gemv_q4_0_q8_0(qs, d, N, K, xq, xd, y)  # noqa: E731
     else:
@@ -578,7 +586,8 @@ def main():
     ap.add_argument("--configs", action="store_true",
                     help="time every workload of the five configurations instead (one JSON line each)")
     ap.add_argument("--case", default=None,
-                    help="time one kernel instead: decode_gateup, decode_chain, decode_pdl, lm_head_8192, gemm_b16, "
+                    help="time one kernel instead: decode_gateup, decode_qkv_norm, decode_chain, decode_pdl, lm_head_8192, "
+                         "gemm_b16, "
                          "gemm_b64, moe_T16")
     args = ap.parse_args()
     ws, rank, local = _dist()

@@ -158,9 +158,10 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
                          cudaStream_t st) {
     const int64_t B = a.K / QK;
     const int64_t row_bytes = a.K / 2 + B * 2;
-    const int64_t opr = YM == Y_SWIGLU_PAIRS ? 2 : 1;
+    const bool qout = XM == X_RUNTIME ? a.qout != 0 : QOUT;
+    const int64_t opr = (YM == Y_RUNTIME ? a.ymode : YM) == Y_SWIGLU_PAIRS ? 2 : 1;
     // rows per CTA: even; with a Q8_0 output, whole blocks of 32 outputs
-    const int64_t align = QOUT ? QK * opr : 2;
+    const int64_t align = qout ? QK * opr : 2;
     // Large matrices: two CTAs per SM (more warps to hide latency); small
     // ones (decode chains): one per SM, leaving room for the next kernel.
 #ifndef QMM_STREAM_BIG_CTAS_PER_SM
@@ -176,7 +177,7 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
     const int rb = (int)std::min<int64_t>(GROUP_ROWS, rpc);
     const int ckb = (int)std::min<int64_t>(CHUNK_KB, B);
     const int64_t xtile = round_up((int64_t)MT * B * xtile_bytes_per_block(), 128);
-    const int64_t ybuf = QOUT ? round_up(rpc / opr * 4, 128) : 0;
+    const int64_t ybuf = qout ? round_up(rpc / opr * 4, 128) : 0;
     const int64_t nunits = ((rpc + rb - 1) / rb) * ((B + ckb - 1) / ckb);
     // Small matrices (decode chains): stay under ~110 KB so the next chained
     // kernel's CTA can be resident and prefetch beside this one.
@@ -204,14 +205,16 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
     return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
 }
 
-// Batch-1 fused launch over the (input form, output form) combinations.
+// Batch-1 fused launch: one compiled kernel for every (input form, output
+// form) combination, the forms passed at run time -- a decode chain runs one
+// code image from launch to launch.
 template <int XM>
 qmm_status fused_dispatch(const DevInfo* di, const uint8_t* qs, const uint16_t* d, StreamArgs a, bool pairs, bool qout,
                           bool pdl, cudaStream_t st) {
-    if (pairs) return qout ? stream_launch<1, XM, Y_SWIGLU_PAIRS, true>(di, qs, d, a, pdl, st)
-                           : stream_launch<1, XM, Y_SWIGLU_PAIRS, false>(di, qs, d, a, pdl, st);
-    return qout ? stream_launch<1, XM, Y_PLAIN, true>(di, qs, d, a, pdl, st)
-                : stream_launch<1, XM, Y_PLAIN, false>(di, qs, d, a, pdl, st);
+    a.xmode = XM;
+    a.ymode = pairs ? Y_SWIGLU_PAIRS : Y_PLAIN;
+    a.qout = qout ? 1 : 0;
+    return stream_launch<1, X_RUNTIME, Y_RUNTIME, false>(di, qs, d, a, pdl, st);
 }
 
 }  // namespace

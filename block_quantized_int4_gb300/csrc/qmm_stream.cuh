@@ -30,7 +30,11 @@
 
 namespace qmm {
 
-enum YMode { Y_PLAIN = 0, Y_SWIGLU_PAIRS = 1 };
+enum YMode { Y_PLAIN = 0, Y_SWIGLU_PAIRS = 1, Y_RUNTIME = 2 };
+// XMODE = X_RUNTIME / YMODE = Y_RUNTIME: the input and output forms are read
+// from StreamArgs (xmode, ymode, qout) at run time, so one compiled kernel
+// serves every op of a decode chain (one code image for the instruction caches).
+constexpr int X_RUNTIME = 3;
 
 // Tiling constants (overridable at build time for tuning sweeps).
 #ifndef QMM_STREAM_WARPS
@@ -61,6 +65,7 @@ struct StreamArgs {
     uint16_t* xd_out;
     float* y;            // may be NULL when a Q8_0 output is requested
     int64_t ldy;
+    int xmode, ymode, qout;  // the forms, read when the kernel is compiled with X_RUNTIME / Y_RUNTIME
     int8_t* yq;          // QOUT: Q8_0 codes of the output [N_out]
     uint16_t* yd;        // QOUT: Q8_0 scales [N_out / 32]
     int rows_per_cta;    // even
@@ -137,6 +142,9 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
     uint64_t* empty = full + STREAM_MAX_STAGES;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STREAM_MAX_STAGES);
+    const int xmode = XMODE == X_RUNTIME ? a.xmode : XMODE;
+    const int ymode = YMODE == Y_RUNTIME ? a.ymode : YMODE;
+    const bool qout = XMODE == X_RUNTIME ? a.qout != 0 : QOUT;
     const int B = (int)(a.K / QK);
     const XTile xt = xtile_at(smem + STREAM_HDR, MT, B);
     uint8_t* ring = smem + STREAM_HDR + a.xtile_bytes;
@@ -201,24 +209,26 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
     constexpr int NTHR = SW * 32;
     // RMSNorm weights do not depend on the preceding kernel: load them first
     RmsGamma gr;
-    if (XMODE == X_F32 && a.gamma) gr = rms_gamma_load(a.gamma, a.K, tid, NTHR);
+    if (xmode == X_F32 && a.gamma) gr = rms_gamma_load(a.gamma, a.K, tid, NTHR);
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t m0 = (int64_t)blockIdx.y * MT;
     int64_t xrow[MT];
 #pragma unroll
     for (int t = 0; t < MT; ++t) xrow[t] = (m0 + t < a.M) ? m0 + t : -1;
-    if (XMODE == X_Q8) stage_q8<MT>(xt, B, a.xq, a.xd, a.K, xrow, 0, B, tid, NTHR);
-    else if (XMODE == X_F32 && a.gamma)
+    if (xmode == X_Q8) stage_q8<MT>(xt, B, a.xq, a.xd, a.K, xrow, 0, B, tid, NTHR);
+    else if (xmode == X_F32 && a.gamma)
         stage_f32_rmsnorm(xt, a.xf, a.gamma, gr, a.K, a.eps, a.xq_out, a.xd_out, reinterpret_cast<float*>(smem + 256),
                           tid, NTHR, 1);
+    else if (xmode == X_SWIGLU)
+        stage_f32<true>(xt, a.xf, a.K, a.xq_out, a.xd_out, tid, NTHR);
     else
-        stage_f32<XMODE == X_SWIGLU>(xt, a.xf, a.K, a.xq_out, a.xd_out, tid, NTHR);
+        stage_f32<false>(xt, a.xf, a.K, a.xq_out, a.xd_out, tid, NTHR);
     asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
 
     // this warp's rows inside a group: pairs (2w, 2w+1) and (2w+16, 2w+17),
     // so a gate/up pair always sits in one warp
     const int rA = 2 * warp, rB = 2 * warp + 16;
-    constexpr int OPR = YMODE == Y_SWIGLU_PAIRS ? 2 : 1;  // rows per output
+    const int OPR = ymode == Y_SWIGLU_PAIRS ? 2 : 1;  // rows per output
     bool failed = false;
     for (int g = 0; g < ngroups; ++g) {
         const int64_t r0 = row_begin + (int64_t)g * RB;
@@ -275,11 +285,11 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
                     const int lr = p ? rB : rA;
                     if (lr >= nr) continue;
                     const int64_t row = r0 + lr;
-                    if (YMODE == Y_SWIGLU_PAIRS) {
+                    if (ymode == Y_SWIGLU_PAIRS) {
                         const float h = swiglu1(v[t][2 * p], v[t][2 * p + 1]);
                         const int64_t o = row / 2;
                         if (a.y) a.y[xrow[t] * a.ldy + o] = h;
-                        if (QOUT) ybuf[o - row_begin / 2] = h;
+                        if (qout) ybuf[o - row_begin / 2] = h;
                     } else {
                         const bool has1 = lr + 1 < nr;
                         const float o0 = v[t][2 * p] + (a.residual ? a.residual[row] : 0.f);
@@ -288,7 +298,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
                             a.y[xrow[t] * a.ldy + row] = o0;
                             if (has1) a.y[xrow[t] * a.ldy + row + 1] = o1;
                         }
-                        if (QOUT) {
+                        if (qout) {
                             ybuf[row - row_begin] = o0;
                             if (has1) ybuf[row + 1 - row_begin] = o1;
                         }
@@ -297,7 +307,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
             }
         }
     }
-    if (QOUT) {
+    if (qout) {
         // Q8_0 of this CTA's outputs (whole blocks of 32; M == 1): warp w takes
         // blocks 4w.., eight lanes per block, same rounding as the quantizers.
         asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
