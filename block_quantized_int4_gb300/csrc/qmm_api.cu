@@ -633,11 +633,12 @@ qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int
         m.rb = GROUP_ROWS;
         m.ckb = (int)std::min<int64_t>(CHUNK_KB, B);
         m.err = di->err;
-        // Slots per weight pass: one, unless experts average two or more
-        // routed slots (then four per pass).  Measured on the GLM-scale layer
-        // (T = 1 and 16, top-8 of 256): one slot per pass is faster even though
-        // an expert with several slots is streamed once per slot.
-        const int mt = nslots >= 2 * (int64_t)E ? 4 : 1;
+        // Slots per weight pass: four once slots outnumber a quarter of the
+        // experts (experts with several slots are then common, and each pass
+        // streams the expert's weights once), else one.  Measured on the
+        // GLM-scale layer, top-8 of 256: 16 tokens 0.518 ms with four per pass,
+        // 0.552 with two, 0.665 with one; 1 token fastest with one.
+        const int mt = nslots * 4 > (int64_t)E ? 4 : 1;
         const int64_t xtile = round_up((int64_t)mt * B * xtile_bytes_per_block(), 128);
         const int64_t tables = round_up((int64_t)E * 12, 128);  // active list + slot spans in shared memory
         // two CTAs per SM (110 KB each): more warps to hide the dot-product latency

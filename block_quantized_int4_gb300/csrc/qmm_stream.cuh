@@ -351,25 +351,28 @@ struct MoeStreamArgs {
     int* err;
 };
 
-// The unit sequence of one CTA, walked identically by producer and consumers.
+// The unit sequence of one CTA, walked identically by producer and consumers:
+// segments (the rows of one active expert inside the CTA's slice), then per
+// segment its slot passes (MT slots each), then per pass the segment's row
+// groups and K chunks.  So a pass stages its activations once for all the
+// segment's rows.
 struct MoeCursor {
     int64_t gr, gr1;  // position in the row space, end of this CTA's slice
     int64_t N;
-    int rb;
-    // current group
-    int e, nr, nsb, sbeg, send;
+    // current segment: expert e, rows [r, r + nrows), slots [sbeg, send)
+    int e, nrows, sbeg, send;
     int64_t r;
     // active: expert of each active index; span: (first slot, end slot) of
     // each active index -- shared-memory copies of the grouping
-    __device__ bool next_group(const int* active, const int2* span) {
+    __device__ bool next_segment(const int* active, const int2* span) {
         if (gr >= gr1) return false;
         const int ai = (int)(gr / N);
         r = gr - (int64_t)ai * N;
-        nr = (int)min((int64_t)rb, min(N - r, gr1 - gr));
+        nrows = (int)min(N - r, gr1 - gr);
         e = active[ai];
         sbeg = span[ai].x;
         send = span[ai].y;
-        gr += nr;
+        gr += nrows;
         return true;
     }
 };
@@ -418,28 +421,31 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
     cur.gr = total * blockIdx.x / gridDim.x;
     cur.gr1 = total * (blockIdx.x + 1) / gridDim.x;
     cur.N = a.N;
-    cur.rb = a.rb;
+
 
     if (warp == SW) {
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
             int u = 0, issued = 0;
             bool ok = true;
-            while (ok && cur.next_group(s_active, s_span)) {
+            while (ok && cur.next_segment(s_active, s_span)) {
                 const int nsb = (cur.send - cur.sbeg + MT - 1) / MT;
-                const int row = (int)((int64_t)cur.e * a.N + cur.r);
+                const int ngroups = (cur.nrows + a.rb - 1) / a.rb;
                 for (int sb = 0; sb < nsb && ok; ++sb)
-                    for (int kc = 0; kc < nkc; ++kc, ++u) {
-                        const int s = u % S;
-                        if (u >= S && !mbar_wait(&empty[s], ((u / S) - 1) & 1, abort_flag)) {
-                            ok = false;
-                            break;
+                    for (int g = 0; g < ngroups && ok; ++g) {
+                        const int row = (int)((int64_t)cur.e * a.N + cur.r + (int64_t)g * a.rb);
+                        for (int kc = 0; kc < nkc; ++kc, ++u) {
+                            const int s = u % S;
+                            if (u >= S && !mbar_wait(&empty[s], ((u / S) - 1) & 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            uint8_t* st = ring + (size_t)s * STAGE_BYTES;
+                            mbar_arrive_expect_tx(&full[s], unit_bytes);
+                            tma_load_2d(st, &map_q, kc * CKB * 4, row, &full[s], pol);
+                            tma_load_2d(st + STAGE_Q, &map_d, kc * CKB, row, &full[s], pol);
+                            issued = u + 1;
                         }
-                        uint8_t* st = ring + (size_t)s * STAGE_BYTES;
-                        mbar_arrive_expect_tx(&full[s], unit_bytes);
-                        tma_load_2d(st, &map_q, kc * CKB * 4, row, &full[s], pol);
-                        tma_load_2d(st + STAGE_Q, &map_d, kc * CKB, row, &full[s], pol);
-                        issued = u + 1;
                     }
             }
             if (!ok) {
@@ -459,9 +465,10 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
     const int rA = 2 * warp, rB = 2 * warp + 16;
     int u = 0;
     bool failed = false;
-    while (cur.next_group(s_active, s_span)) {
+    while (cur.next_segment(s_active, s_span)) {
         const int nslots = cur.send - cur.sbeg;
         const int nsb = (nslots + MT - 1) / MT;
+        const int ngroups = (cur.nrows + a.rb - 1) / a.rb;
         for (int sb = 0; sb < nsb; ++sb) {
             const int mt = min(MT, nslots - sb * MT);  // slots in this pass
             int slot[MT];
@@ -475,54 +482,59 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
             asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");  // everyone is done with the old tile
             stage_q8<MT>(xt, B, a.xq, a.xd, a.K, xrow, 0, B, tid, NTHR);
             asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
-            float2 acc[MT][2];
+            for (int g = 0; g < ngroups; ++g) {
+                const int64_t r0 = cur.r + (int64_t)g * a.rb;
+                const int nr = (int)min((int64_t)a.rb, cur.r + cur.nrows - r0);
+                float2 acc[MT][2];
 #pragma unroll
-            for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = make_float2(0.f, 0.f);
-            for (int kc = 0; kc < nkc; ++kc, ++u) {
-                const int s = u % S;
-                const bool ok = !failed && mbar_wait(&full[s], (u / S) & 1, abort_flag);
-                if (!ok && !failed) {
-                    if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
-                    *abort_flag = 1;
-                    failed = true;
+                for (int t = 0; t < MT; ++t) acc[t][0] = acc[t][1] = make_float2(0.f, 0.f);
+                for (int kc = 0; kc < nkc; ++kc, ++u) {
+                    const int s = u % S;
+                    const bool ok = !failed && mbar_wait(&full[s], (u / S) & 1, abort_flag);
+                    if (!ok && !failed) {
+                        if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+                        *abort_flag = 1;
+                        failed = true;
+                    }
+                    const int b0 = kc * CKB, nb = min(CKB, B - b0);
+                    constexpr int H = CHUNK_KB / 32;
+                    Quad4 qd[H];
+                    const bool work = ok && rA < nr;
+                    if (work) {
+                        const uint8_t* stq = ring + (size_t)s * STAGE_BYTES + (rA * CKB + lane) * 16;
+                        const uint16_t* std_ =
+                            reinterpret_cast<const uint16_t*>(ring + (size_t)s * STAGE_BYTES + STAGE_Q) + rA * CKB +
+                            lane;
+#pragma unroll
+                        for (int h = 0; h < H; ++h)
+                            if (lane + 32 * h < nb) qd[h] = quad_load(stq + 512 * h, CKB * 16, std_ + 32 * h, CKB);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                    if (work) {
+#pragma unroll
+                        for (int h = 0; h < H; ++h)
+                            if (lane + 32 * h < nb) quad_compute<MT>(qd[h], xt, B, b0 + lane + 32 * h, acc, mt);
+                    }
                 }
-                const int b0 = kc * CKB, nb = min(CKB, B - b0);
-                constexpr int H = CHUNK_KB / 32;
-                Quad4 qd[H];
-                const bool work = ok && rA < cur.nr;
-                if (work) {
-                    const uint8_t* stq = ring + (size_t)s * STAGE_BYTES + (rA * CKB + lane) * 16;
-                    const uint16_t* std_ =
-                        reinterpret_cast<const uint16_t*>(ring + (size_t)s * STAGE_BYTES + STAGE_Q) + rA * CKB + lane;
-#pragma unroll
-                    for (int h = 0; h < H; ++h)
-                        if (lane + 32 * h < nb) qd[h] = quad_load(stq + 512 * h, CKB * 16, std_ + 32 * h, CKB);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                if (work) {
-#pragma unroll
-                    for (int h = 0; h < H; ++h)
-                        if (lane + 32 * h < nb) quad_compute<MT>(qd[h], xt, B, b0 + lane + 32 * h, acc, mt);
-                }
-            }
-            float v[MT][4];
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                v[t][0] = warp_sum(acc[t][0].x);
-                v[t][1] = warp_sum(acc[t][0].y);
-                v[t][2] = warp_sum(acc[t][1].x);
-                v[t][3] = warp_sum(acc[t][1].y);
-            }
-            if (lane == 0 && !failed) {
+                float v[MT][4];
 #pragma unroll
                 for (int t = 0; t < MT; ++t) {
-                    if (slot[t] < 0) continue;
-                    float* yr = a.y + (int64_t)slot[t] * a.N + cur.r;
-                    const int lrs[4] = {rA, rA + 1, rB, rB + 1};
+                    v[t][0] = warp_sum(acc[t][0].x);
+                    v[t][1] = warp_sum(acc[t][0].y);
+                    v[t][2] = warp_sum(acc[t][1].x);
+                    v[t][3] = warp_sum(acc[t][1].y);
+                }
+                if (lane == 0 && !failed) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (lrs[q] < cur.nr) yr[lrs[q]] = v[t][q];
+                    for (int t = 0; t < MT; ++t) {
+                        if (slot[t] < 0) continue;
+                        float* yr = a.y + (int64_t)slot[t] * a.N + r0;
+                        const int lrs[4] = {rA, rA + 1, rB, rB + 1};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            if (lrs[q] < nr) yr[lrs[q]] = v[t][q];
+                    }
                 }
             }
         }
