@@ -14,9 +14,10 @@ file, whose header cites the passages each routine follows:
   (kerneldigest.dev), system architecture.
 * SwiGLU -- TinyLLaMA C++ guide, section 4.4.
 
-Parity status: the fp16 conversion, both quantizers, the block dots and both
-output paths are pinned by the CPU tests.  The router's normalisation and
-tie-break are a reading of a silent page: PARITY UNPINNED for the router.
+Parity status: the fp16 conversion, both quantizers, the block dots, both
+output paths, SwiGLU, RMSNorm and the router are pinned by the CPU tests.  The
+router's normalisation over the k and its tie-break are a reading of a silent
+page; the router is pinned to that reading (stable argsort, library sigmoid).
 """
 from __future__ import annotations
 
@@ -205,7 +206,9 @@ def matmul_dequant(qw, dw, qx, dx) -> np.ndarray:
 # ---------------------------------------------------------------- MoE
 def router_topk(logits, k: int):
     """Sigmoid scores, top-k (ties -> lower index), gates normalised over the k.
-    logits [T][E] fp32 -> (ids int32 [T][k], gates float64 [T][k]).  PARITY UNPINNED."""
+    logits [T][E] fp32 -> (ids int32 [T][k], gates float64 [T][k]).  The
+    selection compares the double sigmoid of each fp32 logit, injective over
+    logits in [-87, 16]; outside that range ties may appear."""
     logits = _c(logits, np.float32)
     T, E = logits.shape
     ids = np.empty((T, k), np.int32)

@@ -30,8 +30,10 @@
  *    section 4.1 (eps is not given there; callers pass it).
  *  - Sigmoid router selecting experts: Colibri page, "Arquitectura del
  *    Sistema" (DeepSeek-V3-style sigmoid router).  Normalisation of the
- *    selected gates, tie-break and absence of bias are this oracle's reading
- *    (the page is silent): PARITY UNPINNED for the router.
+ *    selected gates over the k, tie-break to the lower expert index and
+ *    absence of bias are this oracle's reading (the page is silent); the
+ *    function is pinned to that reading (stable argsort of the logits, the
+ *    library sigmoid, closed forms), not to anything the page fixes.
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - the activation is divided by the fp32 scale d32 = amax/127 (before it is

@@ -292,6 +292,40 @@ def test_router_topk_order_ties_and_normalisation():
         assert ids[t].tolist() == np.argsort(-L[t], kind="stable")[:8].tolist()  # sigmoid is monotone
 
 
+def test_router_topk_against_stable_argsort_and_expit():
+    """The router's selection is the top-k of sigmoid scores; sigmoid is
+    strictly increasing (and injective in double over fp32 logits in
+    [-87, 16]), so it must equal numpy's stable argsort of -logits (ties to
+    the lower index).  Gates: scipy's expit of the chosen logits, normalised
+    over the k."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(21)
+    cases = [
+        rng.standard_normal((64, 256)).astype(np.float32),           # the GLM-scale router
+        rng.integers(-3, 4, (64, 40)).astype(np.float32),             # heavy ties, E not a multiple of 32
+        rng.uniform(-87, 16, (8, 1024)).astype(np.float32),           # the domain's ends
+        np.zeros((3, 17), np.float32),                                # all equal
+    ]
+    for L in cases:
+        T, E = L.shape
+        for k in sorted({1, 2, 8, min(E, 32), E}):
+            if k > E:
+                continue
+            ids, g = O.router_topk(L, k)
+            want = np.argsort(-L.astype(np.float64), axis=1, kind="stable")[:, :k]
+            assert np.array_equal(ids, want), (L.shape, k)
+            s = special.expit(np.take_along_axis(L, want, 1).astype(np.float64))
+            assert np.allclose(g, s / s.sum(1, keepdims=True), rtol=1e-14, atol=0)
+            assert np.allclose(g.sum(1), 1.0, rtol=1e-14)
+    # all-equal logits: the k lowest indices, each gate exactly 1/k
+    ids, g = O.router_topk(np.full((2, 10), 0.25, np.float32), 4)
+    assert ids.tolist() == [[0, 1, 2, 3]] * 2 and (g == 0.25).all()
+    # two candidates: gates sigma(a)/(sigma(a)+sigma(b)), larger logit first
+    ids, g = O.router_topk(np.array([[-1.0, 3.0]], np.float32), 2)
+    sa, sb = 1 / (1 + np.exp(1.0)), 1 / (1 + np.exp(-3.0))
+    assert ids.tolist() == [[1, 0]] and np.allclose(g[0], [sb / (sa + sb), sa / (sa + sb)], rtol=1e-15)
+
+
 def test_swiglu_identities():
     a = np.array([0.0, 1.0, -1.0, 30.0, -30.0, 0.5], np.float64)
     b = np.ones_like(a)
