@@ -297,8 +297,9 @@ def bench_gemm_b16(qmm, torch, reps=20, dev="cuda"):
 
 
 def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
-    """GLM-scale MoE layer, T tokens: quantize x, gate and up expert GEMVs,
-    SwiGLU + Q8_0, down expert GEMV, combine."""
+    """GLM-scale MoE layer, T tokens, from router logits on the device:
+    sigmoid top-k router + slot grouping, quantize x, gate and up expert
+    GEMVs, SwiGLU + Q8_0, down expert GEMV, combine (seven launches)."""
     import numpy as np
     c = workloads.MOE
     H, F, E, k = c["hidden"], c["expert_ffn"], c["experts"], c["top_k"]
@@ -313,13 +314,9 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
         return qs, d
 
     gate, up, down = experts(F, H, 0), experts(F, H, 1000), experts(H, F, 2000)
-    logits = workloads.router_logits(T, E, seed=0)
-    # top-k of sigmoid scores == top-k of logits; gates normalised over the k
-    s = torch.sigmoid(logits.double())
-    top = torch.topk(s, k, dim=1, sorted=True)
-    ids = top.indices.to(torch.int32).to(dev)
-    gts = (top.values / top.values.sum(1, keepdim=True)).float().to(dev)
-    uniq = len(np.unique(top.indices.numpy()))
+    logits = workloads.router_logits(T, E, seed=0).to(dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    gts = torch.empty(T, k, dtype=torch.float32, device=dev)
     x = workloads.activations(T, H, seed=0, device=dev)
     xq = torch.empty(T, H, dtype=torch.int8, device=dev)
     xd = torch.empty(T, H // 32, dtype=torch.int16, device=dev)
@@ -333,14 +330,18 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
 
     def run():
+        # the router (sigmoid top-k) groups the slots by expert in the same launch;
+        # the three expert GEMVs reuse that grouping
+        qmm.qmm_moe_router_topk(logits, T, E, k, ids, gts, ws, wsb)
         qmm.qmm_quantize_q8_0(x, T, H, H, xq, xd)
-        qmm.qmm_moe_gemv(*gate, E, F, H, ids, T, k, xq, xd, 0, yg, ws, wsb)
-        qmm.qmm_moe_gemv(*up, E, F, H, ids, T, k, xq, xd, 0, yu, ws, wsb)
+        qmm.qmm_moe_gemv_pregrouped(*gate, E, F, H, T, k, xq, xd, 0, yg, ws, wsb)
+        qmm.qmm_moe_gemv_pregrouped(*up, E, F, H, T, k, xq, xd, 0, yu, ws, wsb)
         qmm.qmm_swiglu_quantize_q8_0(yg, yu, T * k, F, F, hq, hd)
-        qmm.qmm_moe_gemv(*down, E, H, F, ids, T, k, hq, hd, 1, z, ws, wsb)
+        qmm.qmm_moe_gemv_pregrouped(*down, E, H, F, T, k, hq, hd, 1, z, ws, wsb)
         qmm.qmm_moe_combine(z, gts, T, k, H, y)
 
     g = _graph(torch, run)
+    uniq = len(np.unique(ids.cpu().numpy()))  # bookkeeping for the byte count, outside the timed region
     t = _time_graph(torch, g, reps, 3)
     per = t / reps
     wbytes = uniq * 3 * workloads.q4_0_bytes(F, H)

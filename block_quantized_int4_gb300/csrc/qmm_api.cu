@@ -595,25 +595,29 @@ qmm_status qmm_moe_workspace_size(int32_t E, int32_t T, int32_t k, size_t* bytes
     return QMM_OK;
 }
 
-qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K, const int32_t* ids,
-                        int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd, int x_per_slot, float* y,
-                        void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks shared by qmm_moe_gemv and qmm_moe_gemv_pregrouped (ids
+// is checked by the former only).
+qmm_status moe_check(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K, int32_t T, int32_t k,
+                     const int8_t* xq, const uint16_t* xd, float* y, void* workspace, size_t workspace_bytes) {
     if (E <= 0 || N <= 0 || T < 0 || k <= 0) return QMM_ERR_ARG;
     if (!valid_k(K) || (int64_t)T * k > (1 << 24)) return QMM_ERR_SHAPE;
     if (T == 0) return QMM_OK;
-    if (!w_qs || !w_d || !ids || !xq || !xd || !y) return QMM_ERR_ARG;
+    if (!w_qs || !w_d || !xq || !xd || !y) return QMM_ERR_ARG;
     if (!workspace || workspace_bytes < moe_ws_bytes(E, (int64_t)T * k)) return QMM_ERR_WORKSPACE;
     if (!aligned(w_qs, 16) || !aligned(w_d, 2) || !aligned(xq, 16) || !aligned(xd, 2) || !aligned(y, 4) ||
-        !aligned(ids, 4) || !aligned(workspace, 16))
+        !aligned(workspace, 16))
         return QMM_ERR_ALIGN;
-    const DevInfo* di = device_info();
-    if (!di) return QMM_ERR_DEVICE;
-    cudaStream_t st = S(stream);
-    MoeWs ws = moe_ws(workspace, E);
-    moe_group_kernel<<<1, GROUP_THREADS, 0, st>>>(ids, T * k, E, ws, di->err);
-    qmm_status s = launch_status();
-    if (s != QMM_OK) return s;
+    return QMM_OK;
+}
 
+// The expert GEMV on routing tables already built in the workspace.
+qmm_status moe_apply(const DevInfo* di, const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,
+                     int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd, int x_per_slot, float* y,
+                     MoeWs ws, cudaStream_t st) {
     const int64_t B = K / QK;
     const int64_t nslots = (int64_t)T * k;
     const bool streamable = (B % 8 == 0) && aligned(w_qs, 16) && aligned(w_d, 16) &&
@@ -713,6 +717,62 @@ qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int
             break;
     }
     return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
+}
+
+}  // namespace
+
+extern "C" {
+
+qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K, const int32_t* ids,
+                        int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd, int x_per_slot, float* y,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+    qmm_status s = moe_check(w_qs, w_d, E, N, K, T, k, xq, xd, y, workspace, workspace_bytes);
+    if (s != QMM_OK || T == 0) return s;
+    if (!ids) return QMM_ERR_ARG;
+    if (!aligned(ids, 4)) return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    cudaStream_t st = S(stream);
+    MoeWs ws = moe_ws(workspace, E);
+    moe_group_kernel<<<1, GROUP_THREADS, 0, st>>>(ids, T * k, E, ws, di->err);
+    s = launch_status();
+    if (s != QMM_OK) return s;
+    return moe_apply(di, w_qs, w_d, E, N, K, T, k, xq, xd, x_per_slot, y, ws, st);
+}
+
+qmm_status qmm_moe_gemv_pregrouped(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,
+                                   int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd, int x_per_slot,
+                                   float* y, const void* workspace, size_t workspace_bytes, void* stream) {
+    void* wsp = const_cast<void*>(workspace);
+    qmm_status s = moe_check(w_qs, w_d, E, N, K, T, k, xq, xd, y, wsp, workspace_bytes);
+    if (s != QMM_OK || T == 0) return s;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    return moe_apply(di, w_qs, w_d, E, N, K, T, k, xq, xd, x_per_slot, y, moe_ws(wsp, E), S(stream));
+}
+
+qmm_status qmm_moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids, float* gates,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+    if (T < 0 || E <= 0 || k <= 0) return QMM_ERR_ARG;
+    if (E > QMM_ROUTER_MAX_EXPERTS || k > QMM_ROUTER_MAX_K || k > E || (int64_t)T * k > (1 << 24) ||
+        (int64_t)T * E > (int64_t(1) << 40))
+        return QMM_ERR_SHAPE;
+    if (T == 0) return QMM_OK;
+    if (!logits || !ids || !gates) return QMM_ERR_ARG;
+    if (workspace && workspace_bytes < moe_ws_bytes(E, (int64_t)T * k)) return QMM_ERR_WORKSPACE;
+    if (!aligned(logits, 4) || !aligned(ids, 4) || !aligned(gates, 4) || (workspace && !aligned(workspace, 16)))
+        return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    static_assert(QMM_ROUTER_MAX_EXPERTS == ROUTE_MAX_E && QMM_ROUTER_MAX_K == ROUTE_MAX_K, "router limits");
+    const int warps = ROUTE_THREADS / 32;
+    // Grouping needs every token's ids in one block; without it, one warp
+    // per token over as many CTAs as that takes (up to 4 per SM).
+    const int grid = workspace ? 1 : (int)std::min<int64_t>(((int64_t)T + warps - 1) / warps, 4 * (int64_t)di->sms);
+    const MoeWs ws = workspace ? moe_ws(workspace, E) : MoeWs{};
+    moe_route_kernel<<<grid, ROUTE_THREADS, 0, S(stream)>>>(logits, T, E, k, ids, gates, ws, workspace ? 1 : 0,
+                                                            di->err);
+    return launch_status();
 }
 
 qmm_status qmm_moe_combine(const float* z, const float* gates, int32_t T, int32_t k, int64_t N, float* y,

@@ -10,6 +10,8 @@
 // Sistema"; SwiGLU: TinyLLaMA guide section 4.4.
 #pragma once
 
+#include <climits>
+
 #include "qmm_device.cuh"
 
 namespace qmm {
@@ -594,8 +596,9 @@ __host__ __device__ inline size_t moe_ws_bytes(int E, int64_t nslots) {
 // so the order does not change any result).
 constexpr int GROUP_THREADS = 1024;
 
-__global__ void __launch_bounds__(GROUP_THREADS) moe_group_kernel(const int32_t* __restrict__ ids, int nslots, int E,
-                                                                  MoeWs w, int* err) {
+// The whole block builds the tables.  ids may have been written earlier in
+// the same kernel by this block (plain loads after a block barrier).
+__device__ __forceinline__ void moe_group_block(const int32_t* ids, int nslots, int E, MoeWs w, int* err) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) w.counts[e] = 0;
     __syncthreads();
     for (int s = threadIdx.x; s < nslots; s += blockDim.x) {
@@ -655,6 +658,102 @@ __global__ void __launch_bounds__(GROUP_THREADS) moe_group_kernel(const int32_t*
         if (e < 0 || e >= E) continue;
         const int pos = atomicAdd(&w.cursor[e], 1);
         w.slots[pos] = s;
+    }
+}
+
+__global__ void __launch_bounds__(GROUP_THREADS) moe_group_kernel(const int32_t* __restrict__ ids, int nslots, int E,
+                                                                  MoeWs w, int* err) {
+    moe_group_block(ids, nslots, E, w, err);
+}
+
+// ----------------------------------------------------------------------------
+// Sigmoid top-k router (Colibri page, "Arquitectura del Sistema": a sigmoid
+// router picks each token's experts).  Scores s = sigmoid(logit); the k
+// largest are kept, ties to the lower expert index, in decreasing order;
+// gates are the kept scores divided by their sum.  sigmoid is strictly
+// increasing, so the selection compares the logits themselves: no rounding
+// enters it.  One warp per token: lane l holds experts l, l+32, l+64, ...
+// in registers; each of the k rounds is a lane-local scan of the untaken
+// experts followed by a butterfly arg-max (value, then lower index).
+// ----------------------------------------------------------------------------
+constexpr int ROUTE_MAX_E = 1024;
+constexpr int ROUTE_MAX_K = 64;
+constexpr int ROUTE_PER_LANE = ROUTE_MAX_E / 32;
+constexpr int ROUTE_THREADS = 1024;
+
+__device__ __forceinline__ void route_token(const float* __restrict__ lg, int E, int k, int32_t* ids, float* gates,
+                                            int lane) {
+    float v[ROUTE_PER_LANE];
+    uint32_t taken = 0;  // bit i: expert lane + 32 i is chosen already, or does not exist
+    const int nper = (E + 31) >> 5;  // register slots in use
+#pragma unroll
+    for (int i = 0; i < ROUTE_PER_LANE; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = 0.f;
+        if (e < E)
+            v[i] = lg[e];
+        else
+            taken |= 1u << i;
+    }
+    float ssum = 0.f;
+    float keep_s[ROUTE_MAX_K / 32];
+    int keep_id[ROUTE_MAX_K / 32];
+#pragma unroll
+    for (int r = 0; r < ROUTE_MAX_K / 32; ++r) {
+        keep_s[r] = 0.f;
+        keep_id[r] = 0;
+    }
+    for (int j = 0; j < k; ++j) {
+        float bv = 0.f;
+        int bi = INT_MAX;  // none yet
+#pragma unroll
+        for (int i = 0; i < ROUTE_PER_LANE; ++i) {
+            if (i >= nper) break;
+            if (!((taken >> i) & 1u) && (bi == INT_MAX || v[i] > bv)) {  // ascending index: ties keep the lower
+                bv = v[i];
+                bi = lane + 32 * i;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(FULL, bv, o);
+            const int oi = __shfl_xor_sync(FULL, bi, o);
+            if (oi != INT_MAX && (bi == INT_MAX || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        const float s = 1.0f / (1.0f + expf(-bv));
+        ssum += s;  // every lane adds the same scores in the same order
+#pragma unroll
+        for (int r = 0; r < ROUTE_MAX_K / 32; ++r)
+            if (j == lane + 32 * r) {
+                keep_s[r] = s;
+                keep_id[r] = bi;
+            }
+    }
+#pragma unroll
+    for (int r = 0; r < ROUTE_MAX_K / 32; ++r) {
+        const int j = lane + 32 * r;
+        if (j < k) {
+            ids[j] = keep_id[r];
+            gates[j] = keep_s[r] / ssum;
+        }
+    }
+}
+
+// Routes tokens warp by warp; with group != 0 (one CTA) the same block then
+// builds the expert grouping of the chosen ids in w.
+__global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const float* __restrict__ logits, int T, int E,
+                                                                  int k, int32_t* ids, float* gates, MoeWs w,
+                                                                  int group, int* err) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int t = blockIdx.x * nw + warp; t < T; t += gridDim.x * nw)
+        route_token(logits + (int64_t)t * E, E, k, ids + (int64_t)t * k, gates + (int64_t)t * k, lane);
+    if (group) {
+        __syncthreads();
+        moe_group_block(ids, T * k, E, w, err);
     }
 }
 

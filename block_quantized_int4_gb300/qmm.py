@@ -67,6 +67,8 @@ SIGNATURES = {
     "qmm_moe_gemv": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
     "qmm_moe_gemv_static": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P],
     "qmm_moe_combine": [_P, _P, _I32, _I32, _I64, _P, _P],
+    "qmm_moe_router_topk": [_P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P],
+    "qmm_moe_gemv_pregrouped": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
     "qmm_last_device_error": [_P],
 }
 for _name, _args in SIGNATURES.items():
@@ -195,6 +197,19 @@ def qmm_moe_gemv(w_qs, w_d, E, N, K, ids, T, k, xq, xd, x_per_slot, y, workspace
 def qmm_moe_gemv_static(w_qs, w_d, E, N, K, ids, T, k, xq, xd, x_per_slot, y, stream=None):
     _check(_lib.qmm_moe_gemv_static(_ptr(w_qs), _ptr(w_d), E, N, K, _ptr(ids), T, k, _ptr(xq), _ptr(xd),
                                     int(x_per_slot), _ptr(y), _stream(stream)), "qmm_moe_gemv_static")
+
+
+def qmm_moe_router_topk(logits, T, E, k, ids, gates, workspace=None, workspace_bytes=0, stream=None):
+    _check(_lib.qmm_moe_router_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(gates), _ptr(workspace),
+                                    workspace_bytes if workspace is not None else 0, _stream(stream)),
+           "qmm_moe_router_topk")
+
+
+def qmm_moe_gemv_pregrouped(w_qs, w_d, E, N, K, T, k, xq, xd, x_per_slot, y, workspace, workspace_bytes,
+                            stream=None):
+    _check(_lib.qmm_moe_gemv_pregrouped(_ptr(w_qs), _ptr(w_d), E, N, K, T, k, _ptr(xq), _ptr(xd), int(x_per_slot),
+                                        _ptr(y), _ptr(workspace), workspace_bytes, _stream(stream)),
+           "qmm_moe_gemv_pregrouped")
 
 
 def qmm_moe_combine(z, gates, T, k, N, y, stream=None):

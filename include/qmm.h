@@ -269,6 +269,43 @@ QMM_API qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_
                         const int32_t* ids, int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd,
                         int x_per_slot, float* y, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Limits of qmm_moe_router_topk. */
+#define QMM_ROUTER_MAX_EXPERTS 1024
+#define QMM_ROUTER_MAX_K 64
+
+/* Sigmoid top-k router (Colibri page, "Arquitectura del Sistema": a
+ * sigmoid router picks the experts of each token).  For each token t < T:
+ *   s_e = 1 / (1 + exp(-logits[t][e])) in fp32, e < E;
+ *   ids[t][0..k-1] = the k experts of largest score, in decreasing order,
+ *     ties to the lower expert index (sigmoid is strictly increasing, so the
+ *     comparison is made on the logits themselves);
+ *   gates[t][j] = s_{ids[t][j]} / sum_{i<k} s_{ids[t][i]}, the sum taken in
+ *     j order (the normalisation over the k, with no bias, is a reading: the
+ *     page does not say).
+ * logits fp32 [T][E], ids int32 [T][k], gates fp32 [T][k]: device, 4-byte
+ * aligned, caller-owned.  1 <= k <= min(E, QMM_ROUTER_MAX_K),
+ * E <= QMM_ROUTER_MAX_EXPERTS, else QMM_ERR_SHAPE.  Logits must be finite;
+ * the selection equals that of the double-precision sigmoid for logits in
+ * [-87, 16].  T == 0 is a no-op.
+ * workspace: NULL, or device memory of at least qmm_moe_workspace_size(E, T,
+ * k) bytes, 16-byte aligned, contents need not be initialised.  Given one, the
+ * same launch (a single CTA, meant for decode-size T) also groups the chosen
+ * slots by expert there, which is what qmm_moe_gemv_pregrouped reads; without
+ * one, tokens are routed one warp each over as many CTAs as needed. */
+QMM_API qmm_status qmm_moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids,
+                                       float* gates, void* workspace, size_t workspace_bytes, void* stream);
+
+/* qmm_moe_gemv on the slot grouping that qmm_moe_router_topk left in
+ * workspace for the same E, T and k (no ids argument, no grouping launch):
+ * every later expert GEMV of a MoE layer (gate, up, down) reuses one
+ * routing.  The workspace must not be changed in between; an expert id of
+ * the grouping is always in range.  Same arguments, layouts, results and
+ * errors as qmm_moe_gemv otherwise. */
+QMM_API qmm_status qmm_moe_gemv_pregrouped(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,
+                                           int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd,
+                                           int x_per_slot, float* y, const void* workspace, size_t workspace_bytes,
+                                           void* stream);
+
 /* y[t][n] = sum_{j=0..k-1} gates[t][j] * z[t][j][n], j ascending (fixed
  * order, deterministic).  z fp32 [T][k][N], gates fp32 [T][k], y [T][N]. */
 QMM_API qmm_status qmm_moe_combine(const float* z, const float* gates, int32_t T, int32_t k, int64_t N, float* y,

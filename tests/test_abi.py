@@ -121,6 +121,30 @@ def test_chain_validation(qmm):
     assert run([dict(good, flags=2, residual=A16)]) == 1  # pairs with a residual
 
 
+def test_router_and_pregrouped_validation(qmm):
+    """qmm_moe_router_topk: 1 <= k <= min(E, 64), E <= 1024, workspace size
+    and alignment; qmm_moe_gemv_pregrouped: the workspace rules of
+    qmm_moe_gemv.  All rejected on the host."""
+    A16 = 0x10000
+    r = lambda *a: _call(qmm, "qmm_moe_router_topk", *a)  # noqa: E731
+    n = qmm.qmm_moe_workspace_size(256, 16, 8)
+    assert r(A16, 16, 256, 0, A16, A16, None, 0, None) == 1          # k = 0
+    assert r(A16, -1, 256, 8, A16, A16, None, 0, None) == 1          # T < 0
+    assert r(A16, 16, 256, 65, A16, A16, None, 0, None) == 2         # k > QMM_ROUTER_MAX_K
+    assert r(A16, 16, 4, 5, A16, A16, None, 0, None) == 2            # k > E
+    assert r(A16, 16, 1025, 8, A16, A16, None, 0, None) == 2         # E > QMM_ROUTER_MAX_EXPERTS
+    assert r(A16, 0, 256, 8, A16, A16, None, 0, None) == 0           # T = 0: no-op
+    assert r(None, 16, 256, 8, A16, A16, None, 0, None) == 1         # null logits
+    assert r(A16, 16, 256, 8, A16, A16, A16, n - 16, None) == 8      # workspace too small
+    assert r(A16 + 2, 16, 256, 8, A16, A16, None, 0, None) == 3      # logits not 4-byte aligned
+    assert r(A16, 16, 256, 8, A16, A16, A16 + 8, n, None) == 3       # workspace not 16-byte aligned
+    p = lambda *a: _call(qmm, "qmm_moe_gemv_pregrouped", *a)  # noqa: E731
+    assert p(A16, A16, 256, 64, 64, 16, 8, A16, A16, 0, A16, A16, n - 16, None) == 8
+    assert p(A16, A16, 256, 64, 64, 16, 8, A16, A16, 0, A16, None, n, None) == 8
+    assert p(A16, A16, 256, 64, 48, 16, 8, A16, A16, 0, A16, A16, n, None) == 2
+    assert p(A16, A16, 256, 64, 64, 0, 8, A16, A16, 0, A16, A16, n, None) == 0
+
+
 def test_valid_call_without_gpu_reports_device_error(qmm):
     import torch
     if torch.cuda.is_available():
@@ -130,4 +154,5 @@ def test_valid_call_without_gpu_reports_device_error(qmm):
     assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, A16, 1, 2, A16, A16, 0, A16, None) == 4
     arr = (qmm.GemvOp * 1)(qmm.gemv_op(A16, A16, 64, 256, xq=A16, xd=A16, y=A16))
     assert qmm.library_handle().qmm_gemv_chain(arr, 1, A16, 16, None) == 4
+    assert _call(qmm, "qmm_moe_router_topk", A16, 16, 256, 8, A16, A16, None, 0, None) == 4
     assert _call(qmm, "qmm_last_device_error", None) == 4
