@@ -13,6 +13,9 @@ file, whose header cites the passages each routine follows:
 * Q8_0-style int8 activations, sigmoid router -- Colibri page
   (kerneldigest.dev), system architecture.
 * SwiGLU -- TinyLLaMA C++ guide, section 4.4.
+* Per-row-scale int4/int2 containers -- Colibri page, system architecture
+  (layout and scale rule are readings).
+* Q4_0 x fp32 dequantize-then-FMA -- TinyLLaMA C++ guide, section 6.2.
 
 Parity status: the fp16 conversion, both quantizers, the block dots, both
 output paths, SwiGLU, RMSNorm and the router are pinned by the CPU tests.  The
@@ -72,6 +75,11 @@ def _load():
                 "oq_swiglu": [P, P, I, P],
                 "oq_moe_combine": [P, P, I, I, I, P],
                 "oq_rmsnorm": [P, P, I, ctypes.c_double, P],
+                "oq_quantize_rowwise": [P, I, I, I, ctypes.c_int, P, P],
+                "oq_pack_rowwise": [P, I, I, ctypes.c_int, P],
+                "oq_unpack_rowwise": [P, I, I, ctypes.c_int, P],
+                "oq_matmul_rowwise_int": [P, P, I, I, P, P, I, P, P],
+                "oq_matmul_q4_0_f32": [P, P, I, I, P, I, P, P],
             }.items():
                 f = getattr(lib, name)
                 f.restype = None
@@ -201,6 +209,70 @@ def matmul_dequant(qw, dw, qx, dx) -> np.ndarray:
     y = np.empty((M, N), np.float64)
     _load().oq_matmul_dequant(_p(qw), _p(dw), N, K, _p(qx), _p(dx), M, _p(y))
     return y
+
+
+# ---------------------------------------------------------------- per-row containers
+def quantize_rowwise(w, bits: int):
+    """Per-row-scale int4 (bits=4) or int2 (bits=2) codes of w [N][K] (Colibri
+    page's per-row-scale container): (q int8 [N][K], s fp32 [N])."""
+    assert bits in (2, 4)
+    w = _c(w, np.float32)
+    N, K = w.shape
+    q = np.empty((N, K), np.int8)
+    s = np.empty(N, np.float32)
+    _load().oq_quantize_rowwise(_p(w), N, K, K, bits, _p(q), _p(s))
+    return q, s
+
+
+def pack_rowwise(q, bits: int) -> np.ndarray:
+    """Codes u = q + 2^(bits-1), 8/bits per byte, low bits first: uint8 [N][K*bits/8]."""
+    q = _c(q, np.int8)
+    N, K = q.shape
+    out = np.empty((N, K * bits // 8), np.uint8)
+    _load().oq_pack_rowwise(_p(q), N, K, bits, _p(out))
+    return out
+
+
+def unpack_rowwise(packed, K: int, bits: int) -> np.ndarray:
+    packed = _c(packed, np.uint8)
+    N = packed.shape[0]
+    q = np.empty((N, K), np.int8)
+    _load().oq_unpack_rowwise(_p(packed), N, K, bits, _p(q))
+    return q
+
+
+def matmul_rowwise_int(qw, s, qx, dx):
+    """Per-row codes x Q8_0 activations: (y, S) float64 [M][N]."""
+    qw = _c(qw, np.int8)
+    s = _c(s, np.float32)
+    qx = _c(qx, np.int8)
+    dx = _c(dx, np.uint16)
+    if qx.ndim == 1:
+        qx, dx = qx[None], dx[None]
+    N, K = qw.shape
+    M = qx.shape[0]
+    assert s.shape == (N,) and qx.shape[1] == K and dx.shape == (M, K // QK)
+    y = np.empty((M, N), np.float64)
+    S = np.empty((M, N), np.float64)
+    _load().oq_matmul_rowwise_int(_p(qw), _p(s), N, K, _p(qx), _p(dx), M, _p(y), _p(S))
+    return y, S
+
+
+def matmul_q4_0_f32(qw, dw, x):
+    """Q4_0 weights x fp32 activations, dequantize-then-multiply (TinyLLaMA
+    guide 6.2): (y, S) float64 [M][N]."""
+    qw = _c(qw, np.int8)
+    dw = _c(dw, np.uint16)
+    x = _c(x, np.float32)
+    if x.ndim == 1:
+        x = x[None]
+    N, K = qw.shape
+    M = x.shape[0]
+    assert dw.shape == (N, K // QK) and x.shape[1] == K
+    y = np.empty((M, N), np.float64)
+    S = np.empty((M, N), np.float64)
+    _load().oq_matmul_q4_0_f32(_p(qw), _p(dw), N, K, _p(x), M, _p(y), _p(S))
+    return y, S
 
 
 # ---------------------------------------------------------------- MoE

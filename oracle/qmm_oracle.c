@@ -28,6 +28,13 @@
  *    TinyLLaMA guide, section 4.4.
  *  - RMSNorm(x) = x / sqrt(mean(x^2) + eps) (.) gamma: TinyLLaMA guide,
  *    section 4.1 (eps is not given there; callers pass it).
+ *  - Per-row-scale int4 / int2 containers: Colibri page, "Arquitectura del
+ *    Sistema" (int4 container with per-row scales; int4/int2 packing); the
+ *    scale rule is the llama.cpp guide's 2.2 rule applied per row, and the
+ *    bit layout is this oracle's reading (the page gives none).
+ *  - Q4_0 weights x fp32 activations: TinyLLaMA guide, section 6.2 (expand
+ *    the 4-bit values, multiply by the scale, multiply-add with the fp32
+ *    activations).
  *  - Sigmoid router selecting experts: Colibri page, "Arquitectura del
  *    Sistema" (DeepSeek-V3-style sigmoid router).  Normalisation of the
  *    selected gates over the k, tie-break to the lower expert index and
@@ -306,6 +313,112 @@ void oq_matmul_dequant(const int8_t* qw, const uint16_t* dw, int64_t N, int64_t 
                 acc += a * c;
             }
             y[m * N + n] = acc;
+        }
+}
+
+/* ------------------------------------------------------------------ */
+/* Per-row-scale int4 / int2 containers (Colibri page, "Arquitectura   */
+/* del Sistema": an int4 container with per-row scales, int4 and int2  */
+/* packing).  The page gives no layout; the readings taken:            */
+/*  - delta = amax(row)/qmax in fp32, qmax = 2^(bits-1) - 1, the       */
+/*    llama.cpp guide 2.2 rule applied to the whole row;               */
+/*  - q = clamp(rha(w/delta), -2^(bits-1), qmax); a zero row: 0, 0;    */
+/*  - codes u = q + 2^(bits-1), packed 8/bits per byte, element i of   */
+/*    the row in byte i*bits/8 at bit (i mod (8/bits))*bits;           */
+/*  - the scale is kept as fp32.                                       */
+/* ------------------------------------------------------------------ */
+
+void oq_quantize_rowwise(const float* w, int64_t N, int64_t K, int64_t ldw, int bits, int8_t* q, float* s)
+{
+    const int qmax = (1 << (bits - 1)) - 1, qmin = -(1 << (bits - 1));
+    for (int64_t n = 0; n < N; ++n) {
+        const float* v = w + n * ldw;
+        float amax = 0.0f;
+        for (int64_t k = 0; k < K; ++k) {
+            float a = fabsf(v[k]);
+            if (a > amax) amax = a;
+        }
+        float delta = amax / (float)qmax; /* IEEE fp32 division */
+        s[n] = delta;
+        for (int64_t k = 0; k < K; ++k) {
+            int r = 0;
+            if (amax != 0.0f) {
+                r = (int)round_half_away(v[k] / delta);
+                if (r < qmin) r = qmin;
+                if (r > qmax) r = qmax;
+            }
+            q[n * K + k] = (int8_t)r;
+        }
+    }
+}
+
+void oq_pack_rowwise(const int8_t* q, int64_t N, int64_t K, int bits, uint8_t* packed)
+{
+    const int per = 8 / bits, off = 1 << (bits - 1);
+    const int64_t rowb = K / per;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t j = 0; j < rowb; ++j) {
+            unsigned byte = 0;
+            for (int i = 0; i < per; ++i) {
+                unsigned u = (unsigned)(q[n * K + j * per + i] + off);
+                byte |= u << (i * bits);
+            }
+            packed[n * rowb + j] = (uint8_t)byte;
+        }
+}
+
+void oq_unpack_rowwise(const uint8_t* packed, int64_t N, int64_t K, int bits, int8_t* q)
+{
+    const int per = 8 / bits, off = 1 << (bits - 1);
+    const unsigned mask = (1u << bits) - 1u;
+    const int64_t rowb = K / per;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t j = 0; j < rowb; ++j)
+            for (int i = 0; i < per; ++i)
+                q[n * K + j * per + i] = (int8_t)((int)((packed[n * rowb + j] >> (i * bits)) & mask) - off);
+}
+
+/* Per-row codes x Q8_0 activations: y[m][n] = sum_b s[n] * dx[m][b] * dot_b
+   with dot_b the int32 dot over the activation's 32-value block b, combined
+   in double; S[m][n] = sum_b |s[n] * dx[m][b] * dot_b|. */
+void oq_matmul_rowwise_int(const int8_t* qw, const float* s, int64_t N, int64_t K, const int8_t* qx,
+                           const uint16_t* dx, int64_t M, double* y, double* S)
+{
+    int64_t B = K / QK;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t b = 0; b < B; ++b) {
+                int32_t dot = 0;
+                for (int i = 0; i < QK; ++i) dot += (int32_t)qw[n * K + b * QK + i] * (int32_t)qx[m * K + b * QK + i];
+                double t = (double)s[n] * (double)oq_f16_to_f32(dx[m * B + b]) * (double)dot;
+                acc += t;
+                mag += fabs(t);
+            }
+            y[m * N + n] = acc;
+            S[m * N + n] = mag;
+        }
+}
+
+/* Q4_0 weights x fp32 activations, the dequantize-then-FMA flow of the
+   TinyLLaMA guide 6.2 (expand the 4-bit codes, multiply by the block scale,
+   multiply-add with the fp32 activations): y[m][n] = sum_k (dw*qw)[n][k] *
+   x[m][k] in double (each product exact); S[m][n] = sum_k |(dw*qw) x|. */
+void oq_matmul_q4_0_f32(const int8_t* qw, const uint16_t* dw, int64_t N, int64_t K, const float* x, int64_t M,
+                        double* y, double* S)
+{
+    int64_t B = K / QK;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double w = (double)oq_f16_to_f32(dw[n * B + k / QK]) * (double)qw[n * K + k];
+                double t = w * (double)x[m * K + k];
+                acc += t;
+                mag += fabs(t);
+            }
+            y[m * N + n] = acc;
+            S[m * N + n] = mag;
         }
 }
 

@@ -383,3 +383,113 @@ def test_rmsnorm_closed_forms_and_invariants():
     assert np.allclose((y1 ** 2).mean(axis=1), 1.0, rtol=1e-6)
     # eps > 0 shrinks the output towards zero
     assert (np.abs(O.rmsnorm(x, gamma, eps=1.0)) <= np.abs(y)).all()
+
+
+# ----------------------------------------------------------------- per-row int4 / int2 containers
+def test_rowwise_worked_example():
+    g = _golden_kv("rowwise_small.txt")
+    w = np.tile(np.array(g["w"], np.float32), 4)[None]
+    for bits in (4, 2):
+        q, s = O.quantize_rowwise(w, bits)
+        assert s[0] == np.float32(g[f"s{bits}"][0])
+        assert q[0].tolist() == [int(v) for v in g[f"q{bits}"]] * 4
+        packed = O.pack_rowwise(q, bits)
+        per_pattern = len(g[f"p{bits}"])
+        assert packed[0].tolist() == [int(v) for v in g[f"p{bits}"]] * (packed.shape[1] // per_pattern)
+        assert np.array_equal(O.unpack_rowwise(packed, 32, bits), q)
+
+
+def test_rowwise_quantizer_invariants():
+    rng = np.random.default_rng(31)
+    w = (rng.standard_normal((40, 96)) * 0.02).astype(np.float32)
+    w[3] = 0.0  # a zero row
+    w[5, 7] = 1.0  # an outlier
+    for bits in (4, 2):
+        qmax, qmin = 2 ** (bits - 1) - 1, -(2 ** (bits - 1))
+        q, s = O.quantize_rowwise(w, bits)
+        assert q.min() >= qmin and q.max() <= qmax
+        assert s[3] == 0 and (q[3] == 0).all()
+        nz = np.abs(w).max(1) > 0
+        # the scale is amax / qmax in fp32, and the row's largest value reaches +-qmax
+        assert np.array_equal(s, (np.abs(w).max(1) / np.float32(qmax)).astype(np.float32))
+        assert (np.abs(q[nz]).max(1) == qmax).all()
+        # round trip: |w - s q| <= s/2 (up to the fp32 rounding of w/s)
+        err = np.abs(w.astype(np.float64) - s[:, None].astype(np.float64) * q)
+        assert (err <= s[:, None] * (0.5 + 1e-6)).all()
+        # sign symmetry and power-of-two scaling
+        qn, sn = O.quantize_rowwise(-w, bits)
+        assert np.array_equal(qn, -q) and np.array_equal(sn, s)
+        q2, s2 = O.quantize_rowwise(w * 4, bits)
+        assert np.array_equal(q2, q) and np.array_equal(s2, s * 4)
+    # int2 codes are ternary: -2 is never produced (amax/1 maps the extreme to +-1)
+    q, _ = O.quantize_rowwise(w, 2)
+    assert set(np.unique(q)) <= {-1, 0, 1}
+
+
+def test_rowwise_packing_against_bit_loops():
+    rng = np.random.default_rng(32)
+    for bits in (4, 2):
+        per, off = 8 // bits, 2 ** (bits - 1)
+        q = rng.integers(-off, off, (3, 64)).astype(np.int8)  # every code, including -2^(bits-1)
+        packed = O.pack_rowwise(q, bits)
+        for n in range(3):
+            for j in range(64 // per):
+                byte = 0
+                for i in range(per):
+                    byte += (int(q[n, j * per + i]) + off) * (2 ** (bits * i))
+                assert packed[n, j] == byte
+        assert np.array_equal(O.unpack_rowwise(packed, 64, bits), q)
+
+
+def test_matmul_rowwise_int_brute_force_and_q4_0_equivalence():
+    rng = np.random.default_rng(33)
+    N, K, M = 7, 96, 3
+    for bits in (4, 2):
+        off = 2 ** (bits - 1)
+        qw = rng.integers(-off, off, (N, K)).astype(np.int8)
+        s = rng.uniform(0.001, 0.1, N).astype(np.float32)
+        qx = rng.integers(-127, 128, (M, K)).astype(np.int8)
+        dx = O.f32_to_f16_bits(rng.uniform(0.001, 0.1, (M, K // 32)).astype(np.float32))
+        y, S = O.matmul_rowwise_int(qw, s, qx, dx)
+        dxf = np.float16(0) + dx.view(np.float16).astype(np.float64)
+        for m in range(M):
+            for n in range(N):
+                want, mag = 0.0, 0.0
+                for b in range(K // 32):
+                    dot = sum(int(qw[n, 32 * b + i]) * int(qx[m, 32 * b + i]) for i in range(32))
+                    want += float(s[n]) * dxf[m, b] * dot
+                    mag += abs(float(s[n]) * dxf[m, b] * dot)
+                assert abs(y[m, n] - want) <= 1e-12 * mag and abs(S[m, n] - mag) <= 1e-12 * mag
+    # with every row scale an fp16 value, the per-row product equals the Q4_0
+    # product whose block scales all carry that value (same codes)
+    qw = rng.integers(-8, 8, (N, K)).astype(np.int8)
+    s = (2.0 ** rng.integers(-8, -2, N)).astype(np.float32)
+    dw = np.repeat(O.f32_to_f16_bits(s)[:, None], K // 32, 1)
+    y1, S1 = O.matmul_rowwise_int(qw, s, qx, dx)
+    y2, S2 = O.matmul_int(qw, dw, qx, dx)
+    assert np.array_equal(y1, y2) and np.array_equal(S1, S2)
+
+
+def test_matmul_q4_0_f32_against_numpy_and_brute_force():
+    rng = np.random.default_rng(34)
+    N, K, M = 9, 128, 2
+    qw = rng.integers(-8, 8, (N, K)).astype(np.int8)
+    dw = O.f32_to_f16_bits(rng.uniform(0.001, 0.05, (N, K // 32)).astype(np.float32))
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    y, S = O.matmul_q4_0_f32(qw, dw, x)
+    wf = np.repeat(dw.view(np.float16).astype(np.float64), 32, 1) * qw
+    want = x.astype(np.float64) @ wf.T
+    mag = np.abs(x.astype(np.float64)) @ np.abs(wf).T
+    assert np.all(np.abs(y - want) <= 1e-13 * mag)
+    assert np.allclose(S, mag, rtol=1e-13)
+    # one (m, n) by a plain loop
+    acc = 0.0
+    for k in range(K):
+        acc += float(np.float16(dw[4, k // 32].view(np.float16))) * int(qw[4, k]) * float(x[1, k])
+    assert abs(y[1, 4] - acc) <= 1e-13 * mag[1, 4]
+    # x = the dequantized Q8_0 of an activation: equals the Q4_0 x Q8_0 integer path
+    xq, xd = O.quantize_q8_0(x)
+    xdeq = (xq.astype(np.float64) * np.repeat(xd.view(np.float16).astype(np.float64), 32, 1)).astype(np.float32)
+    y3, _ = O.matmul_q4_0_f32(qw, dw, xdeq)
+    y4, S4 = O.matmul_int(qw, dw, xq, xd)
+    assert np.all(np.abs(y3 - y4) <= 1e-13 * S4)
