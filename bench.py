@@ -525,11 +525,49 @@ def run_configs(qmm, torch, dev="cuda"):
     for name, N, K in workloads.large_dense_matrices():
         for M in workloads.LARGE_DENSE["M"]:
             line(3, f"large dense {name} {N}x{K}", N, K, M, product(N, K, M, workloads.LARGE_DENSE["sigma"]))
+    for name, N, K in (("gate", 28672, 8192), ("down", 8192, 28672), ("TinyLLaMA gate/up", 11264, 2048)):
+        for variant in ("int4 per-row x Q8_0", "int2 per-row x Q8_0", "Q4_0 x fp32 (dequantize-then-FMA)"):
+            us, wb = format_variant_us(qmm, torch, variant, N, K)
+            d = {"config": 3, "workload": f"format variant, {variant}, {name} {N}x{K}", "N": N, "K": K, "M": 1,
+                 "us_per_call": round(us, 2), "weight_bytes": wb, "weight_GBps": round(wb / us / 1e3, 1),
+                 "pct_of_hbm_peak": round(100 * wb / us / 1e3 / peak, 1), "peak_kind": peak_kind}
+            print(json.dumps(d), flush=True)
+            out.append(d)
     for T in workloads.MOE["T"]:
         r = bench_moe(qmm, torch, T=T)
         print(json.dumps({"config": 4, **r}), flush=True)
         out.append(r)
     return out
+
+
+def format_variant_us(qmm, torch, variant, N, K, dev="cuda"):
+    """Device time per batch-1 call of a weight-format variant (weights
+    rotated over copies larger than L2) and its weight bytes."""
+    w = workloads.weights(N, K, sigma=0.01, seed=0, index=0, device=dev)
+    if variant.startswith("int"):
+        bits = 4 if variant.startswith("int4") else 2
+        q, sc = qmm.quantize_rowwise(w, bits)
+        xq, xd = qmm.quantize_q8_0(workloads.activations(1, K, seed=0, device=dev))
+        wb = N * K * bits // 8 + 4 * N
+
+        def make():
+            q2, s2 = q.clone(), sc.clone()
+            y = torch.empty(N, device=dev)
+            return lambda: qmm.qmm_gemv_rowwise_q8_0(q2, s2, bits, N, K, xq, xd, y)
+    else:
+        q, sc = qmm.quantize_q4_0(w)
+        x = workloads.activations(1, K, seed=0, device=dev)[0].contiguous()
+        wb = workloads.q4_0_bytes(N, K)
+
+        def make():
+            q2, s2 = q.clone(), sc.clone()
+            y = torch.empty(N, device=dev)
+            return lambda: qmm.qmm_gemv_q4_0_f32_fma(q2, s2, N, K, x, y)
+    del w
+    us = _rotated_us(torch, make, wb)
+    del q, sc
+    torch.cuda.empty_cache()
+    return us, wb
 
 
 # ---------------------------------------------------------------------------- CPU oracle baseline

@@ -11,6 +11,7 @@
 
 #include "qmm.h"
 #include "qmm_chain.cuh"
+#include "qmm_internal.h"
 #include "qmm_kernels.cuh"
 #include "qmm_stream.cuh"
 #include "qmm_mma.h"
@@ -62,6 +63,18 @@ const DevInfo* device_info() {
     }
     return d.ok ? &d : nullptr;
 }
+
+}  // namespace
+
+bool qmm::device_facts(int* sms, int* smem_optin) {
+    const DevInfo* d = device_info();
+    if (!d) return false;
+    *sms = d->sms;
+    *smem_optin = d->smem_optin;
+    return true;
+}
+
+namespace {
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

@@ -68,6 +68,9 @@ SIGNATURES = {
     "qmm_moe_gemv_static": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P],
     "qmm_moe_combine": [_P, _P, _I32, _I32, _I64, _P, _P],
     "qmm_moe_router_topk": [_P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P],
+    "qmm_quantize_rowwise": [_P, _I64, _I64, _I64, _I32, _P, _P, _P],
+    "qmm_gemv_rowwise_q8_0": [_P, _P, _I32, _I64, _I64, _P, _P, _P, _P],
+    "qmm_gemv_q4_0_f32_fma": [_P, _P, _I64, _I64, _P, _P, _P],
     "qmm_moe_gemv_pregrouped": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
     "qmm_last_device_error": [_P],
 }
@@ -199,6 +202,21 @@ def qmm_moe_gemv_static(w_qs, w_d, E, N, K, ids, T, k, xq, xd, x_per_slot, y, st
                                     int(x_per_slot), _ptr(y), _stream(stream)), "qmm_moe_gemv_static")
 
 
+def qmm_quantize_rowwise(w, N, K, ldw, bits, w_q, w_s, stream=None):
+    _check(_lib.qmm_quantize_rowwise(_ptr(w), N, K, ldw, bits, _ptr(w_q), _ptr(w_s), _stream(stream)),
+           "qmm_quantize_rowwise")
+
+
+def qmm_gemv_rowwise_q8_0(w_q, w_s, bits, N, K, xq, xd, y, stream=None):
+    _check(_lib.qmm_gemv_rowwise_q8_0(_ptr(w_q), _ptr(w_s), bits, N, K, _ptr(xq), _ptr(xd), _ptr(y), _stream(stream)),
+           "qmm_gemv_rowwise_q8_0")
+
+
+def qmm_gemv_q4_0_f32_fma(w_qs, w_d, N, K, x, y, stream=None):
+    _check(_lib.qmm_gemv_q4_0_f32_fma(_ptr(w_qs), _ptr(w_d), N, K, _ptr(x), _ptr(y), _stream(stream)),
+           "qmm_gemv_q4_0_f32_fma")
+
+
 def qmm_moe_router_topk(logits, T, E, k, ids, gates, workspace=None, workspace_bytes=0, stream=None):
     _check(_lib.qmm_moe_router_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(gates), _ptr(workspace),
                                     workspace_bytes if workspace is not None else 0, _stream(stream)),
@@ -233,6 +251,16 @@ def quantize_q4_0(w: torch.Tensor):
     qs, d = q4_0_planes(N, K, w.device)
     qmm_quantize_q4_0(w, N, K, w.stride(0), qs, d)
     return qs, d
+
+
+def quantize_rowwise(w: torch.Tensor, bits: int):
+    """Per-row-scale int4 (bits=4) or int2 (bits=2) container of w [N][K]:
+    (codes uint8 [N][K*bits/8], scales fp32 [N])."""
+    N, K = w.shape
+    q = torch.empty(N, K * bits // 8, dtype=torch.uint8, device=w.device)
+    s = torch.empty(N, dtype=torch.float32, device=w.device)
+    qmm_quantize_rowwise(w, N, K, w.stride(0), bits, q, s)
+    return q, s
 
 
 def quantize_q8_0(x: torch.Tensor):

@@ -246,6 +246,50 @@ QMM_API qmm_status qmm_gemv_chain(const qmm_gemv_op* ops, int32_t n_ops, void* w
                           void* stream);
 
 /* ---------------------------------------------------------------------
+ * Weight-format variants of the batch-1 product
+ * ------------------------------------------------------------------- */
+
+/* Largest K of qmm_gemv_rowwise_q8_0 and of qmm_gemv_q4_0_f32_fma (the
+ * activation is staged whole in shared memory). */
+#define QMM_ROWWISE_MAX_K 131072
+#define QMM_F32_FMA_MAX_K 49152
+
+/* Per-row-scale int4 / int2 container (Colibri page, "Arquitectura del
+ * Sistema": an int4 container with per-row scales; int4 and int2 packing).
+ * The page fixes no layout; the reading taken: for row n,
+ *   delta = max_k |w[n][k]| / qmax in fp32, qmax = 2^(bits-1) - 1 (the
+ *     llama.cpp guide's section 2.2 rule applied to the whole row);
+ *   q = clamp(round-half-away(w / delta), -2^(bits-1), qmax) (IEEE fp32
+ *     division); a zero row gets delta = 0 and q = 0;
+ *   codes u = q + 2^(bits-1), 8/bits per byte: element k in byte k*bits/8
+ *     at bit (k mod 8/bits)*bits.
+ * w fp32 [N][K] (row stride ldw >= K, 4-byte aligned) -> w_q uint8
+ * [N][K*bits/8], w_s fp32 [N]; device, caller-owned.  bits is 4 or 2;
+ * K % 32 == 0 (bits 4) or K % 64 == 0 (bits 2), else QMM_ERR_SHAPE.
+ * N == 0 is a no-op. */
+QMM_API qmm_status qmm_quantize_rowwise(const float* w, int64_t N, int64_t K, int64_t ldw, int32_t bits,
+                                        uint8_t* w_q, float* w_s, void* stream);
+
+/* y[n] = w_s[n] * sum_b d_x[b] * sum_{i<32} q_w[n][32b+i] * q_x[32b+i]
+ * (batch 1): per-row codes (layout of qmm_quantize_rowwise) times a Q8_0
+ * activation (xq int8 [K], xd fp16 bits [K/32]); the block dots are exact
+ * int32, the combine fp32.  w_q 16-byte aligned, w_s 4, xq 16, xd 2, y 4.
+ * bits 4 or 2; K % 32 == 0 (bits 4) or K % 64 == 0 (bits 2), K <=
+ * QMM_ROWWISE_MAX_K, else QMM_ERR_SHAPE. */
+QMM_API qmm_status qmm_gemv_rowwise_q8_0(const uint8_t* w_q, const float* w_s, int32_t bits, int64_t N, int64_t K,
+                                         const int8_t* xq, const uint16_t* xd, float* y, void* stream);
+
+/* y[n] = sum_k (d_w[n][k/32] * q_w[n][k]) * x[k] (batch 1): Q4_0 planes (the
+ * layout of qmm_gemv_q4_0_q8_0) times an fp32 activation that is not
+ * quantized, the dequantize-then-multiply-add flow of the TinyLLaMA guide,
+ * section 6.2.  fp32 arithmetic: exact codes, one fp32 sum per 16 values,
+ * the block sum times d_w added to the row's running sum.  w_qs 16-byte
+ * aligned, w_d 2, x 16, y 4; K % 32 == 0 and K <= QMM_F32_FMA_MAX_K, else
+ * QMM_ERR_SHAPE. */
+QMM_API qmm_status qmm_gemv_q4_0_f32_fma(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
+                                         const float* x, float* y, void* stream);
+
+/* ---------------------------------------------------------------------
  * MoE expert-grouped GEMV (Colibri page: only the routed experts of each
  * token are applied; sigmoid router, top-k)
  * ------------------------------------------------------------------- */

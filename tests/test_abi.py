@@ -145,6 +145,31 @@ def test_router_and_pregrouped_validation(qmm):
     assert p(A16, A16, 256, 64, 64, 0, 8, A16, A16, 0, A16, A16, n, None) == 0
 
 
+def test_format_variant_validation(qmm):
+    """Per-row int4/int2 quantizer and GEMV, Q4_0 x fp32 FMA GEMV: bits,
+    K multiples, K limits, alignment, all rejected on the host."""
+    A16 = 0x10000
+    q = lambda *a: _call(qmm, "qmm_quantize_rowwise", *a)  # noqa: E731
+    assert q(A16, 4, 64, 64, 3, A16, A16, None) == 1          # bits not 2 or 4
+    assert q(A16, 4, 96, 96, 2, A16, A16, None) == 2          # int2 needs K % 64 == 0
+    assert q(A16, 4, 48, 48, 4, A16, A16, None) == 2          # int4 needs K % 32 == 0
+    assert q(A16, 4, 64, 32, 4, A16, A16, None) == 1          # ldw < K
+    assert q(A16, 0, 64, 64, 4, A16, A16, None) == 0          # N = 0: no-op
+    assert q(A16 + 2, 4, 64, 64, 4, A16, A16, None) == 3
+    g = lambda *a: _call(qmm, "qmm_gemv_rowwise_q8_0", *a)  # noqa: E731
+    assert g(A16, A16, 3, 8, 64, A16, A16, A16, None) == 1
+    assert g(A16, A16, 2, 8, 96, A16, A16, A16, None) == 2
+    assert g(A16, A16, 4, 8, 131072 + 32, A16, A16, A16, None) == 2   # above QMM_ROWWISE_MAX_K
+    assert g(A16 + 8, A16, 4, 8, 64, A16, A16, A16, None) == 3        # codes not 16-byte aligned
+    assert g(A16, A16, 4, 8, 64, A16 + 4, A16, A16, None) == 3        # xq not 16-byte aligned
+    assert g(A16, A16, 4, 0, 64, A16, A16, A16, None) == 1
+    f = lambda *a: _call(qmm, "qmm_gemv_q4_0_f32_fma", *a)  # noqa: E731
+    assert f(A16, A16, 8, 48, A16, A16, None) == 2                    # K % 32
+    assert f(A16, A16, 8, 49152 + 32, A16, A16, None) == 2            # above QMM_F32_FMA_MAX_K
+    assert f(A16, A16, 8, 64, A16 + 4, A16, None) == 3                # x not 16-byte aligned
+    assert f(None, A16, 8, 64, A16, A16, None) == 1
+
+
 def test_valid_call_without_gpu_reports_device_error(qmm):
     import torch
     if torch.cuda.is_available():
@@ -155,4 +180,7 @@ def test_valid_call_without_gpu_reports_device_error(qmm):
     arr = (qmm.GemvOp * 1)(qmm.gemv_op(A16, A16, 64, 256, xq=A16, xd=A16, y=A16))
     assert qmm.library_handle().qmm_gemv_chain(arr, 1, A16, 16, None) == 4
     assert _call(qmm, "qmm_moe_router_topk", A16, 16, 256, 8, A16, A16, None, 0, None) == 4
+    assert _call(qmm, "qmm_gemv_rowwise_q8_0", A16, A16, 4, 8, 64, A16, A16, A16, None) == 4
+    assert _call(qmm, "qmm_gemv_q4_0_f32_fma", A16, A16, 8, 64, A16, A16, None) == 4
+    assert _call(qmm, "qmm_quantize_rowwise", A16, 4, 64, 64, 2, A16, A16, None) == 4
     assert _call(qmm, "qmm_last_device_error", None) == 4
