@@ -350,6 +350,90 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
             "config": {"workload": c["name"], "T": T, "experts": E, "top_k": k, "hidden": H, "expert_ffn": F}}
 
 
+def bench_moe_store(qmm, torch, T=1, dev="cuda"):
+    """GLM-scale MoE layer with an expert store: all 256 experts (gate, up,
+    down planes; 21.2 MB each) in pinned host memory, 64 of them resident in
+    a slot arena in HBM.  Each decode step: router on the device, its expert
+    ids to the host, store request (copies of missing experts on a copy
+    stream), ids remapped to slots, the layer on the arena, release.  Routing
+    is skewed by a fixed per-expert bias.  Timed end to end (the host reads
+    each step's ids), after as many warm-up steps as timed ones."""
+    import numpy as np
+    c = workloads.MOE
+    H, F, E, k = c["hidden"], c["expert_ffn"], c["experts"], c["top_k"]
+    S, steps = c["store_slots"], c["store_steps"]
+    shapes = {"gate": (F, H), "up": (F, H), "down": (H, F)}
+    host, arena = {}, {}
+    for j, (name, (N, K)) in enumerate(shapes.items()):
+        hq = torch.empty(E, N, K // 2, dtype=torch.uint8, pin_memory=True)
+        hd = torch.empty(E, N, K // 32, dtype=torch.int16, pin_memory=True)
+        tq = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
+        td = torch.empty(N, K // 32, dtype=torch.int16, device=dev)
+        for e in range(E):
+            w = workloads.weights(N, K, sigma=c["sigma"], seed=0, index=1000 * j + e, device=dev)
+            qmm.qmm_quantize_q4_0(w, N, K, K, tq, td)
+            hq[e].copy_(tq)
+            hd[e].copy_(td)
+        host[name] = (hq, hd)
+        arena[name] = (torch.empty(S, N, K // 2, dtype=torch.uint8, device=dev),
+                       torch.empty(S, N, K // 32, dtype=torch.int16, device=dev))
+    slot_of = torch.empty(E, dtype=torch.int32, device=dev)
+    planes = [(host[n][i], arena[n][i]) for n in shapes for i in (0, 1)]
+    store = qmm.ExpertStore(E, S, planes, slot_of)
+    bias = workloads.expert_bias(E, scale=c["store_skew"])
+    logits = [(workloads.router_logits(T, E, seed=10 + i) + bias).to(dev) for i in range(2 * steps)]
+    x = workloads.activations(T, H, seed=0, device=dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    slot_ids = torch.empty_like(ids)
+    gts = torch.empty(T, k, device=dev)
+    xq = torch.empty(T, H, dtype=torch.int8, device=dev)
+    xd = torch.empty(T, H // 32, dtype=torch.int16, device=dev)
+    yg, yu = torch.empty(T * k, F, device=dev), torch.empty(T * k, F, device=dev)
+    hq_, hd_ = torch.empty(T * k, F, dtype=torch.int8, device=dev), torch.empty(T * k, F // 32, dtype=torch.int16, device=dev)
+    z, y = torch.empty(T * k, H, device=dev), torch.empty(T, H, device=dev)
+    wsb = qmm.qmm_moe_workspace_size(E, T, k)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    ids_host = torch.empty(T, k, dtype=torch.int32, pin_memory=True)
+    compute, copy = torch.cuda.current_stream(), torch.cuda.Stream()
+
+    def step(lg):
+        qmm.qmm_moe_router_topk(lg, T, E, k, ids, gts)
+        ids_host.copy_(ids, non_blocking=True)
+        torch.cuda.current_stream().synchronize()  # the host needs the ids to drive the copies
+        store.request(ids_host.view(-1).tolist(), compute, copy)
+        store.map_ids(ids, slot_ids)
+        qmm.qmm_quantize_q8_0(x, T, H, H, xq, xd)
+        ag, au, ad = arena["gate"], arena["up"], arena["down"]
+        qmm.qmm_moe_gemv(ag[0], ag[1], S, F, H, slot_ids, T, k, xq, xd, 0, yg, ws, wsb)
+        qmm.qmm_moe_gemv_pregrouped(au[0], au[1], S, F, H, T, k, xq, xd, 0, yu, ws, wsb)
+        qmm.qmm_swiglu_quantize_q8_0(yg, yu, T * k, F, F, hq_, hd_)
+        qmm.qmm_moe_gemv_pregrouped(ad[0], ad[1], S, H, F, T, k, hq_, hd_, 1, z, ws, wsb)
+        qmm.qmm_moe_combine(z, gts, T, k, H, y)
+        store.release(compute)
+
+    for i in range(steps):  # warm the store
+        step(logits[i])
+    torch.cuda.synchronize()
+    s0 = store.stats()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(compute)
+    for i in range(steps, 2 * steps):
+        step(logits[i])
+    e1.record(compute)
+    torch.cuda.synchronize()
+    per = e0.elapsed_time(e1) / 1e3 / steps
+    s1 = store.stats()
+    hits, misses = s1["hits"] - s0["hits"], s1["misses"] - s0["misses"]
+    copied = s1["bytes_copied"] - s0["bytes_copied"]
+    assert qmm.qmm_last_device_error() == 0
+    return {"metric": "MoE layer with expert store, ms per decode step", "value": round(per * 1e3, 4), "unit": "ms",
+            "tokens_per_s": round(T / per, 1), "hit_rate": round(hits / max(1, hits + misses), 3),
+            "h2d_bytes_per_step": int(copied / steps), "h2d_GBps_avg": round(copied / steps / per / 1e9, 1),
+            "config": {"workload": c["name"] + ", expert store", "T": T, "experts": E, "top_k": k,
+                       "slots_in_hbm": S, "expert_bytes": 3 * workloads.q4_0_bytes(F, H), "routing_skew": c["store_skew"],
+                       "steps": steps}}
+
+
 # ---------------------------------------------------------------------------- single-kernel cases
 def run_case(qmm, torch, name, calls, dev="cuda"):
     """One kernel of the path on one workload shape, called `calls` times
@@ -368,6 +452,8 @@ def run_case(qmm, torch, name, calls, dev="cuda"):
         M = 16 if name == "gemm_b16" else 64
     elif name == "moe_T16":
         return _moe_case(qmm, torch, calls, dev)
+    elif name == "moe_store":
+        return {"case": name, **bench_moe_store(qmm, torch, T=1)}
     elif name in ("decode_chain", "decode_pdl"):  # the whole TinyLLaMA-shaped decode step
         dec = TinyLlamaDecode(qmm, torch)
         ts = _time_calls(torch, dec.chain_step if name == "decode_chain" else dec.step, calls)
@@ -537,6 +623,9 @@ def run_configs(qmm, torch, dev="cuda"):
         r = bench_moe(qmm, torch, T=T)
         print(json.dumps({"config": 4, **r}), flush=True)
         out.append(r)
+    r = bench_moe_store(qmm, torch, T=1)
+    print(json.dumps({"config": 4, **r}), flush=True)
+    out.append(r)
     return out
 
 
@@ -627,7 +716,7 @@ def main():
     ap.add_argument("--case", default=None,
                     help="time one kernel instead: decode_gateup, decode_qkv_norm, decode_chain, decode_pdl, lm_head_8192, "
                          "gemm_b16, "
-                         "gemm_b64, moe_T16")
+                         "gemm_b64, moe_T16, moe_store")
     args = ap.parse_args()
     ws, rank, local = _dist()
 

@@ -66,6 +66,11 @@ const DevInfo* device_info() {
 
 }  // namespace
 
+int* qmm::device_error_word() {
+    const DevInfo* d = device_info();
+    return d ? d->err : nullptr;
+}
+
 bool qmm::device_facts(int* sms, int* smem_optin) {
     const DevInfo* d = device_info();
     if (!d) return false;

@@ -49,6 +49,12 @@ class GemvOp(ctypes.Structure):
                 ("flags", ctypes.c_int32)]
 
 
+class StorePlane(ctypes.Structure):
+    """qmm_store_plane of include/qmm.h (one plane of every expert)."""
+    _fields_ = [("host", ctypes.c_void_p), ("host_stride", ctypes.c_int64), ("dev", ctypes.c_void_p),
+                ("bytes", ctypes.c_int64)]
+
+
 # name -> argtypes (the trailing stream is a void*)
 SIGNATURES = {
     "qmm_quantize_q4_0": [_P, _I64, _I64, _I64, _P, _P, _P],
@@ -69,6 +75,16 @@ SIGNATURES = {
     "qmm_moe_combine": [_P, _P, _I32, _I32, _I64, _P, _P],
     "qmm_moe_router_topk": [_P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P],
     "qmm_quantize_rowwise": [_P, _I64, _I64, _I64, _I32, _P, _P, _P],
+    "qmm_lru_create": [_I32, _I32, ctypes.POINTER(_P)],
+    "qmm_lru_request": [_P, _P, _I32, _I32, _P, _P, _P, _P],
+    "qmm_lru_stats": [_P, _P, _P, _P, _P],
+    "qmm_lru_slot_of": [_P, _I32, _P],
+    "qmm_store_create": [_I32, _I32, ctypes.POINTER(StorePlane), _I32, _P, ctypes.POINTER(_P)],
+    "qmm_store_request": [_P, _P, _I32, _P, _P],
+    "qmm_store_release": [_P, _P],
+    "qmm_store_prefetch": [_P, _P, _I32, _P],
+    "qmm_store_map_ids": [_P, _P, _I64, _P, _P],
+    "qmm_store_stats": [_P, _P, _P, _P, _P, _P],
     "qmm_gemv_rowwise_q8_0": [_P, _P, _I32, _I64, _I64, _P, _P, _P, _P],
     "qmm_gemv_q4_0_f32_fma": [_P, _P, _I64, _I64, _P, _P, _P],
     "qmm_moe_gemv_pregrouped": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
@@ -78,6 +94,9 @@ for _name, _args in SIGNATURES.items():
     _f = getattr(_lib, _name)
     _f.argtypes = _args
     _f.restype = ctypes.c_int
+for _name in ("qmm_lru_destroy", "qmm_store_destroy"):
+    getattr(_lib, _name).argtypes = [_P]
+    getattr(_lib, _name).restype = None
 _lib.qmm_status_string.argtypes = [ctypes.c_int]
 _lib.qmm_status_string.restype = ctypes.c_char_p
 _lib.qmm_abi_version.argtypes = []
@@ -215,6 +234,88 @@ def qmm_gemv_rowwise_q8_0(w_q, w_s, bits, N, K, xq, xd, y, stream=None):
 def qmm_gemv_q4_0_f32_fma(w_qs, w_d, N, K, x, y, stream=None):
     _check(_lib.qmm_gemv_q4_0_f32_fma(_ptr(w_qs), _ptr(w_d), N, K, _ptr(x), _ptr(y), _stream(stream)),
            "qmm_gemv_q4_0_f32_fma")
+
+
+def _i32_array(values):
+    values = [int(v) for v in values]
+    return (ctypes.c_int32 * max(1, len(values)))(*values), len(values)
+
+
+class Lru:
+    """qmm_lru: the store's host-side LRU policy on its own (no device)."""
+
+    def __init__(self, n_keys, n_slots):
+        h = ctypes.c_void_p()
+        _check(_lib.qmm_lru_create(n_keys, n_slots, ctypes.byref(h)), "qmm_lru_create")
+        self._h = h
+
+    def request(self, keys, use=True):
+        """Returns (slot of each key, [(key, slot) loads in order])."""
+        arr, n = _i32_array(keys)
+        slots = (ctypes.c_int32 * max(1, n))()
+        lk = (ctypes.c_int32 * max(1, n))()
+        ls = (ctypes.c_int32 * max(1, n))()
+        nl = ctypes.c_int32()
+        _check(_lib.qmm_lru_request(self._h, arr, n, 1 if use else 0, slots, lk, ls, ctypes.byref(nl)),
+               "qmm_lru_request")
+        return list(slots[:n]), list(zip(lk[:nl.value], ls[:nl.value]))
+
+    def slot_of(self, key):
+        s = ctypes.c_int32()
+        _check(_lib.qmm_lru_slot_of(self._h, key, ctypes.byref(s)), "qmm_lru_slot_of")
+        return s.value
+
+    def stats(self):
+        v = [ctypes.c_int64() for _ in range(4)]
+        _check(_lib.qmm_lru_stats(self._h, *[ctypes.byref(x) for x in v]), "qmm_lru_stats")
+        return dict(zip(("hits", "misses", "evictions", "prefetched"), (x.value for x in v)))
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            _lib.qmm_lru_destroy(self._h)
+            self._h = None
+
+
+class ExpertStore:
+    """qmm_store: experts in host memory, n_slots of them resident on the
+    device.  planes: list of (host tensor [E][...] pinned, device arena
+    tensor [n_slots][...]), each expert's plane contiguous."""
+
+    def __init__(self, E, n_slots, planes, dev_slot_of):
+        arr = (StorePlane * len(planes))()
+        for i, (host, dev) in enumerate(planes):
+            nbytes = dev[0].numel() * dev.element_size()
+            arr[i] = StorePlane(host.data_ptr(), host[0].numel() * host.element_size(), dev.data_ptr(), nbytes)
+        h = ctypes.c_void_p()
+        _check(_lib.qmm_store_create(E, n_slots, arr, len(planes), _ptr(dev_slot_of), ctypes.byref(h)),
+               "qmm_store_create")
+        self._h, self._keep = h, (planes, dev_slot_of)
+
+    def request(self, ids, compute_stream=None, copy_stream=None):
+        arr, n = _i32_array(ids)
+        _check(_lib.qmm_store_request(self._h, arr, n, _stream(compute_stream), _stream(copy_stream)),
+               "qmm_store_request")
+
+    def release(self, compute_stream=None):
+        _check(_lib.qmm_store_release(self._h, _stream(compute_stream)), "qmm_store_release")
+
+    def prefetch(self, ids, copy_stream=None):
+        arr, n = _i32_array(ids)
+        _check(_lib.qmm_store_prefetch(self._h, arr, n, _stream(copy_stream)), "qmm_store_prefetch")
+
+    def map_ids(self, ids, slot_ids, stream=None):
+        _check(_lib.qmm_store_map_ids(self._h, _ptr(ids), ids.numel(), _ptr(slot_ids), _stream(stream)),
+               "qmm_store_map_ids")
+
+    def stats(self):
+        v = [ctypes.c_int64() for _ in range(5)]
+        _check(_lib.qmm_store_stats(self._h, *[ctypes.byref(x) for x in v]), "qmm_store_stats")
+        return dict(zip(("hits", "misses", "evictions", "prefetched", "bytes_copied"), (x.value for x in v)))
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            _lib.qmm_store_destroy(self._h)
+            self._h = None
 
 
 def qmm_moe_router_topk(logits, T, E, k, ids, gates, workspace=None, workspace_bytes=0, stream=None):

@@ -356,6 +356,94 @@ QMM_API qmm_status qmm_moe_combine(const float* z, const float* gates, int32_t T
                            void* stream);
 
 /* ---------------------------------------------------------------------
+ * Expert hot-store (Colibri page, "Arquitectura del Sistema": a
+ * least-recently-used cache of experts per layer, an optional hot store in
+ * RAM or VRAM, and a prefetcher that asks ahead for the experts the next
+ * layer will use).  Host memory holds every expert; the device keeps
+ * n_slots of them in a slot arena that the MoE entries read: remap the
+ * router's expert ids to slot ids (qmm_store_map_ids) and pass the arena
+ * as the expert tensor with E = n_slots.
+ * ------------------------------------------------------------------- */
+
+/* A host-side LRU over keys 0..n_keys-1 and slots 0..n_slots-1 (the
+ * policy of the store, usable on its own; no device needed).
+ *  - A use request (use != 0) needs its keys now: its distinct keys must
+ *    fit in the slots, else QMM_ERR_SHAPE and nothing changes.  Each
+ *    distinct key counts once as a hit or a miss.  All its keys are
+ *    protected from eviction until the next use request.  Keys become most
+ *    recent in request order.
+ *  - A prefetch (use == 0) loads absent keys into slots holding no key of
+ *    the last use request (a key that finds none gets slot -1) and makes
+ *    resident keys most recent.
+ *  - A load takes a never-used slot (slot 0 first), else the least recently
+ *    used slot that is not protected.
+ * slots_out [n] (slot of each key), load_keys / load_slots [n] (the loads,
+ * in order) and n_loads may each be NULL.  Keys out of range: QMM_ERR_ARG. */
+typedef struct qmm_lru qmm_lru;
+QMM_API qmm_status qmm_lru_create(int32_t n_keys, int32_t n_slots, qmm_lru** out);
+QMM_API void qmm_lru_destroy(qmm_lru* lru);
+QMM_API qmm_status qmm_lru_request(qmm_lru* lru, const int32_t* keys, int32_t n, int32_t use, int32_t* slots_out,
+                                   int32_t* load_keys, int32_t* load_slots, int32_t* n_loads);
+QMM_API qmm_status qmm_lru_stats(const qmm_lru* lru, int64_t* hits, int64_t* misses, int64_t* evictions,
+                                 int64_t* prefetched);
+/* Slot of a key, -1 when it is not resident. */
+QMM_API qmm_status qmm_lru_slot_of(const qmm_lru* lru, int32_t key, int32_t* slot);
+
+/* One plane of every expert (e.g. the nibble plane of the gate matrix):
+ * expert e is `bytes` bytes at host + e * host_stride (host memory, pinned
+ * for asynchronous copies; caller-owned, valid for the store's life), and
+ * slot s is `bytes` bytes at dev + s * bytes (device arena of n_slots *
+ * bytes, caller-owned). */
+typedef struct qmm_store_plane {
+    const void* host;
+    int64_t host_stride;
+    void* dev;
+    int64_t bytes;
+} qmm_store_plane;
+
+#define QMM_STORE_MAX_PLANES 16
+
+typedef struct qmm_store qmm_store;
+
+/* A store of E experts in n_slots device slots (n_slots <= E), n_planes
+ * planes per expert (<= QMM_STORE_MAX_PLANES).  dev_slot_of: device int32
+ * [E], caller-owned, kept by the store (slot of each expert or -1); set to
+ * all -1 here (synchronously).  Needs an sm_103 device (the current one). */
+QMM_API qmm_status qmm_store_create(int32_t E, int32_t n_slots, const qmm_store_plane* planes, int32_t n_planes,
+                                    int32_t* dev_slot_of, qmm_store** out);
+/* Frees the store's host state and events (not the caller's buffers).
+ * Work already enqueued stays valid. */
+QMM_API void qmm_store_destroy(qmm_store* store);
+
+/* Makes experts ids[0..n) (host array, duplicates allowed) resident for
+ * work enqueued next on compute_stream: a use request of the LRU; each
+ * missing expert is copied into its slot with one cudaMemcpyAsync per plane
+ * on copy_stream, after the compute stream has passed the release of every
+ * earlier request that used that slot; compute_stream then waits for the
+ * copies, and the device slot table is updated on compute_stream.  The
+ * host does not wait.  copy_stream may equal compute_stream (no overlap).
+ * More distinct experts than slots: QMM_ERR_SHAPE, nothing changes. */
+QMM_API qmm_status qmm_store_request(qmm_store* store, const int32_t* ids, int32_t n, void* compute_stream,
+                                     void* copy_stream);
+/* Marks the end of the last request's use of its slots: call after
+ * enqueuing the work that reads them (on the same compute stream).  If it
+ * is not called, the next request does it first. */
+QMM_API qmm_status qmm_store_release(qmm_store* store, void* compute_stream);
+/* Starts copying experts ids[0..n) (host array) that are absent, on
+ * copy_stream, into slots holding no expert of the last request (the
+ * prefetch of the page's next-layer prediction).  They become usable by the
+ * next qmm_store_request, which waits for these copies. */
+QMM_API qmm_status qmm_store_prefetch(qmm_store* store, const int32_t* ids, int32_t n, void* copy_stream);
+/* slot_ids[i] = slot of expert ids[i] (device int32 arrays of n): the ids
+ * of the expert GEMV for the slot arena.  An expert that is not resident
+ * maps to -1 and sets the device error word (QMM_ERR_BAD_EXPERT_ID); the
+ * MoE entries then skip that slot. */
+QMM_API qmm_status qmm_store_map_ids(qmm_store* store, const int32_t* ids, int64_t n, int32_t* slot_ids,
+                                     void* stream);
+QMM_API qmm_status qmm_store_stats(const qmm_store* store, int64_t* hits, int64_t* misses, int64_t* evictions,
+                                   int64_t* prefetched, int64_t* bytes_copied);
+
+/* ---------------------------------------------------------------------
  * MoE expert GEMV without a caller workspace.  A library addition: the
  * pages have no counterpart (they say nothing about device memory).
  * ------------------------------------------------------------------- */

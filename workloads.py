@@ -55,6 +55,15 @@ def router_logits(T: int, E: int, seed: int = 0, index: int = 900, device="cpu")
     return torch.randn(T, E, generator=g, device=device, dtype=torch.float32)
 
 
+def expert_bias(E: int, scale: float = 1.5, seed: int = 0, index: int = 901, device="cpu") -> torch.Tensor:
+    """A fixed per-expert offset of the router logits, scale * N(0, 1): some
+    experts are routed to much more often than others, which is what gives an
+    expert cache its hits (the pages give no routing statistics; this skew is
+    a synthetic stand-in)."""
+    g = _gen(seed, index, device)
+    return scale * torch.randn(E, generator=g, device=device, dtype=torch.float32)
+
+
 def norm_weights(K: int, seed: int = 0, index: int = 700, device="cpu") -> torch.Tensor:
     g = _gen(seed, index, device)
     return 1.0 + 0.1 * torch.randn(K, generator=g, device=device, dtype=torch.float32)
@@ -85,7 +94,9 @@ LARGE_DENSE = {"name": "large dense decode (hidden 8192, FFN 28672, vocab 128256
 # GLM-scale MoE layer: hidden 6144, 256 experts of gate/up 6144 -> 2048 and
 # down 2048 -> 6144, sigmoid router, top-8.
 MOE = {"name": "GLM-scale MoE expert layer", "hidden": 6144, "expert_ffn": 2048, "experts": 256,
-       "top_k": 8, "T": [1, 16], "sigma": 0.02}
+       "top_k": 8, "T": [1, 16], "sigma": 0.02,
+       # expert store: slots in HBM, decode steps timed, skew of the routing
+       "store_slots": 64, "store_steps": 64, "store_skew": 1.5}
 
 
 def tinyllama_matrices():
