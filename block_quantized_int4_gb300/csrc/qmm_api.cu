@@ -161,7 +161,7 @@ bool valid_k(int64_t K) { return K > 0 && K % QK == 0 && K <= (int64_t)1 << 30; 
 // segments (B % 8 == 0, i.e. K % 256 == 0; d 16-byte aligned) and the staged
 // activation tile fits.
 constexpr int STREAM_XTILE_CAP = 64 * 1024;
-constexpr int64_t CHAIN_MATRIX_BYTES = 64ll << 20;  // below this, leave room for a neighbour CTA
+constexpr int64_t CHAIN_MATRIX_BYTES = 16ll << 20;  // up to this, one CTA per SM and room for a neighbour CTA
 
 bool stream_eligible(int64_t N, int64_t K, const void* qs, const void* d, int MT) {
     const int64_t B = K / QK;
@@ -190,17 +190,29 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
 #endif
     const bool chain_sized = a.N * row_bytes <= CHAIN_MATRIX_BYTES;
     const int64_t ctas = chain_sized ? di->sms : QMM_STREAM_BIG_CTAS_PER_SM * (int64_t)di->sms;
-    const int64_t rpc = round_up((a.N + ctas - 1) / ctas, align);
+    // A CTA's weights arrive through its one producer lane, so in a decode
+    // chain fewer bytes per CTA finish sooner: a Q8_0-output launch takes the
+    // smallest whole-block row count that keeps about two CTAs per SM at most
+    // (TinyLLaMA gate/up: 176 CTAs of 64 rows instead of 88 of 128; the decode
+    // step measured 462 -> 422 us).
+    const int64_t rpc = chain_sized && qout
+                            ? std::max<int64_t>(align, round_up((a.N + 2 * ctas - 1) / (2 * ctas), align))
+                            : round_up((a.N + ctas - 1) / ctas, align);
     const int64_t G = (a.N + rpc - 1) / rpc;
     const int rb = (int)std::min<int64_t>(GROUP_ROWS, rpc);
     const int ckb = (int)std::min<int64_t>(CHUNK_KB, B);
     const int64_t xtile = round_up((int64_t)MT * B * xtile_bytes_per_block(), 128);
     const int64_t ybuf = qout ? round_up(rpc / opr * 4, 128) : 0;
     const int64_t nunits = ((rpc + rb - 1) / rb) * ((B + ckb - 1) / ckb);
-    // Small matrices (decode chains): stay under ~110 KB so the next chained
-    // kernel's CTA can be resident and prefetch beside this one.
-    const int64_t cap = chain_sized ? 110 * 1024 : QMM_STREAM_BIG_SMEM_KB * 1024;  // two CTAs fit on one SM
-    const int64_t room = (cap - STREAM_HDR - xtile - ybuf) / STAGE_BYTES;
+    // a ring stage holds one TMA box pair (rb rows x ckb blocks): sized to it,
+    // so short row groups leave room for more stages
+    const int64_t stage_q = round_up((int64_t)rb * ckb * 16, 128);
+    const int64_t stage_bytes = stage_q + round_up((int64_t)rb * ckb * 2, 128);
+    // Small matrices (decode chains): stay under ~112 KB so the next chained
+    // kernel's CTA is resident beside this one and prefetches its weights
+    // (two such CTAs and their 1 KB reservations fill the SM's 228 KB).
+    const int64_t cap = chain_sized ? 112 * 1024 : QMM_STREAM_BIG_SMEM_KB * 1024;
+    const int64_t room = (cap - STREAM_HDR - xtile - ybuf) / stage_bytes;
     const int64_t nst = std::min<int64_t>({nunits, room, (int64_t)STREAM_MAX_STAGES});
     if (nst < 1) return QMM_ERR_SHAPE;
     CUtensorMap mq, md;
@@ -209,8 +221,10 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
         !make_tensor_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT16, d, (uint64_t)B, (uint64_t)a.N, (uint64_t)B * 2,
                             (uint32_t)ckb, (uint32_t)rb, CU_TENSOR_MAP_SWIZZLE_NONE))
         return QMM_ERR_CUDA;
-    const int smem = (int)(STREAM_HDR + xtile + nst * STAGE_BYTES + ybuf);
+    const int smem = (int)(STREAM_HDR + xtile + nst * stage_bytes + ybuf);
     a.rows_per_cta = (int)rpc;
+    a.stage_bytes = (int)stage_bytes;
+    a.stage_q = (int)stage_q;
     a.rb = rb;
     a.ckb = ckb;
     a.nstages = (int)nst;

@@ -72,6 +72,8 @@ struct StreamArgs {
     int rb;              // rows per group = TMA box rows (even, <= 32)
     int ckb;             // K blocks per chunk = TMA box width in blocks (multiple of 8, <= 64)
     int nstages;
+    int stage_bytes;     // ring stage: nibbles of rb x ckb blocks, then their scales (each part 128-aligned)
+    int stage_q;         // offset of the scales in a stage
     int xtile_bytes;     // multiple of 128
     int* err;
 };
@@ -95,16 +97,23 @@ struct Quad4 {
     float d[4];
 };
 
-__device__ __forceinline__ Quad4 quad_load(const uint8_t* q, int qrs, const uint16_t* dd, int drs) {
+// Rows 16 and 17 further on are read only when the stage holds them (hi):
+// a stage sized to a short row group ends before them.
+__device__ __forceinline__ Quad4 quad_load(const uint8_t* q, int qrs, const uint16_t* dd, int drs, bool hi = true) {
     Quad4 r;
     r.w[0] = lds128(q);
     r.w[1] = lds128(q + qrs);
-    r.w[2] = lds128(q + 16 * qrs);
-    r.w[3] = lds128(q + 17 * qrs);
     r.d[0] = f16_bits_to_f32(dd[0]);
     r.d[1] = f16_bits_to_f32(dd[drs]);
-    r.d[2] = f16_bits_to_f32(dd[16 * drs]);
-    r.d[3] = f16_bits_to_f32(dd[17 * drs]);
+    if (hi) {
+        r.w[2] = lds128(q + 16 * qrs);
+        r.w[3] = lds128(q + 17 * qrs);
+        r.d[2] = f16_bits_to_f32(dd[16 * drs]);
+        r.d[3] = f16_bits_to_f32(dd[17 * drs]);
+    } else {
+        r.w[2] = r.w[3] = make_uint4(0u, 0u, 0u, 0u);
+        r.d[2] = r.d[3] = 0.0f;
+    }
     return r;
 }
 
@@ -148,7 +157,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
     const int B = (int)(a.K / QK);
     const XTile xt = xtile_at(smem + STREAM_HDR, MT, B);
     uint8_t* ring = smem + STREAM_HDR + a.xtile_bytes;
-    float* ybuf = reinterpret_cast<float*>(ring + (size_t)a.nstages * STAGE_BYTES);  // QOUT: this CTA's outputs
+    float* ybuf = reinterpret_cast<float*>(ring + (size_t)a.nstages * a.stage_bytes);  // QOUT: this CTA's outputs
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     const int RB = a.rb, CKB = a.ckb;
@@ -186,10 +195,10 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
                 }
                 const int g = u / nkc, kc = u - g * nkc;
                 const int r0 = (int)(row_begin + (int64_t)g * RB);
-                uint8_t* st = ring + (size_t)s * STAGE_BYTES;
+                uint8_t* st = ring + (size_t)s * a.stage_bytes;
                 mbar_arrive_expect_tx(&full[s], unit_bytes);
                 tma_load_2d(st, &map_q, kc * CKB * 4, r0, &full[s], pol);           // u32 columns
-                tma_load_2d(st + STAGE_Q, &map_d, kc * CKB, r0, &full[s], pol);     // fp16 columns
+                tma_load_2d(st + a.stage_q, &map_d, kc * CKB, r0, &full[s], pol);     // fp16 columns
                 issued = u + 1;
             }
             if (!ok) {
@@ -228,6 +237,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
     // this warp's rows inside a group: pairs (2w, 2w+1) and (2w+16, 2w+17),
     // so a gate/up pair always sits in one warp
     const int rA = 2 * warp, rB = 2 * warp + 16;
+    const bool hi_rows = rB < RB;  // the stage holds this warp's second row pair (RB is even)
     const int OPR = ymode == Y_SWIGLU_PAIRS ? 2 : 1;  // rows per output
     bool failed = false;
     for (int g = 0; g < ngroups; ++g) {
@@ -252,12 +262,12 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
             Quad4 qd[H];
             const bool work = ok && rA < nr;
             if (work) {
-                const uint8_t* stq = ring + (size_t)s * STAGE_BYTES + (rA * CKB + lane) * 16;
-                const uint16_t* std_ = reinterpret_cast<const uint16_t*>(ring + (size_t)s * STAGE_BYTES + STAGE_Q) +
+                const uint8_t* stq = ring + (size_t)s * a.stage_bytes + (rA * CKB + lane) * 16;
+                const uint16_t* std_ = reinterpret_cast<const uint16_t*>(ring + (size_t)s * a.stage_bytes + a.stage_q) +
                                        rA * CKB + lane;
 #pragma unroll
                 for (int h = 0; h < H; ++h)
-                    if (lane + 32 * h < nb) qd[h] = quad_load(stq + 512 * h, CKB * 16, std_ + 32 * h, CKB);
+                    if (lane + 32 * h < nb) qd[h] = quad_load(stq + 512 * h, CKB * 16, std_ + 32 * h, CKB, hi_rows);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);  // stage read: the producer may refill it
