@@ -188,16 +188,16 @@ __global__ void __launch_bounds__(STREAM_THREADS, 1) gemv_chain_kernel(const __g
             asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
             failed = failed || *abort_flag;
             const XTile xt = xtile_at(xbase, 1, B);
-            if (!failed) {
-                if (o.xf && o.gamma) {
-                    stage_f32_rmsnorm(xt, o.xf, o.gamma, gr, o.K, o.eps, const_cast<int8_t*>(o.xq),
-                                      const_cast<uint16_t*>(o.xd), reinterpret_cast<float*>(smem + 256), tid, NTHR, 1);
-                } else if (o.xf) {
-                    stage_f32<false>(xt, o.xf, o.K, const_cast<int8_t*>(o.xq), const_cast<uint16_t*>(o.xd), tid,
-                                     NTHR);
-                } else {
-                    chain_stage_q8(xt, o.xq, o.xd, B, tid, NTHR);
-                }
+            // Staged by every consumer thread even after a timeout: the staging
+            // meets named barriers with all of them, and threads may see the
+            // abort flag at different moments (later work is skipped instead).
+            if (o.xf && o.gamma) {
+                stage_f32_rmsnorm(xt, o.xf, o.gamma, gr, o.K, o.eps, const_cast<int8_t*>(o.xq),
+                                  const_cast<uint16_t*>(o.xd), reinterpret_cast<float*>(smem + 256), tid, NTHR, 1);
+            } else if (o.xf) {
+                stage_f32<false>(xt, o.xf, o.K, const_cast<int8_t*>(o.xq), const_cast<uint16_t*>(o.xd), tid, NTHR);
+            } else {
+                chain_stage_q8(xt, o.xq, o.xd, B, tid, NTHR);
             }
             asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
 

@@ -39,27 +39,74 @@ __device__ __forceinline__ float div_rn_fma(float x, float d, float r) {
     return __fmaf_rn(rem, r, q0);
 }
 
+// The code of one value: round-half-away of RN(v / d32), clamped.  fast:
+// d32 inside the range where div_rn_fma with rc = RN(1/d32) is exact.
+__device__ __forceinline__ int code_of(float v, float d32, float rc, bool fast, bool nonzero, float qmax, float qlo) {
+    if (!nonzero) return 0;
+    const float qf = fast ? div_rn_fma(v, d32, rc) : __fdiv_rn(v, d32);
+    return (int)fminf(fmaxf(roundf(qf), qlo), qmax);
+}
+
+// Codes and scale of one block whose values v[] sit in this lane (the
+// block's amax a already reduced over its lanes).  When every lane of the
+// warp has a == 0 or a in [1e-28, 1e30] -- always, for finite activations and
+// weights of sane magnitude -- the scale is RN(a / qmax) by the FMA-corrected
+// quotient with the constant RN(1/qmax) (folded: qmax is a literal at every
+// call), each quotient RN(v / d32) by div_rn_fma, and the rounding is
+// floor(fl(|q| + 1/2)) for |q| >= 1/2, 0 below, which equals round-half-away
+// for every float (checked exhaustively over [0, 256)), with no branch per
+// value.  Otherwise the general path with the IEEE division.
+template <int NV>
+__device__ __forceinline__ void block_codes(const float (&v)[NV], float a, float qmax, float qlo, int (&c)[NV],
+                                            float& d32) {
+    const bool ok = a == 0.0f || (a >= 1.0e-28f && a <= 1.0e30f);
+    if (__all_sync(FULL, ok)) {
+        d32 = div_rn_fma(a, qmax, 1.0f / qmax);  // a == 0 gives 0
+        const float rc = __frcp_rn(a == 0.0f ? 1.0f : d32);
+        const int kpos = (int)qmax, kneg = (int)(-qlo);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const float qf = div_rn_fma(v[i], d32, rc);
+            const float aq = fabsf(qf);
+            const int k = aq < 0.5f ? 0 : __float2int_rd(__fadd_rn(aq, 0.5f));
+            const int cv = qf < 0.0f ? -min(k, kneg) : min(k, kpos);
+            c[i] = a == 0.0f ? 0 : cv;
+        }
+    } else {
+        d32 = __fdiv_rn(a, qmax);
+        // d32 in [2^-100, 1e30] keeps 1/d32 and every quotient (|x/d32| <= qmax) in range
+        const bool fast = d32 >= 7.8886091e-31f && d32 <= 1.0e30f;
+        const float rc = fast ? __frcp_rn(d32) : 0.f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) c[i] = code_of(v[i], d32, rc, fast, a != 0.0f, qmax, qlo);
+    }
+}
+
 __device__ __forceinline__ Quad quad_codes(float4 v, float qmax, float qlo) {
     float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     a = fmaxf(a, __shfl_xor_sync(FULL, a, 1));
     a = fmaxf(a, __shfl_xor_sync(FULL, a, 2));
     a = fmaxf(a, __shfl_xor_sync(FULL, a, 4));
     Quad r;
-    r.d32 = __fdiv_rn(a, qmax);
     const float vv[4] = {v.x, v.y, v.z, v.w};
-    // d32 in [2^-100, 1e30] keeps 1/d32 and every quotient (|x/d32| <= qmax) in range
-    const bool fast = r.d32 >= 7.8886091e-31f && r.d32 <= 1.0e30f;
-    const float rc = fast ? __frcp_rn(r.d32) : 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        if (a != 0.0f) {
-            const float qf = fast ? div_rn_fma(vv[i], r.d32, rc) : __fdiv_rn(vv[i], r.d32);
-            const float t = roundf(qf);
-            r.c[i] = (int)fminf(fmaxf(t, qlo), qmax);
-        } else {
-            r.c[i] = 0;
-        }
-    }
+    block_codes<4>(vv, a, qmax, qlo, r.c, r.d32);
+    return r;
+}
+
+// The same with a block spread over 4 lanes of 8 values each (lanes 4k..4k+3).
+struct Oct {
+    int c[8];
+    float d32;
+};
+
+__device__ __forceinline__ Oct oct_codes(float4 u, float4 w, float qmax, float qlo) {
+    float a = fmaxf(fmaxf(fmaxf(fabsf(u.x), fabsf(u.y)), fmaxf(fabsf(u.z), fabsf(u.w))),
+                    fmaxf(fmaxf(fabsf(w.x), fabsf(w.y)), fmaxf(fabsf(w.z), fabsf(w.w))));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(FULL, a, 2));
+    Oct r;
+    const float vv[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
+    block_codes<8>(vv, a, qmax, qlo, r.c, r.d32);
     return r;
 }
 
@@ -269,34 +316,40 @@ __device__ __forceinline__ void stage_f32(const XTile& xt, const float* __restri
                                           int nthr, const float* gamma = nullptr, float inv = 1.0f);
 
 // RMSNorm + Q8_0 of one activation row into tile row 0 (TinyLLaMA guide
-// 4.1), for rows of at most RMS_STEPS * 4 blocks per warp: the gamma values
-// a thread needs are loaded first (rms_gamma_load -- they do not depend on
-// the activation, so a kernel loads them before it waits for the producer of
-// x); then every x value is loaded once into registers, the sum of squares
-// is taken from the registers in a fixed order (each lane over its values,
-// then butterfly within the warp, then the warps in order), and the
-// normalized values x_i * inv * gamma_i are quantized from the registers.
-// Longer rows take rms_inv + stage_f32 (two passes).  Threads [0, nthr) of
-// the CTA, named barrier `bar`; red: 33 floats of shared memory.  CTA 0
-// writes the Q8_0 row out when xq_out/xd_out are given.
-constexpr int RMS_STEPS = 4;
+// 4.1), for rows of at most RMS_STEPS * nthr / 4 blocks (each block on 4
+// lanes of 8 values): the gamma values a thread needs are loaded first
+// (rms_gamma_load -- they do not depend on the activation, so a kernel loads
+// them before it waits for the producer of x); then every x value is loaded
+// once into registers, the sum of squares is taken from the registers in a
+// fixed order (each lane over its values, then butterfly within the warp,
+// then the warps in order).  The codes are those of z_i = x_i * gamma_i (a
+// block's codes are the same for any positive multiple of it), formed while
+// warp 0 forms 1/rms; each block's scale is then d_z * 1/rms.  Longer rows
+// take rms_inv + stage_f32 (two passes).  Threads [0, nthr) of the CTA,
+// named barriers bar (by the caller), bar+1 and bar+2; red: 33 floats of
+// shared memory.  CTA 0 writes the Q8_0 row out when xq_out/xd_out are given.
+constexpr int RMS_STEPS = 2;  // blocks per thread group of 4 in the one-pass staging
 
 struct RmsGamma {
-    float4 g[RMS_STEPS];
+    float4 g[2 * RMS_STEPS];
 };
 
-__device__ __forceinline__ bool rms_one_pass(int64_t K, int nthr) { return K / QK <= (nthr >> 5) * 4 * RMS_STEPS; }
+// One pass when every block has its 4 lanes: K / 32 <= RMS_STEPS * nthr / 4.
+__device__ __forceinline__ bool rms_one_pass(int64_t K, int nthr) { return K / QK <= RMS_STEPS * (nthr >> 2); }
 
+// Thread t takes, in step i, values 8p..8p+7 (p = t & 3) of block
+// i * nthr/4 + t/4.
 __device__ __forceinline__ RmsGamma rms_gamma_load(const float* gamma, int64_t K, int tid, int nthr) {
     RmsGamma r;
     const int B = (int)(K / QK);
-    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    const int p = tid & 3;
 #pragma unroll
     for (int i = 0; i < RMS_STEPS; ++i) {
-        const int b = (warp + i * nwarps) * 4 + (lane >> 3);
-        r.g[i] = b < B && rms_one_pass(K, nthr)
-                     ? __ldg(reinterpret_cast<const float4*>(gamma + (int64_t)b * QK + (lane & 7) * 4))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int b = i * (nthr >> 2) + (tid >> 2);
+        const bool in = b < B && rms_one_pass(K, nthr);
+        const float* g = gamma + (int64_t)b * QK + p * 8;
+        r.g[2 * i] = in ? __ldg(reinterpret_cast<const float4*>(g)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        r.g[2 * i + 1] = in ? __ldg(reinterpret_cast<const float4*>(g + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     return r;
 }
@@ -311,58 +364,81 @@ __device__ __forceinline__ void stage_f32_rmsnorm(const XTile& xt, const float* 
         stage_f32<false>(xt, x, K, xq_out, xd_out, tid, nthr, gamma, inv);
         return;
     }
-    const int part = lane & 7;
+    const int p = tid & 3;
     const bool writer = blockIdx.x == 0 && blockIdx.y == 0;
-    float4 v[RMS_STEPS];
+    float4 v[2 * RMS_STEPS];
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < RMS_STEPS; ++i) {
-        const int b = (warp + i * nwarps) * 4 + (lane >> 3);
-        v[i] = b < B ? __ldcg(reinterpret_cast<const float4*>(x + (int64_t)b * QK + part * 4))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int b = i * (nthr >> 2) + (tid >> 2);
+        const float* xb = x + (int64_t)b * QK + p * 8;
+        v[2 * i] = b < B ? __ldcg(reinterpret_cast<const float4*>(xb)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[2 * i + 1] = b < B ? __ldcg(reinterpret_cast<const float4*>(xb + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int i = 0; i < RMS_STEPS; ++i) {
+    for (int i = 0; i < 2 * RMS_STEPS; ++i) {
         ss = __fmaf_rn(v[i].x, v[i].x, ss);
         ss = __fmaf_rn(v[i].y, v[i].y, ss);
         ss = __fmaf_rn(v[i].z, v[i].z, ss);
         ss = __fmaf_rn(v[i].w, v[i].w, ss);
     }
     ss = warp_sum(ss);
+    // The sum of squares goes to warp 0 over barrier bar+1 while the other
+    // warps go on: warp 0 waits for every partial, forms 1/rms and publishes
+    // it over barrier bar+2, which the others wait on only at the end.
     if (lane == 0) red[warp] = ss;
-    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthr) : "memory");
-    if (tid == 0) {
-        float t = 0.f;
-        for (int w = 0; w < nwarps; ++w) t = __fadd_rn(t, red[w]);
-        red[32] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)K), eps)));
+    __threadfence_block();
+    if (warp == 0) {
+        asm volatile("bar.sync %0, %1;" ::"r"(bar + 1), "r"(nthr) : "memory");
+        if (lane == 0) {
+            float t = 0.f;
+            for (int w = 0; w < nwarps; ++w) t = __fadd_rn(t, red[w]);
+            red[32] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)K), eps)));
+        }
+        __threadfence_block();
+        asm volatile("bar.arrive %0, %1;" ::"r"(bar + 2), "r"(nthr) : "memory");
+    } else {
+        asm volatile("bar.arrive %0, %1;" ::"r"(bar + 1), "r"(nthr) : "memory");
     }
-    asm volatile("bar.sync %0, %1;" ::"r"(bar), "r"(nthr) : "memory");
+    // Q8_0 codes of z = x (.) gamma: a block's codes do not change when all of
+    // its values are scaled by 1/rms, so they are formed before 1/rms is
+    // known; only the block scales wait for it (d = d_z * 1/rms).
+    float dz[RMS_STEPS];
+    int sz[RMS_STEPS];
+#pragma unroll
+    for (int i = 0; i < RMS_STEPS; ++i) {
+        dz[i] = 0.f;
+        sz[i] = 0;
+        if (i * (nthr >> 2) >= B) break;  // uniform: no block of this step exists
+        const int b = i * (nthr >> 2) + (tid >> 2);
+        const float4 g0 = gr.g[2 * i], g1 = gr.g[2 * i + 1];
+        const float4 u = make_float4(__fmul_rn(v[2 * i].x, g0.x), __fmul_rn(v[2 * i].y, g0.y),
+                                     __fmul_rn(v[2 * i].z, g0.z), __fmul_rn(v[2 * i].w, g0.w));
+        const float4 w = make_float4(__fmul_rn(v[2 * i + 1].x, g1.x), __fmul_rn(v[2 * i + 1].y, g1.y),
+                                     __fmul_rn(v[2 * i + 1].z, g1.z), __fmul_rn(v[2 * i + 1].w, g1.w));
+        const Oct r = oct_codes(u, w, 127.0f, -127.0f);
+        const int w0 = (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) | ((r.c[3] & 0xff) << 24);
+        const int w1 = (r.c[4] & 0xff) | ((r.c[5] & 0xff) << 8) | ((r.c[6] & 0xff) << 16) | ((r.c[7] & 0xff) << 24);
+        int sum = r.c[0] + r.c[1] + r.c[2] + r.c[3] + r.c[4] + r.c[5] + r.c[6] + r.c[7];
+        sum += __shfl_xor_sync(FULL, sum, 1);
+        sum += __shfl_xor_sync(FULL, sum, 2);
+        dz[i] = r.d32;
+        sz[i] = sum;
+        if (b < B) {
+            int2* plane = reinterpret_cast<int2*>(p < 2 ? &xt.lo[b] : &xt.hi[b]);
+            plane[p & 1] = make_int2(w0, w1);
+            if (writer && xq_out) *reinterpret_cast<int2*>(xq_out + (int64_t)b * QK + p * 8) = make_int2(w0, w1);
+        }
+    }
+    if (warp != 0) asm volatile("bar.sync %0, %1;" ::"r"(bar + 2), "r"(nthr) : "memory");
     const float inv = red[32];
 #pragma unroll
     for (int i = 0; i < RMS_STEPS; ++i) {
-        const int gi = warp + i * nwarps;
-        if (gi * 4 >= B) break;  // warp-uniform
-        const int b = gi * 4 + (lane >> 3);
-        const bool valid = b < B;
-        const float4 g = gr.g[i];
-        const float4 w = make_float4(__fmul_rn(__fmul_rn(v[i].x, inv), g.x), __fmul_rn(__fmul_rn(v[i].y, inv), g.y),
-                                     __fmul_rn(__fmul_rn(v[i].z, inv), g.z), __fmul_rn(__fmul_rn(v[i].w, inv), g.w));
-        const Quad r = quad_codes(w, 127.0f, -127.0f);
-        const int packed =
-            (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) | ((r.c[3] & 0xff) << 24);
-        int s = r.c[0] + r.c[1] + r.c[2] + r.c[3];
-        s += __shfl_xor_sync(FULL, s, 1);
-        s += __shfl_xor_sync(FULL, s, 2);
-        s += __shfl_xor_sync(FULL, s, 4);
-        if (valid) {
-            int* plane = reinterpret_cast<int*>(part < 4 ? &xt.lo[b] : &xt.hi[b]);
-            plane[part & 3] = packed;
-            if (part == 0) {
-                const unsigned short h = f32_to_f16_bits(r.d32);
-                xt.sc[b] = make_int2(__float_as_int(f16_bits_to_f32(h)), s);
-                if (writer && xd_out) xd_out[b] = h;
-            }
-            if (writer && xq_out) *reinterpret_cast<int*>(xq_out + (int64_t)b * QK + part * 4) = packed;
+        const int b = i * (nthr >> 2) + (tid >> 2);
+        if (b < B && p == 0) {
+            const unsigned short h = f32_to_f16_bits(__fmul_rn(dz[i], inv));
+            xt.sc[b] = make_int2(__float_as_int(f16_bits_to_f32(h)), sz[i]);
+            if (writer && xd_out) xd_out[b] = h;
         }
     }
 }
