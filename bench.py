@@ -21,6 +21,7 @@ decode step (the reference arm of this build).
 from __future__ import annotations
 
 import argparse
+import concurrent.futures
 import hashlib
 import json
 import os
@@ -543,8 +544,40 @@ def _rotated_us(torch, make_op, nbytes, calls_min=24):
                 op()
 
     g = _graph(torch, run)
-    t = _time_graph(torch, g, 5, 3)
-    return t / 5 / (reps * copies) * 1e6
+    per_call = _replay_stats(torch, g, reps * copies)
+    _LAST_STATS.clear()
+    _LAST_STATS.update(per_call)
+    return per_call["mean"]
+
+
+_LAST_STATS = {}
+NOMINAL_HBM_GBS = 8000.0  # the nominal HBM3e figure the target is quoted against
+
+
+def _replay_stats(torch, g, calls, replays=20, warmup=3):
+    """Per-call device time (us) of a graph of `calls` calls: each of
+    `replays` replays timed on its own with CUDA events; mean, median, p10,
+    p90 of the per-call averages."""
+    import numpy as np
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
+    ev[0].record(st)
+    for i in range(replays):
+        g.replay()
+        ev[i + 1].record(st)
+    torch.cuda.synchronize()
+    t = np.array([ev[i].elapsed_time(ev[i + 1]) * 1e3 / calls for i in range(replays)])
+    return {"mean": float(t.mean()), "median": float(np.median(t)), "p10": float(np.percentile(t, 10)),
+            "p90": float(np.percentile(t, 90)), "replays": replays, "calls_per_replay": calls}
+
+
+def _stats_keys(stats):
+    return {"us_median": round(stats["median"], 2), "us_p10": round(stats["p10"], 2),
+            "us_p90": round(stats["p90"], 2), "timed_replays": stats["replays"],
+            "calls_per_replay": stats["calls_per_replay"]}
 
 
 def run_configs(qmm, torch, dev="cuda"):
@@ -558,7 +591,8 @@ def run_configs(qmm, torch, dev="cuda"):
         wb = workloads.q4_0_bytes(N, K)
         d = {"config": cfg, "workload": name, "N": N, "K": K, "M": M, "us_per_call": round(us, 2),
              "weight_GBps": round(wb / us / 1e3, 1), "pct_of_hbm_peak": round(100 * wb / us / 1e3 / peak, 1),
-             "TOPS": round(2 * M * N * K / us / 1e6, 2), "peak_kind": peak_kind}
+             "pct_of_nominal_8TBps": round(100 * wb / us / 1e3 / NOMINAL_HBM_GBS, 1),
+             "TOPS": round(2 * M * N * K / us / 1e6, 2), "peak_kind": peak_kind, **_stats_keys(_LAST_STATS)}
         if extra:
             d.update(extra)
         print(json.dumps(d), flush=True)
@@ -585,6 +619,18 @@ def run_configs(qmm, torch, dev="cuda"):
         torch.cuda.empty_cache()
         return us
 
+    # read-only stream reference: a 4 GiB fp32 sum (library reduction), the
+    # third denominator beside the copy peak and the nominal 8 TB/s
+    buf = torch.ones(1 << 30, dtype=torch.float32, device=dev)
+    g = _graph(torch, lambda: buf.sum())
+    rs = _replay_stats(torch, g, 1, replays=10)
+    ro = {"config": "reference", "workload": "read-only stream probe: sum of 4 GiB fp32 (torch)",
+          "us_per_call": round(rs["mean"], 1), "read_GBps": round(buf.numel() * 4 / rs["mean"] / 1e3, 1),
+          "copy_peak_GBps": peak, "peak_kind": peak_kind, "nominal_GBps": NOMINAL_HBM_GBS}
+    print(json.dumps(ro), flush=True)
+    out.append(ro)
+    del buf, g
+    torch.cuda.empty_cache()
     c = workloads.SINGLE_GEMV
     line(0, c["name"] + " (Q8_0 activation in)", c["N"], c["K"], 1, product(c["N"], c["K"], 1, c["sigma"]))
     line(0, c["name"] + " (fp32 activation in, quantized in the launch)", c["N"], c["K"], 1,
@@ -593,9 +639,10 @@ def run_configs(qmm, torch, dev="cuda"):
     for path, fn in (("one persistent launch (qmm_gemv_chain)", dec.chain_step),
                      ("89 launches chained with PDL (qmm_gemv_fused)", dec.step)):
         g = _graph(torch, fn)
-        per = _time_graph(torch, g, 50, 5) / 50
+        stats = _replay_stats(torch, g, 1, replays=100)
+        per = stats["mean"] * 1e-6
         d1 = {"config": 1, "workload": workloads.TINYLLAMA["name"] + ": whole decode step, " + path,
-              "M": 1, "us_per_call": round(per * 1e6, 2), "weight_bytes": dec.weight_bytes,
+              "M": 1, "us_per_call": round(per * 1e6, 2), **_stats_keys(stats), "weight_bytes": dec.weight_bytes,
               "weight_GBps": round(dec.weight_bytes / per / 1e9, 1),
               "pct_of_hbm_peak": round(100 * dec.weight_bytes / per / 1e9 / peak, 1),
               "TOPS": round(2 * dec.weight_bytes / 0.5625 / per / 1e12, 3), "tokens_per_s": round(1 / per, 1),
@@ -616,7 +663,9 @@ def run_configs(qmm, torch, dev="cuda"):
             us, wb = format_variant_us(qmm, torch, variant, N, K)
             d = {"config": 3, "workload": f"format variant, {variant}, {name} {N}x{K}", "N": N, "K": K, "M": 1,
                  "us_per_call": round(us, 2), "weight_bytes": wb, "weight_GBps": round(wb / us / 1e3, 1),
-                 "pct_of_hbm_peak": round(100 * wb / us / 1e3 / peak, 1), "peak_kind": peak_kind}
+                 "pct_of_hbm_peak": round(100 * wb / us / 1e3 / peak, 1),
+                 "pct_of_nominal_8TBps": round(100 * wb / us / 1e3 / NOMINAL_HBM_GBS, 1), "peak_kind": peak_kind,
+                 **_stats_keys(_LAST_STATS)}
             print(json.dumps(d), flush=True)
             out.append(d)
     for T in workloads.MOE["T"]:
@@ -678,10 +727,17 @@ def oracle_decode_sample(torch, rows=256):
 
 
 def oracle_pass(prep, threads):
-    """One pass of the oracle's integer path over the sample; returns weight bytes."""
+    """One pass of the oracle's integer path over the sample; returns weight
+    bytes.  With several threads the matrices run concurrently, one thread
+    each (the oracle's C code runs outside the interpreter lock); splitting a
+    256-row sample matrix over many threads would time thread start-up."""
     from oracle import oracle as O
-    for qw, dw, qx, dx in prep:
-        O.matmul_int(qw, dw, qx, dx, nthreads=threads)
+    if threads <= 1:
+        for qw, dw, qx, dx in prep:
+            O.matmul_int(qw, dw, qx, dx, nthreads=1)
+    else:
+        with concurrent.futures.ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda p: O.matmul_int(*p, nthreads=1), prep))
     return sum(workloads.q4_0_bytes(*p[0].shape) for p in prep)
 
 
@@ -699,6 +755,20 @@ def cpu_oracle_sample(torch, target_s=12.0, threads=None):
         if dt >= target_s:
             break
     return nbytes / dt / 1e9, dt, threads, f"{desc}, {passes} passes"
+
+
+def cpu_dequant_config0(torch, repeats=3):
+    """The oracle's float64 dequantize-then-multiply path on the single
+    2048 x 2048 GEMV (weight GB/s, seconds per product)."""
+    from oracle import oracle as O
+    c = workloads.SINGLE_GEMV
+    qw, dw = O.quantize_q4_0(workloads.weights(c["N"], c["K"], sigma=c["sigma"], seed=0, index=0).numpy())
+    qx, dx = O.quantize_q8_0(workloads.activations(1, c["K"], seed=0).numpy())
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        O.matmul_dequant(qw, dw, qx, dx)
+    dt = (time.perf_counter() - t0) / repeats
+    return workloads.q4_0_bytes(c["N"], c["K"]) / dt / 1e9, dt
 
 
 # ---------------------------------------------------------------------------- main
@@ -804,8 +874,15 @@ def main():
     cpu = None
     if rank == 0 and ws >= 1:
         gbs, dt, thr, desc = cpu_oracle_sample(torch, target_s=args.cpu_seconds)
+        gbs1, dt1, _, desc1 = cpu_oracle_sample(torch, target_s=max(0.5, args.cpu_seconds / 4), threads=1)
+        dq_gbs, dq_s = cpu_dequant_config0(torch)
         cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": thr, "kind": "oracle",
-               "sample": desc + f" ({dt:.1f} s of CPU work)"}
+               "sample": desc + f" ({dt:.1f} s of CPU work)",
+               "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                                 "sample": desc1 + f" ({dt1:.1f} s)"},
+               "dequantize_path_config0": {"value": round(dq_gbs, 4), "unit": "GB/s", "cores": 1,
+                                           "seconds_per_product": round(dq_s, 4),
+                                           "sample": "float64 dequantize-then-multiply, 2048 x 2048 GEMV"}}
     if rank == 0:
         line = {
             "metric": "batch-1 Q4_0xQ8_0 GEMV weight GB/s (TinyLLaMA-1.1B-shaped decode step)",
