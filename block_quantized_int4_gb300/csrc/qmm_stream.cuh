@@ -367,18 +367,19 @@ struct MoeStreamArgs {
 // groups and K chunks.  So a pass stages its activations once for all the
 // segment's rows.
 struct MoeCursor {
-    int64_t gr, gr1;  // position in the row space, end of this CTA's slice
-    int64_t N;
+    // 32-bit positions: the host admits this kernel only when E * N < 2^31
+    int gr, gr1;  // position in the row space, end of this CTA's slice
+    int N;
     // current segment: expert e, rows [r, r + nrows), slots [sbeg, send)
     int e, nrows, sbeg, send;
-    int64_t r;
+    int r;
     // active: expert of each active index; span: (first slot, end slot) of
     // each active index -- shared-memory copies of the grouping
     __device__ bool next_segment(const int* active, const int2* span) {
         if (gr >= gr1) return false;
-        const int ai = (int)(gr / N);
-        r = gr - (int64_t)ai * N;
-        nrows = (int)min(N - r, gr1 - gr);
+        const int ai = gr / N;
+        r = gr - ai * N;
+        nrows = min(N - r, gr1 - gr);
         e = active[ai];
         sbeg = span[ai].x;
         send = span[ai].y;
@@ -428,9 +429,9 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
     __syncthreads();
     const int64_t total = (int64_t)n_active * a.N;
     MoeCursor cur;
-    cur.gr = total * blockIdx.x / gridDim.x;
-    cur.gr1 = total * (blockIdx.x + 1) / gridDim.x;
-    cur.N = a.N;
+    cur.gr = (int)(total * blockIdx.x / gridDim.x);
+    cur.gr1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+    cur.N = (int)a.N;
 
 
     if (warp == SW) {
@@ -508,23 +509,23 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
                     }
                     const int b0 = kc * CKB, nb = min(CKB, B - b0);
                     constexpr int H = CHUNK_KB / 32;
-                    Quad4 qd[H];
                     const bool work = ok && rA < nr;
-                    if (work) {
-                        const uint8_t* stq = ring + (size_t)s * STAGE_BYTES + (rA * CKB + lane) * 16;
-                        const uint16_t* std_ =
-                            reinterpret_cast<const uint16_t*>(ring + (size_t)s * STAGE_BYTES + STAGE_Q) + rA * CKB +
-                            lane;
+                    const uint8_t* stq = ring + (size_t)s * STAGE_BYTES + (rA * CKB + lane) * 16;
+                    const uint16_t* std_ =
+                        reinterpret_cast<const uint16_t*>(ring + (size_t)s * STAGE_BYTES + STAGE_Q) + rA * CKB + lane;
+                    // one 32-block half of the chunk in registers at a time (the
+                    // four-slot kernel would not fit two in its register budget);
+                    // the stage goes back to the producer once its last half is read
 #pragma unroll
-                        for (int h = 0; h < H; ++h)
-                            if (lane + 32 * h < nb) qd[h] = quad_load(stq + 512 * h, CKB * 16, std_ + 32 * h, CKB);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[s]);
-                    if (work) {
-#pragma unroll
-                        for (int h = 0; h < H; ++h)
-                            if (lane + 32 * h < nb) quad_compute<MT>(qd[h], xt, B, b0 + lane + 32 * h, acc, mt);
+                    for (int h = 0; h < H; ++h) {
+                        const bool here = work && lane + 32 * h < nb;
+                        Quad4 qd;
+                        if (here) qd = quad_load(stq + 512 * h, CKB * 16, std_ + 32 * h, CKB);
+                        if (h == H - 1) {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&empty[s]);
+                        }
+                        if (here) quad_compute<MT>(qd, xt, B, b0 + lane + 32 * h, acc, mt);
                     }
                 }
                 float v[MT][4];
