@@ -62,6 +62,23 @@ def _profiled_traffic():
     return traffic if h.hexdigest().startswith(digest) else None
 
 
+def max_over_ranks(torch, times, device):
+    """Each rank's timed-region lengths -> the maximum over ranks of each (one
+    all-reduce; any backend: `device` is where the backend keeps tensors),
+    followed by a barrier."""
+    tt = torch.tensor([float(v) for v in times], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    torch.distributed.barrier()
+    return tt.tolist()
+
+
+def whole_job_gbs(world_size, bytes_per_step_per_rank, steps, seconds):
+    """Weak-scaling whole-job throughput: every rank streams the same
+    weights each step, so the job moves world_size times the bytes in the
+    slowest rank's time."""
+    return world_size * bytes_per_step_per_rank * steps / seconds / 1e9
+
+
 def _peaks():
     try:
         with open(PEAKS_FILE) as f:
@@ -856,14 +873,11 @@ def main():
         torch.cuda.synchronize()
         t_e2e = e0.elapsed_time(e1) / 1e3
     if ws > 1:
-        tt = torch.tensor([t, t_e2e], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t, t_e2e = tt.tolist()
-        torch.distributed.barrier()
+        t, t_e2e = max_over_ranks(torch, [t, t_e2e], "cuda")
 
     per = t / args.steps
-    value = ws * dec.weight_bytes / per / 1e9
-    e2e_value = ws * dec.weight_bytes / (t_e2e / args.steps) / 1e9
+    value = whole_job_gbs(ws, dec.weight_bytes, args.steps, t)
+    e2e_value = whole_job_gbs(ws, dec.weight_bytes, args.steps, t_e2e)
     peak, peak_kind = _peaks()
     achieved = dec.algo_bytes / per / 1e9
     extras = {}
