@@ -264,13 +264,19 @@ __device__ __forceinline__ void stage_q8(const XTile& xt, int Bc, const int8_t* 
     const int64_t B = K / QK;
     for (int i = tid; i < MT * Bc; i += nthr) {
         const int t = i / Bc, b = i - t * Bc;
+        // xrow[t] by a select over the unrolled entries: a run-time index
+        // would put the array in local memory
+        int64_t row = -1;
+#pragma unroll
+        for (int tt = 0; tt < MT; ++tt)
+            if (tt == t) row = xrow[tt];
         int4 lo = make_int4(0, 0, 0, 0), hi = lo;
         float s = 0.f;
-        if (xrow[t] >= 0 && b < nb) {
-            const int8_t* src = xq + xrow[t] * K + (int64_t)(b0 + b) * QK;
+        if (row >= 0 && b < nb) {
+            const int8_t* src = xq + row * K + (int64_t)(b0 + b) * QK;
             lo = *reinterpret_cast<const int4*>(src);
             hi = *reinterpret_cast<const int4*>(src + 16);
-            s = f16_bits_to_f32(xd[xrow[t] * B + b0 + b]);
+            s = f16_bits_to_f32(xd[row * B + b0 + b]);
         }
         xt.lo[i] = lo;
         xt.hi[i] = hi;
