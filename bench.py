@@ -468,6 +468,8 @@ def run_case(qmm, torch, name, calls, dev="cuda"):
     elif name in ("gemm_b16", "gemm_b64"):
         N, K, sigma = workloads.LARGE_DENSE["ffn"], workloads.LARGE_DENSE["hidden"], workloads.LARGE_DENSE["sigma"]
         M = 16 if name == "gemm_b16" else 64
+    elif name == "gemm_b16_dense":  # the batch-16 set of the default line: gate, up, down, lm_head
+        return {"case": name, **bench_gemm_b16(qmm, torch, reps=max(calls, 3))}
     elif name == "moe_T16":
         return _moe_case(qmm, torch, calls, dev)
     elif name == "moe_store":
@@ -802,8 +804,10 @@ def main():
                     help="time every workload of the five configurations instead (one JSON line each)")
     ap.add_argument("--case", default=None,
                     help="time one kernel instead: decode_gateup, decode_qkv_norm, decode_chain, decode_pdl, lm_head_8192, "
-                         "gemm_b16, "
+                         "gemm_b16, gemm_b16_dense, "
                          "gemm_b64, moe_T16, moe_store")
+    ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "mma", "tmem"],
+                    help="small-batch GEMM kernel (qmm_debug_gemm_kernel): automatic choice, warp MMA or tcgen05")
     args = ap.parse_args()
     ws, rank, local = _dist()
 
@@ -821,6 +825,7 @@ def main():
         from block_quantized_int4_gb300 import _build
         _build.build()
         from block_quantized_int4_gb300 import qmm
+        qmm.qmm_debug_gemm_kernel({"auto": 0, "mma": 1, "tmem": 2}[args.gemm_kernel])
         print(json.dumps(run_case(qmm, torch, args.case, max(args.steps, 1))), flush=True)
         return
 

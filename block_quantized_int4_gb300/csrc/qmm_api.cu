@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -37,6 +38,9 @@ struct DevInfo {
 
 std::mutex g_mu;
 DevInfo g_dev[MAX_DEVICES];
+
+// Small-batch GEMM kernel choice (qmm_debug_gemm_kernel), process-wide.
+std::atomic<int> g_gemm_kernel{QMM_GEMM_KERNEL_AUTO};
 
 // Per-device facts, looked up once.  Requires an sm_103 device.
 const DevInfo* device_info() {
@@ -437,10 +441,22 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
     a.y = y;
     a.ldy = ldy;
     cudaStream_t st = S(stream);
-    // Two or more tokens: the warp-MMA kernel (exact fp16 products, fp32
-    // block sums) streams the weights once per 64 tokens.
-    if (M >= 2 && gemm_mma_eligible(N, K, M, w_qs, w_d, xq, xd) && ldy >= N)
-        return gemm_mma_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->sms, di->smem_optin, di->err, st);
+    // Two or more tokens: a tensor-core kernel (exact fp16 products, fp32
+    // block sums).  By default the warp-MMA kernel, which streams the
+    // weights once per 64 tokens; the tcgen05 kernel (weight operand in
+    // tensor memory, up to 16 tokens) when selected, which measures slower
+    // at every shape (its per-block TMEM read-back and rescale cost as much
+    // as the warp kernel's register path, on top of the tensor core's fixed
+    // cost per instruction).
+    if (M >= 2 && ldy >= N) {
+        const int pick = g_gemm_kernel.load();
+        if (pick == QMM_GEMM_KERNEL_TMEM) {
+            if (!gemm_tmem_eligible(N, K, M, w_qs, w_d, xq, xd)) return QMM_ERR_SHAPE;
+            return gemm_tmem_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->sms, di->smem_optin, di->err, st);
+        }
+        if (gemm_mma_eligible(N, K, M, w_qs, w_d, xq, xd))
+            return gemm_mma_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->sms, di->smem_optin, di->err, st);
+    }
     const int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
     const bool streamable = stream_eligible(N, K, w_qs, w_d, mt);
     if (streamable) {
@@ -606,6 +622,13 @@ qmm_status qmm_gemv_chain(const qmm_gemv_op* ops, int32_t n_ops, void* workspace
     cfg.numAttrs = 1;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_chain_kernel, a);
     return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
+}
+
+qmm_status qmm_debug_gemm_kernel(int kernel, int* previous) {
+    if (kernel < QMM_GEMM_KERNEL_AUTO || kernel > QMM_GEMM_KERNEL_TMEM) return QMM_ERR_ARG;
+    const int old = g_gemm_kernel.exchange(kernel);
+    if (previous) *previous = old;
+    return QMM_OK;
 }
 
 qmm_status qmm_debug_block_dots(const uint8_t* w_qs, int64_t N, int64_t K, int64_t M, const int8_t* xq,

@@ -23,3 +23,24 @@ qmm_status gemm_mma_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, 
                            int* err, cudaStream_t st);
 
 }  // namespace qmm
+
+namespace qmm {
+
+// True when the tensor-memory GEMM (qmm_gemm_tmem.cu, tcgen05 with the
+// weight operand in TMEM; used when selected by qmm_debug_gemm_kernel) can
+// take this product: 1 <= M <= 16, K % 256 == 0, all four operand pointers
+// 16-byte aligned.
+bool gemm_tmem_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const void* w_d, const void* xq,
+                        const void* xd);
+
+// Row plan of the tensor-memory GEMM: nst super-tiles of H rows per CTA,
+// `grid` CTAs.
+void gemm_tmem_plan(int64_t N, int sms, int* H, int* nst, int64_t* grid);
+
+// Enqueue y[m*ldy + n] (m < M <= 16, n < N) on `st`; arguments as for
+// gemm_mma_launch.
+qmm_status gemm_tmem_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,
+                            const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy, int sms, int smem_optin,
+                            int* err, cudaStream_t st);
+
+}  // namespace qmm

@@ -66,6 +66,7 @@ SIGNATURES = {
     "qmm_gemv_fused": [_P, _P, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _INT, _P],
     "qmm_gemm_q4_0_q8_0": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P],
     "qmm_debug_block_dots": [_P, _I64, _I64, _I64, _P, _P, _P],
+    "qmm_debug_gemm_kernel": [_INT, ctypes.POINTER(_INT)],
     "qmm_gemv_chain_workspace_size": [_I32, ctypes.POINTER(_SZ)],
     "qmm_gemv_chain": [ctypes.POINTER(GemvOp), _I32, _P, _SZ, _P],
     "qmm_gemv_fused_op": [ctypes.POINTER(GemvOp), _INT, _P],
@@ -175,6 +176,16 @@ def qmm_gemv_fused(w_qs, w_d, N, K, x, xq, xd, residual, y, yq, yd, flags=0, str
 def qmm_gemm_q4_0_q8_0(w_qs, w_d, N, K, M, xq, xd, y, ldy, stream=None):
     _check(_lib.qmm_gemm_q4_0_q8_0(_ptr(w_qs), _ptr(w_d), N, K, M, _ptr(xq), _ptr(xd), _ptr(y), ldy,
                                    _stream(stream)), "qmm_gemm_q4_0_q8_0")
+
+
+GEMM_KERNEL_AUTO, GEMM_KERNEL_MMA, GEMM_KERNEL_TMEM = 0, 1, 2
+
+
+def qmm_debug_gemm_kernel(kernel):
+    """Select the small-batch GEMM kernel; returns the previous setting."""
+    prev = ctypes.c_int(0)
+    _check(_lib.qmm_debug_gemm_kernel(kernel, ctypes.byref(prev)), "qmm_debug_gemm_kernel")
+    return prev.value
 
 
 def qmm_debug_block_dots(w_qs, N, K, M, xq, dots, stream=None):

@@ -176,6 +176,22 @@ QMM_API qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, 
                               int64_t M, const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy,
                               void* stream);
 
+/* Which kernel qmm_gemm_q4_0_q8_0 uses for 2 or more tokens, process-wide,
+ * for testing and timing the kernels on the same inputs:
+ *  - QMM_GEMM_KERNEL_AUTO (the default): the fastest measured, which is
+ *    the warp-MMA kernel at every shape;
+ *  - QMM_GEMM_KERNEL_MMA: the warp-MMA kernel (mma.sync, any M);
+ *  - QMM_GEMM_KERNEL_TMEM: the tcgen05 kernel with the weight operand in
+ *    tensor memory (M <= 16, K % 256 == 0, all four operand planes 16-byte
+ *    aligned; otherwise the GEMM returns QMM_ERR_SHAPE).
+ * Both compute the same fp32 result up to the order of the fp32 sums.
+ * `previous` (may be NULL) receives the old setting; QMM_ERR_ARG for an
+ * unknown kernel.  Not synchronised with GEMM calls on other host threads. */
+#define QMM_GEMM_KERNEL_AUTO 0
+#define QMM_GEMM_KERNEL_MMA 1
+#define QMM_GEMM_KERNEL_TMEM 2
+QMM_API qmm_status qmm_debug_gemm_kernel(int kernel, int* previous);
+
 /* Per-block integer dots, for bit-exact checking: dots[(m*N + n)*B + b] =
  * sum_{i<32} q_w * q_x, int32, computed with the product kernels' own
  * unpack and dot code.  M, N >= 1. */
