@@ -317,7 +317,8 @@ def bench_gemm_b16(qmm, torch, reps=20, dev="cuda"):
 def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
     """GLM-scale MoE layer, T tokens, from router logits on the device:
     sigmoid top-k router + slot grouping, quantize x, gate and up expert
-    GEMVs, SwiGLU + Q8_0, down expert GEMV, combine (seven launches)."""
+    GEMVs with SwiGLU in one launch (interleaved gate/up rows), Q8_0 of h,
+    down expert GEMV, combine (six launches)."""
     import numpy as np
     c = workloads.MOE
     H, F, E, k = c["hidden"], c["expert_ffn"], c["experts"], c["top_k"]
@@ -332,14 +333,16 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
         return qs, d
 
     gate, up, down = experts(F, H, 0), experts(F, H, 1000), experts(H, F, 2000)
+    # gate and up rows interleaved per expert (g0, u0, g1, u1, ...)
+    gu = tuple(torch.stack([g, u], dim=2).reshape(E, 2 * F, g.shape[2]).contiguous() for g, u in zip(gate, up))
+    del gate, up
     logits = workloads.router_logits(T, E, seed=0).to(dev)
     ids = torch.empty(T, k, dtype=torch.int32, device=dev)
     gts = torch.empty(T, k, dtype=torch.float32, device=dev)
     x = workloads.activations(T, H, seed=0, device=dev)
     xq = torch.empty(T, H, dtype=torch.int8, device=dev)
     xd = torch.empty(T, H // 32, dtype=torch.int16, device=dev)
-    yg = torch.empty(T * k, F, device=dev)
-    yu = torch.empty(T * k, F, device=dev)
+    h = torch.empty(T * k, F, device=dev)
     hq = torch.empty(T * k, F, dtype=torch.int8, device=dev)
     hd = torch.empty(T * k, F // 32, dtype=torch.int16, device=dev)
     z = torch.empty(T * k, H, device=dev)
@@ -352,9 +355,8 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
         # the three expert GEMVs reuse that grouping
         qmm.qmm_moe_router_topk(logits, T, E, k, ids, gts, ws, wsb)
         qmm.qmm_quantize_q8_0(x, T, H, H, xq, xd)
-        qmm.qmm_moe_gemv_pregrouped(*gate, E, F, H, T, k, xq, xd, 0, yg, ws, wsb)
-        qmm.qmm_moe_gemv_pregrouped(*up, E, F, H, T, k, xq, xd, 0, yu, ws, wsb)
-        qmm.qmm_swiglu_quantize_q8_0(yg, yu, T * k, F, F, hq, hd)
+        qmm.qmm_moe_gemv_gate_up(*gu, E, 2 * F, H, T, k, xq, xd, 0, h, ws, wsb)
+        qmm.qmm_quantize_q8_0(h, T * k, F, F, hq, hd)
         qmm.qmm_moe_gemv_pregrouped(*down, E, H, F, T, k, hq, hd, 1, z, ws, wsb)
         qmm.qmm_moe_combine(z, gts, T, k, H, y)
 
@@ -472,6 +474,8 @@ def run_case(qmm, torch, name, calls, dev="cuda"):
         return {"case": name, **bench_gemm_b16(qmm, torch, reps=max(calls, 3))}
     elif name == "moe_T16":
         return _moe_case(qmm, torch, calls, dev)
+    elif name in ("moe_layer_T1", "moe_layer_T16"):  # the whole MoE layer of the default line
+        return {"case": name, **bench_moe(qmm, torch, T=1 if name == "moe_layer_T1" else 16, reps=max(calls, 3))}
     elif name == "moe_store":
         return {"case": name, **bench_moe_store(qmm, torch, T=1)}
     elif name in ("decode_chain", "decode_pdl"):  # the whole TinyLLaMA-shaped decode step
@@ -805,7 +809,7 @@ def main():
     ap.add_argument("--case", default=None,
                     help="time one kernel instead: decode_gateup, decode_qkv_norm, decode_chain, decode_pdl, lm_head_8192, "
                          "gemm_b16, gemm_b16_dense, "
-                         "gemm_b64, moe_T16, moe_store")
+                         "gemm_b64, moe_T16, moe_layer_T1, moe_layer_T16, moe_store")
     ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "mma", "tmem"],
                     help="small-batch GEMM kernel (qmm_debug_gemm_kernel): automatic choice, warp MMA or tcgen05")
     args = ap.parse_args()

@@ -114,6 +114,10 @@ __device__ __forceinline__ Oct oct_codes(float4 u, float4 w, float qmax, float q
 // blocks per step (8 lanes per block, one float4 per lane).
 __global__ void quantize_q8_0_kernel(const float* __restrict__ x, int64_t M, int64_t K, int64_t ldx,
                                      int8_t* __restrict__ q, uint16_t* __restrict__ d) {
+    // launched after the kernel that writes the input, possibly early
+    // (programmatic dependent launch): nothing is read before it completes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t B = K / QK;
     const int64_t nblk = M * B;
     const int lane = threadIdx.x & 31;
@@ -142,6 +146,10 @@ __global__ void quantize_q8_0_kernel(const float* __restrict__ x, int64_t M, int
 __global__ void swiglu_quantize_kernel(const float* __restrict__ gate, const float* __restrict__ up, int64_t rows,
                                        int64_t K, int64_t ld, int8_t* __restrict__ q, uint16_t* __restrict__ d,
                                        float* __restrict__ h_out) {
+    // launched after the kernel that writes the input, possibly early
+    // (programmatic dependent launch): nothing is read before it completes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t B = K / QK;
     const int64_t nblk = rows * B;
     const int lane = threadIdx.x & 31;
@@ -679,9 +687,19 @@ __host__ __device__ inline size_t moe_ws_bytes(int E, int64_t nslots) {
 constexpr int GROUP_THREADS = 1024;
 
 // The whole block builds the tables.  ids may have been written earlier in
-// the same kernel by this block (plain loads after a block barrier).
+// the same kernel by this block (plain loads after a block barrier).  The
+// counts and cursors live in shared memory while the sort runs (up to
+// GROUP_SMEM_E experts; beyond that in the workspace itself), so the only
+// global-memory traffic is the final tables, written once.
+constexpr int GROUP_SMEM_E = 2048;
+
 __device__ __forceinline__ void moe_group_block(const int32_t* ids, int nslots, int E, MoeWs w, int* err) {
-    for (int e = threadIdx.x; e < E; e += blockDim.x) w.counts[e] = 0;
+    __shared__ int s_cnt[GROUP_SMEM_E];
+    __shared__ int s_cur[GROUP_SMEM_E];
+    const bool in_smem = E <= GROUP_SMEM_E;
+    int* cnt = in_smem ? s_cnt : w.counts;
+    int* cur = in_smem ? s_cur : w.cursor;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
     for (int s = threadIdx.x; s < nslots; s += blockDim.x) {
         const int e = ids[s];
@@ -689,7 +707,7 @@ __device__ __forceinline__ void moe_group_block(const int32_t* ids, int nslots, 
             atomicOr(err, ERR_BAD_EXPERT);
             continue;
         }
-        atomicAdd(&w.counts[e], 1);
+        atomicAdd(&cnt[e], 1);
     }
     __syncthreads();
     // Exclusive scans of counts (-> offsets) and of (counts > 0) (-> active
@@ -698,8 +716,8 @@ __device__ __forceinline__ void moe_group_block(const int32_t* ids, int nslots, 
     const int e0 = min(E, (int)threadIdx.x * per), e1 = min(E, e0 + per);
     int csum = 0, asum = 0;
     for (int e = e0; e < e1; ++e) {
-        csum += w.counts[e];
-        asum += w.counts[e] > 0;
+        csum += cnt[e];
+        asum += cnt[e] > 0;
     }
     // block-wide exclusive scan of (csum, asum) packed into one 64-bit lane value
     long long v = ((long long)csum << 32) | (unsigned)asum;
@@ -724,9 +742,10 @@ __device__ __forceinline__ void moe_group_block(const int32_t* ids, int nslots, 
     long long excl = incl - v + (wid > 0 ? wsum[wid - 1] : 0);
     int coff = (int)(excl >> 32), aoff = (int)(excl & 0xffffffff);
     for (int e = e0; e < e1; ++e) {
-        const int c = w.counts[e];
+        const int c = cnt[e];
+        if (in_smem) w.counts[e] = c;
         w.offsets[e] = coff;
-        w.cursor[e] = coff;
+        cur[e] = coff;
         if (c > 0) w.active[aoff++] = e;
         coff += c;
     }
@@ -738,13 +757,21 @@ __device__ __forceinline__ void moe_group_block(const int32_t* ids, int nslots, 
     for (int s = threadIdx.x; s < nslots; s += blockDim.x) {
         const int e = ids[s];
         if (e < 0 || e >= E) continue;
-        const int pos = atomicAdd(&w.cursor[e], 1);
+        const int pos = atomicAdd(&cur[e], 1);
         w.slots[pos] = s;
+    }
+    if (in_smem) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += blockDim.x) w.cursor[e] = cur[e];  // each expert's end
     }
 }
 
 __global__ void __launch_bounds__(GROUP_THREADS) moe_group_kernel(const int32_t* __restrict__ ids, int nslots, int E,
                                                                   MoeWs w, int* err) {
+    // launched after the kernel that writes the input, possibly early
+    // (programmatic dependent launch): nothing is read before it completes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     moe_group_block(ids, nslots, E, w, err);
 }
 
@@ -830,6 +857,10 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, int E,
 __global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const float* __restrict__ logits, int T, int E,
                                                                   int k, int32_t* ids, float* gates, MoeWs w,
                                                                   int group, int* err) {
+    // launched after the kernel that writes the input, possibly early
+    // (programmatic dependent launch): nothing is read before it completes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     for (int t = blockIdx.x * nw + warp; t < T; t += gridDim.x * nw)
         route_token(logits + (int64_t)t * E, E, k, ids + (int64_t)t * k, gates + (int64_t)t * k, lane);
@@ -905,6 +936,10 @@ __global__ void __launch_bounds__(ROWS_THREADS) moe_rows_kernel(MoeArgs a) {
 // y[t][n] = sum_j g[t][j] * z[t][j][n], j ascending.
 __global__ void moe_combine_kernel(const float* __restrict__ z, const float* __restrict__ gates, int T, int k,
                                    int64_t N, float* __restrict__ y) {
+    // launched after the kernel that writes the input, possibly early
+    // (programmatic dependent launch): nothing is read before it completes
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int64_t total = (int64_t)T * N;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t t = i / N, n = i - t * N;

@@ -347,7 +347,10 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
 // a few expert boundaries and restages the routed activations only there.
 // Weights of all E experts are one 2D tensor [E*N rows][K/2 bytes].  A row
 // group is applied to MT of the expert's slots per pass; an expert with more
-// routed slots is streamed once per MT slots.
+// routed slots is streamed once per MT slots.  With pairs, each expert's rows
+// interleave its gate and up projections (row 2i gate, 2i + 1 up; a pair
+// always sits in one warp) and the output is SwiGLU of each pair (TinyLLaMA
+// guide section 4.4): the expert FFN's first half in one launch.
 // ============================================================================
 struct MoeStreamArgs {
     int64_t N, K;
@@ -355,7 +358,8 @@ struct MoeStreamArgs {
     const int8_t* xq;
     const uint16_t* xd;
     int x_per_slot;
-    float* y;  // [T*k][N]
+    float* y;   // [T*k][N], or [T*k][N/2] with pairs
+    int pairs;  // rows 2i, 2i+1 of each expert are a (gate, up) pair: y = SwiGLU of the pair
     MoeWs ws;
     int rb, ckb, nstages, xtile_bytes;
     int* err;
@@ -429,8 +433,14 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
     __syncthreads();
     const int64_t total = (int64_t)n_active * a.N;
     MoeCursor cur;
-    cur.gr = (int)(total * blockIdx.x / gridDim.x);
-    cur.gr1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+    if (a.pairs) {  // slices of whole (gate, up) row pairs (N is even)
+        const int64_t tp = total / 2;
+        cur.gr = 2 * (int)(tp * blockIdx.x / gridDim.x);
+        cur.gr1 = 2 * (int)(tp * (blockIdx.x + 1) / gridDim.x);
+    } else {
+        cur.gr = (int)(total * blockIdx.x / gridDim.x);
+        cur.gr1 = (int)(total * (blockIdx.x + 1) / gridDim.x);
+    }
     cur.N = (int)a.N;
 
 
@@ -536,16 +546,36 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
                     v[t][2] = warp_sum(acc[t][1].x);
                     v[t][3] = warp_sum(acc[t][1].y);
                 }
-                if (lane == 0 && !failed) {
+                if (a.pairs && !failed) {
+                    // rows (rA, rA + 1) and (rB, rB + 1) are (gate, up) pairs (r0,
+                    // rA, rB and nr are even); every lane holds the sums, so lane
+                    // 2t + p evaluates the SwiGLU of slot t's pair p
+                    const int tl = lane >> 1, p = lane & 1;
+                    float g = 0.f, uu = 0.f;
+                    int sl = -1;
 #pragma unroll
-                    for (int t = 0; t < MT; ++t) {
-                        if (slot[t] < 0) continue;
-                        float* yr = a.y + (int64_t)slot[t] * a.N + r0;
-                        const int lrs[4] = {rA, rA + 1, rB, rB + 1};
+                    for (int t = 0; t < MT; ++t)
+                        if (t == tl) {
+                            g = p ? v[t][2] : v[t][0];
+                            uu = p ? v[t][3] : v[t][1];
+                            sl = slot[t];
+                        }
+                    const int lr = p ? rB : rA;
+                    if (tl < MT && sl >= 0 && lr < nr)
+                        a.y[(int64_t)sl * (a.N / 2) + (r0 + lr) / 2] = swiglu1(g, uu);
+                } else if (!failed) {
+                    // lane 4t + q writes slot t's row q of the warp (rA, rA + 1, rB, rB + 1)
+                    const int tl = lane >> 2, q = lane & 3;
+                    float o = 0.f;
+                    int sl = -1;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            if (lrs[q] < nr) yr[lrs[q]] = v[t][q];
-                    }
+                    for (int t = 0; t < MT; ++t)
+                        if (t == tl) {
+                            o = q == 0 ? v[t][0] : q == 1 ? v[t][1] : q == 2 ? v[t][2] : v[t][3];
+                            sl = slot[t];
+                        }
+                    const int lr = (q < 2 ? rA : rB) + (q & 1);
+                    if (tl < MT && sl >= 0 && lr < nr) a.y[(int64_t)sl * a.N + r0 + lr] = o;
                 }
             }
         }

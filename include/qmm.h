@@ -366,6 +366,23 @@ QMM_API qmm_status qmm_moe_gemv_pregrouped(const uint8_t* w_qs, const uint16_t* 
                                            int x_per_slot, float* y, const void* workspace, size_t workspace_bytes,
                                            void* stream);
 
+/* The first half of every routed expert's FFN in one launch: gate and up
+ * projections, then SwiGLU (TinyLLaMA guide section 4.4: Swish(x W_gate)
+ * times x W_up, Swish(z) = z sigmoid(z)), on the grouping of
+ * qmm_moe_router_topk as for qmm_moe_gemv_pregrouped.  Each expert's N rows
+ * interleave its two projections: row 2i is gate row i, row 2i + 1 up row i
+ * (N = 2 * F, even).  For every slot s:
+ *   h[s][i] = g / (1 + exp(-g)) * u,   g = y[s][2i], u = y[s][2i + 1],
+ * with y as qmm_moe_gemv_pregrouped would compute it: each of g and u equals
+ * bit for bit what a qmm_moe_gemv_pregrouped call over the same rows gives,
+ * and h what qmm_swiglu_quantize_q8_0 writes as h_out for them.  h fp32
+ * [T*k][N/2], 4-byte aligned.  Requires the streaming path (K % 256 == 0,
+ * w_qs and w_d 16-byte aligned) and N even, else QMM_ERR_SHAPE; other
+ * arguments and errors as qmm_moe_gemv_pregrouped. */
+QMM_API qmm_status qmm_moe_gemv_gate_up(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,
+                                        int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd, int x_per_slot,
+                                        float* h, const void* workspace, size_t workspace_bytes, void* stream);
+
 /* y[t][n] = sum_{j=0..k-1} gates[t][j] * z[t][j][n], j ascending (fixed
  * order, deterministic).  z fp32 [T][k][N], gates fp32 [T][k], y [T][N]. */
 QMM_API qmm_status qmm_moe_combine(const float* z, const float* gates, int32_t T, int32_t k, int64_t N, float* y,

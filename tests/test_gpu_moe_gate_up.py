@@ -1,0 +1,118 @@
+"""qmm_moe_gemv_gate_up -- the gate and up expert GEMVs and SwiGLU (TinyLLaMA
+guide section 4.4) in one launch over interleaved gate/up rows -- against the
+unfused path on the same grouping: every output bit-identical to
+qmm_swiglu_quantize_q8_0's h_out of the two separate qmm_moe_gemv_pregrouped
+outputs (one slot per weight pass and four), and against the oracle's fp64
+SwiGLU of its own gate and up products with the tolerance propagated through
+the SwiGLU."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+import workloads
+from parity import lib
+from test_gpu_moe import Experts
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _interleave(a, b):
+    """Rows of a and b alternated (g0, u0, g1, u1, ...) per expert."""
+    return torch.stack([a, b], dim=2).reshape(a.shape[0], 2 * a.shape[1], a.shape[2]).contiguous()
+
+
+def _layer_inputs(qmm, T, E, k, F, H, x_per_slot, seed):
+    logits = workloads.router_logits(T, E, seed=seed)
+    wsb = qmm.qmm_moe_workspace_size(E, T, k)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    gts = torch.empty(T, k, device=DEV)
+    qmm.qmm_moe_router_topk(logits.to(DEV), T, E, k, ids, gts, ws, wsb)
+    used = np.unique(ids.cpu().numpy())
+    gate = Experts(qmm, E, F, H, used, seed=seed, base_index=0)
+    up = Experts(qmm, E, F, H, used, seed=seed, base_index=1000)
+    x = workloads.activations(T * k if x_per_slot else T, H, seed=seed + 1)
+    xq, xd = qmm.quantize_q8_0(x.to(DEV))
+    return ids.cpu().numpy(), ws, wsb, gate, up, x, xq, xd
+
+
+@pytest.mark.parametrize("T,E,k,F,H,x_per_slot", [(1, 64, 8, 300, 512, 0), (16, 64, 8, 300, 512, 0),
+                                                  (16, 32, 4, 256, 1024, 1), (3, 8, 8, 40, 256, 0)])
+def test_gate_up_equals_separate_gemvs_and_swiglu(T, E, k, F, H, x_per_slot):
+    """Bit-identical to gate and up as two pregrouped launches plus the SwiGLU
+    kernel; 16 tokens x top-8 of 64 experts takes the four-slots-per-pass
+    kernel, one token the one-slot kernel; F not a multiple of the 32-row
+    group leaves ragged pairs at each expert's end; 8 experts x top-8 routes
+    every expert."""
+    qmm = lib()
+    ids, ws, wsb, gate, up, x, xq, xd = _layer_inputs(qmm, T, E, k, F, H, x_per_slot, seed=T + E)
+    gu_qs, gu_d = _interleave(gate.qs, up.qs), _interleave(gate.d, up.d)
+    h = torch.full((T * k, F), float("nan"), device=DEV)
+    qmm.qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, xq, xd, x_per_slot, h, ws, wsb)
+    yg = torch.empty(T * k, F, device=DEV)
+    yu = torch.empty(T * k, F, device=DEV)
+    qmm.qmm_moe_gemv_pregrouped(gate.qs, gate.d, E, F, H, T, k, xq, xd, x_per_slot, yg, ws, wsb)
+    qmm.qmm_moe_gemv_pregrouped(up.qs, up.d, E, F, H, T, k, xq, xd, x_per_slot, yu, ws, wsb)
+    hq = torch.empty(T * k, F, dtype=torch.int8, device=DEV)
+    hd = torch.empty(T * k, F // 32, dtype=torch.int16, device=DEV)
+    h_ref = torch.empty(T * k, F, device=DEV)
+    if F % 32 == 0:
+        qmm.qmm_swiglu_quantize_q8_0(yg, yu, T * k, F, F, hq, hd, h_ref)
+    else:  # the SwiGLU kernel takes whole 32-blocks: pad the rows to the next block
+        Fp = (F + 31) // 32 * 32
+        pad = lambda t: torch.nn.functional.pad(t, (0, Fp - F)).contiguous()  # noqa: E731
+        hp = torch.empty(T * k, Fp, device=DEV)
+        qmm.qmm_swiglu_quantize_q8_0(pad(yg), pad(yu), T * k, Fp, Fp, torch.empty(T * k, Fp, dtype=torch.int8,
+                                     device=DEV), torch.empty(T * k, Fp // 32, dtype=torch.int16, device=DEV), hp)
+        h_ref = hp[:, :F].contiguous()
+    assert qmm.qmm_last_device_error() == 0
+    assert not torch.isnan(h).any()
+    assert torch.equal(h, h_ref)
+
+
+def test_gate_up_vs_oracle_swiglu():
+    """h against SwiGLU of the oracle's fp64 gate and up products: |h - h_ref|
+    <= 1.1 tol_g |u| + |silu(g)| tol_u + 2^-23 |h_ref| + 1e-7, with tol = 1e-5 S +
+    1e-6 the product tolerance and 1.1 >= max |silu'|."""
+    qmm = lib()
+    T, E, k, F, H = 4, 32, 4, 256, 1024
+    ids, ws, wsb, gate, up, x, xq, xd = _layer_inputs(qmm, T, E, k, F, H, 0, seed=21)
+    h = torch.empty(T * k, F, device=DEV)
+    qmm.qmm_moe_gemv_gate_up(_interleave(gate.qs, up.qs), _interleave(gate.d, up.d), E, 2 * F, H, T, k, xq, xd, 0,
+                             h, ws, wsb)
+    assert qmm.qmm_last_device_error() == 0
+    qx, dx = O.quantize_q8_0(x.numpy())
+    flat = ids.reshape(-1)
+    for s in range(T * k):
+        g, Sg = O.matmul_int(*gate.oracle[int(flat[s])], qx[s // k], dx[s // k])
+        u, Su = O.matmul_int(*up.oracle[int(flat[s])], qx[s // k], dx[s // k])
+        g, u, Sg, Su = g[0], u[0], Sg[0], Su[0]
+        sg = g / (1.0 + np.exp(-g))
+        ref = sg * u
+        bound = 1.1 * (1e-5 * Sg + 1e-6) * np.abs(u) + np.abs(sg) * (1e-5 * Su + 1e-6) + 2.0 ** -23 * np.abs(ref) + 1e-7
+        err = np.abs(h[s].cpu().numpy().astype(np.float64) - ref)
+        assert np.all(err <= bound), (s, float(np.max(err - bound)))
+
+
+def test_gate_up_shape_errors():
+    """Odd N (rows that do not pair) and K off the streaming kernel's 256
+    multiple are shape errors; nothing is written."""
+    qmm = lib()
+    T, E, k = 2, 8, 2
+    wsb = qmm.qmm_moe_workspace_size(E, T, k)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    qs = torch.zeros(E, 64, 256, dtype=torch.uint8, device=DEV)
+    d = torch.zeros(E, 64, 16, dtype=torch.int16, device=DEV)
+    xq = torch.zeros(T, 512, dtype=torch.int8, device=DEV)
+    xd = torch.zeros(T, 16, dtype=torch.int16, device=DEV)
+    h = torch.full((T * k, 32), 7.0, device=DEV)
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.qmm_moe_gemv_gate_up(qs, d, E, 63, 512, T, k, xq, xd, 0, h, ws, wsb)
+    assert ei.value.status == 2
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.qmm_moe_gemv_gate_up(qs, d, E, 64, 96, T, k, xq[:, :96].contiguous(), xd[:, :3].contiguous(), 0, h, ws,
+                                 wsb)
+    assert ei.value.status == 2
+    assert torch.all(h == 7.0)
