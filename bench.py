@@ -316,9 +316,14 @@ def bench_gemm_b16(qmm, torch, reps=20, dev="cuda"):
 
 def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
     """GLM-scale MoE layer, T tokens, from router logits on the device:
-    sigmoid top-k router + slot grouping, quantize x, gate and up expert
-    GEMVs with SwiGLU in one launch (interleaved gate/up rows), Q8_0 of h,
-    down expert GEMV, combine (six launches)."""
+    sigmoid top-k router + slot grouping; gate and up expert GEMVs with
+    SwiGLU in one launch (interleaved gate/up rows); down expert GEMV;
+    combine.  With few routed slots (T*k*4 <= E: the expert GEMV takes one
+    slot per weight pass) the two GEMVs quantize their fp32 activations
+    while staging them (four launches: 1 token 49.9 -> 49.1 us); with more,
+    each CTA would requantize four activation rows per expert segment, and
+    standalone Q8_0 launches of x and h are faster (six launches: 16 tokens
+    477.8 -> 469.3 us)."""
     import numpy as np
     c = workloads.MOE
     H, F, E, k = c["hidden"], c["expert_ffn"], c["experts"], c["top_k"]
@@ -340,9 +345,10 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
     ids = torch.empty(T, k, dtype=torch.int32, device=dev)
     gts = torch.empty(T, k, dtype=torch.float32, device=dev)
     x = workloads.activations(T, H, seed=0, device=dev)
+    h = torch.empty(T * k, F, device=dev)
+    in_launch = T * k * 4 <= E
     xq = torch.empty(T, H, dtype=torch.int8, device=dev)
     xd = torch.empty(T, H // 32, dtype=torch.int16, device=dev)
-    h = torch.empty(T * k, F, device=dev)
     hq = torch.empty(T * k, F, dtype=torch.int8, device=dev)
     hd = torch.empty(T * k, F // 32, dtype=torch.int16, device=dev)
     z = torch.empty(T * k, H, device=dev)
@@ -354,10 +360,14 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
         # the router (sigmoid top-k) groups the slots by expert in the same launch;
         # the three expert GEMVs reuse that grouping
         qmm.qmm_moe_router_topk(logits, T, E, k, ids, gts, ws, wsb)
-        qmm.qmm_quantize_q8_0(x, T, H, H, xq, xd)
-        qmm.qmm_moe_gemv_gate_up(*gu, E, 2 * F, H, T, k, xq, xd, 0, h, ws, wsb)
-        qmm.qmm_quantize_q8_0(h, T * k, F, F, hq, hd)
-        qmm.qmm_moe_gemv_pregrouped(*down, E, H, F, T, k, hq, hd, 1, z, ws, wsb)
+        if in_launch:
+            qmm.qmm_moe_gemv_gate_up(*gu, E, 2 * F, H, T, k, x, None, None, 0, h, ws, wsb)
+            qmm.qmm_moe_gemv_pregrouped_f32(*down, E, H, F, T, k, h, 1, z, ws, wsb)
+        else:
+            qmm.qmm_quantize_q8_0(x, T, H, H, xq, xd)
+            qmm.qmm_moe_gemv_gate_up(*gu, E, 2 * F, H, T, k, None, xq, xd, 0, h, ws, wsb)
+            qmm.qmm_quantize_q8_0(h, T * k, F, F, hq, hd)
+            qmm.qmm_moe_gemv_pregrouped(*down, E, H, F, T, k, hq, hd, 1, z, ws, wsb)
         qmm.qmm_moe_combine(z, gts, T, k, H, y)
 
     g = _graph(torch, run)
@@ -367,7 +377,8 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
     wbytes = uniq * 3 * workloads.q4_0_bytes(F, H)
     return {"metric": "MoE layer expert-weight GB/s", "value": round(wbytes / per / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(per * 1e3, 4), "tokens_per_s": round(T / per, 1), "unique_experts": uniq,
-            "config": {"workload": c["name"], "T": T, "experts": E, "top_k": k, "hidden": H, "expert_ffn": F}}
+            "config": {"workload": c["name"], "T": T, "experts": E, "top_k": k, "hidden": H, "expert_ffn": F,
+                       "launches": 4 if in_launch else 6}}
 
 
 def bench_moe_store(qmm, torch, T=1, dev="cuda"):

@@ -673,10 +673,11 @@ qmm_status moe_check(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_
 
 // The expert GEMV on routing tables already built in the workspace.
 // pairs: rows 2i, 2i + 1 of each expert are a (gate, up) pair and y gets
-// SwiGLU of each pair ([T*k][N/2]); streaming kernel only.
+// SwiGLU of each pair ([T*k][N/2]); xf: fp32 activation rows quantized while
+// staging, in place of xq/xd.  Both on the streaming kernel only.
 qmm_status moe_apply(const DevInfo* di, const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,
                      int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd, int x_per_slot, float* y,
-                     MoeWs ws, cudaStream_t st, bool pairs = false) {
+                     MoeWs ws, cudaStream_t st, bool pairs = false, const float* xf = nullptr) {
     const int64_t B = K / QK;
     const int64_t nslots = (int64_t)T * k;
     const bool streamable = (B % 8 == 0) && aligned(w_qs, 16) && aligned(w_d, 16) &&
@@ -690,6 +691,7 @@ qmm_status moe_apply(const DevInfo* di, const uint8_t* w_qs, const uint16_t* w_d
         m.k = k;
         m.xq = xq;
         m.xd = xd;
+        m.xf = xf;
         m.x_per_slot = x_per_slot;
         m.y = y;
         m.pairs = pairs ? 1 : 0;
@@ -736,7 +738,7 @@ qmm_status moe_apply(const DevInfo* di, const uint8_t* w_qs, const uint16_t* w_d
         return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
     }
 
-    if (pairs) return QMM_ERR_SHAPE;  // the fallback writes plain rows only
+    if (pairs || xf) return QMM_ERR_SHAPE;  // the fallback writes plain rows of Q8_0 activations only
     MoeArgs a = {};
     a.qs = w_qs;
     a.d = w_d;
@@ -823,15 +825,31 @@ qmm_status qmm_moe_gemv_pregrouped(const uint8_t* w_qs, const uint16_t* w_d, int
 }
 
 qmm_status qmm_moe_gemv_gate_up(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K, int32_t T,
-                                int32_t k, const int8_t* xq, const uint16_t* xd, int x_per_slot, float* h,
-                                const void* workspace, size_t workspace_bytes, void* stream) {
+                                int32_t k, const float* x, const int8_t* xq, const uint16_t* xd, int x_per_slot,
+                                float* h, const void* workspace, size_t workspace_bytes, void* stream) {
     void* wsp = const_cast<void*>(workspace);
-    qmm_status s = moe_check(w_qs, w_d, E, N, K, T, k, xq, xd, h, wsp, workspace_bytes);
+    // with an fp32 x the Q8_0 planes are not read: check x in their place
+    const int8_t* cq = x ? reinterpret_cast<const int8_t*>(x) : xq;
+    const uint16_t* cd = x ? reinterpret_cast<const uint16_t*>(x) : xd;
+    qmm_status s = moe_check(w_qs, w_d, E, N, K, T, k, cq, cd, h, wsp, workspace_bytes);
     if (s != QMM_OK || T == 0) return s;
     if (N % 2) return QMM_ERR_SHAPE;
     const DevInfo* di = device_info();
     if (!di) return QMM_ERR_DEVICE;
-    return moe_apply(di, w_qs, w_d, E, N, K, T, k, xq, xd, x_per_slot, h, moe_ws(wsp, E), S(stream), true);
+    return moe_apply(di, w_qs, w_d, E, N, K, T, k, xq, xd, x_per_slot, h, moe_ws(wsp, E), S(stream), true, x);
+}
+
+qmm_status qmm_moe_gemv_pregrouped_f32(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,
+                                       int32_t T, int32_t k, const float* x, int x_per_slot, float* y,
+                                       const void* workspace, size_t workspace_bytes, void* stream) {
+    void* wsp = const_cast<void*>(workspace);
+    qmm_status s = moe_check(w_qs, w_d, E, N, K, T, k, reinterpret_cast<const int8_t*>(x),
+                             reinterpret_cast<const uint16_t*>(x), y, wsp, workspace_bytes);
+    if (s != QMM_OK || T == 0) return s;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    return moe_apply(di, w_qs, w_d, E, N, K, T, k, nullptr, nullptr, x_per_slot, y, moe_ws(wsp, E), S(stream), false,
+                     x);
 }
 
 qmm_status qmm_moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids, float* gates,

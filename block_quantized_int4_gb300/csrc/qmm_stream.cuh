@@ -357,6 +357,7 @@ struct MoeStreamArgs {
     int E, k;
     const int8_t* xq;
     const uint16_t* xd;
+    const float* xf;  // fp32 activation rows instead of xq/xd (Q8_0 formed while staging), or NULL
     int x_per_slot;
     float* y;   // [T*k][N], or [T*k][N/2] with pairs
     int pairs;  // rows 2i, 2i+1 of each expert are a (gate, up) pair: y = SwiGLU of the pair
@@ -501,7 +502,26 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
                 xrow[t] = slot[t] < 0 ? -1 : (a.x_per_slot ? slot[t] : slot[t] / a.k);
             }
             asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");  // everyone is done with the old tile
-            stage_q8<MT>(xt, B, a.xq, a.xd, a.K, xrow, 0, B, tid, NTHR);
+            if (a.xf) {
+                // Q8_0 of each fp32 row as qmm_quantize_q8_0 would form it
+#pragma unroll
+                for (int t = 0; t < MT; ++t) {
+                    XTile r = xt;
+                    r.lo += t * B;
+                    r.hi += t * B;
+                    r.sc += t * B;
+                    if (xrow[t] >= 0) {
+                        stage_f32<false>(r, a.xf + xrow[t] * a.K, a.K, nullptr, nullptr, tid, NTHR);
+                    } else {
+                        for (int b = tid; b < B; b += NTHR) {
+                            r.lo[b] = r.hi[b] = make_int4(0, 0, 0, 0);
+                            r.sc[b] = make_int2(0, 0);
+                        }
+                    }
+                }
+            } else {
+                stage_q8<MT>(xt, B, a.xq, a.xd, a.K, xrow, 0, B, tid, NTHR);
+            }
             asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
             for (int g = 0; g < ngroups; ++g) {
                 const int64_t r0 = cur.r + (int64_t)g * a.rb;

@@ -89,7 +89,8 @@ SIGNATURES = {
     "qmm_gemv_rowwise_q8_0": [_P, _P, _I32, _I64, _I64, _P, _P, _P, _P],
     "qmm_gemv_q4_0_f32_fma": [_P, _P, _I64, _I64, _P, _P, _P],
     "qmm_moe_gemv_pregrouped": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
-    "qmm_moe_gemv_gate_up": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
+    "qmm_moe_gemv_gate_up": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _INT, _P, _P, _SZ, _P],
+    "qmm_moe_gemv_pregrouped_f32": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _INT, _P, _P, _SZ, _P],
     "qmm_last_device_error": [_P],
 }
 for _name, _args in SIGNATURES.items():
@@ -343,10 +344,17 @@ def qmm_moe_gemv_pregrouped(w_qs, w_d, E, N, K, T, k, xq, xd, x_per_slot, y, wor
            "qmm_moe_gemv_pregrouped")
 
 
-def qmm_moe_gemv_gate_up(w_qs, w_d, E, N, K, T, k, xq, xd, x_per_slot, h, workspace, workspace_bytes, stream=None):
-    _check(_lib.qmm_moe_gemv_gate_up(_ptr(w_qs), _ptr(w_d), E, N, K, T, k, _ptr(xq), _ptr(xd), int(x_per_slot),
-                                     _ptr(h), _ptr(workspace), workspace_bytes, _stream(stream)),
+def qmm_moe_gemv_gate_up(w_qs, w_d, E, N, K, T, k, x, xq, xd, x_per_slot, h, workspace, workspace_bytes,
+                         stream=None):
+    _check(_lib.qmm_moe_gemv_gate_up(_ptr(w_qs), _ptr(w_d), E, N, K, T, k, _ptr(x), _ptr(xq), _ptr(xd),
+                                     int(x_per_slot), _ptr(h), _ptr(workspace), workspace_bytes, _stream(stream)),
            "qmm_moe_gemv_gate_up")
+
+
+def qmm_moe_gemv_pregrouped_f32(w_qs, w_d, E, N, K, T, k, x, x_per_slot, y, workspace, workspace_bytes, stream=None):
+    _check(_lib.qmm_moe_gemv_pregrouped_f32(_ptr(w_qs), _ptr(w_d), E, N, K, T, k, _ptr(x), int(x_per_slot), _ptr(y),
+                                            _ptr(workspace), workspace_bytes, _stream(stream)),
+           "qmm_moe_gemv_pregrouped_f32")
 
 
 def qmm_moe_combine(z, gates, T, k, N, y, stream=None):

@@ -376,12 +376,29 @@ QMM_API qmm_status qmm_moe_gemv_pregrouped(const uint8_t* w_qs, const uint16_t* 
  * with y as qmm_moe_gemv_pregrouped would compute it: each of g and u equals
  * bit for bit what a qmm_moe_gemv_pregrouped call over the same rows gives,
  * and h what qmm_swiglu_quantize_q8_0 writes as h_out for them.  h fp32
- * [T*k][N/2], 4-byte aligned.  Requires the streaming path (K % 256 == 0,
- * w_qs and w_d 16-byte aligned) and N even, else QMM_ERR_SHAPE; other
- * arguments and errors as qmm_moe_gemv_pregrouped. */
+ * [T*k][N/2], 4-byte aligned.  The activation is the Q8_0 xq/xd as for
+ * qmm_moe_gemv_pregrouped, or, when x is not NULL, fp32 rows x (same row
+ * layout, 16-byte aligned) quantized inside the launch exactly as
+ * qmm_quantize_q8_0 would (xq and xd are then not read).  Requires the
+ * streaming path (K % 256 == 0, w_qs and w_d 16-byte aligned) and N even,
+ * else QMM_ERR_SHAPE; other arguments and errors as
+ * qmm_moe_gemv_pregrouped. */
 QMM_API qmm_status qmm_moe_gemv_gate_up(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,
-                                        int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd, int x_per_slot,
-                                        float* h, const void* workspace, size_t workspace_bytes, void* stream);
+                                        int32_t T, int32_t k, const float* x, const int8_t* xq, const uint16_t* xd,
+                                        int x_per_slot, float* h, const void* workspace, size_t workspace_bytes,
+                                        void* stream);
+
+/* qmm_moe_gemv_pregrouped with fp32 activation rows x (x_per_slot == 0:
+ * [T][K], else [T*k][K]; 16-byte aligned), each quantized to Q8_0 inside
+ * the launch exactly as qmm_quantize_q8_0 would, so the result equals bit
+ * for bit that of qmm_moe_gemv_pregrouped on qmm_quantize_q8_0(x): the
+ * expert GEMV after a SwiGLU with no quantization launch in between.
+ * Requires the streaming path (K % 256 == 0, w_qs and w_d 16-byte aligned),
+ * else QMM_ERR_SHAPE. */
+QMM_API qmm_status qmm_moe_gemv_pregrouped_f32(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N,
+                                               int64_t K, int32_t T, int32_t k, const float* x, int x_per_slot,
+                                               float* y, const void* workspace, size_t workspace_bytes,
+                                               void* stream);
 
 /* y[t][n] = sum_{j=0..k-1} gates[t][j] * z[t][j][n], j ascending (fixed
  * order, deterministic).  z fp32 [T][k][N], gates fp32 [T][k], y [T][N]. */

@@ -50,7 +50,7 @@ def test_gate_up_equals_separate_gemvs_and_swiglu(T, E, k, F, H, x_per_slot):
     ids, ws, wsb, gate, up, x, xq, xd = _layer_inputs(qmm, T, E, k, F, H, x_per_slot, seed=T + E)
     gu_qs, gu_d = _interleave(gate.qs, up.qs), _interleave(gate.d, up.d)
     h = torch.full((T * k, F), float("nan"), device=DEV)
-    qmm.qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, xq, xd, x_per_slot, h, ws, wsb)
+    qmm.qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, None, xq, xd, x_per_slot, h, ws, wsb)
     yg = torch.empty(T * k, F, device=DEV)
     yu = torch.empty(T * k, F, device=DEV)
     qmm.qmm_moe_gemv_pregrouped(gate.qs, gate.d, E, F, H, T, k, xq, xd, x_per_slot, yg, ws, wsb)
@@ -80,7 +80,7 @@ def test_gate_up_vs_oracle_swiglu():
     T, E, k, F, H = 4, 32, 4, 256, 1024
     ids, ws, wsb, gate, up, x, xq, xd = _layer_inputs(qmm, T, E, k, F, H, 0, seed=21)
     h = torch.empty(T * k, F, device=DEV)
-    qmm.qmm_moe_gemv_gate_up(_interleave(gate.qs, up.qs), _interleave(gate.d, up.d), E, 2 * F, H, T, k, xq, xd, 0,
+    qmm.qmm_moe_gemv_gate_up(_interleave(gate.qs, up.qs), _interleave(gate.d, up.d), E, 2 * F, H, T, k, None, xq, xd, 0,
                              h, ws, wsb)
     assert qmm.qmm_last_device_error() == 0
     qx, dx = O.quantize_q8_0(x.numpy())
@@ -109,10 +109,56 @@ def test_gate_up_shape_errors():
     xd = torch.zeros(T, 16, dtype=torch.int16, device=DEV)
     h = torch.full((T * k, 32), 7.0, device=DEV)
     with pytest.raises(qmm.QmmError) as ei:
-        qmm.qmm_moe_gemv_gate_up(qs, d, E, 63, 512, T, k, xq, xd, 0, h, ws, wsb)
+        qmm.qmm_moe_gemv_gate_up(qs, d, E, 63, 512, T, k, None, xq, xd, 0, h, ws, wsb)
     assert ei.value.status == 2
     with pytest.raises(qmm.QmmError) as ei:
-        qmm.qmm_moe_gemv_gate_up(qs, d, E, 64, 96, T, k, xq[:, :96].contiguous(), xd[:, :3].contiguous(), 0, h, ws,
+        qmm.qmm_moe_gemv_gate_up(qs, d, E, 64, 96, T, k, None, xq[:, :96].contiguous(), xd[:, :3].contiguous(), 0, h, ws,
                                  wsb)
     assert ei.value.status == 2
     assert torch.all(h == 7.0)
+
+
+@pytest.mark.parametrize("T,E,k,F,H", [(1, 64, 8, 256, 512), (16, 64, 8, 512, 1024)])
+def test_fp32_activations_equal_quantize_then_gemv(T, E, k, F, H):
+    """fp32 activations quantized inside the launch: qmm_moe_gemv_gate_up with
+    x equals it with qmm_quantize_q8_0(x), and qmm_moe_gemv_pregrouped_f32 on
+    the fp32 SwiGLU output equals qmm_moe_gemv_pregrouped on its Q8_0, bit for
+    bit (one slot per weight pass and four)."""
+    qmm = lib()
+    ids, ws, wsb, gate, up, x, xq, xd = _layer_inputs(qmm, T, E, k, F, H, 0, seed=31 + T)
+    gu_qs, gu_d = _interleave(gate.qs, up.qs), _interleave(gate.d, up.d)
+    xf = x.to(DEV).contiguous()
+    h_q8 = torch.full((T * k, F), float("nan"), device=DEV)
+    qmm.qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, None, xq, xd, 0, h_q8, ws, wsb)
+    h_f32 = torch.full((T * k, F), float("nan"), device=DEV)
+    qmm.qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, xf, None, None, 0, h_f32, ws, wsb)
+    assert torch.equal(h_f32, h_q8)
+    down = Experts(qmm, E, H, F, np.unique(ids), seed=31 + T, base_index=2000)
+    hq, hd = qmm.quantize_q8_0(h_f32)
+    z_q8 = torch.full((T * k, H), float("nan"), device=DEV)
+    qmm.qmm_moe_gemv_pregrouped(down.qs, down.d, E, H, F, T, k, hq, hd, 1, z_q8, ws, wsb)
+    z_f32 = torch.full((T * k, H), float("nan"), device=DEV)
+    qmm.qmm_moe_gemv_pregrouped_f32(down.qs, down.d, E, H, F, T, k, h_f32, 1, z_f32, ws, wsb)
+    assert qmm.qmm_last_device_error() == 0
+    assert not torch.isnan(z_f32).any()
+    assert torch.equal(z_f32, z_q8)
+
+
+def test_fp32_activation_entry_errors():
+    """The fp32 entry needs a 16-byte aligned x and the streaming kernel (K a
+    multiple of 256)."""
+    qmm = lib()
+    T, E, k = 2, 8, 2
+    wsb = qmm.qmm_moe_workspace_size(E, T, k)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    qs = torch.zeros(E, 64, 48, dtype=torch.uint8, device=DEV)
+    d = torch.zeros(E, 64, 3, dtype=torch.int16, device=DEV)
+    x = torch.zeros(T, 100, device=DEV)
+    y = torch.full((T * k, 64), 7.0, device=DEV)
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.qmm_moe_gemv_pregrouped_f32(qs, d, E, 64, 96, T, k, x, 0, y, ws, wsb)
+    assert ei.value.status == 2
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.qmm_moe_gemv_pregrouped_f32(qs, d, E, 64, 96, T, k, x[:, 1:], 0, y, ws, wsb)
+    assert ei.value.status == 3
+    assert torch.all(y == 7.0)
