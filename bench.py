@@ -821,8 +821,9 @@ def main():
                     help="time one kernel instead: decode_gateup, decode_qkv_norm, decode_chain, decode_pdl, lm_head_8192, "
                          "gemm_b16, gemm_b16_dense, "
                          "gemm_b64, moe_T16, moe_layer_T1, moe_layer_T16, moe_store")
-    ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "mma", "tmem"],
-                    help="small-batch GEMM kernel (qmm_debug_gemm_kernel): automatic choice, warp MMA or tcgen05")
+    ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "mma", "tmem", "stream"],
+                    help="small-batch GEMM kernel (qmm_debug_gemm_kernel): automatic choice, warp MMA, tcgen05 or "
+                         "dp4a streaming")
     args = ap.parse_args()
     ws, rank, local = _dist()
 
@@ -840,7 +841,7 @@ def main():
         from block_quantized_int4_gb300 import _build
         _build.build()
         from block_quantized_int4_gb300 import qmm
-        qmm.qmm_debug_gemm_kernel({"auto": 0, "mma": 1, "tmem": 2}[args.gemm_kernel])
+        qmm.qmm_debug_gemm_kernel({"auto": 0, "mma": 1, "tmem": 2, "stream": 3}[args.gemm_kernel])
         print(json.dumps(run_case(qmm, torch, args.case, max(args.steps, 1))), flush=True)
         return
 

@@ -443,8 +443,8 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
     a.y = y;
     a.ldy = ldy;
     cudaStream_t st = S(stream);
-    // Two or more tokens: a tensor-core kernel (exact fp16 products, fp32
-    // block sums).  By default the warp-MMA kernel, which streams the
+    // Two or more tokens: mostly a tensor-core kernel (exact fp16 products,
+    // fp32 block sums).  By default the warp-MMA kernel, which streams the
     // weights once per 64 tokens; the tcgen05 kernel (weight operand in
     // tensor memory, up to 16 tokens) when selected, which measures slower
     // at every shape (its per-block TMEM read-back and rescale cost as much
@@ -456,7 +456,17 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
             if (!gemm_tmem_eligible(N, K, M, w_qs, w_d, xq, xd)) return QMM_ERR_SHAPE;
             return gemm_tmem_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->sms, di->smem_optin, di->err, st);
         }
-        if (gemm_mma_eligible(N, K, M, w_qs, w_d, xq, xd))
+        // 2..4 tokens: the batch-1 GEMV's streaming path, where it measured
+        // faster than warp MMA (x = stream / MMA, us): 2 tokens on every
+        // shape (28672x8192 23.2/43.9, 8192x28672 36.0/48.6, 2048x5632
+        // 6.0/8.0, 2560x2048 4.0/5.0, 5632x2048 5.7/5.7); 3-4 tokens when
+        // N <= 4096 or K >= 8192 and the activation tile fits (2048x5632
+        // 7.0/8.1, 2560x2048 4.4/4.9, 28672x8192 41.7/44.7; but 5632x2048
+        // 6.4/5.6).  From 8 tokens warp MMA wins everywhere.
+        const bool prefer_stream =
+            pick == QMM_GEMM_KERNEL_AUTO &&
+            (M == 2 || (M <= 4 && (N <= 4096 || K >= 8192) && stream_eligible(N, K, w_qs, w_d, 4)));
+        if (pick != QMM_GEMM_KERNEL_STREAM && !prefer_stream && gemm_mma_eligible(N, K, M, w_qs, w_d, xq, xd))
             return gemm_mma_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->sms, di->smem_optin, di->err, st);
     }
     const int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
@@ -627,7 +637,7 @@ qmm_status qmm_gemv_chain(const qmm_gemv_op* ops, int32_t n_ops, void* workspace
 }
 
 qmm_status qmm_debug_gemm_kernel(int kernel, int* previous) {
-    if (kernel < QMM_GEMM_KERNEL_AUTO || kernel > QMM_GEMM_KERNEL_TMEM) return QMM_ERR_ARG;
+    if (kernel < QMM_GEMM_KERNEL_AUTO || kernel > QMM_GEMM_KERNEL_STREAM) return QMM_ERR_ARG;
     const int old = g_gemm_kernel.exchange(kernel);
     if (previous) *previous = old;
     return QMM_OK;

@@ -178,18 +178,22 @@ QMM_API qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, 
 
 /* Which kernel qmm_gemm_q4_0_q8_0 uses for 2 or more tokens, process-wide,
  * for testing and timing the kernels on the same inputs:
- *  - QMM_GEMM_KERNEL_AUTO (the default): the fastest measured, which is
- *    the warp-MMA kernel at every shape;
+ *  - QMM_GEMM_KERNEL_AUTO (the default): the fastest measured: the
+ *    streaming kernel for 2 tokens, and for 3-4 tokens when N <= 4096 or
+ *    K >= 8192; otherwise the warp-MMA kernel;
  *  - QMM_GEMM_KERNEL_MMA: the warp-MMA kernel (mma.sync, any M);
  *  - QMM_GEMM_KERNEL_TMEM: the tcgen05 kernel with the weight operand in
  *    tensor memory (M <= 16, K % 256 == 0, all four operand planes 16-byte
- *    aligned; otherwise the GEMM returns QMM_ERR_SHAPE).
- * Both compute the same fp32 result up to the order of the fp32 sums.
+ *    aligned; otherwise the GEMM returns QMM_ERR_SHAPE);
+ *  - QMM_GEMM_KERNEL_STREAM: the dp4a streaming kernel of the batch-1 GEMV,
+ *    up to 8 tokens per weight pass (more tokens: more passes).
+ * All compute the same fp32 result up to the order of the fp32 sums.
  * `previous` (may be NULL) receives the old setting; QMM_ERR_ARG for an
  * unknown kernel.  Not synchronised with GEMM calls on other host threads. */
 #define QMM_GEMM_KERNEL_AUTO 0
 #define QMM_GEMM_KERNEL_MMA 1
 #define QMM_GEMM_KERNEL_TMEM 2
+#define QMM_GEMM_KERNEL_STREAM 3
 QMM_API qmm_status qmm_debug_gemm_kernel(int kernel, int* previous);
 
 /* Per-block integer dots, for bit-exact checking: dots[(m*N + n)*B + b] =

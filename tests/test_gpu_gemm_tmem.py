@@ -113,7 +113,7 @@ def test_tmem_gemm_ldy(qmm):
 
 def test_tmem_gemm_rejects_what_it_cannot_take(qmm):
     """Forced onto the tensor-memory kernel, 17 tokens or K % 256 != 0 is a
-    shape error and nothing is written; the selector rejects unknown kernels."""
+    shape error and nothing is written; the selector rejects an unknown kernel."""
     N, K = 64, 512
     qw, dw, qx, dx = _rand_codes(N, 17, K, seed=5)
     qs, d = _planes(qmm, qw, dw)
@@ -131,4 +131,22 @@ def test_tmem_gemm_rejects_what_it_cannot_take(qmm):
     assert ei.value.status == 2
     assert torch.all(y == 7.0) and torch.all(y2 == 7.0)
     with pytest.raises(qmm.QmmError):
-        qmm.qmm_debug_gemm_kernel(3)
+        qmm.qmm_debug_gemm_kernel(4)
+
+
+@pytest.mark.parametrize("N,K,M", [(517, 2048, 2), (20000, 8192, 3), (300, 512, 5), (129, 256, 9)])
+def test_streaming_kernel_selected_vs_oracle(N, K, M):
+    """The dp4a streaming path forced for 2..9 tokens (one or two passes of
+    up to 8 tokens over the weights) against the oracle."""
+    q = lib()
+    prev = q.qmm_debug_gemm_kernel(q.GEMM_KERNEL_STREAM)
+    try:
+        qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + M)
+        qs, d = _planes(q, qw, dw)
+        xq, xd = _q8(qx, dx)
+        y = q.gemm(qs, d, xq, xd)
+        ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+        assert_close(y, ref, S, f"stream gemm {N}x{K} M={M}")
+        assert q.qmm_last_device_error() == 0
+    finally:
+        q.qmm_debug_gemm_kernel(prev)
