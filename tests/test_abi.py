@@ -184,3 +184,29 @@ def test_valid_call_without_gpu_reports_device_error(qmm):
     assert _call(qmm, "qmm_gemv_q4_0_f32_fma", A16, A16, 8, 64, A16, A16, None) == 4
     assert _call(qmm, "qmm_quantize_rowwise", A16, 4, 64, 64, 2, A16, A16, None) == 4
     assert _call(qmm, "qmm_last_device_error", None) == 4
+
+
+def test_gemm_kernel_selector_and_moe_fp32_validation(qmm):
+    """qmm_debug_gemm_kernel accepts the four documented kernels, returns the
+    previous choice and rejects others; the fp32-activation and gate/up MoE
+    entries reject bad shapes, workspaces and alignment on the host."""
+    prev = ctypes.c_int(-1)
+    lib = qmm._lib
+    assert lib.qmm_debug_gemm_kernel(3, ctypes.byref(prev)) == 0
+    start = prev.value
+    assert lib.qmm_debug_gemm_kernel(2, ctypes.byref(prev)) == 0 and prev.value == 3
+    assert lib.qmm_debug_gemm_kernel(4, None) == 1
+    assert lib.qmm_debug_gemm_kernel(-1, None) == 1
+    assert lib.qmm_debug_gemm_kernel(start, ctypes.byref(prev)) == 0 and prev.value == 2
+    A16 = 0x10000
+    n = qmm.qmm_moe_workspace_size(256, 16, 8)
+    f = lambda *a: _call(qmm, "qmm_moe_gemv_pregrouped_f32", *a)  # noqa: E731
+    assert f(A16, A16, 256, 64, 64, 16, 8, A16, 0, A16, A16, n - 16, None) == 8  # workspace too small
+    assert f(A16, A16, 256, 64, 48, 16, 8, A16, 0, A16, A16, n, None) == 2       # K % 32
+    assert f(A16, A16, 256, 64, 64, 16, 8, None, 0, A16, A16, n, None) == 1      # no activation
+    assert f(A16, A16, 256, 64, 64, 16, 8, A16 + 4, 0, A16, A16, n, None) == 3   # x not 16-byte aligned
+    assert f(A16, A16, 256, 64, 64, 0, 8, A16, 0, A16, A16, n, None) == 0        # T = 0: no-op
+    g = lambda *a: _call(qmm, "qmm_moe_gemv_gate_up", *a)  # noqa: E731
+    assert g(A16, A16, 256, 63, 256, 16, 8, None, A16, A16, 0, A16, A16, n, None) == 2  # N odd
+    assert g(A16, A16, 256, 64, 256, 16, 8, A16 + 4, None, None, 0, A16, A16, n, None) == 3  # fp32 x misaligned
+    assert g(A16, A16, 256, 64, 256, 16, 8, None, A16, A16, 0, A16, A16, n - 16, None) == 8  # workspace
