@@ -881,8 +881,12 @@ qmm_status qmm_moe_router_topk(const float* logits, int32_t T, int32_t E, int32_
     // per token over as many CTAs as that takes (up to 4 per SM).
     const int grid = workspace ? 1 : (int)std::min<int64_t>(((int64_t)T + warps - 1) / warps, 4 * (int64_t)di->sms);
     const MoeWs ws = workspace ? moe_ws(workspace, E) : MoeWs{};
-    const cudaError_t e = launch(moe_route_kernel, dim3(grid), dim3(ROUTE_THREADS), 0, S(stream), true, logits, T, E,
-                                 k, ids, gates, ws, workspace ? 1 : 0, di->err);
+    // The grouping CTA: one warp per token, 8 to 32 warps (fewer warps make
+    // its block barriers and scan cheaper when few tokens are routed)
+    const int threads = workspace ? (int)std::min<int64_t>(ROUTE_THREADS, std::max<int64_t>(256, 32 * (int64_t)T))
+                                  : ROUTE_THREADS;
+    const cudaError_t e = launch(moe_route_kernel, dim3(grid), dim3(threads), 0, S(stream), true, logits, T, E, k, ids,
+                                 gates, ws, workspace ? 1 : 0, di->err);
     return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
 }
 
