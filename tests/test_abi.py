@@ -210,3 +210,7 @@ def test_gemm_kernel_selector_and_moe_fp32_validation(qmm):
     assert g(A16, A16, 256, 63, 256, 16, 8, None, A16, A16, 0, A16, A16, n, None) == 2  # N odd
     assert g(A16, A16, 256, 64, 256, 16, 8, A16 + 4, None, None, 0, A16, A16, n, None) == 3  # fp32 x misaligned
     assert g(A16, A16, 256, 64, 256, 16, 8, None, A16, A16, 0, A16, A16, n - 16, None) == 8  # workspace
+    lib2 = qmm._lib
+    assert lib2.qmm_debug_tcgen05_mma_cycles(0, 16, 1, 0, ctypes.c_void_p(A16), None) == 1   # iters < 1
+    assert lib2.qmm_debug_tcgen05_mma_cycles(0, 16, 1, 8, None, None) == 1                   # no output
+    assert lib2.qmm_debug_tcgen05_mma_cycles(0, 16, 1, 8, ctypes.c_void_p(A16 + 4), None) == 3  # misaligned

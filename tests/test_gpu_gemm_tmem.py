@@ -150,3 +150,18 @@ def test_streaming_kernel_selected_vs_oracle(N, K, M):
         assert q.qmm_last_device_error() == 0
     finally:
         q.qmm_debug_gemm_kernel(prev)
+
+
+def test_tcgen05_mma_cost_probe():
+    """The measurement hook runs every documented (kind, N, A source) and
+    reports a plausible per-instruction cost (tens of cycles, not zero)."""
+    q = lib()
+    cyc = torch.zeros(1, dtype=torch.int64, device=DEV)
+    for kind, n, a_tmem in ((0, 16, 0), (0, 16, 1), (0, 64, 1), (1, 32, 1), (1, 16, 0)):
+        q.qmm_debug_tcgen05_mma_cycles(kind, n, a_tmem, 64, cyc)
+        torch.cuda.synchronize()
+        per = int(cyc.item()) / (64 * 8)
+        assert 4 <= per <= 2000, (kind, n, a_tmem, per)
+    with pytest.raises(q.QmmError):
+        q.qmm_debug_tcgen05_mma_cycles(1, 64, 1, 64, cyc)  # e4m3 N = 64 is not a probed shape
+    assert q.qmm_last_device_error() == 0
