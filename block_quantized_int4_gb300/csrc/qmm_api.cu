@@ -456,9 +456,10 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
             if (!gemm_tmem_eligible(N, K, M, w_qs, w_d, xq, xd)) return QMM_ERR_SHAPE;
             return gemm_tmem_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->sms, di->smem_optin, di->err, st);
         }
-        // 2..4 tokens: the batch-1 GEMV's streaming path, where it measured
+        // 2..4 tokens: the batch-1 GEMV's streaming path (its row-kernel
+        // fallback where the activation tile does not fit), where it measured
         // faster than warp MMA (x = stream / MMA, us): 2 tokens on every
-        // shape (28672x8192 23.2/43.9, 8192x28672 36.0/48.6, 2048x5632
+        // shape (28672x8192 23.2/43.9, 8192x28672 36.0/48.6 on the fallback, 2048x5632
         // 6.0/8.0, 2560x2048 4.0/5.0, 5632x2048 5.7/5.7); 3-4 tokens when
         // N <= 4096 or K >= 8192 and the activation tile fits (2048x5632
         // 7.0/8.1, 2560x2048 4.4/4.9, 28672x8192 41.7/44.7; but 5632x2048
