@@ -638,7 +638,9 @@ def run_configs(qmm, torch, dev="cuda"):
         d = {"config": cfg, "workload": name, "N": N, "K": K, "M": M, "us_per_call": round(us, 2),
              "weight_GBps": round(wb / us / 1e3, 1), "pct_of_hbm_peak": round(100 * wb / us / 1e3 / peak, 1),
              "pct_of_nominal_8TBps": round(100 * wb / us / 1e3 / NOMINAL_HBM_GBS, 1),
-             "TOPS": round(2 * M * N * K / us / 1e6, 2), "peak_kind": peak_kind, **_stats_keys(_LAST_STATS)}
+             "TOPS": round(2 * M * N * K / us / 1e6, 2),
+             "tokens_per_s": round(M / us * 1e6, 1),  # tokens through this one product per second
+             "peak_kind": peak_kind, **_stats_keys(_LAST_STATS)}
         if extra:
             d.update(extra)
         print(json.dumps(d), flush=True)
