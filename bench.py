@@ -285,11 +285,11 @@ def _flush_l2(torch, buf):
 
 
 # ---------------------------------------------------------------------------- extras
-def bench_gemm_b16(qmm, torch, reps=20, dev="cuda"):
-    """Batch-16 GEMM on the large dense FFN + lm_head shapes (TOPS = 2*M*N*K per second)."""
+def bench_gemm_b16(qmm, torch, reps=20, dev="cuda", M=16):
+    """Batch-M GEMM (16 by default; 2 = a one-draft speculative verify) on the
+    large dense FFN + lm_head shapes (TOPS = 2*M*N*K per second)."""
     mats = workloads.large_dense_matrices()
     sigma = workloads.LARGE_DENSE["sigma"]
-    M = 16
     ws, xs, ys, ops, wbytes = [], [], [], 0, 0
     for i, (_, N, K) in enumerate(mats):
         w = workloads.weights(N, K, sigma=sigma, seed=0, index=100 + i, device=dev)
@@ -308,9 +308,9 @@ def bench_gemm_b16(qmm, torch, reps=20, dev="cuda"):
     g = _graph(torch, run)
     t = _time_graph(torch, g, reps, 3)
     per = t / reps
-    return {"metric": "batch-16 Q4_0xQ8_0 GEMM TOPS", "value": round(ops / per / 1e12, 2), "unit": "TOPS",
+    return {"metric": f"batch-{M} Q4_0xQ8_0 GEMM TOPS", "value": round(ops / per / 1e12, 2), "unit": "TOPS",
             "ms_per_step": round(per * 1e3, 4), "weight_GBps": round(wbytes / per / 1e9, 1),
-            "config": {"workload": workloads.LARGE_DENSE["name"] + ", batch 16", "M": M,
+            "config": {"workload": workloads.LARGE_DENSE["name"] + f", batch {M}", "M": M,
                        "shapes": [[N, K] for _, N, K in mats], "l2": "inputs larger than L2 (987 MB weights)"}}
 
 
@@ -918,6 +918,7 @@ def main():
     extras = {}
     if not args.no_extras and rank == 0:
         extras["gemm_batch16"] = bench_gemm_b16(qmm, torch)
+        extras["gemm_batch2"] = bench_gemm_b16(qmm, torch, M=2)
         extras["moe_T16"] = bench_moe(qmm, torch, T=16)
         extras["moe_T1"] = bench_moe(qmm, torch, T=1)
     cpu = None
