@@ -162,3 +162,71 @@ def test_fp32_activation_entry_errors():
         qmm.qmm_moe_gemv_pregrouped_f32(qs, d, E, 64, 96, T, k, x[:, 1:], 0, y, ws, wsb)
     assert ei.value.status == 3
     assert torch.all(y == 7.0)
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_glm_layer_recipe_full_size(T):
+    """The GLM-scale layer as bench.py runs it (router + grouping; gate/up
+    with SwiGLU in one launch; down; combine; at one token the fp32
+    activations are quantized inside the expert GEMVs, at 16 tokens by
+    standalone launches) equals, bit for bit at every stage, the same layer
+    with separate gate and up launches, the SwiGLU kernel and Q8_0 launches;
+    at one token the output is also within relative L2 1e-4 of the oracle
+    layer (SwiGLU in fp32 vs float64 may move an activation code by one)."""
+    qmm = lib()
+    c = workloads.MOE
+    H, F, E, k = c["hidden"], c["expert_ffn"], c["experts"], c["top_k"]
+    logits = workloads.router_logits(T, E, seed=3)
+    wsb = qmm.qmm_moe_workspace_size(E, T, k)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    ids = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    gts = torch.empty(T, k, device=DEV)
+    qmm.qmm_moe_router_topk(logits.to(DEV), T, E, k, ids, gts, ws, wsb)
+    used = np.unique(ids.cpu().numpy())
+    keep = used if T == 1 else []
+    gate = Experts(qmm, E, F, H, used, seed=3, base_index=0, device_gen=DEV, oracle_ids=keep)
+    up = Experts(qmm, E, F, H, used, seed=3, base_index=1000, device_gen=DEV, oracle_ids=keep)
+    down = Experts(qmm, E, H, F, used, seed=3, base_index=2000, device_gen=DEV, oracle_ids=keep)
+    gu_qs, gu_d = _interleave(gate.qs, up.qs), _interleave(gate.d, up.d)
+    x = workloads.activations(T, H, seed=4)
+    xf = x.to(DEV).contiguous()
+    xq, xd = qmm.quantize_q8_0(xf)
+
+    # the bench recipe
+    h = torch.empty(T * k, F, device=DEV)
+    z = torch.empty(T * k, H, device=DEV)
+    y = torch.empty(T, H, device=DEV)
+    if T * k * 4 <= E:
+        qmm.qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, xf, None, None, 0, h, ws, wsb)
+        qmm.qmm_moe_gemv_pregrouped_f32(down.qs, down.d, E, H, F, T, k, h, 1, z, ws, wsb)
+    else:
+        qmm.qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, None, xq, xd, 0, h, ws, wsb)
+        hq, hd = qmm.quantize_q8_0(h)
+        qmm.qmm_moe_gemv_pregrouped(down.qs, down.d, E, H, F, T, k, hq, hd, 1, z, ws, wsb)
+    qmm.qmm_moe_combine(z, gts, T, k, H, y)
+
+    # the unfused layer
+    yg = torch.empty(T * k, F, device=DEV)
+    yu = torch.empty(T * k, F, device=DEV)
+    qmm.qmm_moe_gemv_pregrouped(gate.qs, gate.d, E, F, H, T, k, xq, xd, 0, yg, ws, wsb)
+    qmm.qmm_moe_gemv_pregrouped(up.qs, up.d, E, F, H, T, k, xq, xd, 0, yu, ws, wsb)
+    h2 = torch.empty(T * k, F, device=DEV)
+    h2q = torch.empty(T * k, F, dtype=torch.int8, device=DEV)
+    h2d = torch.empty(T * k, F // 32, dtype=torch.int16, device=DEV)
+    qmm.qmm_swiglu_quantize_q8_0(yg, yu, T * k, F, F, h2q, h2d, h2)
+    z2 = torch.empty(T * k, H, device=DEV)
+    qmm.qmm_moe_gemv_pregrouped(down.qs, down.d, E, H, F, T, k, h2q, h2d, 1, z2, ws, wsb)
+    y2 = torch.empty(T, H, device=DEV)
+    qmm.qmm_moe_combine(z2, gts, T, k, H, y2)
+    assert qmm.qmm_last_device_error() == 0
+    assert torch.equal(h, h2)
+    assert torch.equal(z, z2)
+    assert torch.equal(y, y2)
+
+    if T == 1:
+        qx, dx = O.quantize_q8_0(x.numpy())
+        ref_ids, ref_g = O.router_topk(logits.numpy(), k)
+        assert np.array_equal(ids.cpu().numpy(), ref_ids)
+        y_ref, _, _ = O.moe_forward(gate.oracle, up.oracle, down.oracle, ref_ids, ref_g.astype(np.float32), qx, dx)
+        rel = np.linalg.norm(y.cpu().numpy() - y_ref) / np.linalg.norm(y_ref)
+        assert rel <= 1e-4, rel
