@@ -5,7 +5,9 @@ Shapes are chosen for the kernel's row plan on a 152-SM GB300: one partial
 MMA tile (rows not a multiple of 32), two tiles per super-tile, several
 super-tiles per CTA with a short last CTA, K of one and of several 8-block
 chunks, 2..16 tokens.  fp32 outputs: |y - y_ref| <= 1e-5*S + 1e-6; with unit
-scales every output is an exact integer and must match bit for bit."""
+scales every output is an exact integer and must match bit for bit.  Also
+here: the dp4a streaming kernel forced through the same selector
+(qmm_debug_gemm_kernel) against the oracle, and the tcgen05.mma cost probe."""
 import numpy as np
 import pytest
 import torch
