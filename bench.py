@@ -382,29 +382,33 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
 
 
 def bench_moe_store(qmm, torch, T=1, dev="cuda"):
-    """GLM-scale MoE layer with an expert store: all 256 experts (gate, up,
-    down planes; 21.2 MB each) in pinned host memory, 64 of them resident in
-    a slot arena in HBM.  Each decode step: router on the device, its expert
-    ids to the host, store request (copies of missing experts on a copy
-    stream), ids remapped to slots, the layer on the arena, release.  Routing
-    is skewed by a fixed per-expert bias.  Timed end to end (the host reads
-    each step's ids), after as many warm-up steps as timed ones."""
+    """GLM-scale MoE layer with an expert store: all 256 experts (interleaved
+    gate/up planes and down planes; 21.2 MB each) in pinned host memory, 64
+    of them resident in a slot arena in HBM.  Each decode step: router on the
+    device, its expert ids to the host, store request (copies of missing
+    experts on a copy stream), ids remapped to slots and grouped, the layer on
+    the arena (gate/up with SwiGLU in one launch, down, combine), release.
+    Routing is skewed by a fixed per-expert bias.  Timed end to end (the host
+    reads each step's ids), after as many warm-up steps as timed ones."""
     import numpy as np
     c = workloads.MOE
     H, F, E, k = c["hidden"], c["expert_ffn"], c["experts"], c["top_k"]
     S, steps = c["store_slots"], c["store_steps"]
-    shapes = {"gate": (F, H), "up": (F, H), "down": (H, F)}
+    # gate/up: rows interleaved per expert (g0, u0, g1, u1, ...), 2F x H
+    shapes = {"gate_up": (2 * F, H, (0, 1)), "down": (H, F, (2,))}
     host, arena = {}, {}
-    for j, (name, (N, K)) in enumerate(shapes.items()):
+    for name, (N, K, kinds) in shapes.items():
         hq = torch.empty(E, N, K // 2, dtype=torch.uint8, pin_memory=True)
         hd = torch.empty(E, N, K // 32, dtype=torch.int16, pin_memory=True)
-        tq = torch.empty(N, K // 2, dtype=torch.uint8, device=dev)
-        td = torch.empty(N, K // 32, dtype=torch.int16, device=dev)
+        rows = N // len(kinds)
+        tq = [torch.empty(rows, K // 2, dtype=torch.uint8, device=dev) for _ in kinds]
+        td = [torch.empty(rows, K // 32, dtype=torch.int16, device=dev) for _ in kinds]
         for e in range(E):
-            w = workloads.weights(N, K, sigma=c["sigma"], seed=0, index=1000 * j + e, device=dev)
-            qmm.qmm_quantize_q4_0(w, N, K, K, tq, td)
-            hq[e].copy_(tq)
-            hd[e].copy_(td)
+            for j, kind in enumerate(kinds):
+                w = workloads.weights(rows, K, sigma=c["sigma"], seed=0, index=1000 * kind + e, device=dev)
+                qmm.qmm_quantize_q4_0(w, rows, K, K, tq[j], td[j])
+            hq[e].copy_(torch.stack(tq, dim=1).reshape(N, K // 2))
+            hd[e].copy_(torch.stack(td, dim=1).reshape(N, K // 32))
         host[name] = (hq, hd)
         arena[name] = (torch.empty(S, N, K // 2, dtype=torch.uint8, device=dev),
                        torch.empty(S, N, K // 32, dtype=torch.int16, device=dev))
@@ -417,10 +421,7 @@ def bench_moe_store(qmm, torch, T=1, dev="cuda"):
     ids = torch.empty(T, k, dtype=torch.int32, device=dev)
     slot_ids = torch.empty_like(ids)
     gts = torch.empty(T, k, device=dev)
-    xq = torch.empty(T, H, dtype=torch.int8, device=dev)
-    xd = torch.empty(T, H // 32, dtype=torch.int16, device=dev)
-    yg, yu = torch.empty(T * k, F, device=dev), torch.empty(T * k, F, device=dev)
-    hq_, hd_ = torch.empty(T * k, F, dtype=torch.int8, device=dev), torch.empty(T * k, F // 32, dtype=torch.int16, device=dev)
+    h = torch.empty(T * k, F, device=dev)
     z, y = torch.empty(T * k, H, device=dev), torch.empty(T, H, device=dev)
     wsb = qmm.qmm_moe_workspace_size(E, T, k)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
@@ -433,12 +434,11 @@ def bench_moe_store(qmm, torch, T=1, dev="cuda"):
         torch.cuda.current_stream().synchronize()  # the host needs the ids to drive the copies
         store.request(ids_host.view(-1).tolist(), compute, copy)
         store.map_ids(ids, slot_ids)
-        qmm.qmm_quantize_q8_0(x, T, H, H, xq, xd)
-        ag, au, ad = arena["gate"], arena["up"], arena["down"]
-        qmm.qmm_moe_gemv(ag[0], ag[1], S, F, H, slot_ids, T, k, xq, xd, 0, yg, ws, wsb)
-        qmm.qmm_moe_gemv_pregrouped(au[0], au[1], S, F, H, T, k, xq, xd, 0, yu, ws, wsb)
-        qmm.qmm_swiglu_quantize_q8_0(yg, yu, T * k, F, F, hq_, hd_)
-        qmm.qmm_moe_gemv_pregrouped(ad[0], ad[1], S, H, F, T, k, hq_, hd_, 1, z, ws, wsb)
+        qmm.qmm_moe_group_ids(slot_ids, T, k, S, ws, wsb)
+        agu, ad = arena["gate_up"], arena["down"]
+        # fp32 activations quantized inside the expert GEMVs (few routed slots per pass)
+        qmm.qmm_moe_gemv_gate_up(agu[0], agu[1], S, 2 * F, H, T, k, x, None, None, 0, h, ws, wsb)
+        qmm.qmm_moe_gemv_pregrouped_f32(ad[0], ad[1], S, H, F, T, k, h, 1, z, ws, wsb)
         qmm.qmm_moe_combine(z, gts, T, k, H, y)
         store.release(compute)
 

@@ -717,7 +717,8 @@ qmm_status moe_apply(const DevInfo* di, const uint8_t* w_qs, const uint16_t* w_d
         // 0.552 with two, 0.665 with one; 1 token fastest with one.
         const int mt = nslots * 4 > (int64_t)E ? 4 : 1;
         const int64_t xtile = round_up((int64_t)mt * B * xtile_bytes_per_block(), 128);
-        const int64_t tables = round_up((int64_t)E * 12, 128);  // active list + slot spans in shared memory
+        // active list (padded to an even count) + 8-byte slot spans in shared memory
+        const int64_t tables = round_up((int64_t)((E + 1) & ~1) * 4 + (int64_t)E * 8, 128);
         // two CTAs per SM (110 KB each): more warps to hide the dot-product latency
         const int64_t nst =
             std::min<int64_t>((110 * 1024 - STREAM_HDR - xtile - tables) / STAGE_BYTES, STREAM_MAX_STAGES);
@@ -822,6 +823,24 @@ qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int
     s = launch_status();
     if (s != QMM_OK) return s;
     return moe_apply(di, w_qs, w_d, E, N, K, T, k, xq, xd, x_per_slot, y, ws, st);
+}
+
+qmm_status qmm_moe_group_ids(const int32_t* ids, int32_t T, int32_t k, int32_t E, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    if (E <= 0 || T < 0 || k <= 0) return QMM_ERR_ARG;
+    if ((int64_t)T * k > (1 << 24)) return QMM_ERR_SHAPE;
+    if (T == 0) return QMM_OK;
+    if (!ids || !workspace) return QMM_ERR_ARG;
+    if (workspace_bytes < moe_ws_bytes(E, (int64_t)T * k)) return QMM_ERR_WORKSPACE;
+    if (!aligned(ids, 4) || !aligned(workspace, 16)) return QMM_ERR_ALIGN;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    if (launch(moe_group_kernel, dim3(1), dim3(GROUP_THREADS), 0, S(stream), true, ids, T * k, E,
+               moe_ws(workspace, E), di->err) != cudaSuccess) {
+        cudaGetLastError();
+        return QMM_ERR_CUDA;
+    }
+    return launch_status();
 }
 
 qmm_status qmm_moe_gemv_pregrouped(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,

@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
     // memory (the walk below consults them for every row group)
     const int n_active = *a.ws.n_active;
     int* s_active = reinterpret_cast<int*>(ring + (size_t)S * STAGE_BYTES);
-    int2* s_span = reinterpret_cast<int2*>(s_active + a.E);
+    int2* s_span = reinterpret_cast<int2*>(s_active + ((a.E + 1) & ~1));  // 8-byte aligned for any E
     for (int i = tid; i < n_active; i += blockDim.x) {
         const int e = a.ws.active[i];
         s_active[i] = e;

@@ -91,6 +91,7 @@ SIGNATURES = {
     "qmm_gemv_q4_0_f32_fma": [_P, _P, _I64, _I64, _P, _P, _P],
     "qmm_moe_gemv_pregrouped": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
     "qmm_moe_gemv_gate_up": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _P, _P, _INT, _P, _P, _SZ, _P],
+    "qmm_moe_group_ids": [_P, _I32, _I32, _I32, _P, _SZ, _P],
     "qmm_moe_gemv_pregrouped_f32": [_P, _P, _I32, _I64, _I64, _I32, _I32, _P, _INT, _P, _P, _SZ, _P],
     "qmm_last_device_error": [_P],
 }
@@ -355,6 +356,11 @@ def qmm_moe_gemv_gate_up(w_qs, w_d, E, N, K, T, k, x, xq, xd, x_per_slot, h, wor
     _check(_lib.qmm_moe_gemv_gate_up(_ptr(w_qs), _ptr(w_d), E, N, K, T, k, _ptr(x), _ptr(xq), _ptr(xd),
                                      int(x_per_slot), _ptr(h), _ptr(workspace), workspace_bytes, _stream(stream)),
            "qmm_moe_gemv_gate_up")
+
+
+def qmm_moe_group_ids(ids, T, k, E, workspace, workspace_bytes, stream=None):
+    _check(_lib.qmm_moe_group_ids(_ptr(ids), T, k, E, _ptr(workspace), workspace_bytes, _stream(stream)),
+           "qmm_moe_group_ids")
 
 
 def qmm_moe_gemv_pregrouped_f32(w_qs, w_d, E, N, K, T, k, x, x_per_slot, y, workspace, workspace_bytes, stream=None):

@@ -370,6 +370,18 @@ QMM_API qmm_status qmm_moe_gemv(const uint8_t* w_qs, const uint16_t* w_d, int32_
 QMM_API qmm_status qmm_moe_router_topk(const float* logits, int32_t T, int32_t E, int32_t k, int32_t* ids,
                                        float* gates, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The slot grouping of qmm_moe_gemv on its own: groups the T*k slots of
+ * ids (int32 [T][k], device, values in [0, E)) by expert into workspace,
+ * exactly the tables qmm_moe_router_topk builds there for its chosen ids.
+ * For ids that do not come from the router (e.g. remapped to the slots of an
+ * expert store) before qmm_moe_gemv_pregrouped, qmm_moe_gemv_pregrouped_f32
+ * or qmm_moe_gemv_gate_up.  An id outside [0, E) is left out of the tables
+ * and sets the device error word (QMM_ERR_BAD_EXPERT_ID).  workspace: >=
+ * qmm_moe_workspace_size(E, T, k) bytes, 16-byte aligned.  T == 0 is a
+ * no-op. */
+QMM_API qmm_status qmm_moe_group_ids(const int32_t* ids, int32_t T, int32_t k, int32_t E, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
 /* qmm_moe_gemv on the slot grouping that qmm_moe_router_topk left in
  * workspace for the same E, T and k (no ids argument, no grouping launch):
  * every later expert GEMV of a MoE layer (gate, up, down) reuses one

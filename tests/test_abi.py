@@ -214,3 +214,9 @@ def test_gemm_kernel_selector_and_moe_fp32_validation(qmm):
     assert lib2.qmm_debug_tcgen05_mma_cycles(0, 16, 1, 0, ctypes.c_void_p(A16), None) == 1   # iters < 1
     assert lib2.qmm_debug_tcgen05_mma_cycles(0, 16, 1, 8, None, None) == 1                   # no output
     assert lib2.qmm_debug_tcgen05_mma_cycles(0, 16, 1, 8, ctypes.c_void_p(A16 + 4), None) == 3  # misaligned
+    gi = lambda *a: _call(qmm, "qmm_moe_group_ids", *a)  # noqa: E731
+    assert gi(A16, 16, 0, 256, A16, n, None) == 1            # k = 0
+    assert gi(A16, 16, 8, 256, None, n, None) == 1           # no workspace
+    assert gi(A16, 16, 8, 256, A16, n - 16, None) == 8       # workspace too small
+    assert gi(A16 + 2, 16, 8, 256, A16, n, None) == 3        # ids misaligned
+    assert gi(A16, 0, 8, 256, A16, n, None) == 0             # T = 0: no-op

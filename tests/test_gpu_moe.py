@@ -44,7 +44,8 @@ def _moe_gemv(qmm, ex, ids, T, k, xq, xd, x_per_slot):
     return y
 
 
-@pytest.mark.parametrize("T,E,k,N,K", [(1, 8, 2, 64, 96), (16, 64, 8, 300, 512), (5, 4, 4, 17, 2048)])
+@pytest.mark.parametrize("T,E,k,N,K", [(1, 8, 2, 64, 96), (16, 64, 8, 300, 512), (5, 4, 4, 17, 2048),
+                                         (5, 33, 4, 64, 512), (16, 33, 8, 40, 256)])
 def test_moe_gemv_shared_x(T, E, k, N, K):
     qmm = lib()
     ids, _ = _ids_gates(T, E, k, seed=T)

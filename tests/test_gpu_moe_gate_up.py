@@ -230,3 +230,48 @@ def test_glm_layer_recipe_full_size(T):
         y_ref, _, _ = O.moe_forward(gate.oracle, up.oracle, down.oracle, ref_ids, ref_g.astype(np.float32), qx, dx)
         rel = np.linalg.norm(y.cpu().numpy() - y_ref) / np.linalg.norm(y_ref)
         assert rel <= 1e-4, rel
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 64, 8), (16, 256, 8), (5, 33, 4)])
+def test_group_ids_tables_and_gate_up_on_them(T, E, k):
+    """qmm_moe_group_ids on ids that are not the router's (random, with
+    duplicates inside a token): the tables equal the counting definition; and
+    on the router's own ids the fused gate/up over these tables equals, bit
+    for bit, the same launch over the router's grouping."""
+    from test_gpu_router import _check_grouping
+    qmm = lib()
+    rng = np.random.default_rng(T * 100 + E)
+    ids_any = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    ids_any[0, :2] = 0  # a duplicate expert inside one token
+    wsb = qmm.qmm_moe_workspace_size(E, T, k)
+    ws = torch.full((wsb,), 0xCD, dtype=torch.uint8, device=DEV)  # need not start initialised
+    qmm.qmm_moe_group_ids(torch.from_numpy(ids_any).to(DEV), T, k, E, ws, wsb)
+    assert qmm.qmm_last_device_error() == 0
+    _check_grouping(ws, ids_any, E)
+
+    F, H = 256, 512
+    ids, ws_r, _, gate, up, x, xq, xd = _layer_inputs(qmm, T, E, k, F, H, 0, seed=T + 7)
+    gu_qs, gu_d = _interleave(gate.qs, up.qs), _interleave(gate.d, up.d)
+    h_r = torch.full((T * k, F), float("nan"), device=DEV)
+    qmm.qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, None, xq, xd, 0, h_r, ws_r, wsb)
+    ws_g = torch.empty(wsb, dtype=torch.uint8, device=DEV)
+    qmm.qmm_moe_group_ids(torch.from_numpy(ids).to(DEV), T, k, E, ws_g, wsb)
+    h_g = torch.full((T * k, F), float("nan"), device=DEV)
+    qmm.qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, None, xq, xd, 0, h_g, ws_g, wsb)
+    assert qmm.qmm_last_device_error() == 0
+    assert torch.equal(h_g, h_r)
+
+
+def test_group_ids_reports_an_id_out_of_range():
+    """An id outside [0, E) is left out of the tables and reported through
+    the device error word; the other slots are grouped."""
+    qmm = lib()
+    T, E, k = 2, 8, 2
+    ids = np.array([[1, 9], [3, 1]], np.int32)
+    wsb = qmm.qmm_moe_workspace_size(E, T, k)
+    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
+    qmm.qmm_last_device_error()
+    qmm.qmm_moe_group_ids(torch.from_numpy(ids).to(DEV), T, k, E, ws, wsb)
+    assert qmm.qmm_last_device_error() == 7
+    w = ws.view(torch.int32).cpu().numpy()
+    assert w[1] == 2 and w[3] == 1 and w[4 * E + 1] == 2  # counts of experts 1 and 3; two active
