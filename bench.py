@@ -485,18 +485,6 @@ def run_case(qmm, torch, name, calls, dev="cuda"):
         return {"case": name, **bench_gemm_b16(qmm, torch, reps=max(calls, 3))}
     elif name == "moe_T16":
         return _moe_case(qmm, torch, calls, dev)
-    elif name == "tcgen05_mma_cost":  # cycles per tcgen05.mma, one issuing thread, independent D slices
-        cyc = torch.zeros(1, dtype=torch.int64, device=dev)
-        iters, rows = 256, []
-        for kind, n, a_tmem in ((0, 16, 0), (0, 16, 1), (0, 32, 1), (0, 32, 0), (0, 64, 1), (1, 16, 1), (1, 32, 1),
-                                (1, 32, 0)):
-            for _ in range(2):  # the second launch is timed warm
-                qmm.qmm_debug_tcgen05_mma_cycles(kind, n, a_tmem, iters, cyc)
-            torch.cuda.synchronize()
-            rows.append({"kind": "f16 (K=16)" if kind == 0 else "f8f6f4 e4m3 (K=32)", "M": 128, "N": n,
-                         "A": "tensor memory" if a_tmem else "shared memory",
-                         "cycles_per_mma": round(int(cyc.item()) / (iters * 8), 1)})
-        return {"case": name, "mmas_per_launch": iters * 8, "rows": rows}
     elif name in ("moe_layer_T1", "moe_layer_T16"):  # the whole MoE layer of the default line
         return {"case": name, **bench_moe(qmm, torch, T=1 if name == "moe_layer_T1" else 16, reps=max(calls, 3))}
     elif name == "moe_store":
@@ -834,7 +822,7 @@ def main():
     ap.add_argument("--case", default=None,
                     help="time one kernel instead: decode_gateup, decode_qkv_norm, decode_chain, decode_pdl, lm_head_8192, "
                          "gemm_b16, gemm_b16_dense, "
-                         "gemm_b64, moe_T16, moe_layer_T1, moe_layer_T16, moe_store, tcgen05_mma_cost")
+                         "gemm_b64, moe_T16, moe_layer_T1, moe_layer_T16, moe_store")
     ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "mma", "tmem", "stream"],
                     help="small-batch GEMM kernel (qmm_debug_gemm_kernel): automatic choice, warp MMA, tcgen05 or "
                          "dp4a streaming")

@@ -609,107 +609,3 @@ qmm_status gemm_tmem_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N,
 
 }  // namespace qmm
 
-// ============================================================================
-// Cost of one tcgen05.mma: one thread issues `iters` x 8 independent MMAs
-// (M = 128, N columns, A from shared or tensor memory, zero operands) into 8
-// D slices, commits, waits (bounded), and writes the elapsed SM clock count.
-// ============================================================================
-namespace qmm {
-namespace tmk {
-
-template <int KIND, int N, bool A_TMEM>  // KIND 0: kind::f16 (K = 16), 1: kind::f8f6f4 e4m3 (K = 32)
-__global__ void __launch_bounds__(128, 1) mma_cost_kernel(unsigned long long* cycles, int iters) {
-    __shared__ __align__(1024) uint8_t sm[32768];
-    __shared__ uint32_t tslot;
-    __shared__ __align__(8) uint64_t bar;
-    const int warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < 32768 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(sm)[i] = 0u;
-    if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tslot)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tm = tslot;
-    if (threadIdx.x == 0) {
-        const uint32_t idesc = (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-        const uint64_t bd = smem_desc(sm + 16384, 256, 128);
-        const uint64_t ad = smem_desc(sm, 128 * 16, 128);
-        const long long t0 = clock64();
-        for (int it = 0; it < iters; ++it) {
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                // A in columns [0, 64), D slices of N columns in [64, 512)
-                const uint32_t d = tm + 64u + (uint32_t)((s * N) % 448);
-                if (KIND == 0 && A_TMEM)
-                    asm volatile("{.reg .pred p; setp.ne.b32 p, 0, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;}"
-                                 ::"r"(d), "r"(tm + (uint32_t)(s * 8)), "l"(bd), "r"(idesc));
-                if (KIND == 0 && !A_TMEM)
-                    asm volatile("{.reg .pred p; setp.ne.b32 p, 0, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;}"
-                                 ::"r"(d), "l"(ad), "l"(bd), "r"(idesc));
-                if (KIND == 1 && A_TMEM)
-                    asm volatile("{.reg .pred p; setp.ne.b32 p, 0, 0; tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;}"
-                                 ::"r"(d), "r"(tm + (uint32_t)(s * 8)), "l"(bd), "r"(idesc));
-                if (KIND == 1 && !A_TMEM)
-                    asm volatile("{.reg .pred p; setp.ne.b32 p, 0, 0; tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;}"
-                                 ::"r"(d), "l"(ad), "l"(bd), "r"(idesc));
-            }
-        }
-        mma_commit(&bar);
-        const uint64_t w0 = global_ns();
-        while (!mbar_try_wait(&bar, 0) && global_ns() - w0 < WAIT_LIMIT_NS) {
-        }
-        *cycles = (unsigned long long)(clock64() - t0);
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(TMEM_COLS) : "memory");
-}
-
-template <int KIND, int N, bool A_TMEM>
-cudaError_t launch_mma_cost(unsigned long long* cycles, int iters, cudaStream_t st) {
-    mma_cost_kernel<KIND, N, A_TMEM><<<1, 128, 0, st>>>(cycles, iters);
-    return cudaGetLastError();
-}
-
-}  // namespace tmk
-
-qmm_status mma_cost_launch(int kind, int n, int a_in_tmem, int iters, unsigned long long* cycles, cudaStream_t st) {
-    using namespace tmk;
-    cudaError_t e;
-    const bool t = a_in_tmem != 0;
-    if (kind == 0 && n == 16) e = t ? launch_mma_cost<0, 16, true>(cycles, iters, st) : launch_mma_cost<0, 16, false>(cycles, iters, st);
-    else if (kind == 0 && n == 32) e = t ? launch_mma_cost<0, 32, true>(cycles, iters, st) : launch_mma_cost<0, 32, false>(cycles, iters, st);
-    else if (kind == 0 && n == 64) e = t ? launch_mma_cost<0, 64, true>(cycles, iters, st) : launch_mma_cost<0, 64, false>(cycles, iters, st);
-    else if (kind == 1 && n == 16) e = t ? launch_mma_cost<1, 16, true>(cycles, iters, st) : launch_mma_cost<1, 16, false>(cycles, iters, st);
-    else if (kind == 1 && n == 32) e = t ? launch_mma_cost<1, 32, true>(cycles, iters, st) : launch_mma_cost<1, 32, false>(cycles, iters, st);
-    else return QMM_ERR_ARG;
-    return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
-}
-
-}  // namespace qmm
-
-extern "C" qmm_status qmm_debug_tcgen05_mma_cycles(int kind, int n, int a_in_tmem, int iters,
-                                                    unsigned long long* cycles, void* stream) {
-    if (!cycles || iters < 1 || iters > (1 << 20)) return QMM_ERR_ARG;
-    if (reinterpret_cast<uintptr_t>(cycles) % 8) return QMM_ERR_ALIGN;
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-        cudaGetLastError();
-        return QMM_ERR_DEVICE;
-    }
-    if (major != 10 || minor != 3) return QMM_ERR_DEVICE;
-    return qmm::mma_cost_launch(kind, n, a_in_tmem, iters, cycles, static_cast<cudaStream_t>(stream));
-}

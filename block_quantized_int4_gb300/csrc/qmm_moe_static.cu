@@ -59,11 +59,13 @@ qmm_status qmm_moe_gemv_static(const uint8_t* w_qs, const uint16_t* w_d, int32_t
     if (E <= 0 || N <= 0 || T < 0 || k <= 0) return QMM_ERR_ARG;
     if (K <= 0 || K % QMM_QK != 0 || K > ((int64_t)1 << 30) || (int64_t)T * k > (1 << 24)) return QMM_ERR_SHAPE;
     if (T == 0) return QMM_OK;
-    if (!w_qs || !w_d || !ids || !xq || !xd || !y) return QMM_ERR_ARG;
+    if (!w_qs || !w_d || !xq || !xd || !y) return QMM_ERR_ARG;
     const auto misaligned = [](const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a != 0; };
-    if (misaligned(w_qs, 16) || misaligned(w_d, 2) || misaligned(xq, 16) || misaligned(xd, 2) || misaligned(y, 4) ||
-        misaligned(ids, 4))
+    if (misaligned(w_qs, 16) || misaligned(w_d, 2) || misaligned(xq, 16) || misaligned(xd, 2) || misaligned(y, 4))
         return QMM_ERR_ALIGN;
+    // the workspace entry checks ids after the other pointers
+    if (!ids) return QMM_ERR_ARG;
+    if (misaligned(ids, 4)) return QMM_ERR_ALIGN;
     size_t need = 0;
     qmm_status s = qmm_moe_workspace_size(E, T, k, &need);
     if (s != QMM_OK) return s;

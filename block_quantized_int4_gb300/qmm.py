@@ -67,7 +67,6 @@ SIGNATURES = {
     "qmm_gemm_q4_0_q8_0": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P],
     "qmm_debug_block_dots": [_P, _I64, _I64, _I64, _P, _P, _P],
     "qmm_debug_gemm_kernel": [_INT, ctypes.POINTER(_INT)],
-    "qmm_debug_tcgen05_mma_cycles": [_INT, _INT, _INT, _INT, _P, _P],
     "qmm_gemv_chain_workspace_size": [_I32, ctypes.POINTER(_SZ)],
     "qmm_gemv_chain": [ctypes.POINTER(GemvOp), _I32, _P, _SZ, _P],
     "qmm_gemv_fused_op": [ctypes.POINTER(GemvOp), _INT, _P],
@@ -190,11 +189,6 @@ def qmm_debug_gemm_kernel(kernel):
     prev = ctypes.c_int(0)
     _check(_lib.qmm_debug_gemm_kernel(kernel, ctypes.byref(prev)), "qmm_debug_gemm_kernel")
     return prev.value
-
-
-def qmm_debug_tcgen05_mma_cycles(kind, n, a_in_tmem, iters, cycles, stream=None):
-    _check(_lib.qmm_debug_tcgen05_mma_cycles(kind, n, int(a_in_tmem), iters, _ptr(cycles), _stream(stream)),
-           "qmm_debug_tcgen05_mma_cycles")
 
 
 def qmm_debug_block_dots(w_qs, N, K, M, xq, dots, stream=None):

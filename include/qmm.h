@@ -54,7 +54,7 @@ extern "C" {
 #endif
 
 #define QMM_QK 32        /* values per block */
-#define QMM_ABI_VERSION 1
+#define QMM_ABI_VERSION 2
 
 typedef enum qmm_status {
     QMM_OK = 0,
@@ -195,17 +195,6 @@ QMM_API qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, 
 #define QMM_GEMM_KERNEL_TMEM 2
 #define QMM_GEMM_KERNEL_STREAM 3
 QMM_API qmm_status qmm_debug_gemm_kernel(int kernel, int* previous);
-
-/* Measurement hook (no counterpart on the pages): SM clock cycles that one
- * thread takes to issue iters x 8 independent tcgen05.mma instructions of
- * M = 128 and N columns on zero operands, commit and see them complete.
- * kind 0: kind::f16 (K = 16), n in {16, 32, 64}; kind 1: kind::f8f6f4 with
- * e4m3 operands (K = 32), n in {16, 32}; the A operand in tensor memory when
- * a_in_tmem != 0, else in shared memory.  One CTA; *cycles (device, 8-byte
- * aligned, caller-owned) receives the count.  1 <= iters <= 2^20, else
- * QMM_ERR_ARG; QMM_ERR_DEVICE off sm_103. */
-QMM_API qmm_status qmm_debug_tcgen05_mma_cycles(int kind, int n, int a_in_tmem, int iters,
-                                                unsigned long long* cycles, void* stream);
 
 /* Per-block integer dots, for bit-exact checking: dots[(m*N + n)*B + b] =
  * sum_{i<32} q_w * q_x, int32, computed with the product kernels' own

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol(qmm):
 
 
 def test_status_strings_and_version(qmm):
-    assert qmm.abi_version() == 1
+    assert qmm.abi_version() == 2
     for code, name in qmm.STATUS.items():
         assert qmm.status_string(code).startswith(name)
     assert "UNKNOWN" in qmm.status_string(99)
@@ -96,6 +96,12 @@ def test_static_scratch_limit_and_arguments(qmm):
     assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, A16, 0, 2, A16, A16, 0, A16, None) == 0
     assert _call(qmm, "qmm_moe_gemv_static", A16 + 2, A16, 8, 64, 64, A16, 1, 2, A16, A16, 0, A16, None) == 3
     assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, None, 1, 2, A16, A16, 0, A16, None) == 1
+    # ids are checked after the other pointers, as qmm_moe_gemv does: a null
+    # ids with a misaligned weight plane is an alignment error in both
+    ws = qmm.qmm_moe_workspace_size(8, 1, 2)
+    assert _call(qmm, "qmm_moe_gemv", A16 + 2, A16, 8, 64, 64, None, 1, 2, A16, A16, 0, A16, A16, ws, None) == 3
+    assert _call(qmm, "qmm_moe_gemv_static", A16 + 2, A16, 8, 64, 64, None, 1, 2, A16, A16, 0, A16, None) == 3
+    assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, A16 + 2, 1, 2, A16, A16, 0, A16, None) == 3
 
 
 def test_chain_validation(qmm):
@@ -210,10 +216,6 @@ def test_gemm_kernel_selector_and_moe_fp32_validation(qmm):
     assert g(A16, A16, 256, 63, 256, 16, 8, None, A16, A16, 0, A16, A16, n, None) == 2  # N odd
     assert g(A16, A16, 256, 64, 256, 16, 8, A16 + 4, None, None, 0, A16, A16, n, None) == 3  # fp32 x misaligned
     assert g(A16, A16, 256, 64, 256, 16, 8, None, A16, A16, 0, A16, A16, n - 16, None) == 8  # workspace
-    lib2 = qmm._lib
-    assert lib2.qmm_debug_tcgen05_mma_cycles(0, 16, 1, 0, ctypes.c_void_p(A16), None) == 1   # iters < 1
-    assert lib2.qmm_debug_tcgen05_mma_cycles(0, 16, 1, 8, None, None) == 1                   # no output
-    assert lib2.qmm_debug_tcgen05_mma_cycles(0, 16, 1, 8, ctypes.c_void_p(A16 + 4), None) == 3  # misaligned
     gi = lambda *a: _call(qmm, "qmm_moe_group_ids", *a)  # noqa: E731
     assert gi(A16, 16, 0, 256, A16, n, None) == 1            # k = 0
     assert gi(A16, 16, 8, 256, None, n, None) == 1           # no workspace

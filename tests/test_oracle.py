@@ -493,3 +493,73 @@ def test_matmul_q4_0_f32_against_numpy_and_brute_force():
     y3, _ = O.matmul_q4_0_f32(qw, dw, xdeq)
     y4, S4 = O.matmul_int(qw, dw, xq, xd)
     assert np.all(np.abs(y3 - y4) <= 1e-13 * S4)
+
+
+# ---------------------------------------------------------------- MoE layer (Colibri page, system architecture)
+def test_moe_forward_integer_grid_closed_form():
+    """moe_forward on an integer grid where every stage is exact, so the
+    layer has a closed form computed here with plain integer arithmetic.
+
+    Per slot j of token t (Colibri page's flow: experts compute, results are
+    combined by the gates; SwiGLU of the TinyLLaMA guide 4.4, silu(gate)*up):
+    - all scales are 1.0, and token t's activation codes are 127 at column
+      2t and 1 at column 2t + 1 (so its Q8_0 block has d = 1);
+    - gate rows hold 0 or 1 at column 2t and 0 at 2t + 1, so a = W_gate x is
+      0 or 127; sigmoid(127) is 1.0 in double, so silu(a) is 0 or 127 exactly;
+    - up rows hold m * s at column 2t + 1 (s in {-1, 0, 1}, m a power of two
+      per expert) and 0 at column 2t, so b = W_up x = m * s;
+    - h = silu(a) * b is 127 * m * s or 0; its Q8_0 block has d = m and codes
+      127 * s (or 0) exactly;
+    - z = W_down h_q = m * (integer dot), and y = sum_j g_j z_j with gates
+      that are exact binary fractions.
+    Ids repeat an expert inside token 1 (each slot is computed on its own), and
+    the experts differ, so a gate/up swap (silu(b) * a is not an integer), a
+    slot-to-expert index slip, or a combine over the wrong axis all change y."""
+    H = F = 32
+    E, T, k = 3, 2, 2
+    ids = np.array([[2, 0], [1, 1]], np.int32)
+    gates = np.array([[0.75, 0.25], [0.625, 0.375]], np.float32)
+    m_of = {0: 1, 1: 2, 2: 4}
+    one = np.uint16(0x3C00)  # fp16 1.0
+    fill = lambda f, e: ((f * 7 + e * 3) % 16) - 8  # noqa: E731  (columns the activations never touch)
+    gate, up, down = {}, {}, {}
+    for e in range(E):
+        g = np.zeros((F, H), np.int8)
+        u = np.zeros((F, H), np.int8)
+        for f in range(F):
+            g[f, 4:] = fill(f, e)
+            u[f, 4:] = fill(f + 1, e)
+            g[f, 0] = 1 if (f + e) % 3 else 0          # token 0's gate column
+            g[f, 2] = 1 if (f + 2 * e) % 4 else 0      # token 1's gate column
+            u[f, 1] = m_of[e] * (((f * 5 + e) % 3) - 1)   # token 0's up column
+            u[f, 3] = m_of[e] * (((f * 3 + 2 * e) % 3) - 1)  # token 1's up column
+        dn = np.array([[((n * 3 + f * 5 + e * 7) % 16) - 8 for f in range(F)] for n in range(H)], np.int8)
+        gate[e] = (g, np.full((F, 1), one))
+        up[e] = (u, np.full((F, 1), one))
+        down[e] = (dn, np.full((H, 1), one))
+    qx = np.zeros((T, H), np.int8)
+    qx[0, 0], qx[0, 1], qx[1, 2], qx[1, 3] = 127, 1, 127, 1
+    dx = np.full((T, 1), one)
+
+    y, z, h = O.moe_forward(gate, up, down, ids, gates, qx, dx)
+
+    # the closed form, in integers
+    z_ref = np.zeros((T, k, H), np.int64)
+    for t in range(T):
+        for j in range(k):
+            e, m = int(ids[t, j]), m_of[int(ids[t, j])]
+            a = gate[e][0].astype(np.int64) @ qx[t].astype(np.int64)
+            b = up[e][0].astype(np.int64) @ qx[t].astype(np.int64)
+            assert set(np.unique(a)) <= {0, 127} and (a == 127).any()
+            assert set(np.unique(b)) <= {-m, 0, m}
+            h_int = np.where(a == 127, 127 * b, 0)
+            assert np.abs(h_int).max() == 127 * m  # so the block scale is m and the codes h / m
+            assert np.array_equal(h[t, j], h_int.astype(np.float32))
+            z_ref[t, j] = m * (down[e][0].astype(np.int64) @ (h_int // m))
+    assert np.array_equal(z, z_ref.astype(np.float64))
+    y_ref = (gates[:, :, None].astype(np.float64) * z_ref).sum(axis=1)
+    assert np.array_equal(y, y_ref)
+    # two values worked out by hand as spot checks of the integer closed form
+    assert z_ref[0, 0, 0] == 4 * 127 * int(
+        sum(down[2][0][0, f] * np.sign(up[2][0][f, 1]) for f in range(F) if gate[2][0][f, 0]))
+    assert y[1, 5] == 0.625 * z_ref[1, 0, 5] + 0.375 * z_ref[1, 1, 5]

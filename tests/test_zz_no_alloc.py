@@ -2,8 +2,10 @@
 library's fixed device scratch (no workspace, no allocation) -- called through
 the C ABI twice in a row with different routings, each output checked
 against qmm_moe_gemv with a caller workspace and against the oracle, within
-the fp32 tolerance |y - y_ref| <= 1e-5 * S + 1e-6.  Collected last so it also
-runs after every other GPU test has used the device."""
+the fp32 tolerance |y - y_ref| <= 1e-5 * S + 1e-6; the second call is
+watched for device allocations (torch's allocator and the driver's free
+memory).  Collected last so it also runs after every other GPU test has used
+the device."""
 import numpy as np
 import pytest
 import torch
@@ -35,12 +37,6 @@ def _with_workspace(qmm, qs, d, E, N, K, ids, T, k, xq, xd, per_slot):
     return y
 
 
-def _static(qmm, qs, d, E, N, K, ids, T, k, xq, xd, per_slot):
-    y = torch.full((T * k, N), float("nan"), device=DEV)
-    qmm.qmm_moe_gemv_static(qs, d, E, N, K, ids, T, k, xq, xd, per_slot, y)
-    return y
-
-
 def test_static_scratch_moe_matches_workspace_entry_twice():
     qmm = lib()
     qmm.qmm_last_device_error()  # start from a clear device error word
@@ -56,11 +52,23 @@ def test_static_scratch_moe_matches_workspace_entry_twice():
     x1 = workloads.activations(T1, K, seed=13)
     x2 = workloads.activations(T2 * k2, K, seed=14)
     cases = [(ids1, T1, k1, x1, 0), (ids2, T2, k2, x2, 1)]
+    # every input and output exists before the first call, so the two calls
+    # below run back to back and the second one can be watched for allocations
     outs = []
-    for ids, T, k, x, per_slot in cases:  # two static calls in a row, nothing in between
+    for ids, T, k, x, per_slot in cases:
         xq, xd = qmm.quantize_q8_0(x.to(DEV))
         ids_d = torch.from_numpy(np.ascontiguousarray(ids, dtype=np.int32)).to(DEV)
-        outs.append((_static(qmm, qs, d, E, N, K, ids_d, T, k, xq, xd, per_slot), xq, xd, ids_d))
+        y = torch.full((T * k, N), float("nan"), device=DEV)
+        outs.append((y, xq, xd, ids_d))
+    torch.cuda.synchronize()
+    mem = []
+    for (ids, T, k, x, per_slot), (y, xq, xd, ids_d) in zip(cases, outs):  # two static calls in a row
+        qmm.qmm_moe_gemv_static(qs, d, E, N, K, ids_d, T, k, xq, xd, per_slot, y)
+        torch.cuda.synchronize()
+        mem.append((torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]))
+    # the second call (the device already set up by the first) allocated
+    # nothing: neither through torch's allocator nor from the driver
+    assert mem[1] == mem[0], mem
     for (ids, T, k, x, per_slot), (y_static, xq, xd, ids_d) in zip(cases, outs):
         y_ws = _with_workspace(qmm, qs, d, E, N, K, ids_d, T, k, xq, xd, per_slot)
         qx, dx = O.quantize_q8_0(x.numpy())
