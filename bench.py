@@ -25,7 +25,6 @@ import concurrent.futures
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -39,27 +38,29 @@ import workloads  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
-# ncu summary of the decode kernel (DRAM traffic per launch) and the sources it was taken from
-DECODE_PROFILE = os.path.join(ROOT, "profiles", "stream_rows_tinyllama_decode.md")
-DECODE_KERNEL_SOURCES = [os.path.join(ROOT, "block_quantized_int4_gb300", "csrc", f)
-                         for f in ("qmm_stream.cuh", "qmm_kernels.cuh", "qmm_device.cuh", "qmm_api.cu")]
+# DRAM traffic per launch of the decode step's kernel from an ncu capture, and
+# the sources it was taken from (a JSON record beside the ncu summaries)
+DECODE_TRAFFIC = os.path.join(ROOT, "profiles", "decode_step_traffic.json")
+
+
+def _sources_digest(paths):
+    h = hashlib.sha256()
+    for path in paths:
+        with open(os.path.join(ROOT, path), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def _profiled_traffic():
-    """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, or None once the kernel sources differ from the captured ones."""
+    """DRAM bytes per launch of the decode kernel from the committed capture
+    record, or None once the kernel sources differ from the captured ones."""
     try:
-        with open(DECODE_PROFILE) as f:
-            text = f.read()
-        traffic = int(re.search(r"traffic_bytes_per_launch:\s*(\d+)", text).group(1))
-        digest = re.search(r"kernel_sources_sha256:\s*([0-9a-f]+)", text).group(1)
-        h = hashlib.sha256()
-        for path in DECODE_KERNEL_SOURCES:
-            with open(path, "rb") as f:
-                h.update(f.read())
+        with open(DECODE_TRAFFIC) as f:
+            rec = json.load(f)
+        digest = _sources_digest(rec["sources"])
     except Exception:
         return None
-    return traffic if h.hexdigest().startswith(digest) else None
+    return int(rec["traffic_bytes_per_launch"]) if digest.startswith(rec["sources_sha256"]) else None
 
 
 def max_over_ranks(torch, times, device):
@@ -614,6 +615,52 @@ def _stats_keys(stats):
             "calls_per_replay": stats["calls_per_replay"]}
 
 
+def product_us(qmm, torch, N, K, M, sigma, fused_f32=False, dev="cuda"):
+    """Device time per call (us) of one Q4_0 x Q8_0 product of M tokens with
+    its weights cold in HBM (rotated over copies larger than L2): the batch-1
+    GEMV (M = 1), the small-batch GEMM, or the fused GEMV on an fp32 input."""
+    w = workloads.weights(N, K, sigma=sigma, seed=0, index=0, device=dev)
+    qs, d = qmm.quantize_q4_0(w)
+    del w
+    x = workloads.activations(M, K, seed=0, device=dev)
+    xq, xd = qmm.quantize_q8_0(x)
+    y = torch.empty(M, N, device=dev)
+
+    def make():
+        q2, d2 = qs.clone(), d.clone()
+        if fused_f32:
+            return lambda: qmm.qmm_gemv_fused(q2, d2, N, K, x[0], None, None, None, y[0], None, None)
+        if M == 1:
+            return lambda: qmm.qmm_gemv_q4_0_q8_0(q2, d2, N, K, xq[0], xd[0], y[0])
+        return lambda: qmm.qmm_gemm_q4_0_q8_0(q2, d2, N, K, M, xq, xd, y, N)
+
+    us = _rotated_us(torch, make, workloads.q4_0_bytes(N, K))
+    del qs, d
+    torch.cuda.empty_cache()
+    return us
+
+
+def bench_gemv_set(qmm, torch, name, mats, sigma, dev="cuda"):
+    """Batch-1 GEMVs (qmm_gemv_q4_0_q8_0, Q8_0 activation in) of a set of
+    matrices, each timed alone with its weights cold in HBM: per matrix and
+    for the set, weight GB/s and the fraction of the measured copy peak."""
+    peak, peak_kind = _peaks()
+    rows, tot_us, tot_b = [], 0.0, 0
+    for mname, N, K in mats:
+        us = product_us(qmm, torch, N, K, 1, sigma, dev=dev)
+        wb = workloads.q4_0_bytes(N, K)
+        tot_us += us
+        tot_b += wb
+        rows.append({"matrix": mname, "N": N, "K": K, "us_per_call": round(us, 2), "us_median": round(
+            _LAST_STATS["median"], 2), "weight_GBps": round(wb / us / 1e3, 1),
+            "frac_of_hbm_peak": round(wb / us / 1e3 / peak, 4)})
+    return {"metric": "batch-1 Q4_0xQ8_0 GEMV weight GB/s", "value": round(tot_b / tot_us / 1e3, 1),
+            "unit": "GB/s", "frac_of_hbm_peak": round(tot_b / tot_us / 1e3 / peak, 4), "peak_kind": peak_kind,
+            "us_per_set": round(tot_us, 2), "weight_bytes": tot_b, "matrices": rows,
+            "config": {"workload": name, "M": 1,
+                       "l2": "each matrix rotated over weight copies at least 3x the L2 (129 MB) in size"}}
+
+
 def run_configs(qmm, torch, dev="cuda"):
     """One JSON line per workload of the five configurations: kernel-only
     device time per call with weights cold in HBM, weight GB/s (and % of the
@@ -635,25 +682,7 @@ def run_configs(qmm, torch, dev="cuda"):
         out.append(d)
 
     def product(N, K, M, sigma, fused_f32=False):
-        w = workloads.weights(N, K, sigma=sigma, seed=0, index=0, device=dev)
-        qs, d = qmm.quantize_q4_0(w)
-        del w
-        x = workloads.activations(M, K, seed=0, device=dev)
-        xq, xd = qmm.quantize_q8_0(x)
-        y = torch.empty(M, N, device=dev)
-
-        def make():
-            q2, d2 = qs.clone(), d.clone()
-            if fused_f32:
-                return lambda: qmm.qmm_gemv_fused(q2, d2, N, K, x[0], None, None, None, y[0], None, None)
-            if M == 1:
-                return lambda: qmm.qmm_gemv_q4_0_q8_0(q2, d2, N, K, xq[0], xd[0], y[0])
-            return lambda: qmm.qmm_gemm_q4_0_q8_0(q2, d2, N, K, M, xq, xd, y, N)
-
-        us = _rotated_us(torch, make, workloads.q4_0_bytes(N, K))
-        del qs, d
-        torch.cuda.empty_cache()
-        return us
+        return product_us(qmm, torch, N, K, M, sigma, fused_f32, dev)
 
     # read-only stream reference: a 4 GiB fp32 sum (library reduction), the
     # third denominator beside the copy peak and the nominal 8 TB/s
@@ -905,6 +934,11 @@ def main():
     achieved = dec.algo_bytes / per / 1e9
     extras = {}
     if not args.no_extras and rank == 0:
+        c0 = workloads.SINGLE_GEMV
+        extras["gemv_config0"] = bench_gemv_set(qmm, torch, c0["name"], [("W", c0["N"], c0["K"])], c0["sigma"])
+        extras["gemv_large_dense_batch1"] = bench_gemv_set(
+            qmm, torch, workloads.LARGE_DENSE["name"] + ", batch 1", workloads.large_dense_matrices(),
+            workloads.LARGE_DENSE["sigma"])
         extras["gemm_batch16"] = bench_gemm_b16(qmm, torch)
         extras["gemm_batch2"] = bench_gemm_b16(qmm, torch, M=2)
         extras["moe_T16"] = bench_moe(qmm, torch, T=16)
