@@ -42,6 +42,10 @@ DevInfo g_dev[MAX_DEVICES];
 // Small-batch GEMM kernel choice (qmm_debug_gemm_kernel), process-wide.
 std::atomic<int> g_gemm_kernel{QMM_GEMM_KERNEL_AUTO};
 
+// Bounded-wait test settings of the streaming kernel (qmm_debug_stream_wait).
+std::atomic<unsigned long long> g_stream_wait_ns{WAIT_LIMIT_NS};
+std::atomic<int> g_stream_withhold{0};
+
 // Per-device facts, looked up once.  Requires an sm_103 device.
 const DevInfo* device_info() {
     int dev = -1;
@@ -234,6 +238,8 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
     a.nstages = (int)nst;
     a.xtile_bytes = (int)xtile;
     a.err = di->err;
+    a.wait_ns = g_stream_wait_ns.load();
+    a.withhold_last = g_stream_withhold.load();
     auto kern = stream_rows_kernel<MT, XM, YM, QOUT>;
     if (!smem_optin(kern, smem, di->smem_optin)) return QMM_ERR_SHAPE;
     dim3 grid((unsigned)G, (unsigned)((a.M + MT - 1) / MT));
@@ -641,6 +647,15 @@ qmm_status qmm_debug_gemm_kernel(int kernel, int* previous) {
     if (kernel < QMM_GEMM_KERNEL_AUTO || kernel > QMM_GEMM_KERNEL_STREAM) return QMM_ERR_ARG;
     const int old = g_gemm_kernel.exchange(kernel);
     if (previous) *previous = old;
+    return QMM_OK;
+}
+
+qmm_status qmm_debug_stream_wait(uint64_t limit_ns, int withhold_last_copy, uint64_t* previous_limit_ns) {
+    if (limit_ns < 1000ull || limit_ns > 10000000000ull || (withhold_last_copy != 0 && withhold_last_copy != 1))
+        return QMM_ERR_ARG;
+    const unsigned long long old = g_stream_wait_ns.exchange(limit_ns);
+    g_stream_withhold.store(withhold_last_copy);
+    if (previous_limit_ns) *previous_limit_ns = old;
     return QMM_OK;
 }
 

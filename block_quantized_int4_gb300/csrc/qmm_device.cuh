@@ -163,12 +163,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (!mbar_try_wait_sleep(bar, parity, 20000)) {
         if (*abort) return false;
-        if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

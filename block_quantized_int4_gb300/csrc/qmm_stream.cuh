@@ -76,6 +76,8 @@ struct StreamArgs {
     int stage_q;         // offset of the scales in a stage
     int xtile_bytes;     // multiple of 128
     int* err;
+    uint64_t wait_ns;    // limit of every bounded wait of the kernel (WAIT_LIMIT_NS normally)
+    int withhold_last;   // test of the bounded waits: the producer never issues its last unit
 };
 
 // 2D tile copy of weight bytes, evicted first from L2 (l2_evict_first_policy).
@@ -187,9 +189,13 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
             const uint64_t pol = l2_evict_first_policy();
             int issued = 0;
             bool ok = true;
-            for (int u = 0; u < nunits; ++u) {
+            // withhold_last: the last unit is never issued (no expect_tx, no
+            // copy), so its consumers' bounded waits run out -- the test of the
+            // timeout path; every issued copy still lands before the CTA ends
+            const int nissue = a.withhold_last ? nunits - 1 : nunits;
+            for (int u = 0; u < nissue; ++u) {
                 const int s = u % S;
-                if (u >= S && !mbar_wait(&empty[s], ((u / S) - 1) & 1, abort_flag)) {
+                if (u >= S && !mbar_wait(&empty[s], ((u / S) - 1) & 1, abort_flag, a.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -204,9 +210,11 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
             if (!ok) {
                 atomicOr(a.err, ERR_TIMEOUT);
                 *abort_flag = 1;
+            }
+            if (!ok || a.withhold_last) {
                 for (int u = max(0, issued - S); u < issued; ++u) {  // let issued copies land
                     const uint64_t t0 = global_ns();
-                    while (!mbar_try_wait(&full[u % S], (u / S) & 1) && global_ns() - t0 < WAIT_LIMIT_NS) {
+                    while (!mbar_try_wait(&full[u % S], (u / S) & 1) && global_ns() - t0 < a.wait_ns) {
                     }
                 }
             }
@@ -250,7 +258,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
             const int u = g * nkc + kc, s = u % S;
             // On a timeout keep going without computing: every later wait returns
             // at once (abort flag), and the kernel ends with the error word set.
-            const bool ok = !failed && mbar_wait(&full[s], (u / S) & 1, abort_flag);
+            const bool ok = !failed && mbar_wait(&full[s], (u / S) & 1, abort_flag, a.wait_ns);
             if (!ok && !failed) {
                 if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
                 *abort_flag = 1;

@@ -67,6 +67,7 @@ SIGNATURES = {
     "qmm_gemm_q4_0_q8_0": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P],
     "qmm_debug_block_dots": [_P, _I64, _I64, _I64, _P, _P, _P],
     "qmm_debug_gemm_kernel": [_INT, ctypes.POINTER(_INT)],
+    "qmm_debug_stream_wait": [ctypes.c_uint64, _INT, ctypes.POINTER(ctypes.c_uint64)],
     "qmm_gemv_chain_workspace_size": [_I32, ctypes.POINTER(_SZ)],
     "qmm_gemv_chain": [ctypes.POINTER(GemvOp), _I32, _P, _SZ, _P],
     "qmm_gemv_fused_op": [ctypes.POINTER(GemvOp), _INT, _P],
@@ -188,6 +189,15 @@ def qmm_debug_gemm_kernel(kernel):
     """Select the small-batch GEMM kernel; returns the previous setting."""
     prev = ctypes.c_int(0)
     _check(_lib.qmm_debug_gemm_kernel(kernel, ctypes.byref(prev)), "qmm_debug_gemm_kernel")
+    return prev.value
+
+
+def qmm_debug_stream_wait(limit_ns, withhold_last_copy=False):
+    """Bound of the streaming kernel's device waits (ns) and the withheld-copy
+    test mode; returns the previous bound."""
+    prev = ctypes.c_uint64(0)
+    _check(_lib.qmm_debug_stream_wait(int(limit_ns), int(bool(withhold_last_copy)), ctypes.byref(prev)),
+           "qmm_debug_stream_wait")
     return prev.value
 
 

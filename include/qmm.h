@@ -196,6 +196,22 @@ QMM_API qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, 
 #define QMM_GEMM_KERNEL_STREAM 3
 QMM_API qmm_status qmm_debug_gemm_kernel(int kernel, int* previous);
 
+/* Test hook of the failure handling of the streaming GEMV kernel (the
+ * kernel of qmm_gemv_fused, qmm_gemv_fused_op, qmm_gemv_q4_0_f32 and the
+ * 1-8 token qmm_gemm_q4_0_q8_0): every wait on the device is bounded, and
+ * this sets the bound of the launches that follow, process-wide:
+ * limit_ns in [1e3, 1e10] (the default is 2e9, two seconds).  With
+ * withhold_last_copy = 1 the producer of every CTA never issues its last
+ * weight copy, so the consumers' wait for it runs out: the launch ends
+ * without writing the outputs that depend on it, the device error word
+ * gets QMM_ERR_TIMEOUT (read with qmm_last_device_error), and the context
+ * stays usable; every copy that was issued lands before the CTA ends.
+ * withhold_last_copy = 0 restores normal operation.  `previous_limit_ns`
+ * (may be NULL) receives the old bound.  QMM_ERR_ARG outside those ranges.
+ * Not synchronised with launches on other host threads.  No counterpart on
+ * the pages. */
+QMM_API qmm_status qmm_debug_stream_wait(uint64_t limit_ns, int withhold_last_copy, uint64_t* previous_limit_ns);
+
 /* Per-block integer dots, for bit-exact checking: dots[(m*N + n)*B + b] =
  * sum_{i<32} q_w * q_x, int32, computed with the product kernels' own
  * unpack and dot code.  M, N >= 1. */

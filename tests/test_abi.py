@@ -222,3 +222,15 @@ def test_gemm_kernel_selector_and_moe_fp32_validation(qmm):
     assert gi(A16, 16, 8, 256, A16, n - 16, None) == 8       # workspace too small
     assert gi(A16 + 2, 16, 8, 256, A16, n, None) == 3        # ids misaligned
     assert gi(A16, 0, 8, 256, A16, n, None) == 0             # T = 0: no-op
+
+
+def test_stream_wait_hook_arguments(qmm):
+    """qmm_debug_stream_wait: bound in [1e3, 1e10] ns, withhold flag 0 or 1;
+    returns the previous bound (two seconds by default)."""
+    lib = qmm._lib
+    prev = ctypes.c_uint64(0)
+    assert lib.qmm_debug_stream_wait(999, 0, None) == 1
+    assert lib.qmm_debug_stream_wait(10_000_000_001, 0, None) == 1
+    assert lib.qmm_debug_stream_wait(1_000_000, 2, None) == 1
+    assert lib.qmm_debug_stream_wait(1_000_000, 0, ctypes.byref(prev)) == 0 and prev.value == 2_000_000_000
+    assert lib.qmm_debug_stream_wait(2_000_000_000, 0, ctypes.byref(prev)) == 0 and prev.value == 1_000_000

@@ -8,7 +8,7 @@ import torch
 
 from oracle import oracle as O
 import workloads
-from parity import lib, u16, assert_close
+from parity import lib, u16, assert_close, check_rmsnorm_q8_0
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -107,10 +107,10 @@ def _planes_to_oracle(qs, d, N, K):
 
 
 def test_chain_first_op_and_end_to_end_against_oracle():
-    """Op 0: the GPU's Q8_0 of RMSNorm(x) against the oracle's (codes within
-    one step, scales equal on nearly every block: fp32 sums in another order
-    may move a rounding boundary); its output against the oracle's product of
-    the GPU's own codes.  Then the oracle runs the whole chain on its own
+    """Op 0: the GPU's Q8_0 of RMSNorm(x): codes bit-exact against the
+    oracle's Q8_0 of fl(x * gamma), scales within one fp16 step of
+    fp16(d32_z / rms); its output against the oracle's product of the GPU's
+    own codes.  Then the oracle runs the whole chain on its own
     (RMSNorm, Q8_0 of each intermediate) and the logits agree to a relative
     L2 of 1e-3."""
     qmm = lib()
@@ -126,8 +126,7 @@ def test_chain_first_op_and_end_to_end_against_oracle():
     a_ref = O.rmsnorm(x, ga.cpu().numpy(), eps=1e-5)
     qa, da = O.quantize_q8_0(a_ref)
     gqa, gda = dec.a0[0].cpu().numpy()[None], u16(dec.a0[1])[None]
-    assert (np.abs(gqa.astype(int) - qa.astype(int)) <= 1).all()
-    assert (gqa == qa).mean() > 0.99 and (gda == da).mean() > 0.95
+    check_rmsnorm_q8_0(x[0], ga.cpu().numpy(), 1e-5, gqa[0], gda[0], "op 0 staging")
     # QKV of the GPU's own codes: the Q8_0 output within one step of the oracle's
     yq_ref, S = O.matmul_int(*_planes_to_oracle(*qkv, Q, H), gqa, gda)
     qy, dy = O.quantize_q8_0(yq_ref.astype(np.float32))

@@ -1,7 +1,9 @@
 """Expert hot-store on the device: over a sequence of routed decode steps
-with evictions, a separate copy stream and prefetch of the next step's
-experts, the expert GEMV on the slot arena (ids remapped by the store) is
-bit-identical to the same GEMV on all experts resident; the store's hit and
+with evictions (and experts loaded again after one), a separate copy stream
+and prefetch of the next step's experts, the expert GEMV on the slot arena
+(ids remapped by the store) matches the oracle's product with each slot's
+routed expert within |y - y_ref| <= 1e-5 * S + 1e-6, and is bit-identical to
+the same GEMV on all experts resident; the store's hit and
 miss counts follow the host policy; an expert that is not resident maps to
 -1 and is reported."""
 import numpy as np
@@ -10,7 +12,7 @@ import torch
 
 from oracle import oracle as O
 import workloads
-from parity import lib
+from parity import lib, u16, assert_close, planes_to_oracle
 from test_store_lru import RefLru
 
 pytestmark = pytest.mark.gpu
@@ -48,10 +50,13 @@ def test_store_gemv_equals_all_resident(separate_copy_stream, prefetch):
     x = workloads.activations(T, K, seed=3)
     xq, xd = qmm.quantize_q8_0(x.to(DEV))
     outs, refs = [], []
+    seen, reloaded = set(), set()  # experts loaded before; experts loaded again after an eviction
     for i, ids in enumerate(steps):
         flat = ids.reshape(-1).tolist()
+        reloaded |= {e for e in flat if e in seen and e not in ref.res}
         store.request(flat, compute, copy)
         ref.request(flat, use=True)
+        seen |= set(flat)
         ids_d = torch.from_numpy(ids).to(DEV)
         slot_ids = torch.empty_like(ids_d)
         store.map_ids(ids_d, slot_ids)
@@ -60,6 +65,7 @@ def test_store_gemv_equals_all_resident(separate_copy_stream, prefetch):
         store.release(compute)
         if prefetch and i + 1 < len(steps):
             nxt = steps[i + 1].reshape(-1).tolist()
+            reloaded |= {e for e in nxt if e in seen and e not in ref.res}
             store.prefetch(nxt, copy)
             ref.request(nxt, use=False)
         y_ref = torch.empty(T * k, N, device=DEV)
@@ -69,6 +75,18 @@ def test_store_gemv_equals_all_resident(separate_copy_stream, prefetch):
     assert qmm.qmm_last_device_error() == 0
     for i, (a, b) in enumerate(zip(outs, refs)):
         assert torch.equal(a, b), f"step {i}"
+    # every slot of every step against the oracle's product with the routed
+    # expert (read from the all-resident planes), including experts that
+    # were evicted and loaded again
+    assert reloaded, "the routing never brought an evicted expert back"
+    qx, dx = xq.cpu().numpy(), u16(xd)
+    Wo = {}
+    for i, ids in enumerate(steps):
+        for s_, e in enumerate(ids.reshape(-1).tolist()):
+            if e not in Wo:
+                Wo[e] = planes_to_oracle(qs[e], d[e], N, K)
+            y_ref, S = O.matmul_int(*Wo[e], qx[s_ // k], dx[s_ // k])
+            assert_close(outs[i][s_][None], y_ref, S, f"step {i} slot {s_} (expert {e})")
     st = store.stats()
     assert {k_: st[k_] for k_ in ("hits", "misses", "evictions", "prefetched")} == ref.stats
     assert st["misses"] > 0 and st["evictions"] > 0 and st["hits"] > 0
