@@ -220,6 +220,9 @@ class TinyLlamaDecode:
         self.op_array = (qmm.GemvOp * self.n_ops)(*self.op_list)
         self.ws_bytes = qmm.qmm_gemv_chain_workspace_size(self.n_ops)
         self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # counters: zero, left zero
+        self.dchain = (qmm.ChainOp * self.n_ops)(*self.decode_ops())
+        self.dws_bytes = qmm.qmm_decode_chain_workspace_size(self.dchain)
+        self.dws = torch.zeros(self.dws_bytes, dtype=torch.uint8, device=dev)  # zero before its first use
 
     def _ops(self):
         """The decode step as qmm_gemv_op descriptors, in order.  Per layer
@@ -242,6 +245,34 @@ class TinyLlamaDecode:
             h_in = h_out
         ops.append(op(*self.lm_head, self.V, H, x=h_in, norm_w=self.norm_final, norm_eps=eps, y=self.logits))
         return ops
+
+    def decode_ops(self, intermediates=False):
+        """The same step as qmm_chain_op descriptors for qmm_decode_chain: each
+        op names the op whose output it reads (src) and adds (residual); the
+        hand-over lives in the workspace.  Only the logits are written out,
+        unless `intermediates` (then also h1 -> hmid and each layer's output
+        -> h, as in step())."""
+        q, H, F, eps = self.qmm, self.H, self.F, self.eps
+        ops = []
+        for li, Lw in enumerate(self.layers):
+            g_attn, g_ffn = self.norms[li]
+            base, prev_down = 4 * li, 4 * li - 1
+            first = li == 0
+            ops.append(q.chain_op(*Lw["qkv"], self.Q, H, src=-1 if first else prev_down,
+                                  x=self.x_in if first else None, norm_w=g_attn, norm_eps=eps))
+            ops.append(q.chain_op(*Lw["o"], H, H, src=base, residual=-2 if first else prev_down,
+                                  x=self.x_in if first else None, y=self.hmid if intermediates else None))
+            ops.append(q.chain_op(*Lw["gu"], 2 * F, H, src=base + 1, norm_w=g_ffn, norm_eps=eps,
+                                  flags=q.Y_SWIGLU_PAIRS))
+            ops.append(q.chain_op(*Lw["down"], H, F, src=base + 2, residual=base + 1,
+                                  y=self.h[li % 2] if intermediates else None))
+        ops.append(q.chain_op(*self.lm_head, self.V, H, src=4 * self.L - 1, norm_w=self.norm_final, norm_eps=eps,
+                              y=self.logits))
+        return ops
+
+    def decode_step(self, stream=None):
+        """The step as one launch with flagged hand-over between its ops."""
+        self.qmm.qmm_decode_chain(self.dchain, self.dws, self.dws_bytes, stream=stream)
 
     def step(self, stream=None):
         """The step as 89 GEMV launches chained with programmatic dependent launch."""

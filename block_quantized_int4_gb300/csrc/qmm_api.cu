@@ -12,6 +12,7 @@
 
 #include "qmm.h"
 #include "qmm_chain.cuh"
+#include "qmm_decode.cuh"
 #include "qmm_internal.h"
 #include "qmm_kernels.cuh"
 #include "qmm_stream.cuh"

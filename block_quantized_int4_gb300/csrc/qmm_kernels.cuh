@@ -368,27 +368,18 @@ __device__ __forceinline__ RmsGamma rms_gamma_load(const float* gamma, int64_t K
     return r;
 }
 
-__device__ __forceinline__ void stage_f32_rmsnorm(const XTile& xt, const float* x, const float* gamma,
-                                                  const RmsGamma& gr, int64_t K, float eps, int8_t* xq_out,
-                                                  uint16_t* xd_out, float* red, int tid, int nthr, int bar) {
+// The one-pass staging once this thread's values are in registers: v[2i],
+// v[2i+1] hold values 8p..8p+7 (p = tid & 3) of block i * nthr/4 + tid/4
+// (zero past the row).  Shared by every source of x (plain loads here; the
+// decode chain's flagged buffers).
+__device__ __forceinline__ void stage_rmsnorm_regs(const XTile& xt, const float4 (&v)[2 * RMS_STEPS],
+                                                   const RmsGamma& gr, int64_t K, float eps, int8_t* xq_out,
+                                                   uint16_t* xd_out, float* red, int tid, int nthr, int bar) {
     const int B = (int)(K / QK);
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
-    if (!rms_one_pass(K, nthr)) {
-        const float inv = rms_inv(x, K, eps, red, tid, nthr, bar);
-        stage_f32<false>(xt, x, K, xq_out, xd_out, tid, nthr, gamma, inv);
-        return;
-    }
     const int p = tid & 3;
     const bool writer = blockIdx.x == 0 && blockIdx.y == 0;
-    float4 v[2 * RMS_STEPS];
     float ss = 0.f;
-#pragma unroll
-    for (int i = 0; i < RMS_STEPS; ++i) {
-        const int b = i * (nthr >> 2) + (tid >> 2);
-        const float* xb = x + (int64_t)b * QK + p * 8;
-        v[2 * i] = b < B ? __ldcg(reinterpret_cast<const float4*>(xb)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[2 * i + 1] = b < B ? __ldcg(reinterpret_cast<const float4*>(xb + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
 #pragma unroll
     for (int i = 0; i < 2 * RMS_STEPS; ++i) {
         ss = __fmaf_rn(v[i].x, v[i].x, ss);
@@ -457,23 +448,78 @@ __device__ __forceinline__ void stage_f32_rmsnorm(const XTile& xt, const float* 
     }
 }
 
+__device__ __forceinline__ void stage_f32_rmsnorm(const XTile& xt, const float* x, const float* gamma,
+                                                  const RmsGamma& gr, int64_t K, float eps, int8_t* xq_out,
+                                                  uint16_t* xd_out, float* red, int tid, int nthr, int bar) {
+    const int B = (int)(K / QK);
+    if (!rms_one_pass(K, nthr)) {
+        const float inv = rms_inv(x, K, eps, red, tid, nthr, bar);
+        stage_f32<false>(xt, x, K, xq_out, xd_out, tid, nthr, gamma, inv);
+        return;
+    }
+    const int p = tid & 3;
+    float4 v[2 * RMS_STEPS];
+#pragma unroll
+    for (int i = 0; i < RMS_STEPS; ++i) {
+        const int b = i * (nthr >> 2) + (tid >> 2);
+        const float* xb = x + (int64_t)b * QK + p * 8;
+        v[2 * i] = b < B ? __ldcg(reinterpret_cast<const float4*>(xb)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[2 * i + 1] = b < B ? __ldcg(reinterpret_cast<const float4*>(xb + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    stage_rmsnorm_regs(xt, v, gr, K, eps, xq_out, xd_out, red, tid, nthr, bar);
+}
+
+// Each warp of stage_f32 takes 4 blocks per step (8 lanes per block, one
+// float4 per lane); STAGE_STEPS steps are loaded before any is quantized, so
+// the activation costs one memory round trip per STAGE_STEPS * nwarps * 4
+// blocks.  This quantizes one round: v[i] holds values part*4..part*4+3
+// (part = lane & 7) of block (g0 + i * nwarps) * 4 + lane / 8.  Shared by
+// every source of x (plain loads here; the decode chain's flagged buffers).
+constexpr int STAGE_STEPS = 8;
+
+__device__ __forceinline__ void stage_f32_quantize(const XTile& xt, const float4 (&v)[STAGE_STEPS], int g0, int B,
+                                                   int8_t* __restrict__ xq_out, uint16_t* __restrict__ xd_out,
+                                                   int lane, int nwarps) {
+    const int part = lane & 7;  // which 4 values of the block
+    const bool writer = blockIdx.x == 0 && blockIdx.y == 0;
+#pragma unroll
+    for (int i = 0; i < STAGE_STEPS; ++i) {
+        const int g = g0 + i * nwarps;
+        if (g * 4 >= B) break;  // warp-uniform
+        const int b = g * 4 + (lane >> 3);
+        const bool valid = b < B;
+        Quad r = quad_codes(v[i], 127.0f, -127.0f);
+        const int packed =
+            (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) | ((r.c[3] & 0xff) << 24);
+        int s = r.c[0] + r.c[1] + r.c[2] + r.c[3];
+        s += __shfl_xor_sync(FULL, s, 1);
+        s += __shfl_xor_sync(FULL, s, 2);
+        s += __shfl_xor_sync(FULL, s, 4);
+        if (valid) {
+            int* plane = reinterpret_cast<int*>(part < 4 ? &xt.lo[b] : &xt.hi[b]);
+            plane[part & 3] = packed;
+            if (part == 0) {
+                const unsigned short h = f32_to_f16_bits(r.d32);
+                xt.sc[b] = make_int2(__float_as_int(f16_bits_to_f32(h)), s);
+                if (writer && xd_out) xd_out[b] = h;
+            }
+            if (writer && xq_out) *reinterpret_cast<int*>(xq_out + (int64_t)b * QK + part * 4) = packed;
+        }
+    }
+}
+
 template <bool GATE_UP>
 __device__ __forceinline__ void stage_f32(const XTile& xt, const float* __restrict__ x, int64_t K,
                                           int8_t* __restrict__ xq_out, uint16_t* __restrict__ xd_out, int tid,
                                           int nthr, const float* gamma, float inv) {
-    // Each warp takes 4 blocks per step (8 lanes per block, one float4 per
-    // lane).  Up to STEPS steps are loaded before any is quantized, so the
-    // activation costs one memory round trip per STEPS * nwarps * 4 blocks.
-    constexpr int STEPS = 8;
     const int B = (int)(K / QK);
     const int lane = tid & 31;
     const int warp = tid >> 5, nwarps = nthr >> 5;
     const int part = lane & 7;  // which 4 values of the block
-    const bool writer = blockIdx.x == 0 && blockIdx.y == 0;
-    for (int g0 = warp; g0 * 4 < B; g0 += nwarps * STEPS) {
-        float4 v[STEPS];
+    for (int g0 = warp; g0 * 4 < B; g0 += nwarps * STAGE_STEPS) {
+        float4 v[STAGE_STEPS];
 #pragma unroll
-        for (int i = 0; i < STEPS; ++i) {
+        for (int i = 0; i < STAGE_STEPS; ++i) {
             const int b = (g0 + i * nwarps) * 4 + (lane >> 3);
             v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (b < B) {
@@ -490,30 +536,7 @@ __device__ __forceinline__ void stage_f32(const XTile& xt, const float* __restri
                 }
             }
         }
-#pragma unroll
-        for (int i = 0; i < STEPS; ++i) {
-            const int g = g0 + i * nwarps;
-            if (g * 4 >= B) break;  // warp-uniform
-            const int b = g * 4 + (lane >> 3);
-            const bool valid = b < B;
-            Quad r = quad_codes(v[i], 127.0f, -127.0f);
-            const int packed =
-                (r.c[0] & 0xff) | ((r.c[1] & 0xff) << 8) | ((r.c[2] & 0xff) << 16) | ((r.c[3] & 0xff) << 24);
-            int s = r.c[0] + r.c[1] + r.c[2] + r.c[3];
-            s += __shfl_xor_sync(FULL, s, 1);
-            s += __shfl_xor_sync(FULL, s, 2);
-            s += __shfl_xor_sync(FULL, s, 4);
-            if (valid) {
-                int* plane = reinterpret_cast<int*>(part < 4 ? &xt.lo[b] : &xt.hi[b]);
-                plane[part & 3] = packed;
-                if (part == 0) {
-                    const unsigned short h = f32_to_f16_bits(r.d32);
-                    xt.sc[b] = make_int2(__float_as_int(f16_bits_to_f32(h)), s);
-                    if (writer && xd_out) xd_out[b] = h;
-                }
-                if (writer && xq_out) *reinterpret_cast<int*>(xq_out + (int64_t)b * QK + part * 4) = packed;
-            }
-        }
+        stage_f32_quantize(xt, v, g0, B, xq_out, xd_out, lane, nwarps);
     }
 }
 

@@ -234,3 +234,42 @@ def test_stream_wait_hook_arguments(qmm):
     assert lib.qmm_debug_stream_wait(1_000_000, 2, None) == 1
     assert lib.qmm_debug_stream_wait(1_000_000, 0, ctypes.byref(prev)) == 0 and prev.value == 2_000_000_000
     assert lib.qmm_debug_stream_wait(2_000_000_000, 0, ctypes.byref(prev)) == 0 and prev.value == 1_000_000
+
+
+def test_decode_chain_validation_and_workspace(qmm):
+    """qmm_decode_chain_workspace_size validates the chain on the host: op
+    links point backwards, shapes, the one-pass RMSNorm limit, alignment;
+    the workspace is 256 bytes plus 8 bytes per output value a later op reads."""
+    A16 = 0x10000
+    op = qmm.chain_op
+    ok = [op(A16, A16, 2560, 2048, src=-1, x=A16, norm_w=A16),
+          op(A16, A16, 2048, 2048, src=0, residual=-2, x=A16),
+          op(A16, A16, 11264, 2048, src=1, norm_w=A16, flags=qmm.Y_SWIGLU_PAIRS),
+          op(A16, A16, 2048, 5632, src=2, residual=1),
+          op(A16, A16, 32000, 2048, src=3, norm_w=A16, y=A16)]
+    assert qmm.qmm_decode_chain_workspace_size(ok) == 256 + 8 * (2560 + 2048 + 5632 + 2048)
+
+    def status(ops):
+        arr = (qmm.ChainOp * len(ops))(*ops)
+        n = ctypes.c_size_t(0)
+        return qmm._lib.qmm_decode_chain_workspace_size(arr, len(ops), ctypes.byref(n))
+
+    assert status(ok) == 0
+    assert status([op(A16, A16, 64, 256, src=0, x=A16)]) == 1                       # src not an earlier op
+    assert status([op(A16, A16, 64, 256)]) == 1                                     # src -1 without x
+    assert status([op(A16, A16, 63, 256, x=A16)]) == 2                              # N odd
+    assert status([op(A16, A16, 64, 288, x=A16)]) == 2                              # K % 256
+    assert status([op(A16, A16, 64, 8192, x=A16, norm_w=A16)]) == 2                 # RMSNorm beyond one pass
+    assert status([op(A16, A16, 64, 256, x=A16, residual=-2, flags=qmm.Y_SWIGLU_PAIRS)]) == 1  # residual + pairs
+    assert status([op(A16, A16, 64, 256, x=A16), op(A16, A16, 64, 512, src=0)]) == 2  # input longer than src
+    assert status([op(A16 + 8, A16, 64, 256, x=A16)]) == 3                          # weights misaligned
+    assert status([op(A16, A16, 64, 256, x=A16, xq=A16)]) == 1                      # xq without xd
+    lib = qmm._lib
+    arr = (qmm.ChainOp * len(ok))(*ok)
+    need = qmm.qmm_decode_chain_workspace_size(ok)
+    assert lib.qmm_decode_chain(arr, len(ok), ctypes.c_void_p(A16), need - 16, None) == 8  # workspace too small
+    assert lib.qmm_decode_chain(arr, len(ok), ctypes.c_void_p(A16 + 8), need, None) == 3   # misaligned workspace
+    prev = ctypes.c_uint64(0)
+    assert lib.qmm_debug_decode_wait(999, None) == 1
+    assert lib.qmm_debug_decode_wait(1_000_000, ctypes.byref(prev)) == 0 and prev.value == 2_000_000_000
+    assert lib.qmm_debug_decode_wait(2_000_000_000, ctypes.byref(prev)) == 0 and prev.value == 1_000_000
