@@ -120,6 +120,29 @@ bool smem_optin(K kernel, int bytes, int optin) {
     return true;
 }
 
+// Prefer the largest shared-memory carve-out for a kernel, once per (kernel,
+// device): launches of one kernel with small and large shared-memory needs
+// then share an SM configuration, so a chained launch's CTAs can become
+// resident beside those of the launch before it instead of waiting for the
+// SM to drain and be reconfigured.
+std::set<std::pair<const void*, int>> g_carve_done;
+
+template <typename K>
+bool max_carveout(K kernel) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(reinterpret_cast<const void*>(kernel), dev);
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if (g_carve_done.count(key)) return true;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    g_carve_done.insert(key);
+    return true;
+}
+
 int grid_for(int64_t work_items, int per_sm, int sms) {
     int64_t g = std::min<int64_t>(work_items, (int64_t)sms * per_sm);
     return (int)std::max<int64_t>(g, 1);
@@ -212,6 +235,8 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
     const int ckb = (int)std::min<int64_t>(CHUNK_KB, B);
     const int64_t xtile = round_up((int64_t)MT * B * xtile_bytes_per_block(), 128);
     const int64_t ybuf = qout ? round_up(rpc / opr * 4, 128) : 0;
+    const bool rpre = a.residual != nullptr && a.M == 1 && opr == 1;
+    const int64_t rbuf = rpre ? round_up(rpc * 4, 128) : 0;
     const int64_t nunits = ((rpc + rb - 1) / rb) * ((B + ckb - 1) / ckb);
     // a ring stage holds one TMA box pair (rb rows x ckb blocks): sized to it,
     // so short row groups leave room for more stages
@@ -221,7 +246,7 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
     // kernel's CTA is resident beside this one and prefetches its weights
     // (two such CTAs and their 1 KB reservations fill the SM's 228 KB).
     const int64_t cap = chain_sized ? 112 * 1024 : QMM_STREAM_BIG_SMEM_KB * 1024;
-    const int64_t room = (cap - STREAM_HDR - xtile - ybuf) / stage_bytes;
+    const int64_t room = (cap - STREAM_HDR - xtile - ybuf - rbuf) / stage_bytes;
     const int64_t nst = std::min<int64_t>({nunits, room, (int64_t)STREAM_MAX_STAGES});
     if (nst < 1) return QMM_ERR_SHAPE;
     CUtensorMap mq, md;
@@ -230,8 +255,10 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
         !make_tensor_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT16, d, (uint64_t)B, (uint64_t)a.N, (uint64_t)B * 2,
                             (uint32_t)ckb, (uint32_t)rb, CU_TENSOR_MAP_SWIZZLE_NONE))
         return QMM_ERR_CUDA;
-    const int smem = (int)(STREAM_HDR + xtile + nst * stage_bytes + ybuf);
+    const int smem = (int)(STREAM_HDR + xtile + nst * stage_bytes + ybuf + rbuf);
     a.rows_per_cta = (int)rpc;
+    a.ybuf_bytes = (int)ybuf;
+    a.rbuf = rpre ? 1 : 0;
     a.stage_bytes = (int)stage_bytes;
     a.stage_q = (int)stage_q;
     a.rb = rb;
@@ -242,7 +269,7 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
     a.wait_ns = g_stream_wait_ns.load();
     a.withhold_last = g_stream_withhold.load();
     auto kern = stream_rows_kernel<MT, XM, YM, QOUT>;
-    if (!smem_optin(kern, smem, di->smem_optin)) return QMM_ERR_SHAPE;
+    if (!smem_optin(kern, smem, di->smem_optin) || !max_carveout(kern)) return QMM_ERR_SHAPE;
     dim3 grid((unsigned)G, (unsigned)((a.M + MT - 1) / MT));
     cudaError_t e = launch(kern, grid, dim3(STREAM_THREADS), smem, st, pdl, mq, md, a);
     return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);

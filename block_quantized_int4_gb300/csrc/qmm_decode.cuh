@@ -88,17 +88,17 @@ __device__ __forceinline__ uint64_t fword(float v, uint32_t flag) {
 }
 
 __device__ __forceinline__ void fstore1(uint64_t* p, float v, uint32_t flag) {
-    asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(fword(v, flag)) : "memory");
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(fword(v, flag)) : "memory");
 }
 
 __device__ __forceinline__ void fstore2(uint64_t* p, float v0, float v1, uint32_t flag) {  // p 16-byte aligned
-    asm volatile("st.volatile.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(fword(v0, flag)), "l"(fword(v1, flag))
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(fword(v0, flag)), "l"(fword(v1, flag))
                  : "memory");
 }
 
 __device__ __forceinline__ ulonglong2 fload2(const uint64_t* p) {  // p 16-byte aligned
     ulonglong2 r;
-    asm volatile("ld.volatile.global.v2.u64 {%0, %1}, [%2];" : "=l"(r.x), "=l"(r.y) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(r.x), "=l"(r.y) : "l"(p) : "memory");
     return r;
 }
 
@@ -146,21 +146,22 @@ __device__ __forceinline__ void stage_flagged_rmsnorm(const XTile& xt, const uin
     const int p = tid & 3;
     ulonglong2 r[RMS_STEPS][4];
     Spin sp = {0, 0};
+    unsigned pending = 0;  // words still to read: bit 4i + j (only those are read again)
+#pragma unroll
+    for (int i = 0; i < RMS_STEPS; ++i)
+        if (i * (NTHR >> 2) + (tid >> 2) < B) pending |= 0xfu << (4 * i);
     for (;;) {
-        bool ok = true;
 #pragma unroll
         for (int i = 0; i < RMS_STEPS; ++i) {
-            const int b = i * (NTHR >> 2) + (tid >> 2);
-            if (b < B) {
-                const uint64_t* w = src + (int64_t)b * QK + p * 8;
+            const uint64_t* w = src + (int64_t)(i * (NTHR >> 2) + (tid >> 2)) * QK + p * 8;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 4; ++j)
+                if (pending & (1u << (4 * i + j))) {
                     r[i][j] = fload2(w + 2 * j);
-                    ok = ok && fok(r[i][j], flag);
+                    if (fok(r[i][j], flag)) pending &= ~(1u << (4 * i + j));
                 }
-            }
         }
-        if (ok) break;
+        if (!pending) break;
         if (!sp.again(a, abort_flag)) {
             give_up(a, abort_flag);
             break;
@@ -193,19 +194,22 @@ __device__ __forceinline__ void stage_flagged_f32(const XTile& xt, const uint64_
     for (int g0 = warp; g0 * 4 < B; g0 += nwarps * STAGE_STEPS) {
         ulonglong2 r[STAGE_STEPS][2];
         Spin sp = {0, 0};
+        unsigned pending = 0;  // words still to read: bit 2i + j (only those are read again)
+#pragma unroll
+        for (int i = 0; i < STAGE_STEPS; ++i)
+            if ((g0 + i * nwarps) * 4 + (lane >> 3) < B) pending |= 3u << (2 * i);
         for (;;) {
-            bool ok = true;
 #pragma unroll
             for (int i = 0; i < STAGE_STEPS; ++i) {
-                const int b = (g0 + i * nwarps) * 4 + (lane >> 3);
-                if (b < B) {
-                    const uint64_t* w = src + (int64_t)b * QK + part * 4;
-                    r[i][0] = fload2(w);
-                    r[i][1] = fload2(w + 2);
-                    ok = ok && fok(r[i][0], flag) && fok(r[i][1], flag);
-                }
+                const uint64_t* w = src + (int64_t)((g0 + i * nwarps) * 4 + (lane >> 3)) * QK + part * 4;
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (pending & (1u << (2 * i + j))) {
+                        r[i][j] = fload2(w + 2 * j);
+                        if (fok(r[i][j], flag)) pending &= ~(1u << (2 * i + j));
+                    }
             }
-            if (ok) break;
+            if (!pending) break;
             if (!sp.again(a, abort_flag)) {
                 give_up(a, abort_flag);
                 break;

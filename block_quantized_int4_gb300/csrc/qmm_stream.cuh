@@ -76,6 +76,8 @@ struct StreamArgs {
     int stage_q;         // offset of the scales in a stage
     int xtile_bytes;     // multiple of 128
     int* err;
+    int ybuf_bytes;      // QOUT: shared-memory bytes of the CTA's outputs (after the ring)
+    int rbuf;            // the CTA's residual values are read into shared memory (after ybuf) up front
     uint64_t wait_ns;    // limit of every bounded wait of the kernel (WAIT_LIMIT_NS normally)
     int withhold_last;   // test of the bounded waits: the producer never issues its last unit
 };
@@ -160,6 +162,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
     const XTile xt = xtile_at(smem + STREAM_HDR, MT, B);
     uint8_t* ring = smem + STREAM_HDR + a.xtile_bytes;
     float* ybuf = reinterpret_cast<float*>(ring + (size_t)a.nstages * a.stage_bytes);  // QOUT: this CTA's outputs
+    float* rbuf = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ybuf) + a.ybuf_bytes);  // residual slice
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     const int RB = a.rb, CKB = a.ckb;
@@ -228,6 +231,10 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
     RmsGamma gr;
     if (xmode == X_F32 && a.gamma) gr = rms_gamma_load(a.gamma, a.K, tid, NTHR);
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the residual values of this CTA's rows are read now, their latency
+    // overlapping the staging's, and kept in shared memory for the epilogue
+    // (read there, they would add a memory round trip at the very end)
+    const float rv = a.rbuf && tid < nrows ? __ldcg(a.residual + row_begin + tid) : 0.f;
     const int64_t m0 = (int64_t)blockIdx.y * MT;
     int64_t xrow[MT];
 #pragma unroll
@@ -240,6 +247,10 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
         stage_f32<true>(xt, a.xf, a.K, a.xq_out, a.xd_out, tid, NTHR);
     else
         stage_f32<false>(xt, a.xf, a.K, a.xq_out, a.xd_out, tid, NTHR);
+    if (a.rbuf) {
+        if (tid < nrows) rbuf[tid] = rv;
+        for (int i = tid + NTHR; i < nrows; i += NTHR) rbuf[i] = __ldcg(a.residual + row_begin + i);
+    }
     asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");
 
     // this warp's rows inside a group: pairs (2w, 2w+1) and (2w+16, 2w+17),
@@ -310,8 +321,11 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
                         if (qout) ybuf[o - row_begin / 2] = h;
                     } else {
                         const bool has1 = lr + 1 < nr;
-                        const float o0 = v[t][2 * p] + (a.residual ? a.residual[row] : 0.f);
-                        const float o1 = has1 ? v[t][2 * p + 1] + (a.residual ? a.residual[row + 1] : 0.f) : 0.f;
+                        const float r0v = a.rbuf ? rbuf[row - row_begin] : a.residual ? a.residual[row] : 0.f;
+                        const float r1v =
+                            !has1 ? 0.f : a.rbuf ? rbuf[row + 1 - row_begin] : a.residual ? a.residual[row + 1] : 0.f;
+                        const float o0 = v[t][2 * p] + r0v;
+                        const float o1 = has1 ? v[t][2 * p + 1] + r1v : 0.f;
                         if (a.y) {
                             a.y[xrow[t] * a.ldy + row] = o0;
                             if (has1) a.y[xrow[t] * a.ldy + row + 1] = o1;
