@@ -9,8 +9,8 @@ lm_head 2048->32000: 89 dependent GEMVs per step.  The residual stream stays
 fp32 and is RMSNorm-ed and quantized to Q8_0 inside the GEMV that reads it;
 QKV and gate/up hand the next GEMV a Q8_0 output; O and down add the
 residual.  The step runs as 89 launches chained with programmatic dependent
-launch (qmm_gemv_fused_op), replayed from a CUDA graph; the one-launch form
-(qmm_gemv_chain) gives identical outputs and is timed by --configs.  581,861,376 weight bytes per step (> L2, so no flush).
+launch (qmm_gemv_fused_op), replayed from a CUDA graph.  581,861,376 weight
+bytes per step (> L2, so no flush).
 
 Also reported on the same line (`also`): batch-16 GEMM TOPS on the large
 dense FFN + lm_head shapes, and the GLM-scale MoE layer.
@@ -217,12 +217,6 @@ class TinyLlamaDecode:
 
         self.op_list = self._ops()
         self.n_ops = len(self.op_list)
-        self.op_array = (qmm.GemvOp * self.n_ops)(*self.op_list)
-        self.ws_bytes = qmm.qmm_gemv_chain_workspace_size(self.n_ops)
-        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)  # counters: zero, left zero
-        self.dchain = (qmm.ChainOp * self.n_ops)(*self.decode_ops())
-        self.dws_bytes = qmm.qmm_decode_chain_workspace_size(self.dchain)
-        self.dws = torch.zeros(self.dws_bytes, dtype=torch.uint8, device=dev)  # zero before its first use
 
     def _ops(self):
         """The decode step as qmm_gemv_op descriptors, in order.  Per layer
@@ -246,43 +240,10 @@ class TinyLlamaDecode:
         ops.append(op(*self.lm_head, self.V, H, x=h_in, norm_w=self.norm_final, norm_eps=eps, y=self.logits))
         return ops
 
-    def decode_ops(self, intermediates=False):
-        """The same step as qmm_chain_op descriptors for qmm_decode_chain: each
-        op names the op whose output it reads (src) and adds (residual); the
-        hand-over lives in the workspace.  Only the logits are written out,
-        unless `intermediates` (then also h1 -> hmid and each layer's output
-        -> h, as in step())."""
-        q, H, F, eps = self.qmm, self.H, self.F, self.eps
-        ops = []
-        for li, Lw in enumerate(self.layers):
-            g_attn, g_ffn = self.norms[li]
-            base, prev_down = 4 * li, 4 * li - 1
-            first = li == 0
-            ops.append(q.chain_op(*Lw["qkv"], self.Q, H, src=-1 if first else prev_down,
-                                  x=self.x_in if first else None, norm_w=g_attn, norm_eps=eps))
-            ops.append(q.chain_op(*Lw["o"], H, H, src=base, residual=-2 if first else prev_down,
-                                  x=self.x_in if first else None, y=self.hmid if intermediates else None))
-            ops.append(q.chain_op(*Lw["gu"], 2 * F, H, src=base + 1, norm_w=g_ffn, norm_eps=eps,
-                                  flags=q.Y_SWIGLU_PAIRS))
-            ops.append(q.chain_op(*Lw["down"], H, F, src=base + 2, residual=base + 1,
-                                  y=self.h[li % 2] if intermediates else None))
-        ops.append(q.chain_op(*self.lm_head, self.V, H, src=4 * self.L - 1, norm_w=self.norm_final, norm_eps=eps,
-                              y=self.logits))
-        return ops
-
-    def decode_step(self, stream=None):
-        """The step as one launch with flagged hand-over between its ops."""
-        self.qmm.qmm_decode_chain(self.dchain, self.dws, self.dws_bytes, stream=stream)
-
     def step(self, stream=None):
         """The step as 89 GEMV launches chained with programmatic dependent launch."""
         for o in self.op_list:
             self.qmm.qmm_gemv_fused_op(o, self.qmm.CHAIN, stream=stream)
-
-    def chain_step(self, stream=None):
-        """The step as one persistent launch of the whole chain."""
-        self.qmm.qmm_gemv_chain(self.op_array, self.n_ops, self.ws, self.ws_bytes, stream=stream)
-
 
 def _graph(torch, fn):
     s = torch.cuda.Stream()
@@ -521,9 +482,9 @@ def run_case(qmm, torch, name, calls, dev="cuda"):
         return {"case": name, **bench_moe(qmm, torch, T=1 if name == "moe_layer_T1" else 16, reps=max(calls, 3))}
     elif name == "moe_store":
         return {"case": name, **bench_moe_store(qmm, torch, T=1)}
-    elif name in ("decode_chain", "decode_pdl"):  # the whole TinyLLaMA-shaped decode step
+    elif name == "decode_pdl":  # the whole TinyLLaMA-shaped decode step
         dec = TinyLlamaDecode(qmm, torch)
-        ts = _time_calls(torch, dec.chain_step if name == "decode_chain" else dec.step, calls)
+        ts = _time_calls(torch, dec.step, calls)
         return {"case": name, "us_per_call": [round(t * 1e6, 2) for t in ts],
                 "weight_GBps_best": round(dec.weight_bytes / min(ts) / 1e9, 1)}
     else:
@@ -732,8 +693,7 @@ def run_configs(qmm, torch, dev="cuda"):
     line(0, c["name"] + " (fp32 activation in, quantized in the launch)", c["N"], c["K"], 1,
          product(c["N"], c["K"], 1, c["sigma"], fused_f32=True))
     dec = TinyLlamaDecode(qmm, torch)
-    for path, fn in (("one persistent launch (qmm_gemv_chain)", dec.chain_step),
-                     ("89 launches chained with PDL (qmm_gemv_fused)", dec.step)):
+    for path, fn in (("89 launches chained with PDL (qmm_gemv_fused_op)", dec.step),):
         g = _graph(torch, fn)
         stats = _replay_stats(torch, g, 1, replays=100)
         per = stats["mean"] * 1e-6
@@ -880,7 +840,7 @@ def main():
     ap.add_argument("--configs", action="store_true",
                     help="time every workload of the five configurations instead (one JSON line each)")
     ap.add_argument("--case", default=None,
-                    help="time one kernel instead: decode_gateup, decode_qkv_norm, decode_chain, decode_pdl, lm_head_8192, "
+                    help="time one kernel instead: decode_gateup, decode_qkv_norm, decode_pdl, lm_head_8192, "
                          "gemm_b16, gemm_b16_dense, "
                          "gemm_b64, moe_T16, moe_layer_T1, moe_layer_T16, moe_store")
     ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "mma", "tmem", "stream"],
@@ -922,8 +882,6 @@ def main():
     from block_quantized_int4_gb300 import qmm
 
     dec = TinyLlamaDecode(qmm, torch)
-    # the 89 PDL-chained launches measured faster than the one-launch chain
-    # (qmm_gemv_chain) on this workload; both give identical outputs
     g = _graph(torch, dec.step)
 
     # e2e through the C ABI with host buffers: pinned x in, logits out, every step

@@ -11,8 +11,6 @@
 #include <utility>
 
 #include "qmm.h"
-#include "qmm_chain.cuh"
-#include "qmm_decode.cuh"
 #include "qmm_internal.h"
 #include "qmm_kernels.cuh"
 #include "qmm_stream.cuh"
@@ -532,7 +530,7 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
 
 namespace {
 
-// Host checks of one qmm_gemv_op (shared by the single-op and chain entries).
+// Host checks of one qmm_gemv_op.
 qmm_status validate_op(const qmm_gemv_op& o) {
     if (o.N <= 0 || (o.flags & ~QMM_Y_SWIGLU_PAIRS)) return QMM_ERR_ARG;
     if (!valid_k(o.K) || o.K % 256 != 0 || o.K > 40960 || o.N >= (int64_t(1) << 31)) return QMM_ERR_SHAPE;
@@ -588,87 +586,6 @@ qmm_status qmm_gemv_fused_op(const qmm_gemv_op* op, int flags, void* stream) {
     cudaStream_t st = S(stream);
     return o.x ? fused_dispatch<X_F32>(di, o.w_qs, o.w_d, a, pairs, qout, pdl, st)
                : fused_dispatch<X_Q8>(di, o.w_qs, o.w_d, a, pairs, qout, pdl, st);
-}
-
-qmm_status qmm_gemv_chain_workspace_size(int32_t n_ops, size_t* bytes) {
-    if (!bytes || n_ops < 1 || n_ops > QMM_CHAIN_MAX_OPS) return QMM_ERR_ARG;
-    *bytes = (size_t)(n_ops * 4 + 15) / 16 * 16;
-    return QMM_OK;
-}
-
-qmm_status qmm_gemv_chain(const qmm_gemv_op* ops, int32_t n_ops, void* workspace, size_t workspace_bytes,
-                          void* stream) {
-    static_assert(QMM_CHAIN_MAX_OPS == CHAIN_MAX_OPS, "chain size");
-    if (!ops || n_ops < 1 || n_ops > QMM_CHAIN_MAX_OPS) return QMM_ERR_ARG;
-    if (!workspace || workspace_bytes < (size_t)n_ops * 4) return QMM_ERR_WORKSPACE;
-    if (!aligned(workspace, 4)) return QMM_ERR_ALIGN;
-    // validate every op first: nothing is launched on an error
-    for (int i = 0; i < n_ops; ++i) {
-        const qmm_status v = validate_op(ops[i]);
-        if (v != QMM_OK) return v;
-    }
-    const DevInfo* di = device_info();
-    if (!di) return QMM_ERR_DEVICE;
-    const int per_sm = 1;  // one CTA per SM: the whole ring per SM for weight look-ahead
-    const int G = per_sm * di->sms;
-    ChainArgs a = {};
-    a.n_ops = n_ops;
-    int64_t xtile = 0, ybuf = 0;
-    for (int i = 0; i < n_ops; ++i) {
-        const qmm_gemv_op& o = ops[i];
-        ChainOp& c = a.ops[i];
-        const bool pairs = o.flags & QMM_Y_SWIGLU_PAIRS;
-        const bool qout = o.yq != nullptr;
-        const int64_t opr = pairs ? 2 : 1;
-        const int64_t B = o.K / QK;
-        c.qs = o.w_qs;
-        c.d = o.w_d;
-        c.xf = o.x;
-        c.gamma = o.x ? o.norm_w : nullptr;
-        c.eps = o.norm_eps;
-        c.xq = o.xq;  // with x: optional output of the staged activation
-        c.xd = o.x && !o.xq ? nullptr : o.xd;
-        c.residual = o.residual;
-        c.y = o.y;
-        c.yq = qout ? o.yq : nullptr;
-        c.yd = qout ? o.yd : nullptr;
-        c.N = (int)o.N;
-        c.K = (int)o.K;
-        c.rows_per_cta = (int)round_up((o.N + G - 1) / G, qout ? QK * opr : 2);
-        c.ckb = (int)std::min<int64_t>(CHUNK_KB, B);
-        c.pairs = pairs ? 1 : 0;
-        xtile = std::max(xtile, B * xtile_bytes_per_block());
-        if (qout) ybuf = std::max<int64_t>(ybuf, c.rows_per_cta / opr * 4);
-    }
-    a.xtile_bytes = (int)round_up(xtile, 128);
-    ybuf = round_up(std::max<int64_t>(ybuf, 4), 128);
-    const int64_t room = (di->smem_optin - STREAM_HDR - a.xtile_bytes - ybuf) / STAGE_BYTES;
-    const int64_t nst = std::min<int64_t>(room, STREAM_MAX_STAGES);
-    if (nst < 2) return QMM_ERR_SHAPE;
-    a.nstages = (int)nst;
-    a.counters = static_cast<unsigned*>(workspace);
-    a.err = di->err;
-    const int smem = (int)(STREAM_HDR + a.xtile_bytes + nst * STAGE_BYTES + ybuf);
-    if (!smem_optin(gemv_chain_kernel, smem, di->smem_optin)) return QMM_ERR_SHAPE;
-    int resident = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, gemv_chain_kernel, STREAM_THREADS, smem) !=
-            cudaSuccess ||
-        resident < per_sm) {
-        cudaGetLastError();
-        return QMM_ERR_DEVICE;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)G);
-    cfg.blockDim = dim3(STREAM_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = S(stream);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: they wait on one another
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_chain_kernel, a);
-    return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
 }
 
 qmm_status qmm_debug_gemm_kernel(int kernel, int* previous) {

@@ -370,8 +370,7 @@ __device__ __forceinline__ RmsGamma rms_gamma_load(const float* gamma, int64_t K
 
 // The one-pass staging once this thread's values are in registers: v[2i],
 // v[2i+1] hold values 8p..8p+7 (p = tid & 3) of block i * nthr/4 + tid/4
-// (zero past the row).  Shared by every source of x (plain loads here; the
-// decode chain's flagged buffers).
+// (zero past the row).
 __device__ __forceinline__ void stage_rmsnorm_regs(const XTile& xt, const float4 (&v)[2 * RMS_STEPS],
                                                    const RmsGamma& gr, int64_t K, float eps, int8_t* xq_out,
                                                    uint16_t* xd_out, float* red, int tid, int nthr, int bar) {
@@ -473,8 +472,7 @@ __device__ __forceinline__ void stage_f32_rmsnorm(const XTile& xt, const float* 
 // float4 per lane); STAGE_STEPS steps are loaded before any is quantized, so
 // the activation costs one memory round trip per STAGE_STEPS * nwarps * 4
 // blocks.  This quantizes one round: v[i] holds values part*4..part*4+3
-// (part = lane & 7) of block (g0 + i * nwarps) * 4 + lane / 8.  Shared by
-// every source of x (plain loads here; the decode chain's flagged buffers).
+// (part = lane & 7) of block (g0 + i * nwarps) * 4 + lane / 8.
 constexpr int STAGE_STEPS = 8;
 
 __device__ __forceinline__ void stage_f32_quantize(const XTile& xt, const float4 (&v)[STAGE_STEPS], int g0, int B,

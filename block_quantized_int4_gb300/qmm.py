@@ -41,20 +41,12 @@ _lib = ctypes.CDLL(LIB_PATH)
 _P, _I64, _I32, _INT, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int, ctypes.c_size_t
 
 class GemvOp(ctypes.Structure):
-    """qmm_gemv_op of include/qmm.h (one op of qmm_gemv_chain)."""
+    """qmm_gemv_op of include/qmm.h (one batch-1 GEMV of a decode step)."""
     _fields_ = [("w_qs", ctypes.c_void_p), ("w_d", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("x", ctypes.c_void_p), ("norm_w", ctypes.c_void_p), ("xq", ctypes.c_void_p),
                 ("xd", ctypes.c_void_p), ("residual", ctypes.c_void_p), ("y", ctypes.c_void_p),
                 ("yq", ctypes.c_void_p), ("yd", ctypes.c_void_p), ("norm_eps", ctypes.c_float),
                 ("flags", ctypes.c_int32)]
-
-
-class ChainOp(ctypes.Structure):
-    """qmm_chain_op of include/qmm.h (one op of qmm_decode_chain)."""
-    _fields_ = [("w_qs", ctypes.c_void_p), ("w_d", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
-                ("src", ctypes.c_int32), ("residual", ctypes.c_int32), ("x", ctypes.c_void_p),
-                ("norm_w", ctypes.c_void_p), ("norm_eps", ctypes.c_float), ("flags", ctypes.c_int32),
-                ("y", ctypes.c_void_p), ("xq", ctypes.c_void_p), ("xd", ctypes.c_void_p)]
 
 
 class StorePlane(ctypes.Structure):
@@ -76,11 +68,6 @@ SIGNATURES = {
     "qmm_debug_block_dots": [_P, _I64, _I64, _I64, _P, _P, _P],
     "qmm_debug_gemm_kernel": [_INT, ctypes.POINTER(_INT)],
     "qmm_debug_stream_wait": [ctypes.c_uint64, _INT, ctypes.POINTER(ctypes.c_uint64)],
-    "qmm_decode_chain_workspace_size": [_P, _I32, ctypes.POINTER(_SZ)],
-    "qmm_decode_chain": [_P, _I32, _P, _SZ, _P],
-    "qmm_debug_decode_wait": [ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64)],
-    "qmm_gemv_chain_workspace_size": [_I32, ctypes.POINTER(_SZ)],
-    "qmm_gemv_chain": [ctypes.POINTER(GemvOp), _I32, _P, _SZ, _P],
     "qmm_gemv_fused_op": [ctypes.POINTER(GemvOp), _INT, _P],
     "qmm_moe_workspace_size": [_I32, _I32, _I32, ctypes.POINTER(_SZ)],
     "qmm_moe_gemv": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
@@ -226,50 +213,6 @@ def gemv_op(w_qs, w_d, N, K, x=None, xq=None, xd=None, residual=None, y=None, yq
 
 def qmm_gemv_fused_op(op, flags=0, stream=None):
     _check(_lib.qmm_gemv_fused_op(ctypes.byref(op), int(flags), _stream(stream)), "qmm_gemv_fused_op")
-
-
-def qmm_gemv_chain_workspace_size(n_ops) -> int:
-    out = _SZ(0)
-    _check(_lib.qmm_gemv_chain_workspace_size(n_ops, ctypes.byref(out)), "qmm_gemv_chain_workspace_size")
-    return out.value
-
-
-def qmm_gemv_chain(ops, n_ops, workspace, workspace_bytes, stream=None):
-    """ops: a sequence of GemvOp (or a ctypes array of them)."""
-    arr = ops if isinstance(ops, ctypes.Array) else (GemvOp * len(ops))(*ops)
-    _check(_lib.qmm_gemv_chain(arr, n_ops, _ptr(workspace), workspace_bytes, _stream(stream)), "qmm_gemv_chain")
-
-
-def chain_op(w_qs, w_d, N, K, src=-1, residual=-1, x=None, norm_w=None, norm_eps=1e-5, flags=0, y=None, xq=None,
-             xd=None):
-    """A qmm_chain_op from tensors (or None / raw pointers) and op indices."""
-    return ChainOp(_ptr(w_qs), _ptr(w_d), N, K, int(src), int(residual), _ptr(x), _ptr(norm_w), float(norm_eps),
-                   int(flags), _ptr(y), _ptr(xq), _ptr(xd))
-
-
-def _chain_array(ops):
-    return ops if isinstance(ops, ctypes.Array) else (ChainOp * len(ops))(*ops)
-
-
-def qmm_decode_chain_workspace_size(ops) -> int:
-    arr = _chain_array(ops)
-    out = _SZ(0)
-    _check(_lib.qmm_decode_chain_workspace_size(arr, len(arr), ctypes.byref(out)), "qmm_decode_chain_workspace_size")
-    return out.value
-
-
-def qmm_decode_chain(ops, workspace, workspace_bytes, stream=None):
-    """ops: a sequence of ChainOp (or a ctypes array of them)."""
-    arr = _chain_array(ops)
-    _check(_lib.qmm_decode_chain(arr, len(arr), _ptr(workspace), workspace_bytes, _stream(stream)),
-           "qmm_decode_chain")
-
-
-def qmm_debug_decode_wait(limit_ns):
-    """Bound of qmm_decode_chain's device waits (ns); returns the previous one."""
-    prev = ctypes.c_uint64(0)
-    _check(_lib.qmm_debug_decode_wait(int(limit_ns), ctypes.byref(prev)), "qmm_debug_decode_wait")
-    return prev.value
 
 
 def qmm_moe_workspace_size(E, T, k) -> int:

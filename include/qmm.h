@@ -219,7 +219,7 @@ QMM_API qmm_status qmm_debug_block_dots(const uint8_t* w_qs, int64_t N, int64_t 
                                 int32_t* dots, void* stream);
 
 /* ---------------------------------------------------------------------
- * A chain of dependent batch-1 GEMVs in one launch (a decode step's
+ * One batch-1 GEMV of a decode step described by an op (a decode step's
  * projections, TinyLLaMA guide section 5 graph; each op as qmm_gemv_fused)
  * ------------------------------------------------------------------- */
 
@@ -255,105 +255,6 @@ typedef struct qmm_gemv_op {
 /* One op as one launch of the streaming GEMV kernel.  flags: 0 or
  * QMM_CHAIN (programmatic dependent launch, as for qmm_gemv_q4_0_f32). */
 QMM_API qmm_status qmm_gemv_fused_op(const qmm_gemv_op* op, int flags, void* stream);
-
-#define QMM_CHAIN_MAX_OPS 96
-
-/* Bytes of workspace qmm_gemv_chain needs for n_ops ops (one completion
- * counter per op). */
-QMM_API qmm_status qmm_gemv_chain_workspace_size(int32_t n_ops, size_t* bytes);
-
-/* Runs ops[0..n_ops) in order as one persistent cooperative launch (one CTA
- * per SM): op i starts once op i-1 has finished on every CTA, so op i may
- * read any output of an earlier op.  Results are those of calling
- * qmm_gemv_fused for each op in turn.  The weights of all ops stream from
- * HBM back to back, ahead of the activations.
- *  - ops: host array of n_ops (1..QMM_CHAIN_MAX_OPS) descriptors, read
- *    during the call (copied into the launch).
- *  - workspace: device, >= qmm_gemv_chain_workspace_size bytes, 4-byte
- *    aligned, and ALL ZERO before the first call.  A call that completes
- *    leaves it zero again, so it can be reused by the next call on the same
- *    stream (including replays of a captured graph).  After a call that
- *    reported QMM_ERR_TIMEOUT through qmm_last_device_error it must be
- *    zeroed again.  Two chains must not share a workspace concurrently.
- *  - An op's outputs must not alias its own inputs.  An op may overwrite
- *    a buffer that an earlier op read (ops run strictly one after another).
- * Returns QMM_ERR_DEVICE if the device cannot hold one CTA per SM. */
-QMM_API qmm_status qmm_gemv_chain(const qmm_gemv_op* ops, int32_t n_ops, void* workspace, size_t workspace_bytes,
-                          void* stream);
-
-/* ---------------------------------------------------------------------
- * A decode step as one launch with flagged hand-over between its ops
- * ------------------------------------------------------------------- */
-
-#define QMM_DECODE_MAX_OPS 96
-#define QMM_DECODE_MAX_K 16384
-
-/* One op of qmm_decode_chain: y = W x (+ residual), or SwiGLU of row pairs,
- * with Q4_0 weights and the input quantized to Q8_0 (optionally RMSNorm-ed
- * first) -- the batch-1 product of the llama.cpp guide (kenji.blog/id),
- * section 2.2, on the TinyLLaMA C++ guide's block format (section 6.1), in
- * the layer graph of its section 5.2 (RMSNorm 4.1, SwiGLU 4.4).
- *  - w_qs [N][K/2], w_d [N][K/32]: Q4_0 planes, device, 16-byte aligned.
- *    N even, 2 <= N < 2^31; K a multiple of 256, 256 <= K <= QMM_DECODE_MAX_K.
- *  - src: where the input (K values) comes from: -1 = x (fp32 [K], device,
- *    16-byte aligned, written before the call); j (0 <= j < this op's
- *    index) = the first K values of op j's output.
- *  - residual: -1 none; -2 = x (its first N values); j = op j's output
- *    (its first N values), added to each output (not with SwiGLU pairs).
- *  - norm_w: RMSNorm weight [K] (16-byte aligned; K <= 4096) applied to the
- *    input before Q8_0, with norm_eps; NULL: no RMSNorm.
- *  - flags: 0, or QMM_Y_SWIGLU_PAIRS (rows 2n, 2n + 1 are a gate/up pair;
- *    output n = SwiGLU(gate, up), N/2 outputs).
- *  - y: optional fp32 copy of the output ([N] or [N/2]), device, 4-byte
- *    aligned.  The output an op hands to later ops lives in the workspace.
- *  - xq, xd: optional (both or neither): the Q8_0 activation this op staged
- *    (int8 [K] 16-byte aligned, fp16 bits [K/32]), for inspection. */
-typedef struct qmm_chain_op {
-    const uint8_t* w_qs;
-    const uint16_t* w_d;
-    int64_t N, K;
-    int32_t src;
-    int32_t residual;
-    const float* x;
-    const float* norm_w;
-    float norm_eps;
-    int32_t flags;
-    float* y;
-    int8_t* xq;
-    uint16_t* xd;
-} qmm_chain_op;
-
-/* Bytes of workspace qmm_decode_chain needs for this chain: a 256-byte
- * control block plus 8 bytes per output value that a later op reads.
- * Validates the chain as qmm_decode_chain does. */
-QMM_API qmm_status qmm_decode_chain_workspace_size(const qmm_chain_op* ops, int32_t n_ops, size_t* bytes);
-
-/* Runs ops[0..n_ops) (1..QMM_DECODE_MAX_OPS) as one persistent cooperative
- * launch, one CTA per SM.  Each CTA streams the weight rows of all its ops
- * back to back into shared memory, ahead of the activations; an op's
- * outputs that later ops read are stored in the workspace as 64-bit words
- * that carry the value and a flag naming the op and the call, and a CTA
- * starts an op as soon as the words it reads carry that op's flag.  Results
- * are bit-identical to running each op through qmm_gemv_fused_op in turn
- * (same per-row arithmetic, Q8_0 rule and RMSNorm reduction order).
- *  - ops: host array, read during the call (copied into the launch).
- *  - workspace: device, >= qmm_decode_chain_workspace_size bytes, 16-byte
- *    aligned, ALL ZERO before its first use.  It keeps a call counter
- *    between calls, so calls (and replays of a captured graph) reuse it
- *    without clearing it; it stays valid after a call that timed out.  Two
- *    chains must not use one workspace concurrently.
- *  - Every wait on the device is bounded (two seconds by default,
- *    qmm_debug_decode_wait); on expiry the launch ends early and
- *    qmm_last_device_error reports QMM_ERR_TIMEOUT.
- * Returns QMM_ERR_CUDA if the device cannot hold one CTA per SM. */
-QMM_API qmm_status qmm_decode_chain(const qmm_chain_op* ops, int32_t n_ops, void* workspace, size_t workspace_bytes,
-                                    void* stream);
-
-/* Bound of qmm_decode_chain's device waits for the launches that follow,
- * limit_ns in [1e3, 1e10] (default 2e9); `previous_limit_ns` (may be NULL)
- * receives the old bound.  QMM_ERR_ARG outside that range.  No counterpart
- * on the pages. */
-QMM_API qmm_status qmm_debug_decode_wait(uint64_t limit_ns, uint64_t* previous_limit_ns);
 
 /* ---------------------------------------------------------------------
  * Weight-format variants of the batch-1 product

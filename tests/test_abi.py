@@ -104,27 +104,22 @@ def test_static_scratch_limit_and_arguments(qmm):
     assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, A16 + 2, 1, 2, A16, A16, 0, A16, None) == 3
 
 
-def test_chain_validation(qmm):
-    """qmm_gemv_chain rejects bad descriptors before any launch."""
+def test_fused_op_validation(qmm):
+    """qmm_gemv_fused_op rejects bad descriptors before any launch."""
     A16 = 0x10000
-    ws = qmm.qmm_gemv_chain_workspace_size(3)
-    assert ws >= 12 and ws % 16 == 0
     good = dict(w_qs=A16, w_d=A16, N=64, K=256, xq=A16, xd=A16, yq=A16, yd=A16)
 
-    def run(ops, n=None, wsp=A16, wsb=ws):
-        arr = (qmm.GemvOp * len(ops))(*[qmm.gemv_op(**o) for o in ops])
-        return qmm.library_handle().qmm_gemv_chain(arr, len(ops) if n is None else n, wsp, wsb, None)
+    def run(o, flags=0):
+        op = qmm.gemv_op(**o)
+        return qmm.library_handle().qmm_gemv_fused_op(ctypes.byref(op), flags, None)
 
-    assert run([good], n=0) == 1
-    assert run([good], n=97) == 1                        # more than QMM_CHAIN_MAX_OPS
-    assert run([good], wsp=None) == 8
-    assert run([good], wsb=2) == 8
-    assert run([good, dict(good, K=288)]) == 2          # K % 256 != 0
-    assert run([good, dict(good, flags=4)]) == 1        # only Y_SWIGLU_PAIRS allowed
-    assert run([good, dict(good, N=48)]) == 2           # Q8_0 output needs N % 32 == 0
-    assert run([dict(good, w_d=A16 + 2)]) == 3          # scale plane 16-byte aligned
-    assert run([dict(good, yq=None, yd=None)]) == 1     # no output at all
-    assert run([dict(good, flags=2, residual=A16)]) == 1  # pairs with a residual
+    assert run(good, flags=1) == 1                  # only QMM_CHAIN (4) as a call flag
+    assert run(dict(good, K=288)) == 2             # K % 256 != 0
+    assert run(dict(good, flags=4)) == 1           # only Y_SWIGLU_PAIRS as an op flag
+    assert run(dict(good, N=48)) == 2              # Q8_0 output needs N % 32 == 0
+    assert run(dict(good, w_d=A16 + 2)) == 3       # scale plane 16-byte aligned
+    assert run(dict(good, yq=None, yd=None)) == 1  # no output at all
+    assert run(dict(good, flags=2, residual=A16)) == 1  # pairs with a residual
 
 
 def test_router_and_pregrouped_validation(qmm):
@@ -183,8 +178,8 @@ def test_valid_call_without_gpu_reports_device_error(qmm):
     A16 = 0x10000
     assert _call(qmm, "qmm_gemv_q4_0_q8_0", A16, A16, 64, 64, A16, A16, A16, None) == 4
     assert _call(qmm, "qmm_moe_gemv_static", A16, A16, 8, 64, 64, A16, 1, 2, A16, A16, 0, A16, None) == 4
-    arr = (qmm.GemvOp * 1)(qmm.gemv_op(A16, A16, 64, 256, xq=A16, xd=A16, y=A16))
-    assert qmm.library_handle().qmm_gemv_chain(arr, 1, A16, 16, None) == 4
+    op = qmm.gemv_op(A16, A16, 64, 256, xq=A16, xd=A16, y=A16)
+    assert qmm.library_handle().qmm_gemv_fused_op(ctypes.byref(op), 0, None) == 4
     assert _call(qmm, "qmm_moe_router_topk", A16, 16, 256, 8, A16, A16, None, 0, None) == 4
     assert _call(qmm, "qmm_gemv_rowwise_q8_0", A16, A16, 4, 8, 64, A16, A16, A16, None) == 4
     assert _call(qmm, "qmm_gemv_q4_0_f32_fma", A16, A16, 8, 64, A16, A16, None) == 4
@@ -234,42 +229,3 @@ def test_stream_wait_hook_arguments(qmm):
     assert lib.qmm_debug_stream_wait(1_000_000, 2, None) == 1
     assert lib.qmm_debug_stream_wait(1_000_000, 0, ctypes.byref(prev)) == 0 and prev.value == 2_000_000_000
     assert lib.qmm_debug_stream_wait(2_000_000_000, 0, ctypes.byref(prev)) == 0 and prev.value == 1_000_000
-
-
-def test_decode_chain_validation_and_workspace(qmm):
-    """qmm_decode_chain_workspace_size validates the chain on the host: op
-    links point backwards, shapes, the one-pass RMSNorm limit, alignment;
-    the workspace is 256 bytes plus 8 bytes per output value a later op reads."""
-    A16 = 0x10000
-    op = qmm.chain_op
-    ok = [op(A16, A16, 2560, 2048, src=-1, x=A16, norm_w=A16),
-          op(A16, A16, 2048, 2048, src=0, residual=-2, x=A16),
-          op(A16, A16, 11264, 2048, src=1, norm_w=A16, flags=qmm.Y_SWIGLU_PAIRS),
-          op(A16, A16, 2048, 5632, src=2, residual=1),
-          op(A16, A16, 32000, 2048, src=3, norm_w=A16, y=A16)]
-    assert qmm.qmm_decode_chain_workspace_size(ok) == 256 + 8 * (2560 + 2048 + 5632 + 2048)
-
-    def status(ops):
-        arr = (qmm.ChainOp * len(ops))(*ops)
-        n = ctypes.c_size_t(0)
-        return qmm._lib.qmm_decode_chain_workspace_size(arr, len(ops), ctypes.byref(n))
-
-    assert status(ok) == 0
-    assert status([op(A16, A16, 64, 256, src=0, x=A16)]) == 1                       # src not an earlier op
-    assert status([op(A16, A16, 64, 256)]) == 1                                     # src -1 without x
-    assert status([op(A16, A16, 63, 256, x=A16)]) == 2                              # N odd
-    assert status([op(A16, A16, 64, 288, x=A16)]) == 2                              # K % 256
-    assert status([op(A16, A16, 64, 8192, x=A16, norm_w=A16)]) == 2                 # RMSNorm beyond one pass
-    assert status([op(A16, A16, 64, 256, x=A16, residual=-2, flags=qmm.Y_SWIGLU_PAIRS)]) == 1  # residual + pairs
-    assert status([op(A16, A16, 64, 256, x=A16), op(A16, A16, 64, 512, src=0)]) == 2  # input longer than src
-    assert status([op(A16 + 8, A16, 64, 256, x=A16)]) == 3                          # weights misaligned
-    assert status([op(A16, A16, 64, 256, x=A16, xq=A16)]) == 1                      # xq without xd
-    lib = qmm._lib
-    arr = (qmm.ChainOp * len(ok))(*ok)
-    need = qmm.qmm_decode_chain_workspace_size(ok)
-    assert lib.qmm_decode_chain(arr, len(ok), ctypes.c_void_p(A16), need - 16, None) == 8  # workspace too small
-    assert lib.qmm_decode_chain(arr, len(ok), ctypes.c_void_p(A16 + 8), need, None) == 3   # misaligned workspace
-    prev = ctypes.c_uint64(0)
-    assert lib.qmm_debug_decode_wait(999, None) == 1
-    assert lib.qmm_debug_decode_wait(1_000_000, ctypes.byref(prev)) == 0 and prev.value == 2_000_000_000
-    assert lib.qmm_debug_decode_wait(2_000_000_000, ctypes.byref(prev)) == 0 and prev.value == 1_000_000

@@ -1,7 +1,8 @@
-"""qmm_gemv_chain: a chain of dependent GEMVs in one launch gives exactly the
-outputs of the same ops run one by one through qmm_gemv_fused (same per-row
-arithmetic), and the oracle's within the fp32 tolerance for the first op and
-a propagated tolerance for the chain."""
+"""A small decoder stack run as the decode step's fused GEMV launches
+(qmm_gemv_fused_op): the first op against the oracle (bit-exact RMSNorm ->
+Q8_0 codes, fp32 tolerance on the product), the whole stack against the
+oracle's own stack within a relative L2 of 1e-3, and the same result from a
+replayed CUDA graph of the chained (programmatic dependent launch) form."""
 import numpy as np
 import pytest
 import torch
@@ -78,25 +79,35 @@ class MiniDecode:
             t.fill_(0)
 
 
-def test_chain_equals_ops_one_by_one_and_leaves_workspace_zero():
+def test_chained_launches_from_a_graph_equal_plain_launches():
+    """The ops launched with programmatic dependent launch from a replayed
+    CUDA graph give exactly the outputs of plain launches, replay after
+    replay."""
     qmm = lib()
     qmm.qmm_last_device_error()
     dec = MiniDecode(qmm)
     dec.run_one_by_one()
     torch.cuda.synchronize()
     ref = dec.snapshot()
-    dec.reset_outputs()
     ops = dec.ops()
-    wsb = qmm.qmm_gemv_chain_workspace_size(len(ops))
-    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
-    for rep in range(2):  # twice in a row on the same workspace
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for op in ops:
+            qmm.qmm_gemv_fused_op(op, qmm.CHAIN, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for op in ops:
+            qmm.qmm_gemv_fused_op(op, qmm.CHAIN, stream=torch.cuda.current_stream())
+    for rep in range(3):
         dec.reset_outputs()
-        qmm.qmm_gemv_chain(ops, len(ops), ws, wsb)
-        assert qmm.qmm_last_device_error() == 0
-        got = dec.snapshot()
-        for i, (a, b) in enumerate(zip(got, ref)):
-            assert torch.equal(a, b), f"output {i} differs from the one-by-one ops (call {rep})"
-        assert int(ws.count_nonzero()) == 0
+        g.replay()
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(zip(dec.snapshot(), ref)):
+            assert torch.equal(a, b), f"output {i} differs from the plain launches (replay {rep})"
+    assert qmm.qmm_last_device_error() == 0
 
 
 def _planes_to_oracle(qs, d, N, K):
@@ -106,7 +117,7 @@ def _planes_to_oracle(qs, d, N, K):
     return O.unpack_q4_0_blocks(blocks, N, K)
 
 
-def test_chain_first_op_and_end_to_end_against_oracle():
+def test_first_op_and_end_to_end_against_oracle():
     """Op 0: the GPU's Q8_0 of RMSNorm(x): codes bit-exact against the
     oracle's Q8_0 of fl(x * gamma), scales within one fp16 step of
     fp16(d32_z / rms); its output against the oracle's product of the GPU's
@@ -115,10 +126,7 @@ def test_chain_first_op_and_end_to_end_against_oracle():
     L2 of 1e-3."""
     qmm = lib()
     dec = MiniDecode(qmm, L=1)
-    ops = dec.ops()
-    wsb = qmm.qmm_gemv_chain_workspace_size(len(ops))
-    ws = torch.zeros(wsb, dtype=torch.uint8, device=DEV)
-    qmm.qmm_gemv_chain(ops, len(ops), ws, wsb)
+    dec.run_one_by_one()
     assert qmm.qmm_last_device_error() == 0
     H, Q, F, V = dec.H, dec.Q, dec.F, dec.V
     (qkv, o, gu, down, (ga, gf)) = dec.layers[0]
@@ -151,22 +159,3 @@ def test_chain_first_op_and_end_to_end_against_oracle():
     assert np.isfinite(g).all()
     rel = np.linalg.norm(g - logits[0]) / np.linalg.norm(logits[0])
     assert rel < 1e-3, rel
-
-
-def test_chain_full_decode_step_equals_per_op_chain():
-    """The TinyLLaMA-shaped decode step of bench.py (89 ops, 22 layers): the
-    one-launch chain and the 89 PDL-chained launches give identical, finite
-    logits."""
-    qmm = lib()
-    import bench
-    dec = bench.TinyLlamaDecode(qmm, torch, seed=3)
-    dec.step()
-    torch.cuda.synchronize()
-    ref = dec.logits.clone()
-    href = dec.h[(dec.L - 1) % 2].clone()
-    dec.logits.fill_(0)
-    dec.chain_step()
-    assert qmm.qmm_last_device_error() == 0
-    assert torch.isfinite(ref).all()
-    assert torch.equal(dec.logits, ref)
-    assert torch.equal(dec.h[(dec.L - 1) % 2], href)
