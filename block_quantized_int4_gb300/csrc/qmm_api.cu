@@ -664,6 +664,8 @@ qmm_status moe_apply(const DevInfo* di, const uint8_t* w_qs, const uint16_t* w_d
         m.xd = xd;
         m.xf = xf;
         m.x_per_slot = x_per_slot;
+        m.nslots = (int)nslots;
+        m.slots_smem = nslots <= MOE_SMEM_SLOTS ? 1 : 0;
         m.y = y;
         m.pairs = pairs ? 1 : 0;
         m.ws = ws;
@@ -677,8 +679,9 @@ qmm_status moe_apply(const DevInfo* di, const uint8_t* w_qs, const uint16_t* w_d
         // 0.552 with two, 0.665 with one; 1 token fastest with one.
         const int mt = nslots * 4 > (int64_t)E ? 4 : 1;
         const int64_t xtile = round_up((int64_t)mt * B * xtile_bytes_per_block(), 128);
-        // active list (padded to an even count) + 8-byte slot spans in shared memory
-        const int64_t tables = round_up((int64_t)((E + 1) & ~1) * 4 + (int64_t)E * 8, 128);
+        // routing tables in shared memory: active list and slot starts (E each),
+        // the slot list when short, count and end
+        const int64_t tables = round_up((int64_t)E * 8 + (m.slots_smem ? nslots * 4 : 0) + 8, 128);
         // two CTAs per SM (110 KB each): more warps to hide the dot-product latency
         const int64_t nst =
             std::min<int64_t>((110 * 1024 - STREAM_HDR - xtile - tables) / STAGE_BYTES, STREAM_MAX_STAGES);

@@ -676,7 +676,11 @@ __global__ void block_dots_kernel(const uint8_t* __restrict__ qs, int64_t N, int
 // ============================================================================
 
 // Workspace (int32 words): counts[E] | offsets[E+1] | cursor[E] | active[E]
-// | n_active[1] | slot_list[T*k]
+// | n_active[1] | slot_list[T*k].  counts and offsets are per expert id;
+// active[i] is the i-th routed expert (ascending id), cursor[i] the start of
+// its slots in slot_list (i < n_active; its end is cursor[i + 1], or
+// offsets[E] for the last), so a kernel can read its routing in one round
+// of independent loads.
 struct MoeWs {
     int* counts;
     int* offsets;
@@ -714,7 +718,77 @@ constexpr int GROUP_THREADS = 1024;
 // global-memory traffic is the final tables, written once.
 constexpr int GROUP_SMEM_E = 2048;
 
+// Few slots (one token's top-k, up to 32): each thread derives the tables of
+// its experts directly from the slot ids -- counts, offsets and active
+// positions by comparing against every slot -- with no scan, no atomics and
+// two block barriers.  Slots of one expert keep their slot order.
+constexpr int GROUP_FEW = 32;
+
+// The tables of a few slots (nslots <= GROUP_FEW) built from their ids by
+// the whole block: warp 0 holds one slot per lane and finds, with warp
+// intrinsics, each slot's first occurrence and its place in the slot list;
+// then every thread derives the counts, offsets and active position of its
+// experts by comparing against the slots (fixed-trip, unrolled).  Every
+// word the workspace layout defines is written.  f_id / f_first: GROUP_FEW
+// ints of shared memory each.
+__device__ __forceinline__ void moe_group_few_tables(const int32_t* ids, int nslots, int E, MoeWs w, int* f_id,
+                                                     int* f_first, int* err) {
+    if (threadIdx.x < 32) {
+        const int s = threadIdx.x;
+        int e = s < nslots ? ids[s] : -1;
+        if (s < nslots && (e < 0 || e >= E)) {
+            atomicOr(err, ERR_BAD_EXPERT);
+            e = -1;
+        }
+        const unsigned same = __match_any_sync(FULL, e);
+        const bool first = e >= 0 && (__ffs(same) - 1) == s;
+        f_id[s] = e;
+        f_first[s] = first ? 1 : 0;
+        // place in the slot list: every valid slot of a lower expert, then the
+        // earlier slots of the same expert
+        int pos = __popc(same & ((1u << s) - 1u));
+#pragma unroll
+        for (int t = 0; t < GROUP_FEW; ++t) {
+            const int v = __shfl_sync(FULL, e, t);
+            pos += v >= 0 && v < e;
+        }
+        if (e >= 0) w.slots[pos] = s;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        int cnt = 0, below = 0, dist_below = 0;
+#pragma unroll
+        for (int t = 0; t < GROUP_FEW; ++t) {
+            const int v = f_id[t];  // -1 past nslots
+            cnt += v == e;
+            below += v >= 0 && v < e;
+            dist_below += f_first[t] && v < e;
+        }
+        if (e == E) {  // every valid slot, every routed expert
+            w.offsets[E] = below;
+            *w.n_active = dist_below;
+            continue;
+        }
+        w.offsets[e] = below;
+        w.counts[e] = cnt;
+        if (cnt > 0) {
+            w.active[dist_below] = e;
+            w.cursor[dist_below] = below;
+        }
+    }
+}
+
+__device__ __forceinline__ void moe_group_few(const int32_t* ids, int nslots, int E, MoeWs w, int* err) {
+    __shared__ int f_id[GROUP_FEW];     // slot id, or -1 (none, or an id outside [0, E))
+    __shared__ int f_first[GROUP_FEW];  // 1 if no earlier slot has the same id
+    moe_group_few_tables(ids, nslots, E, w, f_id, f_first, err);
+}
+
 __device__ __forceinline__ void moe_group_block(const int32_t* ids, int nslots, int E, MoeWs w, int* err) {
+    if (nslots <= GROUP_FEW) {
+        moe_group_few(ids, nslots, E, w, err);
+        return;
+    }
     __shared__ int s_cnt[GROUP_SMEM_E];
     __shared__ int s_cur[GROUP_SMEM_E];
     const bool in_smem = E <= GROUP_SMEM_E;
@@ -781,10 +855,11 @@ __device__ __forceinline__ void moe_group_block(const int32_t* ids, int nslots, 
         const int pos = atomicAdd(&cur[e], 1);
         w.slots[pos] = s;
     }
-    if (in_smem) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < E; e += blockDim.x) w.cursor[e] = cur[e];  // each expert's end
-    }
+    // cursor[i]: the start of the i-th active expert's slots (the sort's own
+    // cursors are no longer needed)
+    __syncthreads();
+    const int na = *w.n_active;
+    for (int i = threadIdx.x; i < na; i += blockDim.x) w.cursor[i] = w.offsets[w.active[i]];
 }
 
 __global__ void __launch_bounds__(GROUP_THREADS) moe_group_kernel(const int32_t* __restrict__ ids, int nslots, int E,
@@ -811,13 +886,15 @@ constexpr int ROUTE_MAX_K = 64;
 constexpr int ROUTE_PER_LANE = ROUTE_MAX_E / 32;
 constexpr int ROUTE_THREADS = 1024;
 
+// PER_LANE: register slots per lane (E <= 32 * PER_LANE).
+template <int PER_LANE = ROUTE_PER_LANE>
 __device__ __forceinline__ void route_token(const float* __restrict__ lg, int E, int k, int32_t* ids, float* gates,
                                             int lane) {
-    float v[ROUTE_PER_LANE];
+    float v[PER_LANE];
     uint32_t taken = 0;  // bit i: expert lane + 32 i is chosen already, or does not exist
     const int nper = (E + 31) >> 5;  // register slots in use
 #pragma unroll
-    for (int i = 0; i < ROUTE_PER_LANE; ++i) {
+    for (int i = 0; i < PER_LANE; ++i) {
         const int e = lane + 32 * i;
         v[i] = 0.f;
         if (e < E)
@@ -837,7 +914,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, int E,
         float bv = 0.f;
         int bi = INT_MAX;  // none yet
 #pragma unroll
-        for (int i = 0; i < ROUTE_PER_LANE; ++i) {
+        for (int i = 0; i < PER_LANE; ++i) {
             if (i >= nper) break;
             if (!((taken >> i) & 1u) && (bi == INT_MAX || v[i] > bv)) {  // ascending index: ties keep the lower
                 bv = v[i];
@@ -873,6 +950,84 @@ __device__ __forceinline__ void route_token(const float* __restrict__ lg, int E,
     }
 }
 
+// The same selection and gates for a few tokens (T * k <= GROUP_FEW) and
+// E <= 32 * (blockDim.x / 32) experts, with the whole block: per token, warp
+// w ranks the logits of experts 32w .. 32w + 31 among themselves (value,
+// then lower index) and keeps its best k as candidates; each candidate is
+// then ranked among all candidates, and the one of rank j is the token's
+// j-th choice.  The k best of every warp hold the k best overall, so for
+// finite logits the choice is that of route_token; the gates are formed as
+// there (fp32 sigmoid with expf, their sum in choice order, one division
+// each).  Every step is a fixed-trip, branch-free loop of independent
+// operations (one warp alone runs a dependent chain at a few cycles per
+// operation, so trip counts and divisions would cost microseconds).
+// ids/gates: [T][k] in shared memory; cand: 2 * 32 * (blockDim.x / 32)
+// words of shared memory.  Every thread of the block.
+__device__ __forceinline__ void route_few_block(const float* __restrict__ logits, int T, int E, int k, int32_t* ids,
+                                                float* gates, int* cand) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (E + 31) >> 5;
+    const int nc = nw * k;  // candidate slots: k per warp
+    float* cv = reinterpret_cast<float*>(cand);
+    int* ci = cand + 32 * (blockDim.x >> 5);
+    for (int t = 0; t < T; ++t) {
+        // slots a warp with fewer than k experts leaves empty rank last
+        for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+            cv[c] = -INFINITY;
+            ci[c] = INT_MAX;
+        }
+        __syncthreads();
+        if (warp < nw) {
+            const int e = 32 * warp + lane;
+            const bool valid = e < E;
+            const float v = valid ? logits[(int64_t)t * E + e] : -INFINITY;
+            const int me = valid ? e : INT_MAX;
+            int rank = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float vj = __shfl_sync(FULL, v, j);
+                const int ej = __shfl_sync(FULL, me, j);
+                rank += (vj > v) | ((vj == v) & (ej < me));
+            }
+            if (valid && rank < k) {
+                cv[warp * k + rank] = v;
+                ci[warp * k + rank] = e;
+            }
+        }
+        __syncthreads();
+        float sc = 0.f;
+        int my = -1;
+        if ((int)threadIdx.x < nc) {
+            const float v = cv[threadIdx.x];
+            const int e = ci[threadIdx.x];
+            int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+            int d = 0;
+            for (; d + 4 <= nc; d += 4) {
+                r0 += (cv[d] > v) | ((cv[d] == v) & (ci[d] < e));
+                r1 += (cv[d + 1] > v) | ((cv[d + 1] == v) & (ci[d + 1] < e));
+                r2 += (cv[d + 2] > v) | ((cv[d + 2] == v) & (ci[d + 2] < e));
+                r3 += (cv[d + 3] > v) | ((cv[d + 3] == v) & (ci[d + 3] < e));
+            }
+            for (; d < nc; ++d) r0 += (cv[d] > v) | ((cv[d] == v) & (ci[d] < e));
+            const int rank = r0 + r1 + r2 + r3;
+            if (e != INT_MAX && rank < k) {
+                ids[t * k + rank] = e;
+                sc = 1.0f / (1.0f + expf(-v));
+                gates[t * k + rank] = sc;
+                my = rank;
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float ssum = 0.f;
+            for (int j = 0; j < k; ++j) ssum += gates[t * k + j];  // choice order, as route_token
+            cv[0] = ssum;
+        }
+        __syncthreads();
+        if (my >= 0) gates[t * k + my] = sc / cv[0];
+        __syncthreads();
+    }
+}
+
 // Routes tokens warp by warp; with group != 0 (one CTA) the same block then
 // builds the expert grouping of the chosen ids in w.
 __global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const float* __restrict__ logits, int T, int E,
@@ -883,6 +1038,21 @@ __global__ void __launch_bounds__(ROUTE_THREADS) moe_route_kernel(const float* _
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (group && T * k <= GROUP_FEW && E <= (int)blockDim.x) {
+        // a decode-size batch: the block-wide top-k, then the grouping, both on
+        // the choices in shared memory
+        __shared__ int r_ids[GROUP_FEW], r_first[GROUP_FEW];
+        __shared__ float r_gates[GROUP_FEW];
+        __shared__ int r_cand[2 * ROUTE_THREADS];
+        __shared__ int r_fid[GROUP_FEW];
+        route_few_block(logits, T, E, k, r_ids, r_gates, r_cand);
+        if ((int)threadIdx.x < T * k) {
+            ids[threadIdx.x] = r_ids[threadIdx.x];
+            gates[threadIdx.x] = r_gates[threadIdx.x];
+        }
+        moe_group_few_tables(r_ids, T * k, E, w, r_fid, r_first, err);
+        return;
+    }
     for (int t = blockIdx.x * nw + warp; t < T; t += gridDim.x * nw)
         route_token(logits + (int64_t)t * E, E, k, ids + (int64_t)t * k, gates + (int64_t)t * k, lane);
     if (group) {

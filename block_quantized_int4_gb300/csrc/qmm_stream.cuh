@@ -377,6 +377,8 @@ __global__ void __launch_bounds__(STREAM_THREADS, MT <= 2 ? 2 : 1)
 struct MoeStreamArgs {
     int64_t N, K;
     int E, k;
+    int nslots;       // T * k
+    int slots_smem;   // the slot list is copied into shared memory (nslots <= MOE_SMEM_SLOTS)
     const int8_t* xq;
     const uint16_t* xd;
     const float* xf;  // fp32 activation rows instead of xq/xd (Q8_0 formed while staging), or NULL
@@ -393,23 +395,26 @@ struct MoeStreamArgs {
 // segment its slot passes (MT slots each), then per pass the segment's row
 // groups and K chunks.  So a pass stages its activations once for all the
 // segment's rows.
+constexpr int MOE_SMEM_SLOTS = 1024;
+
 struct MoeCursor {
     // 32-bit positions: the host admits this kernel only when E * N < 2^31
     int gr, gr1;  // position in the row space, end of this CTA's slice
     int N;
+    int n_active, total;  // routed experts; valid slots (end of the last span)
     // current segment: expert e, rows [r, r + nrows), slots [sbeg, send)
     int e, nrows, sbeg, send;
     int r;
-    // active: expert of each active index; span: (first slot, end slot) of
-    // each active index -- shared-memory copies of the grouping
-    __device__ bool next_segment(const int* active, const int2* span) {
+    // active: expert of each active index; start: first slot of each active
+    // index -- shared-memory copies of the grouping
+    __device__ bool next_segment(const int* active, const int* start) {
         if (gr >= gr1) return false;
         const int ai = gr / N;
         r = gr - ai * N;
         nrows = min(N - r, gr1 - gr);
         e = active[ai];
-        sbeg = span[ai].x;
-        send = span[ai].y;
+        sbeg = start[ai];
+        send = ai + 1 < n_active ? start[ai + 1] : total;
         gr += nrows;
         return true;
     }
@@ -443,19 +448,32 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the grouping written by the kernel before
 
-    // the active-expert list and each one's slot span, read once into shared
-    // memory (the walk below consults them for every row group)
-    const int n_active = *a.ws.n_active;
+    // The routing, read once into shared memory in one round of independent
+    // loads (the walk below consults it for every row group): the active
+    // experts and the start of each one's slots, for every possible active
+    // index (those past n_active are not used), the count and the end, and
+    // (when short enough) the slot list itself.
     int* s_active = reinterpret_cast<int*>(ring + (size_t)S * STAGE_BYTES);
-    int2* s_span = reinterpret_cast<int2*>(s_active + ((a.E + 1) & ~1));  // 8-byte aligned for any E
-    for (int i = tid; i < n_active; i += blockDim.x) {
-        const int e = a.ws.active[i];
-        s_active[i] = e;
-        s_span[i] = make_int2(a.ws.offsets[e], a.ws.offsets[e + 1]);
+    int* s_start = s_active + a.E;
+    int* s_slots = s_start + a.E;
+    int* s_count = s_slots + (a.slots_smem ? a.nslots : 0);  // n_active, total
+    for (int i = tid; i < a.E; i += blockDim.x) {
+        s_active[i] = a.ws.active[i];
+        s_start[i] = a.ws.cursor[i];
+    }
+    if (a.slots_smem)
+        for (int i = tid; i < a.nslots; i += blockDim.x) s_slots[i] = a.ws.slots[i];
+    if (tid == 0) {
+        s_count[0] = *a.ws.n_active;
+        s_count[1] = a.ws.offsets[a.E];
     }
     __syncthreads();
+    const int n_active = s_count[0];
+    const int* slot_list = a.slots_smem ? s_slots : a.ws.slots;
     const int64_t total = (int64_t)n_active * a.N;
     MoeCursor cur;
+    cur.n_active = n_active;
+    cur.total = s_count[1];
     if (a.pairs) {  // slices of whole (gate, up) row pairs (N is even)
         const int64_t tp = total / 2;
         cur.gr = 2 * (int)(tp * blockIdx.x / gridDim.x);
@@ -472,7 +490,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
             const uint64_t pol = l2_evict_first_policy();
             int u = 0, issued = 0;
             bool ok = true;
-            while (ok && cur.next_segment(s_active, s_span)) {
+            while (ok && cur.next_segment(s_active, s_start)) {
                 const int nsb = (cur.send - cur.sbeg + MT - 1) / MT;
                 const int ngroups = (cur.nrows + a.rb - 1) / a.rb;
                 for (int sb = 0; sb < nsb && ok; ++sb)
@@ -509,7 +527,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
     const int rA = 2 * warp, rB = 2 * warp + 16;
     int u = 0;
     bool failed = false;
-    while (cur.next_segment(s_active, s_span)) {
+    while (cur.next_segment(s_active, s_start)) {
         const int nslots = cur.send - cur.sbeg;
         const int nsb = (nslots + MT - 1) / MT;
         const int ngroups = (cur.nrows + a.rb - 1) / a.rb;
@@ -520,7 +538,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
                 const int j = sb * MT + t;
-                slot[t] = j < nslots ? a.ws.slots[cur.sbeg + j] : -1;
+                slot[t] = j < nslots ? slot_list[cur.sbeg + j] : -1;
                 xrow[t] = slot[t] < 0 ? -1 : (a.x_per_slot ? slot[t] : slot[t] / a.k);
             }
             asm volatile("bar.sync 1, %0;" ::"r"(NTHR) : "memory");  // everyone is done with the old tile

@@ -41,8 +41,9 @@ def _check_router(ids, gates, logits, k):
 def _check_grouping(ws, ids, E):
     """Tables (int32 words): counts[E] | offsets[E+1] | cursor[E] | active[E]
     | n_active | slots[T*k]: counts per expert, exclusive offsets, active
-    experts in ascending order, each expert's slot span holding exactly the
-    slots routed to it (in any order)."""
+    experts in ascending order with the start of each one's slots, each
+    expert's slot span holding exactly the slots routed to it (in any
+    order)."""
     w = ws.view(torch.int32).cpu().numpy()
     flat = ids.reshape(-1)
     counts = np.bincount(flat, minlength=E)
@@ -54,6 +55,8 @@ def _check_grouping(ws, ids, E):
     n_active = w[4 * E + 1]
     assert n_active == len(active)
     assert np.array_equal(w[a0:a0 + n_active], active)
+    c0 = 2 * E + 1  # cursor[i]: the start of the i-th active expert's slots
+    assert np.array_equal(w[c0:c0 + n_active], offsets[active])
     slots = w[4 * E + 2:4 * E + 2 + flat.size]
     for e in active:
         span = slots[offsets[e]:offsets[e + 1]]
