@@ -23,31 +23,35 @@
 // Work layout (one CTA per SM):
 //  - A CTA owns nst consecutive super-tiles of H <= 256 weight rows (two MMA
 //    tiles of 128 rows) and walks each over all of K in chunks of 8 blocks.
-//  - warp 9: TMA producer.  Per chunk one stage: the nibble tile (H rows x
+//  - warp 17: TMA producer.  Per chunk one stage: the nibble tile (H rows x
 //    128 B, 128-byte swizzled), its scales (H x 8 fp16), the chunk's Q8_0
 //    codes of the 16 token rows and their scales (rows >= M are zero-filled).
-//  - warps 0..7: worker w owns rows 128 (w / 4) + 32 (w % 4) + lane of the
-//    super-tile, i.e. TMEM lanes 32 (w % 4) .. + 31 of MMA tile w / 4.  For
-//    block j it reads the dot slice of block j (tcgen05.ld), writes the fp16
-//    codes of block j + 8 into the slice the MMA of block j has finished
-//    with (tcgen05.st), signals, and then adds d_w * d_x * dot into its 16
-//    per-token fp32 sums.  Warp w also turns block w of each chunk's
-//    activation codes into the fp16 B operand in shared memory.
-//  - warps 8 and 10: one lane each issues the MMAs of one tile (warp 8 also
-//    allocates TMEM): per block, two M=128 N=16 K=16 MMAs into the block's
-//    slice, then one commit to that tile's barrier.
+//  - warps 0..15: worker w owns rows 128 ((w / 4) % 2) + 32 (w % 4) + lane of
+//    the super-tile, i.e. TMEM lanes 32 (w % 4) .. + 31 of MMA tile
+//    (w / 4) % 2, and the blocks of parity w / 8 of every chunk: two workers
+//    share each row, each with its own sums, added through shared memory at
+//    the end of a super-tile (per-pair mbarriers, bounded waits).  For its
+//    block j a worker reads the dot slice of block j (tcgen05.ld), writes the
+//    fp16 codes of block j + 8 into the slice the MMA of block j has
+//    finished with (tcgen05.st), signals, and then adds d_w * d_x * dot into
+//    its 16 per-token fp32 sums.  Warps 0..7 also turn block w of each
+//    chunk's activation codes into the fp16 B operand in shared memory.
+//  - warps 16 and 18: one lane each issues the MMAs of one tile (warp 16
+//    also allocates TMEM): per block, two M=128 N=16 K=16 MMAs into the
+//    block's slice, then one commit to that tile's barrier.
 // TMEM: 8 slots (block mod 8) x 2 tiles x (16 columns of A + 16 of D).
 // Every wait is bounded; on expiry the kernel sets the device error word,
 // lets its own copies and MMAs finish, frees TMEM and returns.
 //
-// Measured on GB300 (16 tokens, 28672 x 8192): 115-117 us per call against
-// 66-77 us for the warp-MMA kernel, so the library routes to this kernel
-// only when asked (qmm_debug_gemm_kernel).  Each tcgen05.mma costs the
-// tensor core about 45 cycles whatever N (16..64), K and operand kind, so
-// the 1024 MMAs of a 192-row share take ~23 us; the bound that binds is the
-// worker warps' per-block work (nibble conversion, TMEM store and load,
-// rescale), about as many instructions per row and block as the warp-MMA
-// kernel's register path spends.
+// Measured on GB300 (16 tokens, 28672 x 8192): 84 us per call (8 workers:
+// 115-117 us) against 44.5 us for the warp-MMA kernel's 16-warp layout, so
+// the library routes to this kernel only when asked (qmm_debug_gemm_kernel).
+// Each tcgen05.mma costs the tensor core about 45 cycles whatever N (16..64),
+// K and operand kind, so the 1024 MMAs of a 192-row share take ~23 us; the
+// bound that binds is the workers' per-block work (nibble conversion, TMEM
+// store and load, rescale), about as many instructions per row and block as
+// the warp-MMA kernel's register path spends, with the TMEM round trip on
+// top.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -65,16 +69,18 @@ namespace tmk {
 
 constexpr int NTOK = 16;      // MMA N: token columns per launch
 constexpr int KB = 8;         // K blocks per chunk (one 128-byte nibble box column); also the TMEM slot count
-constexpr int WORKERS = 8;    // worker warps
-constexpr int WARP_MMA = 8, WARP_TMA = 9, WARP_MMA1 = 10;  // MMA issuers of tile 0 and tile 1
-constexpr int THREADS = 352;
+constexpr int WORKERS = 16;   // worker warps: two per TMEM lane quarter of each tile, one per parity of the blocks
+constexpr int PER_BLOCK = 8;  // worker warps that write the A slice of one block (4 lane quarters x 2 tiles)
+constexpr int WARP_MMA = 16, WARP_TMA = 17, WARP_MMA1 = 18;  // MMA issuers of tile 0 and tile 1
+constexpr int THREADS = 19 * 32;
+constexpr int RED_BYTES = 2 * 128 * NTOK * 4;  // the odd-block warps' sums of a super-tile, per row
 constexpr int MAX_STAGES = 8;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int XQ_BYTES = NTOK * KB * 32;  // activation codes of one chunk
 constexpr int XD_BYTES = NTOK * KB * 2;   // their scales
 constexpr int BBUF = KB * 1024;           // fp16 B operand of one chunk: [block][half][k chunk][token][16 B]
 constexpr int SXB = KB * NTOK * 4;        // d_x of one chunk as fp32: [block][token]
-constexpr int NBARS = 2 * MAX_STAGES + 2 + 3 * KB + 2;
+constexpr int NBARS = 2 * MAX_STAGES + 2 + 3 * KB + 2 + 2 * PER_BLOCK;
 
 struct Args {
     int64_t N, K, M, ldy;
@@ -83,7 +89,7 @@ struct Args {
     int nst;          // super-tiles per CTA
     int nstages;
     int stage_bytes;  // H * 144 + XQ_BYTES + XD_BYTES, rounded up to 1024
-    int off_bbuf, off_sx, off_bar;  // from the 1024-aligned base
+    int off_bbuf, off_sx, off_red, off_bar;  // from the 1024-aligned base
     int* err;
 };
 
@@ -233,6 +239,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t* ready = b_full + 2;               // [KB] 8 worker warps: A written, D read
     uint64_t* full = ready + KB;                // [2][KB] MMA commit per tile: D of the slot's block complete
     uint64_t* mma_done = full + 2 * KB;         // [2]  final MMA commit per issuer
+    uint64_t* red_full = mma_done + 2;          // [8] odd-block warp of a row slice wrote its sums
+    uint64_t* red_empty = red_full + PER_BLOCK; // [8] even-block warp of it has read them
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -248,14 +256,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&raw_full[s], 1);
             mbar_init(&raw_empty[s], WORKERS);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&b_full[i], WORKERS);
+        for (int i = 0; i < 2; ++i) mbar_init(&b_full[i], KB);  // warps 0..7 stage one block each
         for (int j = 0; j < KB; ++j) {
-            mbar_init(&ready[j], WORKERS);
+            mbar_init(&ready[j], PER_BLOCK);
             mbar_init(&full[j], 1);
             mbar_init(&full[KB + j], 1);
         }
         mbar_init(&mma_done[0], 1);
         mbar_init(&mma_done[1], 1);
+        for (int p = 0; p < PER_BLOCK; ++p) {
+            mbar_init(&red_full[p], 1);
+            mbar_init(&red_empty[p], 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -356,17 +368,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else {
-        // ---------------- workers
-        const int tile = warp >> 2, q = warp & 3;
+        // ---------------- workers: warp w owns TMEM lane quarter q = w & 3 of tile
+        // (w >> 2) & 1, and the blocks of parity hf = w >> 3 of every chunk, so
+        // two warps share each row's work and every SM sub-partition holds four
+        // workers; the two keep their own sums, added at the end of a super-tile
+        const int q = warp & 3, tile = (warp >> 2) & 1, hf = warp >> 3;
         const int rl = tile * 128 + q * 32 + lane;  // row inside the super-tile
         const int rs = min(rl, H - 1);              // its shared-memory row (lanes past H read a valid row)
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(tile * 32);
         uint64_t* fullt = full + tile * KB;  // this tile's MMA commits
         float* sx = reinterpret_cast<float*>(base + a.off_sx);
+        float* red = reinterpret_cast<float*>(base + a.off_red) + ((tile * 128 + q * 32 + lane) * NTOK);
         // the super-tile's rows reach this warp
         auto active = [&](int st) { return row_cta + (int64_t)st * H + tile * 128 + q * 32 < min(a.N, row_cta + (int64_t)(st + 1) * H); };
-        // B operand and d_x of chunk gc from its stage: warp w takes block w,
-        // lane = (half, token)
+        // B operand and d_x of chunk gc from its stage (warps 0..7): warp w
+        // takes block w, lane = (half, token)
         auto stage_b = [&](int gc) {
             const uint8_t* sp = base + (size_t)(gc % S) * a.stage_bytes;
             const int half = lane >> 4, tok = lane & 15;
@@ -402,15 +418,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint4 sc_cur = make_uint4(0u, 0u, 0u, 0u), sc_next = sc_cur;
         uint32_t v[16];
         if (ok) {
-            // chunk 0: B operand, A of its 8 blocks, the rows' scales
+            // chunk 0: B operand, A of this warp's 4 blocks, the rows' scales
             ok = warp_wait(&raw_full[0], 0, abort_flag);
             if (ok) {
                 const uint8_t* sp = base;
-                stage_b(0);
+                if (warp < KB) stage_b(0);
                 const bool act = active(0);
                 if (act) sc_cur = lds128(sp + H * 128 + rs * 16);
 #pragma unroll
-                for (int jj = 0; jj < KB; ++jj) {
+                for (int jj = hf; jj < KB; jj += 2) {
                     if (act) {
                         convert(sp, jj);
                         tmem_wait_st();
@@ -420,16 +436,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lane == 0) mbar_arrive(&ready[jj]);
                 }
                 if (lane == 0) mbar_arrive(&raw_empty[0]);
-                // the dot slice of block 0 on its way
-                ok = warp_wait(&fullt[0], 0, abort_flag);
+                // the dot slice of this warp's first block on its way
+                ok = warp_wait(&fullt[hf], 0, abort_flag);
                 tc_fence_after();
-                if (ok && act) tmem_ld16(tl + 16u, v);
+                if (ok && act) tmem_ld16(tl + (uint32_t)(hf * 64) + 16u, v);
             }
         }
         // Iteration (gc, jj) rescales block j = 8 gc + jj and converts block
         // j + 8 into the slot the MMA of block j has finished with.  The TMEM
-        // load of block j was issued at the end of the iteration before, and
-        // the store of block j + 8 completes while block j is rescaled.
+        // load of block j was issued at the end of this warp's iteration before,
+        // and the store of block j + 8 completes while block j is rescaled.
         // Chunk-level positions advance by counters (no divisions in the loop):
         // st / c = super-tile and chunk inside it of gc; sn / pn = stage and
         // its phase parity of chunk gn; x3 = gc mod 3.
@@ -448,17 +464,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint8_t* nib = spn + rs * 128;
             const int r7 = rs & 7;
 #pragma unroll
-            for (int jj = 0; jj < KB; ++jj) {
+            for (int jj = hf; jj < KB; jj += 2) {
                 // chunk gn's B buffer held chunk gc - 1, whose MMAs are complete
                 // (the commit waited for before this block's load covers every earlier MMA)
-                if (jj == 0 && has_next) stage_b(gn);
+                if (jj == 0 && has_next && warp < KB) stage_b(gn);
                 if (actn) {
                     const uint4 w = lds128(nib + ((jj ^ r7) << 4));
                     uint32_t av[16];
                     weights_f16(w, av);
                     tmem_st16(tl + (uint32_t)(jj * 64), av);
                 }
-                if (jj == KB - 1 && actn) sc_next = lds128(spn + H * 128 + rs * 16);
+                if (jj + 2 >= KB && actn) sc_next = lds128(spn + H * 128 + rs * 16);
                 if (act) {
                     tmem_wait_ld_regs(v);
                     const uint32_t sw = jj < 2 ? sc_cur.x : jj < 4 ? sc_cur.y : jj < 6 ? sc_cur.z : sc_cur.w;
@@ -482,13 +498,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0 && has_next) {
                     mbar_arrive(&ready[jj]);
-                    if (jj == KB - 1) mbar_arrive(&raw_empty[sn]);
+                    if (jj + 2 >= KB) mbar_arrive(&raw_empty[sn]);
                 }
-                // the next block's dot slice: (gc, jj + 1), or block 0 of chunk gn
-                if (jj < KB - 1 || has_next) {
-                    if (!(ok = warp_wait(&fullt[(jj + 1) % KB], (jj == KB - 1 ? gn : gc) & 1, abort_flag))) break;
+                // this warp's next block's dot slice: (gc, jj + 2), or its first of chunk gn
+                const bool wrap = jj + 2 >= KB;
+                if (!wrap || has_next) {
+                    const int jn = wrap ? hf : jj + 2;
+                    if (!(ok = warp_wait(&fullt[jn], (wrap ? gn : gc) & 1, abort_flag))) break;
                     tc_fence_after();
-                    if (jj == KB - 1 ? actn : act) tmem_ld16(tl + (uint32_t)(((jj + 1) % KB) * 64 + 16), v);
+                    if (wrap ? actn : act) tmem_ld16(tl + (uint32_t)(jn * 64 + 16), v);
                 }
             }
             if (!ok) break;
@@ -499,13 +517,32 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             x3 = x3 == 2 ? 0 : x3 + 1;
             if (++c == nch) {
-                // end of the super-tile: write its rows, restart the sums
-                const int64_t row = row_cta + (int64_t)st * H + rl;
-                if (act && rl < H && row < a.N) {
+                // end of the super-tile: the odd-block warp of each row slice hands
+                // its sums to the even-block warp (warp - 8), which writes the rows
+                const int pair = warp & 7;
+                if (hf == 1) {
+                    if (st > 0 && !(ok = warp_wait(&red_empty[pair], (st - 1) & 1, abort_flag))) break;
+#pragma unroll
+                    for (int t = 0; t < NTOK / 2; ++t) reinterpret_cast<float2*>(red)[t] = acc[t];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&red_full[pair]);
+                } else {
+                    if (!(ok = warp_wait(&red_full[pair], st & 1, abort_flag))) break;
+                    const int64_t row = row_cta + (int64_t)st * H + rl;
 #pragma unroll
                     for (int t = 0; t < NTOK / 2; ++t) {
-                        if (2 * t < a.M) a.y[(int64_t)(2 * t) * a.ldy + row] = acc[t].x;
-                        if (2 * t + 1 < a.M) a.y[(int64_t)(2 * t + 1) * a.ldy + row] = acc[t].y;
+                        const float2 o = reinterpret_cast<const float2*>(red)[t];
+                        acc[t].x += o.x;
+                        acc[t].y += o.y;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&red_empty[pair]);
+                    if (act && rl < H && row < a.N) {
+#pragma unroll
+                        for (int t = 0; t < NTOK / 2; ++t) {
+                            if (2 * t < a.M) a.y[(int64_t)(2 * t) * a.ldy + row] = acc[t].x;
+                            if (2 * t + 1 < a.M) a.y[(int64_t)(2 * t + 1) * a.ldy + row] = acc[t].y;
+                        }
                     }
                 }
 #pragma unroll
@@ -582,14 +619,15 @@ qmm_status gemm_tmem_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N,
     a.H = H;
     a.nst = nst;
     a.stage_bytes = (H * 144 + XQ_BYTES + XD_BYTES + 1023) / 1024 * 1024;
-    const int fixed = 2 * BBUF + 3 * SXB + 1024 + 1024;  // B buffers, d_x, barriers, alignment slack
+    const int fixed = 2 * BBUF + 3 * SXB + RED_BYTES + 1024 + 1024;  // B buffers, d_x, sums, barriers, slack
     const int64_t chunks = (int64_t)nst * (K / (QK * KB));
     const int64_t ns = std::min<int64_t>({(int64_t)MAX_STAGES, (smem_optin - fixed) / a.stage_bytes, chunks});
     if (ns < 1 || grid > 0x7fffffff) return QMM_ERR_SHAPE;
     a.nstages = (int)ns;
     a.off_bbuf = (int)ns * a.stage_bytes;
     a.off_sx = a.off_bbuf + 2 * BBUF;
-    a.off_bar = a.off_sx + 3 * SXB;
+    a.off_red = a.off_sx + 3 * SXB;
+    a.off_bar = a.off_red + RED_BYTES;
     a.err = err;
     const int smem = a.off_bar + 1024 + 1024;
     CUtensorMap mq, md, mxq, mxd;
