@@ -491,16 +491,19 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
         // 2..4 tokens: the batch-1 GEMV's streaming path (its row-kernel
         // fallback where the activation tile does not fit), where it measured
         // faster than warp MMA (x = stream / MMA, us): 2 tokens on every
-        // shape (28672x8192 23.2/43.9, 8192x28672 36.0/48.6 on the fallback, 2048x5632
-        // 6.0/8.0, 2560x2048 4.0/5.0, 5632x2048 5.7/5.7); 3-4 tokens when
-        // N <= 4096 or K >= 8192 and the activation tile fits (2048x5632
-        // 7.0/8.1, 2560x2048 4.4/4.9, 28672x8192 41.7/44.7; but 5632x2048
-        // 6.4/5.6).  From 8 tokens warp MMA wins everywhere.
+        // shape (28672x8192 23.2/31.9 against the 16-warp layout, 8192x28672
+        // 36.0/48.6 on the fallback, 2048x5632 6.0/8.0, 2560x2048 4.0/5.0,
+        // 5632x2048 5.7/5.7); 3-4 tokens when N <= 4096 or K >= 8192, the
+        // activation tile fits and the 16-warp layout does not apply
+        // (2048x5632 7.0/8.1, 2560x2048 4.4/4.9; but 5632x2048 6.4/5.6, and
+        // 28672x8192 41.7 against 31.9 for the 16-warp layout).  From 8
+        // tokens warp MMA wins everywhere.
+        const bool wide = pick != QMM_GEMM_KERNEL_MMA_GROUPS && gemm_wide_planned(N, M, xd, di->sms);
         const bool prefer_stream =
             pick == QMM_GEMM_KERNEL_AUTO &&
-            (M == 2 || (M <= 4 && (N <= 4096 || K >= 8192) && stream_eligible(N, K, w_qs, w_d, 4)));
+            (M == 2 || (M <= 4 && !wide && (N <= 4096 || K >= 8192) && stream_eligible(N, K, w_qs, w_d, 4)));
         if (pick != QMM_GEMM_KERNEL_STREAM && !prefer_stream && gemm_mma_eligible(N, K, M, w_qs, w_d, xq, xd))
-            return gemm_mma_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->sms, di->smem_optin, di->err, st);
+            return gemm_mma_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, di->sms, di->smem_optin, di->err, st, wide);
     }
     const int mt = M == 1 ? 1 : M == 2 ? 2 : M <= 4 ? 4 : 8;
     const bool streamable = stream_eligible(N, K, w_qs, w_d, mt);
@@ -589,7 +592,7 @@ qmm_status qmm_gemv_fused_op(const qmm_gemv_op* op, int flags, void* stream) {
 }
 
 qmm_status qmm_debug_gemm_kernel(int kernel, int* previous) {
-    if (kernel < QMM_GEMM_KERNEL_AUTO || kernel > QMM_GEMM_KERNEL_STREAM) return QMM_ERR_ARG;
+    if (kernel < QMM_GEMM_KERNEL_AUTO || kernel > QMM_GEMM_KERNEL_MMA_GROUPS) return QMM_ERR_ARG;
     const int old = g_gemm_kernel.exchange(kernel);
     if (previous) *previous = old;
     return QMM_OK;

@@ -558,7 +558,520 @@ qmm_status launch_nt(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_
     return launch_shape<NT, 1>(w_qs, w_d, N, K, M, xq, xd, y, ldy, r16, smem_optin, err, st);
 }
 
+
+// ================================================================ wide variant
+// The same arithmetic for up to 16 tokens, laid out for more warps and less
+// repeated work per weight byte:
+//  - 16 warps (4 per SM sub-partition, up to 128 registers each) instead of
+//    8 consumers + a producer, so that the fixed-latency chains of one warp
+//    (fragment load -> conversion -> two dependent MMAs -> rescale) are
+//    hidden by the others;
+//  - a unit is ALL rows of the CTA (RPC = 16 KPB WT rows) x 16 blocks, so the
+//    activation fragments of a unit are built once per CTA instead of once
+//    per row group;
+//  - warp (rh, kp) takes row tiles rh WT .. rh WT + WT - 1 and the KPB
+//    contiguous blocks kp KPB .. of every unit (KPB x 16 / KPB = 16 warps);
+//  - one ring stage holds everything a unit reads: the nibble and scale
+//    tiles of the rows and the Q8_0 codes and scales of the tokens, all by
+//    TMA, S - 1 units ahead, so no load of the loop waits on L2 or HBM;
+//  - weight fragments come from ldmatrix: one x4 load gives a lane its word
+//    of rows g and g + 8 for two blocks, in place of four 32-bit loads;
+//  - the nibbles enter the MMA as fp16 subnormals: the masked bit pattern u
+//    (or 16 v) of each half word IS the fp16 value u * 2^-24 (16 v * 2^-24),
+//    so a fragment register is one AND of the word (no second constant to
+//    merge in); every product and block sum is that of the integer codes
+//    times 2^-24, exact in fp32, and the 2^24 is folded into the staged d_x
+//    (a power of two: the rescaled fp32 result is unchanged, bit for bit);
+//  - the fp16 activation fragments of unit u + 1 are built from the stage
+//    (warp w: block w of the unit, lane = (token, half block)) while unit u
+//    is computed, handed over through mbarriers (two buffers);
+//  - no producer warp: the hand-over keeps every warp within one unit of
+//    the others, so once the last warp has finished unit u - 1 its stage is
+//    free, and lane 0 of warp 0 refills it with unit u - 1 + S.
+namespace widek {
+
+constexpr int CW = 16;
+constexpr int THREADS = CW * 32;
+constexpr int UKB = 16;  // blocks per unit: two 8-block nibble columns
+constexpr int MAX_STAGES = 8;
+
+template <int NT, int WT, int KPB>
+struct Shape {
+    static constexpr int KP = UKB / KPB;  // warps splitting a unit's blocks
+    static constexpr int RH = CW / KP;    // warps splitting the rows (= KPB)
+    static constexpr int RPC = 16 * RH * WT;
+    static constexpr int TK = 8 * NT;  // token rows of a launch
+    // stage: nibble columns [2][RPC][128] (128-byte swizzled) | weight scales
+    // [RPC][16] fp16 (32-byte swizzled) | codes [4][TK][128] (4 blocks per
+    // 128-byte box, 128-byte swizzled) | activation scales [TK][16] fp16
+    static constexpr int QB = 2 * RPC * 128;
+    static constexpr int OFF_XQ = QB + RPC * UKB * 2;
+    static constexpr int OFF_XD = OFF_XQ + 4 * TK * 128;
+    static constexpr int STAGE = (OFF_XD + TK * UKB * 2 + 1023) / 1024 * 1024;
+    static constexpr int XBUF = UKB * NT * 512;  // fp16 B fragments of a unit
+    static constexpr int XSC = UKB * NT * 64;    // per token pair: seeds (even, odd), 2^24 d_x (even, odd)
+    static constexpr int RED = RH * (KP - 1) * WT * NT * 512;  // partial sums, aliased on the ring
+    static constexpr int ITEMS = UKB * TK * 2;                  // (block, token, half) staging items
+    static_assert(RH * KP == CW && KPB % 2 == 0 && ITEMS % 32 == 0 && ITEMS <= THREADS, "warp split");
+    static_assert(OFF_XQ % 1024 == 0 && (TK * 128) % 1024 == 0, "swizzled boxes start on 1024 bytes");
+};
+
+struct Args {
+    int64_t N, K, M, ldy;
+    float* y;
+    int nstages;
+    int off_xbuf, off_xsc;  // from the 1024-aligned base; the ring starts at 1024
+    int* err;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// 2D tile copy that stays in L2 (the activation codes: every CTA reads them).
+__device__ __forceinline__ void tma2d_keep(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3D tile copies (the nibble columns of a unit in one box, the code boxes
+// of a unit in one box): weights evicted first, activation codes kept.
+__device__ __forceinline__ void tma3d_ef(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma3d_keep(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// One word of a weight row -> the four fragment registers of the encoding
+// above: (u_0, u_2), (u_1, u_3), (16 v_0, 16 v_2), (16 v_1, 16 v_3) as fp16
+// bit patterns, u / v the low / high nibbles of bytes 0..3 (codes q + 8).
+__device__ __forceinline__ void nibbles_sub(uint32_t w, uint32_t (&o)[4]) {
+    const uint32_t w8 = w >> 8;
+    o[0] = w & 0x000F000Fu;
+    o[1] = w8 & 0x000F000Fu;
+    o[2] = w & 0x00F000F0u;
+    o[3] = w8 & 0x00F000F0u;
+}
+
+// Every wait is bounded; a plain try_wait lets the hardware hold the warp
+// until the phase completes (or its own short limit passes).
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort || global_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+    return true;
+}
+
+template <int NT, int WT, int KPB>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_d,
+                     const __grid_constant__ CUtensorMap map_xq, const __grid_constant__ CUtensorMap map_xd, Args a) {
+    using SH = Shape<NT, WT, KPB>;
+    constexpr int KP = SH::KP, RPC = SH::RPC, QB = SH::QB, TK = SH::TK;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(base);  // [MAX_STAGES] TMA bytes of a stage
+    uint64_t* xfull = full + MAX_STAGES;                  // [2] fragments of a unit built (16 warps)
+    uint64_t* xempty = xfull + 2;                         // [2] unit computed (16 warps)
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(xempty + 2);
+    uint8_t* ring = base + 1024;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = (int)(a.K / QK);
+    const int S = a.nstages;  // >= 2
+    const int64_t row_begin = (int64_t)blockIdx.x * RPC;
+    const int nunits = (B + UKB - 1) / UKB;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&xfull[b], CW);
+            mbar_init(&xempty[b], CW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // The four copies of unit u into stage u % S (nibble columns, weight
+    // scales, activation codes, activation scales), one each by lane 0 of
+    // warps 0..3, in parallel (one thread issuing all of them serialises
+    // their issue cost on the path every warp waits for).  Warp 0 announces
+    // the unit's bytes; a copy may land before that (the barrier's byte
+    // count may go negative, and its phase cannot complete before warp 0
+    // arrives).  Boxes past K (a last half unit) or past the rows are
+    // zero-filled and count in full.  The activations come from the kernel
+    // before: only the first unit's weight copies go out before that wait.
+    const bool issuer = lane == 0 && warp < 4;
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int u, bool weights, bool acts) {
+        const int s = u % S, b0 = u * UKB;
+        uint8_t* st = ring + (size_t)s * SH::STAGE;
+        if (warp == 0 && weights) {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * RPC * 128 + RPC * UKB * 2 + 4 * TK * 128 + TK * UKB * 2));
+            tma3d_ef(st, &map_q, 0, (int)row_begin, b0 / 8, &full[s], pol);
+        } else if (warp == 1 && weights) {
+            tma2d(st + QB, &map_d, b0, (int)row_begin, &full[s], pol);
+        } else if (warp == 2 && acts) {
+            tma3d_keep(st + SH::OFF_XQ, &map_xq, 0, (int)blockIdx.y * TK, b0 / 4, &full[s]);
+        } else if (warp == 3 && acts) {
+            tma2d_keep(st + SH::OFF_XD, &map_xd, b0, (int)blockIdx.y * TK, &full[s]);
+        }
+    };
+    int issued = min(S, nunits);
+    if (issuer && nunits > 0) issue(0, true, false);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (issuer && nunits > 0) {
+        issue(0, false, true);
+        for (int u = 1; u < issued; ++u) issue(u, true, true);
+    }
+
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int kp = warp % KP, rh = warp / KP;
+    const int fb = kp * KPB, kb = fb >> 3, c0 = fb & 7;  // first block of the warp; its column, slot in it
+    const int64_t m0 = (int64_t)blockIdx.y * TK;
+    uint8_t* xbuf = base + a.off_xbuf;
+    float4* xsc = reinterpret_cast<float4*>(base + a.off_xsc);
+    constexpr int XSC_N = SH::XSC / 16;
+
+    // staging item of this thread: block sb of the unit, token st_tok, half block sh
+    const bool stager = warp * 32 < SH::ITEMS;  // warp-uniform
+    const int sh = lane & 1, st_tok = (lane >> 1) & (TK - 1), sb = (warp * 32 + lane) / (2 * TK);
+    // its 16 code bytes in a stage: box sb / 4, row st_tok, 16-byte chunk
+    // (2 (sb % 4) + sh) ^ (st_tok % 8) of the 128-byte swizzle
+    const int xq_off = SH::OFF_XQ + (sb >> 2) * TK * 128 + st_tok * 128 + ((((sb & 3) * 2 + sh) ^ (st_tok & 7)) << 4);
+    const int xd_off = SH::OFF_XD + (st_tok * UKB + sb) * 2;
+    const uint32_t x_mul = sh ? 0x2C002C00u : 0x3C003C00u;  // 1/16 or 1
+    const uint32_t x_add = sh ? 0xD480D480u : 0xE480E480u;  // -72 or -1152
+    // Unit u's fp16 B fragments and (seed, d_x) pairs into buffer buf.
+    auto stage_x = [&](int u, int buf) {
+        const uint8_t* st = ring + (size_t)(u % S) * SH::STAGE;
+        const uint4 px = lds128(st + xq_off);
+        int sum = __dp4a((int)px.x, 0x01010101, 0);
+        sum = __dp4a((int)px.y, 0x01010101, sum);
+        sum = __dp4a((int)px.z, 0x01010101, sum);
+        sum = __dp4a((int)px.w, 0x01010101, sum);
+        const int other = __shfl_xor_sync(FULL, sum, 1);
+        // lane (g, t) of token tile j = tok / 8 holds word t of token g = tok % 8,
+        // in chunk (t + g / 2) mod 4 of the token's 64 bytes; this thread writes
+        // the low or high 8 bytes of each chunk
+        uint8_t* dst = xbuf + buf * SH::XBUF + (sb * NT * 32 + st_tok * 4) * 16 + sh * 8;
+        const int rot = (st_tok >> 1) & 3;
+        const uint32_t w4[4] = {px.x, px.y, px.z, px.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            // (1152 + x) * mul + add = x (low half) or x / 16 (high half), exact
+            uint2 p;
+            p.x = hfma2((w4[t] & 0x00FF00FFu) ^ 0x64806480u, x_mul, x_add);
+            p.y = hfma2(((w4[t] >> 8) & 0x00FF00FFu) ^ 0x64806480u, x_mul, x_add);
+            *reinterpret_cast<uint2*>(dst + ((rot + t) & 3) * 16) = p;
+        }
+        if (sh == 0) {
+            float* xs = reinterpret_cast<float*>(xsc + buf * XSC_N);
+            const int pr = (sb * TK + st_tok) >> 1, od = st_tok & 1;
+            // MMA seed: the products carry 2^-24 and the codes u = q + 8, so
+            // -8 * 2^-24 * (sum of the block's codes) leaves 2^-24 * sum q x
+            xs[pr * 4 + od] = (float)(-8 * (sum + other)) * 0x1p-24f;
+            xs[pr * 4 + 2 + od] = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(st + xd_off)) * 0x1p24f;
+        }
+    };
+    // B fragment slot of this lane (the rotation above, read back)
+    const int fslot = (lane & ~3) | (((lane & 3) + (lane >> 3)) & 3);
+
+    float2 acc[WT][NT][2];
+#pragma unroll
+    for (int i = 0; i < WT; ++i)
+#pragma unroll
+        for (int j = 0; j < NT; ++j) acc[i][j][0] = acc[i][j][1] = make_float2(0.f, 0.f);
+    // scale-tile offsets (fp16 units) of this lane's rows: the tile is
+    // [RPC][16] fp16, 32-byte swizzled (16-byte chunk ^= (row >> 2) & 1)
+    int doff[WT][2];
+    // ldmatrix row addresses: lane l gives row l % 8 of matrix l / 8 = (row
+    // half hr, block of the pair bsel); both stay fixed, only the tile moves
+    uint32_t qaddr[WT];
+    {
+        const int hr = (lane >> 3) & 1, bsel = lane >> 4, rr = lane & 7;
+#pragma unroll
+        for (int i = 0; i < WT; ++i) {
+            const int rt = (rh * WT + i) * 16;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = rt + g8 + 8 * h;
+                doff[i][h] = r * UKB + (((kb ^ ((r >> 2) & 1)) << 3) | c0);
+            }
+            const int r = rt + 8 * hr + rr;
+            qaddr[i] = (uint32_t)(kb * RPC * 128 + r * 128 + (((c0 + bsel) ^ rr) << 4));
+        }
+    }
+    bool failed = false;
+    auto fail = [&]() {
+        if (!failed) {
+            if (lane == 0) atomicOr(a.err, ERR_TIMEOUT);
+            *abort_flag = 1;
+            failed = true;
+        }
+    };
+
+    // prologue: unit 0's fragments built
+    if (nunits > 0) {
+        if (!wait_phase(&full[0], 0, abort_flag)) fail();
+        if (stager && !failed) stage_x(0, 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xfull[0]);
+    }
+    for (int u = 0; u < nunits; ++u) {
+        const int s = u % S, buf = u & 1;
+        // every warp has finished unit u - 1: its stage may be refilled and
+        // its fragment buffer (buf ^ 1) overwritten
+        if (u >= 1 && !failed && !wait_phase(&xempty[buf ^ 1], ((u - 1) >> 1) & 1, abort_flag)) fail();
+        if (u >= 1 && issued < nunits && !failed) {
+            if (issuer) issue(issued, true, true);
+            ++issued;
+        }
+        // unit u: its stage was waited for before its fragments were built
+        if (!failed && !wait_phase(&xfull[buf], (u >> 1) & 1, abort_flag)) fail();
+        const int nb = min(UKB, B - u * UKB);
+        const bool work = !failed && fb < nb;
+        const uint8_t* st = ring + (size_t)s * SH::STAGE;
+        const uint32_t st_u32 = smem_u32(st);
+        const uint8_t* xf0 = xbuf + buf * SH::XBUF + fslot * 16;
+        const float4* xs0 = xsc + buf * XSC_N + t4;
+        // the weight scales of this lane's rows for the warp's KPB blocks
+        uint32_t dq[WT][2][KPB / 2];
+        if (work) {
+            const uint16_t* sd = reinterpret_cast<const uint16_t*>(st + QB);
+#pragma unroll
+            for (int i = 0; i < WT; ++i)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if constexpr (KPB == 4) {
+                        const uint2 v = *reinterpret_cast<const uint2*>(sd + doff[i][h]);
+                        dq[i][h][0] = v.x;
+                        dq[i][h][1] = v.y;
+                    } else {
+                        dq[i][h][0] = *reinterpret_cast<const uint32_t*>(sd + doff[i][h]);
+                    }
+                }
+        }
+        // blocks fb + 2 bp and fb + 2 bp + 1 of unit u against all row tiles
+        auto compute_pair = [&](int bp) {
+            // the word of rows g and g + 8 of each row tile for both blocks
+            uint32_t wq[WT][4];
+#pragma unroll
+            for (int i = 0; i < WT; ++i) ldsm_x4(st_u32 + (qaddr[i] ^ (uint32_t)(bp << 5)), wq[i]);
+#pragma unroll
+            for (int bs = 0; bs < 2; ++bs) {
+                const int b = fb + 2 * bp + bs;  // block inside the unit
+                const uint8_t* xf = xf0 + b * NT * 512;
+                const float4* xs = xs0 + b * NT * 4;
+                uint4 f[NT];
+                float4 cs[NT];
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    f[j] = *reinterpret_cast<const uint4*>(xf + j * 512);
+                    cs[j] = xs[j * 4];
+                }
+#pragma unroll
+                for (int i = 0; i < WT; ++i) {
+                    uint32_t q0[4], q1[4];
+                    nibbles_sub(wq[i][2 * bs], q0);
+                    nibbles_sub(wq[i][2 * bs + 1], q1);
+                    const uint32_t a0[4] = {q0[0], q1[0], q0[1], q1[1]};
+                    const uint32_t a1[4] = {q0[2], q1[2], q0[3], q1[3]};
+                    float dw[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) dw[h] = f16_bits_to_f32((unsigned short)(dq[i][h][bp] >> (16 * bs)));
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const float c4[4] = {cs[j].x, cs[j].y, cs[j].x, cs[j].y};
+                        const float2 sx = make_float2(cs[j].z, cs[j].w);
+                        float dd[4];
+                        mma16816(dd, a0, f[j].x, f[j].y, c4);
+                        mma16816(dd, a1, f[j].z, f[j].w, dd);  // 2^-24 x the integer block dots
+                        acc[i][j][0] =
+                            ffma2_scaled(make_float2(dw[0], dw[0]), sx, make_float2(dd[0], dd[1]), acc[i][j][0]);
+                        acc[i][j][1] =
+                            ffma2_scaled(make_float2(dw[1], dw[1]), sx, make_float2(dd[2], dd[3]), acc[i][j][1]);
+                    }
+                }
+            }
+        };
+        if (work) compute_pair(0);
+        // unit u + 1's fragments, between the two halves of unit u's work so
+        // that their latency hides behind it
+        if (u + 1 < nunits) {
+            if (!failed && !wait_phase(&full[(u + 1) % S], ((u + 1) / S) & 1, abort_flag)) fail();
+            if (stager && !failed) stage_x(u + 1, buf ^ 1);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xfull[buf ^ 1]);
+        }
+        if constexpr (KPB == 4) {
+            if (work) compute_pair(1);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xempty[buf]);  // unit read: its stage and fragments may be reused
+    }
+    if (failed && tid == 0) {  // copies still in flight land before the ring is reused or the CTA exits
+        for (int u = max(0, issued - S); u < issued; ++u) {
+            const uint64_t t0 = global_ns();
+            while (!mbar_try_wait(&full[u % S], (u / S) & 1) && global_ns() - t0 < WAIT_LIMIT_NS) {
+            }
+        }
+    }
+
+    // ---------------- the KP warps of each row set add their sums; kp 0 writes y.
+    // The partial sums go to the ring, which every warp has finished reading
+    // and no copy fills any more (each was waited for).
+    __syncthreads();
+    constexpr int SLOT = WT * NT * 128;  // floats per warp
+    float* red = reinterpret_cast<float*>(ring);
+    if (kp > 0) {
+        float* rp = red + (rh * (KP - 1) + kp - 1) * SLOT + lane;
+#pragma unroll
+        for (int i = 0; i < WT; ++i)
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                float* q = rp + (i * NT + j) * 128;
+                q[0] = acc[i][j][0].x;
+                q[32] = acc[i][j][0].y;
+                q[64] = acc[i][j][1].x;
+                q[96] = acc[i][j][1].y;
+            }
+    }
+    __syncthreads();
+    if (kp == 0 && !failed) {
+#pragma unroll 1
+        for (int p = 1; p < KP; ++p) {
+            const float* rp = red + (rh * (KP - 1) + p - 1) * SLOT + lane;
+#pragma unroll
+            for (int i = 0; i < WT; ++i)
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const float* q = rp + (i * NT + j) * 128;
+                    acc[i][j][0].x += q[0];
+                    acc[i][j][0].y += q[32];
+                    acc[i][j][1].x += q[64];
+                    acc[i][j][1].y += q[96];
+                }
+        }
+#pragma unroll
+        for (int i = 0; i < WT; ++i)
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int64_t m = m0 + 8 * j + 2 * t4;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t row = row_begin + (rh * WT + i) * 16 + g8 + 8 * h;
+                    if (row >= a.N) continue;
+                    if (m < a.M) a.y[m * a.ldy + row] = acc[i][j][h].x;
+                    if (m + 1 < a.M) a.y[(m + 1) * a.ldy + row] = acc[i][j][h].y;
+                }
+            }
+    }
+}
+
+template <int NT, int WT, int KPB>
+qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, const int8_t* xq,
+                  const uint16_t* xd, float* y, int64_t ldy, int smem_optin, int* err, cudaStream_t st) {
+    using SH = Shape<NT, WT, KPB>;
+    const int64_t B = K / QK;
+    const int64_t nunits = (B + UKB - 1) / UKB;
+    const int fixed = 1024 + 2 * SH::XBUF + 2 * SH::XSC + 1024;  // barriers, buffers, alignment slack
+    const int64_t nst = std::min<int64_t>({(int64_t)MAX_STAGES, (smem_optin - fixed) / SH::STAGE, nunits + 1});
+    if (nst < 2) return QMM_ERR_SHAPE;
+    // the ring also holds the final partial sums
+    const int64_t ring = std::max<int64_t>(nst * SH::STAGE, SH::RED);
+    Args a = {};
+    a.N = N;
+    a.K = K;
+    a.M = M;
+    a.ldy = ldy;
+    a.y = y;
+    a.nstages = (int)nst;
+    a.off_xbuf = 1024 + (int)ring;
+    a.off_xsc = a.off_xbuf + 2 * SH::XBUF;
+    a.err = err;
+    const int64_t smem = a.off_xsc + 2 * SH::XSC + 1024;
+    if (smem > smem_optin) return QMM_ERR_SHAPE;
+    CUtensorMap mq, md, mxq, mxd;
+    // nibbles as [K / 256 chunks of 128 bytes][N rows][128]: one box = the
+    // unit's two columns; codes as [K / 128][M][128]: one box = its 4 blocks
+    // of 4 (each a 128-byte row per token)
+    const uint64_t dq3[3] = {128, (uint64_t)N, (uint64_t)K / 256}, sq3[2] = {(uint64_t)K / 2, 128};
+    const uint32_t bq3[3] = {128, (uint32_t)SH::RPC, 2};
+    const uint64_t dx3[3] = {128, (uint64_t)M, (uint64_t)K / 128}, sx3[2] = {(uint64_t)K, 128};
+    const uint32_t bx3[3] = {128, (uint32_t)SH::TK, 4};
+    if (!make_tensor_map_3d(&mq, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_qs, dq3, sq3, bq3, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT16, w_d, (uint64_t)B, (uint64_t)N, (uint64_t)B * 2,
+                            (uint32_t)UKB, (uint32_t)SH::RPC, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_tensor_map_3d(&mxq, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, dx3, sx3, bx3, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_2d(&mxd, CU_TENSOR_MAP_DATA_TYPE_UINT16, xd, (uint64_t)B, (uint64_t)M, (uint64_t)B * 2,
+                            (uint32_t)UKB, (uint32_t)SH::TK, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return QMM_ERR_CUDA;
+    auto kern = gemm_wide_kernel<NT, WT, KPB>;
+    if (!allow_smem(kern, smem_optin)) return QMM_ERR_SHAPE;
+    const dim3 grid((unsigned)((N + SH::RPC - 1) / SH::RPC), (unsigned)((M + SH::TK - 1) / SH::TK));
+    kern<<<grid, THREADS, (int)smem, st>>>(mq, md, mxq, mxd, a);
+    return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+}
+
+// Rows per CTA at one CTA per SM: the wide layout takes 32- or 64-row
+// granules; it is used when that costs no more CTA rows than the 16-row
+// granule of the group kernel (within 8%) and gives each warp two or three
+// row tiles: 96, 128 or 192 rows per CTA.  With one row tile per warp the
+// per-unit hand-over and staging cost more than the 16 warps save (measured:
+// 8192 x 28672 at 16 tokens 91 us against 69 us, 4096 x 14336 40 against 28),
+// and 256 rows leave room for two stages only.  Its TMA copies of the
+// activation scales want them 16-byte aligned.  Returns false (nothing
+// launched) where the plan does not qualify.
+// Rows per CTA of the wide plan (96, 128 or 192), or 0 where it does not qualify.
+int plan_rows(int64_t N, int sms) {
+    const int64_t need = (N + sms - 1) / sms;
+    const int64_t r16 = round_up(need, 16);
+    const auto ok = [&](int64_t g) { return round_up(need, g) * 100 <= r16 * 108; };
+    if (need > 64 && need <= 192 && ok(64)) return need <= 128 ? 128 : 192;
+    if (need > 64 && need <= 96 && ok(32)) return 96;  // three 32-row sets
+    return 0;
+}
+
+template <int NT>
+bool plan_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, const int8_t* xq,
+                 const uint16_t* xd, float* y, int64_t ldy, int sms, int smem_optin, int* err, cudaStream_t st,
+                 qmm_status* out) {
+    if (reinterpret_cast<uintptr_t>(xd) % 16 != 0) return false;
+    switch (plan_rows(N, sms)) {
+        case 128: *out = launch<NT, 2, 4>(w_qs, w_d, N, K, M, xq, xd, y, ldy, smem_optin, err, st); return true;
+        case 192: *out = launch<NT, 3, 4>(w_qs, w_d, N, K, M, xq, xd, y, ldy, smem_optin, err, st); return true;
+        case 96: *out = launch<NT, 3, 2>(w_qs, w_d, N, K, M, xq, xd, y, ldy, smem_optin, err, st); return true;
+        default: return false;
+    }
+}
+
+}  // namespace widek
+
 }  // namespace mmak
+
+bool gemm_wide_planned(int64_t N, int64_t M, const void* xd, int sms) {
+    return M >= 1 && M <= 16 && reinterpret_cast<uintptr_t>(xd) % 16 == 0 && mmak::widek::plan_rows(N, sms) > 0;
+}
 
 bool gemm_mma_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const void* w_d, const void* xq,
                        const void* xd) {
@@ -569,7 +1082,13 @@ bool gemm_mma_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const 
 
 qmm_status gemm_mma_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,
                            const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy, int sms, int smem_optin,
-                           int* err, cudaStream_t st) {
+                           int* err, cudaStream_t st, bool wide) {
+    qmm_status s = QMM_OK;
+    if (wide && M <= 8 && mmak::widek::plan_launch<1>(w_qs, w_d, N, K, M, xq, xd, y, ldy, sms, smem_optin, err, st, &s))
+        return s;
+    if (wide && M > 8 && M <= 16 &&
+        mmak::widek::plan_launch<2>(w_qs, w_d, N, K, M, xq, xd, y, ldy, sms, smem_optin, err, st, &s))
+        return s;
     if (M <= 8) return mmak::launch_nt<1>(w_qs, w_d, N, K, M, xq, xd, y, ldy, sms, smem_optin, err, st);
     if (M <= 16) return mmak::launch_nt<2>(w_qs, w_d, N, K, M, xq, xd, y, ldy, sms, smem_optin, err, st);
     if (M <= 32) return mmak::launch_nt<4>(w_qs, w_d, N, K, M, xq, xd, y, ldy, sms, smem_optin, err, st);

@@ -15,12 +15,19 @@ namespace qmm {
 bool gemm_mma_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const void* w_d, const void* xq,
                        const void* xd);
 
+// True when gemm_mma_launch (wide = true) takes the 16-warp layout for this
+// product: up to 16 tokens, xd 16-byte aligned, and a row plan of 96, 128 or
+// 192 rows per CTA at one CTA per SM (ceil(N / sms) in 65..192).
+bool gemm_wide_planned(int64_t N, int64_t M, const void* xd, int sms);
+
 // Enqueue y[m*ldy + n] (m < M, n < N) on `st`.  `sms` and `smem_optin` are
 // the device's SM count and opt-in shared memory per block; `err` is the
 // device error word (an expired bounded wait sets ERR_TIMEOUT in it).
+// `wide`: up to 16 tokens, take the 16-warp layout where its row plan
+// qualifies; otherwise (and when false) the row-group kernel.
 qmm_status gemm_mma_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,
                            const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy, int sms, int smem_optin,
-                           int* err, cudaStream_t st);
+                           int* err, cudaStream_t st, bool wide);
 
 }  // namespace qmm
 

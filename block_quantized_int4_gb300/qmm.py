@@ -180,7 +180,7 @@ def qmm_gemm_q4_0_q8_0(w_qs, w_d, N, K, M, xq, xd, y, ldy, stream=None):
                                    _stream(stream)), "qmm_gemm_q4_0_q8_0")
 
 
-GEMM_KERNEL_AUTO, GEMM_KERNEL_MMA, GEMM_KERNEL_TMEM, GEMM_KERNEL_STREAM = 0, 1, 2, 3
+GEMM_KERNEL_AUTO, GEMM_KERNEL_MMA, GEMM_KERNEL_TMEM, GEMM_KERNEL_STREAM, GEMM_KERNEL_MMA_GROUPS = 0, 1, 2, 3, 4
 
 
 def qmm_debug_gemm_kernel(kernel):

@@ -180,8 +180,12 @@ QMM_API qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, 
  * for testing and timing the kernels on the same inputs:
  *  - QMM_GEMM_KERNEL_AUTO (the default): the fastest measured: the
  *    streaming kernel for 2 tokens, and for 3-4 tokens when N <= 4096 or
- *    K >= 8192; otherwise the warp-MMA kernel;
- *  - QMM_GEMM_KERNEL_MMA: the warp-MMA kernel (mma.sync, any M);
+ *    K >= 8192 unless the 16-warp layout below applies; otherwise the
+ *    warp-MMA kernels;
+ *  - QMM_GEMM_KERNEL_MMA: the warp-MMA kernels (mma.sync, any M): up to 16
+ *    tokens the 16-warp layout where its row plan qualifies (ceil(N / SMs)
+ *    in 65..192 rows, xd 16-byte aligned), else the row-group kernel;
+ *  - QMM_GEMM_KERNEL_MMA_GROUPS: the warp-MMA row-group kernel alone;
  *  - QMM_GEMM_KERNEL_TMEM: the tcgen05 kernel with the weight operand in
  *    tensor memory (M <= 16, K % 256 == 0, all four operand planes 16-byte
  *    aligned; otherwise the GEMM returns QMM_ERR_SHAPE);
@@ -194,6 +198,7 @@ QMM_API qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, 
 #define QMM_GEMM_KERNEL_MMA 1
 #define QMM_GEMM_KERNEL_TMEM 2
 #define QMM_GEMM_KERNEL_STREAM 3
+#define QMM_GEMM_KERNEL_MMA_GROUPS 4
 QMM_API qmm_status qmm_debug_gemm_kernel(int kernel, int* previous);
 
 /* Test hook of the failure handling of the streaming GEMV kernel (the

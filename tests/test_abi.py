@@ -188,15 +188,16 @@ def test_valid_call_without_gpu_reports_device_error(qmm):
 
 
 def test_gemm_kernel_selector_and_moe_fp32_validation(qmm):
-    """qmm_debug_gemm_kernel accepts the four documented kernels, returns the
+    """qmm_debug_gemm_kernel accepts the five documented kernels, returns the
     previous choice and rejects others; the fp32-activation and gate/up MoE
     entries reject bad shapes, workspaces and alignment on the host."""
     prev = ctypes.c_int(-1)
     lib = qmm._lib
     assert lib.qmm_debug_gemm_kernel(3, ctypes.byref(prev)) == 0
     start = prev.value
-    assert lib.qmm_debug_gemm_kernel(2, ctypes.byref(prev)) == 0 and prev.value == 3
-    assert lib.qmm_debug_gemm_kernel(4, None) == 1
+    assert lib.qmm_debug_gemm_kernel(4, ctypes.byref(prev)) == 0 and prev.value == 3
+    assert lib.qmm_debug_gemm_kernel(2, ctypes.byref(prev)) == 0 and prev.value == 4
+    assert lib.qmm_debug_gemm_kernel(5, None) == 1
     assert lib.qmm_debug_gemm_kernel(-1, None) == 1
     assert lib.qmm_debug_gemm_kernel(start, ctypes.byref(prev)) == 0 and prev.value == 2
     A16 = 0x10000

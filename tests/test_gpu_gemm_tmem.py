@@ -133,7 +133,7 @@ def test_tmem_gemm_rejects_what_it_cannot_take(qmm):
     assert ei.value.status == 2
     assert torch.all(y == 7.0) and torch.all(y2 == 7.0)
     with pytest.raises(qmm.QmmError):
-        qmm.qmm_debug_gemm_kernel(4)
+        qmm.qmm_debug_gemm_kernel(5)
 
 
 @pytest.mark.parametrize("N,K,M", [(517, 2048, 2), (20000, 8192, 3), (300, 512, 5), (129, 256, 9)])

@@ -1,0 +1,130 @@
+"""The 16-warp layout of the warp-MMA small-batch GEMM (up to 16 tokens,
+taken where its row plan qualifies) against the oracle and against the
+row-group kernel on the same inputs.
+
+Shapes are chosen for the row plan on a 152-SM GB300 (rows per CTA =
+ceil(N / 152) rounded up to the 64-row granule, else the 32-row one): two or
+three 64-row sets per CTA and three 32-row sets, each with a short last CTA
+(and two shapes whose plans stay on the row-group kernel); K of half a unit (8 blocks), one and a half units, four units and
+many units (the stage ring wraps several times); 2..16 tokens with ragged
+token tiles.  fp32 outputs: |y - y_ref| <= 1e-5*S + 1e-6; with unit scales
+every output is an exact integer and must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from parity import lib, assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+# N -> (rows per CTA, granule) on 152 SMs: the three plans of the 16-warp
+# layout (two or three row tiles per warp), then two that stay on the
+# row-group kernel (one row tile per warp would be the wide plan)
+ROW_PLANS = {18000: (128, 64), 27000: (192, 64), 13000: (96, 32), 7400: (64, 64), 3000: (32, 32)}
+
+
+@pytest.fixture
+def qmm():
+    q = lib()
+    prev = q.qmm_debug_gemm_kernel(q.GEMM_KERNEL_MMA)  # 2..4 tokens too, not the streaming kernel
+    yield q
+    q.qmm_debug_gemm_kernel(prev)
+
+
+def _rand_codes(N, M, K, seed):
+    rng = np.random.default_rng(seed)
+    qw = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    dw = rng.integers(0x1000, 0x2C00, size=(N, K // 32)).astype(np.uint16)
+    qx = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    dx = rng.integers(0x1000, 0x3C00, size=(M, K // 32)).astype(np.uint16)
+    return qw, dw, qx, dx
+
+
+def _planes(q, qw, dw):
+    N, K = qw.shape
+    blocks = torch.from_numpy(O.pack_q4_0_blocks(qw, dw).reshape(-1).copy()).to(DEV)
+    qs, d = q.q4_0_planes(N, K)
+    q.qmm_repack_q4_0(blocks, N, K, qs, d)
+    return qs, d
+
+
+def _q8(qx, dx):
+    return torch.from_numpy(qx).to(DEV), torch.from_numpy(dx.view(np.int16)).to(DEV)
+
+
+def test_row_plans_are_the_intended_ones():
+    """The shapes below exercise the granules named in ROW_PLANS only on a
+    152-SM part; elsewhere they still run (other plans), so this is a note."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip(f"{sms} SMs: the row plans differ from the ones the shapes were chosen for")
+    for N, (rpc, g) in ROW_PLANS.items():
+        need = -(-N // sms)
+        assert -(-need // g) * g == rpc
+
+
+@pytest.mark.parametrize("N", sorted(ROW_PLANS))
+@pytest.mark.parametrize("K,M", [(256, 16), (768, 9), (2048, 2), (2048, 8), (2048, 13)])
+def test_wide_vs_oracle(qmm, N, K, M):
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + K + M)
+    qs, d = _planes(qmm, qw, dw)
+    xq, xd = _q8(qx, dx)
+    y = qmm.gemm(qs, d, xq, xd)
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y, ref, S, f"wide gemm {N}x{K} M={M}")
+    assert qmm.qmm_last_device_error() == 0
+
+
+@pytest.mark.parametrize("N,K,M", [(28672, 8192, 16), (8192, 28672, 16), (13000, 8192, 5)])
+def test_wide_large_k_sampled_rows(qmm, N, K, M):
+    """Full-size FFN products: about 1500 sampled rows (both ends included)
+    against the oracle and against the row-group kernel (same exact block
+    dots, fp32 sums in another order)."""
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + M)
+    qs, d = _planes(qmm, qw, dw)
+    xq, xd = _q8(qx, dx)
+    y = qmm.gemm(qs, d, xq, xd)
+    rng = np.random.default_rng(K)
+    rows = np.unique(np.concatenate([np.arange(64), np.arange(N - 64, N), rng.integers(0, N, 1372)]))
+    ref, S = O.matmul_int(qw, dw, qx, dx, rows=rows, nthreads=8)
+    assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, S, f"wide gemm {N}x{K} M={M} sampled")
+    qmm.qmm_debug_gemm_kernel(qmm.GEMM_KERNEL_MMA_GROUPS)
+    y2 = qmm.gemm(qs, d, xq, xd)
+    qmm.qmm_debug_gemm_kernel(qmm.GEMM_KERNEL_MMA)
+    sel = torch.from_numpy(rows).to(DEV)
+    diff = (y - y2).abs()[:, sel].double().cpu().numpy()
+    assert np.all(diff <= 2e-5 * S + 2e-6)
+    assert torch.isfinite(y).all() and qmm.qmm_last_device_error() == 0
+
+
+@pytest.mark.parametrize("N,K,M", [(27000, 8192, 16), (7400, 2048, 11), (13000, 768, 16)])
+def test_wide_integer_grid_exact(qmm, N, K, M):
+    """d = 1 on both sides, full-magnitude codes: every output is an exact
+    integer and must be equal (a wrong fragment, swizzle or block pairing
+    changes some of them)."""
+    rng = np.random.default_rng(N + M)
+    w = rng.integers(-7, 8, size=(N, K)).astype(np.float32)
+    w[:, ::32] = 7
+    x = rng.integers(-127, 128, size=(M, K)).astype(np.float32)
+    x[:, 5::32] = 127
+    qs, d = qmm.quantize_q4_0(torch.from_numpy(w).to(DEV))
+    xq, xd = qmm.quantize_q8_0(torch.from_numpy(x).to(DEV))
+    y = qmm.gemm(qs, d, xq, xd)
+    exact = (x.astype(np.float64) @ w.astype(np.float64).T).astype(np.float32)
+    assert np.array_equal(y.cpu().numpy(), exact)
+    assert qmm.qmm_last_device_error() == 0
+
+
+def test_wide_ldy(qmm):
+    """Output row stride > N: the columns past N stay untouched."""
+    N, K, M, ldy = 27000, 1024, 16, 27008
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=9)
+    qs, d = _planes(qmm, qw, dw)
+    xq, xd = _q8(qx, dx)
+    y = torch.full((M, ldy), 7.0, device=DEV)
+    qmm.qmm_gemm_q4_0_q8_0(qs, d, N, K, M, xq, xd, y, ldy)
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y[:, :N], ref, S, "wide ldy")
+    assert torch.all(y[:, N:] == 7.0)
