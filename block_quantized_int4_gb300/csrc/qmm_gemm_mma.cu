@@ -3,13 +3,14 @@
 // mma.sync m16n8k16 with fp16 operands and fp32 accumulation.
 //
 // Exact integer block dots on a float MMA: the weight codes q = u - 8 lie in
-// [-8, 7] and the activation codes in [-127, 127]; both are exact in fp16,
-// every product is exact, and a block's 32-term sum is an integer of
-// magnitude at most 32 * 8 * 127 = 32,512, exact in fp32.  So the MMA result
-// of one block is the integer dot of the method (llama.cpp guide,
-// kenji.blog/id, section 2.2: y ~ Delta * Delta_x * sum q * q_x), and the
-// rescale d_w * d_x * dot plus the sum over blocks are fp32 operations, as in
-// the GEMV kernels.
+// [-8, 7] and the activation codes in [-127, 127]; both are exact in fp16
+// (the weights as subnormals scaled by 2^-24, see the operand encodings
+// below), every product is exact, and a block's 32-term sum is an integer of
+// magnitude at most 32 * 8 * 127 = 32,512 (times 2^-24), exact in fp32.  So
+// the MMA result of one block is the integer dot of the method (llama.cpp
+// guide, kenji.blog/id, section 2.2: y ~ Delta * Delta_x * sum q * q_x) up to
+// a power of two, and the rescale d_w * d_x * dot plus the sum over blocks
+// are fp32 operations, as in the GEMV kernels.
 //
 // Why this instruction on sm_103a: tcgen05 has no integer MMA kind here, and
 // with 8..64 token columns a 128-row tcgen05 MMA is latency-bound, whereas
@@ -100,27 +101,30 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
     return r;
 }
 
-// Operand encodings (fp16 bit patterns: 0x6400 = 1024 with unit spacing, so
-// OR-ing a small integer n into the mantissa gives 1024 + n exactly; 0xE480 =
-// -1152, 0x2C00 = 1/16, 0xD480 = -72).
+// Operand encodings (fp16 bit patterns; 0xE480 = -1152, 0x2C00 = 1/16,
+// 0xD480 = -72).
 //
 // Weights: one word of a weight row (bytes 4t..4t+3 of a block, byte i =
 // u_i | v_i << 4 with u = element 4t+i, v = element 16+4t+i, codes stored as
-// q + 8) -> four fp16 pairs, with no arithmetic beyond masking:
-//   o[0] = 1024 + u for elements (4t, 4t+2), o[1] the same for (4t+1, 4t+3),
-//   o[2] = 1024 + 16 v for elements (16+4t, 16+4t+2), o[3] for (16+4t+1, ..+3).
+// q + 8) -> four fp16 pairs by masking alone, as fp16 subnormals: a half
+// word holding the bit pattern n is the fp16 value n * 2^-24, so
+//   o[0] = u * 2^-24 for elements (4t, 4t+2), o[1] the same for (4t+1, 4t+3),
+//   o[2] = 16 v * 2^-24 for elements (16+4t, 16+4t+2), o[3] for (16+4t+1, ..+3),
+// each one AND of the word with one constant.
 // Activations: the low half block as x itself, the high half as x / 16 (exact:
-// (1152 + x) / 16 - 72).  Then the low-half MMA sums (1024 + u) x = (q + 1032) x
-// and the high-half MMA sums (1024 + 16 v) x / 16 = (q + 72) x, so seeding the
-// accumulator with c = -(1032 * sum x_lo + 72 * sum x_hi) leaves exactly
-// sum q * x.  Every product and partial sum is an integer below 2^23 in
-// magnitude, exact in fp32.
-__device__ __forceinline__ void nibbles_to_f16(uint32_t w, uint32_t (&o)[4]) {
+// (1152 + x) / 16 - 72).  Then the low-half MMA sums 2^-24 u x = 2^-24 (q + 8) x
+// and the high-half MMA sums 2^-24 16 v x / 16 = 2^-24 (q + 8) x, so seeding
+// the accumulator with c = -8 * 2^-24 * (sum x_lo + sum x_hi) leaves exactly
+// 2^-24 * sum q * x: every product is an integer times 2^-24 and every
+// partial sum an integer below 2^23 in magnitude times 2^-24, exact in fp32.
+// The 2^24 goes into the staged activation scale (a power of two, so the
+// rescaled fp32 result is the same as with unscaled integers, bit for bit).
+__device__ __forceinline__ void nibbles_sub(uint32_t w, uint32_t (&o)[4]) {
     const uint32_t w8 = w >> 8;
-    o[0] = (w & 0x000F000Fu) ^ 0x64006400u;
-    o[1] = (w8 & 0x000F000Fu) ^ 0x64006400u;
-    o[2] = (w & 0x00F000F0u) ^ 0x64006400u;
-    o[3] = (w8 & 0x00F000F0u) ^ 0x64006400u;
+    o[0] = w & 0x000F000Fu;
+    o[1] = w8 & 0x000F000Fu;
+    o[2] = w & 0x00F000F0u;
+    o[3] = w8 & 0x00F000F0u;
 }
 
 // One word of activation codes (four int8 x0..x3) -> the B fragment pair
@@ -311,10 +315,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 l = codes_lo_f16(lo.w), h = codes_hi_f16(hi.w);
                 dst[(rot + 3) & 3] = make_uint4(l.x, l.y, h.x, h.y);
                 const int pr = (bl * NT * 8 + tok) >> 1, od = tok & 1;
-                const float c = (float)(-(1032 * slo + 72 * shi));
+                const float c = (float)(-8 * (slo + shi)) * 0x1p-24f;
                 xs[pr * 8 + od] = c;
                 xs[pr * 8 + 2 + od] = c;
-                xs[pr * 8 + 4 + od] = f16_bits_to_f32((unsigned short)ps[r]);
+                xs[pr * 8 + 4 + od] = f16_bits_to_f32((unsigned short)ps[r]) * 0x1p24f;
             }
         }
     };
@@ -377,8 +381,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int i = 0; i < TW; ++i) {
                         const uint8_t* bx = bx0 + i * 16 * 128 + sw;
                         uint32_t q0[4], q1[4];
-                        nibbles_to_f16(*reinterpret_cast<const uint32_t*>(bx), q0);
-                        nibbles_to_f16(*reinterpret_cast<const uint32_t*>(bx + 8 * 128), q1);
+                        nibbles_sub(*reinterpret_cast<const uint32_t*>(bx), q0);
+                        nibbles_sub(*reinterpret_cast<const uint32_t*>(bx + 8 * 128), q1);
                         ah[i][0][0] = q0[0], ah[i][0][1] = q1[0], ah[i][0][2] = q0[1], ah[i][0][3] = q1[1];
                         ah[i][1][0] = q0[2], ah[i][1][1] = q1[2], ah[i][1][2] = q0[3], ah[i][1][3] = q1[3];
 #pragma unroll
@@ -399,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int i = 0; i < TW; ++i) {
                             float dd[4];
                             mma16816(dd, ah[i][0], f.x, f.y, c4);
-                            mma16816(dd, ah[i][1], f.z, f.w, dd);  // exact integer block dots
+                            mma16816(dd, ah[i][1], f.z, f.w, dd);  // 2^-24 x the integer block dots
                             acc[i][j][0] = ffma2_scaled(make_float2(dw[i][0], dw[i][0]), sx,
                                                         make_float2(dd[0], dd[1]), acc[i][j][0]);
                             acc[i][j][1] = ffma2_scaled(make_float2(dw[i][1], dw[i][1]), sx,
@@ -656,17 +660,6 @@ __device__ __forceinline__ void tma3d_keep(void* dst, const CUtensorMap* map, in
         "[%5];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
-}
-
-// One word of a weight row -> the four fragment registers of the encoding
-// above: (u_0, u_2), (u_1, u_3), (16 v_0, 16 v_2), (16 v_1, 16 v_3) as fp16
-// bit patterns, u / v the low / high nibbles of bytes 0..3 (codes q + 8).
-__device__ __forceinline__ void nibbles_sub(uint32_t w, uint32_t (&o)[4]) {
-    const uint32_t w8 = w >> 8;
-    o[0] = w & 0x000F000Fu;
-    o[1] = w8 & 0x000F000Fu;
-    o[2] = w & 0x00F000F0u;
-    o[3] = w8 & 0x00F000F0u;
 }
 
 // Every wait is bounded; a plain try_wait lets the hardware hold the warp
@@ -1042,13 +1035,17 @@ qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K
 // and 256 rows leave room for two stages only.  Its TMA copies of the
 // activation scales want them 16-byte aligned.  Returns false (nothing
 // launched) where the plan does not qualify.
-// Rows per CTA of the wide plan (96, 128 or 192), or 0 where it does not qualify.
-int plan_rows(int64_t N, int sms) {
+// Rows per CTA of the wide plan (96, 128 or 192), or 0 where it does not
+// qualify.  The 96-row plan (three 32-row sets, 8 warps splitting a unit's
+// blocks) only for 9..16 tokens: with 8 or fewer the row-group kernel
+// measured faster there (14336 x 4096: 14.5 against 15.1 us at 8 tokens,
+// 20.7 against 18.5 at 16).
+int plan_rows(int64_t N, int64_t M, int sms) {
     const int64_t need = (N + sms - 1) / sms;
     const int64_t r16 = round_up(need, 16);
     const auto ok = [&](int64_t g) { return round_up(need, g) * 100 <= r16 * 108; };
     if (need > 64 && need <= 192 && ok(64)) return need <= 128 ? 128 : 192;
-    if (need > 64 && need <= 96 && ok(32)) return 96;  // three 32-row sets
+    if (M > 8 && need > 64 && need <= 96 && ok(32)) return 96;  // three 32-row sets
     return 0;
 }
 
@@ -1057,7 +1054,7 @@ bool plan_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
                  const uint16_t* xd, float* y, int64_t ldy, int sms, int smem_optin, int* err, cudaStream_t st,
                  qmm_status* out) {
     if (reinterpret_cast<uintptr_t>(xd) % 16 != 0) return false;
-    switch (plan_rows(N, sms)) {
+    switch (plan_rows(N, M, sms)) {
         case 128: *out = launch<NT, 2, 4>(w_qs, w_d, N, K, M, xq, xd, y, ldy, smem_optin, err, st); return true;
         case 192: *out = launch<NT, 3, 4>(w_qs, w_d, N, K, M, xq, xd, y, ldy, smem_optin, err, st); return true;
         case 96: *out = launch<NT, 3, 2>(w_qs, w_d, N, K, M, xq, xd, y, ldy, smem_optin, err, st); return true;
@@ -1070,7 +1067,7 @@ bool plan_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
 }  // namespace mmak
 
 bool gemm_wide_planned(int64_t N, int64_t M, const void* xd, int sms) {
-    return M >= 1 && M <= 16 && reinterpret_cast<uintptr_t>(xd) % 16 == 0 && mmak::widek::plan_rows(N, sms) > 0;
+    return M >= 1 && M <= 16 && reinterpret_cast<uintptr_t>(xd) % 16 == 0 && mmak::widek::plan_rows(N, M, sms) > 0;
 }
 
 bool gemm_mma_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const void* w_d, const void* xq,

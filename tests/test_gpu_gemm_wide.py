@@ -67,6 +67,7 @@ def test_row_plans_are_the_intended_ones():
 
 @pytest.mark.parametrize("N", sorted(ROW_PLANS))
 @pytest.mark.parametrize("K,M", [(256, 16), (768, 9), (2048, 2), (2048, 8), (2048, 13)])
+# (the 96-row plan, N = 13000, takes 9..16 tokens; 2 and 8 run on the row-group kernel there)
 def test_wide_vs_oracle(qmm, N, K, M):
     qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + K + M)
     qs, d = _planes(qmm, qw, dw)
