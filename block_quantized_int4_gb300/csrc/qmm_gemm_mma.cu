@@ -623,6 +623,7 @@ struct Shape {
 struct Args {
     int64_t N, K, M, ldy;
     float* y;
+    int nchunk;  // row chunks of RPC rows per CTA (the last CTA may have fewer)
     int nstages;
     int off_xbuf, off_xsc;  // from the 1024-aligned base; the ring starts at 1024
     int* err;
@@ -673,7 +674,9 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
     return true;
 }
 
-template <int NT, int WT, int KPB>
+// MULTI: the CTA may walk several row chunks (nchunk > 1); the single-chunk
+// instances leave that bookkeeping out (it costs registers at the 128 cap).
+template <int NT, int WT, int KPB, bool MULTI>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_d,
                      const __grid_constant__ CUtensorMap map_xq, const __grid_constant__ CUtensorMap map_xd, Args a) {
@@ -689,8 +692,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = (int)(a.K / QK);
     const int S = a.nstages;  // >= 2
-    const int64_t row_begin = (int64_t)blockIdx.x * RPC;
-    const int nunits = (B + UKB - 1) / UKB;
+    const int nunits = (B + UKB - 1) / UKB;  // per chunk
+    // this CTA's chunks of RPC rows: chunk0 .. chunk0 + nck - 1, walked one
+    // after the other through one unit sequence v = chunk * nunits + unit
+    const int64_t chunk0 = MULTI ? (int64_t)blockIdx.x * a.nchunk : (int64_t)blockIdx.x;
+    const int nck = MULTI ? (int)min((int64_t)a.nchunk, (a.N + RPC - 1) / RPC - chunk0) : 1;
+    const int V = MULTI ? nck * nunits : nunits;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
@@ -715,8 +722,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // before: only the first unit's weight copies go out before that wait.
     const bool issuer = lane == 0 && warp < 4;
     const uint64_t pol = l2_evict_first_policy();
-    auto issue = [&](int u, bool weights, bool acts) {
-        const int s = u % S, b0 = u * UKB;
+    auto issue = [&](int v, bool weights, bool acts) {
+        const int ck = MULTI ? v / nunits : 0;
+        const int s = v % S, b0 = (v - ck * nunits) * UKB;
+        const int row_begin = (int)((chunk0 + ck) * RPC);
         uint8_t* st = ring + (size_t)s * SH::STAGE;
         if (warp == 0 && weights) {
             mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * RPC * 128 + RPC * UKB * 2 + 4 * TK * 128 + TK * UKB * 2));
@@ -729,12 +738,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             tma2d_keep(st + SH::OFF_XD, &map_xd, b0, (int)blockIdx.y * TK, &full[s]);
         }
     };
-    int issued = min(S, nunits);
-    if (issuer && nunits > 0) issue(0, true, false);
+    int issued = min(S, V);
+    if (issuer && V > 0) issue(0, true, false);
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (issuer && nunits > 0) {
+    if (issuer && V > 0) {
         issue(0, false, true);
-        for (int u = 1; u < issued; ++u) issue(u, true, true);
+        for (int v = 1; v < issued; ++v) issue(v, true, true);
     }
 
     const int g8 = lane >> 2, t4 = lane & 3;
@@ -755,8 +764,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t x_mul = sh ? 0x2C002C00u : 0x3C003C00u;  // 1/16 or 1
     const uint32_t x_add = sh ? 0xD480D480u : 0xE480E480u;  // -72 or -1152
     // Unit u's fp16 B fragments and (seed, d_x) pairs into buffer buf.
-    auto stage_x = [&](int u, int buf) {
-        const uint8_t* st = ring + (size_t)(u % S) * SH::STAGE;
+    auto stage_x = [&](int v, int buf) {
+        const uint8_t* st = ring + (size_t)(v % S) * SH::STAGE;
         const uint4 px = lds128(st + xq_off);
         int sum = __dp4a((int)px.x, 0x01010101, 0);
         sum = __dp4a((int)px.y, 0x01010101, sum);
@@ -823,24 +832,87 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     };
 
+    // The KP warps of each row set add their sums of a chunk in shared memory
+    // (`red`: a stage every warp has finished with, which no copy fills until
+    // this returns); kp 0 writes y.  Every thread calls this at the same
+    // points (it holds two CTA barriers).
+    constexpr int SLOT = WT * NT * 128;  // floats per warp
+    auto reduce_store = [&](int64_t row_begin, float* red) {
+        if (kp > 0) {
+            float* rp = red + (rh * (KP - 1) + kp - 1) * SLOT + lane;
+#pragma unroll
+            for (int i = 0; i < WT; ++i)
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    float* q = rp + (i * NT + j) * 128;
+                    q[0] = acc[i][j][0].x;
+                    q[32] = acc[i][j][0].y;
+                    q[64] = acc[i][j][1].x;
+                    q[96] = acc[i][j][1].y;
+                }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(THREADS) : "memory");
+        if (kp == 0 && !failed) {
+#pragma unroll 1
+            for (int p = 1; p < KP; ++p) {
+                const float* rp = red + (rh * (KP - 1) + p - 1) * SLOT + lane;
+#pragma unroll
+                for (int i = 0; i < WT; ++i)
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const float* q = rp + (i * NT + j) * 128;
+                        acc[i][j][0].x += q[0];
+                        acc[i][j][0].y += q[32];
+                        acc[i][j][1].x += q[64];
+                        acc[i][j][1].y += q[96];
+                    }
+            }
+#pragma unroll
+            for (int i = 0; i < WT; ++i)
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const int64_t m = m0 + 8 * j + 2 * t4;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int64_t row = row_begin + (rh * WT + i) * 16 + g8 + 8 * h;
+                        if (row >= a.N) continue;
+                        if (m < a.M) a.y[m * a.ldy + row] = acc[i][j][h].x;
+                        if (m + 1 < a.M) a.y[(m + 1) * a.ldy + row] = acc[i][j][h].y;
+                    }
+                }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(THREADS) : "memory");  // red read before the stage is refilled
+#pragma unroll
+        for (int i = 0; i < WT; ++i)
+#pragma unroll
+            for (int j = 0; j < NT; ++j) acc[i][j][0] = acc[i][j][1] = make_float2(0.f, 0.f);
+    };
+
     // prologue: unit 0's fragments built
-    if (nunits > 0) {
+    if (V > 0) {
         if (!wait_phase(&full[0], 0, abort_flag)) fail();
         if (stager && !failed) stage_x(0, 0);
         __syncwarp();
         if (lane == 0) mbar_arrive(&xfull[0]);
     }
-    for (int u = 0; u < nunits; ++u) {
-        const int s = u % S, buf = u & 1;
-        // every warp has finished unit u - 1: its stage may be refilled and
+    int u = 0, ck = 0;  // unit inside the chunk, chunk of this CTA
+    for (int v = 0; v < V; ++v) {
+        const int s = v % S, buf = v & 1;
+        // every warp has finished unit v - 1: its stage may be refilled and
         // its fragment buffer (buf ^ 1) overwritten
-        if (u >= 1 && !failed && !wait_phase(&xempty[buf ^ 1], ((u - 1) >> 1) & 1, abort_flag)) fail();
-        if (u >= 1 && issued < nunits && !failed) {
+        if (v >= 1 && !failed && !wait_phase(&xempty[buf ^ 1], ((v - 1) >> 1) & 1, abort_flag)) fail();
+        // a chunk ended with unit v - 1: its sums out, through that unit's stage
+        if constexpr (MULTI) {
+            if (v >= 1 && u == 0)
+                reduce_store((chunk0 + ck - 1) * RPC,
+                             reinterpret_cast<float*>(ring + (size_t)((v - 1) % S) * SH::STAGE));
+        }
+        if (v >= 1 && issued < V && !failed) {
             if (issuer) issue(issued, true, true);
             ++issued;
         }
-        // unit u: its stage was waited for before its fragments were built
-        if (!failed && !wait_phase(&xfull[buf], (u >> 1) & 1, abort_flag)) fail();
+        // unit v: its stage was waited for before its fragments were built
+        if (!failed && !wait_phase(&xfull[buf], (v >> 1) & 1, abort_flag)) fail();
         const int nb = min(UKB, B - u * UKB);
         const bool work = !failed && fb < nb;
         const uint8_t* st = ring + (size_t)s * SH::STAGE;
@@ -908,11 +980,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         };
         if (work) compute_pair(0);
-        // unit u + 1's fragments, between the two halves of unit u's work so
+        // unit v + 1's fragments, between the two halves of unit v's work so
         // that their latency hides behind it
-        if (u + 1 < nunits) {
-            if (!failed && !wait_phase(&full[(u + 1) % S], ((u + 1) / S) & 1, abort_flag)) fail();
-            if (stager && !failed) stage_x(u + 1, buf ^ 1);
+        if (v + 1 < V) {
+            if (!failed && !wait_phase(&full[(v + 1) % S], ((v + 1) / S) & 1, abort_flag)) fail();
+            if (stager && !failed) stage_x(v + 1, buf ^ 1);
             __syncwarp();
             if (lane == 0) mbar_arrive(&xfull[buf ^ 1]);
         }
@@ -921,72 +993,34 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&xempty[buf]);  // unit read: its stage and fragments may be reused
+        if (++u == nunits) {
+            u = 0;
+            if constexpr (MULTI) ++ck;
+        }
     }
     if (failed && tid == 0) {  // copies still in flight land before the ring is reused or the CTA exits
-        for (int u = max(0, issued - S); u < issued; ++u) {
+        for (int w = max(0, issued - S); w < issued; ++w) {
             const uint64_t t0 = global_ns();
-            while (!mbar_try_wait(&full[u % S], (u / S) & 1) && global_ns() - t0 < WAIT_LIMIT_NS) {
+            while (!mbar_try_wait(&full[w % S], (w / S) & 1) && global_ns() - t0 < WAIT_LIMIT_NS) {
             }
         }
     }
 
-    // ---------------- the KP warps of each row set add their sums; kp 0 writes y.
-    // The partial sums go to the ring, which every warp has finished reading
-    // and no copy fills any more (each was waited for).
+    // ---------------- the last chunk's sums, through the ring (every warp has
+    // finished reading it and no copy fills it any more: each was waited for)
     __syncthreads();
-    constexpr int SLOT = WT * NT * 128;  // floats per warp
-    float* red = reinterpret_cast<float*>(ring);
-    if (kp > 0) {
-        float* rp = red + (rh * (KP - 1) + kp - 1) * SLOT + lane;
-#pragma unroll
-        for (int i = 0; i < WT; ++i)
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                float* q = rp + (i * NT + j) * 128;
-                q[0] = acc[i][j][0].x;
-                q[32] = acc[i][j][0].y;
-                q[64] = acc[i][j][1].x;
-                q[96] = acc[i][j][1].y;
-            }
-    }
-    __syncthreads();
-    if (kp == 0 && !failed) {
-#pragma unroll 1
-        for (int p = 1; p < KP; ++p) {
-            const float* rp = red + (rh * (KP - 1) + p - 1) * SLOT + lane;
-#pragma unroll
-            for (int i = 0; i < WT; ++i)
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const float* q = rp + (i * NT + j) * 128;
-                    acc[i][j][0].x += q[0];
-                    acc[i][j][0].y += q[32];
-                    acc[i][j][1].x += q[64];
-                    acc[i][j][1].y += q[96];
-                }
-        }
-#pragma unroll
-        for (int i = 0; i < WT; ++i)
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                const int64_t m = m0 + 8 * j + 2 * t4;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int64_t row = row_begin + (rh * WT + i) * 16 + g8 + 8 * h;
-                    if (row >= a.N) continue;
-                    if (m < a.M) a.y[m * a.ldy + row] = acc[i][j][h].x;
-                    if (m + 1 < a.M) a.y[(m + 1) * a.ldy + row] = acc[i][j][h].y;
-                }
-            }
-    }
+    if (V > 0) reduce_store((chunk0 + nck - 1) * RPC, reinterpret_cast<float*>(ring));
 }
 
-template <int NT, int WT, int KPB>
+template <int NT, int WT, int KPB, bool MULTI>
 qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, const int8_t* xq,
-                  const uint16_t* xd, float* y, int64_t ldy, int smem_optin, int* err, cudaStream_t st) {
+                  const uint16_t* xd, float* y, int64_t ldy, int nchunk, int smem_optin, int* err, cudaStream_t st) {
     using SH = Shape<NT, WT, KPB>;
+    if (MULTI != (nchunk > 1)) return QMM_ERR_SHAPE;
     const int64_t B = K / QK;
-    const int64_t nunits = (B + UKB - 1) / UKB;
+    const int64_t nunits = (B + UKB - 1) / UKB * nchunk;
+    // a chunk that ends before the last adds its sums in one stage
+    if (nchunk > 1 && SH::RED > SH::STAGE) return QMM_ERR_SHAPE;
     const int fixed = 1024 + 2 * SH::XBUF + 2 * SH::XSC + 1024;  // barriers, buffers, alignment slack
     const int64_t nst = std::min<int64_t>({(int64_t)MAX_STAGES, (smem_optin - fixed) / SH::STAGE, nunits + 1});
     if (nst < 2) return QMM_ERR_SHAPE;
@@ -998,6 +1032,7 @@ qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K
     a.M = M;
     a.ldy = ldy;
     a.y = y;
+    a.nchunk = nchunk;
     a.nstages = (int)nst;
     a.off_xbuf = 1024 + (int)ring;
     a.off_xsc = a.off_xbuf + 2 * SH::XBUF;
@@ -1019,34 +1054,52 @@ qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K
         !make_tensor_map_2d(&mxd, CU_TENSOR_MAP_DATA_TYPE_UINT16, xd, (uint64_t)B, (uint64_t)M, (uint64_t)B * 2,
                             (uint32_t)UKB, (uint32_t)SH::TK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return QMM_ERR_CUDA;
-    auto kern = gemm_wide_kernel<NT, WT, KPB>;
+    auto kern = gemm_wide_kernel<NT, WT, KPB, MULTI>;
     if (!allow_smem(kern, smem_optin)) return QMM_ERR_SHAPE;
-    const dim3 grid((unsigned)((N + SH::RPC - 1) / SH::RPC), (unsigned)((M + SH::TK - 1) / SH::TK));
+    const int64_t chunks = (N + SH::RPC - 1) / SH::RPC;
+    const dim3 grid((unsigned)((chunks + nchunk - 1) / nchunk), (unsigned)((M + SH::TK - 1) / SH::TK));
     kern<<<grid, THREADS, (int)smem, st>>>(mq, md, mxq, mxd, a);
     return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
-// Rows per CTA at one CTA per SM: the wide layout takes 32- or 64-row
-// granules; it is used when that costs no more CTA rows than the 16-row
-// granule of the group kernel (within 8%) and gives each warp two or three
-// row tiles: 96, 128 or 192 rows per CTA.  With one row tile per warp the
-// per-unit hand-over and staging cost more than the 16 warps save (measured:
-// 8192 x 28672 at 16 tokens 91 us against 69 us, 4096 x 14336 40 against 28),
-// and 256 rows leave room for two stages only.  Its TMA copies of the
-// activation scales want them 16-byte aligned.  Returns false (nothing
-// launched) where the plan does not qualify.
-// Rows per CTA of the wide plan (96, 128 or 192), or 0 where it does not
-// qualify.  The 96-row plan (three 32-row sets, 8 warps splitting a unit's
-// blocks) only for 9..16 tokens: with 8 or fewer the row-group kernel
-// measured faster there (14336 x 4096: 14.5 against 15.1 us at 8 tokens,
-// 20.7 against 18.5 at 16).
-int plan_rows(int64_t N, int64_t M, int sms) {
+// Row plan at one CTA per SM: chunks of `rpc` rows (two or three row tiles
+// per warp), `nchunk` of them per CTA, or rpc = 0 where the layout does not
+// qualify.  It is used when its rows per CTA (nchunk * rpc) exceed those of
+// the row-group kernel's 16-row granule by at most 8%.
+//  - up to 192 rows per CTA: one chunk of 128 or 192 rows, or 96 rows (three
+//    32-row sets, 8 warps splitting a unit's blocks) for 9..16 tokens only
+//    (with 8 or fewer the row-group kernel measured faster there: 14336 x
+//    4096 14.5 against 15.1 us at 8 tokens, 20.7 against 18.5 at 16).  With
+//    one row tile per warp the per-unit hand-over and staging cost more
+//    than the 16 warps save (8192 x 28672 at 16 tokens 91 us against 69 us,
+//    4096 x 14336 40 against 28), and 256 rows leave room for two stages.
+//  - more: several chunks of 128 or 192 rows, whichever needs fewer rows
+//    per CTA (192 on a tie).
+struct Plan {
+    int rpc = 0, nchunk = 1;
+};
+
+Plan plan_rows(int64_t N, int64_t M, int sms) {
+    Plan p;
     const int64_t need = (N + sms - 1) / sms;
     const int64_t r16 = round_up(need, 16);
-    const auto ok = [&](int64_t g) { return round_up(need, g) * 100 <= r16 * 108; };
-    if (need > 64 && need <= 192 && ok(64)) return need <= 128 ? 128 : 192;
-    if (M > 8 && need > 64 && need <= 96 && ok(32)) return 96;  // three 32-row sets
-    return 0;
+    const auto ok = [&](int64_t rows) { return rows * 100 <= r16 * 108; };
+    if (need <= 64) return p;
+    if (need <= 192) {
+        if (ok(round_up(need, 64))) p.rpc = need <= 128 ? 128 : 192;
+        else if (M > 8 && need <= 96 && ok(round_up(need, 32))) p.rpc = 96;
+        return p;
+    }
+    const int64_t n128 = ((N + 127) / 128 + sms - 1) / sms, n192 = ((N + 191) / 192 + sms - 1) / sms;
+    if (n192 * 192 <= n128 * 128) {
+        p.rpc = 192;
+        p.nchunk = (int)n192;
+    } else {
+        p.rpc = 128;
+        p.nchunk = (int)n128;
+    }
+    if (!ok((int64_t)p.rpc * p.nchunk) || p.nchunk > (1 << 20)) p = Plan();
+    return p;
 }
 
 template <int NT>
@@ -1054,10 +1107,20 @@ bool plan_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
                  const uint16_t* xd, float* y, int64_t ldy, int sms, int smem_optin, int* err, cudaStream_t st,
                  qmm_status* out) {
     if (reinterpret_cast<uintptr_t>(xd) % 16 != 0) return false;
-    switch (plan_rows(N, M, sms)) {
-        case 128: *out = launch<NT, 2, 4>(w_qs, w_d, N, K, M, xq, xd, y, ldy, smem_optin, err, st); return true;
-        case 192: *out = launch<NT, 3, 4>(w_qs, w_d, N, K, M, xq, xd, y, ldy, smem_optin, err, st); return true;
-        case 96: *out = launch<NT, 3, 2>(w_qs, w_d, N, K, M, xq, xd, y, ldy, smem_optin, err, st); return true;
+    const Plan p = plan_rows(N, M, sms);
+    const bool multi = p.nchunk > 1;
+    switch (p.rpc) {
+        case 128:
+            *out = multi ? launch<NT, 2, 4, true>(w_qs, w_d, N, K, M, xq, xd, y, ldy, p.nchunk, smem_optin, err, st)
+                         : launch<NT, 2, 4, false>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, smem_optin, err, st);
+            return true;
+        case 192:
+            *out = multi ? launch<NT, 3, 4, true>(w_qs, w_d, N, K, M, xq, xd, y, ldy, p.nchunk, smem_optin, err, st)
+                         : launch<NT, 3, 4, false>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, smem_optin, err, st);
+            return true;
+        case 96:  // one chunk only
+            *out = launch<NT, 3, 2, false>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, smem_optin, err, st);
+            return true;
         default: return false;
     }
 }
@@ -1067,7 +1130,7 @@ bool plan_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
 }  // namespace mmak
 
 bool gemm_wide_planned(int64_t N, int64_t M, const void* xd, int sms) {
-    return M >= 1 && M <= 16 && reinterpret_cast<uintptr_t>(xd) % 16 == 0 && mmak::widek::plan_rows(N, M, sms) > 0;
+    return M >= 1 && M <= 16 && reinterpret_cast<uintptr_t>(xd) % 16 == 0 && mmak::widek::plan_rows(N, M, sms).rpc > 0;
 }
 
 bool gemm_mma_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const void* w_d, const void* xq,

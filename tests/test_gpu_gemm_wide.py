@@ -118,6 +118,42 @@ def test_wide_integer_grid_exact(qmm, N, K, M):
     assert qmm.qmm_last_device_error() == 0
 
 
+# N -> (chunk rows, chunks per CTA) on 152 SMs for the plans that walk several
+# row chunks per CTA; each has a last CTA with fewer chunks and a last chunk
+# with fewer rows
+MULTI_PLANS = {58000: (192, 2), 110000: (192, 4), 128256: (128, 7)}
+
+
+@pytest.mark.parametrize("N", sorted(MULTI_PLANS))
+@pytest.mark.parametrize("K,M", [(768, 16), (2048, 4), (2048, 9)])
+def test_wide_several_chunks_per_cta(qmm, N, K, M):
+    """Rows at every chunk and CTA boundary (and 2000 more) against the oracle."""
+    rpc, nchunk = MULTI_PLANS[N]
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + K + M)
+    qs, d = _planes(qmm, qw, dw)
+    xq, xd = _q8(qx, dx)
+    y = qmm.gemm(qs, d, xq, xd)
+    rng = np.random.default_rng(N + M)
+    edges = np.arange(0, N, rpc)
+    rows = np.unique(np.clip(np.concatenate([edges, edges - 1, edges + 15, edges + rpc - 1, rng.integers(0, N, 2000),
+                                             np.arange(N - 40, N)]), 0, N - 1))
+    ref, S = O.matmul_int(qw, dw, qx, dx, rows=rows, nthreads=8)
+    assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, S, f"wide gemm {N}x{K} M={M} chunks")
+    assert torch.isfinite(y).all() and qmm.qmm_last_device_error() == 0
+
+
+def test_multi_chunk_plans_are_the_intended_ones():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip(f"{sms} SMs: the row plans differ from the ones the shapes were chosen for")
+    for N, (rpc, nchunk) in MULTI_PLANS.items():
+        need = -(-N // sms)
+        per = {r: -(-(-(-N // r)) // sms) for r in (128, 192)}
+        pick = 192 if per[192] * 192 <= per[128] * 128 else 128
+        assert (pick, per[pick]) == (rpc, nchunk)
+        assert pick * per[pick] * 100 <= -(-need // 16) * 16 * 108
+
+
 def test_wide_ldy(qmm):
     """Output row stride > N: the columns past N stay untouched."""
     N, K, M, ldy = 27000, 1024, 16, 27008
