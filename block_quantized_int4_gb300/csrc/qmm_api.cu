@@ -498,7 +498,7 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
         // (2048x5632 7.0/8.1, 2560x2048 4.4/4.9; but 5632x2048 6.4/5.6, and
         // 28672x8192 41.7 against 31.9 for the 16-warp layout).  From 8
         // tokens warp MMA wins everywhere.
-        const bool wide = pick != QMM_GEMM_KERNEL_MMA_GROUPS && gemm_wide_planned(N, M, xd, di->sms);
+        const bool wide = pick != QMM_GEMM_KERNEL_MMA_GROUPS && gemm_wide_planned(N, K, M, xd, di->sms);
         const bool prefer_stream =
             pick == QMM_GEMM_KERNEL_AUTO &&
             (M == 2 || (M <= 4 && !wide && (N <= 4096 || K >= 8192) && stream_eligible(N, K, w_qs, w_d, 4)));

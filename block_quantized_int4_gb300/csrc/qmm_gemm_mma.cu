@@ -674,9 +674,19 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
     return true;
 }
 
-// MULTI: the CTA may walk several row chunks (nchunk > 1); the single-chunk
-// instances leave that bookkeeping out (it costs registers at the 128 cap).
-template <int NT, int WT, int KPB, bool MULTI>
+// Modes: ONE chunk of rows per CTA; MULTI: the CTA walks several row chunks
+// (nchunk > 1; the other instances leave that bookkeeping out, it costs
+// registers at the 128 cap); SPLIT: a cluster of nsplit CTAs shares one
+// chunk, rank r taking the r-th share of the units (of K), and ranks
+// 1..nsplit-1 hand their sums to rank 0 through distributed shared memory,
+// which adds them in rank order (deterministic) and writes y.
+enum Mode { ONE = 0, MULTI = 1, SPLIT = 2 };
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int NT, int WT, int KPB, int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_wide_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_d,
                      const __grid_constant__ CUtensorMap map_xq, const __grid_constant__ CUtensorMap map_xd, Args a) {
@@ -692,12 +702,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = (int)(a.K / QK);
     const int S = a.nstages;  // >= 2
-    const int nunits = (B + UKB - 1) / UKB;  // per chunk
+    constexpr bool multi = MODE == MULTI, split = MODE == SPLIT;
+    // units of a chunk this CTA takes: u_lo .. u_lo + nunits - 1 (all of K
+    // but with SPLIT)
+    int nunits = (B + UKB - 1) / UKB, u_lo = 0;
+    uint32_t rank = 0, nsplit = 1;
+    if constexpr (split) {
+        asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+        asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(nsplit));
+        const int per = (nunits + (int)nsplit - 1) / (int)nsplit;
+        u_lo = min(nunits, (int)rank * per);
+        nunits = min(nunits, u_lo + per) - u_lo;
+    }
     // this CTA's chunks of RPC rows: chunk0 .. chunk0 + nck - 1, walked one
     // after the other through one unit sequence v = chunk * nunits + unit
-    const int64_t chunk0 = MULTI ? (int64_t)blockIdx.x * a.nchunk : (int64_t)blockIdx.x;
-    const int nck = MULTI ? (int)min((int64_t)a.nchunk, (a.N + RPC - 1) / RPC - chunk0) : 1;
-    const int V = MULTI ? nck * nunits : nunits;
+    const int64_t chunk0 = multi ? (int64_t)blockIdx.x * a.nchunk : split ? (int64_t)(blockIdx.x / nsplit)
+                                                                         : (int64_t)blockIdx.x;
+    const int nck = multi ? (int)min((int64_t)a.nchunk, (a.N + RPC - 1) / RPC - chunk0) : 1;
+    const int V = multi ? nck * nunits : nunits;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
@@ -723,8 +745,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool issuer = lane == 0 && warp < 4;
     const uint64_t pol = l2_evict_first_policy();
     auto issue = [&](int v, bool weights, bool acts) {
-        const int ck = MULTI ? v / nunits : 0;
-        const int s = v % S, b0 = (v - ck * nunits) * UKB;
+        const int ck = multi ? v / nunits : 0;
+        const int s = v % S, b0 = (u_lo + v - ck * nunits) * UKB;
         const int row_begin = (int)((chunk0 + ck) * RPC);
         uint8_t* st = ring + (size_t)s * SH::STAGE;
         if (warp == 0 && weights) {
@@ -837,7 +859,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // this returns); kp 0 writes y.  Every thread calls this at the same
     // points (it holds two CTA barriers).
     constexpr int SLOT = WT * NT * 128;  // floats per warp
-    auto reduce_store = [&](int64_t row_begin, float* red) {
+    // kp > 0 warps' sums into red, then added into kp 0's acc (one barrier)
+    auto reduce_partials = [&](float* red) {
         if (kp > 0) {
             float* rp = red + (rh * (KP - 1) + kp - 1) * SLOT + lane;
 #pragma unroll
@@ -852,7 +875,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
         }
         asm volatile("bar.sync 1, %0;" ::"r"(THREADS) : "memory");
-        if (kp == 0 && !failed) {
+        if (kp == 0) {
 #pragma unroll 1
             for (int p = 1; p < KP; ++p) {
                 const float* rp = red + (rh * (KP - 1) + p - 1) * SLOT + lane;
@@ -867,6 +890,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                         acc[i][j][1].y += q[96];
                     }
             }
+        }
+    };
+    // kp 0 warps write their rows of the chunk starting at row_begin
+    auto store_rows = [&](int64_t row_begin) {
+        if (kp == 0 && !failed) {
 #pragma unroll
             for (int i = 0; i < WT; ++i)
 #pragma unroll
@@ -881,6 +909,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
         }
+    };
+    // a chunk's sums out through red, acc cleared; every thread calls this
+    // at the same points (it holds two CTA barriers)
+    auto reduce_store = [&](int64_t row_begin, float* red) {
+        reduce_partials(red);
+        store_rows(row_begin);
         asm volatile("bar.sync 1, %0;" ::"r"(THREADS) : "memory");  // red read before the stage is refilled
 #pragma unroll
         for (int i = 0; i < WT; ++i)
@@ -902,7 +936,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // its fragment buffer (buf ^ 1) overwritten
         if (v >= 1 && !failed && !wait_phase(&xempty[buf ^ 1], ((v - 1) >> 1) & 1, abort_flag)) fail();
         // a chunk ended with unit v - 1: its sums out, through that unit's stage
-        if constexpr (MULTI) {
+        if constexpr (multi) {
             if (v >= 1 && u == 0)
                 reduce_store((chunk0 + ck - 1) * RPC,
                              reinterpret_cast<float*>(ring + (size_t)((v - 1) % S) * SH::STAGE));
@@ -913,7 +947,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         // unit v: its stage was waited for before its fragments were built
         if (!failed && !wait_phase(&xfull[buf], (v >> 1) & 1, abort_flag)) fail();
-        const int nb = min(UKB, B - u * UKB);
+        const int nb = min(UKB, B - (u_lo + u) * UKB);
         const bool work = !failed && fb < nb;
         const uint8_t* st = ring + (size_t)s * SH::STAGE;
         const uint32_t st_u32 = smem_u32(st);
@@ -995,7 +1029,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) mbar_arrive(&xempty[buf]);  // unit read: its stage and fragments may be reused
         if (++u == nunits) {
             u = 0;
-            if constexpr (MULTI) ++ck;
+            if constexpr (multi) ++ck;
         }
     }
     if (failed && tid == 0) {  // copies still in flight land before the ring is reused or the CTA exits
@@ -1009,23 +1043,69 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------- the last chunk's sums, through the ring (every warp has
     // finished reading it and no copy fills it any more: each was waited for)
     __syncthreads();
-    if (V > 0) reduce_store((chunk0 + nck - 1) * RPC, reinterpret_cast<float*>(ring));
+    if constexpr (split) {
+        // this CTA's sums in kp 0's acc; then (after every CTA of the cluster
+        // has done so, so rank 0's ring is free) ranks > 0 write theirs into
+        // rank 0's ring, slot (rank - 1, rh), and rank 0 adds them in order
+        float* red = reinterpret_cast<float*>(ring);
+        reduce_partials(red);
+        cluster_sync_all();
+        if (rank > 0 && kp == 0) {
+            uint32_t dst;
+            asm("mapa.shared::cluster.u32 %0, %1, 0;"
+                : "=r"(dst)
+                : "r"(smem_u32(red + ((rank - 1) * SH::RH + rh) * SLOT + lane)));
+#pragma unroll
+            for (int i = 0; i < WT; ++i)
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const uint32_t q = dst + (uint32_t)((i * NT + j) * 128 * 4);
+                    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(q), "f"(acc[i][j][0].x) : "memory");
+                    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(q + 128), "f"(acc[i][j][0].y) : "memory");
+                    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(q + 256), "f"(acc[i][j][1].x) : "memory");
+                    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(q + 384), "f"(acc[i][j][1].y) : "memory");
+                }
+        }
+        cluster_sync_all();
+        if (rank == 0 && kp == 0) {
+#pragma unroll 1
+            for (uint32_t r = 1; r < nsplit; ++r) {
+                const float* rp = red + ((r - 1) * SH::RH + rh) * SLOT + lane;
+#pragma unroll
+                for (int i = 0; i < WT; ++i)
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const float* q = rp + (i * NT + j) * 128;
+                        acc[i][j][0].x += q[0];
+                        acc[i][j][0].y += q[32];
+                        acc[i][j][1].x += q[64];
+                        acc[i][j][1].y += q[96];
+                    }
+            }
+            store_rows(chunk0 * RPC);
+        }
+    } else {
+        if (V > 0) reduce_store((chunk0 + nck - 1) * RPC, reinterpret_cast<float*>(ring));
+    }
 }
 
-template <int NT, int WT, int KPB, bool MULTI>
+template <int NT, int WT, int KPB, int MODE>
 qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, const int8_t* xq,
-                  const uint16_t* xd, float* y, int64_t ldy, int nchunk, int smem_optin, int* err, cudaStream_t st) {
+                  const uint16_t* xd, float* y, int64_t ldy, int nchunk, int nsplit, int smem_optin, int* err,
+                  cudaStream_t st) {
     using SH = Shape<NT, WT, KPB>;
-    if (MULTI != (nchunk > 1)) return QMM_ERR_SHAPE;
+    if ((MODE == MULTI) != (nchunk > 1) || (MODE == SPLIT) != (nsplit > 1) || nsplit > 8) return QMM_ERR_SHAPE;
     const int64_t B = K / QK;
-    const int64_t nunits = (B + UKB - 1) / UKB * nchunk;
-    // a chunk that ends before the last adds its sums in one stage
+    const int64_t nunits = ((B + UKB - 1) / UKB + nsplit - 1) / nsplit * nchunk;
+    // a chunk that ends before the last adds its sums in one stage; the
+    // ranks of a split hand theirs to rank 0's ring
     if (nchunk > 1 && SH::RED > SH::STAGE) return QMM_ERR_SHAPE;
     const int fixed = 1024 + 2 * SH::XBUF + 2 * SH::XSC + 1024;  // barriers, buffers, alignment slack
     const int64_t nst = std::min<int64_t>({(int64_t)MAX_STAGES, (smem_optin - fixed) / SH::STAGE, nunits + 1});
     if (nst < 2) return QMM_ERR_SHAPE;
     // the ring also holds the final partial sums
-    const int64_t ring = std::max<int64_t>(nst * SH::STAGE, SH::RED);
+    const int64_t ring = std::max<int64_t>({nst * SH::STAGE, (int64_t)SH::RED,
+                                            (int64_t)(nsplit - 1) * SH::RH * WT * NT * 512});
     Args a = {};
     a.N = N;
     a.K = K;
@@ -1054,11 +1134,30 @@ qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K
         !make_tensor_map_2d(&mxd, CU_TENSOR_MAP_DATA_TYPE_UINT16, xd, (uint64_t)B, (uint64_t)M, (uint64_t)B * 2,
                             (uint32_t)UKB, (uint32_t)SH::TK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return QMM_ERR_CUDA;
-    auto kern = gemm_wide_kernel<NT, WT, KPB, MULTI>;
+    auto kern = gemm_wide_kernel<NT, WT, KPB, MODE>;
     if (!allow_smem(kern, smem_optin)) return QMM_ERR_SHAPE;
     const int64_t chunks = (N + SH::RPC - 1) / SH::RPC;
-    const dim3 grid((unsigned)((chunks + nchunk - 1) / nchunk), (unsigned)((M + SH::TK - 1) / SH::TK));
-    kern<<<grid, THREADS, (int)smem, st>>>(mq, md, mxq, mxd, a);
+    const dim3 grid((unsigned)((chunks + nchunk - 1) / nchunk * nsplit), (unsigned)((M + SH::TK - 1) / SH::TK));
+    if (MODE != SPLIT) {
+        kern<<<grid, THREADS, (int)smem, st>>>(mq, md, mxq, mxd, a);
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)nsplit;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, mq, md, mxq, mxd, a) != cudaSuccess) {
+            cudaGetLastError();
+            return QMM_ERR_CUDA;
+        }
+    }
     return cudaGetLastError() == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
@@ -1075,16 +1174,27 @@ qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K
 //    4096 x 14336 40 against 28), and 256 rows leave room for two stages.
 //  - more: several chunks of 128 or 192 rows, whichever needs fewer rows
 //    per CTA (192 on a tie).
+//  - fewer rows (at most 64 per SM): 128-row chunks, each shared by a cluster
+//    of nsplit = min(8, SMs / chunks) >= 2 CTAs splitting K, when every
+//    rank gets at least 6 units of 16 blocks.
 struct Plan {
-    int rpc = 0, nchunk = 1;
+    int rpc = 0, nchunk = 1, nsplit = 1;
 };
 
-Plan plan_rows(int64_t N, int64_t M, int sms) {
+Plan plan_rows(int64_t N, int64_t K, int64_t M, int sms) {
     Plan p;
     const int64_t need = (N + sms - 1) / sms;
     const int64_t r16 = round_up(need, 16);
     const auto ok = [&](int64_t rows) { return rows * 100 <= r16 * 108; };
-    if (need <= 64) return p;
+    if (need <= 64) {
+        const int64_t chunks = (N + 127) / 128, units = (K / QK + UKB - 1) / UKB;
+        const int64_t ns = std::min<int64_t>(8, sms / chunks);
+        if (ns >= 2 && units >= 6 * ns) {
+            p.rpc = 128;
+            p.nsplit = (int)ns;
+        }
+        return p;
+    }
     if (need <= 192) {
         if (ok(round_up(need, 64))) p.rpc = need <= 128 ? 128 : 192;
         else if (M > 8 && need <= 96 && ok(round_up(need, 32))) p.rpc = 96;
@@ -1107,19 +1217,20 @@ bool plan_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
                  const uint16_t* xd, float* y, int64_t ldy, int sms, int smem_optin, int* err, cudaStream_t st,
                  qmm_status* out) {
     if (reinterpret_cast<uintptr_t>(xd) % 16 != 0) return false;
-    const Plan p = plan_rows(N, M, sms);
-    const bool multi = p.nchunk > 1;
+    const Plan p = plan_rows(N, K, M, sms);
+    const int nc = p.nchunk, ns = p.nsplit;
     switch (p.rpc) {
         case 128:
-            *out = multi ? launch<NT, 2, 4, true>(w_qs, w_d, N, K, M, xq, xd, y, ldy, p.nchunk, smem_optin, err, st)
-                         : launch<NT, 2, 4, false>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, smem_optin, err, st);
+            *out = ns > 1   ? launch<NT, 2, 4, SPLIT>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, ns, smem_optin, err, st)
+                   : nc > 1 ? launch<NT, 2, 4, MULTI>(w_qs, w_d, N, K, M, xq, xd, y, ldy, nc, 1, smem_optin, err, st)
+                            : launch<NT, 2, 4, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, 1, smem_optin, err, st);
             return true;
         case 192:
-            *out = multi ? launch<NT, 3, 4, true>(w_qs, w_d, N, K, M, xq, xd, y, ldy, p.nchunk, smem_optin, err, st)
-                         : launch<NT, 3, 4, false>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, smem_optin, err, st);
+            *out = nc > 1 ? launch<NT, 3, 4, MULTI>(w_qs, w_d, N, K, M, xq, xd, y, ldy, nc, 1, smem_optin, err, st)
+                          : launch<NT, 3, 4, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, 1, smem_optin, err, st);
             return true;
         case 96:  // one chunk only
-            *out = launch<NT, 3, 2, false>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, smem_optin, err, st);
+            *out = launch<NT, 3, 2, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, 1, smem_optin, err, st);
             return true;
         default: return false;
     }
@@ -1129,8 +1240,8 @@ bool plan_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
 
 }  // namespace mmak
 
-bool gemm_wide_planned(int64_t N, int64_t M, const void* xd, int sms) {
-    return M >= 1 && M <= 16 && reinterpret_cast<uintptr_t>(xd) % 16 == 0 && mmak::widek::plan_rows(N, M, sms).rpc > 0;
+bool gemm_wide_planned(int64_t N, int64_t K, int64_t M, const void* xd, int sms) {
+    return M >= 1 && M <= 16 && reinterpret_cast<uintptr_t>(xd) % 16 == 0 && mmak::widek::plan_rows(N, K, M, sms).rpc > 0;
 }
 
 bool gemm_mma_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const void* w_d, const void* xq,

@@ -18,8 +18,10 @@ bool gemm_mma_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const 
 // True when gemm_mma_launch (wide = true) takes the 16-warp layout for this
 // product: up to 16 tokens, xd 16-byte aligned, and a row plan at one CTA
 // per SM of 128 or 192 rows per CTA (ceil(N / sms) in 65..192), 96 rows for
-// 9..16 tokens, or several chunks of 128 or 192 rows per CTA for larger N.
-bool gemm_wide_planned(int64_t N, int64_t M, const void* xd, int sms);
+// 9..16 tokens, several chunks of 128 or 192 rows per CTA for larger N, or
+// for smaller N with long K, 128-row chunks split over K by clusters of 2..8
+// CTAs.
+bool gemm_wide_planned(int64_t N, int64_t K, int64_t M, const void* xd, int sms);
 
 // Enqueue y[m*ldy + n] (m < M, n < N) on `st`.  `sms` and `smem_optin` are
 // the device's SM count and opt-in shared memory per block; `err` is the

@@ -154,6 +154,42 @@ def test_multi_chunk_plans_are_the_intended_ones():
         assert pick * per[pick] * 100 <= -(-need // 16) * 16 * 108
 
 
+# N, K -> CTAs per cluster splitting K (128-row chunks) on 152 SMs
+SPLIT_PLANS = {(8192, 28672): 2, (4096, 14336): 4, (2048, 28672): 8, (5000, 16640): 3}
+
+
+@pytest.mark.parametrize("N,K", sorted(SPLIT_PLANS))
+@pytest.mark.parametrize("M", [16, 5])
+def test_wide_split_k_clusters(qmm, N, K, M):
+    """K shared by the CTAs of a cluster (uneven shares and a last half unit
+    for K = 16640): sampled rows, both ends and every chunk edge, against the
+    oracle; the same call twice gives the same bits (the ranks' sums are
+    added in a fixed order)."""
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + K + M)
+    qs, d = _planes(qmm, qw, dw)
+    xq, xd = _q8(qx, dx)
+    y = qmm.gemm(qs, d, xq, xd)
+    y2 = qmm.gemm(qs, d, xq, xd)
+    assert torch.equal(y, y2)
+    rng = np.random.default_rng(N + M)
+    edges = np.arange(0, N, 128)
+    rows = np.unique(np.clip(np.concatenate([edges, edges - 1, edges + 127, rng.integers(0, N, 600),
+                                             np.arange(N - 20, N)]), 0, N - 1))
+    ref, S = O.matmul_int(qw, dw, qx, dx, rows=rows, nthreads=8)
+    assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, S, f"split-K gemm {N}x{K} M={M}")
+    assert torch.isfinite(y).all() and qmm.qmm_last_device_error() == 0
+
+
+def test_split_plans_are_the_intended_ones():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip(f"{sms} SMs: the row plans differ from the ones the shapes were chosen for")
+    for (N, K), ns in SPLIT_PLANS.items():
+        assert -(-N // sms) <= 64
+        chunks = -(-N // 128)
+        assert min(8, sms // chunks) == ns and -(-(K // 32) // 16) >= 6 * ns
+
+
 def test_wide_ldy(qmm):
     """Output row stride > N: the columns past N stay untouched."""
     N, K, M, ldy = 27000, 1024, 16, 27008
