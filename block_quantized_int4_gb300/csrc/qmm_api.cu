@@ -529,6 +529,40 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
     return rows_launch<8, X_Q8>(di, a, false, st);
 }
 
+qmm_status qmm_gemm_workspace_size(int64_t K, int64_t M, size_t* bytes) {
+    if (!bytes || M < 0) return QMM_ERR_ARG;
+    if (!valid_k(K)) return QMM_ERR_SHAPE;
+    *bytes = gemm_prep_bytes(K, M);
+    return QMM_OK;
+}
+
+qmm_status qmm_gemm_q4_0_q8_0_ws(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,
+                                 const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+    // qmm_gemm_q4_0_q8_0's checks, in its order, then the workspace's
+    if (N < 0 || M < 0 || ldy < N) return QMM_ERR_ARG;
+    if (!valid_k(K) || N == 0 || M == 0 || M > 65535 * 8) return QMM_ERR_SHAPE;
+    if (!w_qs || !w_d || !xq || !xd || !y) return QMM_ERR_ARG;
+    if (!aligned(w_qs, 16) || !aligned(w_d, 2) || !aligned(xq, 16) || !aligned(xd, 2) || !aligned(y, 4))
+        return QMM_ERR_ALIGN;
+    const size_t need = gemm_prep_bytes(K, M);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 128))) return QMM_ERR_WORKSPACE;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    // The prepared path where qmm_gemm_q4_0_q8_0 would take the 16-warp
+    // layout (same kernel choice, same results bit for bit); elsewhere the
+    // workspace is not used.
+    const int pick = g_gemm_kernel.load();
+    if (need > 0 && M >= 3 && (pick == QMM_GEMM_KERNEL_AUTO || pick == QMM_GEMM_KERNEL_MMA) && aligned(xd, 16) &&
+        gemm_mma_eligible(N, K, M, w_qs, w_d, xq, xd)) {
+        const WidePlan p = gemm_wide_plan(N, K, M, di->sms);
+        if (p.rpc > 0)
+            return gemm_prep_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, p, workspace, di->smem_optin, di->err,
+                                    S(stream));
+    }
+    return qmm_gemm_q4_0_q8_0(w_qs, w_d, N, K, M, xq, xd, y, ldy, stream);
+}
+
 }  // extern "C"
 
 namespace {

@@ -15,6 +15,27 @@ namespace qmm {
 bool gemm_mma_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const void* w_d, const void* xq,
                        const void* xd);
 
+// Row plan of the 16-warp layout: rpc rows per chunk (96, 128 or 192; 0
+// where the layout does not apply), nchunk chunks per CTA, nsplit CTAs per
+// cluster splitting K.
+struct WidePlan {
+    int rpc, nchunk, nsplit;
+};
+WidePlan gemm_wide_plan(int64_t N, int64_t K, int64_t M, int sms);
+
+// Bytes of the prepared activation of qmm_gemm_q4_0_q8_0_ws for K and M
+// (1..16 tokens; 0 otherwise): one record of fp16 B fragments, MMA seeds and
+// scaled d_x per 16 blocks of K.
+size_t gemm_prep_bytes(int64_t K, int64_t M);
+
+// The 16-warp layout with the activation prepared once into `workspace`
+// (>= gemm_prep_bytes, 128-byte aligned) by a launch ahead of the product;
+// plan p from gemm_wide_plan (rpc > 0), xd 16-byte aligned.  Both launches
+// use programmatic dependent launch.
+qmm_status gemm_prep_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,
+                            const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy, const WidePlan& p,
+                            void* workspace, int smem_optin, int* err, cudaStream_t st);
+
 // True when gemm_mma_launch (wide = true) takes the 16-warp layout for this
 // product: up to 16 tokens, xd 16-byte aligned, and a row plan at one CTA
 // per SM of 128 or 192 rows per CTA (ceil(N / sms) in 65..192), 96 rows for

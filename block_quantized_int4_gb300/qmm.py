@@ -65,6 +65,8 @@ SIGNATURES = {
     "qmm_gemv_q4_0_f32": [_P, _P, _I64, _I64, _P, _P, _P, _P, _P, _INT, _P],
     "qmm_gemv_fused": [_P, _P, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _INT, _P],
     "qmm_gemm_q4_0_q8_0": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P],
+    "qmm_gemm_workspace_size": [_I64, _I64, ctypes.POINTER(_SZ)],
+    "qmm_gemm_q4_0_q8_0_ws": [_P, _P, _I64, _I64, _I64, _P, _P, _P, _I64, _P, _SZ, _P],
     "qmm_debug_block_dots": [_P, _I64, _I64, _I64, _P, _P, _P],
     "qmm_debug_gemm_kernel": [_INT, ctypes.POINTER(_INT)],
     "qmm_debug_stream_wait": [ctypes.c_uint64, _INT, ctypes.POINTER(ctypes.c_uint64)],
@@ -178,6 +180,17 @@ def qmm_gemv_fused(w_qs, w_d, N, K, x, xq, xd, residual, y, yq, yd, flags=0, str
 def qmm_gemm_q4_0_q8_0(w_qs, w_d, N, K, M, xq, xd, y, ldy, stream=None):
     _check(_lib.qmm_gemm_q4_0_q8_0(_ptr(w_qs), _ptr(w_d), N, K, M, _ptr(xq), _ptr(xd), _ptr(y), ldy,
                                    _stream(stream)), "qmm_gemm_q4_0_q8_0")
+
+
+def qmm_gemm_workspace_size(K, M) -> int:
+    out = _SZ(0)
+    _check(_lib.qmm_gemm_workspace_size(K, M, ctypes.byref(out)), "qmm_gemm_workspace_size")
+    return out.value
+
+
+def qmm_gemm_q4_0_q8_0_ws(w_qs, w_d, N, K, M, xq, xd, y, ldy, workspace, workspace_bytes, stream=None):
+    _check(_lib.qmm_gemm_q4_0_q8_0_ws(_ptr(w_qs), _ptr(w_d), N, K, M, _ptr(xq), _ptr(xd), _ptr(y), ldy,
+                                      _ptr(workspace), workspace_bytes, _stream(stream)), "qmm_gemm_q4_0_q8_0_ws")
 
 
 GEMM_KERNEL_AUTO, GEMM_KERNEL_MMA, GEMM_KERNEL_TMEM, GEMM_KERNEL_STREAM, GEMM_KERNEL_MMA_GROUPS = 0, 1, 2, 3, 4
@@ -409,9 +422,15 @@ def gemv(qs, d, xq, xd, out=None):
     return y
 
 
-def gemm(qs, d, xq, xd, out=None):
+def gemm(qs, d, xq, xd, out=None, workspace=None):
+    """y = the GEMM of qmm_gemm_q4_0_q8_0; with `workspace` (a uint8 device
+    tensor of at least qmm_gemm_workspace_size(K, M) bytes) through
+    qmm_gemm_q4_0_q8_0_ws."""
     N, K = qs.shape[0], qs.shape[1] * 2
     M = xq.shape[0]
     y = out if out is not None else torch.empty(M, N, dtype=torch.float32, device=qs.device)
-    qmm_gemm_q4_0_q8_0(qs, d, N, K, M, xq, xd, y, y.stride(0))
+    if workspace is None:
+        qmm_gemm_q4_0_q8_0(qs, d, N, K, M, xq, xd, y, y.stride(0))
+    else:
+        qmm_gemm_q4_0_q8_0_ws(qs, d, N, K, M, xq, xd, y, y.stride(0), workspace, workspace.numel())
     return y

@@ -176,6 +176,30 @@ QMM_API qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, 
                               int64_t M, const int8_t* xq, const uint16_t* xd, float* y, int64_t ldy,
                               void* stream);
 
+/* Device workspace bytes of qmm_gemm_q4_0_q8_0_ws for K and M: for 1..16
+ * tokens one 9216 * ceil(M / 8)-byte record per 512 columns of K (rounded
+ * up); 0 otherwise.  QMM_ERR_ARG for a NULL bytes or M < 0, QMM_ERR_SHAPE
+ * for K <= 0 or K % 32 != 0. */
+QMM_API qmm_status qmm_gemm_workspace_size(int64_t K, int64_t M, size_t* bytes);
+
+/* qmm_gemm_q4_0_q8_0 with a caller-owned device workspace (at least
+ * qmm_gemm_workspace_size bytes, 128-byte aligned, contents irrelevant and
+ * overwritten; one call at a time per workspace).  Where the 16-warp
+ * warp-MMA layout applies (3..16 tokens, see qmm_debug_gemm_kernel; xd
+ * 16-byte aligned) a first launch forms the activation's MMA operand once
+ * for the whole call into the workspace, and every CTA of the product copies
+ * it from there instead of forming it itself; the results are those of
+ * qmm_gemm_q4_0_q8_0 bit for bit.  Elsewhere the workspace is not used and
+ * the call is qmm_gemm_q4_0_q8_0.  Host checks as qmm_gemm_q4_0_q8_0's, then
+ * QMM_ERR_WORKSPACE for a workspace that is NULL, smaller than required or
+ * misaligned (when the required size is not 0).  Both launches use
+ * programmatic dependent launch: the product's weights stream while the
+ * kernel before on `stream` finishes; xq and xd are read only after it has
+ * completed. */
+QMM_API qmm_status qmm_gemm_q4_0_q8_0_ws(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
+                                         int64_t M, const int8_t* xq, const uint16_t* xd, float* y,
+                                         int64_t ldy, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Which kernel qmm_gemm_q4_0_q8_0 uses for 2 or more tokens, process-wide,
  * for testing and timing the kernels on the same inputs:
  *  - QMM_GEMM_KERNEL_AUTO (the default): the fastest measured: the

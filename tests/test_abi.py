@@ -84,6 +84,35 @@ def test_workspace_rules(qmm):
     assert _call(qmm, "qmm_moe_gemv", A16, A16, 256, 64, 64, A16, 16, 8, A16, A16, 0, A16, None, n, None) == 8
 
 
+def test_gemm_workspace_size_and_rules(qmm):
+    """qmm_gemm_workspace_size: one record of 9216 * ceil(M / 8) bytes per 512
+    columns of K (rounded up) for 1..16 tokens, 0 otherwise; the workspace
+    entry checks the product's arguments first (same statuses as the plain
+    entry), then the workspace (NULL, too small, misaligned: QMM_ERR_WORKSPACE),
+    all before any device call."""
+    assert qmm.qmm_gemm_workspace_size(8192, 16) == 16 * 18432
+    assert qmm.qmm_gemm_workspace_size(8192, 8) == 16 * 9216
+    assert qmm.qmm_gemm_workspace_size(768, 9) == 2 * 18432    # a last half unit is a whole record
+    assert qmm.qmm_gemm_workspace_size(2048, 17) == 0
+    assert qmm.qmm_gemm_workspace_size(2048, 0) == 0
+    out = ctypes.c_size_t(0)
+    lib = qmm.library_handle()
+    assert lib.qmm_gemm_workspace_size(48, 4, ctypes.byref(out)) == 2
+    assert lib.qmm_gemm_workspace_size(64, -1, ctypes.byref(out)) == 1
+    assert lib.qmm_gemm_workspace_size(64, 4, None) == 1
+    A16 = 0x10000
+    n = qmm.qmm_gemm_workspace_size(8192, 16)
+    ws = lambda *a: _call(qmm, "qmm_gemm_q4_0_q8_0_ws", *a)  # noqa: E731
+    assert ws(A16, A16, -1, 8192, 16, A16, A16, A16, 64, A16, n, None) == 1       # as the plain entry
+    assert ws(A16, A16, 64, 48, 16, A16, A16, A16, 64, A16, n, None) == 2
+    assert ws(A16, A16 + 1, 64, 8192, 16, A16, A16, A16, 64, A16, n, None) == 3
+    assert ws(A16, A16, 64, 8192, 16, A16, A16, A16, 64, None, n, None) == 8      # no workspace
+    assert ws(A16, A16, 64, 8192, 16, A16, A16, A16, 64, A16, n - 16, None) == 8  # too small
+    assert ws(A16, A16, 64, 8192, 16, A16, A16, A16, 64, A16 + 64, n, None) == 8  # not 128-byte aligned
+    # no workspace needed (17 tokens): the plain entry's path, here without a device
+    assert ws(A16, A16, 64, 8192, 17, A16, A16, A16, 64, None, 0, None) == 4
+
+
 def test_static_scratch_limit_and_arguments(qmm):
     """qmm_moe_gemv_static checks its fixed scratch limit (256 KiB) on the
     host before touching a device."""

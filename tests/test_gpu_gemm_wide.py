@@ -201,3 +201,46 @@ def test_wide_ldy(qmm):
     ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
     assert_close(y[:, :N], ref, S, "wide ldy")
     assert torch.all(y[:, N:] == 7.0)
+
+
+# (N, K, M) through every plan of the 16-warp layout (one chunk of 96 / 128 /
+# 192 rows, several chunks, clusters splitting K) and one plan it does not take
+WS_CASES = [(27000, 2048, 16), (27000, 768, 9), (18000, 2048, 5), (13000, 2048, 12), (110000, 768, 16),
+            (128256, 512, 4), (8192, 28672, 16), (5000, 16640, 9), (2048, 28672, 3), (3000, 2048, 16)]
+
+
+@pytest.mark.parametrize("N,K,M", WS_CASES)
+def test_workspace_path_matches_staged_path(qmm, N, K, M):
+    """qmm_gemm_q4_0_q8_0_ws (the activation's MMA operand formed once into
+    the workspace, which starts out full of junk) gives the staged path's
+    results bit for bit; sampled rows also against the oracle."""
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + 3 * K + M)
+    qs, d = _planes(qmm, qw, dw)
+    xq, xd = _q8(qx, dx)
+    y0 = qmm.gemm(qs, d, xq, xd)
+    nbytes = qmm.qmm_gemm_workspace_size(K, M)
+    ws = torch.full((max(nbytes, 1),), 0xAB, dtype=torch.uint8, device=DEV)
+    y1 = qmm.gemm(qs, d, xq, xd, workspace=ws)
+    assert torch.equal(y0, y1)
+    rng = np.random.default_rng(N)
+    rows = np.unique(np.concatenate([np.arange(40), np.arange(N - 40, N), rng.integers(0, N, 400)]))
+    ref, S = O.matmul_int(qw, dw, qx, dx, rows=rows, nthreads=8)
+    assert_close(y1[:, torch.from_numpy(rows).to(DEV)], ref, S, f"workspace gemm {N}x{K} M={M}")
+    assert qmm.qmm_last_device_error() == 0
+
+
+def test_workspace_path_integer_grid_exact(qmm):
+    """d = 1 on both sides through the workspace path: exact integers."""
+    N, K, M = 27000, 8192, 16
+    rng = np.random.default_rng(7)
+    w = rng.integers(-7, 8, size=(N, K)).astype(np.float32)
+    w[:, 3::32] = -7  # every block's max |w| is 7: d = 1
+    x = rng.integers(-127, 128, size=(M, K)).astype(np.float32)
+    x[:, 9::32] = -127
+    qs, d = qmm.quantize_q4_0(torch.from_numpy(w).to(DEV))
+    xq, xd = qmm.quantize_q8_0(torch.from_numpy(x).to(DEV))
+    ws = torch.empty(qmm.qmm_gemm_workspace_size(K, M), dtype=torch.uint8, device=DEV)
+    y = qmm.gemm(qs, d, xq, xd, workspace=ws)
+    exact = (x.astype(np.float64) @ w.astype(np.float64).T).astype(np.float32)
+    assert np.array_equal(y.cpu().numpy(), exact)
+    assert qmm.qmm_last_device_error() == 0
