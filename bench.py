@@ -280,10 +280,14 @@ def _flush_l2(torch, buf):
 # ---------------------------------------------------------------------------- extras
 def bench_gemm_b16(qmm, torch, reps=20, dev="cuda", M=16):
     """Batch-M GEMM (16 by default; 2 = a one-draft speculative verify) on the
-    large dense FFN + lm_head shapes (TOPS = 2*M*N*K per second)."""
+    large dense FFN + lm_head shapes (TOPS = 2*M*N*K per second), through
+    qmm_gemm_q4_0_q8_0_ws."""
     mats = workloads.large_dense_matrices()
     sigma = workloads.LARGE_DENSE["sigma"]
     ws, xs, ys, ops, wbytes = [], [], [], 0, 0
+    # one workspace for the set: the calls run one after another on one stream
+    wsb = max(max(1, qmm.qmm_gemm_workspace_size(K, M)) for _, N, K in mats)
+    work = torch.empty(wsb, dtype=torch.uint8, device=dev)
     for i, (_, N, K) in enumerate(mats):
         w = workloads.weights(N, K, sigma=sigma, seed=0, index=100 + i, device=dev)
         ws.append((qmm.quantize_q4_0(w), N, K))
@@ -296,7 +300,7 @@ def bench_gemm_b16(qmm, torch, reps=20, dev="cuda", M=16):
 
     def run():
         for ((qs, d), N, K), (xq, xd), y in zip(ws, xs, ys):
-            qmm.qmm_gemm_q4_0_q8_0(qs, d, N, K, M, xq, xd, y, N)
+            qmm.qmm_gemm_q4_0_q8_0_ws(qs, d, N, K, M, xq, xd, y, N, work, wsb)
 
     g = _graph(torch, run)
     t = _time_graph(torch, g, reps, 3)
@@ -471,9 +475,9 @@ def run_case(qmm, torch, name, calls, dev="cuda"):
             (c["qkv"], c["hidden"], c["sigma"])
     elif name == "lm_head_8192":
         N, K, sigma = workloads.LARGE_DENSE["vocab"], workloads.LARGE_DENSE["hidden"], workloads.LARGE_DENSE["sigma"]
-    elif name in ("gemm_b16", "gemm_b64"):
+    elif name in ("gemm_b16", "gemm_b64", "gemm_b16_ws"):
         N, K, sigma = workloads.LARGE_DENSE["ffn"], workloads.LARGE_DENSE["hidden"], workloads.LARGE_DENSE["sigma"]
-        M = 16 if name == "gemm_b16" else 64
+        M = 64 if name == "gemm_b64" else 16
     elif name == "gemm_b16_dense":  # the batch-16 set of the default line: gate, up, down, lm_head
         return {"case": name, **bench_gemm_b16(qmm, torch, reps=max(calls, 3))}
     elif name == "moe_T16":
@@ -508,6 +512,9 @@ def run_case(qmm, torch, name, calls, dev="cuda"):
         op = lambda: qmm.qmm_gemv_fused_op(o1, qmm.CHAIN)  # noqa: E731
     elif M == 1:
         op = lambda: qmm.qmm_gemv_q4_0_q8_0(qs, d, N, K, xq, xd, y)  # noqa: E731
+    elif name == "gemm_b16_ws":  # the workspace entry: activation operand prepared once per call
+        work = torch.empty(qmm.qmm_gemm_workspace_size(K, M), dtype=torch.uint8, device=dev)
+        op = lambda: qmm.qmm_gemm_q4_0_q8_0_ws(qs, d, N, K, M, xq, xd, y, N, work, work.numel())  # noqa: E731
     else:
         op = lambda: qmm.qmm_gemm_q4_0_q8_0(qs, d, N, K, M, xq, xd, y, N)  # noqa: E731
     ts = _time_calls(torch, op, calls)
@@ -617,6 +624,9 @@ def product_us(qmm, torch, N, K, M, sigma, fused_f32=False, dev="cuda"):
     x = workloads.activations(M, K, seed=0, device=dev)
     xq, xd = qmm.quantize_q8_0(x)
     y = torch.empty(M, N, device=dev)
+    # the small-batch GEMM through its workspace entry (the activation operand
+    # formed once per call where the 16-warp layout applies)
+    ws = torch.empty(max(1, qmm.qmm_gemm_workspace_size(K, M)), dtype=torch.uint8, device=dev)
 
     def make():
         q2, d2 = qs.clone(), d.clone()
@@ -624,7 +634,7 @@ def product_us(qmm, torch, N, K, M, sigma, fused_f32=False, dev="cuda"):
             return lambda: qmm.qmm_gemv_fused(q2, d2, N, K, x[0], None, None, None, y[0], None, None)
         if M == 1:
             return lambda: qmm.qmm_gemv_q4_0_q8_0(q2, d2, N, K, xq[0], xd[0], y[0])
-        return lambda: qmm.qmm_gemm_q4_0_q8_0(q2, d2, N, K, M, xq, xd, y, N)
+        return lambda: qmm.qmm_gemm_q4_0_q8_0_ws(q2, d2, N, K, M, xq, xd, y, N, ws, ws.numel())
 
     us = _rotated_us(torch, make, workloads.q4_0_bytes(N, K))
     del qs, d
@@ -841,7 +851,7 @@ def main():
                     help="time every workload of the five configurations instead (one JSON line each)")
     ap.add_argument("--case", default=None,
                     help="time one kernel instead: decode_gateup, decode_qkv_norm, decode_pdl, lm_head_8192, "
-                         "gemm_b16, gemm_b16_dense, "
+                         "gemm_b16, gemm_b16_ws, gemm_b16_dense, "
                          "gemm_b64, moe_T16, moe_layer_T1, moe_layer_T16, moe_store")
     ap.add_argument("--gemm-kernel", default="auto", choices=["auto", "mma", "tmem", "stream"],
                     help="small-batch GEMM kernel (qmm_debug_gemm_kernel): automatic choice, warp MMA, tcgen05 or "
