@@ -455,9 +455,13 @@ cudaError_t launch_ex(Kern kernel, dim3 grid, int threads, size_t smem, cudaStre
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Everything the product needs is checked and encoded first; only then are
+// the preparation launch and the product launched, so a call that fails
+// before its launches enqueues nothing.
 template <int NT, int WT, int KPB, int MODE>
-qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, float* y, int64_t ldy,
-                  const uint8_t* rec, int nchunk, int nsplit, int smem_optin, int* err, cudaStream_t st) {
+qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, const int8_t* xq,
+                  const uint16_t* xd, float* y, int64_t ldy, uint8_t* rec, int nchunk, int nsplit, int smem_optin,
+                  int* err, cudaStream_t st) {
     using SH = Shape<NT, WT, KPB>;
     if ((MODE == MULTI) != (nchunk > 1) || (MODE == SPLIT) != (nsplit > 1) || nsplit > 8) return QMM_ERR_SHAPE;
     if (nchunk > 1 && SH::RED > SH::STAGE) return QMM_ERR_SHAPE;
@@ -491,6 +495,12 @@ qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K
     if (!allow_smem(kern, smem_optin)) return QMM_ERR_SHAPE;
     const int64_t chunks = (N + SH::RPC - 1) / SH::RPC;
     const dim3 grid((unsigned)((chunks + nchunk - 1) / nchunk * nsplit), 1);
+    const int64_t units_all = (B + UKB - 1) / UKB;
+    if (launch_ex(prep_kernel<NT>, dim3((unsigned)units_all), UKB * 16 * NT, 0, st, 1, xq, xd, K, M, rec) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return QMM_ERR_CUDA;
+    }
     if (launch_ex(kern, grid, THREADS, (size_t)smem, st, nsplit, mq, md, a) != cudaSuccess) {
         cudaGetLastError();
         return QMM_ERR_CUDA;
@@ -502,22 +512,17 @@ template <int NT>
 qmm_status launch_nt(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, const int8_t* xq,
                      const uint16_t* xd, float* y, int64_t ldy, const WidePlan& p, uint8_t* ws, int smem_optin,
                      int* err, cudaStream_t st) {
-    const int64_t units = (K / QK + UKB - 1) / UKB;
-    if (launch_ex(prep_kernel<NT>, dim3((unsigned)units), UKB * 16 * NT, 0, st, 1, xq, xd, K, M, ws) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return QMM_ERR_CUDA;
-    }
     const int nc = p.nchunk, ns = p.nsplit;
     switch (p.rpc) {
         case 128:
-            return ns > 1   ? launch<NT, 2, 4, SPLIT>(w_qs, w_d, N, K, M, y, ldy, ws, 1, ns, smem_optin, err, st)
-                   : nc > 1 ? launch<NT, 2, 4, MULTI>(w_qs, w_d, N, K, M, y, ldy, ws, nc, 1, smem_optin, err, st)
-                            : launch<NT, 2, 4, ONE>(w_qs, w_d, N, K, M, y, ldy, ws, 1, 1, smem_optin, err, st);
+            return ns > 1 ? launch<NT, 2, 4, SPLIT>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, ns, smem_optin, err, st)
+                   : nc > 1
+                       ? launch<NT, 2, 4, MULTI>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, nc, 1, smem_optin, err, st)
+                       : launch<NT, 2, 4, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, 1, smem_optin, err, st);
         case 192:
-            return nc > 1 ? launch<NT, 3, 4, MULTI>(w_qs, w_d, N, K, M, y, ldy, ws, nc, 1, smem_optin, err, st)
-                          : launch<NT, 3, 4, ONE>(w_qs, w_d, N, K, M, y, ldy, ws, 1, 1, smem_optin, err, st);
-        case 96: return launch<NT, 3, 2, ONE>(w_qs, w_d, N, K, M, y, ldy, ws, 1, 1, smem_optin, err, st);
+            return nc > 1 ? launch<NT, 3, 4, MULTI>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, nc, 1, smem_optin, err, st)
+                          : launch<NT, 3, 4, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, 1, smem_optin, err, st);
+        case 96: return launch<NT, 3, 2, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, 1, smem_optin, err, st);
         default: return QMM_ERR_SHAPE;
     }
 }

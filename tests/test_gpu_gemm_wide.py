@@ -244,3 +244,49 @@ def test_workspace_path_integer_grid_exact(qmm):
     exact = (x.astype(np.float64) @ w.astype(np.float64).T).astype(np.float32)
     assert np.array_equal(y.cpu().numpy(), exact)
     assert qmm.qmm_last_device_error() == 0
+
+
+def test_workspace_entry_edges(qmm):
+    """The workspace entry with ldy > N (columns past N untouched); with 17
+    tokens (no workspace needed: the plain entry's path); with xd only 2-byte
+    aligned (the 16-warp layout does not apply: same results as the plain
+    entry); and one workspace reused by back-to-back calls of different K on
+    one stream (each call's preparation waits for the call before)."""
+    N, K = 27000, 1024
+    # ldy > N
+    qw, dw, qx, dx = _rand_codes(N, 16, K, seed=21)
+    qs, d = _planes(qmm, qw, dw)
+    xq, xd = _q8(qx, dx)
+    ws = torch.empty(qmm.qmm_gemm_workspace_size(K, 16), dtype=torch.uint8, device=DEV)
+    ldy = N + 40
+    y = torch.full((16, ldy), 7.0, device=DEV)
+    qmm.qmm_gemm_q4_0_q8_0_ws(qs, d, N, K, 16, xq, xd, y, ldy, ws, ws.numel())
+    assert torch.equal(y[:, :N], qmm.gemm(qs, d, xq, xd)) and torch.all(y[:, N:] == 7.0)
+    # 17 tokens: no workspace
+    assert qmm.qmm_gemm_workspace_size(K, 17) == 0
+    qw7, dw7, qx7, dx7 = _rand_codes(N, 17, K, seed=22)
+    xq7, xd7 = _q8(qx7, dx7)
+    y7 = torch.empty(17, N, device=DEV)
+    qmm.qmm_gemm_q4_0_q8_0_ws(qs, d, N, K, 17, xq7, xd7, y7, N, None, 0)
+    assert torch.equal(y7, qmm.gemm(qs, d, xq7, xd7))
+    # xd 2-byte aligned only
+    xd_buf = torch.zeros(16 * (K // 32) + 8, dtype=torch.int16, device=DEV)
+    xd_odd = xd_buf[1:1 + 16 * (K // 32)].view(16, K // 32)
+    xd_odd.copy_(xd)
+    assert xd_odd.data_ptr() % 16 == 2
+    y2 = torch.empty(16, N, device=DEV)
+    qmm.qmm_gemm_q4_0_q8_0_ws(qs, d, N, K, 16, xq, xd_odd, y2, N, ws, ws.numel())
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y2, ref, S, "workspace entry, xd 2-byte aligned")
+    # one workspace, calls of different K back to back
+    K2 = 4096
+    qw2, dw2, qx2, dx2 = _rand_codes(N, 16, K2, seed=23)
+    qs2, d2 = _planes(qmm, qw2, dw2)
+    xq2, xd2 = _q8(qx2, dx2)
+    big = torch.empty(qmm.qmm_gemm_workspace_size(K2, 16), dtype=torch.uint8, device=DEV)
+    ya = torch.empty(16, N, device=DEV)
+    yb = torch.empty(16, N, device=DEV)
+    qmm.qmm_gemm_q4_0_q8_0_ws(qs2, d2, N, K2, 16, xq2, xd2, ya, N, big, big.numel())
+    qmm.qmm_gemm_q4_0_q8_0_ws(qs, d, N, K, 16, xq, xd, yb, N, big, big.numel())
+    assert torch.equal(ya, qmm.gemm(qs2, d2, xq2, xd2)) and torch.equal(yb, qmm.gemm(qs, d, xq, xd))
+    assert qmm.qmm_last_device_error() == 0
