@@ -19,7 +19,13 @@
 // form) and the per-block rescale is applied to the accumulator fragment in
 // registers.
 //
-// Work layout:
+// Two layouts live here: the row-group kernel (gemm_mma_kernel, any token
+// count) described next, and the 16-warp layout for up to 16 tokens
+// (gemm_wide_kernel, further down), which qmm_gemm_q4_0_q8_0 takes where its
+// row plan qualifies.  The workspace entry's variant of the 16-warp layout is
+// in qmm_gemm_prep.cu.
+//
+// Row-group kernel, work layout:
 //  - A CTA owns rows_per_cta consecutive weight rows (a multiple of the
 //    group height R = 16, 32, 48 or 64), walked group by group; each group is
 //    streamed in units of UKB blocks by a producer warp: one 2D TMA copy of
@@ -497,7 +503,10 @@ qmm_status launch_nt(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_
 //    is computed, handed over through mbarriers (two buffers);
 //  - no producer warp: the hand-over keeps every warp within one unit of
 //    the others, so once the last warp has finished unit u - 1 its stage is
-//    free, and lane 0 of warp 0 refills it with unit u - 1 + S.
+//    free, and lanes 0 of warps 0..3 refill it with unit u - 1 + S (one of
+//    the unit's four copies each);
+//  - modes: one chunk of rows per CTA, several (large N), or a cluster of
+//    CTAs splitting K over one chunk (small N, long K); see the kernel.
 namespace widek {
 
 constexpr int CW = 16;
