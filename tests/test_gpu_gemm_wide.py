@@ -204,9 +204,9 @@ def test_wide_ldy(qmm):
 
 
 # (N, K, M) through every plan of the 16-warp layout (one chunk of 96 / 128 /
-# 192 rows, several chunks, clusters splitting K) and one plan it does not take
+# 192 rows, several chunks, clusters splitting K), which both entries take
 WS_CASES = [(27000, 2048, 16), (27000, 768, 9), (18000, 2048, 5), (13000, 2048, 12), (110000, 768, 16),
-            (128256, 512, 4), (8192, 28672, 16), (5000, 16640, 9), (2048, 28672, 3), (3000, 2048, 16)]
+            (128256, 512, 4), (8192, 28672, 16), (5000, 16640, 9), (2048, 28672, 3)]
 
 
 @pytest.mark.parametrize("N,K,M", WS_CASES)
@@ -289,4 +289,23 @@ def test_workspace_entry_edges(qmm):
     qmm.qmm_gemm_q4_0_q8_0_ws(qs2, d2, N, K2, 16, xq2, xd2, ya, N, big, big.numel())
     qmm.qmm_gemm_q4_0_q8_0_ws(qs, d, N, K, 16, xq, xd, yb, N, big, big.numel())
     assert torch.equal(ya, qmm.gemm(qs2, d2, xq2, xd2)) and torch.equal(yb, qmm.gemm(qs, d, xq, xd))
+    assert qmm.qmm_last_device_error() == 0
+
+
+@pytest.mark.parametrize("N,K,M", [(5632, 2048, 16), (2048, 5632, 9), (2560, 2048, 8), (1000, 8192, 5),
+                                   (300, 28672, 12), (4096, 14336, 7), (3000, 2048, 16)])
+def test_workspace_small_products(qmm, N, K, M):
+    """Small products through the workspace entry (the 16-warp layout does not
+    apply to most of them: the entry falls back to the plain one, which must
+    then ignore the workspace; the two long-K shapes split K over clusters)
+    against the oracle, all rows."""
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + K + M + 1)
+    qs, d = _planes(qmm, qw, dw)
+    xq, xd = _q8(qx, dx)
+    ws = torch.full((qmm.qmm_gemm_workspace_size(K, M),), 0x5A, dtype=torch.uint8, device=DEV)
+    y = qmm.gemm(qs, d, xq, xd, workspace=ws)
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y, ref, S, f"workspace gemm small N {N}x{K} M={M}")
+    y2 = qmm.gemm(qs, d, xq, xd, workspace=ws)
+    assert torch.equal(y, y2)
     assert qmm.qmm_last_device_error() == 0
