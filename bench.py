@@ -903,6 +903,13 @@ def main():
         g.replay()
         logits_host.copy_(dec.logits, non_blocking=True)
 
+    # the same with the step's 89 C-ABI calls issued from Python every step
+    # (host-side validation, ctypes and launch cost included; no graph)
+    def e2e_eager_step():
+        dec.x_in.copy_(x_host, non_blocking=True)
+        dec.step()
+        logits_host.copy_(dec.logits, non_blocking=True)
+
     for _ in range(max(3, args.warmup)):
         g.replay()
     torch.cuda.synchronize()
@@ -923,12 +930,23 @@ def main():
         e1.record(st)
         torch.cuda.synchronize()
         t_e2e = e0.elapsed_time(e1) / 1e3
+        # eager e2e leg
+        for _ in range(3):
+            e2e_eager_step()
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(args.steps):
+            e2e_eager_step()
+        e1.record(st)
+        torch.cuda.synchronize()
+        t_eager = e0.elapsed_time(e1) / 1e3
     if ws > 1:
-        t, t_e2e = max_over_ranks(torch, [t, t_e2e], "cuda")
+        t, t_e2e, t_eager = max_over_ranks(torch, [t, t_e2e, t_eager], "cuda")
 
     per = t / args.steps
     value = whole_job_gbs(ws, dec.weight_bytes, args.steps, t)
     e2e_value = whole_job_gbs(ws, dec.weight_bytes, args.steps, t_e2e)
+    eager_value = whole_job_gbs(ws, dec.weight_bytes, args.steps, t_eager)
     peak, peak_kind = _peaks()
     achieved = dec.algo_bytes / per / 1e9
     extras = {}
@@ -974,6 +992,9 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": dec.H * 4,
                     "d2h_bytes_per_step": dec.V * 4},
+            "e2e_eager": {"value": round(eager_value, 1), "unit": "GB/s", "ms_per_step": round(t_eager / args.steps * 1e3, 4),
+                          "h2d_bytes_per_step": dec.H * 4, "d2h_bytes_per_step": dec.V * 4,
+                          "how": "the 89 qmm_gemv_fused_op calls issued from Python (ctypes) every step, no graph"},
             "gpu_launches": dec.launches_per_step * args.steps,
             "clocks": clk.summary(),
             "also": extras,
