@@ -588,17 +588,8 @@ qmm_status validate_op(const qmm_gemv_op& o) {
     return QMM_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-qmm_status qmm_gemv_fused_op(const qmm_gemv_op* op, int flags, void* stream) {
-    if (!op || (flags & ~QMM_CHAIN)) return QMM_ERR_ARG;
-    const qmm_gemv_op& o = *op;
-    const qmm_status v = validate_op(o);
-    if (v != QMM_OK) return v;
-    const DevInfo* di = device_info();
-    if (!di) return QMM_ERR_DEVICE;
+// One checked op as one launch of the streaming kernel.
+qmm_status launch_op(const qmm_gemv_op& o, int flags, const DevInfo* di, void* stream) {
     const bool pairs = o.flags & QMM_Y_SWIGLU_PAIRS, qout = o.yq != nullptr;
     StreamArgs a = {};
     a.N = o.N;
@@ -623,6 +614,35 @@ qmm_status qmm_gemv_fused_op(const qmm_gemv_op* op, int flags, void* stream) {
     cudaStream_t st = S(stream);
     return o.x ? fused_dispatch<X_F32>(di, o.w_qs, o.w_d, a, pairs, qout, pdl, st)
                : fused_dispatch<X_Q8>(di, o.w_qs, o.w_d, a, pairs, qout, pdl, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+qmm_status qmm_gemv_fused_op(const qmm_gemv_op* op, int flags, void* stream) {
+    if (!op || (flags & ~QMM_CHAIN)) return QMM_ERR_ARG;
+    const qmm_status v = validate_op(*op);
+    if (v != QMM_OK) return v;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    return launch_op(*op, flags, di, stream);
+}
+
+qmm_status qmm_gemv_fused_ops(const qmm_gemv_op* ops, int32_t n, int flags, void* stream) {
+    if (n < 0 || (n > 0 && !ops) || (flags & ~QMM_CHAIN)) return QMM_ERR_ARG;
+    for (int32_t i = 0; i < n; ++i) {
+        const qmm_status v = validate_op(ops[i]);
+        if (v != QMM_OK) return v;
+    }
+    if (n == 0) return QMM_OK;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    for (int32_t i = 0; i < n; ++i) {
+        const qmm_status s = launch_op(ops[i], flags, di, stream);
+        if (s != QMM_OK) return s;
+    }
+    return QMM_OK;
 }
 
 qmm_status qmm_debug_gemm_kernel(int kernel, int* previous) {

@@ -71,6 +71,7 @@ SIGNATURES = {
     "qmm_debug_gemm_kernel": [_INT, ctypes.POINTER(_INT)],
     "qmm_debug_stream_wait": [ctypes.c_uint64, _INT, ctypes.POINTER(ctypes.c_uint64)],
     "qmm_gemv_fused_op": [ctypes.POINTER(GemvOp), _INT, _P],
+    "qmm_gemv_fused_ops": [ctypes.POINTER(GemvOp), _I32, _INT, _P],
     "qmm_moe_workspace_size": [_I32, _I32, _I32, ctypes.POINTER(_SZ)],
     "qmm_moe_gemv": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P, _SZ, _P],
     "qmm_moe_gemv_static": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P],
@@ -226,6 +227,15 @@ def gemv_op(w_qs, w_d, N, K, x=None, xq=None, xd=None, residual=None, y=None, yq
 
 def qmm_gemv_fused_op(op, flags=0, stream=None):
     _check(_lib.qmm_gemv_fused_op(ctypes.byref(op), int(flags), _stream(stream)), "qmm_gemv_fused_op")
+
+
+def gemv_op_array(ops):
+    """A contiguous qmm_gemv_op array (for qmm_gemv_fused_ops) from GemvOp structs."""
+    return (GemvOp * len(ops))(*ops)
+
+
+def qmm_gemv_fused_ops(op_array, n, flags=0, stream=None):
+    _check(_lib.qmm_gemv_fused_ops(op_array, int(n), int(flags), _stream(stream)), "qmm_gemv_fused_ops")
 
 
 def qmm_moe_workspace_size(E, T, k) -> int:

@@ -285,6 +285,13 @@ typedef struct qmm_gemv_op {
  * QMM_CHAIN (programmatic dependent launch, as for qmm_gemv_q4_0_f32). */
 QMM_API qmm_status qmm_gemv_fused_op(const qmm_gemv_op* op, int flags, void* stream);
 
+/* A chain of ops in one call: ops[0..n) each as qmm_gemv_fused_op(&ops[i],
+ * flags, stream), in order.  Every op is checked before anything is
+ * launched; the first bad op's status is returned and nothing is launched.
+ * A launch that fails returns QMM_ERR_CUDA after the launches before it.
+ * n == 0 is a no-op; ops host memory, read during the call only. */
+QMM_API qmm_status qmm_gemv_fused_ops(const qmm_gemv_op* ops, int32_t n, int flags, void* stream);
+
 /* ---------------------------------------------------------------------
  * Weight-format variants of the batch-1 product
  * ------------------------------------------------------------------- */

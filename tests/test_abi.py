@@ -151,6 +151,26 @@ def test_fused_op_validation(qmm):
     assert run(dict(good, flags=2, residual=A16)) == 1  # pairs with a residual
 
 
+def test_fused_ops_chain_validation(qmm):
+    """qmm_gemv_fused_ops checks every op before launching any: the first bad
+    op's status; bad counts, a NULL array and unknown flags are QMM_ERR_ARG;
+    an empty chain is a no-op; a valid chain reaches the device check."""
+    A16 = 0x10000
+    good = qmm.gemv_op(A16, A16, 64, 256, xq=A16, xd=A16, yq=A16, yd=A16)
+    bad_k = qmm.gemv_op(A16, A16, 64, 288, xq=A16, xd=A16, yq=A16, yd=A16)
+    bad_al = qmm.gemv_op(A16, A16 + 2, 64, 256, xq=A16, xd=A16, yq=A16, yd=A16)
+    lib = qmm.library_handle()
+    arr = qmm.gemv_op_array([good, good, bad_k, bad_al])
+    assert lib.qmm_gemv_fused_ops(arr, 4, 0, None) == 2      # op 2 is the first bad one
+    arr2 = qmm.gemv_op_array([good, bad_al, bad_k])
+    assert lib.qmm_gemv_fused_ops(arr2, 3, 0, None) == 3
+    assert lib.qmm_gemv_fused_ops(arr, -1, 0, None) == 1
+    assert lib.qmm_gemv_fused_ops(None, 2, 0, None) == 1
+    assert lib.qmm_gemv_fused_ops(arr, 2, 1, None) == 1      # only QMM_CHAIN as a call flag
+    assert lib.qmm_gemv_fused_ops(None, 0, 0, None) == 0
+    assert lib.qmm_gemv_fused_ops(arr, 2, 4, None) == 4      # valid ops: no device here
+
+
 def test_router_and_pregrouped_validation(qmm):
     """qmm_moe_router_topk: 1 <= k <= min(E, 64), E <= 1024, workspace size
     and alignment; qmm_moe_gemv_pregrouped: the workspace rules of

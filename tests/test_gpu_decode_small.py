@@ -110,6 +110,26 @@ def test_chained_launches_from_a_graph_equal_plain_launches():
     assert qmm.qmm_last_device_error() == 0
 
 
+def test_op_chain_entry_equals_plain_launches():
+    """qmm_gemv_fused_ops (the whole op list in one call, chained and plain)
+    gives exactly the outputs of one qmm_gemv_fused_op call per op."""
+    qmm = lib()
+    qmm.qmm_last_device_error()
+    dec = MiniDecode(qmm)
+    dec.run_one_by_one()
+    torch.cuda.synchronize()
+    ref = dec.snapshot()
+    ops = dec.ops()
+    arr = qmm.gemv_op_array(ops)
+    for flags in (0, qmm.CHAIN):
+        dec.reset_outputs()
+        qmm.qmm_gemv_fused_ops(arr, len(ops), flags)
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(zip(dec.snapshot(), ref)):
+            assert torch.equal(a, b), f"output {i} differs from one call per op (flags {flags})"
+    assert qmm.qmm_last_device_error() == 0
+
+
 def _planes_to_oracle(qs, d, N, K):
     blocks = np.zeros((N, K // 32, 18), np.uint8)
     blocks[..., :2] = u16(d).reshape(N, K // 32, 1).view(np.uint8)
