@@ -127,6 +127,16 @@ def test_op_chain_entry_equals_plain_launches():
         torch.cuda.synchronize()
         for i, (a, b) in enumerate(zip(dec.snapshot(), ref)):
             assert torch.equal(a, b), f"output {i} differs from one call per op (flags {flags})"
+    # a bad last op: its status, and nothing of the chain launched
+    bad = qmm.gemv_op(ops[0].w_qs, ops[0].w_d, 64, 288, xq=dec.a0[0], xd=dec.a0[1], y=dec.logits)
+    arr_bad = qmm.gemv_op_array(ops + [bad])
+    dec.reset_outputs()
+    torch.cuda.synchronize()
+    with pytest.raises(qmm.QmmError) as ei:
+        qmm.qmm_gemv_fused_ops(arr_bad, len(ops) + 1, qmm.CHAIN)
+    assert ei.value.status == 2
+    torch.cuda.synchronize()
+    assert all(torch.count_nonzero(t) == 0 for t in dec.buffers())
     assert qmm.qmm_last_device_error() == 0
 
 
