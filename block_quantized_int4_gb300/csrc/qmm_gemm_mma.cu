@@ -1108,7 +1108,7 @@ bool plan_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
 
 WidePlan gemm_wide_plan(int64_t N, int64_t K, int64_t M, int sms) {
     const mmak::widek::Plan p = mmak::widek::plan_rows(N, K, M, sms);
-    return WidePlan{p.rpc, p.nchunk, p.nsplit};
+    return WidePlan{p.rpc, p.nchunk, p.nsplit, sms};
 }
 
 bool gemm_wide_planned(int64_t N, int64_t K, int64_t M, const void* xd, int sms) {

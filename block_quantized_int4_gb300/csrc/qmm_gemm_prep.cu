@@ -37,7 +37,16 @@ constexpr int CW = 16;
 constexpr int THREADS = CW * 32;
 constexpr int UKB = 16;  // blocks per unit
 constexpr int MAX_STAGES = 8;
-enum Mode { ONE = 0, MULTI = 1, SPLIT = 2 };
+// Modes: ONE chunk of rows per CTA; MULTI: nchunk chunks per CTA; SPLIT: a
+// cluster of CTAs splitting one chunk's K; EVEN: the (chunk, unit) sequence
+// of the whole product cut into equal runs, one per CTA.  A chunk cut between
+// two CTAs: the later CTA meets the chunk's end at the start of its run, so
+// it stores its partial sums into y and raises the chunk's flag in the
+// workspace; the earlier CTA meets the chunk's start at the end of its run,
+// long after, adds those partial sums to its own (one fixed order) and
+// writes y.
+enum Mode { ONE = 0, MULTI = 1, SPLIT = 2, EVEN = 3 };
+constexpr int MAX_FLAGS = 4096;  // chunks an EVEN product may have (one flag word each)
 
 // One unit's prepared record for NT token tiles (TK = 8 NT token rows):
 //   fragments [16 blocks][NT tiles][32 lanes] x 16 bytes: lane (g, t) of
@@ -58,10 +67,12 @@ struct Rec {
 template <int NT>
 __global__ void __launch_bounds__(UKB * 16 * NT) prep_kernel(const int8_t* __restrict__ xq,
                                                              const uint16_t* __restrict__ xd, int64_t K, int64_t M,
-                                                             uint8_t* __restrict__ rec) {
+                                                             uint8_t* __restrict__ rec, int* __restrict__ flags) {
     constexpr int TK = 8 * NT;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");  // the codes come from the kernel before
+    if (blockIdx.x == 0)  // the EVEN mode's chunk flags start lowered
+        for (int i = threadIdx.x; i < MAX_FLAGS; i += blockDim.x) flags[i] = 0;
     const int B = (int)(K / QK);
     const int tid = threadIdx.x, sh = tid & 1, tok = (tid >> 1) & (TK - 1), bl = tid / (2 * TK);
     const int b = blockIdx.x * UKB + bl;
@@ -114,6 +125,8 @@ struct Args {
     int64_t N, K, M, ldy;
     float* y;
     const uint8_t* rec;  // prepared records, one per unit of K
+    int* flags;          // EVEN: one word per chunk, lowered by the preparation launch
+    int64_t units_total;  // EVEN: chunks x units per chunk
     int nchunk, nstages;
     int* err;
 };
@@ -123,7 +136,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     gemm_prep_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_d, Args a) {
     using SH = Shape<NT, WT, KPB>;
     constexpr int KP = SH::KP, RPC = SH::RPC, QB = SH::QB;
-    constexpr bool multi = MODE == MULTI, split = MODE == SPLIT;
+    constexpr bool multi = MODE == MULTI, split = MODE == SPLIT, even = MODE == EVEN;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* full = reinterpret_cast<uint64_t*>(base);                    // [MAX_STAGES] a unit's bytes landed
@@ -142,10 +155,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         u_lo = min(nunits, (int)rank * per);
         nunits = min(nunits, u_lo + per) - u_lo;
     }
-    const int64_t chunk0 = multi ? (int64_t)blockIdx.x * a.nchunk : split ? (int64_t)(blockIdx.x / nsplit)
-                                                                         : (int64_t)blockIdx.x;
+    // EVEN: this CTA's run [g0, g1) of the product's (chunk, unit) sequence
+    const int64_t g0 = even ? a.units_total * blockIdx.x / gridDim.x : 0;
+    const int64_t g1 = even ? a.units_total * (blockIdx.x + 1) / gridDim.x : 0;
+    const int64_t chunk0 = even    ? g0 / nunits
+                           : multi ? (int64_t)blockIdx.x * a.nchunk
+                           : split ? (int64_t)(blockIdx.x / nsplit)
+                                   : (int64_t)blockIdx.x;
+    const int u0 = even ? (int)(g0 - chunk0 * nunits) : 0;  // first unit, inside its chunk
     const int nck = multi ? (int)min((int64_t)a.nchunk, (a.N + RPC - 1) / RPC - chunk0) : 1;
-    const int V = multi ? nck * nunits : nunits;
+    const int V = even ? (int)(g1 - g0) : multi ? nck * nunits : nunits;
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -164,9 +183,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     // are evicted first from L2; the records, read by every CTA, are not.
     const uint64_t pol = l2_evict_first_policy();
     auto issue = [&](int v, bool weights, bool acts) {
-        const int ck = multi ? v / nunits : 0;
-        const int s = v % S, u = u_lo + v - ck * nunits, b0 = u * UKB;
-        const int row_begin = (int)((chunk0 + ck) * RPC);
+        int64_t c;
+        int u;
+        if constexpr (even) {
+            const int64_t g = g0 + v;
+            c = g / nunits;
+            u = (int)(g - c * nunits);
+        } else {
+            const int ck = multi ? v / nunits : 0;
+            c = chunk0 + ck;
+            u = u_lo + v - ck * nunits;
+        }
+        const int s = v % S, b0 = u * UKB;
+        const int row_begin = (int)(c * RPC);
         uint8_t* st = ring + (size_t)s * SH::STAGE;
         if (lane == 0 && weights) {
             mbar_arrive_expect_tx(&full[s], (uint32_t)SH::TX);
@@ -266,7 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     };
 
-    int u = 0, ck = 0;  // unit inside the chunk, chunk of this CTA
+    int u = u0, ck = 0;  // unit inside the chunk, chunk of this CTA (from chunk0)
     for (int v = 0; v < V; ++v) {
         const int s = v % S;
         if (!failed && !wait_phase(&full[s], (v / S) & 1, abort_flag)) {
@@ -341,7 +370,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // v + S (at a chunk's end the refill waits for the chunk's sums, which
         // go through this stage).  The counter only grows: after the n-th use
         // of stage s the last arrival sees (n + 1) * 16 - 1.
-        const bool chunk_end = multi && u == nunits - 1;
+        const bool chunk_end = (multi && u == nunits - 1) || (even && (u == nunits - 1 || v == V - 1));
         __syncwarp();
         unsigned prev = 0;
         if (lane == 0) {
@@ -354,12 +383,52 @@ __global__ void __launch_bounds__(THREADS, 1)
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             issue(v + S, true, true);
         }
-        if constexpr (multi) {
+        if constexpr (multi || even) {
             if (chunk_end) {
+                const int64_t c = chunk0 + ck;
+                // EVEN: which ends of chunk c this CTA's run holds
+                const bool has_start = !even || c * nunits >= g0, has_end = !even || (c + 1) * nunits <= g1;
                 asm volatile("bar.sync 1, %0;" ::"r"(THREADS) : "memory");  // every warp done with the chunk
                 reduce_partials(reinterpret_cast<float*>(ring + (size_t)s * SH::STAGE));
-                store_rows((chunk0 + ck) * RPC);
+                if (!has_end) {
+                    // the end of the chunk was the next CTA's, done at the start of
+                    // its run: wait for its partial sums in y (bounded), add them
+                    if (tid == 0) {
+                        const uint64_t t0 = global_ns();
+                        int f = 0;
+                        while (!*abort_flag) {
+                            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(f) : "l"(a.flags + c) : "memory");
+                            if (f || global_ns() - t0 > WAIT_LIMIT_NS) break;
+                        }
+                        if (!f) {
+                            atomicOr(a.err, ERR_TIMEOUT);
+                            *abort_flag = 1;
+                        }
+                    }
+                    asm volatile("bar.sync 1, %0;" ::"r"(THREADS) : "memory");
+                    if (*abort_flag) failed = true;
+                    if (kp == 0 && !failed) {
+#pragma unroll
+                        for (int i = 0; i < WT; ++i)
+#pragma unroll
+                            for (int j = 0; j < NT; ++j) {
+                                const int64_t m = m0 + 8 * j + 2 * t4;
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    const int64_t row = c * RPC + (rh * WT + i) * 16 + g8 + 8 * h;
+                                    if (row >= a.N) continue;
+                                    if (m < a.M) acc[i][j][h].x += __ldcg(a.y + m * a.ldy + row);
+                                    if (m + 1 < a.M) acc[i][j][h].y += __ldcg(a.y + (m + 1) * a.ldy + row);
+                                }
+                            }
+                    }
+                }
+                store_rows(c * RPC);  // whole chunk or its start (with the end added): final; its end only: partial
                 asm volatile("bar.sync 1, %0;" ::"r"(THREADS) : "memory");  // the sums read before the refill
+                if (!has_start && tid == 0) {  // the partial sums are in y: raise the chunk's flag
+                    __threadfence();
+                    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(a.flags + c), "r"(1) : "memory");
+                }
 #pragma unroll
                 for (int i = 0; i < WT; ++i)
 #pragma unroll
@@ -372,7 +441,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (++u == nunits) {
             u = 0;
-            if constexpr (multi) ++ck;
+            if constexpr (multi || even) ++ck;
         }
     }
     if (failed && tid == 0) {  // copies still in flight land before the ring is reused or the CTA exits
@@ -423,7 +492,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             store_rows(chunk0 * RPC);
         }
-    } else if constexpr (!multi) {
+    } else if constexpr (!multi && !even) {
         if (V > 0) {
             reduce_partials(reinterpret_cast<float*>(ring));
             store_rows(chunk0 * RPC);
@@ -461,12 +530,18 @@ cudaError_t launch_ex(Kern kernel, dim3 grid, int threads, size_t smem, cudaStre
 template <int NT, int WT, int KPB, int MODE>
 qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M, const int8_t* xq,
                   const uint16_t* xd, float* y, int64_t ldy, uint8_t* rec, int nchunk, int nsplit, int smem_optin,
-                  int* err, cudaStream_t st) {
+                  int* err, cudaStream_t st, int sms_even = 0) {
     using SH = Shape<NT, WT, KPB>;
     if ((MODE == MULTI) != (nchunk > 1) || (MODE == SPLIT) != (nsplit > 1) || nsplit > 8) return QMM_ERR_SHAPE;
-    if (nchunk > 1 && SH::RED > SH::STAGE) return QMM_ERR_SHAPE;
+    if ((nchunk > 1 || MODE == EVEN) && SH::RED > SH::STAGE) return QMM_ERR_SHAPE;
     const int64_t B = K / QK;
-    const int64_t units = ((B + UKB - 1) / UKB + nsplit - 1) / nsplit * nchunk;
+    const int64_t units_all = (B + UKB - 1) / UKB;
+    const int64_t chunks = (N + SH::RPC - 1) / SH::RPC;
+    // EVEN: one run per SM, each at least a chunk long (so a chunk is cut at
+    // most once), and one flag word per chunk
+    if (MODE == EVEN && (chunks < sms_even || chunks > MAX_FLAGS)) return QMM_ERR_SHAPE;
+    const int64_t units = MODE == EVEN ? (chunks * units_all + sms_even - 1) / sms_even
+                                       : (units_all + nsplit - 1) / nsplit * nchunk;
     const int fixed = 1024 + 1024;  // barriers and counters, alignment slack
     const int64_t nst = std::min<int64_t>({(int64_t)MAX_STAGES, (smem_optin - fixed) / SH::STAGE, units});
     if (nst < 1) return QMM_ERR_SHAPE;
@@ -481,6 +556,8 @@ qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K
     a.ldy = ldy;
     a.y = y;
     a.rec = rec;
+    a.flags = reinterpret_cast<int*>(rec + units_all * Rec<NT>::BYTES);
+    a.units_total = chunks * units_all;
     a.nchunk = nchunk;
     a.nstages = (int)nst;
     a.err = err;
@@ -493,11 +570,9 @@ qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K
         return QMM_ERR_CUDA;
     auto kern = gemm_prep_kernel<NT, WT, KPB, MODE>;
     if (!allow_smem(kern, smem_optin)) return QMM_ERR_SHAPE;
-    const int64_t chunks = (N + SH::RPC - 1) / SH::RPC;
-    const dim3 grid((unsigned)((chunks + nchunk - 1) / nchunk * nsplit), 1);
-    const int64_t units_all = (B + UKB - 1) / UKB;
-    if (launch_ex(prep_kernel<NT>, dim3((unsigned)units_all), UKB * 16 * NT, 0, st, 1, xq, xd, K, M, rec) !=
-        cudaSuccess) {
+    const dim3 grid(MODE == EVEN ? (unsigned)sms_even : (unsigned)((chunks + nchunk - 1) / nchunk * nsplit), 1);
+    if (launch_ex(prep_kernel<NT>, dim3((unsigned)units_all), UKB * 16 * NT, 0, st, 1, xq, xd, K, M, rec,
+                  a.flags) != cudaSuccess) {
         cudaGetLastError();
         return QMM_ERR_CUDA;
     }
@@ -513,6 +588,16 @@ qmm_status launch_nt(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_
                      const uint16_t* xd, float* y, int64_t ldy, const WidePlan& p, uint8_t* ws, int smem_optin,
                      int* err, cudaStream_t st) {
     const int nc = p.nchunk, ns = p.nsplit;
+    // several chunks per CTA: the even cut over the SMs of 192-row chunks,
+    // where every SM's run is at least a chunk long and the busiest CTA's
+    // rows drop by 3% or more (lm_head 128256 rows: 896 -> 844 per SM, 16
+    // tokens 182.0 -> 175.7 us; at 58000 rows, 384 -> 383, the cut's own
+    // cost made it 2-4% slower)
+    if (nc > 1) {
+        const int64_t c192 = (N + 191) / 192;
+        if (c192 >= p.sms && c192 <= MAX_FLAGS && c192 * 192 * 100 <= (int64_t)nc * p.rpc * p.sms * 97)
+            return launch<NT, 3, 4, EVEN>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, 1, smem_optin, err, st, p.sms);
+    }
     switch (p.rpc) {
         case 128:
             return ns > 1 ? launch<NT, 2, 4, SPLIT>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, ns, smem_optin, err, st)
@@ -532,7 +617,8 @@ qmm_status launch_nt(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_
 size_t gemm_prep_bytes(int64_t K, int64_t M) {
     if (M < 1 || M > 16 || K <= 0) return 0;
     const int64_t units = (K / QK + prepk::UKB - 1) / prepk::UKB;
-    return (size_t)units * (size_t)(M <= 8 ? prepk::Rec<1>::BYTES : prepk::Rec<2>::BYTES);
+    return (size_t)units * (size_t)(M <= 8 ? prepk::Rec<1>::BYTES : prepk::Rec<2>::BYTES) +
+           (size_t)prepk::MAX_FLAGS * sizeof(int);
 }
 
 qmm_status gemm_prep_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K, int64_t M,

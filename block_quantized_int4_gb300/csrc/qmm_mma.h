@@ -17,15 +17,16 @@ bool gemm_mma_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const 
 
 // Row plan of the 16-warp layout: rpc rows per chunk (96, 128 or 192; 0
 // where the layout does not apply), nchunk chunks per CTA, nsplit CTAs per
-// cluster splitting K.
+// cluster splitting K; sms the SM count it was made for.
 struct WidePlan {
-    int rpc, nchunk, nsplit;
+    int rpc, nchunk, nsplit, sms;
 };
 WidePlan gemm_wide_plan(int64_t N, int64_t K, int64_t M, int sms);
 
-// Bytes of the prepared activation of qmm_gemm_q4_0_q8_0_ws for K and M
-// (1..16 tokens; 0 otherwise): one record of fp16 B fragments, MMA seeds and
-// scaled d_x per 16 blocks of K.
+// Bytes of the workspace of qmm_gemm_q4_0_q8_0_ws for K and M (1..16
+// tokens; 0 otherwise): one record of fp16 B fragments, MMA seeds and scaled
+// d_x per 16 blocks of K, then 4096 flag words for products cut evenly over
+// the SMs.
 size_t gemm_prep_bytes(int64_t K, int64_t M);
 
 // The 16-warp layout with the activation prepared once into `workspace`

@@ -178,7 +178,9 @@ QMM_API qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, 
 
 /* Device workspace bytes of qmm_gemm_q4_0_q8_0_ws for K and M: for 1..16
  * tokens one 9216 * ceil(M / 8)-byte record per 512 columns of K (rounded
- * up); 0 otherwise.  QMM_ERR_ARG for a NULL bytes or M < 0, QMM_ERR_SHAPE
+ * up) plus 16 KiB of flag words (a large product is cut evenly over the SMs;
+ * a row chunk cut between two CTAs is finished through y and a flag); 0
+ * otherwise.  QMM_ERR_ARG for a NULL bytes or M < 0, QMM_ERR_SHAPE
  * for K <= 0 or K % 32 != 0. */
 QMM_API qmm_status qmm_gemm_workspace_size(int64_t K, int64_t M, size_t* bytes);
 

@@ -86,13 +86,15 @@ def test_workspace_rules(qmm):
 
 def test_gemm_workspace_size_and_rules(qmm):
     """qmm_gemm_workspace_size: one record of 9216 * ceil(M / 8) bytes per 512
-    columns of K (rounded up) for 1..16 tokens, 0 otherwise; the workspace
+    columns of K (rounded up) and 16 KiB of flags for 1..16 tokens, 0
+    otherwise; the workspace
     entry checks the product's arguments first (same statuses as the plain
     entry), then the workspace (NULL, too small, misaligned: QMM_ERR_WORKSPACE),
     all before any device call."""
-    assert qmm.qmm_gemm_workspace_size(8192, 16) == 16 * 18432
-    assert qmm.qmm_gemm_workspace_size(8192, 8) == 16 * 9216
-    assert qmm.qmm_gemm_workspace_size(768, 9) == 2 * 18432    # a last half unit is a whole record
+    flags = 4096 * 4  # the even cut's flag words
+    assert qmm.qmm_gemm_workspace_size(8192, 16) == 16 * 18432 + flags
+    assert qmm.qmm_gemm_workspace_size(8192, 8) == 16 * 9216 + flags
+    assert qmm.qmm_gemm_workspace_size(768, 9) == 2 * 18432 + flags    # a last half unit is a whole record
     assert qmm.qmm_gemm_workspace_size(2048, 17) == 0
     assert qmm.qmm_gemm_workspace_size(2048, 0) == 0
     out = ctypes.c_size_t(0)

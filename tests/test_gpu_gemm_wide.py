@@ -203,10 +203,11 @@ def test_wide_ldy(qmm):
     assert torch.all(y[:, N:] == 7.0)
 
 
-# (N, K, M) through every plan of the 16-warp layout (one chunk of 96 / 128 /
-# 192 rows, several chunks, clusters splitting K), which both entries take
-WS_CASES = [(27000, 2048, 16), (27000, 768, 9), (18000, 2048, 5), (13000, 2048, 12), (110000, 768, 16),
-            (128256, 512, 4), (8192, 28672, 16), (5000, 16640, 9), (2048, 28672, 3)]
+# (N, K, M) through the 16-warp plans both entries take (one chunk of 96 / 128
+# / 192 rows per CTA, clusters splitting K); large N, where the workspace
+# entry cuts the product evenly over the SMs instead, is test_workspace_even_cut
+WS_CASES = [(27000, 2048, 16), (27000, 768, 9), (18000, 2048, 5), (13000, 2048, 12), (8192, 28672, 16),
+            (5000, 16640, 9), (2048, 28672, 3)]
 
 
 @pytest.mark.parametrize("N,K,M", WS_CASES)
@@ -308,4 +309,28 @@ def test_workspace_small_products(qmm, N, K, M):
     assert_close(y, ref, S, f"workspace gemm small N {N}x{K} M={M}")
     y2 = qmm.gemm(qs, d, xq, xd, workspace=ws)
     assert torch.equal(y, y2)
+    assert qmm.qmm_last_device_error() == 0
+
+
+@pytest.mark.parametrize("N,K,M", [(128256, 768, 16), (58000, 2048, 9), (110000, 512, 4), (40000, 1024, 16),
+                                   (110000, 768, 16), (128256, 512, 4), (128256, 2048, 7)])
+def test_workspace_even_cut(qmm, N, K, M):
+    """Large N through the workspace entry: where it pays (lm_head-sized N),
+    the product's (chunk, unit) sequence cut evenly over the SMs, chunks cut
+    between two CTAs finished through y and a flag; elsewhere several chunks
+    per CTA.  Rows at every 192-row chunk edge (and more) against the oracle,
+    and the same bits on a second call."""
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + 5 * K + M)
+    qs, d = _planes(qmm, qw, dw)
+    xq, xd = _q8(qx, dx)
+    ws = torch.full((qmm.qmm_gemm_workspace_size(K, M),), 0x77, dtype=torch.uint8, device=DEV)
+    y = qmm.gemm(qs, d, xq, xd, workspace=ws)
+    y2 = qmm.gemm(qs, d, xq, xd, workspace=ws)
+    assert torch.equal(y, y2)
+    rng = np.random.default_rng(N)
+    edges = np.arange(0, N, 192)
+    rows = np.unique(np.clip(np.concatenate([edges, edges - 1, edges + 100, rng.integers(0, N, 1500),
+                                             np.arange(N - 30, N)]), 0, N - 1))
+    ref, S = O.matmul_int(qw, dw, qx, dx, rows=rows, nthreads=8)
+    assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, S, f"workspace even cut {N}x{K} M={M}")
     assert qmm.qmm_last_device_error() == 0
