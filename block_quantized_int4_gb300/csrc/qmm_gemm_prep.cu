@@ -17,7 +17,9 @@
 //    arrival counter), so no warp is held to the pace of the slowest one
 //    except through the ring's depth.
 // The fp32 results are those of the staged layout bit for bit (same
-// fragments, same MMA and accumulation order, same reductions).
+// fragments, same MMA and accumulation order, same reductions), except under
+// the EVEN mode below, where a row chunk cut between two CTAs sums its two
+// parts separately (then added in one fixed order: the same bits every call).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
