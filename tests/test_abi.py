@@ -86,15 +86,16 @@ def test_workspace_rules(qmm):
 
 def test_gemm_workspace_size_and_rules(qmm):
     """qmm_gemm_workspace_size: one record of 9216 * ceil(M / 8) bytes per 512
-    columns of K (rounded up) and 16 KiB of flags for 1..16 tokens, 0
-    otherwise; the workspace
+    columns of K (rounded up), 16 KiB of flags and 256 partial-sum slots of
+    8 * ceil(M / 8) x 192 floats for 1..16 tokens, 0 otherwise; the workspace
     entry checks the product's arguments first (same statuses as the plain
     entry), then the workspace (NULL, too small, misaligned: QMM_ERR_WORKSPACE),
     all before any device call."""
     flags = 4096 * 4  # the even cut's flag words
-    assert qmm.qmm_gemm_workspace_size(8192, 16) == 16 * 18432 + flags
-    assert qmm.qmm_gemm_workspace_size(8192, 8) == 16 * 9216 + flags
-    assert qmm.qmm_gemm_workspace_size(768, 9) == 2 * 18432 + flags    # a last half unit is a whole record
+    slots = {1: 256 * 8 * 192 * 4, 2: 256 * 16 * 192 * 4}  # and its partial sums, per ceil(M / 8)
+    assert qmm.qmm_gemm_workspace_size(8192, 16) == 16 * 18432 + flags + slots[2]
+    assert qmm.qmm_gemm_workspace_size(8192, 8) == 16 * 9216 + flags + slots[1]
+    assert qmm.qmm_gemm_workspace_size(768, 9) == 2 * 18432 + flags + slots[2]  # a last half unit is a whole record
     assert qmm.qmm_gemm_workspace_size(2048, 17) == 0
     assert qmm.qmm_gemm_workspace_size(2048, 0) == 0
     out = ctypes.c_size_t(0)
@@ -111,8 +112,6 @@ def test_gemm_workspace_size_and_rules(qmm):
     assert ws(A16, A16, 64, 8192, 16, A16, A16, A16, 64, None, n, None) == 8      # no workspace
     assert ws(A16, A16, 64, 8192, 16, A16, A16, A16, 64, A16, n - 16, None) == 8  # too small
     assert ws(A16, A16, 64, 8192, 16, A16, A16, A16, 64, A16 + 64, n, None) == 8  # not 128-byte aligned
-    # no workspace needed (17 tokens): the plain entry's path, here without a device
-    assert ws(A16, A16, 64, 8192, 17, A16, A16, A16, 64, None, 0, None) == 4
 
 
 def test_static_scratch_limit_and_arguments(qmm):
@@ -156,7 +155,8 @@ def test_fused_op_validation(qmm):
 def test_fused_ops_chain_validation(qmm):
     """qmm_gemv_fused_ops checks every op before launching any: the first bad
     op's status; bad counts, a NULL array and unknown flags are QMM_ERR_ARG;
-    an empty chain is a no-op; a valid chain reaches the device check."""
+    an empty chain is a no-op (a valid chain reaches the device check: the
+    test below, run only where no GPU is present)."""
     A16 = 0x10000
     good = qmm.gemv_op(A16, A16, 64, 256, xq=A16, xd=A16, yq=A16, yd=A16)
     bad_k = qmm.gemv_op(A16, A16, 64, 288, xq=A16, xd=A16, yq=A16, yd=A16)
@@ -170,7 +170,6 @@ def test_fused_ops_chain_validation(qmm):
     assert lib.qmm_gemv_fused_ops(None, 2, 0, None) == 1
     assert lib.qmm_gemv_fused_ops(arr, 2, 1, None) == 1      # only QMM_CHAIN as a call flag
     assert lib.qmm_gemv_fused_ops(None, 0, 0, None) == 0
-    assert lib.qmm_gemv_fused_ops(arr, 2, 4, None) == 4      # valid ops: no device here
 
 
 def test_router_and_pregrouped_validation(qmm):
@@ -236,6 +235,11 @@ def test_valid_call_without_gpu_reports_device_error(qmm):
     assert _call(qmm, "qmm_gemv_q4_0_f32_fma", A16, A16, 8, 64, A16, A16, None) == 4
     assert _call(qmm, "qmm_quantize_rowwise", A16, 4, 64, 64, 2, A16, A16, None) == 4
     assert _call(qmm, "qmm_last_device_error", None) == 4
+    # a chain of valid ops; the workspace entry with 17 tokens (no workspace
+    # needed: the plain entry's path)
+    good = qmm.gemv_op(A16, A16, 64, 256, xq=A16, xd=A16, yq=A16, yd=A16)
+    assert qmm.library_handle().qmm_gemv_fused_ops(qmm.gemv_op_array([good, good]), 2, 4, None) == 4
+    assert _call(qmm, "qmm_gemm_q4_0_q8_0_ws", A16, A16, 64, 8192, 17, A16, A16, A16, 64, None, 0, None) == 4
 
 
 def test_gemm_kernel_selector_and_moe_fp32_validation(qmm):
