@@ -555,7 +555,7 @@ qmm_status qmm_gemm_q4_0_q8_0_ws(const uint8_t* w_qs, const uint16_t* w_d, int64
     const int pick = g_gemm_kernel.load();
     if (need > 0 && M >= 3 && (pick == QMM_GEMM_KERNEL_AUTO || pick == QMM_GEMM_KERNEL_MMA) && aligned(xd, 16) &&
         gemm_mma_eligible(N, K, M, w_qs, w_d, xq, xd)) {
-        const WidePlan p = gemm_wide_plan(N, K, M, di->sms);
+        const WidePlan p = gemm_wide_plan(N, K, M, di->sms, false);
         if (p.rpc > 0)
             return gemm_prep_launch(w_qs, w_d, N, K, M, xq, xd, y, ldy, p, workspace, di->smem_optin, di->err,
                                     S(stream));

@@ -1040,24 +1040,43 @@ qmm_status launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K
 //    4096 x 14336 40 against 28), and 256 rows leave room for two stages.
 //  - more: several chunks of 128 or 192 rows, whichever needs fewer rows
 //    per CTA (192 on a tie).
-//  - fewer rows (at most 64 per SM): 128-row chunks, each shared by a cluster
-//    of nsplit = min(8, SMs / chunks) >= 2 CTAs splitting K, when every
-//    rank gets at least 6 units of 16 blocks.
+//  - fewer rows (at most 64 per SM): chunks of 128 or 192 rows, each shared
+//    by a cluster of nsplit = min(4, SMs / chunks) >= 2 CTAs splitting K,
+//    when every rank gets at least 6 units of 16 blocks; of the two, the
+//    one with fewer rows x units on the busiest CTA, 192-row chunks counted
+//    at 0.9 for their cheaper blocks (three row tiles per warp: 8192 x 28672
+//    at 16 tokens 59.9 -> 51.7 us, 4 tokens 43.1 -> 37.0).  Clusters of up
+//    to 4 CTAs of one SM each pack a GB300's 152 SMs (76, 46 and 36 of them
+//    at once: 152, 138, 144 CTAs); of 5 to 8, 28, 23, 15 and 15 fit (140,
+//    138, 105, 120 CTAs), and 5-CTA clusters behind the workspace entry's
+//    preparation launch measured 19-28% slower than 3-CTA ones.  With
+//    split192 false only 128-row chunks are split: the workspace entry's
+//    plan, where 3-CTA clusters placed behind the previous product's tail
+//    varied from run to run (the batch-16 dense set 0.296-0.311 ms against
+//    0.300 steady with 2-CTA clusters).
 struct Plan {
     int rpc = 0, nchunk = 1, nsplit = 1;
 };
 
-Plan plan_rows(int64_t N, int64_t K, int64_t M, int sms) {
+Plan plan_rows(int64_t N, int64_t K, int64_t M, int sms, bool split192 = true) {
     Plan p;
     const int64_t need = (N + sms - 1) / sms;
     const int64_t r16 = round_up(need, 16);
     const auto ok = [&](int64_t rows) { return rows * 100 <= r16 * 108; };
     if (need <= 64) {
-        const int64_t chunks = (N + 127) / 128, units = (K / QK + UKB - 1) / UKB;
-        const int64_t ns = std::min<int64_t>(8, sms / chunks);
-        if (ns >= 2 && units >= 6 * ns) {
-            p.rpc = 128;
-            p.nsplit = (int)ns;
+        const int64_t units = (K / QK + UKB - 1) / UKB;
+        int64_t best = 0;  // rows x units of the busiest CTA, 192-row chunks weighted 0.9
+        for (const int rpc : {192, 128}) {
+            if (rpc == 192 && !split192) continue;
+            const int64_t chunks = (N + rpc - 1) / rpc;
+            const int64_t ns = std::min<int64_t>(4, sms / chunks);
+            if (ns < 2 || units < 6 * ns) continue;
+            const int64_t cost = rpc * ((units + ns - 1) / ns) * (rpc == 192 ? 9 : 10);
+            if (best == 0 || cost < best) {
+                best = cost;
+                p.rpc = rpc;
+                p.nsplit = (int)ns;
+            }
         }
         return p;
     }
@@ -1092,8 +1111,9 @@ bool plan_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
                             : launch<NT, 2, 4, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, 1, smem_optin, err, st);
             return true;
         case 192:
-            *out = nc > 1 ? launch<NT, 3, 4, MULTI>(w_qs, w_d, N, K, M, xq, xd, y, ldy, nc, 1, smem_optin, err, st)
-                          : launch<NT, 3, 4, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, 1, smem_optin, err, st);
+            *out = ns > 1   ? launch<NT, 3, 4, SPLIT>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, ns, smem_optin, err, st)
+                   : nc > 1 ? launch<NT, 3, 4, MULTI>(w_qs, w_d, N, K, M, xq, xd, y, ldy, nc, 1, smem_optin, err, st)
+                            : launch<NT, 3, 4, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, 1, smem_optin, err, st);
             return true;
         case 96:  // one chunk only
             *out = launch<NT, 3, 2, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, 1, 1, smem_optin, err, st);
@@ -1106,8 +1126,8 @@ bool plan_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_t K,
 
 }  // namespace mmak
 
-WidePlan gemm_wide_plan(int64_t N, int64_t K, int64_t M, int sms) {
-    const mmak::widek::Plan p = mmak::widek::plan_rows(N, K, M, sms);
+WidePlan gemm_wide_plan(int64_t N, int64_t K, int64_t M, int sms, bool split192) {
+    const mmak::widek::Plan p = mmak::widek::plan_rows(N, K, M, sms, split192);
     return WidePlan{p.rpc, p.nchunk, p.nsplit, sms};
 }
 

@@ -17,9 +17,12 @@
 //    arrival counter), so no warp is held to the pace of the slowest one
 //    except through the ring's depth.
 // The fp32 results are those of the staged layout bit for bit (same
-// fragments, same MMA and accumulation order, same reductions), except under
-// the EVEN mode below, where a row chunk cut between two CTAs sums its two
-// parts separately (then added in one fixed order: the same bits every call).
+// fragments, same MMA and accumulation order, same reductions) under the same
+// row plan.  The plans differ in two places: under the EVEN mode below, a
+// row chunk cut between two CTAs sums its two parts separately (then added
+// in one fixed order: the same bits every call); and K is split over
+// clusters sharing 128-row chunks only (the plain entry also splits 192-row
+// chunks).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -607,8 +610,9 @@ qmm_status launch_nt(const uint8_t* w_qs, const uint16_t* w_d, int64_t N, int64_
                        ? launch<NT, 2, 4, MULTI>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, nc, 1, smem_optin, err, st)
                        : launch<NT, 2, 4, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, 1, smem_optin, err, st);
         case 192:
-            return nc > 1 ? launch<NT, 3, 4, MULTI>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, nc, 1, smem_optin, err, st)
-                          : launch<NT, 3, 4, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, 1, smem_optin, err, st);
+            return ns > 1   ? launch<NT, 3, 4, SPLIT>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, ns, smem_optin, err, st)
+                   : nc > 1 ? launch<NT, 3, 4, MULTI>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, nc, 1, smem_optin, err, st)
+                            : launch<NT, 3, 4, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, 1, smem_optin, err, st);
         case 96: return launch<NT, 3, 2, ONE>(w_qs, w_d, N, K, M, xq, xd, y, ldy, ws, 1, 1, smem_optin, err, st);
         default: return QMM_ERR_SHAPE;
     }

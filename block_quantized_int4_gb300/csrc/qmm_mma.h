@@ -17,11 +17,13 @@ bool gemm_mma_eligible(int64_t N, int64_t K, int64_t M, const void* w_qs, const 
 
 // Row plan of the 16-warp layout: rpc rows per chunk (96, 128 or 192; 0
 // where the layout does not apply), nchunk chunks per CTA, nsplit CTAs per
-// cluster splitting K; sms the SM count it was made for.
+// cluster splitting K; sms the SM count it was made for.  split192: whether
+// K may be split over clusters sharing 192-row chunks (the plain entry's
+// plan) or over 128-row chunks only (the workspace entry's).
 struct WidePlan {
     int rpc, nchunk, nsplit, sms;
 };
-WidePlan gemm_wide_plan(int64_t N, int64_t K, int64_t M, int sms);
+WidePlan gemm_wide_plan(int64_t N, int64_t K, int64_t M, int sms, bool split192);
 
 // Bytes of the workspace of qmm_gemm_q4_0_q8_0_ws for K and M (1..16
 // tokens; 0 otherwise): one record of fp16 B fragments, MMA seeds and scaled
@@ -41,8 +43,8 @@ qmm_status gemm_prep_launch(const uint8_t* w_qs, const uint16_t* w_d, int64_t N,
 // product: up to 16 tokens, xd 16-byte aligned, and a row plan at one CTA
 // per SM of 128 or 192 rows per CTA (ceil(N / sms) in 65..192), 96 rows for
 // 9..16 tokens, several chunks of 128 or 192 rows per CTA for larger N, or
-// for smaller N with long K, 128-row chunks split over K by clusters of 2..8
-// CTAs.
+// for smaller N with long K, 128- or 192-row chunks split over K by clusters
+// of 2..4 CTAs.
 bool gemm_wide_planned(int64_t N, int64_t K, int64_t M, const void* xd, int sms);
 
 // Enqueue y[m*ldy + n] (m < M, n < N) on `st`.  `sms` and `smem_optin` are

@@ -191,9 +191,11 @@ QMM_API qmm_status qmm_gemm_workspace_size(int64_t K, int64_t M, size_t* bytes);
  * 16-byte aligned) a first launch forms the activation's MMA operand once
  * for the whole call into the workspace, and every CTA of the product copies
  * it from there instead of forming it itself; the results are those of
- * qmm_gemm_q4_0_q8_0 bit for bit, except where a large product is cut evenly
- * over the SMs (a row chunk cut between two CTAs sums its two parts
- * separately; same tolerance, the same bits on every call).  Elsewhere the workspace is not used and
+ * qmm_gemm_q4_0_q8_0 bit for bit, except where the two take different row
+ * plans: a large product cut evenly over the SMs (a row chunk cut between
+ * two CTAs sums its two parts separately), and a small-N, long-K product
+ * whose K the plain entry splits over clusters sharing 192-row chunks (here
+ * 128-row chunks); same tolerance, the same bits on every call.  Elsewhere the workspace is not used and
  * the call is qmm_gemm_q4_0_q8_0.  Host checks as qmm_gemm_q4_0_q8_0's, then
  * QMM_ERR_WORKSPACE for a workspace that is NULL, smaller than required or
  * misaligned (when the required size is not 0).  Both launches use

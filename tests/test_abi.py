@@ -86,16 +86,15 @@ def test_workspace_rules(qmm):
 
 def test_gemm_workspace_size_and_rules(qmm):
     """qmm_gemm_workspace_size: one record of 9216 * ceil(M / 8) bytes per 512
-    columns of K (rounded up), 16 KiB of flags and 256 partial-sum slots of
-    8 * ceil(M / 8) x 192 floats for 1..16 tokens, 0 otherwise; the workspace
+    columns of K (rounded up) and 16 KiB of flags for 1..16 tokens, 0
+    otherwise; the workspace
     entry checks the product's arguments first (same statuses as the plain
     entry), then the workspace (NULL, too small, misaligned: QMM_ERR_WORKSPACE),
     all before any device call."""
     flags = 4096 * 4  # the even cut's flag words
-    slots = {1: 256 * 8 * 192 * 4, 2: 256 * 16 * 192 * 4}  # and its partial sums, per ceil(M / 8)
-    assert qmm.qmm_gemm_workspace_size(8192, 16) == 16 * 18432 + flags + slots[2]
-    assert qmm.qmm_gemm_workspace_size(8192, 8) == 16 * 9216 + flags + slots[1]
-    assert qmm.qmm_gemm_workspace_size(768, 9) == 2 * 18432 + flags + slots[2]  # a last half unit is a whole record
+    assert qmm.qmm_gemm_workspace_size(8192, 16) == 16 * 18432 + flags
+    assert qmm.qmm_gemm_workspace_size(8192, 8) == 16 * 9216 + flags
+    assert qmm.qmm_gemm_workspace_size(768, 9) == 2 * 18432 + flags    # a last half unit is a whole record
     assert qmm.qmm_gemm_workspace_size(2048, 17) == 0
     assert qmm.qmm_gemm_workspace_size(2048, 0) == 0
     out = ctypes.c_size_t(0)

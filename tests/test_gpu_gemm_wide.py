@@ -154,8 +154,11 @@ def test_multi_chunk_plans_are_the_intended_ones():
         assert pick * per[pick] * 100 <= -(-need // 16) * 16 * 108
 
 
-# N, K -> CTAs per cluster splitting K (128-row chunks) on 152 SMs
-SPLIT_PLANS = {(8192, 28672): 2, (4096, 14336): 4, (2048, 28672): 8, (5000, 16640): 3}
+# N, K -> (chunk rows, CTAs per cluster splitting K) on 152 SMs: 192-row
+# chunks where the busiest CTA's rows x units, counted at 0.9, are fewer;
+# clusters of at most 4
+SPLIT_PLANS = {(8192, 28672): (192, 3), (8000, 16640): (192, 3), (4096, 14336): (128, 4), (2048, 28672): (128, 4),
+               (5000, 16640): (128, 3)}
 
 
 @pytest.mark.parametrize("N,K", sorted(SPLIT_PLANS))
@@ -172,8 +175,9 @@ def test_wide_split_k_clusters(qmm, N, K, M):
     y2 = qmm.gemm(qs, d, xq, xd)
     assert torch.equal(y, y2)
     rng = np.random.default_rng(N + M)
-    edges = np.arange(0, N, 128)
-    rows = np.unique(np.clip(np.concatenate([edges, edges - 1, edges + 127, rng.integers(0, N, 600),
+    rpc = SPLIT_PLANS[(N, K)][0]
+    edges = np.arange(0, N, rpc)
+    rows = np.unique(np.clip(np.concatenate([edges, edges - 1, edges + rpc - 1, rng.integers(0, N, 600),
                                              np.arange(N - 20, N)]), 0, N - 1))
     ref, S = O.matmul_int(qw, dw, qx, dx, rows=rows, nthreads=8)
     assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, S, f"split-K gemm {N}x{K} M={M}")
@@ -184,10 +188,15 @@ def test_split_plans_are_the_intended_ones():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     if sms != 152:
         pytest.skip(f"{sms} SMs: the row plans differ from the ones the shapes were chosen for")
-    for (N, K), ns in SPLIT_PLANS.items():
+    for (N, K), plan in SPLIT_PLANS.items():
         assert -(-N // sms) <= 64
-        chunks = -(-N // 128)
-        assert min(8, sms // chunks) == ns and -(-(K // 32) // 16) >= 6 * ns
+        units = -(-(K // 32) // 16)
+        costs = {}
+        for rpc in (192, 128):
+            ns = min(4, sms // -(-N // rpc))
+            if ns >= 2 and units >= 6 * ns:
+                costs[(rpc, ns)] = rpc * -(-units // ns) * (9 if rpc == 192 else 10)
+        assert min(costs, key=costs.get) == plan
 
 
 def test_wide_ldy(qmm):
@@ -204,10 +213,12 @@ def test_wide_ldy(qmm):
 
 
 # (N, K, M) through the 16-warp plans both entries take (one chunk of 96 / 128
-# / 192 rows per CTA, clusters splitting K); large N, where the workspace
-# entry cuts the product evenly over the SMs instead, is test_workspace_even_cut
-WS_CASES = [(27000, 2048, 16), (27000, 768, 9), (18000, 2048, 5), (13000, 2048, 12), (8192, 28672, 16),
-            (5000, 16640, 9), (2048, 28672, 3)]
+# / 192 rows per CTA, clusters splitting 128-row chunks' K); large N, where
+# the workspace entry cuts the product evenly over the SMs instead, is
+# test_workspace_even_cut, and the shapes whose K the plain entry splits over
+# 192-row chunks are test_workspace_split_plans'
+WS_CASES = [(27000, 2048, 16), (27000, 768, 9), (18000, 2048, 5), (13000, 2048, 12), (5000, 16640, 9),
+            (2048, 28672, 3)]
 
 
 @pytest.mark.parametrize("N,K,M", WS_CASES)
@@ -227,6 +238,28 @@ def test_workspace_path_matches_staged_path(qmm, N, K, M):
     rows = np.unique(np.concatenate([np.arange(40), np.arange(N - 40, N), rng.integers(0, N, 400)]))
     ref, S = O.matmul_int(qw, dw, qx, dx, rows=rows, nthreads=8)
     assert_close(y1[:, torch.from_numpy(rows).to(DEV)], ref, S, f"workspace gemm {N}x{K} M={M}")
+    assert qmm.qmm_last_device_error() == 0
+
+
+@pytest.mark.parametrize("N,K,M", [(8192, 28672, 16), (8000, 16640, 9), (8192, 28672, 4)])
+def test_workspace_split_plans(qmm, N, K, M):
+    """Where the plain entry splits K over clusters sharing 192-row chunks,
+    the workspace entry splits 128-row chunks (2- or 3-CTA clusters): sampled
+    rows at both chunk sizes' edges against the oracle, and the same bits on
+    a second call."""
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=N + 7 * K + M)
+    qs, d = _planes(qmm, qw, dw)
+    xq, xd = _q8(qx, dx)
+    ws = torch.full((qmm.qmm_gemm_workspace_size(K, M),), 0x3C, dtype=torch.uint8, device=DEV)
+    y = qmm.gemm(qs, d, xq, xd, workspace=ws)
+    y2 = qmm.gemm(qs, d, xq, xd, workspace=ws)
+    assert torch.equal(y, y2)
+    rng = np.random.default_rng(N + M)
+    edges = np.concatenate([np.arange(0, N, 128), np.arange(0, N, 192)])
+    rows = np.unique(np.clip(np.concatenate([edges, edges - 1, rng.integers(0, N, 400), np.arange(N - 20, N)]),
+                             0, N - 1))
+    ref, S = O.matmul_int(qw, dw, qx, dx, rows=rows, nthreads=8)
+    assert_close(y[:, torch.from_numpy(rows).to(DEV)], ref, S, f"workspace split plan {N}x{K} M={M}")
     assert qmm.qmm_last_device_error() == 0
 
 
