@@ -325,7 +325,9 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
     while staging them (four launches: 1 token 49.9 -> 49.1 us); with more,
     each CTA would requantize four activation rows per expert segment, and
     standalone Q8_0 launches of x and h are faster (six launches: 16 tokens
-    477.8 -> 469.3 us)."""
+    477.8 -> 469.3 us).  One graph replay runs the layer on three routings
+    in turn (back to back, as consecutive layers run), so no layer finds its
+    experts' weights in L2 from the layer before; the time is per layer."""
     import numpy as np
     c = workloads.MOE
     H, F, E, k = c["hidden"], c["expert_ffn"], c["experts"], c["top_k"]
@@ -343,9 +345,13 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
     # gate and up rows interleaved per expert (g0, u0, g1, u1, ...)
     gu = tuple(torch.stack([g, u], dim=2).reshape(E, 2 * F, g.shape[2]).contiguous() for g, u in zip(gate, up))
     del gate, up
-    logits = workloads.router_logits(T, E, seed=0).to(dev)
-    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
-    gts = torch.empty(T, k, dtype=torch.float32, device=dev)
+    # R routings (router logits of seeds 0..R-1): one graph replay runs the
+    # layer once on each, so consecutive layers read different experts and no
+    # expert's weights are still in L2 from the layer before
+    R = 3
+    logits = [workloads.router_logits(T, E, seed=r).to(dev) for r in range(R)]
+    ids = [torch.empty(T, k, dtype=torch.int32, device=dev) for _ in range(R)]
+    gts = [torch.empty(T, k, dtype=torch.float32, device=dev) for _ in range(R)]
     x = workloads.activations(T, H, seed=0, device=dev)
     h = torch.empty(T * k, F, device=dev)
     in_launch = T * k * 4 <= E
@@ -358,10 +364,10 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
     wsb = qmm.qmm_moe_workspace_size(E, T, k)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
 
-    def run():
+    def layer(r):
         # the router (sigmoid top-k) groups the slots by expert in the same launch;
         # the three expert GEMVs reuse that grouping
-        qmm.qmm_moe_router_topk(logits, T, E, k, ids, gts, ws, wsb)
+        qmm.qmm_moe_router_topk(logits[r], T, E, k, ids[r], gts[r], ws, wsb)
         if in_launch:
             qmm.qmm_moe_gemv_gate_up(*gu, E, 2 * F, H, T, k, x, None, None, 0, h, ws, wsb)
             qmm.qmm_moe_gemv_pregrouped_f32(*down, E, H, F, T, k, h, 1, z, ws, wsb)
@@ -370,17 +376,23 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
             qmm.qmm_moe_gemv_gate_up(*gu, E, 2 * F, H, T, k, None, xq, xd, 0, h, ws, wsb)
             qmm.qmm_quantize_q8_0(h, T * k, F, F, hq, hd)
             qmm.qmm_moe_gemv_pregrouped(*down, E, H, F, T, k, hq, hd, 1, z, ws, wsb)
-        qmm.qmm_moe_combine(z, gts, T, k, H, y)
+        qmm.qmm_moe_combine(z, gts[r], T, k, H, y)
+
+    def run():
+        for r in range(R):
+            layer(r)
 
     g = _graph(torch, run)
-    uniq = len(np.unique(ids.cpu().numpy()))  # bookkeeping for the byte count, outside the timed region
+    # bookkeeping for the byte count, outside the timed region
+    uniq = [len(np.unique(i.cpu().numpy())) for i in ids]
     t = _time_graph(torch, g, reps, 3)
-    per = t / reps
-    wbytes = uniq * 3 * workloads.q4_0_bytes(F, H)
+    per = t / (reps * R)  # one layer
+    wbytes = sum(uniq) / R * 3 * workloads.q4_0_bytes(F, H)
     return {"metric": "MoE layer expert-weight GB/s", "value": round(wbytes / per / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(per * 1e3, 4), "tokens_per_s": round(T / per, 1), "unique_experts": uniq,
             "config": {"workload": c["name"], "T": T, "experts": E, "top_k": k, "hidden": H, "expert_ffn": F,
-                       "launches": 4 if in_launch else 6}}
+                       "launches": 4 if in_launch else 6, "routings": R,
+                       "l2": "each replay runs the layer on 3 routings in turn (router logits of seeds 0, 1, 2)"}}
 
 
 def bench_moe_store(qmm, torch, T=1, dev="cuda"):
