@@ -365,17 +365,18 @@ def bench_moe(qmm, torch, T=16, reps=10, dev="cuda"):
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
 
     def layer(r):
-        # the router (sigmoid top-k) groups the slots by expert in the same launch;
-        # the three expert GEMVs reuse that grouping
-        qmm.qmm_moe_router_topk(logits[r], T, E, k, ids[r], gts[r], ws, wsb)
         if in_launch:
-            qmm.qmm_moe_gemv_gate_up(*gu, E, 2 * F, H, T, k, x, None, None, 0, h, ws, wsb)
-            qmm.qmm_moe_gemv_pregrouped_f32(*down, E, H, F, T, k, h, 1, z, ws, wsb)
-        else:
-            qmm.qmm_quantize_q8_0(x, T, H, H, xq, xd)
-            qmm.qmm_moe_gemv_gate_up(*gu, E, 2 * F, H, T, k, None, xq, xd, 0, h, ws, wsb)
-            qmm.qmm_quantize_q8_0(h, T * k, F, F, hq, hd)
-            qmm.qmm_moe_gemv_pregrouped(*down, E, H, F, T, k, hq, hd, 1, z, ws, wsb)
+            # the layer entry: router + grouping, gate/up + SwiGLU, down, combine;
+            # the down launch streams its weights before the gate/up launch ends
+            qmm.qmm_moe_layer_f32(logits[r], T, E, k, *gu, *down, H, F, x, ids[r], gts[r], h, z, y, ws, wsb)
+            return
+        # the router (sigmoid top-k) groups the slots by expert in the same
+        # launch; the expert GEMVs reuse that grouping
+        qmm.qmm_moe_router_topk(logits[r], T, E, k, ids[r], gts[r], ws, wsb)
+        qmm.qmm_quantize_q8_0(x, T, H, H, xq, xd)
+        qmm.qmm_moe_gemv_gate_up(*gu, E, 2 * F, H, T, k, None, xq, xd, 0, h, ws, wsb)
+        qmm.qmm_quantize_q8_0(h, T * k, F, F, hq, hd)
+        qmm.qmm_moe_gemv_pregrouped(*down, E, H, F, T, k, hq, hd, 1, z, ws, wsb)
         qmm.qmm_moe_combine(z, gts[r], T, k, H, y)
 
     def run():

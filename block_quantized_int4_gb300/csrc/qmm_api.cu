@@ -699,18 +699,54 @@ qmm_status moe_check(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_
     return QMM_OK;
 }
 
+// Whether the streaming expert GEMV takes this expert tensor (the fp32 and
+// SwiGLU-pair forms require it).
+bool moe_streamable(const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K) {
+    const int64_t B = K / QK;
+    return (B % 8 == 0) && aligned(w_qs, 16) && aligned(w_d, 16) && (int64_t)E * N < (int64_t(1) << 31) &&
+           E <= 2048 && 4 * B * xtile_bytes_per_block() <= STREAM_XTILE_CAP;
+}
+
+// Ring stages of the streaming expert GEMV (0: it does not fit), and the
+// sizes that decide them: slots per weight pass, activation tile, tables.
+struct MoeStreamSizes {
+    int mt;
+    int64_t xtile, tables, nst;
+};
+MoeStreamSizes moe_stream_sizes(int32_t E, int64_t K, int64_t nslots) {
+    MoeStreamSizes z;
+    const int64_t B = K / QK;
+    // Slots per weight pass: four once slots outnumber a quarter of the
+    // experts (experts with several slots are then common, and each pass
+    // streams the expert's weights once), else one.  Measured on the
+    // GLM-scale layer, top-8 of 256: 16 tokens 0.518 ms with four per pass,
+    // 0.552 with two, 0.665 with one; 1 token fastest with one.
+    z.mt = nslots * 4 > (int64_t)E ? 4 : 1;
+    z.xtile = round_up((int64_t)z.mt * B * xtile_bytes_per_block(), 128);
+    // routing tables in shared memory: active list and slot starts (E each),
+    // the slot list when short, count and end
+    z.tables = round_up((int64_t)E * 8 + (nslots <= MOE_SMEM_SLOTS ? nslots * 4 : 0) + 8, 128);
+    // two CTAs per SM (110 KB each): more warps to hide the dot-product latency
+    z.nst = std::max<int64_t>(
+        0, std::min<int64_t>((110 * 1024 - STREAM_HDR - z.xtile - z.tables) / STAGE_BYTES, STREAM_MAX_STAGES));
+    return z;
+}
+
+// Launch chaining of moe_apply (MoeStreamArgs late_trigger / tables_ready).
+constexpr int CHAIN_LATE_TRIGGER = 1, CHAIN_TABLES_READY = 2;
+
 // The expert GEMV on routing tables already built in the workspace.
 // pairs: rows 2i, 2i + 1 of each expert are a (gate, up) pair and y gets
 // SwiGLU of each pair ([T*k][N/2]); xf: fp32 activation rows quantized while
-// staging, in place of xq/xd.  Both on the streaming kernel only.
+// staging, in place of xq/xd.  Both on the streaming kernel only.  chain:
+// CHAIN_* bits, only for launches whose order on the stream the caller
+// fixes (qmm_moe_layer_f32).
 qmm_status moe_apply(const DevInfo* di, const uint8_t* w_qs, const uint16_t* w_d, int32_t E, int64_t N, int64_t K,
                      int32_t T, int32_t k, const int8_t* xq, const uint16_t* xd, int x_per_slot, float* y,
-                     MoeWs ws, cudaStream_t st, bool pairs = false, const float* xf = nullptr) {
+                     MoeWs ws, cudaStream_t st, bool pairs = false, const float* xf = nullptr, int chain = 0) {
     const int64_t B = K / QK;
     const int64_t nslots = (int64_t)T * k;
-    const bool streamable = (B % 8 == 0) && aligned(w_qs, 16) && aligned(w_d, 16) &&
-                            (int64_t)E * N < (int64_t(1) << 31) && E <= 2048 &&
-                            4 * B * xtile_bytes_per_block() <= STREAM_XTILE_CAP;
+    const bool streamable = moe_streamable(w_qs, w_d, E, N, K);
     if (streamable) {
         MoeStreamArgs m = {};
         m.N = N;
@@ -729,19 +765,11 @@ qmm_status moe_apply(const DevInfo* di, const uint8_t* w_qs, const uint16_t* w_d
         m.rb = GROUP_ROWS;
         m.ckb = (int)std::min<int64_t>(CHUNK_KB, B);
         m.err = di->err;
-        // Slots per weight pass: four once slots outnumber a quarter of the
-        // experts (experts with several slots are then common, and each pass
-        // streams the expert's weights once), else one.  Measured on the
-        // GLM-scale layer, top-8 of 256: 16 tokens 0.518 ms with four per pass,
-        // 0.552 with two, 0.665 with one; 1 token fastest with one.
-        const int mt = nslots * 4 > (int64_t)E ? 4 : 1;
-        const int64_t xtile = round_up((int64_t)mt * B * xtile_bytes_per_block(), 128);
-        // routing tables in shared memory: active list and slot starts (E each),
-        // the slot list when short, count and end
-        const int64_t tables = round_up((int64_t)E * 8 + (m.slots_smem ? nslots * 4 : 0) + 8, 128);
-        // two CTAs per SM (110 KB each): more warps to hide the dot-product latency
-        const int64_t nst =
-            std::min<int64_t>((110 * 1024 - STREAM_HDR - xtile - tables) / STAGE_BYTES, STREAM_MAX_STAGES);
+        m.late_trigger = (chain & CHAIN_LATE_TRIGGER) ? 1 : 0;
+        m.tables_ready = (chain & CHAIN_TABLES_READY) ? 1 : 0;
+        const MoeStreamSizes z = moe_stream_sizes(E, K, nslots);
+        const int mt = z.mt;
+        const int64_t xtile = z.xtile, tables = z.tables, nst = z.nst;
         if (nst < 1) return QMM_ERR_SHAPE;
         m.nstages = (int)nst;
         m.xtile_bytes = (int)xtile;
@@ -770,7 +798,7 @@ qmm_status moe_apply(const DevInfo* di, const uint8_t* w_qs, const uint16_t* w_d
         return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
     }
 
-    if (pairs || xf) return QMM_ERR_SHAPE;  // the fallback writes plain rows of Q8_0 activations only
+    if (pairs || xf || chain) return QMM_ERR_SHAPE;  // the fallback: plain rows of Q8_0 activations only
     MoeArgs a = {};
     a.qs = w_qs;
     a.d = w_d;
@@ -942,6 +970,44 @@ qmm_status qmm_moe_combine(const float* z, const float* gates, int32_t T, int32_
     const cudaError_t e = launch(moe_combine_kernel, dim3(grid_for((total + 255) / 256, 16, di->sms)), dim3(256), 0,
                                  S(stream), true, z, gates, T, k, N, y);
     return e == cudaSuccess ? launch_status() : (cudaGetLastError(), QMM_ERR_CUDA);
+}
+
+qmm_status qmm_moe_layer_f32(const float* logits, int32_t T, int32_t E, int32_t k, const uint8_t* gu_qs,
+                             const uint16_t* gu_d, const uint8_t* down_qs, const uint16_t* down_d, int64_t H,
+                             int64_t F, const float* x, int32_t* ids, float* gates, float* h, float* z, float* y,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    // every check of the four launches before the first
+    if (T < 0 || E <= 0 || k <= 0 || H <= 0 || F <= 0) return QMM_ERR_ARG;
+    if (E > QMM_ROUTER_MAX_EXPERTS || k > QMM_ROUTER_MAX_K || k > E || (int64_t)T * k > (1 << 24) ||
+        (int64_t)T * E > (int64_t(1) << 40) || !valid_k(H) || !valid_k(F))
+        return QMM_ERR_SHAPE;
+    if (T == 0) return QMM_OK;
+    if (!logits || !ids || !gates || !gu_qs || !gu_d || !down_qs || !down_d || !x || !h || !z || !y)
+        return QMM_ERR_ARG;
+    const int64_t nslots = (int64_t)T * k;
+    if (!workspace || workspace_bytes < moe_ws_bytes(E, nslots)) return QMM_ERR_WORKSPACE;
+    if (!aligned(logits, 4) || !aligned(ids, 4) || !aligned(gates, 4) || !aligned(workspace, 16) ||
+        !aligned(gu_qs, 16) || !aligned(down_qs, 16) || !aligned(gu_d, 2) || !aligned(down_d, 2) ||
+        !aligned(x, 16) || !aligned(h, 16) || !aligned(z, 4) || !aligned(y, 4))
+        return QMM_ERR_ALIGN;
+    if (!moe_streamable(gu_qs, gu_d, E, 2 * F, H) || !moe_streamable(down_qs, down_d, E, H, F) ||
+        moe_stream_sizes(E, H, nslots).nst < 1 || moe_stream_sizes(E, F, nslots).nst < 1)
+        return QMM_ERR_SHAPE;
+    const DevInfo* di = device_info();
+    if (!di) return QMM_ERR_DEVICE;
+    qmm_status s = qmm_moe_router_topk(logits, T, E, k, ids, gates, workspace, workspace_bytes, stream);
+    if (s != QMM_OK) return s;
+    const MoeWs ws = moe_ws(workspace, E);
+    // The gate/up launch lets its dependents start only once the router has
+    // completed, so the down launch reads the grouping and streams weights
+    // before its own wait (which only its activation reads need).
+    s = moe_apply(di, gu_qs, gu_d, E, 2 * F, H, T, k, nullptr, nullptr, 0, h, ws, S(stream), true, x,
+                  CHAIN_LATE_TRIGGER);
+    if (s != QMM_OK) return s;
+    s = moe_apply(di, down_qs, down_d, E, H, F, T, k, nullptr, nullptr, 1, z, ws, S(stream), false, h,
+                  CHAIN_TABLES_READY);
+    if (s != QMM_OK) return s;
+    return qmm_moe_combine(z, gates, T, k, H, y, stream);
 }
 
 qmm_status qmm_last_device_error(void* stream) {

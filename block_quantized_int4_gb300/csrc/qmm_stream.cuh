@@ -388,6 +388,15 @@ struct MoeStreamArgs {
     MoeWs ws;
     int rb, ckb, nstages, xtile_bytes;
     int* err;
+    // Launch chaining (programmatic dependent launch):
+    //  - late_trigger: let dependents start only after this grid's wait for
+    //    its predecessor (the gate/up launch after the router, so that the
+    //    grouping is complete before the down launch can start);
+    //  - tables_ready: the grouping was complete before this grid could start
+    //    (the down launch after such a gate/up launch): it is read, and the
+    //    producer streams weights, before the wait; only the consumers, which
+    //    read the activations, wait.
+    int late_trigger, tables_ready;
 };
 
 // The unit sequence of one CTA, walked identically by producer and consumers:
@@ -445,29 +454,32 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
         fence_mbar_init();
     }
     __syncthreads();
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // the grouping written by the kernel before
+    if (!a.late_trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // the grouping written by the kernel before (unless complete before this grid started)
+    if (!a.tables_ready) asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // The routing, read once into shared memory in one round of independent
     // loads (the walk below consults it for every row group): the active
     // experts and the start of each one's slots, for every possible active
     // index (those past n_active are not used), the count and the end, and
-    // (when short enough) the slot list itself.
+    // (when short enough) the slot list itself.  Read from L2 (.cg), so that
+    // no line an earlier grid left in this SM's L1 is used.
     int* s_active = reinterpret_cast<int*>(ring + (size_t)S * STAGE_BYTES);
     int* s_start = s_active + a.E;
     int* s_slots = s_start + a.E;
     int* s_count = s_slots + (a.slots_smem ? a.nslots : 0);  // n_active, total
     for (int i = tid; i < a.E; i += blockDim.x) {
-        s_active[i] = a.ws.active[i];
-        s_start[i] = a.ws.cursor[i];
+        s_active[i] = __ldcg(a.ws.active + i);
+        s_start[i] = __ldcg(a.ws.cursor + i);
     }
     if (a.slots_smem)
-        for (int i = tid; i < a.nslots; i += blockDim.x) s_slots[i] = a.ws.slots[i];
+        for (int i = tid; i < a.nslots; i += blockDim.x) s_slots[i] = __ldcg(a.ws.slots + i);
     if (tid == 0) {
-        s_count[0] = *a.ws.n_active;
-        s_count[1] = a.ws.offsets[a.E];
+        s_count[0] = __ldcg(a.ws.n_active);
+        s_count[1] = __ldcg(a.ws.offsets + a.E);
     }
     __syncthreads();
+    if (a.late_trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int n_active = s_count[0];
     const int* slot_list = a.slots_smem ? s_slots : a.ws.slots;
     const int64_t total = (int64_t)n_active * a.N;
@@ -527,6 +539,7 @@ __global__ void __launch_bounds__(STREAM_THREADS, 2)
     const int rA = 2 * warp, rB = 2 * warp + 16;
     int u = 0;
     bool failed = false;
+    if (a.tables_ready) asm volatile("griddepcontrol.wait;" ::: "memory");  // the activations
     while (cur.next_segment(s_active, s_start)) {
         const int nslots = cur.send - cur.sbeg;
         const int nsb = (nslots + MT - 1) / MT;

@@ -77,6 +77,7 @@ SIGNATURES = {
     "qmm_moe_gemv_static": [_P, _P, _I32, _I64, _I64, _P, _I32, _I32, _P, _P, _INT, _P, _P],
     "qmm_moe_combine": [_P, _P, _I32, _I32, _I64, _P, _P],
     "qmm_moe_router_topk": [_P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P],
+    "qmm_moe_layer_f32": [_P, _I32, _I32, _I32, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "qmm_quantize_rowwise": [_P, _I64, _I64, _I64, _I32, _P, _P, _P],
     "qmm_lru_create": [_I32, _I32, ctypes.POINTER(_P)],
     "qmm_lru_request": [_P, _P, _I32, _I32, _P, _P, _P, _P],
@@ -355,6 +356,14 @@ def qmm_moe_router_topk(logits, T, E, k, ids, gates, workspace=None, workspace_b
     _check(_lib.qmm_moe_router_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(gates), _ptr(workspace),
                                     workspace_bytes if workspace is not None else 0, _stream(stream)),
            "qmm_moe_router_topk")
+
+
+def qmm_moe_layer_f32(logits, T, E, k, gu_qs, gu_d, down_qs, down_d, H, F, x, ids, gates, h, z, y, workspace,
+                      workspace_bytes, stream=None):
+    _check(_lib.qmm_moe_layer_f32(_ptr(logits), T, E, k, _ptr(gu_qs), _ptr(gu_d), _ptr(down_qs), _ptr(down_d), H, F,
+                                  _ptr(x), _ptr(ids), _ptr(gates), _ptr(h), _ptr(z), _ptr(y), _ptr(workspace),
+                                  workspace_bytes, _stream(stream)),
+           "qmm_moe_layer_f32")
 
 
 def qmm_moe_gemv_pregrouped(w_qs, w_d, E, N, K, T, k, xq, xd, x_per_slot, y, workspace, workspace_bytes,

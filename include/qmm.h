@@ -454,6 +454,32 @@ QMM_API qmm_status qmm_moe_gemv_pregrouped_f32(const uint8_t* w_qs, const uint16
 QMM_API qmm_status qmm_moe_combine(const float* z, const float* gates, int32_t T, int32_t k, int64_t N, float* y,
                            void* stream);
 
+/* One MoE FFN layer on fp32 activations, from router logits (Colibri page,
+ * "Arquitectura del Sistema": router, routed experts, combined result;
+ * TinyLLaMA guide section 4.4: SwiGLU), as four launches on stream, with
+ * the results of these calls in this order:
+ *   qmm_moe_router_topk(logits, T, E, k, ids, gates, workspace, ...);
+ *   qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, x, NULL, NULL, 0, h, ...);
+ *   qmm_moe_gemv_pregrouped_f32(down_qs, down_d, E, H, F, T, k, h, 1, z, ...);
+ *   qmm_moe_combine(z, gates, T, k, H, y);
+ * bit for bit.  gu_qs/gu_d: each expert's 2F interleaved gate/up rows of H
+ * columns; down_qs/down_d: each expert's H rows of F columns; x fp32 [T][H]
+ * and h fp32 [T*k][F] (16-byte aligned), z fp32 [T*k][H], y fp32 [T][H],
+ * ids int32 [T][k], gates fp32 [T][k]; workspace as for
+ * qmm_moe_router_topk, required.  Because the launches' order is fixed
+ * here, the down launch reads the grouping and starts streaming its weights
+ * before the gate/up launch has finished (the gate/up launch lets it start
+ * only after the router has completed); only its activation reads wait.
+ * Every check of the four calls is made before the first launch; the
+ * streaming path is required for both expert tensors (H and F multiples of
+ * 256, planes 16-byte aligned), else QMM_ERR_SHAPE.  The fastest measured
+ * form for few routed slots (T * k * 4 <= E); with more, Q8_0 launches of
+ * x and h ahead of the Q8_0-input expert GEMVs measured 2% faster. */
+QMM_API qmm_status qmm_moe_layer_f32(const float* logits, int32_t T, int32_t E, int32_t k, const uint8_t* gu_qs,
+                                     const uint16_t* gu_d, const uint8_t* down_qs, const uint16_t* down_d,
+                                     int64_t H, int64_t F, const float* x, int32_t* ids, float* gates, float* h,
+                                     float* z, float* y, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------------
  * Expert hot-store (Colibri page, "Arquitectura del Sistema": a
  * least-recently-used cache of experts per layer, an optional hot store in

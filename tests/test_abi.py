@@ -173,7 +173,8 @@ def test_fused_ops_chain_validation(qmm):
 
 def test_router_and_pregrouped_validation(qmm):
     """qmm_moe_router_topk: 1 <= k <= min(E, 64), E <= 1024, workspace size
-    and alignment; qmm_moe_gemv_pregrouped: the workspace rules of
+    and alignment; qmm_moe_layer_f32: the checks of its four launches, all
+    made before the first; qmm_moe_gemv_pregrouped: the workspace rules of
     qmm_moe_gemv.  All rejected on the host."""
     A16 = 0x10000
     r = lambda *a: _call(qmm, "qmm_moe_router_topk", *a)  # noqa: E731
@@ -188,6 +189,20 @@ def test_router_and_pregrouped_validation(qmm):
     assert r(A16, 16, 256, 8, A16, A16, A16, n - 16, None) == 8      # workspace too small
     assert r(A16 + 2, 16, 256, 8, A16, A16, None, 0, None) == 3      # logits not 4-byte aligned
     assert r(A16, 16, 256, 8, A16, A16, A16 + 8, n, None) == 3       # workspace not 16-byte aligned
+    ly = lambda T, k, H, F, ptrs, ws, wsb: _call(qmm, "qmm_moe_layer_f32", A16, T, 256, k, *ptrs[:4], H, F,  # noqa: E731
+                                                  *ptrs[4:], ws, wsb, None)
+    ok = [A16] * 10  # gu_qs, gu_d, down_qs, down_d, x, ids, gates, h, z, y
+    assert ly(-1, 8, 512, 256, ok, A16, n) == 1                       # T < 0
+    assert ly(16, 0, 512, 256, ok, A16, n) == 1                       # k = 0
+    assert ly(16, 8, 500, 256, ok, A16, n) == 2                       # H % 32
+    assert ly(0, 8, 512, 256, ok, A16, n) == 0                        # T = 0: no-op
+    assert ly(16, 8, 512, 256, ok[:9] + [None], A16, n) == 1          # no y
+    assert ly(16, 8, 512, 256, ok, A16, n - 16) == 8                  # workspace too small
+    assert ly(16, 8, 512, 256, ok, None, n) == 8                      # workspace required
+    assert ly(16, 8, 512, 256, ok[:4] + [A16 + 4] + ok[5:], A16, n) == 3  # x not 16-byte aligned
+    assert ly(16, 8, 512, 256, [A16 + 8] + ok[1:], A16, n) == 3       # gate/up nibbles not 16-byte aligned
+    assert ly(16, 8, 512, 96, ok, A16, n) == 2                        # F: no streaming path
+    assert ly(16, 8, 512, 256, [A16, A16 + 2] + ok[2:], A16, n) == 2  # gate/up scales: no streaming path
     p = lambda *a: _call(qmm, "qmm_moe_gemv_pregrouped", *a)  # noqa: E731
     assert p(A16, A16, 256, 64, 64, 16, 8, A16, A16, 0, A16, A16, n - 16, None) == 8
     assert p(A16, A16, 256, 64, 64, 16, 8, A16, A16, 0, A16, None, n, None) == 8

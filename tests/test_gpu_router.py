@@ -165,3 +165,57 @@ def test_moe_layer_from_router_logits_end_to_end():
     y_ref, _, _ = O.moe_forward(gate.oracle, up.oracle, down.oracle, ids_ref, gates_ref.astype(np.float32), qx, dx)
     rel = np.linalg.norm(y.cpu().numpy() - y_ref) / np.linalg.norm(y_ref)
     assert rel <= 1e-4, rel
+
+
+@pytest.mark.parametrize("T,E,k,H,F", [(1, 256, 8, 512, 256), (3, 8, 8, 256, 512), (16, 64, 8, 512, 256)])
+def test_moe_layer_entry_equals_its_four_calls(T, E, k, H, F):
+    """qmm_moe_layer_f32 (router, gate/up + SwiGLU, down, combine as one call,
+    the down launch reading the grouping and streaming weights before the
+    gate/up launch ends) gives ids, gates, h, z and y of the four separate
+    calls bit for bit, for two layers back to back on different routings
+    (one slot per weight pass, every expert routed, four slots per pass);
+    and the layer against the oracle's (relative L2 <= 1e-4, as the layer
+    test above)."""
+    qmm = lib()
+    gate = Experts(qmm, E, F, H, np.arange(E), seed=17, base_index=0, oracle_ids=[])
+    up = Experts(qmm, E, F, H, np.arange(E), seed=17, base_index=1000, oracle_ids=[])
+    down = Experts(qmm, E, H, F, np.arange(E), seed=17, base_index=2000, oracle_ids=[])
+    gu_qs = torch.stack([gate.qs, up.qs], dim=2).reshape(E, 2 * F, H // 2).contiguous()
+    gu_d = torch.stack([gate.d, up.d], dim=2).reshape(E, 2 * F, H // 32).contiguous()
+    wsb = qmm.qmm_moe_workspace_size(E, T, k)
+    logits = [workloads.router_logits(T, E, seed=40 + r).to(DEV).contiguous() for r in range(2)]
+    xs = [workloads.activations(T, H, seed=50 + r).to(DEV).contiguous() for r in range(2)]
+
+    def bufs():
+        return dict(ids=torch.full((T, k), -7, dtype=torch.int32, device=DEV),
+                    gates=torch.full((T, k), float("nan"), device=DEV),
+                    h=torch.full((T * k, F), float("nan"), device=DEV),
+                    z=torch.full((T * k, H), float("nan"), device=DEV),
+                    y=torch.full((T, H), float("nan"), device=DEV),
+                    ws=torch.full((wsb,), 0x3A, dtype=torch.uint8, device=DEV))
+
+    sep = [bufs() for _ in range(2)]
+    for r, b in enumerate(sep):
+        qmm.qmm_moe_router_topk(logits[r], T, E, k, b["ids"], b["gates"], b["ws"], wsb)
+        qmm.qmm_moe_gemv_gate_up(gu_qs, gu_d, E, 2 * F, H, T, k, xs[r], None, None, 0, b["h"], b["ws"], wsb)
+        qmm.qmm_moe_gemv_pregrouped_f32(down.qs, down.d, E, H, F, T, k, b["h"], 1, b["z"], b["ws"], wsb)
+        qmm.qmm_moe_combine(b["z"], b["gates"], T, k, H, b["y"])
+    one = [bufs() for _ in range(2)]
+    for r, b in enumerate(one):  # back to back on the stream
+        qmm.qmm_moe_layer_f32(logits[r], T, E, k, gu_qs, gu_d, down.qs, down.d, H, F, xs[r], b["ids"], b["gates"],
+                              b["h"], b["z"], b["y"], b["ws"], wsb)
+    assert qmm.qmm_last_device_error() == 0
+    for a, b in zip(sep, one):
+        for key in ("ids", "gates", "h", "z", "y"):
+            assert torch.equal(a[key], b[key]), key
+        assert not torch.isnan(b["y"]).any()
+    # the layer against the oracle's layer (the fp32 activations quantized as qmm_quantize_q8_0 does)
+    ids_ref, gates_ref = O.router_topk(logits[0].cpu().numpy(), k)
+    assert np.array_equal(one[0]["ids"].cpu().numpy(), ids_ref)
+    gate.oracle_from_planes(ids_ref.reshape(-1))
+    up.oracle_from_planes(ids_ref.reshape(-1))
+    down.oracle_from_planes(ids_ref.reshape(-1))
+    qx, dx = O.quantize_q8_0(xs[0].cpu().numpy())
+    y_ref, _, _ = O.moe_forward(gate.oracle, up.oracle, down.oracle, ids_ref, gates_ref.astype(np.float32), qx, dx)
+    rel = np.linalg.norm(one[0]["y"].cpu().numpy() - y_ref) / np.linalg.norm(y_ref)
+    assert rel <= 1e-4, rel
