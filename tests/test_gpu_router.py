@@ -173,9 +173,9 @@ def test_moe_layer_entry_equals_its_four_calls(T, E, k, H, F):
     the down launch reading the grouping and streaming weights before the
     gate/up launch ends) gives ids, gates, h, z and y of the four separate
     calls bit for bit, for two layers back to back on different routings
-    (one slot per weight pass, every expert routed, four slots per pass);
-    and the layer against the oracle's (relative L2 <= 1e-4, as the layer
-    test above)."""
+    (one slot per weight pass, every expert routed, four slots per pass),
+    called directly and replayed from a CUDA graph; and the layer against
+    the oracle's (relative L2 <= 1e-4, as the layer test above)."""
     qmm = lib()
     gate = Experts(qmm, E, F, H, np.arange(E), seed=17, base_index=0, oracle_ids=[])
     up = Experts(qmm, E, F, H, np.arange(E), seed=17, base_index=1000, oracle_ids=[])
@@ -209,6 +209,33 @@ def test_moe_layer_entry_equals_its_four_calls(T, E, k, H, F):
         for key in ("ids", "gates", "h", "z", "y"):
             assert torch.equal(a[key], b[key]), key
         assert not torch.isnan(b["y"]).any()
+    # the same two layers captured in a CUDA graph and replayed twice (the
+    # launches keep their programmatic dependencies as graph edges)
+    gph = [bufs() for _ in range(2)]
+
+    def run():
+        for r, b in enumerate(gph):
+            qmm.qmm_moe_layer_f32(logits[r], T, E, k, gu_qs, gu_d, down.qs, down.d, H, F, xs[r], b["ids"],
+                                  b["gates"], b["h"], b["z"], b["y"], b["ws"], wsb)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for b in gph:
+        b["y"].fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert qmm.qmm_last_device_error() == 0
+    for a, b in zip(sep, gph):
+        for key in ("ids", "gates", "h", "z", "y"):
+            assert torch.equal(a[key], b[key]), key
     # the layer against the oracle's layer (the fp32 activations quantized as qmm_quantize_q8_0 does)
     ids_ref, gates_ref = O.router_topk(logits[0].cpu().numpy(), k)
     assert np.array_equal(one[0]["ids"].cpu().numpy(), ids_ref)
