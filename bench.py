@@ -16,7 +16,7 @@ Also reported on the same line (`also`): batch-16 GEMM TOPS on the large
 dense FFN + lm_head shapes, and the GLM-scale MoE layer.
 
 `--impl reference` times the CPU oracle on a bounded row sample of the same
-decode step (the reference arm of this build).
+decode step (the reference arm: a deliberately plain program, for context).
 """
 from __future__ import annotations
 
