@@ -189,14 +189,17 @@ bool valid_k(int64_t K) { return K > 0 && K % QK == 0 && K <= (int64_t)1 << 30; 
 
 // Streaming kernel: eligible when the scale plane can be bulk-copied in row
 // segments (B % 8 == 0, i.e. K % 256 == 0; d 16-byte aligned) and the staged
-// activation tile fits.
+// activation tile fits: up to 64 KB at two CTAs per SM; for two tokens up to
+// 96 KB at one CTA per SM (a 220 KB ring: 8192 x 28672 at 2 tokens 35.8 ->
+// 32.6 us against the row kernel, the batch-2 dense set 0.185 -> 0.181 ms).
 constexpr int STREAM_XTILE_CAP = 64 * 1024;
+constexpr int STREAM_XTILE_CAP_ONE_CTA = 96 * 1024;
 constexpr int64_t CHAIN_MATRIX_BYTES = 16ll << 20;  // up to this, one CTA per SM and room for a neighbour CTA
 
 bool stream_eligible(int64_t N, int64_t K, const void* qs, const void* d, int MT) {
     const int64_t B = K / QK;
     return (B % 8 == 0) && aligned(qs, 16) && aligned(d, 16) && N < (int64_t(1) << 31) &&
-           (int64_t)MT * B * xtile_bytes_per_block() <= STREAM_XTILE_CAP;
+           (int64_t)MT * B * xtile_bytes_per_block() <= (MT == 2 ? STREAM_XTILE_CAP_ONE_CTA : STREAM_XTILE_CAP);
 }
 
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
@@ -219,7 +222,9 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
 #define QMM_STREAM_BIG_SMEM_KB 110
 #endif
     const bool chain_sized = a.N * row_bytes <= CHAIN_MATRIX_BYTES;
-    const int64_t ctas = chain_sized ? di->sms : QMM_STREAM_BIG_CTAS_PER_SM * (int64_t)di->sms;
+    // an activation tile above the two-CTA cap: one CTA per SM
+    const bool one_cta = (int64_t)MT * B * xtile_bytes_per_block() > STREAM_XTILE_CAP;
+    const int64_t ctas = chain_sized || one_cta ? di->sms : QMM_STREAM_BIG_CTAS_PER_SM * (int64_t)di->sms;
     // A CTA's weights arrive through its one producer lane, so in a decode
     // chain fewer bytes per CTA finish sooner: a Q8_0-output launch takes the
     // smallest whole-block row count that keeps about two CTAs per SM at most
@@ -243,7 +248,7 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
     // Small matrices (decode chains): stay under ~112 KB so the next chained
     // kernel's CTA is resident beside this one and prefetches its weights
     // (two such CTAs and their 1 KB reservations fill the SM's 228 KB).
-    const int64_t cap = chain_sized ? 112 * 1024 : QMM_STREAM_BIG_SMEM_KB * 1024;
+    const int64_t cap = chain_sized ? 112 * 1024 : one_cta ? 220 * 1024 : QMM_STREAM_BIG_SMEM_KB * 1024;
     const int64_t room = (cap - STREAM_HDR - xtile - ybuf - rbuf) / stage_bytes;
     const int64_t nst = std::min<int64_t>({nunits, room, (int64_t)STREAM_MAX_STAGES});
     if (nst < 1) return QMM_ERR_SHAPE;
@@ -492,7 +497,8 @@ qmm_status qmm_gemm_q4_0_q8_0(const uint8_t* w_qs, const uint16_t* w_d, int64_t 
         // fallback where the activation tile does not fit), where it measured
         // faster than warp MMA (x = stream / MMA, us): 2 tokens on every
         // shape (28672x8192 23.2/31.9 against the 16-warp layout, 8192x28672
-        // 36.0/48.6 on the fallback, 2048x5632 6.0/8.0, 2560x2048 4.0/5.0,
+        // 32.6 at one CTA per SM, where the 16-warp layout splitting K over
+        // clusters takes 37.0 at 4 tokens, 2048x5632 6.0/8.0, 2560x2048 4.0/5.0,
         // 5632x2048 5.7/5.7); 3-4 tokens when N <= 4096 or K >= 8192, the
         // activation tile fits and the 16-warp layout does not apply
         // (2048x5632 7.0/8.1, 2560x2048 4.4/4.9; but 5632x2048 6.4/5.6, and

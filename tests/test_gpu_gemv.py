@@ -214,8 +214,8 @@ def _sampled_rows(N, n, seed):
                                         ("dense.lm_head", 128256, 8192, 1), ("dense.gate", 28672, 8192, 16),
                                         ("dense.lm_head", 128256, 8192, 16), ("dense.up", 28672, 8192, 64),
                                         ("batched.gate", 5632, 2048, 64),
-                                        # 2 tokens: the streaming kernel, and its row-kernel fallback for the
-                                        # long-K down projection (activation tile above the streaming cap)
+                                        # 2 tokens: the streaming kernel, at one CTA per SM for the long-K
+                                        # down projection (an activation tile above the two-CTA cap)
                                         ("dense.gate", 28672, 8192, 2), ("dense.down", 8192, 28672, 2),
                                         ("dense.up", 28672, 8192, 4)])
 def test_full_size_sampled_rows(name, N, K, M):
