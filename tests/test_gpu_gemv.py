@@ -172,6 +172,23 @@ def test_gemm_row_groups_and_ragged_edges(M, K):
     assert qmm.qmm_last_device_error() == 0
 
 
+@pytest.mark.parametrize("K", [26368, 39168, 39424])
+def test_two_tokens_long_k(K):
+    """Two tokens with a K whose two-token activation tile is above the
+    streaming kernel's two-CTA cap: just above it (824 blocks) and at the
+    one-CTA cap (1224 blocks: one CTA per SM), and just past that (1232
+    blocks: the row kernel).  All rows against the oracle."""
+    qmm = lib()
+    N, M = 1000, 2
+    qw, dw, qx, dx = _rand_codes(N, M, K, seed=K)
+    qs, d = _to_device_planes(qmm, qw, dw)
+    xq, xd = _dev_q8(qx, dx)
+    y = qmm.gemm(qs, d, xq, xd)
+    ref, S = O.matmul_int(qw, dw, qx, dx, nthreads=8)
+    assert_close(y, ref, S, f"gemm {N}x{K} M={M}")
+    assert qmm.qmm_last_device_error() == 0
+
+
 def test_gemm_ldy_and_chunked_k():
     """Output row stride > N, and K too long to stage for 8 tokens at once."""
     qmm = lib()
