@@ -227,17 +227,17 @@ qmm_status stream_launch(const DevInfo* di, const uint8_t* qs, const uint16_t* d
     const int64_t ctas = chain_sized || one_cta ? di->sms : QMM_STREAM_BIG_CTAS_PER_SM * (int64_t)di->sms;
     // A CTA's weights arrive through its one producer lane, so in a decode
     // chain fewer bytes per CTA finish sooner: a Q8_0-output launch, a
-    // one-token launch of the fused (chain) entries, and a one-token product
-    // of more than 4096 rows (the kernel fits two CTAs per SM at one token)
-    // take the smallest row count (whole 32-output blocks with a Q8_0
-    // output, else pairs) that keeps about two CTAs per SM at most
+    // one-token launch of the fused (chain) entries, and a one- or two-token
+    // product of more than 4096 rows (the kernel fits two CTAs per SM up to
+    // two tokens) take the smallest row count (whole 32-output blocks with a
+    // Q8_0 output, else pairs) that keeps about two CTAs per SM at most
     // (TinyLLaMA gate/up: 176 CTAs of 64 rows instead of 88 of 128, the
     // decode step 462 -> 422 us; O and down: 256 CTAs of 8 rows instead of
-    // 147 of 14, 0.361 -> 0.358 ms; 5632 x 2048 alone 4.80 -> 4.25 us, but
-    // 2048 x 2048 alone 3.27 -> 3.30).  With 4 tokens the kernel holds one
-    // CTA per SM, and twice the CTAs ran in two waves (2048 x 5632 7.1 ->
-    // 10.8 us); with 2, 2048-row products measured 2-3% slower.
-    const bool two_per_sm = qout || (MT == 1 && (XM == X_RUNTIME || a.N > 4096));
+    // 147 of 14, 0.361 -> 0.358 ms; 5632 x 2048 alone 4.80 -> 4.25 us at one
+    // token, 5.75 -> 5.08 at two; but 2048-row products alone 1-3% slower:
+    // 2048 x 2048 3.27 -> 3.30).  With 4 tokens the kernel holds one CTA per
+    // SM, and twice the CTAs ran in two waves (2048 x 5632 7.1 -> 10.8 us).
+    const bool two_per_sm = qout || (MT == 1 && XM == X_RUNTIME) || (MT <= 2 && a.N > 4096);
     const int64_t rpc = chain_sized && two_per_sm
                             ? std::max<int64_t>(align, round_up((a.N + 2 * ctas - 1) / (2 * ctas), align))
                             : round_up((a.N + ctas - 1) / ctas, align);
